@@ -1,0 +1,154 @@
+/*
+ * gdn.h -- C ABI of the chunked gated delta rule (Gated DeltaNet) operator
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operator.  For one sequence and one head, with a recurrent state S of
+ * shape d_k x d_v (fp32), per token t:
+ *     alpha_t = exp(g_t)                         (g_t <= 0, given in log space)
+ *     S       <- alpha_t S                       (forget)
+ *     v_old   =  S^T k_t                         (read what is stored for k_t)
+ *     S       <- S + beta_t k_t (v_t - v_old)^T  (write the error, not the value)
+ *     o_t     =  scale * S^T q_t                 (look up with the query)
+ * Sources: "Research Sprint Day 1 - Verifying the flash-linear-attention
+ * Gated DeltaNet kernel on GB10", section "The GDN update" (the loop);
+ * "Research Sprint Day 2 - Rooflines", GDN update equation
+ * S_t = S_{t-1}(alpha_t (I - beta_t k_t k_t^T)) + beta_t v_t k_t^T (the same
+ * map on the transposed d_v x d_k state) and its GDN layer pseudocode step 5
+ * (g kept in log space, accumulated as a cumsum); the cuLA issue #126
+ * reproduction (scale = D^-0.5 passed to the kernel, fp32 (1,H,D,D) state,
+ * caller-allocated out/final_state).  The library evaluates it chunk by chunk
+ * (64 tokens), which reaches the same result in exact arithmetic.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or keeps a pointer after the call
+ *     returns.  Scratch memory is the caller's `workspace`.
+ *   - Tensors are contiguous, row-major, in the shapes given below.  bf16
+ *     tensors (q, k, v, beta, out, d_out, dq, dk, dv, dbeta) are raw IEEE
+ *     bfloat16 bit patterns (gdn_bf16) and must be 16-byte aligned; fp32
+ *     tensors must be 16-byte aligned; cu_seqlens 4-byte aligned.
+ *   - Dense inputs: q, k (B,T,H,d_k); v, out (B,T,H,d_v); g, beta (B,T,H);
+ *     states (B,H,d_k,d_v) with state[n,h,i,j] = key i, value j.
+ *   - Packed variable-length inputs (cu_seqlens != NULL): the tensors hold
+ *     (1,T,H,.) with N = B sequences concatenated along T; cu_seqlens is a
+ *     device int32 array of N+1 offsets, cu_seqlens[0] = 0,
+ *     non-decreasing, cu_seqlens[N] = T.  The state starts afresh at each
+ *     sequence (from initial_state[n] or zero); states are (N,H,d_k,d_v).
+ *   - Supported sizes: d_k in {64, 128}; d_v in {64, 128, 256}; T >= 0;
+ *     B >= 1 and H >= 1 (each at most 65535); B*T*H*max(d_k,d_v) < 2^40.
+ *     Every g must be <= 0 (the
+ *     documented domain: alpha = exp(g) in (0,1]).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument errors are found on the host and returned before any launch.
+ *     Errors that only the device can see (malformed cu_seqlens, a bounded
+ *     wait that ran out) are recorded in a per-device error word; the
+ *     affected blocks write nothing.  Read and clear it with
+ *     gdn_get_last_device_error().
+ *   - Results are deterministic: the same inputs give bitwise-identical
+ *     outputs on every launch (no atomics on data paths).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+/* IEEE bfloat16 stored as its 16-bit pattern. */
+typedef uint16_t gdn_bf16;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null required pointer, negative/zero size, bad workspace */
+    GDN_ERR_UNSUPPORTED = 2,   /* d_k / d_v outside the supported set, size too large */
+    GDN_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    GDN_ERR_BAD_SEQLENS = 4,   /* device found cu_seqlens not 0 .. T non-decreasing */
+    GDN_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (kernel returned early) */
+    GDN_ERR_CUDA = 6           /* a CUDA runtime call failed (launch, sync, copy) */
+} gdn_status;
+
+/* Chunk length used by the library (tokens per chunk). */
+#define GDN_CHUNK 64
+
+/* Human-readable name of a status code (static string, never NULL). */
+GDN_API const char* gdn_status_string(gdn_status status);
+
+/*
+ * Bytes of device workspace gdn_chunk_fwd needs for these sizes (may be 0).
+ * varlen != 0 when cu_seqlens will be given (B is then the sequence count).
+ */
+GDN_API size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
+ * Forward.  Reads q, k, v, g, beta (and initial_state, cu_seqlens when not
+ * NULL); writes out (bf16, round-to-nearest-even) and, when final_state is
+ * not NULL, the fp32 state after each sequence's last token.
+ *   q, k          (B,T,H,d_k) bf16          v, out (B,T,H,d_v) bf16
+ *   g             (B,T,H) fp32, log decay   beta   (B,T,H) bf16
+ *   scale         readout scale (usually d_k^-0.5)
+ *   initial_state (N,H,d_k,d_v) fp32 or NULL (zeros)
+ *   cu_seqlens    NULL (dense) or device int32[N+1] (packed; N = B)
+ *   final_state   (N,H,d_k,d_v) fp32 or NULL (not written)
+ *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size()
+ *                 bytes (may be NULL when that size is 0)
+ * Returns GDN_OK once the work is enqueued on `stream`.
+ */
+GDN_API gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                         const float* g, const gdn_bf16* beta, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         gdn_bf16* out, float* final_state,
+                         int B, int T, int H, int d_k, int d_v,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace gdn_chunk_bwd needs for these sizes. */
+GDN_API size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
+ * Backward (reverse mode of gdn_chunk_fwd).  Given the forward inputs and the
+ * upstream gradients d_out (B,T,H,d_v) bf16 and d_final_state
+ * (N,H,d_k,d_v) fp32 or NULL (zero), writes
+ *   dq, dk (B,T,H,d_k) bf16;  dv (B,T,H,d_v) bf16;
+ *   dg (B,T,H) fp32 -- gradient w.r.t. the per-token g (not its cumsum);
+ *   dbeta (B,T,H) bf16 -- gradient w.r.t. beta as passed;
+ *   d_initial_state (N,H,d_k,d_v) fp32, or NULL (not written).
+ * The chunk-start states are recomputed into `workspace`.
+ * Returns GDN_OK once the work is enqueued on `stream`.
+ */
+GDN_API gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                         const float* g, const gdn_bf16* beta, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         const gdn_bf16* d_out, const float* d_final_state,
+                         gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                         gdn_bf16* dbeta, float* d_initial_state,
+                         int B, int T, int H, int d_k, int d_v,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word of
+ * the current device: GDN_OK, GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT
+ * (GDN_ERR_CUDA if the synchronisation or the read itself failed).
+ */
+GDN_API gdn_status gdn_get_last_device_error(cudaStream_t stream);
+
+/*
+ * Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all entry points).  Library bookkeeping with no counterpart
+ * on the pages; lets a caller count the kernels inside a timed region.
+ */
+GDN_API uint64_t gdn_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

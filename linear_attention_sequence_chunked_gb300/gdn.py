@@ -1,0 +1,204 @@
+"""Thin Python binding of the C ABI in include/gdn.h.
+
+Every function here only marshals arguments (tensor -> device pointer,
+stream -> handle) and checks the returned status; all arithmetic runs in the
+CUDA kernels of ``_build/libgdn.so``.  There is no CPU fallback: if the
+library is missing or no GPU is present, calls raise.
+
+Low-level names mirror the C ABI (gdn_chunk_fwd, gdn_chunk_bwd, ...).  The
+two convenience wrappers (chunk_gated_delta_rule_fwd / _bwd) allocate the
+outputs and the workspace with torch and then call the same entry points.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+GDN_OK = 0
+STATUS_NAMES = {
+    0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
+    4: "GDN_ERR_BAD_SEQLENS", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_CUDA",
+}
+HEADER = os.path.join(_build.ROOT, "include", "gdn.h")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def header_functions():
+    """Names of the functions declared in include/gdn.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)
+
+
+def load():
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing (run build())")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.gdn_status_string.argtypes = [i]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_chunk_fwd_workspace_size.argtypes = [i] * 6
+        lib.gdn_chunk_fwd_workspace_size.restype = sz
+        lib.gdn_chunk_bwd_workspace_size.argtypes = [i] * 6
+        lib.gdn_chunk_bwd_workspace_size.restype = sz
+        lib.gdn_chunk_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp, sz, vp]
+        lib.gdn_chunk_fwd.restype = i
+        lib.gdn_chunk_bwd.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp, sz, vp]
+        lib.gdn_chunk_bwd.restype = i
+        lib.gdn_get_last_device_error.argtypes = [vp]
+        lib.gdn_get_last_device_error.restype = i
+        lib.gdn_kernel_launches.argtypes = []
+        lib.gdn_kernel_launches.restype = ctypes.c_uint64
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+# ----------------------------------------------------------------------------
+# C ABI mirrors
+# ----------------------------------------------------------------------------
+
+def gdn_status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def gdn_chunk_fwd_workspace_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_chunk_fwd_workspace_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
+def gdn_chunk_bwd_workspace_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_chunk_bwd_workspace_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                  B, T, H, d_k, d_v, workspace=None, workspace_bytes=0, stream=None):
+    st = load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                              _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                              _ptr(final_state), B, T, H, d_k, d_v, _ptr(workspace),
+                              int(workspace_bytes), _stream(stream))
+    _check(st, "gdn_chunk_fwd")
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
+                  dq, dk, dv, dg, dbeta, d_initial_state, B, T, H, d_k, d_v,
+                  workspace=None, workspace_bytes=0, stream=None):
+    st = load().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                              _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out),
+                              _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                              _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
+                              _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "gdn_chunk_bwd")
+
+
+def gdn_get_last_device_error(stream=None) -> int:
+    return int(load().gdn_get_last_device_error(_stream(stream)))
+
+
+def gdn_kernel_launches() -> int:
+    return int(load().gdn_kernel_launches())
+
+
+# ----------------------------------------------------------------------------
+# convenience wrappers (torch tensors in, torch tensors out)
+# ----------------------------------------------------------------------------
+
+def _dims(q, v, cu_seqlens):
+    Bq, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if cu_seqlens is not None:
+        if Bq != 1:
+            raise ValueError("packed inputs must have batch extent 1")
+        B = int(cu_seqlens.numel()) - 1
+    else:
+        B = Bq
+    return B, T, H, d_k, d_v
+
+
+def _workspace(nbytes, device):
+    import torch
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
+                               cu_seqlens=None, output_final_state=True, stream=None):
+    """Allocate outputs and run gdn_chunk_fwd.  Returns (out, final_state)."""
+    import torch
+    B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = d_k ** -0.5
+    out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    fs = (torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=v.device)
+          if output_final_state else None)
+    nbytes = gdn_chunk_fwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+    ws = _workspace(nbytes, v.device)
+    gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs,
+                  B, T, H, d_k, d_v, ws, nbytes, stream)
+    return out, fs
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=None, initial_state=None,
+                               cu_seqlens=None, d_final_state=None, stream=None):
+    """Allocate gradients and run gdn_chunk_bwd.  Returns a dict of tensors."""
+    import torch
+    B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = d_k ** -0.5
+    dev = v.device
+    res = dict(dq=torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+               dk=torch.empty(k.shape, dtype=torch.bfloat16, device=dev),
+               dv=torch.empty(v.shape, dtype=torch.bfloat16, device=dev),
+               dg=torch.empty(g.shape, dtype=torch.float32, device=dev),
+               dbeta=torch.empty(beta.shape, dtype=torch.bfloat16, device=dev),
+               d_initial_state=torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=dev))
+    nbytes = gdn_chunk_bwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+    ws = _workspace(nbytes, dev)
+    gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
+                  res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"],
+                  res["d_initial_state"], B, T, H, d_k, d_v, ws, nbytes, stream)
+    return res

@@ -1,0 +1,82 @@
+"""The C ABI library: it builds, loads, exports every function that
+include/gdn.h declares, and rejects bad arguments on the host before any
+CUDA call (so these tests need no GPU)."""
+
+import ctypes
+
+import pytest
+
+from linear_attention_sequence_chunked_gb300 import build, gdn
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gdn.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = gdn.header_functions()
+    assert set(names) >= {"gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_fwd_workspace_size",
+                          "gdn_chunk_bwd_workspace_size", "gdn_get_last_device_error",
+                          "gdn_status_string"}
+    raw = ctypes.CDLL(gdn.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = gdn.gdn_status_string(code)
+        assert s.startswith(gdn.STATUS_NAMES[code])
+    assert gdn.gdn_status_string(99) == "GDN_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+def _fwd(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=1.0, initial_state=None,
+                cu_seqlens=None, out=FAKE, final_state=None, B=1, T=64, H=1, d_k=64, d_v=64)
+    args.update(over)
+    lib = gdn.load()
+    return lib.gdn_chunk_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"],
+                             args["scale"], args["initial_state"], args["cu_seqlens"], args["out"],
+                             args["final_state"], args["B"], args["T"], args["H"], args["d_k"],
+                             args["d_v"], None, 0, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=96), 2), (dict(d_k=256), 2), (dict(d_v=32), 2), (dict(d_v=192), 2),
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(beta=None), 1),
+    (dict(k=FAKE + 2), 3), (dict(out=FAKE + 8), 3), (dict(final_state=FAKE + 4), 3),
+    (dict(cu_seqlens=FAKE + 2), 3),
+    (dict(B=70000), 2),
+])
+def test_forward_host_validation(lib, over, code):
+    assert _fwd(**over) == code
+
+
+def test_backward_host_validation(lib):
+    l = gdn.load()
+    need = gdn.gdn_chunk_bwd_workspace_size(1, 128, 1, 64, 64, 0)
+    assert need > 0
+
+    def call(ws, ws_bytes, d_k=64, dq=FAKE):
+        return l.gdn_chunk_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, None, FAKE, None,
+                               dq, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 1, d_k, 64,
+                               ws, ws_bytes, None)
+    assert call(None, 0) == 1                   # workspace missing
+    assert call(FAKE, need - 1) == 1            # workspace too small
+    assert call(FAKE + 16, need) == 3           # workspace not 256-byte aligned
+    assert call(FAKE, need, d_k=32) == 2
+    assert call(FAKE, need, dq=None) == 1
+
+
+def test_workspace_sizes(lib):
+    assert gdn.gdn_chunk_fwd_workspace_size(4, 4096, 16, 128, 128, 0) >= 0
+    a = gdn.gdn_chunk_bwd_workspace_size(4, 4096, 16, 128, 128, 0)
+    b = gdn.gdn_chunk_bwd_workspace_size(4, 8192, 16, 128, 128, 0)
+    assert b > a > 4 * 64 * 16 * 128 * 128 * 4  # at least one fp32 state per chunk
+    assert gdn.gdn_chunk_bwd_workspace_size(1, 4096, 16, 96, 128, 0) == 0  # unsupported
