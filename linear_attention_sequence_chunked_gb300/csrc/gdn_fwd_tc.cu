@@ -28,6 +28,7 @@
 // share one region per 64 key columns ([K rows 0-63 ; Q rows 64-127]) so
 // that [K;Q] K^T is a single M = 128 product.
 #include <cuda.h>
+#include <string.h>
 
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
@@ -54,7 +55,7 @@ constexpr uint32_t kColPD = 256;  // P Delta, M = 64
 constexpr uint32_t kColS = 320;   // K^T (dec o Delta), M = d_k
 
 template <int K>
-struct TcSmem {
+struct TcSmem {  // instantiated for K = 128 only (d_k = 64 zero-fills the upper half)
     static constexpr int kRegions = K / 64;             // 64-column key regions
     static constexpr int kRegionBytes = 128 * 128;      // [K;Q] rows x 128 B
     static constexpr int kStageBytes = kRegions * kRegionBytes;
@@ -223,18 +224,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         *abort_flag = 0;
-        tma_prefetch_desc(&tmap_k);
-        tma_prefetch_desc(&tmap_q);
+        if (p.d_k == 128) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_q);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
+    const int dk = p.d_k;                                       // 64 or 128
     const long long row_base = static_cast<long long>(b) * p.T;  // token-row of t = 0
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
     const long long slot0 = chunk_slot_base(p.cu_seqlens, n, p.T);
-    const long long KV = static_cast<long long>(K) * V;
+    const long long KV = static_cast<long long>(dk) * V;
     const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
 
     // TMA issue for chunk ci into stage ci % kStages (thread 0 only)
@@ -243,20 +247,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar = bar_tma0 + 8 * st;
         uint8_t* base = sm + L::oStage + st * L::kStageBytes;
         const int z = static_cast<int>(row_base + t0 + ci * kChunk);
-        mbar_arrive_expect_tx(bar, L::kStageBytes);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
+        mbar_arrive_expect_tx(bar, (dk / 64) * L::kRegionBytes);
+        for (int r = 0; r < dk / 64; ++r) {
             tma_load_3d(smem_u32(base + r * L::kRegionBytes), &tmap_k, r * 64, h, z, bar);
             tma_load_3d(smem_u32(base + r * L::kRegionBytes + 64 * 128), &tmap_q, r * 64, h, z, bar);
         }
     };
-    if (threadIdx.x == 0) {
+    // d_k = 64: the upper 64 key columns of every K/Q tile are zero and never loaded
+    if (dk < 64 * R) {
+        for (int st = 0; st < kStages; ++st) {
+            uint4* z = reinterpret_cast<uint4*>(sm + L::oStage + st * L::kStageBytes + (dk / 64) * L::kRegionBytes);
+            const int n16 = (R - dk / 64) * L::kRegionBytes / 16;
+            for (int i = threadIdx.x; i < n16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+    }
+    // d_k = 128 streams K/Q tiles with TMA; d_k = 64 loads them with plain
+    // vector loads (only the first key region is populated).
+    const bool use_tma = dk == 64 * R;
+    if (use_tma && threadIdx.x == 0) {
         for (int ci = 0; ci < kStages && ci < nchunks; ++ci) issue_tma(ci);
     }
 
     // ---- state slice in registers: M = d_k accumulator row ownership ----
     // d_k = 128: thread r owns row r.  d_k = 64: M = 64 layout.
-    const int srow = (K == 128) ? static_cast<int>(threadIdx.x) : m64_row(warp, lane);
+    // S update accumulator is M = 128: thread r owns state row r; rows >= d_k
+    // stay zero (their key columns are zero-filled).
+    const int srow = static_cast<int>(threadIdx.x) < dk ? static_cast<int>(threadIdx.x) : -1;
+    static_assert(K == 128, "one instantiation");
     float S[kVs];
 #pragma unroll
     for (int j = 0; j < kVs; ++j) S[j] = 0.f;
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             S[j] = t4.x; S[j + 1] = t4.y; S[j + 2] = t4.z; S[j + 3] = t4.w;
         }
     }
-    if (srow >= 0) store_split_row(Shi, Slo, srow, S);
+    store_split_row(Shi, Slo, threadIdx.x, S);  // rows >= d_k are zero
     fence_proxy_async_smem();
     __syncthreads();
 
@@ -287,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
     };
     const bool want_out = p.out != nullptr;
-    int tma_issued = min(kStages, nchunks);  // chunks whose K/Q load was issued
+    int tma_issued = use_tma ? min(kStages, nchunks) : 0;  // chunks whose K/Q load was issued
     int tma_done = 0;                         // chunks whose K/Q load was waited for
 
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -320,10 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
         }
-        // wait for this chunk's K/Q tiles
-        {
+        // this chunk's K/Q tiles
+        if (use_tma) {
             const bool ok = mbar_wait(bar_tma0 + 8 * st, (ci / kStages) & 1, prm.wait_limit);
             if (!ok) *abort_flag = 1;
+        } else {
+            for (int e = threadIdx.x; e < 2 * 64 * 8; e += kThreads) {
+                const int which = e >> 9;          // 0: K, 1: Q
+                const int r = (e >> 3) & 63, ch = e & 7;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (r < nv) {
+                    const uint16_t* src = which ? p.q : p.k;
+                    val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
+                }
+                *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+            }
+            fence_proxy_async_smem();
         }
         __syncthreads();
         if (*abort_flag) { aborted = true; break; }
@@ -472,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (*abort_flag) { aborted = true; break; }
         // the K/Q stage of this chunk is free: prefetch chunk ci + kStages
-        if (ci + kStages < nchunks) {
+        if (use_tma && ci + kStages < nchunks) {
             if (threadIdx.x == 0) issue_tma(ci + kStages);
             tma_issued = ci + kStages + 1;
         }
@@ -481,13 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             float row[64];
             const float gC = gam[63];
-            // M = d_k accumulator: d_k = 128 -> lane = row; 64 -> M = 64 layout
+            // M = 128 accumulator: lane = state row
             ld_row64(tmem, warp, kColS, row);
-            if (srow >= 0) {
 #pragma unroll
-                for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
-                store_split_row(Shi, Slo, srow, S);
-            }
+            for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
+            store_split_row(Shi, Slo, threadIdx.x, S);
             if (want_out) {
                 const bool mine = mrow >= 0 && mrow < nv;
                 const float gi = mine ? gam[mrow] : 0.f;
@@ -571,12 +600,15 @@ bool make_qk_map(CUtensorMap* m, const uint16_t* base, long long rows, int H, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int K>
-cudaError_t launch_tc_k(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+cudaError_t launch_tc(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    constexpr int K = 128;
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
     if (rows == 0) return launch_fwd_simt(a, stream);  // nothing to load: state pass-through only
-    CUtensorMap mk, mq;
-    if (!make_qk_map(&mk, a.k, rows, a.H, K) || !make_qk_map(&mq, a.q, rows, a.H, K)) return cudaErrorInvalidValue;
+    CUtensorMap mk, mq;  // used only for d_k = 128 (d_k = 64 tiles use plain loads)
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    if (a.d_k == 128 && (!make_qk_map(&mk, a.k, rows, a.H, a.d_k) || !make_qk_map(&mq, a.q, rows, a.H, a.d_k)))
+        return cudaErrorInvalidValue;
     const int smem = TcSmem<K>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(gdn_fwd_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -589,8 +621,7 @@ cudaError_t launch_tc_k(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stre
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
-    if (a.d_k == 64) return launch_tc_k<64>(a, wait_limit, stream);
-    return launch_tc_k<128>(a, wait_limit, stream);
+    return launch_tc(a, wait_limit, stream);
 }
 
 }  // namespace gdn

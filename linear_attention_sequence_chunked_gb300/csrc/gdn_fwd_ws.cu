@@ -1,0 +1,719 @@
+// Chunked gated delta rule forward, warp-specialised tensor-core version.
+//
+// One CTA (256 threads) per (64-column value slice, head, sequence).  Two
+// warpgroups run concurrently, one chunk apart:
+//
+//   prep  (warps 4-7), chunk c+1:  g cumsum; [K;Q] K^T on the tensor cores;
+//         A = beta_i (k_i.k_j) exp(G_i - G_j) (j < i) and the causal score
+//         P = (q_i.k_j) exp(G_i - G_j) (j <= i); T = (I + A)^-1 in fp32 on the
+//         CUDA cores; T and P written as bf16 hi/lo operand tiles.
+//   chain (warps 0-3), chunk c:    K S, Q S -> R = beta o (V - gam o (K S));
+//         Delta = T R; S <- gam_n S + K^T (dec o Delta); O = scale
+//         [gam o (Q S) + P Delta].  S (fp32) lives in the chain's registers.
+//
+// The algebra is the one of the single-warpgroup kernel (gdn_fwd_tc.cu):
+// Delta = T R equals u - w S0 of the WY form (u = T diag(beta) V,
+// w = T diag(beta gam) K), i.e. beta_i times the error v_i - v_old_i of the
+// "Research Sprint Day 1" GDN update loop; decay is kept as a running sum of
+// g ("Research Sprint Day 2 - Rooflines", GDN pseudocode step 5).  Computed
+// MMA operands are split into bf16 hi + lo parts (fla issue #1550 traces the
+// error of bf16 chunk kernels to rounding these intermediates), all
+// accumulation is fp32 in tensor memory.
+//
+// Hand-offs are mbarriers (bounded waits): stage full (TMA), gram done,
+// prep ready (T, P, gates of a chunk), T/gate slot free, P free, and the
+// chain's own MMA completions.  Warpgroup-internal ordering uses named
+// barriers 1 (chain) and 2 (prep).
+#include <cuda.h>
+#include <string.h>
+
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace gdn {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 256;
+constexpr int kVs = 64;
+constexpr int kStages = 2;
+constexpr int kLd = 65;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kDk = 128;  // key width of the tiles (d_k = 64 zero-fills the upper half)
+
+constexpr uint32_t kColG = 0;
+constexpr uint32_t kColKS = 64;
+constexpr uint32_t kColQS = 128;
+constexpr uint32_t kColD = 192;
+constexpr uint32_t kColPD = 256;
+constexpr uint32_t kColS = 320;
+
+constexpr int kRegionBytes = 128 * 128;             // [K rows ; Q rows] x 128 B
+constexpr int kRegions = kDk / 64;
+constexpr int kStageBytes = kRegions * kRegionBytes;
+constexpr int kTile64 = 64 * 128;
+constexpr int kTileS = kDk * 128;
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr int oStage = 0;
+constexpr int oShi = oStage + kStages * kStageBytes;
+constexpr int oSlo = oShi + kTileS;
+constexpr int oRhi = oSlo + kTileS;
+constexpr int oRlo = oRhi + kTile64;
+constexpr int oDhi = oRlo + kTile64;
+constexpr int oDlo = oDhi + kTile64;
+constexpr int oPhi = oDlo + kTile64;
+constexpr int oPlo = oPhi + kTile64;
+constexpr int oT = oPlo + kTile64;                  // [slot][hi,lo] tiles
+constexpr int oA = oT + 4 * kTile64;
+constexpr int oTf = oA + 64 * kLd * 4;
+constexpr int oX = oTf + 64 * kLd * 4;
+constexpr int oVec = oX + 3 * 256 * 4;              // [slot][g, beta, G, gam, dec] x 64 fp32
+constexpr int kVecFloats = 5 * 64;
+constexpr int oBar = oVec + 2 * kVecFloats * 4;
+constexpr int kBars = 16;
+constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
+constexpr int kBytes = oMisc + 16;
+constexpr int kAlloc = kBytes + 1024;
+static_assert(kAlloc <= 232448, "shared memory");
+
+// barrier indices
+enum {
+    B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
+    B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_PFREE = 11,
+    B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15
+};
+
+__device__ __forceinline__ void named_bar(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(128) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
+    return a | (b << 16);
+}
+
+__device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_lo, int row, const float* x) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = x[ch * 8 + 2 * e], b = x[ch * 8 + 2 * e + 1];
+            const float ah = __bfloat162float(__float2bfloat16_rn(a));
+            const float bh = __bfloat162float(__float2bfloat16_rn(b));
+            h[e] = pack_bf16x2(ah, bh);
+            l[e] = pack_bf16x2(a - ah, b - bh);
+        }
+        const uint32_t off = sw128_offset(row, ch * 16);
+        *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
+
+__device__ __forceinline__ void ld_row64(uint32_t tmem, int sub, uint32_t col, float* v) {
+    const uint32_t a = tmem + (static_cast<uint32_t>(sub * 32) << 16) + col;
+    tmem_ld16(a, v);
+    tmem_ld16(a + 16, v + 16);
+    tmem_ld16(a + 32, v + 32);
+    tmem_ld16(a + 48, v + 48);
+    tmem_ld_wait();
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// exp(x) for x <= 0 through the hardware base-2 exponential.
+__device__ __forceinline__ float exp_nonpos(float x) { return exp2f(x * kLog2e); }
+
+// fp32 inverse of the unit lower triangular (I + A) by the prep warpgroup
+// (p = 0..127).  A strictly lower, row stride kLd; writes Tf (upper zero).
+// Diagonal 16x16 blocks: right-looking forward substitution per column (the
+// dependent chain is one FMA per step).  Off-diagonal blocks by distance:
+// T_IJ = -T_II sum_{J <= L < I} A_IL T_LJ.
+__device__ __forceinline__ void tri_inverse_wg(const float* A, float* Tf, float* X, int p) {
+    for (int e = p; e < 64 * 64; e += 128) {
+        const int i = e >> 6, j = e & 63;
+        if ((i >> 4) < (j >> 4)) Tf[i * kLd + j] = 0.f;
+    }
+    if (p < 64) {
+        const int o = (p >> 4) * 16;
+        const int c = p & 15;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = (i == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float cm = (m < c) ? 0.f : acc[m];
+            acc[m] = cm;
+#pragma unroll
+            for (int i = m + 1; i < 16; ++i) acc[i] = fmaf(-A[(o + i) * kLd + o + m], cm, acc[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Tf[(o + i) * kLd + o + c] = acc[i];
+    }
+    named_bar(2);
+    for (int dist = 1; dist < 4; ++dist) {
+        const int nblk = 4 - dist;
+        for (int e = p; e < nblk * 256; e += 128) {
+            const int bi = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int I = bi + dist, J = bi;
+            float acc0 = 0.f, acc1 = 0.f;
+            for (int L = J; L < I; ++L)
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    acc0 = fmaf(A[(I * 16 + r) * kLd + L * 16 + m], Tf[(L * 16 + m) * kLd + J * 16 + c], acc0);
+                    acc1 = fmaf(A[(I * 16 + r) * kLd + L * 16 + m + 1], Tf[(L * 16 + m + 1) * kLd + J * 16 + c], acc1);
+                }
+            X[bi * 256 + r * 16 + c] = acc0 + acc1;
+        }
+        named_bar(2);
+        for (int e = p; e < nblk * 256; e += 128) {
+            const int bi = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int I = bi + dist, J = bi;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                acc0 = fmaf(Tf[(I * 16 + r) * kLd + I * 16 + m], X[bi * 256 + m * 16 + c], acc0);
+                acc1 = fmaf(Tf[(I * 16 + r) * kLd + I * 16 + m + 1], X[bi * 256 + (m + 1) * 16 + c], acc1);
+            }
+            Tf[(I * 16 + r) * kLd + J * 16 + c] = -(acc0 + acc1);
+        }
+        named_bar(2);
+    }
+}
+
+struct WsParams {
+    FwdArgs a;
+    uint32_t wait_limit;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                      const WsParams prm) {
+    const FwdArgs& p = prm.a;
+    const int vs = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int H = p.H, V = p.d_v, dk = p.d_k;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+    const bool use_tma = dk == kDk;
+    const long long row_base = static_cast<long long>(b) * p.T;
+    const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+    const bool want_out = p.out != nullptr;
+    const uint32_t wl = prm.wait_limit;
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kBars; ++i) mbar_init(bar(i), 1);
+        fence_mbar_init();
+        *abort_flag = 0;
+        if (use_tma) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_q);
+        }
+    }
+    // d_k = 64: the upper key region of every stage stays zero
+    if (!use_tma) {
+        for (int st = 0; st < kStages; ++st) {
+            uint4* z = reinterpret_cast<uint4*>(sm + oStage + st * kStageBytes + kRegionBytes);
+            for (int i = tid; i < kRegionBytes / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    auto issue_tma = [&](int ci) {
+        const int st = ci % kStages;
+        uint8_t* base = sm + oStage + st * kStageBytes;
+        const int z = static_cast<int>(row_base + t0 + ci * kChunk);
+        mbar_arrive_expect_tx(bar(B_FULL0 + st), kStageBytes);
+#pragma unroll
+        for (int r = 0; r < kRegions; ++r) {
+            tma_load_3d(smem_u32(base + r * kRegionBytes), &tmap_k, r * 64, h, z, bar(B_FULL0 + st));
+            tma_load_3d(smem_u32(base + r * kRegionBytes + 64 * 128), &tmap_q, r * 64, h, z, bar(B_FULL0 + st));
+        }
+    };
+
+    if (warp < 4) {
+        // ======================= chain warpgroup =======================
+        const int t = tid;
+        const int mrow = m64_row(warp, lane);
+        const int srow = t < dk ? t : -1;
+        const long long KV = static_cast<long long>(dk) * V;
+        const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
+        const long long slot0 = chunk_slot_base(p.cu_seqlens, n, p.T);
+        const float scale = p.scale;
+        uint8_t* Shi = sm + oShi;
+        uint8_t* Slo = sm + oSlo;
+        uint8_t* Rhi = sm + oRhi;
+        uint8_t* Rlo = sm + oRlo;
+        uint8_t* Dhi = sm + oDhi;
+        uint8_t* Dlo = sm + oDlo;
+        int tma_issued = 0, tma_done = 0;
+        if (use_tma && t == 0) {
+            for (int ci = 0; ci < kStages && ci < nchunks; ++ci) issue_tma(ci);
+        }
+        if (use_tma) tma_issued = min(kStages, nchunks);
+
+        float S[kVs];
+#pragma unroll
+        for (int j = 0; j < kVs; ++j) S[j] = 0.f;
+        if (srow >= 0 && p.initial_state) {
+            const float* src = p.initial_state + state_off + static_cast<long long>(srow) * V;
+#pragma unroll
+            for (int j = 0; j < kVs; j += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(src + j);
+                S[j] = t4.x; S[j + 1] = t4.y; S[j + 2] = t4.z; S[j + 3] = t4.w;
+            }
+        }
+        store_split_row(Shi, Slo, t, S);
+        fence_proxy_async_smem();
+        named_bar(1);
+
+        bool aborted = false;
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int c0 = t0 + ci * kChunk;
+            const int nv = min(kChunk, t1 - c0);
+            const int st = ci & 1, slot = ci & 1;
+            const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
+            const uint32_t stage_a = smem_u32(sm + oStage + st * kStageBytes);
+            const float* vec = reinterpret_cast<const float*>(sm + oVec) + slot * kVecFloats;
+            const float* bv = vec + 64;
+            const float* gam = vec + 192;
+            const float* dec = vec + 256;
+
+            if (p.chunk_states && srow >= 0) {
+                float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
+#pragma unroll
+                for (int j = 0; j < kVs; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
+            uint4 vraw[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
+            if (mrow >= 0 && mrow < nv) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
+            }
+            // K/Q tiles of this chunk
+            if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
+            named_bar(1);
+            if (*abort_flag) { aborted = true; break; }
+            tma_done = ci + 1;
+
+            // ---- C1: K S and Q S ----
+            if (t == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                    const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                    const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                    mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
+                    mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                }
+                mma_commit(bar(B_KS));
+                if (want_out) {
+#pragma unroll
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                        const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                        mma_bf16(tmem + kColQS, a_q, b_hi, id_s, s > 0);
+                        mma_bf16(tmem + kColQS, a_q, b_lo, id_s, 1);
+                    }
+                }
+            }
+            __syncwarp();
+            bool ok = mbar_wait(bar(B_READY0 + slot), ph2, wl);
+            ok = mbar_wait(bar(B_KS), ph, wl) && ok;
+            if (!ok) *abort_flag = 1;
+            tc_fence_after();
+            named_bar(1);
+            if (*abort_flag) { aborted = true; break; }
+
+            // ---- C2: R = beta o (V - gam o (K S)) ----
+            {
+                float row[64];
+                ld_row64(tmem, warp, kColKS, row);
+                if (mrow >= 0) {
+                    const float bj = bv[mrow], gj = gam[mrow];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int c = ch * 8 + 2 * m;
+                            row[c] = bj * (__uint_as_float(w4[m] << 16) - gj * row[c]);
+                            row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
+                        }
+                    }
+                    store_split_row(Rhi, Rlo, mrow, row);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(1);
+
+            // ---- C3: Delta = T R ----
+            if (t == 0) {
+                tc_fence_after();
+                constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64);
+                const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t th = desc_sw128(thi + s * 32, 0, 1024);
+                    const uint64_t tl = desc_sw128(tlo + s * 32, 0, 1024);
+                    const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                    const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColD, th, rh, id, s > 0);
+                    mma_bf16(tmem + kColD, th, rl, id, 1);
+                    mma_bf16(tmem + kColD, tl, rh, id, 1);
+                }
+                mma_commit(bar(B_D));
+            }
+            __syncwarp();
+            if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
+            tc_fence_after();
+            named_bar(1);
+            if (*abort_flag) { aborted = true; break; }
+
+            // ---- C4: Delta tiles and dec o Delta tiles ----
+            {
+                float row[64];
+                ld_row64(tmem, warp, kColD, row);
+                if (mrow >= 0) {
+                    store_split_row(Dhi, Dlo, mrow, row);
+                    const float dj = dec[mrow];
+#pragma unroll
+                    for (int c = 0; c < kVs; ++c) row[c] *= dj;
+                    store_split_row(Rhi, Rlo, mrow, row);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(1);
+
+            // ---- C5: S update and P Delta ----
+            if (t == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
+                constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
+                    const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                    const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColS, ak, rh, id_s, s > 0);
+                    mma_bf16(tmem + kColS, ak, rl, id_s, 1);
+                }
+                mma_commit(bar(B_S));
+                if (want_out) {
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ph_ = desc_sw128(smem_u32(sm + oPhi) + s * 32, 0, 1024);
+                        const uint64_t pl_ = desc_sw128(smem_u32(sm + oPlo) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                        const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
+                        mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
+                        mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                    }
+                }
+                mma_commit(bar(B_PD));
+            }
+            __syncwarp();
+            if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
+            tc_fence_after();
+            named_bar(1);
+            if (*abort_flag) { aborted = true; break; }
+            // every MMA that reads this chunk's K/Q stage has completed
+            if (t == 0) {
+                if (use_tma) {
+                    if (ci + kStages < nchunks) issue_tma(ci + kStages);
+                } else {
+                    mbar_arrive(bar(B_SFREE0 + st));
+                }
+            }
+            if (use_tma && ci + kStages < nchunks) tma_issued = ci + kStages + 1;
+
+            // ---- C6: state update ----
+            {
+                float row[64];
+                const float gC = gam[63];
+                ld_row64(tmem, warp, kColS, row);
+#pragma unroll
+                for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                store_split_row(Shi, Slo, t, S);
+            }
+            if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
+            tc_fence_after();
+            named_bar(1);
+            if (*abort_flag) { aborted = true; break; }
+            if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
+            // ---- output ----
+            if (want_out) {
+                const bool mine = mrow >= 0 && mrow < nv;
+                const float gi = mine ? gam[mrow] : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(
+                    p.out + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
+                const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+#pragma unroll
+                for (int q16 = 0; q16 < 4; ++q16) {
+                    float qs[16], pd[16];
+                    tmem_ld16(tmem + lane_base + kColQS + q16 * 16, qs);
+                    tmem_ld16(tmem + lane_base + kColPD + q16 * 16, pd);
+                    tmem_ld_wait();
+                    if (mine) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = half * 8 + 2 * e;
+                                w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]),
+                                                    scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                            }
+                            dst[q16 * 2 + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(1);
+            if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
+            if (*abort_flag) { aborted = true; break; }
+        }
+        if (aborted) {
+            if (t == 0) {
+                record_error(p.err, kErrTimeout);
+                mma_commit(bar(B_DRAIN0));
+                mbar_wait(bar(B_DRAIN0), 0, wl);
+                for (int ci = tma_done; ci < tma_issued; ++ci)
+                    mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
+            }
+        } else if (p.final_state && srow >= 0) {
+            float* dst = p.final_state + state_off + static_cast<long long>(srow) * V;
+#pragma unroll
+            for (int j = 0; j < kVs; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+    } else {
+        // ======================= prep warpgroup =======================
+        const int q = tid - 128;          // 0..127
+        const int sub = warp - 4;         // TMEM subpartition
+        float* Am = reinterpret_cast<float*>(sm + oA);
+        float* Tf = reinterpret_cast<float*>(sm + oTf);
+        float* X = reinterpret_cast<float*>(sm + oX);
+        bool aborted = false;
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int c0 = t0 + ci * kChunk;
+            const int nv = min(kChunk, t1 - c0);
+            const int st = ci & 1, slot = ci & 1;
+            const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
+            uint8_t* stage = sm + oStage + st * kStageBytes;
+            float* vec = reinterpret_cast<float*>(sm + oVec) + slot * kVecFloats;
+            float* gv = vec;
+            float* bv = vec + 64;
+            float* Gv = vec + 128;
+            float* gam = vec + 192;
+            float* dec = vec + 256;
+
+            // gates of this chunk into its slot (free once the chain finished chunk ci - 2)
+            bool ok = true;
+            if (ci >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((ci - 2) >> 1) & 1, wl);
+            if (!ok) *abort_flag = 1;
+            named_bar(2);
+            if (*abort_flag) { aborted = true; break; }
+            if (q < 64) {
+                const long long idx = (row_base + c0 + q) * H + h;
+                gv[q] = (q < nv) ? p.g[idx] : 0.f;
+                bv[q] = (q < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
+            }
+            named_bar(2);
+            if (q < 32) {
+                const float a = gv[2 * q];
+                const float bb = a + gv[2 * q + 1];
+                float s = bb;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, s, off);
+                    if (q >= off) s += o;
+                }
+                const float base = s - bb;
+                Gv[2 * q] = base + a;
+                Gv[2 * q + 1] = s;
+                gam[2 * q] = exp_nonpos(base + a);
+                gam[2 * q + 1] = exp_nonpos(s);
+            }
+            named_bar(2);
+            if (q < 64) dec[q] = exp_nonpos(Gv[63] - Gv[q]);
+
+            // K/Q tiles
+            if (!use_tma) {
+                ok = true;
+                if (ci >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((ci - 2) >> 1) & 1, wl);
+                if (!ok) *abort_flag = 1;
+                named_bar(2);
+                if (*abort_flag) { aborted = true; break; }
+                for (int e = q; e < 2 * 64 * 8; e += 128) {
+                    const int which = e >> 9;
+                    const int r = (e >> 3) & 63, ch = e & 7;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (r < nv) {
+                        const uint16_t* src = which ? p.q : p.k;
+                        val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
+                    }
+                    *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+                }
+                fence_proxy_async_smem();
+                named_bar(2);
+                if (q == 0) mbar_arrive(bar(B_FULL0 + st));
+            }
+            if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
+            named_bar(2);
+            if (*abort_flag) { aborted = true; break; }
+
+            // gram [K;Q] K^T
+            if (q == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 128, 64);
+                const uint32_t stage_a = smem_u32(stage);
+#pragma unroll
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    const uint64_t a_kq = desc_sw128(stage_a + koff, 0, 1024);
+                    mma_bf16(tmem + kColG, a_kq, a_kq, id_g, s > 0);
+                }
+                mma_commit(bar(B_GRAM));
+            }
+            __syncwarp();
+            if (!mbar_wait(bar(B_GRAM), ph, wl)) *abort_flag = 1;
+            tc_fence_after();
+            named_bar(2);
+            if (*abort_flag) { aborted = true; break; }
+
+            float prow[64];
+            {
+                float row[64];
+                ld_row64(tmem, sub, kColG, row);
+                if (q < 64) {
+                    const float Gi = Gv[q], bi = bv[q];
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        Am[q * kLd + j] = (j < q) ? bi * row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+                } else {
+                    const int i = q - 64;
+                    const float Gi = Gv[i];
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) prow[j] = (j <= i) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+                }
+            }
+            tc_fence_before();
+            named_bar(2);
+            tri_inverse_wg(Am, Tf, X, q);
+            if (q < 64) {
+                float row[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) row[j] = Tf[q * kLd + j];
+                store_split_row(sm + oT + (slot * 2 + 0) * kTile64, sm + oT + (slot * 2 + 1) * kTile64, q, row);
+            }
+            // P tiles are single-buffered: wait until the chain's P Delta of chunk ci - 1 is done
+            ok = true;
+            if (ci >= 1) ok = mbar_wait(bar(B_PFREE), (ci - 1) & 1, wl);
+            if (!ok) *abort_flag = 1;
+            if (q >= 64 && ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
+            fence_proxy_async_smem();
+            named_bar(2);
+            if (*abort_flag) { aborted = true; break; }
+            if (q == 0) mbar_arrive(bar(B_READY0 + slot));
+        }
+        if (aborted && q == 0) {
+            record_error(p.err, kErrTimeout);
+            mma_commit(bar(B_DRAIN1));
+            mbar_wait(bar(B_DRAIN1), 0, wl);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 3-D view {d (inner), head, token row} of a (rows, H, 128) bf16 tensor; box
+// {64, 1, 64} = 64 token rows x 128 bytes, 128-byte swizzled.
+bool make_qk_map(CUtensorMap* m, const uint16_t* base, long long rows, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDk), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDk) * 2, static_cast<cuuint64_t>(H) * kDk * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
+    if (rows == 0) return launch_fwd_simt(a, stream);  // nothing to load: state pass-through only
+    CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    if (a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gdn_fwd_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    if (e != cudaSuccess) return e;
+    WsParams prm{a, wait_limit};
+    dim3 grid(a.d_v / kVs, a.H, a.N);
+    gdn_fwd_ws_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

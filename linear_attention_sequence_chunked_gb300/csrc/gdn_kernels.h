@@ -58,6 +58,8 @@ constexpr int kBwdVs = 32;
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
 // Tensor-core forward; wait_limit bounds every mbarrier wait (polls).
 cudaError_t launch_fwd_tc(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
+// Warp-specialised tensor-core forward (prep and chain warpgroups).
+cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 constexpr uint32_t kDefaultWaitLimit = 4000000u;
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_reduce(const float* dq_part, const float* dk_part, const float* dg_part,
