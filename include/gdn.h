@@ -141,6 +141,34 @@ GDN_API gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
 GDN_API gdn_status gdn_get_last_device_error(cudaStream_t stream);
 
 /*
+ * Backward without any allocation: gdn_chunk_bwd with the same arguments
+ * except the workspace, which comes from a device array built into the
+ * library (GDN_NOALLOC_SCRATCH_BYTES bytes, held by every device that loads
+ * the library until the process exits).  The pages have no counterpart; it
+ * exists for callers that may not allocate device memory themselves (a
+ * runtime that fixes its memory plan at start-up, a plugin whose host
+ * framework owns all allocations), which therefore cannot supply a
+ * workspace.  The caller still allocates and passes inputs and outputs.
+ *   - Sizes whose workspace (gdn_chunk_bwd_workspace_size) exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES return GDN_ERR_UNSUPPORTED before any launch.
+ *   - The first call on a device looks up the array's device address (a
+ *     host-side runtime query); make that first call before any stream
+ *     capture.
+ *   - All calls in the process share the one array per device: calls whose
+ *     work overlaps on the GPU (e.g. on two streams at once) race and give
+ *     wrong results.  Serialise them.
+ * Never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+GDN_API gdn_status gdn_chunk_bwd_noalloc(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                         const float* g, const gdn_bf16* beta, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         const gdn_bf16* d_out, const float* d_final_state,
+                         gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                         gdn_bf16* dbeta, float* d_initial_state,
+                         int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
+
+/*
  * Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points).  Library bookkeeping with no counterpart
  * on the pages; lets a caller count the kernels inside a timed region.

@@ -70,6 +70,8 @@ def load():
         lib.gdn_chunk_bwd.restype = i
         lib.gdn_get_last_device_error.argtypes = [vp]
         lib.gdn_get_last_device_error.restype = i
+        lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
+        lib.gdn_chunk_bwd_noalloc.restype = i
         lib.gdn_kernel_launches.argtypes = []
         lib.gdn_kernel_launches.restype = ctypes.c_uint64
         _lib = lib
@@ -132,6 +134,19 @@ def gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_f
                               _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "gdn_chunk_bwd")
+
+
+def gdn_chunk_bwd_noalloc(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
+                          dq, dk, dv, dg, dbeta, d_initial_state, B, T, H, d_k, d_v, stream=None):
+    """gdn_chunk_bwd without a workspace argument: for callers that may not
+    allocate device memory, the scratch comes from a fixed array inside the
+    library (GDN_NOALLOC_SCRATCH_BYTES).  Calls that overlap on the GPU race."""
+    st = load().gdn_chunk_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                      _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out),
+                                      _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                      _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
+                                      _stream(stream))
+    _check(st, "gdn_chunk_bwd_noalloc")
 
 
 def gdn_get_last_device_error(stream=None) -> int:

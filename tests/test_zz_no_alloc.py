@@ -1,0 +1,66 @@
+"""The backward entry point that allocates nothing (gdn_chunk_bwd_noalloc).
+
+Some callers may not allocate device memory themselves -- a runtime that
+fixes its memory plan at start-up, or a plugin whose host framework owns all
+device allocations -- so they cannot pass the workspace gdn_chunk_bwd needs.
+gdn_chunk_bwd_noalloc takes its scratch from an array built into the library
+instead.  This file is collected last on purpose: it checks the variant
+against the ordinary entry point, twice in a row (the shared scratch keeps
+the previous call's contents), and it passes alone or after the other tests.
+"""
+
+import numpy as np
+import pytest
+
+from linear_attention_sequence_chunked_gb300 import gdn
+from linear_attention_sequence_chunked_gb300 import workloads as W
+from oracle import metrics
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_bwd(wl):
+    import torch
+    d = G.to_device(wl)
+    B = wl.n_seq
+    dev = "cuda"
+    out = dict(dq=torch.empty(d["q"].shape, dtype=torch.bfloat16, device=dev),
+               dk=torch.empty(d["k"].shape, dtype=torch.bfloat16, device=dev),
+               dv=torch.empty(d["v"].shape, dtype=torch.bfloat16, device=dev),
+               dg=torch.empty(d["g"].shape, dtype=torch.float32, device=dev),
+               dbeta=torch.empty(d["beta"].shape, dtype=torch.bfloat16, device=dev),
+               dS0=torch.empty((B, wl.H, wl.d_k, wl.d_v), dtype=torch.float32, device=dev))
+    gdn.gdn_chunk_bwd_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.scale,
+                              d["initial_state"], d["cu_seqlens"], d["d_out"], d["d_final_state"],
+                              out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], out["dS0"],
+                              B, wl.T, wl.H, wl.d_k, wl.d_v)
+    assert gdn.gdn_get_last_device_error() == 0
+    res = {n: G.bf16_to_np(out[n]) for n in ("dq", "dk", "dv", "dbeta")}
+    res["dg"] = out["dg"].cpu().numpy()
+    res["dS0"] = out["dS0"].cpu().numpy()
+    return res
+
+
+def test_noalloc_backward_matches_workspace_backward_twice():
+    wl = W.random_workload(B=2, T=200, H=2, d_k=128, d_v=128, seed=21, beta_max=2.0,
+                           initial_state=True, with_grad=True, d_final_state=True)
+    ref = G.run_bwd(wl)
+    for call in range(2):
+        res = _noalloc_bwd(wl)
+        for name in ref:
+            e = metrics.rel_l2(res[name], ref[name])
+            assert np.all(np.isfinite(res[name])), (call, name)
+            assert e <= G.TOL_RMS_GRAD, (call, name, e)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    import torch
+    # B=8, T=4096, H=16, d=128 needs far more than the built-in scratch
+    need = gdn.gdn_chunk_bwd_workspace_size(8, 4096, 16, 128, 128, 0)
+    assert need > (64 << 20)
+    x = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: rejected first
+    with pytest.raises(gdn.GdnError) as err:
+        gdn.gdn_chunk_bwd_noalloc(x, x, x, x, x, 1.0, None, None, x, None, x, x, x, x, x, None,
+                                  8, 4096, 16, 128, 128)
+    assert err.value.status == 2
