@@ -126,7 +126,7 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens;
     a.out = out; a.final_state = final_state; a.chunk_states = nullptr;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
-    if (!launched(gdn::launch_fwd_tc(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    if (!launched(gdn::launch_fwd_ws(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 
