@@ -40,7 +40,6 @@ using namespace sm100;
 constexpr int kThreads = 256;
 constexpr int kVs = 64;
 constexpr int kStages = 2;
-constexpr int kLd = 65;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kDk = 128;  // key width of the tiles (d_k = 64 zero-fills the upper half)
 
@@ -68,10 +67,8 @@ constexpr int oDlo = oDhi + kTile64;
 constexpr int oPhi = oDlo + kTile64;
 constexpr int oPlo = oPhi + kTile64;
 constexpr int oT = oPlo + kTile64;                  // [slot][hi,lo] tiles
-constexpr int oA = oT + 4 * kTile64;
-constexpr int oTf = oA + 64 * kLd * 4;
-constexpr int oX = oTf + 64 * kLd * 4;
-constexpr int oVec = oX + 3 * 256 * 4;              // [slot][g, beta, G, gam, dec] x 64 fp32
+constexpr int oA = oT + 4 * kTile64;                // A^T fp32 [64][64] (prep)
+constexpr int oVec = oA + 64 * 64 * 4;              // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
 constexpr int kBars = 16;
@@ -97,6 +94,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
     return a | (b << 16);
 }
 
+// Two fp32 -> packed bf16x2 (round to nearest even), element a in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 64 values of one row into
+// the swizzled rows `row` of two 128-byte-wide operand tiles.
 __device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_lo, int row, const float* x) {
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
@@ -104,10 +110,8 @@ __device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float a = x[ch * 8 + 2 * e], b = x[ch * 8 + 2 * e + 1];
-            const float ah = __bfloat162float(__float2bfloat16_rn(a));
-            const float bh = __bfloat162float(__float2bfloat16_rn(b));
-            h[e] = pack_bf16x2(ah, bh);
-            l[e] = pack_bf16x2(a - ah, b - bh);
+            h[e] = cvt_bf16x2(a, b);
+            l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
         }
         const uint32_t off = sw128_offset(row, ch * 16);
         *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -130,63 +134,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // exp(x) for x <= 0 through the hardware base-2 exponential.
 __device__ __forceinline__ float exp_nonpos(float x) { return exp2f(x * kLog2e); }
-
-// fp32 inverse of the unit lower triangular (I + A) by the prep warpgroup
-// (p = 0..127).  A strictly lower, row stride kLd; writes Tf (upper zero).
-// Diagonal 16x16 blocks: right-looking forward substitution per column (the
-// dependent chain is one FMA per step).  Off-diagonal blocks by distance:
-// T_IJ = -T_II sum_{J <= L < I} A_IL T_LJ.
-__device__ __forceinline__ void tri_inverse_wg(const float* A, float* Tf, float* X, int p) {
-    for (int e = p; e < 64 * 64; e += 128) {
-        const int i = e >> 6, j = e & 63;
-        if ((i >> 4) < (j >> 4)) Tf[i * kLd + j] = 0.f;
-    }
-    if (p < 64) {
-        const int o = (p >> 4) * 16;
-        const int c = p & 15;
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = (i == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float cm = (m < c) ? 0.f : acc[m];
-            acc[m] = cm;
-#pragma unroll
-            for (int i = m + 1; i < 16; ++i) acc[i] = fmaf(-A[(o + i) * kLd + o + m], cm, acc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) Tf[(o + i) * kLd + o + c] = acc[i];
-    }
-    named_bar(2);
-    for (int dist = 1; dist < 4; ++dist) {
-        const int nblk = 4 - dist;
-        for (int e = p; e < nblk * 256; e += 128) {
-            const int bi = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int I = bi + dist, J = bi;
-            float acc0 = 0.f, acc1 = 0.f;
-            for (int L = J; L < I; ++L)
-#pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    acc0 = fmaf(A[(I * 16 + r) * kLd + L * 16 + m], Tf[(L * 16 + m) * kLd + J * 16 + c], acc0);
-                    acc1 = fmaf(A[(I * 16 + r) * kLd + L * 16 + m + 1], Tf[(L * 16 + m + 1) * kLd + J * 16 + c], acc1);
-                }
-            X[bi * 256 + r * 16 + c] = acc0 + acc1;
-        }
-        named_bar(2);
-        for (int e = p; e < nblk * 256; e += 128) {
-            const int bi = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int I = bi + dist, J = bi;
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                acc0 = fmaf(Tf[(I * 16 + r) * kLd + I * 16 + m], X[bi * 256 + m * 16 + c], acc0);
-                acc1 = fmaf(Tf[(I * 16 + r) * kLd + I * 16 + m + 1], X[bi * 256 + (m + 1) * 16 + c], acc1);
-            }
-            Tf[(I * 16 + r) * kLd + J * 16 + c] = -(acc0 + acc1);
-        }
-        named_bar(2);
-    }
-}
 
 struct WsParams {
     FwdArgs a;
@@ -291,6 +238,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar(1);
 
+        // value row of this slice (row mrow of the chunk), packed bf16; the
+        // next chunk's row is fetched as soon as the current one is consumed
+        uint4 vraw[8];
+        auto load_v = [&](int cj) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
+            const int cc0 = t0 + cj * kChunk;
+            if (cj < nchunks && mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.v + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
+            }
+        };
+        load_v(0);
         bool aborted = false;
         for (int ci = 0; ci < nchunks; ++ci) {
             const int c0 = t0 + ci * kChunk;
@@ -308,15 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kVs; j += 4)
                     *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-            }
-            uint4 vraw[8];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
-            if (mrow >= 0 && mrow < nv) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
             }
             // K/Q tiles of this chunk
             if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
@@ -377,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_split_row(Rhi, Rlo, mrow, row);
                 }
             }
+            load_v(ci + 1);
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(1);
@@ -384,13 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- C3: Delta = T R ----
             if (t == 0) {
                 tc_fence_after();
-                constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64);
+                // A = T read MN-major from the T^T tile (row j holds column j of T)
+                constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 64, 64);
                 const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
                 const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    const uint64_t th = desc_sw128(thi + s * 32, 0, 1024);
-                    const uint64_t tl = desc_sw128(tlo + s * 32, 0, 1024);
+                    const uint64_t th = desc_sw128(thi + s * 2048, kTile64, 1024);
+                    const uint64_t tl = desc_sw128(tlo + s * 2048, kTile64, 1024);
                     const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
                     const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
                     mma_bf16(tmem + kColD, th, rh, id, s > 0);
@@ -530,9 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ======================= prep warpgroup =======================
         const int q = tid - 128;          // 0..127
         const int sub = warp - 4;         // TMEM subpartition
-        float* Am = reinterpret_cast<float*>(sm + oA);
-        float* Tf = reinterpret_cast<float*>(sm + oTf);
-        float* X = reinterpret_cast<float*>(sm + oX);
+        float* At = reinterpret_cast<float*>(sm + oA);  // A^T, row stride 64
+        // named barrier of warps 4-5 only (the A / inverse half)
+        auto half_bar = [] { asm volatile("bar.sync 3, 64;" ::: "memory"); };
         bool aborted = false;
         for (int ci = 0; ci < nchunks; ++ci) {
             const int c0 = t0 + ci * kChunk;
@@ -621,36 +576,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
 
-            float prow[64];
-            {
-                float row[64];
-                ld_row64(tmem, sub, kColG, row);
-                if (q < 64) {
+            // The two halves of the warpgroup now work side by side:
+            //   warps 4-5 (q < 64):  A row q -> A^T in shared memory -> T = (I + A)^-1
+            //   warps 6-7 (q >= 64): causal score row q - 64 -> P tiles
+            if (q < 64) {
+                {
+                    float row[64];
+                    ld_row64(tmem, sub, kColG, row);
                     const float Gi = Gv[q], bi = bv[q];
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        Am[q * kLd + j] = (j < q) ? bi * row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
-                } else {
+                        At[j * 64 + q] = (j < q) ? bi * row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+                }
+                tc_fence_before();
+                half_bar();
+                // Column c = q of T by right-looking forward substitution:
+                // x = e_c; for m: for i > m: x_i -= A_im x_m.  Row m of A^T is
+                // read as broadcast 16-byte loads; the dependent chain is one
+                // FMA per step.
+                float x[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) x[i] = (i == q) ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < 63; ++m) {
+                    const float xm = x[m];
+                    const float4* arow = reinterpret_cast<const float4*>(At + m * 64);
+#pragma unroll
+                    for (int i4 = (m + 1) >> 2; i4 < 16; ++i4) {
+                        const float4 a4 = arow[i4];
+                        if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
+                        if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
+                        if (4 * i4 + 2 > m) x[4 * i4 + 2] = fmaf(-a4.z, xm, x[4 * i4 + 2]);
+                        if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
+                    }
+                }
+                // column q of T = row q of the T^T tile (read MN-major by the MMA)
+                store_split_row(sm + oT + (slot * 2 + 0) * kTile64, sm + oT + (slot * 2 + 1) * kTile64, q, x);
+                ok = true;
+            } else {
+                float prow[64];
+                {
+                    float row[64];
+                    ld_row64(tmem, sub, kColG, row);
                     const int i = q - 64;
                     const float Gi = Gv[i];
 #pragma unroll
                     for (int j = 0; j < 64; ++j) prow[j] = (j <= i) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
                 }
+                tc_fence_before();
+                // P tiles are single-buffered: wait until the chain's P Delta of chunk ci - 1 is done
+                ok = true;
+                if (ci >= 1) ok = mbar_wait(bar(B_PFREE), (ci - 1) & 1, wl);
+                if (!ok) *abort_flag = 1;
+                if (ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
             }
-            tc_fence_before();
-            named_bar(2);
-            tri_inverse_wg(Am, Tf, X, q);
-            if (q < 64) {
-                float row[64];
-#pragma unroll
-                for (int j = 0; j < 64; ++j) row[j] = Tf[q * kLd + j];
-                store_split_row(sm + oT + (slot * 2 + 0) * kTile64, sm + oT + (slot * 2 + 1) * kTile64, q, row);
-            }
-            // P tiles are single-buffered: wait until the chain's P Delta of chunk ci - 1 is done
-            ok = true;
-            if (ci >= 1) ok = mbar_wait(bar(B_PFREE), (ci - 1) & 1, wl);
-            if (!ok) *abort_flag = 1;
-            if (q >= 64 && ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
             fence_proxy_async_smem();
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
