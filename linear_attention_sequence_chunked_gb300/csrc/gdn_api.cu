@@ -57,23 +57,20 @@ long long chunk_slots(int B, int T, int varlen) {
     return static_cast<long long>(B) * ((T + gdn::kChunk - 1) / gdn::kChunk);
 }
 
+// Backward workspace: per-chunk start states and T operand tiles (pass 1),
+// per-chunk end-state gradients (pass 2).
 struct BwdLayout {
-    size_t states, dq, dk, dg, dbeta, total;
+    size_t states, dstates, tiles, total;
 };
 
 BwdLayout bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     BwdLayout L{};
-    const long long rows = static_cast<long long>(varlen ? 1 : B) * T * H;
-    const int slices = d_v / gdn::kBwdVs;
-    const size_t states = round_up(sizeof(float) * chunk_slots(B, T, varlen) * H * d_k * d_v);
-    const size_t part_k = round_up(sizeof(float) * slices * rows * d_k);
-    const size_t part_r = round_up(sizeof(float) * slices * rows);
+    const long long slots = chunk_slots(B, T, varlen);
+    const size_t per_state = sizeof(float) * static_cast<size_t>(d_k) * d_v;
     L.states = 0;
-    L.dq = states;
-    L.dk = L.dq + part_k;
-    L.dg = L.dk + part_k;
-    L.dbeta = L.dg + part_r;
-    L.total = L.dbeta + part_r;
+    L.dstates = round_up(per_state * slots * H);
+    L.tiles = L.dstates + round_up(per_state * slots * H);
+    L.total = L.tiles + round_up(static_cast<size_t>(gdn::kChunkTBytes) * slots * H);
     return L;
 }
 
@@ -157,29 +154,33 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     if (!err) return GDN_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
     float* states = reinterpret_cast<float*>(ws + L.states);
+    float* dstates = reinterpret_cast<float*>(ws + L.dstates);
+    uint8_t* tiles = reinterpret_cast<uint8_t*>(ws + L.tiles);
 
+    // pass 1: chunk-start states and T tiles (forward state pass, no output)
     gdn::FwdArgs f{};
     f.q = q; f.k = k; f.v = v; f.g = g; f.beta = beta; f.scale = scale;
     f.initial_state = initial_state; f.cu_seqlens = cu_seqlens;
-    f.out = nullptr; f.final_state = nullptr; f.chunk_states = states;
+    f.out = nullptr; f.final_state = nullptr; f.chunk_states = states; f.chunk_T = tiles;
     f.N = B; f.T = T; f.H = H; f.d_k = d_k; f.d_v = d_v; f.err = err;
-    if (!launched(gdn::launch_fwd_simt(f, stream))) return GDN_ERR_CUDA;
+    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
 
-    gdn::BwdArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
-    a.cu_seqlens = cu_seqlens; a.d_out = d_out; a.d_final_state = d_final_state;
-    a.chunk_states = states;
-    a.dq_part = reinterpret_cast<float*>(ws + L.dq);
-    a.dk_part = reinterpret_cast<float*>(ws + L.dk);
-    a.dg_part = reinterpret_cast<float*>(ws + L.dg);
-    a.dbeta_part = reinterpret_cast<float*>(ws + L.dbeta);
-    a.dv = dv; a.d_initial_state = d_initial_state;
-    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
-    if (!launched(gdn::launch_bwd_simt(a, stream))) return GDN_ERR_CUDA;
-    const long long rows = static_cast<long long>(varlen ? 1 : B) * T * H;
-    if (rows > 0 && !launched(gdn::launch_bwd_reduce(a.dq_part, a.dk_part, a.dg_part, a.dbeta_part,
-                                         d_v / gdn::kBwdVs, rows, d_k, dq, dk, dg, dbeta, stream)))
-        return GDN_ERR_CUDA;
+    // pass 2: reverse chain of state gradients
+    gdn::BwdChainArgs c{};
+    c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
+    c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;
+    c.chunk_dstates = dstates; c.d_initial_state = d_initial_state;
+    c.N = B; c.T = T; c.H = H; c.d_k = d_k; c.d_v = d_v; c.err = err;
+    if (!launched(gdn::launch_bwd_chain(c, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+
+    // pass 3: chunk-parallel local gradients
+    gdn::BwdLocalArgs l{};
+    l.q = q; l.k = k; l.v = v; l.g = g; l.beta = beta; l.d_out = d_out; l.scale = scale;
+    l.cu_seqlens = cu_seqlens; l.chunk_states = states; l.chunk_dstates = dstates; l.chunk_T = tiles;
+    l.dq = dq; l.dk = dk; l.dv = dv; l.dg = dg; l.dbeta = dbeta;
+    l.N = B; l.T = T; l.H = H; l.d_k = d_k; l.d_v = d_v; l.err = err;
+    l.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
+    if (l.max_chunks > 0 && !launched(gdn::launch_bwd_local(l, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

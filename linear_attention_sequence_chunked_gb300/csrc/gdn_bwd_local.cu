@@ -1,0 +1,640 @@
+// Backward, pass 3: every local gradient of one chunk, chunk-parallel, on the
+// tensor cores.
+//
+// Given the chunk's start state S0 and its T operand tiles (pass 1) and the
+// gradient dS w.r.t. its end state (pass 2), the reverse mode of the chunk
+// forward (gdn_common.cuh) gives, with Bhat = diag(beta) V - diag(beta gam) K S0,
+// R = beta o (V - gam o (K S0)), Delta = T R:
+//   dDelta = scale P^T dO + dec o (K dS);   dBhat = T^T dDelta
+//   dP = scale dO Delta^T  -> dQK = dP o M,  dG from dP o P
+//   dA = -(dBhat Delta^T) o strict  -> dKK = dA o beta_i Ms,  dbeta, dG
+//   dV = beta o dBhat
+//   dQ = scale gam o (dO S0^T) + dQK K
+//   dK = dQK^T Q + dKK K + dKK^T K + (dec o Delta) dS^T - (beta gam o dBhat) S0^T
+//   dbeta, dgam, dG (decays), dg = reverse running sum of dG in the chunk.
+// Sums over value columns (dP, dA, dO S0^T, the S-terms of dK) accumulate in
+// tensor memory across 64-column value slices, so each CTA writes complete
+// gradients: no partial sums leave the chip.  One CTA (128 threads) per
+// (chunk, head, sequence).  Computed MMA operands are split into bf16 hi + lo,
+// accumulation is fp32.
+#include <cuda.h>
+
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+#include "gdn_tc_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace gdn {
+
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kThreads = 128;
+constexpr int kVs = 64;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kTileS = kDk * 128;  // 128 rows x 128 B
+
+// TMEM columns
+constexpr uint32_t cdA = 0;     // dA (M = 64)
+constexpr uint32_t cdP = 64;    // dP (M = 64)
+constexpr uint32_t cU = 128;    // dO S0^T (M = 64, N = 128)
+constexpr uint32_t cdK = 256;   // dK (M = 64, N = 128)
+constexpr uint32_t cX1 = 384;   // scratch (M = 64)
+constexpr uint32_t cX2 = 448;   // scratch (M = 64)
+
+// shared memory (1024-aligned tiles)
+constexpr int oKQ = 0;                          // [K;Q] regions, 2 x 16 KB
+constexpr int oT = oKQ + 2 * kRegionBytes;      // T^T-layout tiles hi, lo
+constexpr int oP = oT + 2 * kTile64;            // P tiles hi, lo [i][j]
+constexpr int oSA = oP + 2 * kTile64;           // S0 tiles hi, lo [d][v]
+constexpr int oSB = oSA + 2 * kTileS;           // dS tiles hi, lo [d][v]
+constexpr int oDO = oSB + 2 * kTileS;           // dO raw [i][v]
+constexpr int oRA = oDO + kTile64;              // R -> Delta (hi, lo) [j][v]; later dKK [i][j]
+constexpr int oRB = oRA + 2 * kTile64;          // dDelta -> dec o Delta; later dQK [i][j]
+constexpr int oRC = oRB + 2 * kTile64;          // -dBhat [i][v]
+constexpr int oRD = oRC + 2 * kTile64;          // Y = -beta gam dBhat [i][v]
+constexpr int oVec = oRD + 2 * kTile64;         // g, beta, G, gam, dec, colsum
+constexpr int oRed = oVec + 6 * 64 * 4;         // 8 floats reduction scratch
+constexpr int oBar = oRed + 64;
+constexpr int oMisc = oBar + 8;
+constexpr int kBytes = oMisc + 16;
+constexpr int kAlloc = kBytes + 1024;
+static_assert(kAlloc <= 232448, "shared memory");
+constexpr int oE = oSA;  // fp32 64 x 65 scratch for column sums (after the slices)
+
+__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLocalArgs p) {
+    const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int H = p.H, V = p.d_v, dk = p.d_k;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+    const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+    if (ci >= nchunks) return;
+    const int c0 = t0 + ci * kChunk;
+    const int nv = min(kChunk, t1 - c0);
+    const long long row_base = static_cast<long long>(b) * p.T;
+    const long long slot = chunk_slot_base(p.cu_seqlens, n, p.T) + ci;
+    const long long KV = static_cast<long long>(dk) * V;
+    const float scale = p.scale;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gv = reinterpret_cast<float*>(sm + oVec);
+    float* bv = gv + 64;
+    float* Gv = gv + 128;
+    float* gam = gv + 192;
+    float* dec = gv + 256;
+    float* colsum = gv + 320;
+    float* red = reinterpret_cast<float*>(sm + oRed);
+    uint64_t* barp = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
+    const uint32_t bar = smem_u32(barp);
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    // ---- K/Q tiles (plain 16-byte loads, rows beyond the chunk are zero) ----
+    for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
+        const int which = e >> 10;                // 0: K, 1: Q
+        const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
+        const int r = (e >> 3) & 63, ch = e & 7;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < nv && region * 64 < dk) {
+            const uint16_t* src = which ? p.q : p.k;
+            val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                  region * 64 + ch * 8);
+        }
+        *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+    }
+    // ---- T operand tiles of this chunk (written by pass 1, already swizzled) ----
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(p.chunk_T + (slot * H + h) * static_cast<long long>(kChunkTBytes));
+        uint4* dst = reinterpret_cast<uint4*>(sm + oT);
+        for (int e = tid; e < kChunkTBytes / 16; e += kThreads) dst[e] = src[e];
+    }
+    if (tid < 64) {
+        const long long idx = (row_base + c0 + tid) * H + h;
+        gv[tid] = (tid < nv) ? p.g[idx] : 0.f;
+        bv[tid] = (tid < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (tid < 32) {
+        const float a = gv[2 * tid];
+        const float bb = a + gv[2 * tid + 1];
+        float s = bb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, s, off);
+            if (tid >= off) s += o;
+        }
+        const float base = s - bb;
+        Gv[2 * tid] = base + a;
+        Gv[2 * tid + 1] = s;
+        gam[2 * tid] = exp_nonpos(base + a);
+        gam[2 * tid + 1] = exp_nonpos(s);
+    }
+    __syncthreads();
+    if (tid < 64) dec[tid] = exp_nonpos(Gv[63] - Gv[tid]);
+
+    uint32_t phase = 0;
+    bool failed = false;  // a bounded wait ran out (reported through the error word)
+    auto mma_sync_wait = [&]() {
+        if (tid == 0) mma_commit(bar);
+        __syncwarp();
+        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) failed = true;
+        phase ^= 1u;
+        tc_fence_after();
+    };
+    const uint32_t aKQ = smem_u32(sm + oKQ);
+    auto kdesc_K = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + (s & 3) * 32, 0, 1024); };
+    auto kdesc_Q = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + 64 * 128 + (s & 3) * 32, 0, 1024); };
+    // K or Q read MN-major as a B operand [K = token][N = key column], N = 128
+    auto mn_K = [&](int s) { return desc_sw128(aKQ + s * 2048, kRegionBytes, 1024); };
+    auto mn_Q = [&](int s) { return desc_sw128(aKQ + 64 * 128 + s * 2048, kRegionBytes, 1024); };
+    auto t64 = [&](int off) { return smem_u32(sm + off); };
+
+    // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+#pragma unroll
+        for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
+    }
+    mma_sync_wait();
+    const int mrow = m64_row(warp, lane);
+    {
+        float row[64];
+        ld_row64(tmem, warp, cX1, row);
+        if (mrow >= 0) {
+            const float Gi = Gv[mrow];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) row[j] = (j <= mrow) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+            store_split_row(sm + oP, sm + oP + kTile64, mrow, row);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // per-row accumulators (thread mrow) across value slices
+    float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
+    const int nslices = V / kVs;
+    for (int vs = 0; vs < nslices; ++vs) {
+        // ---- slice loads: S0, dS (fp32 -> hi/lo tiles), dO, V row ----
+        {
+            float srow[64], drow[64];
+            const int d = tid;  // state row
+#pragma unroll
+            for (int j = 0; j < 64; ++j) { srow[j] = 0.f; drow[j] = 0.f; }
+            if (d < dk) {
+                const float* s0 = p.chunk_states + (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs;
+                const float* s1 = p.chunk_dstates + (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(s0 + j);
+                    const float4 b4 = *reinterpret_cast<const float4*>(s1 + j);
+                    srow[j] = a4.x; srow[j + 1] = a4.y; srow[j + 2] = a4.z; srow[j + 3] = a4.w;
+                    drow[j] = b4.x; drow[j + 1] = b4.y; drow[j + 2] = b4.z; drow[j + 3] = b4.w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc_SdS = fmaf(srow[j], drow[j], acc_SdS);
+            store_split_row(sm + oSA, sm + oSA + kTileS, d, srow);
+            store_split_row(sm + oSB, sm + oSB + kTileS, d, drow);
+        }
+        for (int e = tid; e < 64 * 8; e += kThreads) {
+            const int r = e >> 3, ch = e & 7;
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (r < nv)
+                val = *reinterpret_cast<const uint4*>(
+                    p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
+            *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = val;
+        }
+        float vrow[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) vrow[j] = 0.f;
+        if (mrow >= 0 && mrow < nv) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) unpack8(src[ch], vrow + ch * 8);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- batch 1: K S0 -> X1, P^T dO -> X2 ----
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+            constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+            for (int s = 0; s < kDk / 16; ++s) {
+                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
+                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
+                mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
+                mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
+            }
+        }
+        mma_sync_wait();
+        float ks0[64], pdo[64];
+        ld_row64(tmem, warp, cX1, ks0);
+        ld_row64(tmem, warp, cX2, pdo);
+        if (mrow >= 0) {
+            float row[64];
+            const float bj = bv[mrow], gj = gam[mrow];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
+            store_split_row(sm + oRA, sm + oRA + kTile64, mrow, row);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- batch 2: K dS -> X1, Delta = T R -> X2 ----
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+            constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+            for (int s = 0; s < kDk / 16; ++s) {
+                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
+                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
+                const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
+                const uint64_t rh = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                const uint64_t rl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                mma_bf16(tmem + cX2, th, rh, id_t, s > 0);
+                mma_bf16(tmem + cX2, th, rl, id_t, 1);
+                mma_bf16(tmem + cX2, tl, rh, id_t, 1);
+            }
+        }
+        mma_sync_wait();
+        {
+            // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
+            // dd = dec * sum_v (K dS) Delta for the decay term of dG
+            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+            const float dj = (mrow >= 0) ? dec[mrow] : 0.f;
+            float dd = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float kds[16], dl[16];
+                tmem_ld16(tmem + lb + cX1 + g * 16, kds);
+                tmem_ld16(tmem + lb + cX2 + g * 16, dl);
+                tmem_ld_wait();
+                if (mrow >= 0) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        dd = fmaf(kds[c], dl[c], dd);
+                        kds[c] = fmaf(scale, pdo[g * 16 + c], dj * kds[c]);
+                    }
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g, kds);
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g + 1, kds + 8);
+                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 2 * g, dl);
+                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 2 * g + 1, dl + 8);
+                }
+            }
+            acc_dd = fmaf(dj, dd, acc_dd);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- batch 3: dBhat = T^T dDelta -> X1;  dP += dO Delta^T ----
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
+            constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
+                const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
+                const uint64_t dh = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                const uint64_t dl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                mma_bf16(tmem + cX1, th, dh, id_b, s > 0);
+                mma_bf16(tmem + cX1, th, dl, id_b, 1);
+                mma_bf16(tmem + cX1, tl, dh, id_b, 1);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
+                mma_bf16(tmem + cdP, ao, dl, id_p, 1);
+            }
+        }
+        mma_sync_wait();
+        {
+            // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RC, Y -> RD,
+            // dec o Delta (Delta re-read from X2) -> RB
+            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+            const bool mine = mrow >= 0;
+            const float bi = mine ? bv[mrow] : 0.f, gi = mine ? gam[mrow] : 0.f, dj = mine ? dec[mrow] : 0.f;
+            float sv = 0.f, sk = 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.dv + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float db[16], dl[16];
+                tmem_ld16(tmem + lb + cX1 + g * 16, db);
+                tmem_ld16(tmem + lb + cX2 + g * 16, dl);
+                tmem_ld_wait();
+                if (mine) {
+                    float t16[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        sv = fmaf(vrow[g * 16 + c], db[c], sv);
+                        sk = fmaf(ks0[g * 16 + c], db[c], sk);
+                    }
+                    if (mrow < nv) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
+                            dst[2 * g + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) t16[c] = -db[c];
+                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, 2 * g, t16);
+                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, 2 * g + 1, t16 + 8);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
+                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, 2 * g, t16);
+                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, 2 * g + 1, t16 + 8);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) t16[c] = dj * dl[c];
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g, t16);
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g + 1, t16 + 8);
+                }
+            }
+            acc_dbeta += sv - gi * sk;
+            acc_dgam -= bi * sk;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- batch 4: dA += (-dBhat) Delta^T; U += dO S0^T; dK += (dec o Delta) dS^T + Y S0^T ----
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
+            constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+            const uint32_t first = vs > 0 ? 1u : 0u;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t ch_ = desc_sw128(t64(oRC) + s * 32, 0, 1024);
+                const uint64_t cl_ = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
+                const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                mma_bf16(tmem + cdA, ch_, dh, id_c, (first || s > 0) ? 1u : 0u);
+                mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
+                mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
+                // B = S0 / dS tile read K-major: [N = key row d][K = value column]
+                const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
+                const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
+                const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
+                const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
+                const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                mma_bf16(tmem + cU, ao, sah, id_n, (first || s > 0) ? 1u : 0u);
+                mma_bf16(tmem + cU, ao, sal, id_n, 1);
+                const uint64_t eh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                const uint64_t el = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
+                const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
+                mma_bf16(tmem + cdK, eh, sbh, id_n, (first || s > 0) ? 1u : 0u);
+                mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
+                mma_bf16(tmem + cdK, el, sbh, id_n, 1);
+                mma_bf16(tmem + cdK, yh, sah, id_n, 1);
+                mma_bf16(tmem + cdK, yh, sal, id_n, 1);
+                mma_bf16(tmem + cdK, yl, sah, id_n, 1);
+            }
+        }
+        mma_sync_wait();
+        __syncthreads();
+    }
+
+    // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+#pragma unroll
+        for (int s = 0; s < kDk / 16; ++s) {
+            mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
+            mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
+        }
+    }
+    mma_sync_wait();
+    float* E = reinterpret_cast<float*>(sm + oE);  // 64 x 65: column-sum terms
+    float rowsum = 0.f, dbeta_a = 0.f;
+    {
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const bool mine = mrow >= 0;
+        const int i = mine ? mrow : 0;
+        const float Gi = Gv[i], bi = bv[i];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float kk[16], da[16], qk[16], dp[16];
+            tmem_ld16(tmem + lb + cX1 + g * 16, kk);
+            tmem_ld16(tmem + lb + cdA + g * 16, da);
+            tmem_ld16(tmem + lb + cX2 + g * 16, qk);
+            tmem_ld16(tmem + lb + cdP + g * 16, dp);
+            tmem_ld_wait();
+            if (mine) {
+                float dkk[16], dqk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int j = g * 16 + c;
+                    const float m = (j <= i) ? exp_nonpos(Gi - Gv[j]) : 0.f;
+                    // A side (strictly lower): dA o (K K^T o Ms)
+                    const float kkm = (j < i) ? kk[c] * m : 0.f;
+                    const float a = (j < i) ? da[c] : 0.f;
+                    dbeta_a = fmaf(a, kkm, dbeta_a);
+                    const float dms = a * bi * kkm;
+                    dkk[c] = a * bi * m;
+                    // P side (diagonal included): dQK = dP o M and dP o P
+                    const float dpm = scale * dp[c] * m;
+                    dqk[c] = dpm;
+                    const float e = dms + dpm * qk[c];
+                    rowsum += e;
+                    E[i * 65 + j] = e;
+                }
+                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, 2 * g, dkk);
+                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, 2 * g + 1, dkk + 8);
+                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, 2 * g, dqk);
+                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, 2 * g + 1, dqk + 8);
+            }
+        }
+    }
+    // <dS, S0> over the whole slice set (gam_n term of dgam)
+    {
+        float v = acc_SdS;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[warp] = v;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 64) {
+        float c = 0.f;
+        for (int i = 0; i < 64; ++i) c += E[i * 65 + tid];
+        colsum[tid] = c;
+    }
+    // ---- final products: dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
+        constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+            const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+            const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+            const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+            mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
+            mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
+            mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
+            mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
+            const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+            const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+            const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+            const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+            mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
+            mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
+            mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
+            mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
+        }
+    }
+    mma_sync_wait();
+    __syncthreads();
+    // ---- outputs of row mrow ----
+    float dG = 0.f, dbeta = 0.f;
+    {
+        const bool mine = mrow >= 0;
+        const int i = mine ? mrow : 0;
+        const float gi = gam[i];
+        // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
+        float dgam = acc_dgam;
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        for (int c16 = 0; c16 < 8; ++c16) {
+            float u[16], q2[16], kk2[16];
+            tmem_ld16(tmem + lb + cU + c16 * 16, u);
+            tmem_ld16(tmem + lb + cX1 + c16 * 16, q2);
+            tmem_ld16(tmem + lb + cdK + c16 * 16, kk2);
+            tmem_ld_wait();
+            if (!mine) continue;
+            const int region = c16 >> 2, cc = (c16 & 3) * 16;
+            float qrow[16];
+            {
+                const uint8_t* base = sm + oKQ + region * kRegionBytes + 64 * 128;
+                unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2)), qrow);
+                unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dgam = fmaf(scale * qrow[e], u[e], dgam);
+            if (i < nv && c16 * 16 < dk) {
+                uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+                uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t wq[4], wk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = half * 8 + 2 * e;
+                        wq[e] = pack_bf16x2(fmaf(scale * gi, u[c], q2[c]), fmaf(scale * gi, u[c + 1], q2[c + 1]));
+                        wk[e] = pack_bf16x2(kk2[c], kk2[c + 1]);
+                    }
+                    dq[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    dkp[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                }
+            }
+        }
+        if (mine) {
+            if (i == 63) dgam += red[0] + red[1] + red[2] + red[3];
+            dG = rowsum - colsum[i] - acc_dd + dgam * gi;
+            dbeta = acc_dbeta + dbeta_a;
+        }
+    }
+    // dG_63 also collects the decay terms sum_j dd_j
+    {
+        float v = (mrow >= 0) ? acc_dd : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[4 + warp] = v;
+    }
+    __syncthreads();
+    if (mrow >= 0) {
+        if (mrow == 63) dG += red[4] + red[5] + red[6] + red[7];
+        colsum[mrow] = dG;  // reuse as dG vector
+        bv[mrow] = dbeta;   // reuse as dbeta vector
+    }
+    __syncthreads();
+    // dg = reverse running sum of dG over the chunk (warp 0)
+    if (tid < 32) {
+        const int i0 = 63 - 2 * tid, i1 = 62 - 2 * tid;
+        const float a = colsum[i0], bb = colsum[i1];
+        float s = a + bb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, s, off);
+            if (tid >= off) s += o;
+        }
+        const float base = s - (a + bb);
+        if (i0 < nv) {
+            const long long row = (row_base + c0 + i0) * H + h;
+            p.dg[row] = base + a;
+            p.dbeta[row] = f32_to_bf16(bv[i0]);
+        }
+        if (i1 < nv) {
+            const long long row = (row_base + c0 + i1) * H + h;
+            p.dg[row] = s;
+            p.dbeta[row] = f32_to_bf16(bv[i1]);
+        }
+    }
+    if (failed) {
+        record_error(p.err, kErrTimeout);
+        if (tid == 0) {  // let every MMA this CTA issued land before the TMEM is released
+            mma_commit(bar);
+            mbar_wait(bar, phase, kDefaultWaitLimit);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
+    if (a.max_chunks == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gdn_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.max_chunks, a.H, a.N);
+    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

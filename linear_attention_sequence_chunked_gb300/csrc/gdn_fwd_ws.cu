@@ -1,4 +1,5 @@
-// Chunked gated delta rule forward, warp-specialised tensor-core version.
+// Chunked gated delta rule, warp-specialised tensor-core chunk chain: the
+// forward, and the reverse-chunk chain of state gradients of the backward.
 //
 // One CTA (256 threads) per (64-column value slice, head, sequence).  Two
 // warpgroups run concurrently, one chunk apart:
@@ -11,7 +12,16 @@
 //         Delta = T R; S <- gam_n S + K^T (dec o Delta); O = scale
 //         [gam o (Q S) + P Delta].  S (fp32) lives in the chain's registers.
 //
-// The algebra is the one of the single-warpgroup kernel (gdn_fwd_tc.cu):
+// Backward mode walks the chunks from last to first with the same prep; the
+// chain carries dS, the gradient w.r.t. a chunk's end state, and steps it to
+// the chunk's start state by the reverse mode of the update above:
+//         dDelta = scale P^T dO + dec o (K dS);   dBhat = T^T dDelta;
+//         dS <- gam_n dS + Q^T (scale gam o dO) - K^T (beta gam o dBhat).
+// T and P are the same operand tiles read in the other major order.  Per
+// chunk it stores dS (end-state gradient) for the chunk-parallel gradient
+// pass; the forward in state mode stores each chunk's start state and its T
+// tiles for the same pass.
+//
 // Delta = T R equals u - w S0 of the WY form (u = T diag(beta) V,
 // w = T diag(beta gam) K), i.e. beta_i times the error v_i - v_old_i of the
 // "Research Sprint Day 1" GDN update loop; decay is kept as a running sum of
@@ -29,6 +39,7 @@
 
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
+#include "gdn_tc_common.cuh"
 #include "sm100_ptx.cuh"
 
 namespace gdn {
@@ -36,12 +47,12 @@ namespace gdn {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kThreads = 256;
 constexpr int kVs = 64;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kDk = 128;  // key width of the tiles (d_k = 64 zero-fills the upper half)
 
 constexpr uint32_t kColG = 0;
 constexpr uint32_t kColKS = 64;
@@ -50,10 +61,8 @@ constexpr uint32_t kColD = 192;
 constexpr uint32_t kColPD = 256;
 constexpr uint32_t kColS = 320;
 
-constexpr int kRegionBytes = 128 * 128;             // [K rows ; Q rows] x 128 B
 constexpr int kRegions = kDk / 64;
 constexpr int kStageBytes = kRegions * kRegionBytes;
-constexpr int kTile64 = 64 * 128;
 constexpr int kTileS = kDk * 128;
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -74,8 +83,10 @@ constexpr int oBar = oVec + 2 * kVecFloats * 4;
 constexpr int kBars = 16;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
-constexpr int kAlloc = kBytes + 1024;
-static_assert(kAlloc <= 232448, "shared memory");
+constexpr int oDOt = (kBytes + 1023) / 1024 * 1024;  // backward: dO tile [i][v] bf16
+template <bool kBwd>
+constexpr int alloc_bytes() { return (kBwd ? oDOt + kTile64 : kBytes) + 1024; }
+static_assert(alloc_bytes<true>() <= 232448, "shared memory");
 
 // barrier indices
 enum {
@@ -84,66 +95,37 @@ enum {
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15
 };
 
-__device__ __forceinline__ void named_bar(int id) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(128) : "memory");
-}
+__device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, 128); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
-    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
-    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
-    return a | (b << 16);
-}
-
-// Two fp32 -> packed bf16x2 (round to nearest even), element a in the low half.
-__device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
-    return r;
-}
-
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 64 values of one row into
-// the swizzled rows `row` of two 128-byte-wide operand tiles.
-__device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_lo, int row, const float* x) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = x[ch * 8 + 2 * e], b = x[ch * 8 + 2 * e + 1];
-            h[e] = cvt_bf16x2(a, b);
-            l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
-        }
-        const uint32_t off = sw128_offset(row, ch * 16);
-        *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-}
-
-__device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
-
-__device__ __forceinline__ void ld_row64(uint32_t tmem, int sub, uint32_t col, float* v) {
-    const uint32_t a = tmem + (static_cast<uint32_t>(sub * 32) << 16) + col;
-    tmem_ld16(a, v);
-    tmem_ld16(a + 16, v + 16);
-    tmem_ld16(a + 32, v + 32);
-    tmem_ld16(a + 48, v + 48);
-    tmem_ld_wait();
-}
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-// exp(x) for x <= 0 through the hardware base-2 exponential.
-__device__ __forceinline__ float exp_nonpos(float x) { return exp2f(x * kLog2e); }
+// Arguments of both directions.
+struct ChainArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;            // forward
+    const uint16_t* d_out;        // backward
+    const float* g;
+    const uint16_t* beta;
+    float scale;
+    const float* state_in;        // forward: initial state; backward: final-state gradient (may be null)
+    const int32_t* cu_seqlens;
+    uint16_t* out;                // forward output (may be null)
+    float* state_out;             // forward: final state; backward: initial-state gradient (may be null)
+    float* chunk_states;          // forward: chunk start states; backward: chunk end-state gradients (may be null)
+    uint8_t* chunk_T;             // forward: T operand tiles of every chunk (may be null)
+    int N, T, H, d_k, d_v;
+    int* err;
+};
 
 struct WsParams {
-    FwdArgs a;
+    ChainArgs a;
     uint32_t wait_limit;
 };
 
+template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
-                      const WsParams prm) {
-    const FwdArgs& p = prm.a;
+    gdn_chain_ws_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                        const WsParams prm) {
+    const ChainArgs& p = prm.a;
     const int vs = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int H = p.H, V = p.d_v, dk = p.d_k;
     const int tid = threadIdx.x;
@@ -161,8 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool use_tma = dk == kDk;
     const long long row_base = static_cast<long long>(b) * p.T;
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
-    const bool want_out = p.out != nullptr;
+    const bool want_out = !kBwd && p.out != nullptr;
     const uint32_t wl = prm.wait_limit;
+    // iteration it works on chunk chunk_of(it): forward in order, backward reversed
+    auto chunk_of = [&](int it) { return kBwd ? nchunks - 1 - it : it; };
+    const long long slot0 = chunk_slot_base(p.cu_seqlens, n, p.T);  // first per-chunk workspace slot
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -172,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBars; ++i) mbar_init(bar(i), 1);
         fence_mbar_init();
         *abort_flag = 0;
-        if (use_tma) {
+        if (use_tma && nchunks > 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_q);
         }
@@ -190,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    auto issue_tma = [&](int ci) {
-        const int st = ci % kStages;
+    auto issue_tma = [&](int it) {
+        const int st = it % kStages;
         uint8_t* base = sm + oStage + st * kStageBytes;
-        const int z = static_cast<int>(row_base + t0 + ci * kChunk);
+        const int z = static_cast<int>(row_base + t0 + chunk_of(it) * kChunk);
         mbar_arrive_expect_tx(bar(B_FULL0 + st), kStageBytes);
 #pragma unroll
         for (int r = 0; r < kRegions; ++r) {
@@ -209,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int srow = t < dk ? t : -1;
         const long long KV = static_cast<long long>(dk) * V;
         const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
-        const long long slot0 = chunk_slot_base(p.cu_seqlens, n, p.T);
         const float scale = p.scale;
         uint8_t* Shi = sm + oShi;
         uint8_t* Slo = sm + oSlo;
@@ -226,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float S[kVs];
 #pragma unroll
         for (int j = 0; j < kVs; ++j) S[j] = 0.f;
-        if (srow >= 0 && p.initial_state) {
-            const float* src = p.initial_state + state_off + static_cast<long long>(srow) * V;
+        if (srow >= 0 && p.state_in) {
+            const float* src = p.state_in + state_off + static_cast<long long>(srow) * V;
 #pragma unroll
             for (int j = 0; j < kVs; j += 4) {
                 const float4 t4 = *reinterpret_cast<const float4*>(src + j);
@@ -238,234 +222,449 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar(1);
 
-        // value row of this slice (row mrow of the chunk), packed bf16; the
-        // next chunk's row is fetched as soon as the current one is consumed
-        uint4 vraw[8];
-        auto load_v = [&](int cj) {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
-            const int cc0 = t0 + cj * kChunk;
-            if (cj < nchunks && mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.v + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
-            }
-        };
-        load_v(0);
         bool aborted = false;
-        for (int ci = 0; ci < nchunks; ++ci) {
-            const int c0 = t0 + ci * kChunk;
-            const int nv = min(kChunk, t1 - c0);
-            const int st = ci & 1, slot = ci & 1;
-            const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
-            const uint32_t stage_a = smem_u32(sm + oStage + st * kStageBytes);
-            const float* vec = reinterpret_cast<const float*>(sm + oVec) + slot * kVecFloats;
-            const float* bv = vec + 64;
-            const float* gam = vec + 192;
-            const float* dec = vec + 256;
-
-            if (p.chunk_states && srow >= 0) {
-                float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
+        if constexpr (!kBwd) {
+            // value row of this slice (row mrow of the chunk), packed bf16; the
+            // next chunk's row is fetched as soon as the current one is consumed
+            uint4 vraw[8];
+            auto load_v = [&](int cj) {
 #pragma unroll
-                for (int j = 0; j < kVs; j += 4)
-                    *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-            }
-            // K/Q tiles of this chunk
-            if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
-            named_bar(1);
-            if (*abort_flag) { aborted = true; break; }
-            tma_done = ci + 1;
-
-            // ---- C1: K S and Q S ----
-            if (t == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+                for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
+                const int cc0 = t0 + cj * kChunk;
+                if (cj < nchunks && mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        p.v + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
 #pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
-                    const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                    const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                    mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
-                    mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                    for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
                 }
-                mma_commit(bar(B_KS));
-                if (want_out) {
+            };
+            load_v(0);
+            for (int ci = 0; ci < nchunks; ++ci) {
+                const int c0 = t0 + ci * kChunk;
+                const int nv = min(kChunk, t1 - c0);
+                const int st = ci & 1, slot = ci & 1;
+                const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
+                const uint32_t stage_a = smem_u32(sm + oStage + st * kStageBytes);
+                const float* vec = reinterpret_cast<const float*>(sm + oVec) + slot * kVecFloats;
+                const float* bv = vec + 64;
+                const float* gam = vec + 192;
+                const float* dec = vec + 256;
+
+                if (p.chunk_states && srow >= 0) {
+                    float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
+#pragma unroll
+                    for (int j = 0; j < kVs; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                }
+                // K/Q tiles of this chunk
+                if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                tma_done = ci + 1;
+
+                // ---- C1: K S and Q S ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
 #pragma unroll
                     for (int s = 0; s < kDk / 16; ++s) {
                         const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                        const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                        const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
                         const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
                         const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                        mma_bf16(tmem + kColQS, a_q, b_hi, id_s, s > 0);
-                        mma_bf16(tmem + kColQS, a_q, b_lo, id_s, 1);
+                        mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
+                        mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
                     }
-                }
-            }
-            __syncwarp();
-            bool ok = mbar_wait(bar(B_READY0 + slot), ph2, wl);
-            ok = mbar_wait(bar(B_KS), ph, wl) && ok;
-            if (!ok) *abort_flag = 1;
-            tc_fence_after();
-            named_bar(1);
-            if (*abort_flag) { aborted = true; break; }
-
-            // ---- C2: R = beta o (V - gam o (K S)) ----
-            {
-                float row[64];
-                ld_row64(tmem, warp, kColKS, row);
-                if (mrow >= 0) {
-                    const float bj = bv[mrow], gj = gam[mrow];
+                    mma_commit(bar(B_KS));
+                    if (want_out) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int c = ch * 8 + 2 * m;
-                            row[c] = bj * (__uint_as_float(w4[m] << 16) - gj * row[c]);
-                            row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
+                        for (int s = 0; s < kDk / 16; ++s) {
+                            const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                            const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                            const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                            const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                            mma_bf16(tmem + kColQS, a_q, b_hi, id_s, s > 0);
+                            mma_bf16(tmem + kColQS, a_q, b_lo, id_s, 1);
                         }
                     }
-                    store_split_row(Rhi, Rlo, mrow, row);
                 }
-            }
-            load_v(ci + 1);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(1);
-
-            // ---- C3: Delta = T R ----
-            if (t == 0) {
+                __syncwarp();
+                bool ok = mbar_wait(bar(B_READY0 + slot), ph2, wl);
+                ok = mbar_wait(bar(B_KS), ph, wl) && ok;
+                if (!ok) *abort_flag = 1;
                 tc_fence_after();
-                // A = T read MN-major from the T^T tile (row j holds column j of T)
-                constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 64, 64);
-                const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
-                const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t th = desc_sw128(thi + s * 2048, kTile64, 1024);
-                    const uint64_t tl = desc_sw128(tlo + s * 2048, kTile64, 1024);
-                    const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                    const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + kColD, th, rh, id, s > 0);
-                    mma_bf16(tmem + kColD, th, rl, id, 1);
-                    mma_bf16(tmem + kColD, tl, rh, id, 1);
-                }
-                mma_commit(bar(B_D));
-            }
-            __syncwarp();
-            if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
-            tc_fence_after();
-            named_bar(1);
-            if (*abort_flag) { aborted = true; break; }
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
 
-            // ---- C4: Delta tiles and dec o Delta tiles ----
-            {
-                float row[64];
-                ld_row64(tmem, warp, kColD, row);
-                if (mrow >= 0) {
-                    store_split_row(Dhi, Dlo, mrow, row);
-                    const float dj = dec[mrow];
+                // ---- C2: R = beta o (V - gam o (K S)) ----
+                {
+                    float row[64];
+                    ld_row64(tmem, warp, kColKS, row);
+                    if (mrow >= 0) {
+                        const float bj = bv[mrow], gj = gam[mrow];
 #pragma unroll
-                    for (int c = 0; c < kVs; ++c) row[c] *= dj;
-                    store_split_row(Rhi, Rlo, mrow, row);
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const int c = ch * 8 + 2 * m;
+                                row[c] = bj * (__uint_as_float(w4[m] << 16) - gj * row[c]);
+                                row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
+                            }
+                        }
+                        store_split_row(Rhi, Rlo, mrow, row);
+                    }
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(1);
+                load_v(ci + 1);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
 
-            // ---- C5: S update and P Delta ----
-            if (t == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
-                constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
-                    const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                    const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + kColS, ak, rh, id_s, s > 0);
-                    mma_bf16(tmem + kColS, ak, rl, id_s, 1);
-                }
-                mma_commit(bar(B_S));
-                if (want_out) {
+                // ---- C3: Delta = T R ----
+                if (t == 0) {
+                    tc_fence_after();
+                    // A = T read MN-major from the T^T tile (row j holds column j of T)
+                    constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 64, 64);
+                    const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                    const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        const uint64_t ph_ = desc_sw128(smem_u32(sm + oPhi) + s * 32, 0, 1024);
-                        const uint64_t pl_ = desc_sw128(smem_u32(sm + oPlo) + s * 32, 0, 1024);
-                        const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                        const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
-                        mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
-                        mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                        const uint64_t th = desc_sw128(thi + s * 2048, kTile64, 1024);
+                        const uint64_t tl = desc_sw128(tlo + s * 2048, kTile64, 1024);
+                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColD, th, rh, id, s > 0);
+                        mma_bf16(tmem + kColD, th, rl, id, 1);
+                        mma_bf16(tmem + kColD, tl, rh, id, 1);
+                    }
+                    mma_commit(bar(B_D));
+                }
+                __syncwarp();
+                if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+
+                // ---- C4: Delta tiles and dec o Delta tiles ----
+                {
+                    float row[64];
+                    ld_row64(tmem, warp, kColD, row);
+                    if (mrow >= 0) {
+                        store_split_row(Dhi, Dlo, mrow, row);
+                        const float dj = dec[mrow];
+#pragma unroll
+                        for (int c = 0; c < kVs; ++c) row[c] *= dj;
+                        store_split_row(Rhi, Rlo, mrow, row);
                     }
                 }
-                mma_commit(bar(B_PD));
-            }
-            __syncwarp();
-            if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
-            tc_fence_after();
-            named_bar(1);
-            if (*abort_flag) { aborted = true; break; }
-            // every MMA that reads this chunk's K/Q stage has completed
-            if (t == 0) {
-                if (use_tma) {
-                    if (ci + kStages < nchunks) issue_tma(ci + kStages);
-                } else {
-                    mbar_arrive(bar(B_SFREE0 + st));
-                }
-            }
-            if (use_tma && ci + kStages < nchunks) tma_issued = ci + kStages + 1;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
 
-            // ---- C6: state update ----
-            {
-                float row[64];
-                const float gC = gam[63];
-                ld_row64(tmem, warp, kColS, row);
+                // ---- C5: S update and P Delta ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
+                    constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
 #pragma unroll
-                for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
-                store_split_row(Shi, Slo, t, S);
-            }
-            if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
-            tc_fence_after();
-            named_bar(1);
-            if (*abort_flag) { aborted = true; break; }
-            if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
-            // ---- output ----
-            if (want_out) {
-                const bool mine = mrow >= 0 && mrow < nv;
-                const float gi = mine ? gam[mrow] : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(
-                    p.out + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
-                const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
+                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColS, ak, rh, id_s, s > 0);
+                        mma_bf16(tmem + kColS, ak, rl, id_s, 1);
+                    }
+                    mma_commit(bar(B_S));
+                    if (want_out) {
 #pragma unroll
-                for (int q16 = 0; q16 < 4; ++q16) {
-                    float qs[16], pd[16];
-                    tmem_ld16(tmem + lane_base + kColQS + q16 * 16, qs);
-                    tmem_ld16(tmem + lane_base + kColPD + q16 * 16, pd);
-                    tmem_ld_wait();
-                    if (mine) {
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ph_ = desc_sw128(smem_u32(sm + oPhi) + s * 32, 0, 1024);
+                            const uint64_t pl_ = desc_sw128(smem_u32(sm + oPlo) + s * 32, 0, 1024);
+                            const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                            const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
+                            mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
+                            mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                        }
+                    }
+                    mma_commit(bar(B_PD));
+                }
+                __syncwarp();
+                if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                // every MMA that reads this chunk's K/Q stage has completed
+                if (t == 0) {
+                    if (use_tma) {
+                        if (ci + kStages < nchunks) issue_tma(ci + kStages);
+                    } else {
+                        mbar_arrive(bar(B_SFREE0 + st));
+                    }
+                }
+                if (use_tma && ci + kStages < nchunks) tma_issued = ci + kStages + 1;
+
+                // ---- C6: state update ----
+                {
+                    float row[64];
+                    const float gC = gam[63];
+                    ld_row64(tmem, warp, kColS, row);
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t w4[4];
+                    for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                    store_split_row(Shi, Slo, t, S);
+                }
+                if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
+                // ---- output ----
+                if (want_out) {
+                    const bool mine = mrow >= 0 && mrow < nv;
+                    const float gi = mine ? gam[mrow] : 0.f;
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.out + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
+                    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int c = half * 8 + 2 * e;
-                                w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]),
-                                                    scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                    for (int q16 = 0; q16 < 4; ++q16) {
+                        float qs[16], pd[16];
+                        tmem_ld16(tmem + lane_base + kColQS + q16 * 16, qs);
+                        tmem_ld16(tmem + lane_base + kColPD + q16 * 16, pd);
+                        tmem_ld_wait();
+                        if (mine) {
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = half * 8 + 2 * e;
+                                    w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]),
+                                                        scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                                }
+                                dst[q16 * 2 + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
-                            dst[q16 * 2 + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
                     }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
+                if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
+                if (*abort_flag) { aborted = true; break; }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(1);
-            if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
-            if (*abort_flag) { aborted = true; break; }
+        } else {
+            // dO row of this slice (row mrow of the chunk), packed bf16; the
+            // next chunk's row is fetched as soon as the current one is consumed
+            uint4 oraw[8];
+            auto load_do = [&](int it) {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) oraw[ch] = make_uint4(0, 0, 0, 0);
+                if (it >= nchunks) return;
+                const int cc0 = t0 + chunk_of(it) * kChunk;
+                if (mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        p.d_out + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) oraw[ch] = src[ch];
+                }
+            };
+            load_do(0);
+            uint8_t* dOt = sm + oDOt;
+            for (int it = 0; it < nchunks; ++it) {
+                const int ci = chunk_of(it);
+                const int st = it & 1, slot = it & 1;
+                const uint32_t ph = it & 1, ph2 = (it >> 1) & 1;
+                const uint32_t stage_a = smem_u32(sm + oStage + st * kStageBytes);
+                const float* vec = reinterpret_cast<const float*>(sm + oVec) + slot * kVecFloats;
+                const float* bv = vec + 64;
+                const float* gam = vec + 192;
+                const float* dec = vec + 256;
+
+                // gradient w.r.t. this chunk's end state, for the chunk-parallel pass
+                if (p.chunk_states && srow >= 0) {
+                    float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
+#pragma unroll
+                    for (int j = 0; j < kVs; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                }
+                // dO tile (single buffer: the previous chunk's P^T dO has completed)
+                if (mrow >= 0) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(dOt + sw128_offset(mrow, ch * 16)) = oraw[ch];
+                }
+                fence_proxy_async_smem();
+                // K/Q tiles of this chunk
+                if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                tma_done = it + 1;
+
+                // ---- C1: K dS (stage and dS tiles only) ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                        const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                        mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
+                        mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                    }
+                    mma_commit(bar(B_KS));
+                }
+                __syncwarp();
+                // gates, T and P of this chunk from the prep warpgroup
+                if (!mbar_wait(bar(B_READY0 + slot), ph2, wl)) *abort_flag = 1;
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+
+                // ---- P^T dO (A = P tile read MN-major) ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t p_hi = desc_sw128(smem_u32(sm + oPhi) + s * 2048, kTile64, 1024);
+                        const uint64_t p_lo = desc_sw128(smem_u32(sm + oPlo) + s * 2048, kTile64, 1024);
+                        const uint64_t b_o = desc_sw128(smem_u32(dOt) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
+                        mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
+                    }
+                    mma_commit(bar(B_PD));
+                }
+                // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
+                if (mrow >= 0) {
+                    float row[64];
+                    const float gi = scale * gam[mrow];  // dO rows beyond the chunk are zero
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) unpack8(oraw[ch], row + ch * 8);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) row[c] *= gi;
+                    store_split_row(Dhi, Dlo, mrow, row);
+                }
+                load_do(it + 1);
+                __syncwarp();
+                bool ok = mbar_wait(bar(B_KS), ph, wl);
+                ok = mbar_wait(bar(B_PD), ph, wl) && ok;
+                if (!ok) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
+
+                // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
+                {
+                    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+                    const float dj = (mrow >= 0) ? dec[mrow] : 0.f;
+#pragma unroll
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        float kds[16], pdo[16];
+                        tmem_ld16(tmem + lane_base + kColKS + g4 * 16, kds);
+                        tmem_ld16(tmem + lane_base + kColQS + g4 * 16, pdo);
+                        tmem_ld_wait();
+                        if (mrow >= 0) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
+                            store_split_chunk(Rhi, Rlo, mrow, 2 * g4, kds);
+                            store_split_chunk(Rhi, Rlo, mrow, 2 * g4 + 1, kds + 8);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
+
+                // ---- C3: dBhat = T^T dDelta (A = T tile read K-major) ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64);
+                    const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                    const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t th = desc_sw128(thi + s * 32, 0, 1024);
+                        const uint64_t tl = desc_sw128(tlo + s * 32, 0, 1024);
+                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColD, th, rh, id, s > 0);
+                        mma_bf16(tmem + kColD, th, rl, id, 1);
+                        mma_bf16(tmem + kColD, tl, rh, id, 1);
+                    }
+                    mma_commit(bar(B_D));
+                }
+                __syncwarp();
+                if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+
+                // ---- C4: X = -beta gam o dBhat -> R tiles (dDelta consumed) ----
+                {
+                    float row[64];
+                    ld_row64(tmem, warp, kColD, row);
+                    if (mrow >= 0) {
+                        const float f = -bv[mrow] * gam[mrow];
+#pragma unroll
+                        for (int c = 0; c < kVs; ++c) row[c] *= f;
+                        store_split_row(Rhi, Rlo, mrow, row);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
+
+                // ---- C5: K^T X + Q^T G (A = K^T, Q^T read MN-major from the stage) ----
+                if (t == 0) {
+                    tc_fence_after();
+                    constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
+                        const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
+                        const uint64_t xh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                        const uint64_t xl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                        const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                        const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + kColS, ak, xh, id, s > 0);
+                        mma_bf16(tmem + kColS, ak, xl, id, 1);
+                        mma_bf16(tmem + kColS, aq, gh, id, 1);
+                        mma_bf16(tmem + kColS, aq, gl, id, 1);
+                    }
+                    mma_commit(bar(B_S));
+                }
+                __syncwarp();
+                if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                named_bar(1);
+                if (*abort_flag) { aborted = true; break; }
+                // every MMA that reads this chunk's K/Q stage has completed
+                if (t == 0) {
+                    if (use_tma) {
+                        if (it + kStages < nchunks) issue_tma(it + kStages);
+                    } else {
+                        mbar_arrive(bar(B_SFREE0 + st));
+                    }
+                }
+                if (use_tma && it + kStages < nchunks) tma_issued = it + kStages + 1;
+
+                // ---- C6: dS <- gam_n dS + (K^T X + Q^T G) ----
+                {
+                    float row[64];
+                    const float gC = gam[63];
+                    ld_row64(tmem, warp, kColS, row);
+#pragma unroll
+                    for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                    store_split_row(Shi, Slo, t, S);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar(1);
+                if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
+                if (*abort_flag) { aborted = true; break; }
+            }
         }
         if (aborted) {
             if (t == 0) {
@@ -475,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ci = tma_done; ci < tma_issued; ++ci)
                     mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
             }
-        } else if (p.final_state && srow >= 0) {
-            float* dst = p.final_state + state_off + static_cast<long long>(srow) * V;
+        } else if (p.state_out && srow >= 0) {
+            float* dst = p.state_out + state_off + static_cast<long long>(srow) * V;
 #pragma unroll
             for (int j = 0; j < kVs; j += 4)
                 *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -489,11 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // named barrier of warps 4-5 only (the A / inverse half)
         auto half_bar = [] { asm volatile("bar.sync 3, 64;" ::: "memory"); };
         bool aborted = false;
-        for (int ci = 0; ci < nchunks; ++ci) {
+        for (int it = 0; it < nchunks; ++it) {
+            const int ci = chunk_of(it);
             const int c0 = t0 + ci * kChunk;
             const int nv = min(kChunk, t1 - c0);
-            const int st = ci & 1, slot = ci & 1;
-            const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
+            const int st = it & 1, slot = it & 1;
+            const uint32_t ph = it & 1, ph2 = (it >> 1) & 1;
             uint8_t* stage = sm + oStage + st * kStageBytes;
             float* vec = reinterpret_cast<float*>(sm + oVec) + slot * kVecFloats;
             float* gv = vec;
@@ -502,9 +702,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* gam = vec + 192;
             float* dec = vec + 256;
 
-            // gates of this chunk into its slot (free once the chain finished chunk ci - 2)
+            // gates of this chunk into its slot (free once the chain finished iteration it - 2)
             bool ok = true;
-            if (ci >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((ci - 2) >> 1) & 1, wl);
+            if (it >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((it - 2) >> 1) & 1, wl);
             if (!ok) *abort_flag = 1;
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
@@ -535,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K/Q tiles
             if (!use_tma) {
                 ok = true;
-                if (ci >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((ci - 2) >> 1) & 1, wl);
+                if (it >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((it - 2) >> 1) & 1, wl);
                 if (!ok) *abort_flag = 1;
                 named_bar(2);
                 if (*abort_flag) { aborted = true; break; }
@@ -610,8 +810,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
                     }
                 }
-                // column q of T = row q of the T^T tile (read MN-major by the MMA)
-                store_split_row(sm + oT + (slot * 2 + 0) * kTile64, sm + oT + (slot * 2 + 1) * kTile64, q, x);
+                // column q of T = row q of the T^T tile (read MN-major for T, K-major for T^T)
+                uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
+                uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
+                store_split_row(t_hi, t_lo, q, x);
+                if (!kBwd && p.chunk_T && vs == 0) {
+                    // the same operand rows, for the chunk-parallel gradient pass
+                    uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t off = sw128_offset(q, ch * 16);
+                        dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
+                        dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
+                    }
+                }
                 ok = true;
             } else {
                 float prow[64];
@@ -624,9 +836,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 64; ++j) prow[j] = (j <= i) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
                 }
                 tc_fence_before();
-                // P tiles are single-buffered: wait until the chain's P Delta of chunk ci - 1 is done
+                // P tiles are single-buffered: wait until the chain's product with the
+                // P tiles of iteration it - 1 (P Delta forward, P^T dO backward) is done
                 ok = true;
-                if (ci >= 1) ok = mbar_wait(bar(B_PFREE), (ci - 1) & 1, wl);
+                if (it >= 1) ok = mbar_wait(bar(B_PFREE), (it - 1) & 1, wl);
                 if (!ok) *abort_flag = 1;
                 if (ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
             }
@@ -646,35 +859,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 3-D view {d (inner), head, token row} of a (rows, H, 128) bf16 tensor; box
-// {64, 1, 64} = 64 token rows x 128 bytes, 128-byte swizzled.
-bool make_qk_map(CUtensorMap* m, const uint16_t* base, long long rows, int H) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDk), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDk) * 2, static_cast<cuuint64_t>(H) * kDk * 2};
-    cuuint32_t box[3] = {64, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+template <bool kBwd>
+cudaError_t launch_chain(const ChainArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
+    CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    if (rows > 0 && a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
+        return cudaErrorInvalidValue;
+    constexpr int smem = alloc_bytes<kBwd>();
+    cudaError_t e = cudaFuncSetAttribute(gdn_chain_ws_kernel<kBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    WsParams prm{a, wait_limit};
+    dim3 grid(a.d_v / kVs, a.H, a.N);
+    gdn_chain_ws_kernel<kBwd><<<grid, kThreads, smem, stream>>>(mk, mq, prm);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -682,17 +881,21 @@ bool make_qk_map(CUtensorMap* m, const uint16_t* base, long long rows, int H) {
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
     if (rows == 0) return launch_fwd_simt(a, stream);  // nothing to load: state pass-through only
-    CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
-    memset(&mk, 0, sizeof(mk));
-    memset(&mq, 0, sizeof(mq));
-    if (a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
-        return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gdn_fwd_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
-    if (e != cudaSuccess) return e;
-    WsParams prm{a, wait_limit};
-    dim3 grid(a.d_v / kVs, a.H, a.N);
-    gdn_fwd_ws_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, prm);
-    return cudaGetLastError();
+    ChainArgs c{};
+    c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
+    c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = a.out; c.state_out = a.final_state;
+    c.chunk_states = a.chunk_states; c.chunk_T = a.chunk_T;
+    c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err;
+    return launch_chain<false>(c, wait_limit, stream);
+}
+
+cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    ChainArgs c{};
+    c.q = a.q; c.k = a.k; c.v = nullptr; c.d_out = a.d_out; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
+    c.state_in = a.d_final_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.state_out = a.d_initial_state;
+    c.chunk_states = a.chunk_dstates; c.chunk_T = nullptr;
+    c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err;
+    return launch_chain<true>(c, wait_limit, stream);
 }
 
 }  // namespace gdn

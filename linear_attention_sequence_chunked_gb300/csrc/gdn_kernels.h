@@ -19,6 +19,7 @@ struct FwdArgs {
     uint16_t* out;          // may be null: skip the output
     float* final_state;     // may be null
     float* chunk_states;    // may be null: per-chunk start states [slot][H][d_k][d_v]
+    uint8_t* chunk_T;       // may be null: per-chunk T operand tiles [slot][H][2 x 8 KB]
     int N;                  // sequences (B dense, or cu_seqlens length - 1)
     int T;                  // tokens per batch row (dense) / total tokens (packed)
     int H;
@@ -27,22 +28,18 @@ struct FwdArgs {
     int* err;               // device error word
 };
 
-struct BwdArgs {
+// Backward pass 2 (reverse state-gradient chain; the chunk chain kernel in
+// backward mode).
+struct BwdChainArgs {
     const uint16_t* q;
     const uint16_t* k;
-    const uint16_t* v;
     const float* g;
     const uint16_t* beta;
+    const uint16_t* d_out;
     float scale;
     const int32_t* cu_seqlens;
-    const uint16_t* d_out;
     const float* d_final_state;   // may be null
-    const float* chunk_states;    // [slot][H][d_k][d_v]
-    float* dq_part;               // [slices][rows][d_k]
-    float* dk_part;               // [slices][rows][d_k]
-    float* dg_part;               // [slices][rows]
-    float* dbeta_part;            // [slices][rows]
-    uint16_t* dv;
+    float* chunk_dstates;         // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
     float* d_initial_state;       // may be null
     int N;
     int T;
@@ -52,19 +49,45 @@ struct BwdArgs {
     int* err;
 };
 
-// Value columns handled by one backward block.
-constexpr int kBwdVs = 32;
+// Backward pass 3 (chunk-parallel local gradients).
+struct BwdLocalArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const float* g;
+    const uint16_t* beta;
+    const uint16_t* d_out;
+    float scale;
+    const int32_t* cu_seqlens;
+    const float* chunk_states;    // [slot][H][d_k][d_v]: start state of each chunk
+    const float* chunk_dstates;   // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
+    const uint8_t* chunk_T;       // [slot][H][2 x 8 KB]
+    uint16_t* dq;
+    uint16_t* dk;
+    uint16_t* dv;
+    float* dg;
+    uint16_t* dbeta;
+    int N;
+    int T;
+    int H;
+    int d_k;
+    int d_v;
+    int max_chunks;               // chunks of the longest sequence (grid.x)
+    int* err;
+};
+
+// Bytes of one chunk's T operand tiles in the backward workspace.
+constexpr int kChunkTBytes = 2 * 64 * 128;
+
+// Backward pass 2: the chunk chain kernel of the forward in backward mode.
+cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStream_t stream);
+// Backward pass 3: one CTA per (chunk, head, sequence).
+cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream);
 
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
-// Tensor-core forward; wait_limit bounds every mbarrier wait (polls).
-cudaError_t launch_fwd_tc(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
-// Warp-specialised tensor-core forward (prep and chain warpgroups).
+// Warp-specialised tensor-core forward (prep and chain warpgroups);
+// wait_limit bounds every mbarrier wait (polls).
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 constexpr uint32_t kDefaultWaitLimit = 4000000u;
-cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd_reduce(const float* dq_part, const float* dk_part, const float* dg_part,
-                              const float* dbeta_part, int slices, long long rows, int d_k,
-                              uint16_t* dq, uint16_t* dk, float* dg, uint16_t* dbeta,
-                              cudaStream_t stream);
 
 }  // namespace gdn

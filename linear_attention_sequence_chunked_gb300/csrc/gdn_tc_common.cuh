@@ -1,0 +1,133 @@
+// Helpers shared by the tensor-core kernels: operand-tile writes (bf16 hi/lo
+// split into 128-byte-swizzled rows), TMEM row loads, decay exponentials,
+// named barriers and the TMA tensor maps of q/k.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm100_ptx.cuh"
+
+namespace gdn {
+namespace tc {
+
+using namespace sm100;
+
+constexpr int kTile64 = 64 * 128;        // 64 rows x 128 bytes (64 bf16)
+constexpr int kRegionBytes = 128 * 128;  // [K rows 0-63 ; Q rows 64-127] x 128 bytes
+constexpr int kDk = 128;                 // key width of the tiles
+
+// bar.sync on a named barrier for `count` threads
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
+    return a | (b << 16);
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even), element a in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 64 values of one row into
+// the swizzled rows `row` of two 128-byte-wide operand tiles.
+__device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_lo, int row, const float* x) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = x[ch * 8 + 2 * e], b = x[ch * 8 + 2 * e + 1];
+            h[e] = cvt_bf16x2(a, b);
+            l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
+        }
+        const uint32_t off = sw128_offset(row, ch * 16);
+        *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// One 16-byte chunk (8 values, columns 8*ch .. 8*ch+7) of a split row.
+__device__ __forceinline__ void store_split_chunk(uint8_t* tile_hi, uint8_t* tile_lo, int row, int ch,
+                                                  const float* x8) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = x8[2 * e], b = x8[2 * e + 1];
+        h[e] = cvt_bf16x2(a, b);
+        l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
+    }
+    const uint32_t off = sw128_offset(row, ch * 16);
+    *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Rows of M = 64 accumulators (cta_group::1): rows 16w..16w+15 sit in lanes
+// 32w..32w+15 of TMEM subpartition w; lanes 16..31 are unused.
+__device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
+
+// 64 fp32 columns of this thread's TMEM lane (subpartition `sub`).
+__device__ __forceinline__ void ld_row64(uint32_t tmem, int sub, uint32_t col, float* v) {
+    const uint32_t a = tmem + (static_cast<uint32_t>(sub * 32) << 16) + col;
+    tmem_ld16(a, v);
+    tmem_ld16(a + 16, v + 16);
+    tmem_ld16(a + 32, v + 32);
+    tmem_ld16(a + 48, v + 48);
+    tmem_ld_wait();
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// exp(x) for x <= 0 through the hardware base-2 exponential.
+__device__ __forceinline__ float exp_nonpos(float x) { return exp2f(x * kLog2e); }
+
+// Unpack 8 bf16 (one uint4) into fp32.
+__device__ __forceinline__ void unpack8(const uint4& raw, float* out) {
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        out[2 * m] = __uint_as_float(w4[m] << 16);
+        out[2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 3-D view {d (inner), head, token row} of a (rows, H, 128) bf16 tensor; box
+// {64, 1, 64} = 64 token rows x 128 bytes, 128-byte swizzled.
+inline bool make_qk_map(CUtensorMap* m, const uint16_t* base, long long rows, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDk), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDk) * 2, static_cast<cuuint64_t>(H) * kDk * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+}  // namespace gdn
