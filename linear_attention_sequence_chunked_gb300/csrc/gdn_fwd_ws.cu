@@ -77,7 +77,9 @@ constexpr int oPhi = oDlo + kTile64;
 constexpr int oPlo = oPhi + kTile64;
 constexpr int oT = oPlo + kTile64;                  // [slot][hi,lo] tiles
 constexpr int oA = oT + 4 * kTile64;                // A^T fp32 [64][64] (prep)
-constexpr int oVec = oA + 64 * 64 * 4;              // [slot][g, beta, G, gam, dec] x 64 fp32
+constexpr int oTf = oA + 64 * 64 * 4;               // fp32 32x32 blocks T_00, T_11, T_10, X (prep)
+constexpr int kTB = 32 * 32;                        // floats per 32x32 block
+constexpr int oVec = oTf + 4 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
 constexpr int kBars = 16;
@@ -685,8 +687,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = tid - 128;          // 0..127
         const int sub = warp - 4;         // TMEM subpartition
         float* At = reinterpret_cast<float*>(sm + oA);  // A^T, row stride 64
+        float* T00 = reinterpret_cast<float*>(sm + oTf);  // row-major 32x32 blocks of T
+        float* T11 = T00 + kTB;
+        float* T10 = T00 + 2 * kTB;
+        float* Xb = T00 + 3 * kTB;                         // A_10 T_00
         // named barrier of warps 4-5 only (the A / inverse half)
         auto half_bar = [] { asm volatile("bar.sync 3, 64;" ::: "memory"); };
+        // gates (g, beta) of row q of a chunk, fetched one chunk ahead
+        float g_pre = 0.f, b_pre = 0.f;
+        auto load_gates = [&](int it) {
+            g_pre = 0.f;
+            b_pre = 0.f;
+            if (q < 64 && it < nchunks) {
+                const int cc0 = t0 + chunk_of(it) * kChunk;
+                if (q < min(kChunk, t1 - cc0)) {
+                    const long long idx = (row_base + cc0 + q) * H + h;
+                    g_pre = p.g[idx];
+                    b_pre = bf16_to_f32(p.beta[idx]);
+                }
+            }
+        };
+        load_gates(0);
         bool aborted = false;
         for (int it = 0; it < nchunks; ++it) {
             const int ci = chunk_of(it);
@@ -709,10 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
             if (q < 64) {
-                const long long idx = (row_base + c0 + q) * H + h;
-                gv[q] = (q < nv) ? p.g[idx] : 0.f;
-                bv[q] = (q < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
+                gv[q] = g_pre;
+                bv[q] = b_pre;
             }
+            load_gates(it + 1);
             named_bar(2);
             if (q < 32) {
                 const float a = gv[2 * q];
@@ -777,8 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) { aborted = true; break; }
 
             // The two halves of the warpgroup now work side by side:
-            //   warps 4-5 (q < 64):  A row q -> A^T in shared memory -> T = (I + A)^-1
+            //   warps 4-5 (q < 64):  A row q -> A^T in shared memory -> the 32x32
+            //                        diagonal block of T that holds column q
             //   warps 6-7 (q >= 64): causal score row q - 64 -> P tiles
+            // then all four warps form the off-diagonal block of T
+            // (T = (I + A)^-1 = [[T_00, 0], [T_10, T_11]], T_bb = (I + A_bb)^-1,
+            // T_10 = -T_11 A_10 T_00) and write T as bf16 hi/lo operand tiles.
             if (q < 64) {
                 {
                     float row[64];
@@ -790,19 +815,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 half_bar();
-                // Column c = q of T by right-looking forward substitution:
-                // x = e_c; for m: for i > m: x_i -= A_im x_m.  Row m of A^T is
-                // read as broadcast 16-byte loads; the dependent chain is one
-                // FMA per step.
-                float x[64];
+                // column c of T_bb (b = q / 32) by right-looking forward
+                // substitution: x = e_c; for m: for i > m: x_i -= A_im x_m.  Row
+                // m of A^T is read as broadcast 16-byte loads.
+                const int b = q >> 5, c = q & 31;
+                float x[32];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) x[i] = (i == q) ? 1.f : 0.f;
+                for (int i = 0; i < 32; ++i) x[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 63; ++m) {
+                for (int m = 0; m < 31; ++m) {
                     const float xm = x[m];
-                    const float4* arow = reinterpret_cast<const float4*>(At + m * 64);
+                    const float4* arow = reinterpret_cast<const float4*>(At + (32 * b + m) * 64 + 32 * b);
 #pragma unroll
-                    for (int i4 = (m + 1) >> 2; i4 < 16; ++i4) {
+                    for (int i4 = (m + 1) >> 2; i4 < 8; ++i4) {
                         const float4 a4 = arow[i4];
                         if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
                         if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
@@ -810,20 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
                     }
                 }
-                // column q of T = row q of the T^T tile (read MN-major for T, K-major for T^T)
-                uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
-                uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
-                store_split_row(t_hi, t_lo, q, x);
-                if (!kBwd && p.chunk_T && vs == 0) {
-                    // the same operand rows, for the chunk-parallel gradient pass
-                    uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
+                float* Tbb = b ? T11 : T00;
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint32_t off = sw128_offset(q, ch * 16);
-                        dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
-                        dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
-                    }
-                }
+                for (int i = 0; i < 32; ++i) Tbb[i * 32 + c] = x[i];
                 ok = true;
             } else {
                 float prow[64];
@@ -842,6 +856,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it >= 1) ok = mbar_wait(bar(B_PFREE), (it - 1) & 1, wl);
                 if (!ok) *abort_flag = 1;
                 if (ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
+            }
+            named_bar(2);
+            {
+                // X = A_10 T_00, thread q: row r = q / 4, columns c8 .. c8 + 7
+                const int r = q >> 2, c8 = (q & 3) * 8;
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float a = At[k * 64 + 32 + r];
+                    const float4 t0 = *reinterpret_cast<const float4*>(T00 + k * 32 + c8);
+                    const float4 t1 = *reinterpret_cast<const float4*>(T00 + k * 32 + c8 + 4);
+                    acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
+                    acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+                    acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
+                    acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
+                }
+                *reinterpret_cast<float4*>(Xb + r * 32 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(Xb + r * 32 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                named_bar(2);
+                // T_10 = -T_11 X (T_11 unit lower triangular)
+                float4 u0 = *reinterpret_cast<const float4*>(Xb + r * 32 + c8);
+                float4 u1 = *reinterpret_cast<const float4*>(Xb + r * 32 + c8 + 4);
+                acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+                acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+                for (int k = 0; k < r; ++k) {
+                    const float a = T11[r * 32 + k];
+                    const float4 v0 = *reinterpret_cast<const float4*>(Xb + k * 32 + c8);
+                    const float4 v1 = *reinterpret_cast<const float4*>(Xb + k * 32 + c8 + 4);
+                    acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
+                    acc[2] = fmaf(a, v0.z, acc[2]); acc[3] = fmaf(a, v0.w, acc[3]);
+                    acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
+                    acc[6] = fmaf(a, v1.z, acc[6]); acc[7] = fmaf(a, v1.w, acc[7]);
+                }
+                *reinterpret_cast<float4*>(T10 + r * 32 + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+                *reinterpret_cast<float4*>(T10 + r * 32 + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+            }
+            named_bar(2);
+            {
+                // column col of T = row col of the T^T tile (read MN-major for T,
+                // K-major for T^T); this thread writes its entries 32 hf .. 32 hf + 31
+                const int col = q & 63, hf = q >> 6;
+                const float* src = col < 32 ? (hf ? T10 : T00) : (hf ? T11 : nullptr);
+                const int cc = col & 31;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = src ? src[i * 32 + cc] : 0.f;
+                uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
+                uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(t_hi, t_lo, col, 4 * hf + c4, v + 8 * c4);
+                if (!kBwd && p.chunk_T && vs == 0) {
+                    // the same operand bytes, for the chunk-parallel gradient pass
+                    uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t off = sw128_offset(col, (4 * hf + c4) * 16);
+                        dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
+                        dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
+                    }
+                }
             }
             fence_proxy_async_smem();
             named_bar(2);
