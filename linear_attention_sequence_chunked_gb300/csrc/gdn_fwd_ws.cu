@@ -31,9 +31,9 @@
 // accumulation is fp32 in tensor memory.
 //
 // Hand-offs are mbarriers (bounded waits): stage full (TMA), gram done,
-// prep ready (T, P, gates of a chunk), T/gate slot free, P free, and the
-// chain's own MMA completions.  Warpgroup-internal ordering uses named
-// barriers 1 (chain) and 2 (prep).
+// prep ready (T, P, gates of a chunk), slot free (T, P, gates double-buffered
+// by chunk parity), and the chain's own MMA completions.  Warpgroup-internal
+// ordering uses named barriers 1 (chain) and 2 (prep).
 #include <cuda.h>
 #include <string.h>
 
@@ -60,6 +60,7 @@ constexpr uint32_t kColQS = 128;
 constexpr uint32_t kColD = 192;
 constexpr uint32_t kColPD = 256;
 constexpr uint32_t kColS = 320;
+constexpr uint32_t kColQK = 384;  // prep: Q K^T (K K^T at kColG)
 
 constexpr int kRegions = kDk / 64;
 constexpr int kStageBytes = kRegions * kRegionBytes;
@@ -73,27 +74,26 @@ constexpr int oRhi = oSlo + kTileS;
 constexpr int oRlo = oRhi + kTile64;
 constexpr int oDhi = oRlo + kTile64;
 constexpr int oDlo = oDhi + kTile64;
-constexpr int oPhi = oDlo + kTile64;
-constexpr int oPlo = oPhi + kTile64;
-constexpr int oT = oPlo + kTile64;                  // [slot][hi,lo] tiles
+constexpr int oP = oDlo + kTile64;                  // [slot][hi,lo] P tiles
+constexpr int oT = oP + 4 * kTile64;                // [slot][hi,lo] T tiles
 constexpr int oA = oT + 4 * kTile64;                // A^T fp32 [64][64] (prep)
-constexpr int oTf = oA + 64 * 64 * 4;               // fp32 32x32 blocks T_00, T_11, T_10, X (prep)
+constexpr int oTf = oA + 64 * 64 * 4;               // fp32 32x32 blocks T_00, T_11, T_10 (prep)
 constexpr int kTB = 32 * 32;                        // floats per 32x32 block
-constexpr int oVec = oTf + 4 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
+constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
 constexpr int kBars = 16;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
-constexpr int oDOt = (kBytes + 1023) / 1024 * 1024;  // backward: dO tile [i][v] bf16
-template <bool kBwd>
-constexpr int alloc_bytes() { return (kBwd ? oDOt + kTile64 : kBytes) + 1024; }
-static_assert(alloc_bytes<true>() <= 232448, "shared memory");
+// backward: the dO tile [i][v] bf16 shares the R tiles' space (dead between
+// the previous chunk's K^T X and this chunk's dDelta)
+constexpr int kAlloc = kBytes + 1024;
+static_assert(kAlloc <= 232448, "shared memory");
 
 // barrier indices
 enum {
     B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
-    B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_PFREE = 11,
+    B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10,
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15
 };
 
@@ -163,6 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_q);
         }
+    }
+    // the upper-right 16x16 blocks of the 32x32 inverse blocks T_00, T_11 stay zero
+    for (int i = tid; i < 2 * 16 * 16; i += kThreads) {
+        float* tb = reinterpret_cast<float*>(sm + oTf) + (i >> 8) * kTB;
+        tb[((i >> 4) & 15) * 32 + 16 + (i & 15)] = 0.f;
     }
     // d_k = 64: the upper key region of every stage stays zero
     if (!use_tma) {
@@ -380,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (want_out) {
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
-                            const uint64_t ph_ = desc_sw128(smem_u32(sm + oPhi) + s * 32, 0, 1024);
-                            const uint64_t pl_ = desc_sw128(smem_u32(sm + oPlo) + s * 32, 0, 1024);
+                            const uint64_t ph_ = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 32, 0, 1024);
+                            const uint64_t pl_ = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 32, 0, 1024);
                             const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
                             const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
                             mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
@@ -419,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
-                if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
                 // ---- output ----
                 if (want_out) {
                     const bool mine = mrow >= 0 && mrow < nv;
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             load_do(0);
-            uint8_t* dOt = sm + oDOt;
+            uint8_t* dOt = sm + oRhi;
             for (int it = 0; it < nchunks; ++it) {
                 const int ci = chunk_of(it);
                 const int st = it & 1, slot = it & 1;
@@ -529,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        const uint64_t p_hi = desc_sw128(smem_u32(sm + oPhi) + s * 2048, kTile64, 1024);
-                        const uint64_t p_lo = desc_sw128(smem_u32(sm + oPlo) + s * 2048, kTile64, 1024);
+                        const uint64_t p_hi = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 2048, kTile64, 1024);
+                        const uint64_t p_lo = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 2048, kTile64, 1024);
                         const uint64_t b_o = desc_sw128(smem_u32(dOt) + s * 2048, kTile64, 1024);
                         mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
                         mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
@@ -555,7 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
-                if (t == 0) mbar_arrive(bar(B_PFREE));  // P tiles consumed
 
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
@@ -690,9 +693,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* T00 = reinterpret_cast<float*>(sm + oTf);  // row-major 32x32 blocks of T
         float* T11 = T00 + kTB;
         float* T10 = T00 + 2 * kTB;
-        float* Xb = T00 + 3 * kTB;                         // A_10 T_00
-        // named barrier of warps 4-5 only (the A / inverse half)
-        auto half_bar = [] { asm volatile("bar.sync 3, 64;" ::: "memory"); };
         // gates (g, beta) of row q of a chunk, fetched one chunk ahead
         float g_pre = 0.f, b_pre = 0.f;
         auto load_gates = [&](int it) {
@@ -778,16 +778,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
 
-            // gram [K;Q] K^T
+            // gram K K^T and Q K^T (two M = 64 products)
             if (q == 0) {
                 tc_fence_after();
-                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 128, 64);
+                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
                 const uint32_t stage_a = smem_u32(stage);
 #pragma unroll
                 for (int s = 0; s < kDk / 16; ++s) {
                     const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                    const uint64_t a_kq = desc_sw128(stage_a + koff, 0, 1024);
-                    mma_bf16(tmem + kColG, a_kq, a_kq, id_g, s > 0);
+                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                    const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                    mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
+                    mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
                 }
                 mma_commit(bar(B_GRAM));
             }
@@ -797,37 +799,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
 
-            // The two halves of the warpgroup now work side by side:
-            //   warps 4-5 (q < 64):  A row q -> A^T in shared memory -> the 32x32
-            //                        diagonal block of T that holds column q
-            //   warps 6-7 (q >= 64): causal score row q - 64 -> P tiles
-            // then all four warps form the off-diagonal block of T
-            // (T = (I + A)^-1 = [[T_00, 0], [T_10, T_11]], T_bb = (I + A_bb)^-1,
-            // T_10 = -T_11 A_10 T_00) and write T as bf16 hi/lo operand tiles.
-            if (q < 64) {
+            // All four warps form the chunk's decayed products: thread (warp w,
+            // lane l) takes row i = 16 (w - 4) + l % 16 and columns 32 (l / 16) ..
+            // + 31.  The decay e^{G_i - G_j} is formed once and used for A
+            // (j < i) and P (j <= i).  Then warps 4-5 invert the four 16x16
+            // diagonal blocks of I + A, and all four warps join the blocks level
+            // by level: with T = (I + A)^-1 split into 2x2 blocks,
+            // T_bb = (I + A_bb)^-1 and T_10 = -T_11 A_10 T_00, first inside each
+            // 32x32 diagonal block (16x16 blocks), then for the 64x64 matrix
+            // (32x32 blocks).  The products' scratch X lives in the unused upper
+            // triangle of A^T.
+            {
+                const int i = 16 * sub + (lane & 15), hf = lane >> 4, j0 = 32 * hf;
+                const float Gi = Gv[i], bi = bv[i];
+                float mdec[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) mdec[k] = (j0 + k <= i) ? exp_nonpos(Gi - Gv[j0 + k]) : 0.f;
+                // the M = 64 products sit in lanes 0-15 of each subpartition: lane
+                // l < 16 loads row i, lane l + 16 takes its upper 32 columns
+                const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
                 {
-                    float row[64];
-                    ld_row64(tmem, sub, kColG, row);
-                    const float Gi = Gv[q], bi = bv[q];
+                    float lo[32], up[32];
+                    tmem_ld16(lb + kColG, lo);
+                    tmem_ld16(lb + kColG + 16, lo + 16);
+                    tmem_ld16(lb + kColG + 32, up);
+                    tmem_ld16(lb + kColG + 48, up + 16);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        At[j * 64 + q] = (j < q) ? bi * row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+                    for (int k = 0; k < 32; ++k) {
+                        const float kk = __shfl_sync(0xffffffffu, up[k], lane & 15);
+                        lo[k] = (j0 + k < i) ? bi * (hf ? kk : lo[k]) * mdec[k] : 0.f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) At[(j0 + k) * 64 + i] = lo[k];
                 }
-                tc_fence_before();
-                half_bar();
-                // column c of T_bb (b = q / 32) by right-looking forward
-                // substitution: x = e_c; for m: for i > m: x_i -= A_im x_m.  Row
-                // m of A^T is read as broadcast 16-byte loads.
-                const int b = q >> 5, c = q & 31;
-                float x[32];
+                {
+                    float lo[32], up[32];
+                    tmem_ld16(lb + kColQK, lo);
+                    tmem_ld16(lb + kColQK + 16, lo + 16);
+                    tmem_ld16(lb + kColQK + 32, up);
+                    tmem_ld16(lb + kColQK + 48, up + 16);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = (i == c) ? 1.f : 0.f;
+                    for (int k = 0; k < 32; ++k) {
+                        const float qk = __shfl_sync(0xffffffffu, up[k], lane & 15);
+                        lo[k] = (hf ? qk : lo[k]) * mdec[k];
+                    }
+                    // P tiles of this slot are free: the chain finished iteration it - 2
+                    uint8_t* p_hi = sm + oP + (2 * slot) * kTile64;
+                    uint8_t* p_lo = sm + oP + (2 * slot + 1) * kTile64;
 #pragma unroll
-                for (int m = 0; m < 31; ++m) {
+                    for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(p_hi, p_lo, i, 4 * hf + c4, lo + 8 * c4);
+                }
+            }
+            tc_fence_before();
+            named_bar(2);
+            if (q < 64) {
+                // column c of the 16x16 diagonal block d = q / 16 by right-looking
+                // forward substitution: x = e_c; for m: for i > m: x_i -= A_im x_m.
+                // Row m of A^T is read as broadcast 16-byte loads.
+                const int d = q >> 4, c = q & 15;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+                const float* ablk = At + 16 * d * 64 + 16 * d;
+#pragma unroll
+                for (int m = 0; m < 15; ++m) {
                     const float xm = x[m];
-                    const float4* arow = reinterpret_cast<const float4*>(At + (32 * b + m) * 64 + 32 * b);
+                    const float4* arow = reinterpret_cast<const float4*>(ablk + m * 64);
 #pragma unroll
-                    for (int i4 = (m + 1) >> 2; i4 < 8; ++i4) {
+                    for (int i4 = (m + 1) >> 2; i4 < 4; ++i4) {
                         const float4 a4 = arow[i4];
                         if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
                         if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
@@ -835,31 +876,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
                     }
                 }
-                float* Tbb = b ? T11 : T00;
+                // into the 32x32 block T_bb (b = d / 2) at rows/columns 16 (d % 2) ..
+                float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * 33 + c;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) Tbb[i * 32 + c] = x[i];
-                ok = true;
-            } else {
-                float prow[64];
-                {
-                    float row[64];
-                    ld_row64(tmem, sub, kColG, row);
-                    const int i = q - 64;
-                    const float Gi = Gv[i];
+                for (int i = 0; i < 16; ++i) tb[i * 32] = x[i];
+            }
+            ok = true;
+            named_bar(2);
+            {
+                // lower-left 16x16 block of T_bb (b = q / 64): X = A_10 T_00 (16x16
+                // blocks of the 32x32 diagonal block), thread q: row r, columns c4 .. c4 + 3
+                const int b = q >> 6, r = (q >> 2) & 15, c4 = (q & 3) * 4;
+                float* tb = b ? T11 : T00;
+                const int o = 32 * b;  // first row/column of the 32x32 block in A
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) prow[j] = (j <= i) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
+                for (int k = 0; k < 16; ++k) {
+                    const float a = At[(o + k) * 64 + o + 16 + r];
+                    const float4 t4 = *reinterpret_cast<const float4*>(tb + k * 32 + c4);
+                    acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
+                    acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
                 }
-                tc_fence_before();
-                // P tiles are single-buffered: wait until the chain's product with the
-                // P tiles of iteration it - 1 (P Delta forward, P^T dO backward) is done
-                ok = true;
-                if (it >= 1) ok = mbar_wait(bar(B_PFREE), (it - 1) & 1, wl);
-                if (!ok) *abort_flag = 1;
-                if (ok) store_split_row(sm + oPhi, sm + oPlo, q - 64, prow);
+                float* xs = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
+                *reinterpret_cast<float4*>(xs + r * 64 + c4) = acc;
+                named_bar(2);
+                // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower triangular)
+                acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
+#pragma unroll 4
+                for (int k = 0; k < r; ++k) {
+                    const float a = tb[(16 + r) * 32 + 16 + k];
+                    const float4 v4 = *reinterpret_cast<const float4*>(xs + k * 64 + c4);
+                    acc.x = fmaf(a, v4.x, acc.x); acc.y = fmaf(a, v4.y, acc.y);
+                    acc.z = fmaf(a, v4.z, acc.z); acc.w = fmaf(a, v4.w, acc.w);
+                }
+                *reinterpret_cast<float4*>(tb + (16 + r) * 32 + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
             }
             named_bar(2);
             {
-                // X = A_10 T_00, thread q: row r = q / 4, columns c8 .. c8 + 7
+                // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), thread q:
+                // row r = q / 4, columns c8 .. c8 + 7
                 const int r = q >> 2, c8 = (q & 3) * 8;
                 float acc[8];
 #pragma unroll
@@ -874,18 +929,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
                     acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
                 }
-                *reinterpret_cast<float4*>(Xb + r * 32 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(Xb + r * 32 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
+                *reinterpret_cast<float4*>(xs + r * 64 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(xs + r * 64 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
                 named_bar(2);
                 // T_10 = -T_11 X (T_11 unit lower triangular)
-                float4 u0 = *reinterpret_cast<const float4*>(Xb + r * 32 + c8);
-                float4 u1 = *reinterpret_cast<const float4*>(Xb + r * 32 + c8 + 4);
+                float4 u0 = *reinterpret_cast<const float4*>(xs + r * 64 + c8);
+                float4 u1 = *reinterpret_cast<const float4*>(xs + r * 64 + c8 + 4);
                 acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
                 acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+#pragma unroll 4
                 for (int k = 0; k < r; ++k) {
                     const float a = T11[r * 32 + k];
-                    const float4 v0 = *reinterpret_cast<const float4*>(Xb + k * 32 + c8);
-                    const float4 v1 = *reinterpret_cast<const float4*>(Xb + k * 32 + c8 + 4);
+                    const float4 v0 = *reinterpret_cast<const float4*>(xs + k * 64 + c8);
+                    const float4 v1 = *reinterpret_cast<const float4*>(xs + k * 64 + c8 + 4);
                     acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
                     acc[2] = fmaf(a, v0.z, acc[2]); acc[3] = fmaf(a, v0.w, acc[3]);
                     acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
@@ -943,7 +1000,7 @@ cudaError_t launch_chain(const ChainArgs& a, uint32_t wait_limit, cudaStream_t s
     memset(&mq, 0, sizeof(mq));
     if (rows > 0 && a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
         return cudaErrorInvalidValue;
-    constexpr int smem = alloc_bytes<kBwd>();
+    constexpr int smem = kAlloc;
     cudaError_t e = cudaFuncSetAttribute(gdn_chain_ws_kernel<kBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     WsParams prm{a, wait_limit};
