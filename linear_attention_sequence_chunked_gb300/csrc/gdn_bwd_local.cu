@@ -14,9 +14,10 @@
 //   dbeta, dgam, dG (decays), dg = reverse running sum of dG in the chunk.
 // Sums over value columns (dP, dA, dO S0^T, the S-terms of dK) accumulate in
 // tensor memory across 64-column value slices, so each CTA writes complete
-// gradients: no partial sums leave the chip.  One CTA (128 threads) per
-// (chunk, head, sequence).  Computed MMA operands are split into bf16 hi + lo,
-// accumulation is fp32.
+// gradients: no partial sums leave the chip.  One CTA (256 threads) per
+// (chunk, head, sequence); warps w and w + 4 share a TMEM subpartition and
+// split the 64 columns of each accumulator row between them.  Computed MMA
+// operands are split into bf16 hi + lo, accumulation is fp32.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
@@ -31,7 +32,7 @@ namespace {
 using namespace sm100;
 using namespace tc;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kVs = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileS = kDk * 128;  // 128 rows x 128 B
@@ -56,8 +57,9 @@ constexpr int oRB = oRA + 2 * kTile64;          // dDelta -> dec o Delta; later 
 constexpr int oRC = oRB + 2 * kTile64;          // -dBhat [i][v]
 constexpr int oRD = oRC + 2 * kTile64;          // Y = -beta gam dBhat [i][v]
 constexpr int oVec = oRD + 2 * kTile64;         // g, beta, G, gam, dec, colsum
-constexpr int oRed = oVec + 6 * 64 * 4;         // 8 floats reduction scratch
-constexpr int oBar = oRed + 64;
+constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
+constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half
+constexpr int oBar = oPart + 64 * 8 * 4;
 constexpr int oMisc = oBar + 8;
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
@@ -69,6 +71,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     const int H = p.H, V = p.d_v, dk = p.d_k;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // TMEM subpartition of this warp and the column half it takes of a
+    // 64-column accumulator row
+    const int sub = warp & 3, hc = warp >> 2, col0 = 32 * hc;
     int b, t0, t1;
     if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
@@ -173,15 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
     }
     mma_sync_wait();
-    const int mrow = m64_row(warp, lane);
+    const int mrow = m64_row(sub, lane);
+    const uint32_t lb = static_cast<uint32_t>(sub * 32) << 16;
+    // 32 columns (col0 ..) of accumulator row mrow
+    auto ld_half = [&](uint32_t col, float* v) {
+        tmem_ld16(tmem + lb + col + col0, v);
+        tmem_ld16(tmem + lb + col + col0 + 16, v + 16);
+        tmem_ld_wait();
+    };
     {
-        float row[64];
-        ld_row64(tmem, warp, cX1, row);
+        float row[32];
+        ld_half(cX1, row);
         if (mrow >= 0) {
             const float Gi = Gv[mrow];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) row[j] = (j <= mrow) ? row[j] * exp_nonpos(Gi - Gv[j]) : 0.f;
-            store_split_row(sm + oP, sm + oP + kTile64, mrow, row);
+            for (int k = 0; k < 32; ++k) row[k] = (col0 + k <= mrow) ? row[k] * exp_nonpos(Gi - Gv[col0 + k]) : 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(sm + oP, sm + oP + kTile64, mrow, 4 * hc + c4, row + 8 * c4);
         }
     }
     fence_proxy_async_smem();
@@ -194,15 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     for (int vs = 0; vs < nslices; ++vs) {
         // ---- slice loads: S0, dS (fp32 -> hi/lo tiles), dO, V row ----
         {
-            float srow[64], drow[64];
-            const int d = tid;  // state row
+            // state row d, columns 32 hs .. 32 hs + 31 of the slice
+            const int d = tid & 127, hs = tid >> 7;
+            float srow[32], drow[32];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) { srow[j] = 0.f; drow[j] = 0.f; }
+            for (int j = 0; j < 32; ++j) { srow[j] = 0.f; drow[j] = 0.f; }
             if (d < dk) {
-                const float* s0 = p.chunk_states + (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs;
-                const float* s1 = p.chunk_dstates + (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs;
+                const long long off = (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs + 32 * hs;
+                const float* s0 = p.chunk_states + off;
+                const float* s1 = p.chunk_dstates + off;
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) {
+                for (int j = 0; j < 32; j += 4) {
                     const float4 a4 = *reinterpret_cast<const float4*>(s0 + j);
                     const float4 b4 = *reinterpret_cast<const float4*>(s1 + j);
                     srow[j] = a4.x; srow[j + 1] = a4.y; srow[j + 2] = a4.z; srow[j + 3] = a4.w;
@@ -210,9 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc_SdS = fmaf(srow[j], drow[j], acc_SdS);
-            store_split_row(sm + oSA, sm + oSA + kTileS, d, srow);
-            store_split_row(sm + oSB, sm + oSB + kTileS, d, drow);
+            for (int j = 0; j < 32; ++j) acc_SdS = fmaf(srow[j], drow[j], acc_SdS);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                store_split_chunk(sm + oSA, sm + oSA + kTileS, d, 4 * hs + c4, srow + 8 * c4);
+                store_split_chunk(sm + oSB, sm + oSB + kTileS, d, 4 * hs + c4, drow + 8 * c4);
+            }
         }
         for (int e = tid; e < 64 * 8; e += kThreads) {
             const int r = e >> 3, ch = e & 7;
@@ -222,14 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                     p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
             *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = val;
         }
-        float vrow[64];
+        // columns col0 .. col0 + 31 of value row mrow
+        float vrow[32];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) vrow[j] = 0.f;
+        for (int j = 0; j < 32; ++j) vrow[j] = 0.f;
         if (mrow >= 0 && mrow < nv) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) unpack8(src[ch], vrow + ch * 8);
+            for (int ch = 0; ch < 4; ++ch) unpack8(src[ch], vrow + ch * 8);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -253,15 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
             }
         }
         mma_sync_wait();
-        float ks0[64], pdo[64];
-        ld_row64(tmem, warp, cX1, ks0);
-        ld_row64(tmem, warp, cX2, pdo);
+        float ks0[32], pdo[32];
+        ld_half(cX1, ks0);
+        ld_half(cX2, pdo);
         if (mrow >= 0) {
-            float row[64];
+            float row[32];
             const float bj = bv[mrow], gj = gam[mrow];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
-            store_split_row(sm + oRA, sm + oRA + kTile64, mrow, row);
+            for (int c = 0; c < 32; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 4 * hc + c4, row + 8 * c4);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -292,14 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         {
             // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
             // dd = dec * sum_v (K dS) Delta for the decay term of dG
-            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
             const float dj = (mrow >= 0) ? dec[mrow] : 0.f;
             float dd = 0.f;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 2; ++g) {
                 float kds[16], dl[16];
-                tmem_ld16(tmem + lb + cX1 + g * 16, kds);
-                tmem_ld16(tmem + lb + cX2 + g * 16, dl);
+                tmem_ld16(tmem + lb + cX1 + col0 + g * 16, kds);
+                tmem_ld16(tmem + lb + cX2 + col0 + g * 16, dl);
                 tmem_ld_wait();
                 if (mrow >= 0) {
 #pragma unroll
@@ -307,10 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                         dd = fmaf(kds[c], dl[c], dd);
                         kds[c] = fmaf(scale, pdo[g * 16 + c], dj * kds[c]);
                     }
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g, kds);
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g + 1, kds + 8);
-                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 2 * g, dl);
-                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 2 * g + 1, dl + 8);
+                    const int ch = 4 * hc + 2 * g;
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch, kds);
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch + 1, kds + 8);
+                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, ch, dl);
+                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, ch + 1, dl + 8);
                 }
             }
             acc_dd = fmaf(dj, dd, acc_dd);
@@ -347,17 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         {
             // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RC, Y -> RD,
             // dec o Delta (Delta re-read from X2) -> RB
-            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
             const bool mine = mrow >= 0;
             const float bi = mine ? bv[mrow] : 0.f, gi = mine ? gam[mrow] : 0.f, dj = mine ? dec[mrow] : 0.f;
             float sv = 0.f, sk = 0.f;
             uint4* dst = reinterpret_cast<uint4*>(
-                p.dv + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
+                p.dv + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 2; ++g) {
                 float db[16], dl[16];
-                tmem_ld16(tmem + lb + cX1 + g * 16, db);
-                tmem_ld16(tmem + lb + cX2 + g * 16, dl);
+                tmem_ld16(tmem + lb + cX1 + col0 + g * 16, db);
+                tmem_ld16(tmem + lb + cX2 + col0 + g * 16, dl);
                 tmem_ld_wait();
                 if (mine) {
                     float t16[16];
@@ -376,18 +395,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                             dst[2 * g + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
                     }
+                    const int ch = 4 * hc + 2 * g;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) t16[c] = -db[c];
-                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, 2 * g, t16);
-                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, 2 * g + 1, t16 + 8);
+                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, ch, t16);
+                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, ch + 1, t16 + 8);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
-                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, 2 * g, t16);
-                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, 2 * g + 1, t16 + 8);
+                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, ch, t16);
+                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, ch + 1, t16 + 8);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) t16[c] = dj * dl[c];
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g, t16);
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, 2 * g + 1, t16 + 8);
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch, t16);
+                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch + 1, t16 + 8);
                 }
             }
             acc_dbeta += sv - gi * sk;
@@ -450,23 +470,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     float* E = reinterpret_cast<float*>(sm + oE);  // 64 x 65: column-sum terms
     float rowsum = 0.f, dbeta_a = 0.f;
     {
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
         const bool mine = mrow >= 0;
         const int i = mine ? mrow : 0;
         const float Gi = Gv[i], bi = bv[i];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
             float kk[16], da[16], qk[16], dp[16];
-            tmem_ld16(tmem + lb + cX1 + g * 16, kk);
-            tmem_ld16(tmem + lb + cdA + g * 16, da);
-            tmem_ld16(tmem + lb + cX2 + g * 16, qk);
-            tmem_ld16(tmem + lb + cdP + g * 16, dp);
+            const uint32_t col = col0 + g * 16;
+            tmem_ld16(tmem + lb + cX1 + col, kk);
+            tmem_ld16(tmem + lb + cdA + col, da);
+            tmem_ld16(tmem + lb + cX2 + col, qk);
+            tmem_ld16(tmem + lb + cdP + col, dp);
             tmem_ld_wait();
             if (mine) {
-                float dkk[16], dqk[16];
+                float dkk[16], dqk[16], e16[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const int j = g * 16 + c;
+                    const int j = col + c;
                     const float m = (j <= i) ? exp_nonpos(Gi - Gv[j]) : 0.f;
                     // A side (strictly lower): dA o (K K^T o Ms)
                     const float kkm = (j < i) ? kk[c] * m : 0.f;
@@ -477,14 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                     // P side (diagonal included): dQK = dP o M and dP o P
                     const float dpm = scale * dp[c] * m;
                     dqk[c] = dpm;
-                    const float e = dms + dpm * qk[c];
-                    rowsum += e;
-                    E[i * 65 + j] = e;
+                    e16[c] = dms + dpm * qk[c];
+                    rowsum += e16[c];
                 }
-                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, 2 * g, dkk);
-                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, 2 * g + 1, dkk + 8);
-                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, 2 * g, dqk);
-                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, 2 * g + 1, dqk + 8);
+                // stores after the loop: they may alias the decay loads
+#pragma unroll
+                for (int c = 0; c < 16; ++c) E[i * 65 + col + c] = e16[c];
+                const int ch = 4 * hc + 2 * g;
+                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, ch, dkk);
+                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, ch + 1, dkk + 8);
+                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, ch, dqk);
+                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, ch + 1, dqk + 8);
             }
         }
     }
@@ -530,16 +553,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
     mma_sync_wait();
     __syncthreads();
-    // ---- outputs of row mrow ----
+    // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63) ----
     float dG = 0.f, dbeta = 0.f;
     {
         const bool mine = mrow >= 0;
         const int i = mine ? mrow : 0;
         const float gi = gam[i];
         // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
-        float dgam = acc_dgam;
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-        for (int c16 = 0; c16 < 8; ++c16) {
+        float dgq = 0.f;
+        for (int c16 = 4 * hc; c16 < 4 * hc + 4; ++c16) {
             float u[16], q2[16], kk2[16];
             tmem_ld16(tmem + lb + cU + c16 * 16, u);
             tmem_ld16(tmem + lb + cX1 + c16 * 16, q2);
@@ -554,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
             }
 #pragma unroll
-            for (int e = 0; e < 16; ++e) dgam = fmaf(scale * qrow[e], u[e], dgam);
+            for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[e], dgq);
             if (i < nv && c16 * 16 < dk) {
                 uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
                 uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
@@ -572,22 +594,39 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 }
             }
         }
-        if (mine) {
-            if (i == 63) dgam += red[0] + red[1] + red[2] + red[3];
-            dG = rowsum - colsum[i] - acc_dd + dgam * gi;
-            dbeta = acc_dbeta + dbeta_a;
+        // the row terms of the upper column half join those of the lower half
+        float* part = reinterpret_cast<float*>(sm + oPart) + i * 8;
+        if (mine && hc == 1) {
+            part[0] = acc_dbeta;
+            part[1] = acc_dgam + dgq;
+            part[2] = acc_dd;
+            part[3] = rowsum;
+            part[4] = dbeta_a;
+        }
+        // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
+        {
+            float v = mine ? acc_dd : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) red[8 + warp] = v;
+        }
+        __syncthreads();
+        if (mine && hc == 0) {
+            float dgam = acc_dgam + dgq + part[1];
+            float sdd = 0.f;
+            if (i == 63) {
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    dgam += red[w];
+                    sdd += red[8 + w];
+                }
+            }
+            dG = (rowsum + part[3]) - colsum[i] - (acc_dd + part[2]) + dgam * gi + sdd;
+            dbeta = acc_dbeta + part[0] + dbeta_a + part[4];
         }
     }
-    // dG_63 also collects the decay terms sum_j dd_j
-    {
-        float v = (mrow >= 0) ? acc_dd : 0.f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[4 + warp] = v;
-    }
     __syncthreads();
-    if (mrow >= 0) {
-        if (mrow == 63) dG += red[4] + red[5] + red[6] + red[7];
+    if (mrow >= 0 && hc == 0) {
         colsum[mrow] = dG;  // reuse as dG vector
         bv[mrow] = dbeta;   // reuse as dbeta vector
     }

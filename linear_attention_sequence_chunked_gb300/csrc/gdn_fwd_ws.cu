@@ -78,7 +78,8 @@ constexpr int oP = oDlo + kTile64;                  // [slot][hi,lo] P tiles
 constexpr int oT = oP + 4 * kTile64;                // [slot][hi,lo] T tiles
 constexpr int oA = oT + 4 * kTile64;                // A^T fp32 [64][64] (prep)
 constexpr int oTf = oA + 64 * 64 * 4;               // fp32 32x32 blocks T_00, T_11, T_10 (prep)
-constexpr int kTB = 32 * 32;                        // floats per 32x32 block
+constexpr int kTS = 36;                             // their row stride (16-byte rows, rows on distinct banks)
+constexpr int kTB = 32 * kTS;                       // floats per block
 constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the upper-right 16x16 blocks of the 32x32 inverse blocks T_00, T_11 stay zero
     for (int i = tid; i < 2 * 16 * 16; i += kThreads) {
         float* tb = reinterpret_cast<float*>(sm + oTf) + (i >> 8) * kTB;
-        tb[((i >> 4) & 15) * 32 + 16 + (i & 15)] = 0.f;
+        tb[((i >> 4) & 15) * kTS + 16 + (i & 15)] = 0.f;
     }
     // d_k = 64: the upper key region of every stage stays zero
     if (!use_tma) {
@@ -877,9 +878,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // into the 32x32 block T_bb (b = d / 2) at rows/columns 16 (d % 2) ..
-                float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * 33 + c;
+                float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * (kTS + 1) + c;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) tb[i * 32] = x[i];
+                for (int i = 0; i < 16; ++i) tb[i * kTS] = x[i];
             }
             ok = true;
             named_bar(2);
@@ -893,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const float a = At[(o + k) * 64 + o + 16 + r];
-                    const float4 t4 = *reinterpret_cast<const float4*>(tb + k * 32 + c4);
+                    const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
                     acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
                     acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
                 }
@@ -904,12 +905,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
 #pragma unroll 4
                 for (int k = 0; k < r; ++k) {
-                    const float a = tb[(16 + r) * 32 + 16 + k];
+                    const float a = tb[(16 + r) * kTS + 16 + k];
                     const float4 v4 = *reinterpret_cast<const float4*>(xs + k * 64 + c4);
                     acc.x = fmaf(a, v4.x, acc.x); acc.y = fmaf(a, v4.y, acc.y);
                     acc.z = fmaf(a, v4.z, acc.z); acc.w = fmaf(a, v4.w, acc.w);
                 }
-                *reinterpret_cast<float4*>(tb + (16 + r) * 32 + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                *reinterpret_cast<float4*>(tb + (16 + r) * kTS + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
             }
             named_bar(2);
             {
@@ -922,8 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 8
                 for (int k = 0; k < 32; ++k) {
                     const float a = At[k * 64 + 32 + r];
-                    const float4 t0 = *reinterpret_cast<const float4*>(T00 + k * 32 + c8);
-                    const float4 t1 = *reinterpret_cast<const float4*>(T00 + k * 32 + c8 + 4);
+                    const float4 t0 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8);
+                    const float4 t1 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8 + 4);
                     acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
                     acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
                     acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
@@ -940,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
 #pragma unroll 4
                 for (int k = 0; k < r; ++k) {
-                    const float a = T11[r * 32 + k];
+                    const float a = T11[r * kTS + k];
                     const float4 v0 = *reinterpret_cast<const float4*>(xs + k * 64 + c8);
                     const float4 v1 = *reinterpret_cast<const float4*>(xs + k * 64 + c8 + 4);
                     acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
@@ -948,8 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
                     acc[6] = fmaf(a, v1.z, acc[6]); acc[7] = fmaf(a, v1.w, acc[7]);
                 }
-                *reinterpret_cast<float4*>(T10 + r * 32 + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-                *reinterpret_cast<float4*>(T10 + r * 32 + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+                *reinterpret_cast<float4*>(T10 + r * kTS + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+                *reinterpret_cast<float4*>(T10 + r * kTS + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
             }
             named_bar(2);
             {
@@ -960,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cc = col & 31;
                 float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = src ? src[i * 32 + cc] : 0.f;
+                for (int i = 0; i < 32; ++i) v[i] = src ? src[i * kTS + cc] : 0.f;
                 uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
                 uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
 #pragma unroll
