@@ -59,8 +59,8 @@ constexpr int oRD = oRC + 2 * kTile64;          // Y = -beta gam dBhat [i][v]
 constexpr int oVec = oRD + 2 * kTile64;         // g, beta, G, gam, dec, colsum
 constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
 constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half
-constexpr int oBar = oPart + 64 * 8 * 4;
-constexpr int oMisc = oBar + 8;
+constexpr int oBar = oPart + 64 * 8 * 4;         // MMA completion, state tiles landed
+constexpr int oMisc = oBar + 16;
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 232448, "shared memory");
@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     const int nv = min(kChunk, t1 - c0);
     const long long row_base = static_cast<long long>(b) * p.T;
     const long long slot = chunk_slot_base(p.cu_seqlens, n, p.T) + ci;
-    const long long KV = static_cast<long long>(dk) * V;
     const float scale = p.scale;
 
     extern __shared__ uint8_t smem_raw[];
@@ -97,6 +96,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     uint64_t* barp = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
     const uint32_t bar = smem_u32(barp);
+    const uint32_t sbar = smem_u32(barp + 1);
+    const int nsl = V / kVs;
+    bool s_out = false;  // thread 0: a state-tile copy is in flight
+    // state tiles of value slice vs (bf16 hi/lo operand tiles written by the
+    // state passes, [slot][head][slice][hi, lo]) -> the S0 and dS tiles
+    auto issue_state = [&](int vs) {
+        const long long off = ((slot * H + h) * nsl + vs) * (2LL * dk * 128);
+        const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.chunk_states) + off;
+        const uint8_t* s1 = reinterpret_cast<const uint8_t*>(p.chunk_dstates) + off;
+        const uint32_t nb = dk * 128;
+        s_out = true;
+        mbar_arrive_expect_tx(sbar, 4 * nb);
+        bulk_g2s(smem_u32(sm + oSA), s0, nb, sbar);
+        bulk_g2s(smem_u32(sm + oSA + kTileS), s0 + nb, nb, sbar);
+        bulk_g2s(smem_u32(sm + oSB), s1, nb, sbar);
+        bulk_g2s(smem_u32(sm + oSB + kTileS), s1 + nb, nb, sbar);
+    };
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -104,7 +120,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(sbar, 1);
         fence_mbar_init();
+        issue_state(0);
+    }
+    // d_k = 64: key rows 64-127 of the state tiles stay zero
+    if (dk < kDk) {
+        for (int e = tid; e < 4 * 64 * 8; e += kThreads) {
+            const int tile = e >> 9, r = 64 + ((e >> 3) & 63), ch = e & 7;
+            *reinterpret_cast<uint4*>(sm + (tile < 2 ? oSA : oSB) + (tile & 1) * kTileS + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
     }
     // ---- K/Q tiles (plain 16-byte loads, rows beyond the chunk are zero) ----
     for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
@@ -180,6 +206,29 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     mma_sync_wait();
     const int mrow = m64_row(sub, lane);
     const uint32_t lb = static_cast<uint32_t>(sub * 32) << 16;
+    // the dO tile and the value row of slice vs, fetched into registers one
+    // slice ahead: two 16-byte pieces of the dO tile per thread, and columns
+    // col0 .. col0 + 31 of value row mrow
+    uint4 do_raw[2], v_raw[4];
+    auto fetch_rows = [&](int vs) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
+            do_raw[k] = make_uint4(0, 0, 0, 0);
+            if (r < nv)
+                do_raw[k] = *reinterpret_cast<const uint4*>(
+                    p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) v_raw[ch] = make_uint4(0, 0, 0, 0);
+        if (mrow >= 0 && mrow < nv) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) v_raw[ch] = src[ch];
+        }
+    };
+    fetch_rows(0);
     // 32 columns (col0 ..) of accumulator row mrow
     auto ld_half = [&](uint32_t col, float* v) {
         tmem_ld16(tmem + lb + col + col0, v);
@@ -203,53 +252,43 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
 
     // per-row accumulators (thread mrow) across value slices
     float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
+    uint32_t sphase = 0;
     const int nslices = V / kVs;
     for (int vs = 0; vs < nslices; ++vs) {
-        // ---- slice loads: S0, dS (fp32 -> hi/lo tiles), dO, V row ----
+        // ---- slice loads: S0, dS tiles, dO tile, V row ----
+        // state tiles of this slice (bulk copies issued one slice ahead)
+        if (mbar_wait(sbar, sphase, kDefaultWaitLimit)) {
+            sphase ^= 1u;
+            s_out = false;
+        } else {
+            failed = true;
+        }
         {
-            // state row d, columns 32 hs .. 32 hs + 31 of the slice
+            // <dS, S0> over 32 values of state row d (hi + lo is the fp32 value to ~16 bits)
             const int d = tid & 127, hs = tid >> 7;
-            float srow[32], drow[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) { srow[j] = 0.f; drow[j] = 0.f; }
             if (d < dk) {
-                const long long off = (slot * H + h) * KV + static_cast<long long>(d) * V + vs * kVs + 32 * hs;
-                const float* s0 = p.chunk_states + off;
-                const float* s1 = p.chunk_dstates + off;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(s0 + j);
-                    const float4 b4 = *reinterpret_cast<const float4*>(s1 + j);
-                    srow[j] = a4.x; srow[j + 1] = a4.y; srow[j + 2] = a4.z; srow[j + 3] = a4.w;
-                    drow[j] = b4.x; drow[j + 1] = b4.y; drow[j + 2] = b4.z; drow[j + 3] = b4.w;
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
+                    float ah[8], al[8], bh[8], bl[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sm + oSA + off), ah);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + oSA + kTileS + off), al);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + oSB + off), bh);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + oSB + kTileS + off), bl);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
                 }
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc_SdS = fmaf(srow[j], drow[j], acc_SdS);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                store_split_chunk(sm + oSA, sm + oSA + kTileS, d, 4 * hs + c4, srow + 8 * c4);
-                store_split_chunk(sm + oSB, sm + oSB + kTileS, d, 4 * hs + c4, drow + 8 * c4);
-            }
         }
-        for (int e = tid; e < 64 * 8; e += kThreads) {
-            const int r = e >> 3, ch = e & 7;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < nv)
-                val = *reinterpret_cast<const uint4*>(
-                    p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
-            *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = val;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
+            *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[k];
         }
         // columns col0 .. col0 + 31 of value row mrow
         float vrow[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) vrow[j] = 0.f;
-        if (mrow >= 0 && mrow < nv) {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) unpack8(src[ch], vrow + ch * 8);
-        }
+        for (int ch = 0; ch < 4; ++ch) unpack8(v_raw[ch], vrow + ch * 8);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -452,8 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 mma_bf16(tmem + cdK, yl, sah, id_n, 1);
             }
         }
+        if (vs + 1 < nslices) fetch_rows(vs + 1);  // while the batch runs
         mma_sync_wait();
         __syncthreads();
+        if (tid == 0 && vs + 1 < nslices && !failed) issue_state(vs + 1);  // the S0 / dS tiles are free
     }
 
     // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
@@ -655,9 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
     if (failed) {
         record_error(p.err, kErrTimeout);
-        if (tid == 0) {  // let every MMA this CTA issued land before the TMEM is released
+        if (tid == 0) {  // let every MMA and copy this CTA issued land before it leaves
             mma_commit(bar);
             mbar_wait(bar, phase, kDefaultWaitLimit);
+            if (s_out) mbar_wait(sbar, sphase, kDefaultWaitLimit);
         }
     }
     tc_fence_before();

@@ -230,6 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar(1);
 
+        // This chunk's state tile (forward: start state; backward: gradient
+        // w.r.t. the end state) for the chunk-parallel gradient pass: bulk
+        // copies of the bf16 hi/lo operand tiles, [slot][head][value slice][hi, lo].
+        auto store_state_tiles = [&](int ci) {
+            const long long nsl = V / kVs;
+            uint8_t* dst = reinterpret_cast<uint8_t*>(p.chunk_states) +
+                           (((slot0 + ci) * H + h) * nsl + vs) * (2LL * dk * 128);
+            bulk_s2g(dst, smem_u32(Shi), dk * 128);
+            bulk_s2g(dst + dk * 128, smem_u32(Slo), dk * 128);
+            bulk_commit();
+        };
         bool aborted = false;
         if constexpr (!kBwd) {
             // value row of this slice (row mrow of the chunk), packed bf16; the
@@ -258,12 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* gam = vec + 192;
                 const float* dec = vec + 256;
 
-                if (p.chunk_states && srow >= 0) {
-                    float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
-#pragma unroll
-                    for (int j = 0; j < kVs; j += 4)
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                }
+                if (p.chunk_states && t == 0) store_state_tiles(ci);
                 // K/Q tiles of this chunk
                 if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
                 named_bar(1);
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
+                if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
                 // every MMA that reads this chunk's K/Q stage has completed
@@ -488,12 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* dec = vec + 256;
 
                 // gradient w.r.t. this chunk's end state, for the chunk-parallel pass
-                if (p.chunk_states && srow >= 0) {
-                    float* dst = p.chunk_states + ((slot0 + ci) * H + h) * KV + vs * kVs + static_cast<long long>(srow) * V;
-#pragma unroll
-                    for (int j = 0; j < kVs; j += 4)
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                }
+                if (p.chunk_states && t == 0) store_state_tiles(ci);
                 // dO tile (single buffer: the previous chunk's P^T dO has completed)
                 if (mrow >= 0) {
 #pragma unroll
@@ -644,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
+                if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
                 // every MMA that reads this chunk's K/Q stage has completed
@@ -672,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) { aborted = true; break; }
             }
         }
+        if (p.chunk_states && t == 0) bulk_wait_all();
         if (aborted) {
             if (t == 0) {
                 record_error(p.err, kErrTimeout);

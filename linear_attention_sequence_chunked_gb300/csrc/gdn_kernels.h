@@ -18,7 +18,8 @@ struct FwdArgs {
     const int32_t* cu_seqlens;
     uint16_t* out;          // may be null: skip the output
     float* final_state;     // may be null
-    float* chunk_states;    // may be null: per-chunk start states [slot][H][d_k][d_v]
+    float* chunk_states;    // may be null: per-chunk start states, bf16 hi/lo operand tiles
+                            // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v])
     uint8_t* chunk_T;       // may be null: per-chunk T operand tiles [slot][H][2 x 8 KB]
     int N;                  // sequences (B dense, or cu_seqlens length - 1)
     int T;                  // tokens per batch row (dense) / total tokens (packed)
@@ -39,7 +40,7 @@ struct BwdChainArgs {
     float scale;
     const int32_t* cu_seqlens;
     const float* d_final_state;   // may be null
-    float* chunk_dstates;         // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
+    float* chunk_dstates;         // gradient w.r.t. each chunk's end state, tiles as FwdArgs::chunk_states
     float* d_initial_state;       // may be null
     int N;
     int T;
@@ -59,8 +60,8 @@ struct BwdLocalArgs {
     const uint16_t* d_out;
     float scale;
     const int32_t* cu_seqlens;
-    const float* chunk_states;    // [slot][H][d_k][d_v]: start state of each chunk
-    const float* chunk_dstates;   // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
+    const float* chunk_states;    // start state of each chunk, tiles as FwdArgs::chunk_states
+    const float* chunk_dstates;   // gradient w.r.t. each chunk's end state, same tiles
     const uint8_t* chunk_T;       // [slot][H][2 x 8 KB]
     uint16_t* dq;
     uint16_t* dk;
