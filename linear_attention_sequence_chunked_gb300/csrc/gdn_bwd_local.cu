@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     const float scale = p.scale;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sm = smem_raw + smem_align_pad(smem_raw);  // 1024-aligned, still known to be shared memory
     float* gv = reinterpret_cast<float*>(sm + oVec);
     float* bv = gv + 64;
     float* Gv = gv + 128;

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sm = smem_raw + smem_align_pad(smem_raw);  // 1024-aligned, still known to be shared memory
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oMisc + 4);

@@ -18,6 +18,13 @@ constexpr int kTile64 = 64 * 128;        // 64 rows x 128 bytes (64 bf16)
 constexpr int kRegionBytes = 128 * 128;  // [K rows 0-63 ; Q rows 64-127] x 128 bytes
 constexpr int kDk = 128;                 // key width of the tiles
 
+// Bytes to add to the dynamic shared-memory base for 1024-byte alignment.
+// Offsetting the shared array itself (rather than rounding its address as an
+// integer) lets the compiler keep using shared-memory loads and stores.
+__device__ __forceinline__ uint32_t smem_align_pad(const uint8_t* base) {
+    return (1024u - (smem_u32(base) & 1023u)) & 1023u;
+}
+
 // bar.sync on a named barrier for `count` threads
 __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
