@@ -728,8 +728,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* gam = vec + 192;
             float* dec = vec + 256;
 
-            // gates of this chunk into its slot (free once the chain finished iteration it - 2)
             bool ok = true;
+            // K/Q tiles
+            if (!use_tma) {
+                if (it >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((it - 2) >> 1) & 1, wl);
+                if (!ok) *abort_flag = 1;
+                named_bar(2);
+                if (*abort_flag) { aborted = true; break; }
+                for (int e = q; e < 2 * 64 * 8; e += 128) {
+                    const int which = e >> 9;
+                    const int r = (e >> 3) & 63, ch = e & 7;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (r < nv) {
+                        const uint16_t* src = which ? p.q : p.k;
+                        val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
+                    }
+                    *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+                }
+                fence_proxy_async_smem();
+                named_bar(2);
+                if (q == 0) mbar_arrive(bar(B_FULL0 + st));
+            }
+            if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
+            named_bar(2);
+            if (*abort_flag) { aborted = true; break; }
+
+            // gram K K^T and Q K^T (two M = 64 products), running while the
+            // gates are formed
+            if (q == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
+                const uint32_t stage_a = smem_u32(stage);
+#pragma unroll
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                    const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                    mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
+                    mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
+                }
+                mma_commit(bar(B_GRAM));
+            }
+
+            // gates of this chunk into its slot (free once the chain finished iteration it - 2)
+            ok = true;
             if (it >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((it - 2) >> 1) & 1, wl);
             if (!ok) *abort_flag = 1;
             named_bar(2);
@@ -758,46 +800,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (q < 64) dec[q] = exp_nonpos(Gv[63] - Gv[q]);
 
-            // K/Q tiles
-            if (!use_tma) {
-                ok = true;
-                if (it >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((it - 2) >> 1) & 1, wl);
-                if (!ok) *abort_flag = 1;
-                named_bar(2);
-                if (*abort_flag) { aborted = true; break; }
-                for (int e = q; e < 2 * 64 * 8; e += 128) {
-                    const int which = e >> 9;
-                    const int r = (e >> 3) & 63, ch = e & 7;
-                    uint4 val = make_uint4(0, 0, 0, 0);
-                    if (r < nv) {
-                        const uint16_t* src = which ? p.q : p.k;
-                        val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
-                    }
-                    *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
-                }
-                fence_proxy_async_smem();
-                named_bar(2);
-                if (q == 0) mbar_arrive(bar(B_FULL0 + st));
-            }
-            if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
-            named_bar(2);
-            if (*abort_flag) { aborted = true; break; }
-
-            // gram K K^T and Q K^T (two M = 64 products)
-            if (q == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
-                const uint32_t stage_a = smem_u32(stage);
-#pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
-                    const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
-                    mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
-                    mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
-                }
-                mma_commit(bar(B_GRAM));
-            }
             __syncwarp();
             if (!mbar_wait(bar(B_GRAM), ph, wl)) *abort_flag = 1;
             tc_fence_after();
