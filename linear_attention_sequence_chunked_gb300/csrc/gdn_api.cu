@@ -165,11 +165,11 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     f.N = B; f.T = T; f.H = H; f.d_k = d_k; f.d_v = d_v; f.err = err;
     if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
 
-    // pass 2: reverse chain of state gradients
+    // pass 2: reverse chain of state gradients (T tiles from pass 1)
     gdn::BwdChainArgs c{};
     c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
     c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;
-    c.chunk_dstates = dstates; c.d_initial_state = d_initial_state;
+    c.chunk_dstates = dstates; c.chunk_T = tiles; c.d_initial_state = d_initial_state;
     c.N = B; c.T = T; c.H = H; c.d_k = d_k; c.d_v = d_v; c.err = err;
     if (!launched(gdn::launch_bwd_chain(c, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
 

@@ -94,7 +94,7 @@ static_assert(kAlloc <= 232448, "shared memory");
 // barrier indices
 enum {
     B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
-    B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10,
+    B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_TCOPY = 11,
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15
 };
 
@@ -114,7 +114,8 @@ struct ChainArgs {
     uint16_t* out;                // forward output (may be null)
     float* state_out;             // forward: final state; backward: initial-state gradient (may be null)
     float* chunk_states;          // forward: chunk start states; backward: chunk end-state gradients (may be null)
-    uint8_t* chunk_T;             // forward: T operand tiles of every chunk (may be null)
+    uint8_t* chunk_T;             // T operand tiles of every chunk: written by the forward, read by
+                                  // the backward (may be null: not written / computed in place)
     int N, T, H, d_k, d_v;
     int* err;
 };
@@ -147,6 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long row_base = static_cast<long long>(b) * p.T;
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
     const bool want_out = !kBwd && p.out != nullptr;
+    // the prep forms P only where the chain uses it (output, or P^T dO), and
+    // the backward takes the T tiles the state pass already wrote
+    const bool want_p = kBwd || want_out;
+    const bool load_t = kBwd && p.chunk_T != nullptr;
     const uint32_t wl = prm.wait_limit;
     // iteration it works on chunk chunk_of(it): forward in order, backward reversed
     auto chunk_of = [&](int it) { return kBwd ? nchunks - 1 - it : it; };
@@ -713,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         load_gates(0);
+        bool tcopy_out = false;  // thread q == 0: a T tile copy is in flight (phase tcopy_it & 1)
+        int tcopy_it = 0;
         bool aborted = false;
         for (int it = 0; it < nchunks; ++it) {
             const int ci = chunk_of(it);
@@ -764,8 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
                     const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
                     const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
-                    mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
-                    mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
+                    if (!load_t) mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
+                    if (want_p) mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
                 }
                 mma_commit(bar(B_GRAM));
             }
@@ -776,6 +783,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) *abort_flag = 1;
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
+            if (load_t && q == 0) {
+                // T tiles of this chunk (written by the forward state pass) into the free slot
+                mbar_arrive_expect_tx(bar(B_TCOPY), 2 * kTile64);
+                bulk_g2s(smem_u32(sm + oT + (slot * 2) * kTile64),
+                         p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64), 2 * kTile64, bar(B_TCOPY));
+                tcopy_out = true;
+                tcopy_it = it;
+            }
             if (q < 64) {
                 gv[q] = g_pre;
                 bv[q] = b_pre;
@@ -825,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the M = 64 products sit in lanes 0-15 of each subpartition: lane
                 // l < 16 loads row i, lane l + 16 takes its upper 32 columns
                 const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-                {
+                if (!load_t) {
                     float lo[32], up[32];
                     tmem_ld16(lb + kColG, lo);
                     tmem_ld16(lb + kColG + 16, lo + 16);
@@ -840,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 32; ++k) At[(j0 + k) * 64 + i] = lo[k];
                 }
-                {
+                if (want_p) {
                     float lo[32], up[32];
                     tmem_ld16(lb + kColQK, lo);
                     tmem_ld16(lb + kColQK + 16, lo + 16);
@@ -861,133 +876,142 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             named_bar(2);
-            if (q < 64) {
-                // column c of the 16x16 diagonal block d = q / 16 by right-looking
-                // forward substitution: x = e_c; for m: for i > m: x_i -= A_im x_m.
-                // Row m of A^T is read as broadcast 16-byte loads.
-                const int d = q >> 4, c = q & 15;
-                float x[16];
+            if (!load_t) {
+                if (q < 64) {
+                    // column c of the 16x16 diagonal block d = q / 16 by right-looking
+                    // forward substitution: x = e_c; for m: for i > m: x_i -= A_im x_m.
+                    // Row m of A^T is read as broadcast 16-byte loads.
+                    const int d = q >> 4, c = q & 15;
+                    float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
-                const float* ablk = At + 16 * d * 64 + 16 * d;
+                    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+                    const float* ablk = At + 16 * d * 64 + 16 * d;
 #pragma unroll
-                for (int m = 0; m < 15; ++m) {
-                    const float xm = x[m];
-                    const float4* arow = reinterpret_cast<const float4*>(ablk + m * 64);
+                    for (int m = 0; m < 15; ++m) {
+                        const float xm = x[m];
+                        const float4* arow = reinterpret_cast<const float4*>(ablk + m * 64);
 #pragma unroll
-                    for (int i4 = (m + 1) >> 2; i4 < 4; ++i4) {
-                        const float4 a4 = arow[i4];
-                        if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
-                        if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
-                        if (4 * i4 + 2 > m) x[4 * i4 + 2] = fmaf(-a4.z, xm, x[4 * i4 + 2]);
-                        if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
+                        for (int i4 = (m + 1) >> 2; i4 < 4; ++i4) {
+                            const float4 a4 = arow[i4];
+                            if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
+                            if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
+                            if (4 * i4 + 2 > m) x[4 * i4 + 2] = fmaf(-a4.z, xm, x[4 * i4 + 2]);
+                            if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
+                        }
                     }
-                }
-                // into the 32x32 block T_bb (b = d / 2) at rows/columns 16 (d % 2) ..
-                float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * (kTS + 1) + c;
+                    // into the 32x32 block T_bb (b = d / 2) at rows/columns 16 (d % 2) ..
+                    float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * (kTS + 1) + c;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) tb[i * kTS] = x[i];
-            }
-            ok = true;
-            named_bar(2);
-            {
-                // lower-left 16x16 block of T_bb (b = q / 64): X = A_10 T_00 (16x16
-                // blocks of the 32x32 diagonal block), thread q: row r, columns c4 .. c4 + 3
-                const int b = q >> 6, r = (q >> 2) & 15, c4 = (q & 3) * 4;
-                float* tb = b ? T11 : T00;
-                const int o = 32 * b;  // first row/column of the 32x32 block in A
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a = At[(o + k) * 64 + o + 16 + r];
-                    const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
-                    acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
-                    acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
+                    for (int i = 0; i < 16; ++i) tb[i * kTS] = x[i];
                 }
-                float* xs = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
-                *reinterpret_cast<float4*>(xs + r * 64 + c4) = acc;
+                ok = true;
                 named_bar(2);
-                // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower triangular)
-                acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
-#pragma unroll 4
-                for (int k = 0; k < r; ++k) {
-                    const float a = tb[(16 + r) * kTS + 16 + k];
-                    const float4 v4 = *reinterpret_cast<const float4*>(xs + k * 64 + c4);
-                    acc.x = fmaf(a, v4.x, acc.x); acc.y = fmaf(a, v4.y, acc.y);
-                    acc.z = fmaf(a, v4.z, acc.z); acc.w = fmaf(a, v4.w, acc.w);
-                }
-                *reinterpret_cast<float4*>(tb + (16 + r) * kTS + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-            }
-            named_bar(2);
-            {
-                // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), thread q:
-                // row r = q / 4, columns c8 .. c8 + 7
-                const int r = q >> 2, c8 = (q & 3) * 8;
-                float acc[8];
+                {
+                    // lower-left 16x16 block of T_bb (b = q / 64): X = A_10 T_00 (16x16
+                    // blocks of the 32x32 diagonal block), thread q: row r, columns c4 .. c4 + 3
+                    const int b = q >> 6, r = (q >> 2) & 15, c4 = (q & 3) * 4;
+                    float* tb = b ? T11 : T00;
+                    const int o = 32 * b;  // first row/column of the 32x32 block in A
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                    for (int k = 0; k < 16; ++k) {
+                        const float a = At[(o + k) * 64 + o + 16 + r];
+                        const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
+                        acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
+                        acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
+                    }
+                    float* xs = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
+                    *reinterpret_cast<float4*>(xs + r * 64 + c4) = acc;
+                    named_bar(2);
+                    // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower triangular)
+                    acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
+#pragma unroll 4
+                    for (int k = 0; k < r; ++k) {
+                        const float a = tb[(16 + r) * kTS + 16 + k];
+                        const float4 v4 = *reinterpret_cast<const float4*>(xs + k * 64 + c4);
+                        acc.x = fmaf(a, v4.x, acc.x); acc.y = fmaf(a, v4.y, acc.y);
+                        acc.z = fmaf(a, v4.z, acc.z); acc.w = fmaf(a, v4.w, acc.w);
+                    }
+                    *reinterpret_cast<float4*>(tb + (16 + r) * kTS + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                }
+                named_bar(2);
+                {
+                    // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), thread q:
+                    // row r = q / 4, columns c8 .. c8 + 7
+                    const int r = q >> 2, c8 = (q & 3) * 8;
+                    float acc[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    const float a = At[k * 64 + 32 + r];
-                    const float4 t0 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8);
-                    const float4 t1 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8 + 4);
-                    acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
-                    acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
-                    acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
-                    acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
-                }
-                float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
-                *reinterpret_cast<float4*>(xs + r * 64 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(xs + r * 64 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                named_bar(2);
-                // T_10 = -T_11 X (T_11 unit lower triangular)
-                float4 u0 = *reinterpret_cast<const float4*>(xs + r * 64 + c8);
-                float4 u1 = *reinterpret_cast<const float4*>(xs + r * 64 + c8 + 4);
-                acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
-                acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+                    for (int k = 0; k < 32; ++k) {
+                        const float a = At[k * 64 + 32 + r];
+                        const float4 t0 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8);
+                        const float4 t1 = *reinterpret_cast<const float4*>(T00 + k * kTS + c8 + 4);
+                        acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
+                        acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+                        acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
+                        acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
+                    }
+                    float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
+                    *reinterpret_cast<float4*>(xs + r * 64 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    *reinterpret_cast<float4*>(xs + r * 64 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    named_bar(2);
+                    // T_10 = -T_11 X (T_11 unit lower triangular)
+                    float4 u0 = *reinterpret_cast<const float4*>(xs + r * 64 + c8);
+                    float4 u1 = *reinterpret_cast<const float4*>(xs + r * 64 + c8 + 4);
+                    acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+                    acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
 #pragma unroll 4
-                for (int k = 0; k < r; ++k) {
-                    const float a = T11[r * kTS + k];
-                    const float4 v0 = *reinterpret_cast<const float4*>(xs + k * 64 + c8);
-                    const float4 v1 = *reinterpret_cast<const float4*>(xs + k * 64 + c8 + 4);
-                    acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
-                    acc[2] = fmaf(a, v0.z, acc[2]); acc[3] = fmaf(a, v0.w, acc[3]);
-                    acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
-                    acc[6] = fmaf(a, v1.z, acc[6]); acc[7] = fmaf(a, v1.w, acc[7]);
+                    for (int k = 0; k < r; ++k) {
+                        const float a = T11[r * kTS + k];
+                        const float4 v0 = *reinterpret_cast<const float4*>(xs + k * 64 + c8);
+                        const float4 v1 = *reinterpret_cast<const float4*>(xs + k * 64 + c8 + 4);
+                        acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
+                        acc[2] = fmaf(a, v0.z, acc[2]); acc[3] = fmaf(a, v0.w, acc[3]);
+                        acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
+                        acc[6] = fmaf(a, v1.z, acc[6]); acc[7] = fmaf(a, v1.w, acc[7]);
+                    }
+                    *reinterpret_cast<float4*>(T10 + r * kTS + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+                    *reinterpret_cast<float4*>(T10 + r * kTS + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
                 }
-                *reinterpret_cast<float4*>(T10 + r * kTS + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-                *reinterpret_cast<float4*>(T10 + r * kTS + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
-            }
-            named_bar(2);
-            {
-                // column col of T = row col of the T^T tile (read MN-major for T,
-                // K-major for T^T); this thread writes its entries 32 hf .. 32 hf + 31
-                const int col = q & 63, hf = q >> 6;
-                const float* src = col < 32 ? (hf ? T10 : T00) : (hf ? T11 : nullptr);
-                const int cc = col & 31;
-                float v[32];
+                named_bar(2);
+                {
+                    // column col of T = row col of the T^T tile (read MN-major for T,
+                    // K-major for T^T); this thread writes its entries 32 hf .. 32 hf + 31
+                    const int col = q & 63, hf = q >> 6;
+                    const float* src = col < 32 ? (hf ? T10 : T00) : (hf ? T11 : nullptr);
+                    const int cc = col & 31;
+                    float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = src ? src[i * kTS + cc] : 0.f;
-                uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
-                uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
+                    for (int i = 0; i < 32; ++i) v[i] = src ? src[i * kTS + cc] : 0.f;
+                    uint8_t* t_hi = sm + oT + (slot * 2 + 0) * kTile64;
+                    uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(t_hi, t_lo, col, 4 * hf + c4, v + 8 * c4);
-                if (!kBwd && p.chunk_T && vs == 0) {
-                    // the same operand bytes, for the chunk-parallel gradient pass
-                    uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
+                    for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(t_hi, t_lo, col, 4 * hf + c4, v + 8 * c4);
+                    if (!kBwd && p.chunk_T && vs == 0) {
+                        // the same operand bytes, for the chunk-parallel gradient pass
+                        uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t off = sw128_offset(col, (4 * hf + c4) * 16);
-                        dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
-                        dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const uint32_t off = sw128_offset(col, (4 * hf + c4) * 16);
+                            dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
+                            dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
+                        }
                     }
                 }
             }
             fence_proxy_async_smem();
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
-            if (q == 0) mbar_arrive(bar(B_READY0 + slot));
+            if (q == 0) {
+                if (load_t) {
+                    if (mbar_wait(bar(B_TCOPY), it & 1, wl)) tcopy_out = false;
+                    else *abort_flag = 1;
+                }
+                if (!tcopy_out) mbar_arrive(bar(B_READY0 + slot));
+            }
         }
+        if (q == 0 && tcopy_out) mbar_wait(bar(B_TCOPY), tcopy_it & 1, wl);  // no copy outlives the CTA
         if (aborted && q == 0) {
             record_error(p.err, kErrTimeout);
             mma_commit(bar(B_DRAIN1));
@@ -1033,7 +1057,7 @@ cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStr
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = nullptr; c.d_out = a.d_out; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.d_final_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.state_out = a.d_initial_state;
-    c.chunk_states = a.chunk_dstates; c.chunk_T = nullptr;
+    c.chunk_states = a.chunk_dstates; c.chunk_T = const_cast<uint8_t*>(a.chunk_T);
     c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err;
     return launch_chain<true>(c, wait_limit, stream);
 }

@@ -41,6 +41,7 @@ struct BwdChainArgs {
     const int32_t* cu_seqlens;
     const float* d_final_state;   // may be null
     float* chunk_dstates;         // gradient w.r.t. each chunk's end state, tiles as FwdArgs::chunk_states
+    const uint8_t* chunk_T;       // T operand tiles of every chunk (from the forward state pass), or null
     float* d_initial_state;       // may be null
     int N;
     int T;
