@@ -121,7 +121,8 @@ GDN_API size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_
  *   dg (B,T,H) fp32 -- gradient w.r.t. the per-token g (not its cumsum);
  *   dbeta (B,T,H) bf16 -- gradient w.r.t. beta as passed;
  *   d_initial_state (N,H,d_k,d_v) fp32, or NULL (not written).
- * The chunk-start states are recomputed into `workspace`.
+ * The chunk-start states and T tiles are recomputed into `workspace`
+ * (256-byte aligned; contents on entry do not matter).
  * Returns GDN_OK once the work is enqueued on `stream`.
  */
 GDN_API gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,

@@ -57,8 +57,24 @@ long long chunk_slots(int B, int T, int varlen) {
     return static_cast<long long>(B) * ((T + gdn::kChunk - 1) / gdn::kChunk);
 }
 
-// Backward workspace: per-chunk start states and T operand tiles (pass 1),
-// per-chunk end-state gradients (pass 2).
+// Per-chunk T operand tiles (both calls' workspace holds them).
+size_t tiles_bytes(int B, int T, int H, int varlen) {
+    return round_up(static_cast<size_t>(gdn::kChunkTBytes) * chunk_slots(B, T, varlen) * H);
+}
+
+// T = (I + A)^-1 of every chunk into `tiles` (chunk-parallel kernel).
+bool launch_tiles(const gdn_bf16* k, const float* g, const gdn_bf16* beta, const int32_t* cu_seqlens,
+                  uint8_t* tiles, int B, int T, int H, int d_k, int* err, cudaStream_t stream) {
+    gdn::ChunkTArgs t{};
+    t.k = k; t.g = g; t.beta = beta; t.cu_seqlens = cu_seqlens; t.chunk_T = tiles;
+    t.N = B; t.T = T; t.H = H; t.d_k = d_k; t.err = err;
+    t.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
+    if (t.max_chunks == 0) return true;
+    return launched(gdn::launch_chunk_t(t, stream));
+}
+
+// Backward workspace: per-chunk start states (pass 1), per-chunk end-state
+// gradients (pass 2), per-chunk T tiles (the chunk-parallel inverse).
 struct BwdLayout {
     size_t states, dstates, tiles, total;
 };
@@ -70,7 +86,7 @@ BwdLayout bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     L.states = 0;
     L.dstates = round_up(per_state * slots * H);
     L.tiles = L.dstates + round_up(per_state * slots * H);
-    L.total = L.tiles + round_up(static_cast<size_t>(gdn::kChunkTBytes) * slots * H);
+    L.total = L.tiles + tiles_bytes(B, T, H, varlen);
     return L;
 }
 
@@ -107,8 +123,6 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
                          gdn_bf16* out, float* final_state,
                          int B, int T, int H, int d_k, int d_v,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     gdn_status st = check_shapes(B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
     if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
@@ -116,12 +130,16 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
     if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
+    (void)workspace;
+    (void)workspace_bytes;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
+    // the forward forms T inside the chunk chain (its prep warpgroup runs one
+    // chunk ahead); the backward computes all T tiles first, chunk-parallel
     gdn::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens;
-    a.out = out; a.final_state = final_state; a.chunk_states = nullptr;
+    a.out = out; a.final_state = final_state; a.chunk_states = nullptr; a.chunk_T = nullptr;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
     if (!launched(gdn::launch_fwd_ws(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
@@ -157,7 +175,9 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     float* dstates = reinterpret_cast<float*>(ws + L.dstates);
     uint8_t* tiles = reinterpret_cast<uint8_t*>(ws + L.tiles);
 
-    // pass 1: chunk-start states and T tiles (forward state pass, no output)
+    // T tiles of every chunk (chunk-parallel), then pass 1: chunk-start states
+    // (forward state pass, no output)
+    if (L.total > 0 && !launch_tiles(k, g, beta, cu_seqlens, tiles, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
     gdn::FwdArgs f{};
     f.q = q; f.k = k; f.v = v; f.g = g; f.beta = beta; f.scale = scale;
     f.initial_state = initial_state; f.cu_seqlens = cu_seqlens;
@@ -165,7 +185,7 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     f.N = B; f.T = T; f.H = H; f.d_k = d_k; f.d_v = d_v; f.err = err;
     if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
 
-    // pass 2: reverse chain of state gradients (T tiles from pass 1)
+    // pass 2: reverse chain of state gradients
     gdn::BwdChainArgs c{};
     c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
     c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;

@@ -1,0 +1,309 @@
+// T = (I + A)^-1 of every chunk, chunk-parallel: the operand tiles that the
+// chunk-chain kernel and the local-gradient pass read.
+//
+// Per (chunk, head, sequence), with G the running sum of g inside the chunk,
+//   A_ij = beta_i (k_i . k_j) exp(G_i - G_j)  (j < i),   T = (I + A)^-1,
+// the triangular inverse of the chunk algebra behind the WY tensors w and u
+// (fla issue #1550, "Intermediate rounding diagnosis", lists it among the
+// intermediates whose bf16 rounding costs accuracy, so it stays fp32 here
+// until the final hi/lo split).  The decay is masked before the exponential,
+// so every exponent is <= 0.
+//
+// One CTA (128 threads) per chunk: K K^T on the tensor cores (one M = 64
+// product into TMEM), A in fp32 in shared memory, T by a blocked inverse
+// (16x16 diagonal blocks by substitution, then the off-diagonal blocks as
+// products, level by level), and T written to global memory as bf16 hi/lo
+// operand tiles in the 128-byte-swizzled layout, tile row c = column c of T.
+// The work of all chunks runs at once (several CTAs per SM), off the serial
+// chunk chain.
+#include <cuda.h>
+
+#include "gdn_common.cuh"
+#include "gdn_kernels.h"
+#include "gdn_tc_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace gdn {
+
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 64;
+constexpr int kKRegion = 64 * 128;   // 64 key rows x 128 bytes (64 key columns)
+constexpr int kTS = 36;              // row stride of the fp32 32x32 T blocks (rows on distinct banks)
+constexpr int kTB = 32 * kTS;
+
+constexpr int oK = 0;                        // K tile, two 64-column regions
+constexpr int oA = oK + 2 * kKRegion;        // A^T fp32 [64][64]
+constexpr int oTf = oA + 64 * 64 * 4;        // T_00, T_11, T_10 fp32 32x32 blocks
+constexpr int oVec = oTf + 3 * kTB * 4;      // g, beta, G x 64 fp32
+constexpr int oBar = oVec + 3 * 64 * 4;
+constexpr int oMisc = oBar + 8;
+constexpr int kBytes = oMisc + 16;
+constexpr int kAlloc = kBytes + 1024;
+
+// One 8-value piece (row `row`, columns 8 ch ..) of the T hi/lo tiles in global memory.
+__device__ __forceinline__ void put_split_global(uint8_t* tile, int row, int ch, const float* x8) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = x8[2 * e], b = x8[2 * e + 1];
+        hw[e] = cvt_bf16x2(a, b);
+        lw[e] = cvt_bf16x2(a - __uint_as_float(hw[e] << 16), b - __uint_as_float(hw[e] & 0xffff0000u));
+    }
+    const uint32_t off = sw128_offset(row, ch * 16);
+    *reinterpret_cast<uint4*>(tile + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(tile + kTile64 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) gdn_chunk_t_kernel(const ChunkTArgs p) {
+    const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int H = p.H, dk = p.d_k;
+    const int q = threadIdx.x;
+    const int warp = q >> 5, lane = q & 31;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+    const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+    if (ci >= nchunks) return;
+    const int c0 = t0 + ci * kChunk;
+    const int nv = min(kChunk, t1 - c0);
+    const long long row_base = static_cast<long long>(b) * p.T;
+    const long long slot = chunk_slot_base(p.cu_seqlens, n, p.T) + ci;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + smem_align_pad(smem_raw);
+    float* At = reinterpret_cast<float*>(sm + oA);  // A^T, row stride 64
+    float* T00 = reinterpret_cast<float*>(sm + oTf);
+    float* T11 = T00 + kTB;
+    float* T10 = T00 + 2 * kTB;
+    float* gv = reinterpret_cast<float*>(sm + oVec);
+    float* bv = gv + 64;
+    float* Gv = gv + 128;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
+    const uint32_t bar = smem_u32(sm + oBar);
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (q == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    // K tile (rows beyond the chunk and key columns beyond d_k are zero)
+    for (int e = q; e < 2 * 64 * 8; e += kThreads) {
+        const int region = e >> 9, r = (e >> 3) & 63, ch = e & 7;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < nv && region * 64 < dk)
+            val = *reinterpret_cast<const uint4*>(p.k + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                  region * 64 + ch * 8);
+        *reinterpret_cast<uint4*>(sm + oK + region * kKRegion + sw128_offset(r, ch * 16)) = val;
+    }
+    if (q < 64) {
+        const long long idx = (row_base + c0 + q) * H + h;
+        gv[q] = (q < nv) ? p.g[idx] : 0.f;
+        bv[q] = (q < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // K K^T (M = 64): rows 16 w .. 16 w + 15 land in lanes 0-15 of subpartition w
+    if (q == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+        const uint32_t ak = smem_u32(sm + oK);
+#pragma unroll
+        for (int s = 0; s < kDk / 16; ++s) {
+            const uint64_t a = desc_sw128(ak + (s >> 2) * kKRegion + (s & 3) * 32, 0, 1024);
+            mma_bf16(tmem, a, a, id, s > 0);
+        }
+        mma_commit(bar);
+    }
+    // running sum G of g in the chunk
+    if (q < 32) {
+        const float a = gv[2 * q];
+        const float bb = a + gv[2 * q + 1];
+        float s = bb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, s, off);
+            if (q >= off) s += o;
+        }
+        Gv[2 * q] = s - bb + a;
+        Gv[2 * q + 1] = s;
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(bar, 0, kDefaultWaitLimit);
+    tc_fence_after();
+    __syncthreads();
+
+    // A: thread (warp w, lane l) takes row i = 16 w + l % 16, columns 32 (l / 16) .. + 31;
+    // lane l < 16 holds the TMEM row, lane l + 16 takes its upper 32 columns
+    {
+        const int i = 16 * warp + (lane & 15), hf = lane >> 4, j0 = 32 * hf;
+        const float Gi = Gv[i], bi = bv[i];
+        float mdec[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mdec[k] = (j0 + k < i) ? exp_nonpos(Gi - Gv[j0 + k]) : 0.f;
+        const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float lo[32], up[32];
+        tmem_ld16(lb, lo);
+        tmem_ld16(lb + 16, lo + 16);
+        tmem_ld16(lb + 32, up);
+        tmem_ld16(lb + 48, up + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float kk = __shfl_sync(0xffffffffu, up[k], lane & 15);
+            lo[k] = bi * (hf ? kk : lo[k]) * mdec[k];
+        }
+        // stores after the loop: they may alias the decay loads
+#pragma unroll
+        for (int k = 0; k < 32; ++k) At[(j0 + k) * 64 + i] = lo[k];
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // T_bb = (I + A_bb)^-1 for the four 16x16 diagonal blocks: column c of
+    // block d (q < 64) by right-looking forward substitution, x = e_c;
+    // for m: for i > m: x_i -= A_im x_m.  Row m of A^T is read as broadcast
+    // 16-byte loads.
+    if (q < 64) {
+        const int d = q >> 4, c = q & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+        const float* ablk = At + 16 * d * 64 + 16 * d;
+#pragma unroll
+        for (int m = 0; m < 15; ++m) {
+            const float xm = x[m];
+            const float4* arow = reinterpret_cast<const float4*>(ablk + m * 64);
+#pragma unroll
+            for (int i4 = (m + 1) >> 2; i4 < 4; ++i4) {
+                const float4 a4 = arow[i4];
+                if (4 * i4 + 0 > m) x[4 * i4 + 0] = fmaf(-a4.x, xm, x[4 * i4 + 0]);
+                if (4 * i4 + 1 > m) x[4 * i4 + 1] = fmaf(-a4.y, xm, x[4 * i4 + 1]);
+                if (4 * i4 + 2 > m) x[4 * i4 + 2] = fmaf(-a4.z, xm, x[4 * i4 + 2]);
+                if (4 * i4 + 3 > m) x[4 * i4 + 3] = fmaf(-a4.w, xm, x[4 * i4 + 3]);
+            }
+        }
+        // into the 32x32 block T_bb (b = d / 2) at rows/columns 16 (d % 2) ..;
+        // the upper-right 16x16 block of T_bb is zero
+        float* tb = (d >> 1 ? T11 : T00) + (16 * (d & 1)) * (kTS + 1) + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) tb[i * kTS] = x[i];
+        if (!(d & 1)) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tb[i * kTS + 16] = 0.f;
+        }
+    }
+    __syncthreads();
+    {
+        // lower-left 16x16 block of T_bb (b = q / 64): X = A_10 T_00 (16x16
+        // blocks of the 32x32 diagonal block), thread q: row r, columns c4 .. c4 + 3
+        const int bb = q >> 6, r = (q >> 2) & 15, c4 = (q & 3) * 4;
+        float* tb = bb ? T11 : T00;
+        const int o = 32 * bb;  // first row/column of the 32x32 block in A
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float a = At[(o + k) * 64 + o + 16 + r];
+            const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
+            acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
+            acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
+        }
+        float* xs = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
+        *reinterpret_cast<float4*>(xs + r * 64 + c4) = acc;
+        __syncthreads();
+        // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower triangular)
+        acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
+#pragma unroll 4
+        for (int k = 0; k < r; ++k) {
+            const float a = tb[(16 + r) * kTS + 16 + k];
+            const float4 v4 = *reinterpret_cast<const float4*>(xs + k * 64 + c4);
+            acc.x = fmaf(a, v4.x, acc.x); acc.y = fmaf(a, v4.y, acc.y);
+            acc.z = fmaf(a, v4.z, acc.z); acc.w = fmaf(a, v4.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(tb + (16 + r) * kTS + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
+    {
+        // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), thread q:
+        // row r = q / 4, columns c8 .. c8 + 7
+        const int r = q >> 2, c8 = (q & 3) * 8;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float a = At[k * 64 + 32 + r];
+            const float4 t0v = *reinterpret_cast<const float4*>(T00 + k * kTS + c8);
+            const float4 t1v = *reinterpret_cast<const float4*>(T00 + k * kTS + c8 + 4);
+            acc[0] = fmaf(a, t0v.x, acc[0]); acc[1] = fmaf(a, t0v.y, acc[1]);
+            acc[2] = fmaf(a, t0v.z, acc[2]); acc[3] = fmaf(a, t0v.w, acc[3]);
+            acc[4] = fmaf(a, t1v.x, acc[4]); acc[5] = fmaf(a, t1v.y, acc[5]);
+            acc[6] = fmaf(a, t1v.z, acc[6]); acc[7] = fmaf(a, t1v.w, acc[7]);
+        }
+        float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
+        *reinterpret_cast<float4*>(xs + r * 64 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(xs + r * 64 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        __syncthreads();
+        // T_10 = -T_11 X (T_11 unit lower triangular)
+        const float4 u0 = *reinterpret_cast<const float4*>(xs + r * 64 + c8);
+        const float4 u1 = *reinterpret_cast<const float4*>(xs + r * 64 + c8 + 4);
+        acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+        acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+#pragma unroll 4
+        for (int k = 0; k < r; ++k) {
+            const float a = T11[r * kTS + k];
+            const float4 v0 = *reinterpret_cast<const float4*>(xs + k * 64 + c8);
+            const float4 v1 = *reinterpret_cast<const float4*>(xs + k * 64 + c8 + 4);
+            acc[0] = fmaf(a, v0.x, acc[0]); acc[1] = fmaf(a, v0.y, acc[1]);
+            acc[2] = fmaf(a, v0.z, acc[2]); acc[3] = fmaf(a, v0.w, acc[3]);
+            acc[4] = fmaf(a, v1.x, acc[4]); acc[5] = fmaf(a, v1.y, acc[5]);
+            acc[6] = fmaf(a, v1.z, acc[6]); acc[7] = fmaf(a, v1.w, acc[7]);
+        }
+        *reinterpret_cast<float4*>(T10 + r * kTS + c8) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+        *reinterpret_cast<float4*>(T10 + r * kTS + c8 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+    }
+    __syncthreads();
+    {
+        // column col of T = row col of the tile (read MN-major for T, K-major
+        // for T^T); this thread writes entries 32 hf .. 32 hf + 31 of it
+        const int col = q & 63, hf = q >> 6;
+        const float* src = col < 32 ? (hf ? T10 : T00) : (hf ? T11 : nullptr);
+        const int cc = col & 31;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = src ? src[i * kTS + cc] : 0.f;
+        uint8_t* tile = p.chunk_T + (slot * H + h) * static_cast<long long>(kChunkTBytes);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) put_split_global(tile, col, 4 * hf + c4, v + 8 * c4);
+    }
+    if (!ok) {  // the product never signalled: record it and let it land before the TMEM is freed
+        record_error(p.err, kErrTimeout);
+        if (q == 0) mbar_wait(bar, 0, kDefaultWaitLimit);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_t(const ChunkTArgs& a, cudaStream_t stream) {
+    if (a.max_chunks == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.max_chunks, a.H, a.N);
+    gdn_chunk_t_kernel<<<grid, kThreads, kAlloc, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -114,8 +114,7 @@ struct ChainArgs {
     uint16_t* out;                // forward output (may be null)
     float* state_out;             // forward: final state; backward: initial-state gradient (may be null)
     float* chunk_states;          // forward: chunk start states; backward: chunk end-state gradients (may be null)
-    uint8_t* chunk_T;             // T operand tiles of every chunk: written by the forward, read by
-                                  // the backward (may be null: not written / computed in place)
+    const uint8_t* chunk_T;       // T operand tiles of every chunk (may be null: formed in place)
     int N, T, H, d_k, d_v;
     int* err;
 };
@@ -149,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
     const bool want_out = !kBwd && p.out != nullptr;
     // the prep forms P only where the chain uses it (output, or P^T dO), and
-    // the backward takes the T tiles the state pass already wrote
+    // takes the T tiles from the chunk-parallel inverse when they are given
     const bool want_p = kBwd || want_out;
-    const bool load_t = kBwd && p.chunk_T != nullptr;
+    const bool load_t = p.chunk_T != nullptr;
     const uint32_t wl = prm.wait_limit;
     // iteration it works on chunk chunk_of(it): forward in order, backward reversed
     auto chunk_of = [&](int it) { return kBwd ? nchunks - 1 - it : it; };
@@ -988,16 +987,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* t_lo = sm + oT + (slot * 2 + 1) * kTile64;
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(t_hi, t_lo, col, 4 * hf + c4, v + 8 * c4);
-                    if (!kBwd && p.chunk_T && vs == 0) {
-                        // the same operand bytes, for the chunk-parallel gradient pass
-                        uint4* dst = reinterpret_cast<uint4*>(p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64));
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            const uint32_t off = sw128_offset(col, (4 * hf + c4) * 16);
-                            dst[off / 16] = *reinterpret_cast<const uint4*>(t_hi + off);
-                            dst[(kTile64 + off) / 16] = *reinterpret_cast<const uint4*>(t_lo + off);
-                        }
-                    }
                 }
             }
             fence_proxy_async_smem();
@@ -1057,7 +1046,7 @@ cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStr
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = nullptr; c.d_out = a.d_out; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.d_final_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.state_out = a.d_initial_state;
-    c.chunk_states = a.chunk_dstates; c.chunk_T = const_cast<uint8_t*>(a.chunk_T);
+    c.chunk_states = a.chunk_dstates; c.chunk_T = a.chunk_T;
     c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err;
     return launch_chain<true>(c, wait_limit, stream);
 }

@@ -20,7 +20,7 @@ struct FwdArgs {
     float* final_state;     // may be null
     float* chunk_states;    // may be null: per-chunk start states, bf16 hi/lo operand tiles
                             // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v])
-    uint8_t* chunk_T;       // may be null: per-chunk T operand tiles [slot][H][2 x 8 KB]
+    const uint8_t* chunk_T; // may be null: per-chunk T operand tiles [slot][H][2 x 8 KB], read
     int N;                  // sequences (B dense, or cu_seqlens length - 1)
     int T;                  // tokens per batch row (dense) / total tokens (packed)
     int H;
@@ -77,6 +77,23 @@ struct BwdLocalArgs {
     int max_chunks;               // chunks of the longest sequence (grid.x)
     int* err;
 };
+
+// T = (I + A)^-1 of every chunk as bf16 hi/lo operand tiles (chunk-parallel).
+struct ChunkTArgs {
+    const uint16_t* k;
+    const float* g;
+    const uint16_t* beta;
+    const int32_t* cu_seqlens;
+    uint8_t* chunk_T;             // [slot][H][2 x 8 KB]
+    int N;
+    int T;
+    int H;
+    int d_k;
+    int max_chunks;               // chunks of the longest sequence (grid.x)
+    int* err;
+};
+
+cudaError_t launch_chunk_t(const ChunkTArgs& a, cudaStream_t stream);
 
 // Bytes of one chunk's T operand tiles in the backward workspace.
 constexpr int kChunkTBytes = 2 * 64 * 128;
