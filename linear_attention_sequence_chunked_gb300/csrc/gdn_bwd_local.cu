@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     uint32_t phase = 0;
     bool failed = false;  // a bounded wait ran out (reported through the error word)
     auto mma_sync_wait = [&]() {
-        if (tid == 0) mma_commit(bar);
-        __syncwarp();
+        if (warp == 0) {
+            if (elect_one()) mma_commit(bar);
+            __syncwarp();
+        }
         if (!mbar_wait(bar, phase, kDefaultWaitLimit)) failed = true;
         phase ^= 1u;
         tc_fence_after();
@@ -197,11 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     auto t64 = [&](int off) { return smem_u32(sm + off); };
 
     // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
-    if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+    if (warp == 0) {
+        if (elect_one()) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
-        for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
+            for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
+        }
+        __syncwarp();
     }
     mma_sync_wait();
     const int mrow = m64_row(sub, lane);
@@ -294,21 +299,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         __syncthreads();
 
         // ---- batch 1: K S0 -> X1, P^T dO -> X2 ----
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-            constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+                constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
-            for (int s = 0; s < kDk / 16; ++s) {
-                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
-                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
-            }
+                for (int s = 0; s < kDk / 16; ++s) {
+                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
+                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
-                mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
-                mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
+                    mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
+                }
             }
+            __syncwarp();
         }
         mma_sync_wait();
         float ks0[32], pdo[32];
@@ -327,25 +335,28 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         __syncthreads();
 
         // ---- batch 2: K dS -> X1, Delta = T R -> X2 ----
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-            constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
-            for (int s = 0; s < kDk / 16; ++s) {
-                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
-                mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
-            }
+                for (int s = 0; s < kDk / 16; ++s) {
+                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
+                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
-                const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
-                const uint64_t rh = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
-                const uint64_t rl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
-                mma_bf16(tmem + cX2, th, rh, id_t, s > 0);
-                mma_bf16(tmem + cX2, th, rl, id_t, 1);
-                mma_bf16(tmem + cX2, tl, rh, id_t, 1);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
+                    const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
+                    const uint64_t rh = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                    const uint64_t rl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + cX2, th, rh, id_t, s > 0);
+                    mma_bf16(tmem + cX2, th, rl, id_t, 1);
+                    mma_bf16(tmem + cX2, tl, rh, id_t, 1);
+                }
             }
+            __syncwarp();
         }
         mma_sync_wait();
         {
@@ -379,28 +390,31 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         __syncthreads();
 
         // ---- batch 3: dBhat = T^T dDelta -> X1;  dP += dO Delta^T ----
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
-            constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
+                constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
-                const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
-                const uint64_t dh = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
-                const uint64_t dl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
-                mma_bf16(tmem + cX1, th, dh, id_b, s > 0);
-                mma_bf16(tmem + cX1, th, dl, id_b, 1);
-                mma_bf16(tmem + cX1, tl, dh, id_b, 1);
-            }
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
+                    const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
+                    const uint64_t dh = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                    const uint64_t dl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + cX1, th, dh, id_b, s > 0);
+                    mma_bf16(tmem + cX1, th, dl, id_b, 1);
+                    mma_bf16(tmem + cX1, tl, dh, id_b, 1);
+                }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
-                mma_bf16(tmem + cdP, ao, dl, id_p, 1);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                    const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                    const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
+                    mma_bf16(tmem + cdP, ao, dl, id_p, 1);
+                }
             }
+            __syncwarp();
         }
         mma_sync_wait();
         {
@@ -457,39 +471,42 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         __syncthreads();
 
         // ---- batch 4: dA += (-dBhat) Delta^T; U += dO S0^T; dK += (dec o Delta) dS^T + Y S0^T ----
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
-            constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
-            const uint32_t first = vs > 0 ? 1u : 0u;
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
+                constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+                const uint32_t first = vs > 0 ? 1u : 0u;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ch_ = desc_sw128(t64(oRC) + s * 32, 0, 1024);
-                const uint64_t cl_ = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
-                const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                mma_bf16(tmem + cdA, ch_, dh, id_c, (first || s > 0) ? 1u : 0u);
-                mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
-                mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
-                // B = S0 / dS tile read K-major: [N = key row d][K = value column]
-                const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
-                const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
-                const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
-                const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
-                const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                mma_bf16(tmem + cU, ao, sah, id_n, (first || s > 0) ? 1u : 0u);
-                mma_bf16(tmem + cU, ao, sal, id_n, 1);
-                const uint64_t eh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-                const uint64_t el = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-                const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
-                const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
-                mma_bf16(tmem + cdK, eh, sbh, id_n, (first || s > 0) ? 1u : 0u);
-                mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
-                mma_bf16(tmem + cdK, el, sbh, id_n, 1);
-                mma_bf16(tmem + cdK, yh, sah, id_n, 1);
-                mma_bf16(tmem + cdK, yh, sal, id_n, 1);
-                mma_bf16(tmem + cdK, yl, sah, id_n, 1);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ch_ = desc_sw128(t64(oRC) + s * 32, 0, 1024);
+                    const uint64_t cl_ = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
+                    const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                    const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cdA, ch_, dh, id_c, (first || s > 0) ? 1u : 0u);
+                    mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
+                    mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
+                    // B = S0 / dS tile read K-major: [N = key row d][K = value column]
+                    const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
+                    const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
+                    const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
+                    const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
+                    const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cU, ao, sah, id_n, (first || s > 0) ? 1u : 0u);
+                    mma_bf16(tmem + cU, ao, sal, id_n, 1);
+                    const uint64_t eh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                    const uint64_t el = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                    const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
+                    const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cdK, eh, sbh, id_n, (first || s > 0) ? 1u : 0u);
+                    mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
+                    mma_bf16(tmem + cdK, el, sbh, id_n, 1);
+                    mma_bf16(tmem + cdK, yh, sah, id_n, 1);
+                    mma_bf16(tmem + cdK, yh, sal, id_n, 1);
+                    mma_bf16(tmem + cdK, yl, sah, id_n, 1);
+                }
             }
+            __syncwarp();
         }
         if (vs + 1 < nslices) fetch_rows(vs + 1);  // while the batch runs
         mma_sync_wait();
@@ -498,14 +515,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
 
     // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
-    if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+    if (warp == 0) {
+        if (elect_one()) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
-        for (int s = 0; s < kDk / 16; ++s) {
-            mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
-            mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
+            for (int s = 0; s < kDk / 16; ++s) {
+                mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
+                mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
+            }
         }
+        __syncwarp();
     }
     mma_sync_wait();
     float* E = reinterpret_cast<float*>(sm + oE);  // 64 x 65: column-sum terms
@@ -568,29 +588,32 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         colsum[tid] = c;
     }
     // ---- final products: dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
-    if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
-        constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
+    if (warp == 0) {
+        if (elect_one()) {
+            tc_fence_after();
+            constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
+            constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-            const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-            const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-            const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-            mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
-            mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
-            mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
-            mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
-            const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
-            const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
-            const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
-            const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
-            mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
-            mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
-            mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
-            mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
+                mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
+                mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
+                mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
+                const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
+                mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
+                mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
+                mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
+            }
         }
+        __syncwarp();
     }
     mma_sync_wait();
     __syncthreads();
@@ -696,8 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
     if (failed) {
         record_error(p.err, kErrTimeout);
-        if (tid == 0) {  // let every MMA and copy this CTA issued land before it leaves
-            mma_commit(bar);
+        if (warp == 0) {  // let every MMA and copy this CTA issued land before it leaves
+            if (elect_one()) mma_commit(bar);
+            __syncwarp();
+        }
+        if (tid == 0) {
             mbar_wait(bar, phase, kDefaultWaitLimit);
             if (s_out) mbar_wait(sbar, sphase, kDefaultWaitLimit);
         }

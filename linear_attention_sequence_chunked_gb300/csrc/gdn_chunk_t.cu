@@ -114,16 +114,19 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_chunk_t_kernel(const ChunkTAr
     const uint32_t tmem = *tslot;
 
     // K K^T (M = 64): rows 16 w .. 16 w + 15 land in lanes 0-15 of subpartition w
-    if (q == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-        const uint32_t ak = smem_u32(sm + oK);
+    if (warp == 0) {
+        if (elect_one()) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+            const uint32_t ak = smem_u32(sm + oK);
 #pragma unroll
-        for (int s = 0; s < kDk / 16; ++s) {
-            const uint64_t a = desc_sw128(ak + (s >> 2) * kKRegion + (s & 3) * 32, 0, 1024);
-            mma_bf16(tmem, a, a, id, s > 0);
+            for (int s = 0; s < kDk / 16; ++s) {
+                const uint64_t a = desc_sw128(ak + (s >> 2) * kKRegion + (s & 3) * 32, 0, 1024);
+                mma_bf16(tmem, a, a, id, s > 0);
+            }
+            mma_commit(bar);
         }
-        mma_commit(bar);
+        __syncwarp();
     }
     // running sum G of g in the chunk
     if (q < 32) {

@@ -61,6 +61,7 @@ constexpr uint32_t kColD = 192;
 constexpr uint32_t kColPD = 256;
 constexpr uint32_t kColS = 320;
 constexpr uint32_t kColQK = 384;  // prep: Q K^T (K K^T at kColG)
+constexpr uint32_t kColQS2 = 448;  // forward: Q S of odd chunks
 
 constexpr int kRegions = kDk / 64;
 constexpr int kStageBytes = kRegions * kRegionBytes;
@@ -247,21 +248,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool aborted = false;
         if constexpr (!kBwd) {
-            // value row of this slice (row mrow of the chunk), packed bf16; the
-            // next chunk's row is fetched as soon as the current one is consumed
-            uint4 vraw[8];
+            // half a value row of this slice (row hrow of the chunk, columns
+            // 32*hf.. of the slice), packed bf16; the next chunk's half row is
+            // fetched as soon as the current one is consumed
+            const int hrow = m64_half_row(warp, lane), hf = lane >> 4;
+            uint4 vraw[4];
             auto load_v = [&](int cj) {
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
+                for (int ch = 0; ch < 4; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
                 const int cc0 = t0 + cj * kChunk;
-                if (cj < nchunks && mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
+                if (cj < nchunks && hrow < min(kChunk, t1 - cc0)) {
                     const uint4* src = reinterpret_cast<const uint4*>(
-                        p.v + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+                        p.v + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) vraw[ch] = src[ch];
+                    for (int ch = 0; ch < 4; ++ch) vraw[ch] = src[ch];
+                }
+            };
+            // Q S goes to one of two column blocks by chunk parity: the output
+            // of chunk c reads its block while chunk c+1's Q S is computed
+            auto col_qs = [](int cj) { return (cj & 1) ? kColQS2 : kColQS; };
+            // C1 of chunk cj: K S and Q S (thread 0, stage cj full)
+            auto issue_c1 = [&](int cj) {
+                const uint32_t stage_c = smem_u32(sm + oStage + (cj & 1) * kStageBytes);
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    const uint64_t a_k = desc_sw128(stage_c + koff, 0, 1024);
+                    const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                    const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                    mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
+                    mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                }
+                mma_commit(bar(B_KS));
+                if (want_out) {
+                    const uint32_t cq = col_qs(cj);
+#pragma unroll
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                        const uint64_t a_q = desc_sw128(stage_c + koff + 64 * 128, 0, 1024);
+                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                        mma_bf16(tmem + cq, a_q, b_hi, id_s, s > 0);
+                        mma_bf16(tmem + cq, a_q, b_lo, id_s, 1);
+                    }
                 }
             };
             load_v(0);
+            if (nchunks > 0) {
+                if (p.chunk_states && t == 0) store_state_tiles(0);
+                if (warp == 0) {
+                    if (__all_sync(0xffffffffu, mbar_wait(bar(B_FULL0), 0, wl))) {
+                        if (elect_one()) issue_c1(0);
+                        __syncwarp();
+                        tma_done = 1;
+                    } else if (lane == 0) {
+                        *abort_flag = 1;
+                    }
+                }
+            }
             for (int ci = 0; ci < nchunks; ++ci) {
                 const int c0 = t0 + ci * kChunk;
                 const int nv = min(kChunk, t1 - c0);
@@ -273,39 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* gam = vec + 192;
                 const float* dec = vec + 256;
 
-                if (p.chunk_states && t == 0) store_state_tiles(ci);
-                // K/Q tiles of this chunk
-                if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
-                tma_done = ci + 1;
-
-                // ---- C1: K S and Q S ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
-#pragma unroll
-                    for (int s = 0; s < kDk / 16; ++s) {
-                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                        const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
-                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                        mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
-                        mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
-                    }
-                    mma_commit(bar(B_KS));
-                    if (want_out) {
-#pragma unroll
-                        for (int s = 0; s < kDk / 16; ++s) {
-                            const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                            const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
-                            const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                            const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                            mma_bf16(tmem + kColQS, a_q, b_hi, id_s, s > 0);
-                            mma_bf16(tmem + kColQS, a_q, b_lo, id_s, 1);
-                        }
-                    }
-                }
+                // K S and Q S of this chunk were issued at the end of the previous one
                 __syncwarp();
                 bool ok = mbar_wait(bar(B_READY0 + slot), ph2, wl);
                 ok = mbar_wait(bar(B_KS), ph, wl) && ok;
@@ -316,22 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C2: R = beta o (V - gam o (K S)) ----
                 {
-                    float row[64];
-                    ld_row64(tmem, warp, kColKS, row);
-                    if (mrow >= 0) {
-                        const float bj = bv[mrow], gj = gam[mrow];
+                    float row[32];
+                    ld_half32(tmem, warp, kColKS, row);
+                    const float bj = bv[hrow], gj = gam[hrow];
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const int c = ch * 8 + 2 * m;
-                                row[c] = bj * (__uint_as_float(w4[m] << 16) - gj * row[c]);
-                                row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
-                            }
+                        for (int m = 0; m < 4; ++m) {
+                            const int c = ch * 8 + 2 * m;
+                            row[c] = bj * (__uint_as_float(w4[m] << 16) - gj * row[c]);
+                            row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
                         }
-                        store_split_row(Rhi, Rlo, mrow, row);
                     }
+                    store_split_half(Rhi, Rlo, hrow, hf, row);
                 }
                 load_v(ci + 1);
                 fence_proxy_async_smem();
@@ -339,23 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(1);
 
                 // ---- C3: Delta = T R ----
-                if (t == 0) {
-                    tc_fence_after();
-                    // A = T read MN-major from the T^T tile (row j holds column j of T)
-                    constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 64, 64);
-                    const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
-                    const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        // A = T read MN-major from the T^T tile (row j holds column j of T)
+                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 64, 64);
+                        const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                        const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t th = desc_sw128(thi + s * 2048, kTile64, 1024);
-                        const uint64_t tl = desc_sw128(tlo + s * 2048, kTile64, 1024);
-                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColD, th, rh, id, s > 0);
-                        mma_bf16(tmem + kColD, th, rl, id, 1);
-                        mma_bf16(tmem + kColD, tl, rh, id, 1);
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t th = desc_sw128(thi + s * 2048, kTile64, 1024);
+                            const uint64_t tl = desc_sw128(tlo + s * 2048, kTile64, 1024);
+                            const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                            const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColD, th, rh, id, s > 0);
+                            mma_bf16(tmem + kColD, th, rl, id, 1);
+                            mma_bf16(tmem + kColD, tl, rh, id, 1);
+                        }
+                        mma_commit(bar(B_D));
                     }
-                    mma_commit(bar(B_D));
+                    __syncwarp();
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
@@ -365,47 +380,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C4: Delta tiles and dec o Delta tiles ----
                 {
-                    float row[64];
-                    ld_row64(tmem, warp, kColD, row);
-                    if (mrow >= 0) {
-                        store_split_row(Dhi, Dlo, mrow, row);
-                        const float dj = dec[mrow];
+                    float row[32];
+                    ld_half32(tmem, warp, kColD, row);
+                    store_split_half(Dhi, Dlo, hrow, hf, row);
+                    const float dj = dec[hrow];
 #pragma unroll
-                        for (int c = 0; c < kVs; ++c) row[c] *= dj;
-                        store_split_row(Rhi, Rlo, mrow, row);
-                    }
+                    for (int c = 0; c < 32; ++c) row[c] *= dj;
+                    store_split_half(Rhi, Rlo, hrow, hf, row);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar(1);
 
                 // ---- C5: S update and P Delta ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
-                    constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
-                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColS, ak, rh, id_s, s > 0);
-                        mma_bf16(tmem + kColS, ak, rl, id_s, 1);
-                    }
-                    mma_commit(bar(B_S));
-                    if (want_out) {
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
+                        constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
-                            const uint64_t ph_ = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 32, 0, 1024);
-                            const uint64_t pl_ = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 32, 0, 1024);
-                            const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                            const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
-                            mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
-                            mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                            const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
+                            const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                            const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColS, ak, rh, id_s, s > 0);
+                            mma_bf16(tmem + kColS, ak, rl, id_s, 1);
                         }
+                        mma_commit(bar(B_S));
+                        if (want_out) {
+#pragma unroll
+                            for (int s = 0; s < 4; ++s) {
+                                const uint64_t ph_ = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 32, 0, 1024);
+                                const uint64_t pl_ = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 32, 0, 1024);
+                                const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                                const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                                mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
+                                mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
+                                mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                            }
+                        }
+                        mma_commit(bar(B_PD));
                     }
-                    mma_commit(bar(B_PD));
+                    __syncwarp();
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
@@ -432,39 +448,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
                     store_split_row(Shi, Slo, t, S);
                 }
-                if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
-                tc_fence_after();
+                fence_proxy_async_smem();
+                tc_fence_before();
                 named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
-                // ---- output ----
-                if (want_out) {
-                    const bool mine = mrow >= 0 && mrow < nv;
-                    const float gi = mine ? gam[mrow] : 0.f;
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        p.out + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs);
-                    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-#pragma unroll
-                    for (int q16 = 0; q16 < 4; ++q16) {
-                        float qs[16], pd[16];
-                        tmem_ld16(tmem + lane_base + kColQS + q16 * 16, qs);
-                        tmem_ld16(tmem + lane_base + kColPD + q16 * 16, pd);
-                        tmem_ld_wait();
-                        if (mine) {
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                uint32_t w4[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int c = half * 8 + 2 * e;
-                                    w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]),
-                                                        scale * fmaf(gi, qs[c + 1], pd[c + 1]));
-                                }
-                                dst[q16 * 2 + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                            }
+                // ---- next chunk's C1, issued ahead of this chunk's output ----
+                if (ci + 1 < nchunks) {
+                    if (p.chunk_states && t == 0) store_state_tiles(ci + 1);
+                    if (warp == 0) {
+                        if (__all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + ((ci + 1) & 1)), ((ci + 1) >> 1) & 1, wl))) {
+                            if (elect_one()) issue_c1(ci + 1);
+                            __syncwarp();
+                            tma_done = ci + 2;
+                        } else if (lane == 0) {
+                            *abort_flag = 1;
                         }
                     }
                 }
-                fence_proxy_async_smem();
+                __syncwarp();
+                if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
+                tc_fence_after();
+                // ---- output ----
+                if (want_out) {
+                    const bool mine = hrow < nv;
+                    const float gi = gam[hrow];
+                    float qs[32], pd[32];
+                    ld_half32_nowait(tmem, warp, col_qs(ci), qs);
+                    ld_half32_nowait(tmem, warp, kColPD, pd);
+                    tmem_ld_wait();
+                    if (mine) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            p.out + ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = j * 8 + 2 * e;
+                                w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]), scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                            }
+                            dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
                 tc_fence_before();
                 named_bar(1);
                 if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
@@ -514,19 +539,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_done = it + 1;
 
                 // ---- C1: K dS (stage and dS tiles only) ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
 #pragma unroll
-                    for (int s = 0; s < kDk / 16; ++s) {
-                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                        const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
-                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                        mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
-                        mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                        for (int s = 0; s < kDk / 16; ++s) {
+                            const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                            const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                            const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                            const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                            mma_bf16(tmem + kColKS, a_k, b_hi, id_s, s > 0);
+                            mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
+                        }
+                        mma_commit(bar(B_KS));
                     }
-                    mma_commit(bar(B_KS));
+                    __syncwarp();
                 }
                 __syncwarp();
                 // gates, T and P of this chunk from the prep warpgroup
@@ -535,18 +563,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) { aborted = true; break; }
 
                 // ---- P^T dO (A = P tile read MN-major) ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t p_hi = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 2048, kTile64, 1024);
-                        const uint64_t p_lo = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 2048, kTile64, 1024);
-                        const uint64_t b_o = desc_sw128(smem_u32(dOt) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
-                        mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t p_hi = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 2048, kTile64, 1024);
+                            const uint64_t p_lo = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 2048, kTile64, 1024);
+                            const uint64_t b_o = desc_sw128(smem_u32(dOt) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
+                            mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
+                        }
+                        mma_commit(bar(B_PD));
                     }
-                    mma_commit(bar(B_PD));
+                    __syncwarp();
                 }
                 // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
                 if (mrow >= 0) {
@@ -590,22 +621,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(1);
 
                 // ---- C3: dBhat = T^T dDelta (A = T tile read K-major) ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64);
-                    const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
-                    const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64);
+                        const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                        const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t th = desc_sw128(thi + s * 32, 0, 1024);
-                        const uint64_t tl = desc_sw128(tlo + s * 32, 0, 1024);
-                        const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                        const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColD, th, rh, id, s > 0);
-                        mma_bf16(tmem + kColD, th, rl, id, 1);
-                        mma_bf16(tmem + kColD, tl, rh, id, 1);
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t th = desc_sw128(thi + s * 32, 0, 1024);
+                            const uint64_t tl = desc_sw128(tlo + s * 32, 0, 1024);
+                            const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                            const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColD, th, rh, id, s > 0);
+                            mma_bf16(tmem + kColD, th, rl, id, 1);
+                            mma_bf16(tmem + kColD, tl, rh, id, 1);
+                        }
+                        mma_commit(bar(B_D));
                     }
-                    mma_commit(bar(B_D));
+                    __syncwarp();
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
@@ -629,23 +663,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(1);
 
                 // ---- C5: K^T X + Q^T G (A = K^T, Q^T read MN-major from the stage) ----
-                if (t == 0) {
-                    tc_fence_after();
-                    constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
-                        const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
-                        const uint64_t xh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                        const uint64_t xl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                        const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                        const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                        mma_bf16(tmem + kColS, ak, xh, id, s > 0);
-                        mma_bf16(tmem + kColS, ak, xl, id, 1);
-                        mma_bf16(tmem + kColS, aq, gh, id, 1);
-                        mma_bf16(tmem + kColS, aq, gl, id, 1);
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
+                            const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
+                            const uint64_t xh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                            const uint64_t xl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                            const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                            const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColS, ak, xh, id, s > 0);
+                            mma_bf16(tmem + kColS, ak, xl, id, 1);
+                            mma_bf16(tmem + kColS, aq, gh, id, 1);
+                            mma_bf16(tmem + kColS, aq, gl, id, 1);
+                        }
+                        mma_commit(bar(B_S));
                     }
-                    mma_commit(bar(B_S));
+                    __syncwarp();
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
@@ -681,9 +718,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.chunk_states && t == 0) bulk_wait_all();
         if (aborted) {
+            if (warp == 0) {
+                if (elect_one()) mma_commit(bar(B_DRAIN0));
+                __syncwarp();
+            }
             if (t == 0) {
                 record_error(p.err, kErrTimeout);
-                mma_commit(bar(B_DRAIN0));
                 mbar_wait(bar(B_DRAIN0), 0, wl);
                 for (int ci = tma_done; ci < tma_issued; ++ci)
                     mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
@@ -761,19 +801,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // gram K K^T and Q K^T (two M = 64 products), running while the
             // gates are formed
-            if (q == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
-                const uint32_t stage_a = smem_u32(stage);
+            if (warp == 4) {
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
+                    const uint32_t stage_a = smem_u32(stage);
 #pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                    const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
-                    const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
-                    if (!load_t) mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
-                    if (want_p) mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                        const uint64_t a_k = desc_sw128(stage_a + koff, 0, 1024);
+                        const uint64_t a_q = desc_sw128(stage_a + koff + 64 * 128, 0, 1024);
+                        if (!load_t) mma_bf16(tmem + kColG, a_k, a_k, id_g, s > 0);
+                        if (want_p) mma_bf16(tmem + kColQK, a_q, a_k, id_g, s > 0);
+                    }
+                    mma_commit(bar(B_GRAM));
                 }
-                mma_commit(bar(B_GRAM));
+                __syncwarp();
             }
 
             // gates of this chunk into its slot (free once the chain finished iteration it - 2)
@@ -783,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar(2);
             if (*abort_flag) { aborted = true; break; }
             if (load_t && q == 0) {
-                // T tiles of this chunk (written by the forward state pass) into the free slot
+                // T tiles of this chunk (from the chunk-parallel inverse) into the free slot
                 mbar_arrive_expect_tx(bar(B_TCOPY), 2 * kTile64);
                 bulk_g2s(smem_u32(sm + oT + (slot * 2) * kTile64),
                          p.chunk_T + ((slot0 + ci) * H + h) * (2LL * kTile64), 2 * kTile64, bar(B_TCOPY));
@@ -1001,10 +1044,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (q == 0 && tcopy_out) mbar_wait(bar(B_TCOPY), tcopy_it & 1, wl);  // no copy outlives the CTA
-        if (aborted && q == 0) {
-            record_error(p.err, kErrTimeout);
-            mma_commit(bar(B_DRAIN1));
-            mbar_wait(bar(B_DRAIN1), 0, wl);
+        if (aborted) {
+            if (warp == 4) {
+                if (elect_one()) mma_commit(bar(B_DRAIN1));
+                __syncwarp();
+            }
+            if (q == 0) {
+                record_error(p.err, kErrTimeout);
+                mbar_wait(bar(B_DRAIN1), 0, wl);
+            }
         }
     }
     tc_fence_before();

@@ -76,6 +76,13 @@ __device__ __forceinline__ void store_split_chunk(uint8_t* tile_hi, uint8_t* til
     *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Half a split row: 32 values, columns 32*hf .. 32*hf+31.
+__device__ __forceinline__ void store_split_half(uint8_t* tile_hi, uint8_t* tile_lo, int row, int hf,
+                                                 const float* x) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) store_split_chunk(tile_hi, tile_lo, row, 4 * hf + ch, x + 8 * ch);
+}
+
 // Rows of M = 64 accumulators (cta_group::1): rows 16w..16w+15 sit in lanes
 // 32w..32w+15 of TMEM subpartition w; lanes 16..31 are unused.
 __device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
@@ -87,6 +94,17 @@ __device__ __forceinline__ void ld_row64(uint32_t tmem, int sub, uint32_t col, f
     tmem_ld16(a + 16, v + 16);
     tmem_ld16(a + 32, v + 32);
     tmem_ld16(a + 48, v + 48);
+    tmem_ld_wait();
+}
+
+// Half rows of M = 64 accumulators, every lane busy: lane l of warp w holds
+// row 16w + (l & 15), columns 32*(l >> 4) .. +31 (no wait).
+__device__ __forceinline__ int m64_half_row(int warp, int lane) { return warp * 16 + (lane & 15); }
+__device__ __forceinline__ void ld_half32_nowait(uint32_t tmem, int sub, uint32_t col, float* v) {
+    tmem_ld_pair32(tmem + (static_cast<uint32_t>(sub * 32) << 16) + col, v);
+}
+__device__ __forceinline__ void ld_half32(uint32_t tmem, int sub, uint32_t col, float* v) {
+    ld_half32_nowait(tmem, sub, col, v);
     tmem_ld_wait();
 }
 
