@@ -16,7 +16,9 @@
 // tensor memory across 64-column value slices, so each CTA writes complete
 // gradients: no partial sums leave the chip.  One CTA (256 threads) per
 // (chunk, head, sequence); warps w and w + 4 share a TMEM subpartition and
-// split the 64 columns of each accumulator row between them.  Computed MMA
+// split the 64 columns of each accumulator row between them, and within a
+// warp lanes l and l + 16 take 16 columns each of row 16 w + l (tcgen05.ld
+// 16x32bx2), so every lane works in each epilogue.  Computed MMA
 // operands are split into bf16 hi + lo, accumulation is fp32.
 #include <cuda.h>
 
@@ -209,12 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         __syncwarp();
     }
     mma_sync_wait();
-    const int mrow = m64_row(sub, lane);
+    // accumulator row of this lane and its 16 columns cb .. cb + 15 of a
+    // 64-column block; lanes 0-15 hold the per-row sums after the pair join
+    const int mrow = m64_half_row(sub, lane);
+    const int cb = col0 + 16 * (lane >> 4);
+    const bool lead = lane < 16;
     const uint32_t lb = static_cast<uint32_t>(sub * 32) << 16;
     // the dO tile and the value row of slice vs, fetched into registers one
     // slice ahead: two 16-byte pieces of the dO tile per thread, and columns
-    // col0 .. col0 + 31 of value row mrow
-    uint4 do_raw[2], v_raw[4];
+    // cb .. cb + 15 of value row mrow
+    uint4 do_raw[2], v_raw[2];
     auto fetch_rows = [&](int vs) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -224,32 +230,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 do_raw[k] = *reinterpret_cast<const uint4*>(
                     p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
         }
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) v_raw[ch] = make_uint4(0, 0, 0, 0);
-        if (mrow >= 0 && mrow < nv) {
+        v_raw[0] = v_raw[1] = make_uint4(0, 0, 0, 0);
+        if (mrow < nv) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) v_raw[ch] = src[ch];
+                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
+            v_raw[0] = src[0];
+            v_raw[1] = src[1];
         }
     };
     fetch_rows(0);
-    // 32 columns (col0 ..) of accumulator row mrow
-    auto ld_half = [&](uint32_t col, float* v) {
-        tmem_ld16(tmem + lb + col + col0, v);
-        tmem_ld16(tmem + lb + col + col0 + 16, v + 16);
-        tmem_ld_wait();
+    // columns cb .. cb + 15 of accumulator row mrow (no wait)
+    auto ld_cols = [&](uint32_t col, float* v) { tmem_ld_pair16(tmem + lb + col + col0, v); };
+    // the two 16-byte chunks of columns cb .. cb + 15 of a split row
+    auto store_cols = [&](int off, int row, const float* x) {
+        store_split_chunk(sm + off, sm + off + kTile64, row, cb >> 3, x);
+        store_split_chunk(sm + off, sm + off + kTile64, row, (cb >> 3) + 1, x + 8);
     };
     {
-        float row[32];
-        ld_half(cX1, row);
-        if (mrow >= 0) {
-            const float Gi = Gv[mrow];
+        float row[16];
+        ld_cols(cX1, row);
+        tmem_ld_wait();
+        const float Gi = Gv[mrow];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) row[k] = (col0 + k <= mrow) ? row[k] * exp_nonpos(Gi - Gv[col0 + k]) : 0.f;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(sm + oP, sm + oP + kTile64, mrow, 4 * hc + c4, row + 8 * c4);
-        }
+        for (int k = 0; k < 16; ++k) row[k] = (cb + k <= mrow) ? row[k] * exp_nonpos(Gi - Gv[cb + k]) : 0.f;
+        store_cols(oP, mrow, row);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -290,10 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
             const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
             *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[k];
         }
-        // columns col0 .. col0 + 31 of value row mrow
-        float vrow[32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) unpack8(v_raw[ch], vrow + ch * 8);
+        // columns cb .. cb + 15 of value row mrow
+        float vrow[16];
+        unpack8(v_raw[0], vrow);
+        unpack8(v_raw[1], vrow + 8);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -319,16 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
             __syncwarp();
         }
         mma_sync_wait();
-        float ks0[32], pdo[32];
-        ld_half(cX1, ks0);
-        ld_half(cX2, pdo);
-        if (mrow >= 0) {
-            float row[32];
+        float ks0[16], pdo[16];
+        ld_cols(cX1, ks0);
+        ld_cols(cX2, pdo);
+        tmem_ld_wait();
+        {
+            float row[16];
             const float bj = bv[mrow], gj = gam[mrow];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, 4 * hc + c4, row + 8 * c4);
+            for (int c = 0; c < 16; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
+            store_cols(oRA, mrow, row);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -362,27 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         {
             // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
             // dd = dec * sum_v (K dS) Delta for the decay term of dG
-            const float dj = (mrow >= 0) ? dec[mrow] : 0.f;
+            const float dj = dec[mrow];
             float dd = 0.f;
+            float kds[16], dl[16];
+            ld_cols(cX1, kds);
+            ld_cols(cX2, dl);
+            tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float kds[16], dl[16];
-                tmem_ld16(tmem + lb + cX1 + col0 + g * 16, kds);
-                tmem_ld16(tmem + lb + cX2 + col0 + g * 16, dl);
-                tmem_ld_wait();
-                if (mrow >= 0) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        dd = fmaf(kds[c], dl[c], dd);
-                        kds[c] = fmaf(scale, pdo[g * 16 + c], dj * kds[c]);
-                    }
-                    const int ch = 4 * hc + 2 * g;
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch, kds);
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch + 1, kds + 8);
-                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, ch, dl);
-                    store_split_chunk(sm + oRA, sm + oRA + kTile64, mrow, ch + 1, dl + 8);
-                }
+            for (int c = 0; c < 16; ++c) {
+                dd = fmaf(kds[c], dl[c], dd);
+                kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
             }
+            store_cols(oRB, mrow, kds);
+            store_cols(oRA, mrow, dl);
             acc_dd = fmaf(dj, dd, acc_dd);
         }
         fence_proxy_async_smem();
@@ -420,49 +416,38 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         {
             // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RC, Y -> RD,
             // dec o Delta (Delta re-read from X2) -> RB
-            const bool mine = mrow >= 0;
-            const float bi = mine ? bv[mrow] : 0.f, gi = mine ? gam[mrow] : 0.f, dj = mine ? dec[mrow] : 0.f;
+            const float bi = bv[mrow], gi = gam[mrow], dj = dec[mrow];
             float sv = 0.f, sk = 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(
-                p.dv + ((row_base + c0 + (mine ? mrow : 0)) * H + h) * static_cast<long long>(V) + vs * kVs + col0);
+            float db[16], dl[16], t16[16];
+            ld_cols(cX1, db);
+            ld_cols(cX2, dl);
+            tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float db[16], dl[16];
-                tmem_ld16(tmem + lb + cX1 + col0 + g * 16, db);
-                tmem_ld16(tmem + lb + cX2 + col0 + g * 16, dl);
-                tmem_ld_wait();
-                if (mine) {
-                    float t16[16];
+            for (int c = 0; c < 16; ++c) {
+                sv = fmaf(vrow[c], db[c], sv);
+                sk = fmaf(ks0[c], db[c], sk);
+            }
+            if (mrow < nv) {
+                uint4* dst = reinterpret_cast<uint4*>(
+                    p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        sv = fmaf(vrow[g * 16 + c], db[c], sv);
-                        sk = fmaf(ks0[g * 16 + c], db[c], sk);
-                    }
-                    if (mrow < nv) {
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t w4[4];
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
-                            dst[2 * g + half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                    }
-                    const int ch = 4 * hc + 2 * g;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) t16[c] = -db[c];
-                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, ch, t16);
-                    store_split_chunk(sm + oRC, sm + oRC + kTile64, mrow, ch + 1, t16 + 8);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
-                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, ch, t16);
-                    store_split_chunk(sm + oRD, sm + oRD + kTile64, mrow, ch + 1, t16 + 8);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) t16[c] = dj * dl[c];
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch, t16);
-                    store_split_chunk(sm + oRB, sm + oRB + kTile64, mrow, ch + 1, t16 + 8);
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
+                    dst[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) t16[c] = -db[c];
+            store_cols(oRC, mrow, t16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
+            store_cols(oRD, mrow, t16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) t16[c] = dj * dl[c];
+            store_cols(oRB, mrow, t16);
             acc_dbeta += sv - gi * sk;
             acc_dgam -= bi * sk;
         }
@@ -531,19 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     float* E = reinterpret_cast<float*>(sm + oE);  // 64 x 65: column-sum terms
     float rowsum = 0.f, dbeta_a = 0.f;
     {
-        const bool mine = mrow >= 0;
-        const int i = mine ? mrow : 0;
+        const int i = mrow;
         const float Gi = Gv[i], bi = bv[i];
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        {
             float kk[16], da[16], qk[16], dp[16];
-            const uint32_t col = col0 + g * 16;
-            tmem_ld16(tmem + lb + cX1 + col, kk);
-            tmem_ld16(tmem + lb + cdA + col, da);
-            tmem_ld16(tmem + lb + cX2 + col, qk);
-            tmem_ld16(tmem + lb + cdP + col, dp);
+            const int col = cb;
+            ld_cols(cX1, kk);
+            ld_cols(cdA, da);
+            ld_cols(cX2, qk);
+            ld_cols(cdP, dp);
             tmem_ld_wait();
-            if (mine) {
+            {
                 float dkk[16], dqk[16], e16[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -564,11 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 // stores after the loop: they may alias the decay loads
 #pragma unroll
                 for (int c = 0; c < 16; ++c) E[i * 65 + col + c] = e16[c];
-                const int ch = 4 * hc + 2 * g;
-                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, ch, dkk);
-                store_split_chunk(sm + oRA, sm + oRA + kTile64, i, ch + 1, dkk + 8);
-                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, ch, dqk);
-                store_split_chunk(sm + oRB, sm + oRB + kTile64, i, ch + 1, dqk + 8);
+                store_cols(oRA, i, dkk);
+                store_cols(oRB, i, dqk);
             }
         }
     }
@@ -617,21 +597,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     }
     mma_sync_wait();
     __syncthreads();
-    // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63) ----
+    // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63: 16-column
+    // groups 4 hc + 2 r + lane / 16 of this lane) ----
     float dG = 0.f, dbeta = 0.f;
     {
-        const bool mine = mrow >= 0;
-        const int i = mine ? mrow : 0;
+        const int i = mrow;
         const float gi = gam[i];
         // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
         float dgq = 0.f;
-        for (int c16 = 4 * hc; c16 < 4 * hc + 4; ++c16) {
+#pragma unroll 1
+        for (int r = 0; r < 2; ++r) {
+            const int c16 = 4 * hc + 2 * r + (lane >> 4);
+            const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
             float u[16], q2[16], kk2[16];
-            tmem_ld16(tmem + lb + cU + c16 * 16, u);
-            tmem_ld16(tmem + lb + cX1 + c16 * 16, q2);
-            tmem_ld16(tmem + lb + cdK + c16 * 16, kk2);
+            tmem_ld_pair16(tmem + lb + cU + cpair, u);
+            tmem_ld_pair16(tmem + lb + cX1 + cpair, q2);
+            tmem_ld_pair16(tmem + lb + cdK + cpair, kk2);
             tmem_ld_wait();
-            if (!mine) continue;
             const int region = c16 >> 2, cc = (c16 & 3) * 16;
             float qrow[16];
             {
@@ -658,24 +640,31 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 }
             }
         }
+        // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
+        {
+            float v = acc_dd;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) red[8 + warp] = v;
+        }
+        // lanes l and l + 16 hold the two column quarters of row i
+        acc_dbeta += __shfl_xor_sync(0xffffffffu, acc_dbeta, 16);
+        acc_dgam += __shfl_xor_sync(0xffffffffu, acc_dgam, 16);
+        dgq += __shfl_xor_sync(0xffffffffu, dgq, 16);
+        acc_dd += __shfl_xor_sync(0xffffffffu, acc_dd, 16);
+        rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
+        dbeta_a += __shfl_xor_sync(0xffffffffu, dbeta_a, 16);
         // the row terms of the upper column half join those of the lower half
         float* part = reinterpret_cast<float*>(sm + oPart) + i * 8;
-        if (mine && hc == 1) {
+        if (lead && hc == 1) {
             part[0] = acc_dbeta;
             part[1] = acc_dgam + dgq;
             part[2] = acc_dd;
             part[3] = rowsum;
             part[4] = dbeta_a;
         }
-        // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
-        {
-            float v = mine ? acc_dd : 0.f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[8 + warp] = v;
-        }
         __syncthreads();
-        if (mine && hc == 0) {
+        if (lead && hc == 0) {
             float dgam = acc_dgam + dgq + part[1];
             float sdd = 0.f;
             if (i == 63) {
@@ -690,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         }
     }
     __syncthreads();
-    if (mrow >= 0 && hc == 0) {
+    if (lead && hc == 0) {
         colsum[mrow] = dG;  // reuse as dG vector
         bv[mrow] = dbeta;   // reuse as dbeta vector
     }

@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         // ======================= chain warpgroup =======================
         const int t = tid;
-        const int mrow = m64_row(warp, lane);
         const int srow = t < dk ? t : -1;
         const long long KV = static_cast<long long>(dk) * V;
         const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
@@ -496,19 +495,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) { aborted = true; break; }
             }
         } else {
-            // dO row of this slice (row mrow of the chunk), packed bf16; the
-            // next chunk's row is fetched as soon as the current one is consumed
-            uint4 oraw[8];
+            // half a dO row of this slice (row hrow of the chunk, columns
+            // 32*hf.. of the slice), packed bf16; the next chunk's half row is
+            // fetched as soon as the current one is consumed
+            const int hrow = m64_half_row(warp, lane), hf = lane >> 4;
+            uint4 oraw[4];
             auto load_do = [&](int it) {
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) oraw[ch] = make_uint4(0, 0, 0, 0);
+                for (int ch = 0; ch < 4; ++ch) oraw[ch] = make_uint4(0, 0, 0, 0);
                 if (it >= nchunks) return;
                 const int cc0 = t0 + chunk_of(it) * kChunk;
-                if (mrow >= 0 && mrow < min(kChunk, t1 - cc0)) {
+                if (hrow < min(kChunk, t1 - cc0)) {
                     const uint4* src = reinterpret_cast<const uint4*>(
-                        p.d_out + ((row_base + cc0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs);
+                        p.d_out + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) oraw[ch] = src[ch];
+                    for (int ch = 0; ch < 4; ++ch) oraw[ch] = src[ch];
                 }
             };
             load_do(0);
@@ -526,11 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // gradient w.r.t. this chunk's end state, for the chunk-parallel pass
                 if (p.chunk_states && t == 0) store_state_tiles(ci);
                 // dO tile (single buffer: the previous chunk's P^T dO has completed)
-                if (mrow >= 0) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(dOt + sw128_offset(mrow, ch * 16)) = oraw[ch];
-                }
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4*>(dOt + sw128_offset(hrow, (4 * hf + ch) * 16)) = oraw[ch];
                 fence_proxy_async_smem();
                 // K/Q tiles of this chunk
                 if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
@@ -580,14 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
                 // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
-                if (mrow >= 0) {
-                    float row[64];
-                    const float gi = scale * gam[mrow];  // dO rows beyond the chunk are zero
+                {
+                    float row[32];
+                    const float gi = scale * gam[hrow];  // dO rows beyond the chunk are zero
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) unpack8(oraw[ch], row + ch * 8);
+                    for (int ch = 0; ch < 4; ++ch) unpack8(oraw[ch], row + ch * 8);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) row[c] *= gi;
-                    store_split_row(Dhi, Dlo, mrow, row);
+                    for (int c = 0; c < 32; ++c) row[c] *= gi;
+                    store_split_half(Dhi, Dlo, hrow, hf, row);
                 }
                 load_do(it + 1);
                 __syncwarp();
@@ -600,21 +599,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
-                    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-                    const float dj = (mrow >= 0) ? dec[mrow] : 0.f;
+                    const float dj = dec[hrow];
+                    float kds[32], pdo[32];
+                    ld_half32_nowait(tmem, warp, kColKS, kds);
+                    ld_half32_nowait(tmem, warp, kColQS, pdo);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) {
-                        float kds[16], pdo[16];
-                        tmem_ld16(tmem + lane_base + kColKS + g4 * 16, kds);
-                        tmem_ld16(tmem + lane_base + kColQS + g4 * 16, pdo);
-                        tmem_ld_wait();
-                        if (mrow >= 0) {
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
-                            store_split_chunk(Rhi, Rlo, mrow, 2 * g4, kds);
-                            store_split_chunk(Rhi, Rlo, mrow, 2 * g4 + 1, kds + 8);
-                        }
-                    }
+                    for (int c = 0; c < 32; ++c) kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
+                    store_split_half(Rhi, Rlo, hrow, hf, kds);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -649,14 +641,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C4: X = -beta gam o dBhat -> R tiles (dDelta consumed) ----
                 {
-                    float row[64];
-                    ld_row64(tmem, warp, kColD, row);
-                    if (mrow >= 0) {
-                        const float f = -bv[mrow] * gam[mrow];
+                    float row[32];
+                    ld_half32(tmem, warp, kColD, row);
+                    const float f = -bv[hrow] * gam[hrow];
 #pragma unroll
-                        for (int c = 0; c < kVs; ++c) row[c] *= f;
-                        store_split_row(Rhi, Rlo, mrow, row);
-                    }
+                    for (int c = 0; c < 32; ++c) row[c] *= f;
+                    store_split_half(Rhi, Rlo, hrow, hf, row);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
