@@ -14,13 +14,22 @@
 //   dbeta, dgam, dG (decays), dg = reverse running sum of dG in the chunk.
 // Sums over value columns (dP, dA, dO S0^T, the S-terms of dK) accumulate in
 // tensor memory across 64-column value slices, so each CTA writes complete
-// gradients: no partial sums leave the chip.  One CTA (256 threads) per
-// (chunk, head, sequence); warps w and w + 4 share a TMEM subpartition and
+// gradients: no partial sums leave the chip.
+//
+// Persistent CTAs (one per SM, 256 threads) walk the (chunk, head, sequence)
+// items with a grid stride.  While one item's chunk-wide products run, the
+// next item's K/Q tiles (TMA), T tiles and first state tiles (bulk copies)
+// land in buffers the current item no longer reads: the K/Q tiles alternate
+// between two buffers, the other one holding the current item's -dBhat-side
+// tiles.  Within an item the dS tiles of the next value slice load as soon as
+// the products that read this slice's dS have completed.  Warps w and w + 4
+// share a TMEM subpartition and
 // split the 64 columns of each accumulator row between them, and within a
 // warp lanes l and l + 16 take 16 columns each of row 16 w + l (tcgen05.ld
 // 16x32bx2), so every lane works in each epilogue.  Computed MMA
 // operands are split into bf16 hi + lo, accumulation is fp32.
 #include <cuda.h>
+#include <string.h>
 
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
@@ -48,43 +57,43 @@ constexpr uint32_t cX1 = 384;   // scratch (M = 64)
 constexpr uint32_t cX2 = 448;   // scratch (M = 64)
 
 // shared memory (1024-aligned tiles)
-constexpr int oKQ = 0;                          // [K;Q] regions, 2 x 16 KB
-constexpr int oT = oKQ + 2 * kRegionBytes;      // T^T-layout tiles hi, lo
-constexpr int oP = oT + 2 * kTile64;            // P tiles hi, lo [i][j]
+constexpr int oKQ0 = 0;                         // [K;Q] regions of even items, 2 x 16 KB
+constexpr int oT = oKQ0 + 2 * kRegionBytes;     // T^T-layout tiles hi, lo
+constexpr int oP = oT + 2 * kTile64;            // P tiles hi, lo [i][j]; later the E scratch
 constexpr int oSA = oP + 2 * kTile64;           // S0 tiles hi, lo [d][v]
 constexpr int oSB = oSA + 2 * kTileS;           // dS tiles hi, lo [d][v]
 constexpr int oDO = oSB + 2 * kTileS;           // dO raw [i][v]
 constexpr int oRA = oDO + kTile64;              // R -> Delta (hi, lo) [j][v]; later dKK [i][j]
-constexpr int oRB = oRA + 2 * kTile64;          // dDelta -> dec o Delta; later dQK [i][j]
-constexpr int oRC = oRB + 2 * kTile64;          // -dBhat [i][v]
-constexpr int oRD = oRC + 2 * kTile64;          // Y = -beta gam dBhat [i][v]
-constexpr int oVec = oRD + 2 * kTile64;         // g, beta, G, gam, dec, colsum
+constexpr int oRB = oRA + 2 * kTile64;          // dDelta -> -dBhat; later dQK [i][j]
+constexpr int oKQ1 = oRB + 2 * kTile64;         // [K;Q] of odd items; the other item's RC, RD tiles
+constexpr int oVec = oKQ1 + 2 * kRegionBytes;   // g, beta, G, gam, dec, colsum
 constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
 constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half
-constexpr int oBar = oPart + 64 * 8 * 4;         // MMA completion, state tiles landed
-constexpr int oMisc = oBar + 16;
+constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles
+constexpr int oMisc = oBar + 32;                // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 232448, "shared memory");
-constexpr int oE = oSA;  // fp32 64 x 65 scratch for column sums (after the slices)
+static_assert(2 * kTile64 * 2 == 2 * kRegionBytes, "RC, RD fill a K/Q buffer");
 
-__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLocalArgs p) {
-    const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+// One (chunk, head, sequence) item.
+struct Item {
+    int ci, h, n, b, t0, t1;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_bwd_local_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                         const BwdLocalArgs p) {
     const int H = p.H, V = p.d_v, dk = p.d_k;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     // TMEM subpartition of this warp and the column half it takes of a
     // 64-column accumulator row
     const int sub = warp & 3, hc = warp >> 2, col0 = 32 * hc;
-    int b, t0, t1;
-    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
-    const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
-    if (ci >= nchunks) return;
-    const int c0 = t0 + ci * kChunk;
-    const int nv = min(kChunk, t1 - c0);
-    const long long row_base = static_cast<long long>(b) * p.T;
-    const long long slot = chunk_slot_base(p.cu_seqlens, n, p.T) + ci;
     const float scale = p.scale;
+    const bool use_tma = dk == kDk;
+    const int nsl = V / kVs;
+    const uint32_t nb = dk * 128;  // bytes of one state tile (hi or lo)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + smem_align_pad(smem_raw);  // 1024-aligned, still known to be shared memory
@@ -97,36 +106,93 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
     float* red = reinterpret_cast<float*>(sm + oRed);
     uint64_t* barp = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oMisc + 4);
     const uint32_t bar = smem_u32(barp);
-    const uint32_t sbar = smem_u32(barp + 1);
-    const int nsl = V / kVs;
-    bool s_out = false;  // thread 0: a state-tile copy is in flight
-    // state tiles of value slice vs (bf16 hi/lo operand tiles written by the
-    // state passes, [slot][head][slice][hi, lo]) -> the S0 and dS tiles
-    auto issue_state = [&](int vs) {
-        const long long off = ((slot * H + h) * nsl + vs) * (2LL * dk * 128);
-        const uint8_t* s0 = reinterpret_cast<const uint8_t*>(p.chunk_states) + off;
-        const uint8_t* s1 = reinterpret_cast<const uint8_t*>(p.chunk_dstates) + off;
-        const uint32_t nb = dk * 128;
-        s_out = true;
-        mbar_arrive_expect_tx(sbar, 4 * nb);
-        bulk_g2s(smem_u32(sm + oSA), s0, nb, sbar);
-        bulk_g2s(smem_u32(sm + oSA + kTileS), s0 + nb, nb, sbar);
-        bulk_g2s(smem_u32(sm + oSB), s1, nb, sbar);
-        bulk_g2s(smem_u32(sm + oSB + kTileS), s1 + nb, nb, sbar);
+    const uint32_t ibar = smem_u32(barp + 1);
+    const uint32_t s0bar = smem_u32(barp + 2);
+    const uint32_t dsbar = smem_u32(barp + 3);
+
+    // item f of the flat (chunk, head, sequence) order; false for chunks past
+    // a sequence's end (and sequences whose bounds are invalid)
+    const int maxc = p.max_chunks;
+    const long long total = static_cast<long long>(maxc) * H * p.N;
+    auto decode = [&](long long f, Item& it) -> bool {
+        it.ci = static_cast<int>(f % maxc);
+        it.h = static_cast<int>((f / maxc) % H);
+        it.n = static_cast<int>(f / (static_cast<long long>(maxc) * H));
+        if (!seq_range(p.cu_seqlens, it.n, p.N, p.T, p.err, it.b, it.t0, it.t1)) return false;
+        return it.ci < (it.t1 - it.t0 + kChunk - 1) / kChunk;
     };
+    auto next_valid = [&](long long f, Item& it) -> long long {
+        while (f < total && !decode(f, it)) f += gridDim.x;
+        return f;
+    };
+    auto first_row = [&](const Item& it) {
+        return static_cast<long long>(it.b) * p.T + it.t0 + static_cast<long long>(it.ci) * kChunk;
+    };
+    auto slot_of = [&](const Item& it) { return chunk_slot_base(p.cu_seqlens, it.n, p.T) + it.ci; };
+
+    // async copies, thread 0; each records what is in flight for the drain
+    bool i_out = false, s0_out = false, ds_out = false;
+    // K/Q (TMA, d_k = 128) and T tiles of item `it` into K/Q buffer kqb
+    auto issue_inputs = [&](const Item& it, uint32_t kqb) {
+        const long long slot = slot_of(it);
+        mbar_arrive_expect_tx(ibar, kChunkTBytes + (use_tma ? 2 * kRegionBytes : 0));
+        if (use_tma) {
+            const int z = static_cast<int>(first_row(it));
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                tma_load_3d(kqb + r * kRegionBytes, &tmap_k, r * 64, it.h, z, ibar);
+                tma_load_3d(kqb + r * kRegionBytes + 64 * 128, &tmap_q, r * 64, it.h, z, ibar);
+            }
+        }
+        bulk_g2s(smem_u32(sm + oT), p.chunk_T + (slot * H + it.h) * static_cast<long long>(kChunkTBytes),
+                 kChunkTBytes, ibar);
+        i_out = true;
+    };
+    // state tiles of value slice vs (bf16 hi/lo operand tiles written by the
+    // state passes, [slot][head][slice][hi, lo])
+    auto state_src = [&](const float* base, const Item& it, int vs) {
+        return reinterpret_cast<const uint8_t*>(base) + ((slot_of(it) * H + it.h) * nsl + vs) * (2LL * dk * 128);
+    };
+    auto issue_s0 = [&](const Item& it, int vs) {
+        const uint8_t* s = state_src(p.chunk_states, it, vs);
+        mbar_arrive_expect_tx(s0bar, 2 * nb);
+        bulk_g2s(smem_u32(sm + oSA), s, nb, s0bar);
+        bulk_g2s(smem_u32(sm + oSA + kTileS), s + nb, nb, s0bar);
+        s0_out = true;
+    };
+    auto issue_ds = [&](const Item& it, int vs) {
+        const uint8_t* s = state_src(p.chunk_dstates, it, vs);
+        mbar_arrive_expect_tx(dsbar, 2 * nb);
+        bulk_g2s(smem_u32(sm + oSB), s, nb, dsbar);
+        bulk_g2s(smem_u32(sm + oSB + kTileS), s + nb, nb, dsbar);
+        ds_out = true;
+    };
+
+    Item cur{};
+    long long f = next_valid(blockIdx.x, cur);
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(bar, 1);
-        mbar_init(sbar, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
-        issue_state(0);
+        *abort_flag = 0;
+        if (use_tma) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_q);
+        }
+        if (f < total) {
+            issue_inputs(cur, smem_u32(sm + oKQ0));
+            issue_s0(cur, 0);
+            issue_ds(cur, 0);
+        }
     }
-    // d_k = 64: key rows 64-127 of the state tiles stay zero
+    // d_k = 64: key rows 64-127 of the state tiles stay zero (the copies
+    // write rows 0-63 only)
     if (dk < kDk) {
         for (int e = tid; e < 4 * 64 * 8; e += kThreads) {
             const int tile = e >> 9, r = 64 + ((e >> 3) & 63), ch = e & 7;
@@ -134,52 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
                 make_uint4(0, 0, 0, 0);
         }
     }
-    // ---- K/Q tiles (plain 16-byte loads, rows beyond the chunk are zero) ----
-    for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
-        const int which = e >> 10;                // 0: K, 1: Q
-        const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
-        const int r = (e >> 3) & 63, ch = e & 7;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < nv && region * 64 < dk) {
-            const uint16_t* src = which ? p.q : p.k;
-            val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
-                                                  region * 64 + ch * 8);
-        }
-        *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
-    }
-    // ---- T operand tiles of this chunk (written by pass 1, already swizzled) ----
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(p.chunk_T + (slot * H + h) * static_cast<long long>(kChunkTBytes));
-        uint4* dst = reinterpret_cast<uint4*>(sm + oT);
-        for (int e = tid; e < kChunkTBytes / 16; e += kThreads) dst[e] = src[e];
-    }
-    if (tid < 64) {
-        const long long idx = (row_base + c0 + tid) * H + h;
-        gv[tid] = (tid < nv) ? p.g[idx] : 0.f;
-        bv[tid] = (tid < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
-    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (tid < 32) {
-        const float a = gv[2 * tid];
-        const float bb = a + gv[2 * tid + 1];
-        float s = bb;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, s, off);
-            if (tid >= off) s += o;
-        }
-        const float base = s - bb;
-        Gv[2 * tid] = base + a;
-        Gv[2 * tid + 1] = s;
-        gam[2 * tid] = exp_nonpos(base + a);
-        gam[2 * tid + 1] = exp_nonpos(s);
-    }
-    __syncthreads();
-    if (tid < 64) dec[tid] = exp_nonpos(Gv[63] - Gv[tid]);
 
     uint32_t phase = 0;
     bool failed = false;  // a bounded wait ran out (reported through the error word)
@@ -188,57 +213,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
             if (elect_one()) mma_commit(bar);
             __syncwarp();
         }
-        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) failed = true;
+        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) {
+            failed = true;
+            *abort_flag = 1;
+        }
         phase ^= 1u;
         tc_fence_after();
     };
-    const uint32_t aKQ = smem_u32(sm + oKQ);
-    auto kdesc_K = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + (s & 3) * 32, 0, 1024); };
-    auto kdesc_Q = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + 64 * 128 + (s & 3) * 32, 0, 1024); };
-    // K or Q read MN-major as a B operand [K = token][N = key column], N = 128
-    auto mn_K = [&](int s) { return desc_sw128(aKQ + s * 2048, kRegionBytes, 1024); };
-    auto mn_Q = [&](int s) { return desc_sw128(aKQ + 64 * 128 + s * 2048, kRegionBytes, 1024); };
-    auto t64 = [&](int off) { return smem_u32(sm + off); };
-
-    // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
-    if (warp == 0) {
-        if (elect_one()) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
-            for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
+    uint32_t iphase = 0, s0phase = 0, dsphase = 0;
+    auto wait_copy = [&](uint32_t b, uint32_t& ph, bool& out) {
+        if (mbar_wait(b, ph, kDefaultWaitLimit)) {
+            ph ^= 1u;
+            out = false;
+        } else {
+            failed = true;
+            *abort_flag = 1;
         }
-        __syncwarp();
-    }
-    mma_sync_wait();
+    };
+
     // accumulator row of this lane and its 16 columns cb .. cb + 15 of a
     // 64-column block; lanes 0-15 hold the per-row sums after the pair join
     const int mrow = m64_half_row(sub, lane);
     const int cb = col0 + 16 * (lane >> 4);
     const bool lead = lane < 16;
     const uint32_t lb = static_cast<uint32_t>(sub * 32) << 16;
-    // the dO tile and the value row of slice vs, fetched into registers one
-    // slice ahead: two 16-byte pieces of the dO tile per thread, and columns
-    // cb .. cb + 15 of value row mrow
-    uint4 do_raw[2], v_raw[2];
-    auto fetch_rows = [&](int vs) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
-            do_raw[k] = make_uint4(0, 0, 0, 0);
-            if (r < nv)
-                do_raw[k] = *reinterpret_cast<const uint4*>(
-                    p.d_out + ((row_base + c0 + r) * H + h) * static_cast<long long>(V) + vs * kVs + ch * 8);
-        }
-        v_raw[0] = v_raw[1] = make_uint4(0, 0, 0, 0);
-        if (mrow < nv) {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.v + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
-            v_raw[0] = src[0];
-            v_raw[1] = src[1];
-        }
-    };
-    fetch_rows(0);
     // columns cb .. cb + 15 of accumulator row mrow (no wait)
     auto ld_cols = [&](uint32_t col, float* v) { tmem_ld_pair16(tmem + lb + col + col0, v); };
     // the two 16-byte chunks of columns cb .. cb + 15 of a split row
@@ -246,279 +244,422 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
         store_split_chunk(sm + off, sm + off + kTile64, row, cb >> 3, x);
         store_split_chunk(sm + off, sm + off + kTile64, row, (cb >> 3) + 1, x + 8);
     };
-    {
-        float row[16];
-        ld_cols(cX1, row);
-        tmem_ld_wait();
-        const float Gi = Gv[mrow];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) row[k] = (cb + k <= mrow) ? row[k] * exp_nonpos(Gi - Gv[cb + k]) : 0.f;
-        store_cols(oP, mrow, row);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
 
-    // per-row accumulators (thread mrow) across value slices
-    float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
-    uint32_t sphase = 0;
-    const int nslices = V / kVs;
-    for (int vs = 0; vs < nslices; ++vs) {
-        // ---- slice loads: S0, dS tiles, dO tile, V row ----
-        // state tiles of this slice (bulk copies issued one slice ahead)
-        if (mbar_wait(sbar, sphase, kDefaultWaitLimit)) {
-            sphase ^= 1u;
-            s_out = false;
-        } else {
-            failed = true;
+    // per-item inputs held in registers, fetched one item (or slice) ahead:
+    // gates of row tid (tid < 64), two 16-byte pieces of the dO tile, and
+    // columns cb .. cb + 15 of value row mrow
+    float g_pre = 0.f, b_pre = 0.f;
+    uint4 do_raw[2], v_raw[2];
+    auto fetch_gates = [&](const Item& it) {
+        g_pre = b_pre = 0.f;
+        const int nvv = min(kChunk, it.t1 - it.t0 - it.ci * kChunk);
+        if (tid < nvv) {
+            const long long idx = (first_row(it) + tid) * H + it.h;
+            g_pre = p.g[idx];
+            b_pre = bf16_to_f32(p.beta[idx]);
         }
-        {
-            // <dS, S0> over 32 values of state row d (hi + lo is the fp32 value to ~16 bits)
-            const int d = tid & 127, hs = tid >> 7;
-            if (d < dk) {
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
-                    float ah[8], al[8], bh[8], bl[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sm + oSA + off), ah);
-                    unpack8(*reinterpret_cast<const uint4*>(sm + oSA + kTileS + off), al);
-                    unpack8(*reinterpret_cast<const uint4*>(sm + oSB + off), bh);
-                    unpack8(*reinterpret_cast<const uint4*>(sm + oSB + kTileS + off), bl);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
-                }
-            }
-        }
+    };
+    auto fetch_rows = [&](const Item& it, int vs) {
+        const int nvv = min(kChunk, it.t1 - it.t0 - it.ci * kChunk);
+        const long long r0 = first_row(it);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
-            *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[k];
+            do_raw[k] = make_uint4(0, 0, 0, 0);
+            if (r < nvv)
+                do_raw[k] = *reinterpret_cast<const uint4*>(
+                    p.d_out + ((r0 + r) * H + it.h) * static_cast<long long>(V) + vs * kVs + ch * 8);
         }
-        // columns cb .. cb + 15 of value row mrow
-        float vrow[16];
-        unpack8(v_raw[0], vrow);
-        unpack8(v_raw[1], vrow + 8);
+        v_raw[0] = v_raw[1] = make_uint4(0, 0, 0, 0);
+        if (mrow < nvv) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.v + ((r0 + mrow) * H + it.h) * static_cast<long long>(V) + vs * kVs + cb);
+            v_raw[0] = src[0];
+            v_raw[1] = src[1];
+        }
+    };
+    if (f < total) {
+        fetch_gates(cur);
+        fetch_rows(cur, 0);
+    }
+
+    for (int k = 0; f < total; ++k) {
+        const int h = cur.h;
+        const int c0 = cur.t0 + cur.ci * kChunk;
+        const int nv = min(kChunk, cur.t1 - c0);
+        const long long row_base = static_cast<long long>(cur.b) * p.T;
+        const uint32_t oKQ = (k & 1) ? oKQ1 : oKQ0;   // this item's K/Q buffer
+        const uint32_t oRC = (k & 1) ? oKQ0 : oKQ1;   // -> dec o Delta, then free
+        const uint32_t oRD = oRC + 2 * kTile64;       // Y = -beta gam dBhat
+        const uint32_t aKQ = smem_u32(sm + oKQ);
+        auto kdesc_K = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + (s & 3) * 32, 0, 1024); };
+        auto kdesc_Q = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + 64 * 128 + (s & 3) * 32, 0, 1024); };
+        // K or Q read MN-major as a B operand [K = token][N = key column], N = 128
+        auto mn_K = [&](int s) { return desc_sw128(aKQ + s * 2048, kRegionBytes, 1024); };
+        auto mn_Q = [&](int s) { return desc_sw128(aKQ + 64 * 128 + s * 2048, kRegionBytes, 1024); };
+        auto t64 = [&](int off) { return smem_u32(sm + off); };
+
+        // ---- item inputs: gates; K/Q (d_k = 64: plain loads), T tiles ----
+        if (tid < 64) {
+            gv[tid] = g_pre;
+            bv[tid] = b_pre;
+        }
+        if (!use_tma) {
+            // rows beyond the chunk and key columns beyond d_k are zero
+            for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
+                const int which = e >> 10;                // 0: K, 1: Q
+                const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
+                const int r = (e >> 3) & 63, ch = e & 7;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (r < nv && region * 64 < dk) {
+                    const uint16_t* src = which ? p.q : p.k;
+                    val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                          region * 64 + ch * 8);
+                }
+                *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+            }
+        }
+        wait_copy(ibar, iphase, i_out);
+        if (use_tma && nv < kChunk) {
+            // the box also read the rows after the chunk: zero them
+            for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
+                const int which = e >> 10, region = (e >> 9) & 1, r = (e >> 3) & 63, ch = e & 7;
+                if (r >= nv)
+                    *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) =
+                        make_uint4(0, 0, 0, 0);
+            }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+        tc_fence_after();
+        if (*abort_flag) break;
+        if (tid < 32) {
+            const float a = gv[2 * tid];
+            const float bb = a + gv[2 * tid + 1];
+            float s = bb;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, s, off);
+                if (tid >= off) s += o;
+            }
+            const float base = s - bb;
+            Gv[2 * tid] = base + a;
+            Gv[2 * tid + 1] = s;
+            gam[2 * tid] = exp_nonpos(base + a);
+            gam[2 * tid + 1] = exp_nonpos(s);
+        }
+        __syncthreads();
+        if (tid < 64) dec[tid] = exp_nonpos(Gv[63] - Gv[tid]);
 
-        // ---- batch 1: K S0 -> X1, P^T dO -> X2 ----
+        // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
         if (warp == 0) {
             if (elect_one()) {
                 tc_fence_after();
-                constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-                constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+                constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
-                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
-                }
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
-                    mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
-                }
+                for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
             }
             __syncwarp();
         }
         mma_sync_wait();
-        float ks0[16], pdo[16];
-        ld_cols(cX1, ks0);
-        ld_cols(cX2, pdo);
-        tmem_ld_wait();
         {
             float row[16];
-            const float bj = bv[mrow], gj = gam[mrow];
+            ld_cols(cX1, row);
+            tmem_ld_wait();
+            const float Gi = Gv[mrow];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
-            store_cols(oRA, mrow, row);
+            for (int kk = 0; kk < 16; ++kk) row[kk] = (cb + kk <= mrow) ? row[kk] * exp_nonpos(Gi - Gv[cb + kk]) : 0.f;
+            store_cols(oP, mrow, row);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- batch 2: K dS -> X1, Delta = T R -> X2 ----
+        // per-row accumulators (thread mrow) across value slices
+        float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
+        for (int vs = 0; vs < nsl; ++vs) {
+            // ---- slice loads: S0 tiles, dO tile, V row ----
+            wait_copy(s0bar, s0phase, s0_out);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int e = tid + kk * kThreads, r = e >> 3, ch = e & 7;
+                *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[kk];
+            }
+            // columns cb .. cb + 15 of value row mrow
+            float vrow[16];
+            unpack8(v_raw[0], vrow);
+            unpack8(v_raw[1], vrow + 8);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+
+            // ---- batch 1: K S0 -> X1, P^T dO -> X2, U += dO S0^T ----
+            if (warp == 0) {
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+                    constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+                    constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+#pragma unroll
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                    }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
+                        mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
+                    }
+                    // B = S0 tile read K-major: [N = key row d][K = value column]
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oSA) + s * 32, 0, 1024), id_n, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024), id_n, 1);
+                    }
+                }
+                __syncwarp();
+            }
+            mma_sync_wait();
+            float ks0[16], pdo[16];
+            ld_cols(cX1, ks0);
+            ld_cols(cX2, pdo);
+            tmem_ld_wait();
+            {
+                float row[16];
+                const float bj = bv[mrow], gj = gam[mrow];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
+                store_cols(oRA, mrow, row);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // the dS tiles of this slice
+            wait_copy(dsbar, dsphase, ds_out);
+            __syncthreads();
+
+            // ---- batch 2: K dS -> X1, Delta = T R -> X2 ----
+            if (warp == 0) {
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+                    constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+                    for (int s = 0; s < kDk / 16; ++s) {
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                    }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
+                        const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
+                        const uint64_t rh = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                        const uint64_t rl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + cX2, th, rh, id_t, s > 0);
+                        mma_bf16(tmem + cX2, th, rl, id_t, 1);
+                        mma_bf16(tmem + cX2, tl, rh, id_t, 1);
+                    }
+                }
+                __syncwarp();
+            }
+            {
+                // <dS, S0> over 32 values of state row d (hi + lo is the fp32
+                // value to ~16 bits), while the batch runs
+                const int d = tid & 127, hs = tid >> 7;
+                if (d < dk) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
+                        float ah[8], al[8], bh[8], bl[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oSA + off), ah);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oSA + kTileS + off), al);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oSB + off), bh);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oSB + kTileS + off), bl);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
+                    }
+                }
+            }
+            mma_sync_wait();
+            {
+                // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
+                // dec o Delta -> RC;  dd = dec * sum_v (K dS) Delta for the decay term of dG
+                const float dj = dec[mrow];
+                float dd = 0.f;
+                float kds[16], dl[16];
+                ld_cols(cX1, kds);
+                ld_cols(cX2, dl);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    dd = fmaf(kds[c], dl[c], dd);
+                    kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
+                }
+                store_cols(oRB, mrow, kds);
+                store_cols(oRA, mrow, dl);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) dl[c] *= dj;
+                store_cols(oRC, mrow, dl);
+                acc_dd = fmaf(dj, dd, acc_dd);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+
+            // ---- batch 3: dBhat = T^T dDelta -> X1;  dP += dO Delta^T;  dK += (dec o Delta) dS^T ----
+            if (warp == 0) {
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
+                    constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
+                    constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
+                        const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                        const uint64_t dl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                        mma_bf16(tmem + cX1, th, dh, id_b, s > 0);
+                        mma_bf16(tmem + cX1, th, dl, id_b, 1);
+                        mma_bf16(tmem + cX1, tl, dh, id_b, 1);
+                    }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cdP, ao, dl, id_p, 1);
+                    }
+                    // B = dS tile read K-major: [N = key row d][K = value column]
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t eh = desc_sw128(t64(oRC) + s * 32, 0, 1024);
+                        const uint64_t el = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
+                        const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
+                        const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdK, eh, sbh, id_n, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
+                        mma_bf16(tmem + cdK, el, sbh, id_n, 1);
+                    }
+                }
+                __syncwarp();
+            }
+            mma_sync_wait();
+            // every product that reads this slice's dS tiles has completed
+            if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1);
+            {
+                // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RB, Y -> RD
+                const float bi = bv[mrow], gi = gam[mrow];
+                float sv = 0.f, sk = 0.f;
+                float db[16], t16[16];
+                ld_cols(cX1, db);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    sv = fmaf(vrow[c], db[c], sv);
+                    sk = fmaf(ks0[c], db[c], sk);
+                }
+                if (mrow < nv) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
+                        dst[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) t16[c] = -db[c];
+                store_cols(oRB, mrow, t16);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
+                store_cols(oRD, mrow, t16);
+                acc_dbeta += sv - gi * sk;
+                acc_dgam -= bi * sk;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+
+            // ---- batch 4: dA += (-dBhat) Delta^T;  dK += Y S0^T ----
+            if (warp == 0) {
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
+                    constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ch_ = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                        const uint64_t cl_ = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdA, ch_, dh, id_c, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
+                        mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
+                        const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
+                        const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
+                        const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
+                        const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdK, yh, sah, id_n, 1);
+                        mma_bf16(tmem + cdK, yh, sal, id_n, 1);
+                        mma_bf16(tmem + cdK, yl, sah, id_n, 1);
+                    }
+                }
+                __syncwarp();
+            }
+            if (vs + 1 < nsl) fetch_rows(cur, vs + 1);  // while the batch runs
+            mma_sync_wait();
+            __syncthreads();
+            if (tid == 0 && vs + 1 < nsl && !failed) issue_s0(cur, vs + 1);  // the S0 tiles are free
+            if (*abort_flag) break;
+        }
+        if (*abort_flag) break;
+
+        // ---- the next item's inputs land while this item's chunk-wide part
+        // runs: K/Q into the other buffer (RC, RD are dead), T, slice 0 states
+        Item nxt{};
+        const long long fn = next_valid(f + gridDim.x, nxt);
+        if (fn < total) {
+            if (tid == 0 && !failed) {
+                issue_inputs(nxt, smem_u32(sm + oRC));
+                issue_s0(nxt, 0);
+                issue_ds(nxt, 0);
+            }
+        }
+
+        // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
         if (warp == 0) {
             if (elect_one()) {
                 tc_fence_after();
-                constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+                constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
                 for (int s = 0; s < kDk / 16; ++s) {
-                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
-                    mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
-                }
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
-                    const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
-                    const uint64_t rh = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
-                    const uint64_t rl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + cX2, th, rh, id_t, s > 0);
-                    mma_bf16(tmem + cX2, th, rl, id_t, 1);
-                    mma_bf16(tmem + cX2, tl, rh, id_t, 1);
+                    mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
+                    mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
                 }
             }
             __syncwarp();
         }
-        mma_sync_wait();
-        {
-            // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
-            // dd = dec * sum_v (K dS) Delta for the decay term of dG
-            const float dj = dec[mrow];
-            float dd = 0.f;
-            float kds[16], dl[16];
-            ld_cols(cX1, kds);
-            ld_cols(cX2, dl);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                dd = fmaf(kds[c], dl[c], dd);
-                kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
-            }
-            store_cols(oRB, mrow, kds);
-            store_cols(oRA, mrow, dl);
-            acc_dd = fmaf(dj, dd, acc_dd);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- batch 3: dBhat = T^T dDelta -> X1;  dP += dO Delta^T ----
-        if (warp == 0) {
-            if (elect_one()) {
-                tc_fence_after();
-                constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
-                constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
-                    const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
-                    const uint64_t dh = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
-                    const uint64_t dl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + cX1, th, dh, id_b, s > 0);
-                    mma_bf16(tmem + cX1, th, dl, id_b, 1);
-                    mma_bf16(tmem + cX1, tl, dh, id_b, 1);
-                }
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                    const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                    const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                    mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
-                    mma_bf16(tmem + cdP, ao, dl, id_p, 1);
-                }
-            }
-            __syncwarp();
+        // gates and the first slice's rows of the next item, while the products run
+        if (fn < total) {
+            fetch_gates(nxt);
+            fetch_rows(nxt, 0);
         }
         mma_sync_wait();
+        // column-sum terms E [64][64] fp32 in the (dead) P tiles, column index
+        // XOR-swizzled by the row so that row-parallel writes and
+        // column-parallel reads both spread over the banks
+        float* E = reinterpret_cast<float*>(sm + oP);
+        float rowsum = 0.f, dbeta_a = 0.f;
         {
-            // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RC, Y -> RD,
-            // dec o Delta (Delta re-read from X2) -> RB
-            const float bi = bv[mrow], gi = gam[mrow], dj = dec[mrow];
-            float sv = 0.f, sk = 0.f;
-            float db[16], dl[16], t16[16];
-            ld_cols(cX1, db);
-            ld_cols(cX2, dl);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                sv = fmaf(vrow[c], db[c], sv);
-                sk = fmaf(ks0[c], db[c], sk);
-            }
-            if (mrow < nv) {
-                uint4* dst = reinterpret_cast<uint4*>(
-                    p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
-                    dst[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 16; ++c) t16[c] = -db[c];
-            store_cols(oRC, mrow, t16);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
-            store_cols(oRD, mrow, t16);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) t16[c] = dj * dl[c];
-            store_cols(oRB, mrow, t16);
-            acc_dbeta += sv - gi * sk;
-            acc_dgam -= bi * sk;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- batch 4: dA += (-dBhat) Delta^T; U += dO S0^T; dK += (dec o Delta) dS^T + Y S0^T ----
-        if (warp == 0) {
-            if (elect_one()) {
-                tc_fence_after();
-                constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
-                constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
-                const uint32_t first = vs > 0 ? 1u : 0u;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ch_ = desc_sw128(t64(oRC) + s * 32, 0, 1024);
-                    const uint64_t cl_ = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
-                    const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                    const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                    mma_bf16(tmem + cdA, ch_, dh, id_c, (first || s > 0) ? 1u : 0u);
-                    mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
-                    mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
-                    // B = S0 / dS tile read K-major: [N = key row d][K = value column]
-                    const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
-                    const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
-                    const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
-                    const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
-                    const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                    mma_bf16(tmem + cU, ao, sah, id_n, (first || s > 0) ? 1u : 0u);
-                    mma_bf16(tmem + cU, ao, sal, id_n, 1);
-                    const uint64_t eh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-                    const uint64_t el = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-                    const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
-                    const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
-                    mma_bf16(tmem + cdK, eh, sbh, id_n, (first || s > 0) ? 1u : 0u);
-                    mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
-                    mma_bf16(tmem + cdK, el, sbh, id_n, 1);
-                    mma_bf16(tmem + cdK, yh, sah, id_n, 1);
-                    mma_bf16(tmem + cdK, yh, sal, id_n, 1);
-                    mma_bf16(tmem + cdK, yl, sah, id_n, 1);
-                }
-            }
-            __syncwarp();
-        }
-        if (vs + 1 < nslices) fetch_rows(vs + 1);  // while the batch runs
-        mma_sync_wait();
-        __syncthreads();
-        if (tid == 0 && vs + 1 < nslices && !failed) issue_state(vs + 1);  // the S0 / dS tiles are free
-    }
-
-    // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
-    if (warp == 0) {
-        if (elect_one()) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
-            for (int s = 0; s < kDk / 16; ++s) {
-                mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
-                mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
-            }
-        }
-        __syncwarp();
-    }
-    mma_sync_wait();
-    float* E = reinterpret_cast<float*>(sm + oE);  // 64 x 65: column-sum terms
-    float rowsum = 0.f, dbeta_a = 0.f;
-    {
-        const int i = mrow;
-        const float Gi = Gv[i], bi = bv[i];
-        {
+            const int i = mrow;
+            const float Gi = Gv[i], bi = bv[i];
             float kk[16], da[16], qk[16], dp[16];
             const int col = cb;
             ld_cols(cX1, kk);
@@ -526,196 +667,200 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
             ld_cols(cX2, qk);
             ld_cols(cdP, dp);
             tmem_ld_wait();
-            {
-                float dkk[16], dqk[16], e16[16];
+            float dkk[16], dqk[16], e16[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int j = col + c;
-                    const float m = (j <= i) ? exp_nonpos(Gi - Gv[j]) : 0.f;
-                    // A side (strictly lower): dA o (K K^T o Ms)
-                    const float kkm = (j < i) ? kk[c] * m : 0.f;
-                    const float a = (j < i) ? da[c] : 0.f;
-                    dbeta_a = fmaf(a, kkm, dbeta_a);
-                    const float dms = a * bi * kkm;
-                    dkk[c] = a * bi * m;
-                    // P side (diagonal included): dQK = dP o M and dP o P
-                    const float dpm = scale * dp[c] * m;
-                    dqk[c] = dpm;
-                    e16[c] = dms + dpm * qk[c];
-                    rowsum += e16[c];
-                }
-                // stores after the loop: they may alias the decay loads
-#pragma unroll
-                for (int c = 0; c < 16; ++c) E[i * 65 + col + c] = e16[c];
-                store_cols(oRA, i, dkk);
-                store_cols(oRB, i, dqk);
+            for (int c = 0; c < 16; ++c) {
+                const int j = col + c;
+                const float m = (j <= i) ? exp_nonpos(Gi - Gv[j]) : 0.f;
+                // A side (strictly lower): dA o (K K^T o Ms)
+                const float kkm = (j < i) ? kk[c] * m : 0.f;
+                const float a = (j < i) ? da[c] : 0.f;
+                dbeta_a = fmaf(a, kkm, dbeta_a);
+                const float dms = a * bi * kkm;
+                dkk[c] = a * bi * m;
+                // P side (diagonal included): dQK = dP o M and dP o P
+                const float dpm = scale * dp[c] * m;
+                dqk[c] = dpm;
+                e16[c] = dms + dpm * qk[c];
+                rowsum += e16[c];
             }
+            // stores after the loop: they may alias the decay loads
+#pragma unroll
+            for (int c = 0; c < 16; ++c) E[i * 64 + ((col + c) ^ (i & 31))] = e16[c];
+            store_cols(oRA, i, dkk);
+            store_cols(oRB, i, dqk);
         }
-    }
-    // <dS, S0> over the whole slice set (gam_n term of dgam)
-    {
-        float v = acc_SdS;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[warp] = v;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid < 64) {
-        float c = 0.f;
-        for (int i = 0; i < 64; ++i) c += E[i * 65 + tid];
-        colsum[tid] = c;
-    }
-    // ---- final products: dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
-    if (warp == 0) {
-        if (elect_one()) {
-            tc_fence_after();
-            constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
-            constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-                const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-                const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
-                mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
-                mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
-                mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
-                const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
-                const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
-                const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
-                const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
-                mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
-                mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
-                mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
-                mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
-            }
-        }
-        __syncwarp();
-    }
-    mma_sync_wait();
-    __syncthreads();
-    // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63: 16-column
-    // groups 4 hc + 2 r + lane / 16 of this lane) ----
-    float dG = 0.f, dbeta = 0.f;
-    {
-        const int i = mrow;
-        const float gi = gam[i];
-        // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
-        float dgq = 0.f;
-#pragma unroll 1
-        for (int r = 0; r < 2; ++r) {
-            const int c16 = 4 * hc + 2 * r + (lane >> 4);
-            const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
-            float u[16], q2[16], kk2[16];
-            tmem_ld_pair16(tmem + lb + cU + cpair, u);
-            tmem_ld_pair16(tmem + lb + cX1 + cpair, q2);
-            tmem_ld_pair16(tmem + lb + cdK + cpair, kk2);
-            tmem_ld_wait();
-            const int region = c16 >> 2, cc = (c16 & 3) * 16;
-            float qrow[16];
-            {
-                const uint8_t* base = sm + oKQ + region * kRegionBytes + 64 * 128;
-                unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2)), qrow);
-                unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[e], dgq);
-            if (i < nv && c16 * 16 < dk) {
-                uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
-                uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t wq[4], wk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = half * 8 + 2 * e;
-                        wq[e] = pack_bf16x2(fmaf(scale * gi, u[c], q2[c]), fmaf(scale * gi, u[c + 1], q2[c + 1]));
-                        wk[e] = pack_bf16x2(kk2[c], kk2[c + 1]);
-                    }
-                    dq[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                    dkp[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-                }
-            }
-        }
-        // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
+        // <dS, S0> over the whole slice set (gam_n term of dgam)
         {
-            float v = acc_dd;
+            float v = acc_SdS;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[8 + warp] = v;
+            if (lane == 0) red[warp] = v;
         }
-        // lanes l and l + 16 hold the two column quarters of row i
-        acc_dbeta += __shfl_xor_sync(0xffffffffu, acc_dbeta, 16);
-        acc_dgam += __shfl_xor_sync(0xffffffffu, acc_dgam, 16);
-        dgq += __shfl_xor_sync(0xffffffffu, dgq, 16);
-        acc_dd += __shfl_xor_sync(0xffffffffu, acc_dd, 16);
-        rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
-        dbeta_a += __shfl_xor_sync(0xffffffffu, dbeta_a, 16);
-        // the row terms of the upper column half join those of the lower half
-        float* part = reinterpret_cast<float*>(sm + oPart) + i * 8;
-        if (lead && hc == 1) {
-            part[0] = acc_dbeta;
-            part[1] = acc_dgam + dgq;
-            part[2] = acc_dd;
-            part[3] = rowsum;
-            part[4] = dbeta_a;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid < 64) {
+            float c = 0.f;
+            for (int i = 0; i < 64; ++i) c += E[i * 64 + (tid ^ (i & 31))];
+            colsum[tid] = c;
+        }
+        // ---- final products: dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
+                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                    const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                    const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                    const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
+                    mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
+                    mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
+                    mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
+                    const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                    const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                    const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                    const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
+                    mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
+                    mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
+                    mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
+                }
+            }
+            __syncwarp();
+        }
+        mma_sync_wait();
+        __syncthreads();
+        // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63: 16-column
+        // groups 4 hc + 2 r + lane / 16 of this lane) ----
+        float dG = 0.f, dbeta = 0.f;
+        {
+            const int i = mrow;
+            const float gi = gam[i];
+            // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
+            float dgq = 0.f;
+#pragma unroll 1
+            for (int r = 0; r < 2; ++r) {
+                const int c16 = 4 * hc + 2 * r + (lane >> 4);
+                const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
+                float u[16], q2[16], kk2[16];
+                tmem_ld_pair16(tmem + lb + cU + cpair, u);
+                tmem_ld_pair16(tmem + lb + cX1 + cpair, q2);
+                tmem_ld_pair16(tmem + lb + cdK + cpair, kk2);
+                tmem_ld_wait();
+                const int region = c16 >> 2, cc = (c16 & 3) * 16;
+                float qrow[16];
+                {
+                    const uint8_t* base = sm + oKQ + region * kRegionBytes + 64 * 128;
+                    unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2)), qrow);
+                    unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[e], dgq);
+                if (i < nv && c16 * 16 < dk) {
+                    uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+                    uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t wq[4], wk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = half * 8 + 2 * e;
+                            wq[e] = pack_bf16x2(fmaf(scale * gi, u[c], q2[c]), fmaf(scale * gi, u[c + 1], q2[c + 1]));
+                            wk[e] = pack_bf16x2(kk2[c], kk2[c + 1]);
+                        }
+                        dq[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        dkp[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    }
+                }
+            }
+            // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
+            {
+                float v = acc_dd;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) red[8 + warp] = v;
+            }
+            // lanes l and l + 16 hold the two column quarters of row i
+            acc_dbeta += __shfl_xor_sync(0xffffffffu, acc_dbeta, 16);
+            acc_dgam += __shfl_xor_sync(0xffffffffu, acc_dgam, 16);
+            dgq += __shfl_xor_sync(0xffffffffu, dgq, 16);
+            acc_dd += __shfl_xor_sync(0xffffffffu, acc_dd, 16);
+            rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
+            dbeta_a += __shfl_xor_sync(0xffffffffu, dbeta_a, 16);
+            // the row terms of the upper column half join those of the lower half
+            float* part = reinterpret_cast<float*>(sm + oPart) + i * 8;
+            if (lead && hc == 1) {
+                part[0] = acc_dbeta;
+                part[1] = acc_dgam + dgq;
+                part[2] = acc_dd;
+                part[3] = rowsum;
+                part[4] = dbeta_a;
+            }
+            __syncthreads();
+            if (lead && hc == 0) {
+                float dgam = acc_dgam + dgq + part[1];
+                float sdd = 0.f;
+                if (i == 63) {
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        dgam += red[w];
+                        sdd += red[8 + w];
+                    }
+                }
+                dG = (rowsum + part[3]) - colsum[i] - (acc_dd + part[2]) + dgam * gi + sdd;
+                dbeta = acc_dbeta + part[0] + dbeta_a + part[4];
+            }
         }
         __syncthreads();
         if (lead && hc == 0) {
-            float dgam = acc_dgam + dgq + part[1];
-            float sdd = 0.f;
-            if (i == 63) {
+            colsum[mrow] = dG;  // reuse as dG vector
+            bv[mrow] = dbeta;   // reuse as dbeta vector
+        }
+        __syncthreads();
+        // dg = reverse running sum of dG over the chunk (warp 0)
+        if (tid < 32) {
+            const int i0 = 63 - 2 * tid, i1 = 62 - 2 * tid;
+            const float a = colsum[i0], bb = colsum[i1];
+            float s = a + bb;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    dgam += red[w];
-                    sdd += red[8 + w];
-                }
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, s, off);
+                if (tid >= off) s += o;
             }
-            dG = (rowsum + part[3]) - colsum[i] - (acc_dd + part[2]) + dgam * gi + sdd;
-            dbeta = acc_dbeta + part[0] + dbeta_a + part[4];
+            const float base = s - (a + bb);
+            if (i0 < nv) {
+                const long long row = (row_base + c0 + i0) * H + h;
+                p.dg[row] = base + a;
+                p.dbeta[row] = f32_to_bf16(bv[i0]);
+            }
+            if (i1 < nv) {
+                const long long row = (row_base + c0 + i1) * H + h;
+                p.dg[row] = s;
+                p.dbeta[row] = f32_to_bf16(bv[i1]);
+            }
         }
-    }
-    __syncthreads();
-    if (lead && hc == 0) {
-        colsum[mrow] = dG;  // reuse as dG vector
-        bv[mrow] = dbeta;   // reuse as dbeta vector
-    }
-    __syncthreads();
-    // dg = reverse running sum of dG over the chunk (warp 0)
-    if (tid < 32) {
-        const int i0 = 63 - 2 * tid, i1 = 62 - 2 * tid;
-        const float a = colsum[i0], bb = colsum[i1];
-        float s = a + bb;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, s, off);
-            if (tid >= off) s += o;
-        }
-        const float base = s - (a + bb);
-        if (i0 < nv) {
-            const long long row = (row_base + c0 + i0) * H + h;
-            p.dg[row] = base + a;
-            p.dbeta[row] = f32_to_bf16(bv[i0]);
-        }
-        if (i1 < nv) {
-            const long long row = (row_base + c0 + i1) * H + h;
-            p.dg[row] = s;
-            p.dbeta[row] = f32_to_bf16(bv[i1]);
-        }
+        __syncthreads();
+        cur = nxt;
+        f = fn;
     }
     if (failed) {
         record_error(p.err, kErrTimeout);
-        if (warp == 0) {  // let every MMA and copy this CTA issued land before it leaves
-            if (elect_one()) mma_commit(bar);
-            __syncwarp();
-        }
-        if (tid == 0) {
-            mbar_wait(bar, phase, kDefaultWaitLimit);
-            if (s_out) mbar_wait(sbar, sphase, kDefaultWaitLimit);
-        }
+    }
+    // let every MMA and copy this CTA issued land before it leaves
+    if (warp == 0) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
+    }
+    if (tid == 0) {
+        mbar_wait(bar, phase, kDefaultWaitLimit);
+        if (i_out) mbar_wait(ibar, iphase, kDefaultWaitLimit);
+        if (s0_out) mbar_wait(s0bar, s0phase, kDefaultWaitLimit);
+        if (ds_out) mbar_wait(dsbar, dsphase, kDefaultWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -726,10 +871,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_local_kernel(const BwdLoc
 
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (a.max_chunks == 0) return cudaSuccess;
+    const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
+    CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    if (rows > 0 && a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.max_chunks, a.H, a.N);
-    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(a);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long items = static_cast<long long>(a.max_chunks) * a.H * a.N;
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, a);
     return cudaGetLastError();
 }
 

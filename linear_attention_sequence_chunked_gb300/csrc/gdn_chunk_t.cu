@@ -146,26 +146,18 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_chunk_t_kernel(const ChunkTAr
     tc_fence_after();
     __syncthreads();
 
-    // A: thread (warp w, lane l) takes row i = 16 w + l % 16, columns 32 (l / 16) .. + 31;
-    // lane l < 16 holds the TMEM row, lane l + 16 takes its upper 32 columns
+    // A: thread (warp w, lane l) takes row i = 16 w + l % 16, columns 32 (l / 16) .. + 31
+    // (lanes l and l + 16 read the two column halves of TMEM row i)
     {
         const int i = 16 * warp + (lane & 15), hf = lane >> 4, j0 = 32 * hf;
         const float Gi = Gv[i], bi = bv[i];
         float mdec[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) mdec[k] = (j0 + k < i) ? exp_nonpos(Gi - Gv[j0 + k]) : 0.f;
-        const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float lo[32], up[32];
-        tmem_ld16(lb, lo);
-        tmem_ld16(lb + 16, lo + 16);
-        tmem_ld16(lb + 32, up);
-        tmem_ld16(lb + 48, up + 16);
-        tmem_ld_wait();
+        float lo[32];
+        ld_half32(tmem, warp, 0, lo);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float kk = __shfl_sync(0xffffffffu, up[k], lane & 15);
-            lo[k] = bi * (hf ? kk : lo[k]) * mdec[k];
-        }
+        for (int k = 0; k < 32; ++k) lo[k] = bi * lo[k] * mdec[k];
         // stores after the loop: they may alias the decay loads
 #pragma unroll
         for (int k = 0; k < 32; ++k) At[(j0 + k) * 64 + i] = lo[k];

@@ -869,36 +869,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mdec[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) mdec[k] = (j0 + k <= i) ? exp_nonpos(Gi - Gv[j0 + k]) : 0.f;
-                // the M = 64 products sit in lanes 0-15 of each subpartition: lane
-                // l < 16 loads row i, lane l + 16 takes its upper 32 columns
-                const uint32_t lb = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+                // the M = 64 products sit in lanes 0-15 of each subpartition:
+                // lanes l and l + 16 read the two column halves of row i
                 if (!load_t) {
-                    float lo[32], up[32];
-                    tmem_ld16(lb + kColG, lo);
-                    tmem_ld16(lb + kColG + 16, lo + 16);
-                    tmem_ld16(lb + kColG + 32, up);
-                    tmem_ld16(lb + kColG + 48, up + 16);
-                    tmem_ld_wait();
+                    float lo[32];
+                    ld_half32(tmem, sub, kColG, lo);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float kk = __shfl_sync(0xffffffffu, up[k], lane & 15);
-                        lo[k] = (j0 + k < i) ? bi * (hf ? kk : lo[k]) * mdec[k] : 0.f;
-                    }
+                    for (int k = 0; k < 32; ++k) lo[k] = (j0 + k < i) ? bi * lo[k] * mdec[k] : 0.f;
 #pragma unroll
                     for (int k = 0; k < 32; ++k) At[(j0 + k) * 64 + i] = lo[k];
                 }
                 if (want_p) {
-                    float lo[32], up[32];
-                    tmem_ld16(lb + kColQK, lo);
-                    tmem_ld16(lb + kColQK + 16, lo + 16);
-                    tmem_ld16(lb + kColQK + 32, up);
-                    tmem_ld16(lb + kColQK + 48, up + 16);
-                    tmem_ld_wait();
+                    float lo[32];
+                    ld_half32(tmem, sub, kColQK, lo);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float qk = __shfl_sync(0xffffffffu, up[k], lane & 15);
-                        lo[k] = (hf ? qk : lo[k]) * mdec[k];
-                    }
+                    for (int k = 0; k < 32; ++k) lo[k] *= mdec[k];
                     // P tiles of this slot are free: the chain finished iteration it - 2
                     uint8_t* p_hi = sm + oP + (2 * slot) * kTile64;
                     uint8_t* p_lo = sm + oP + (2 * slot + 1) * kTile64;
