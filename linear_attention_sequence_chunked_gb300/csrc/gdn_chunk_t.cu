@@ -38,12 +38,13 @@ constexpr int kTB = 32 * kTS;
 
 constexpr int oK = 0;                        // K tile, two 64-column regions
 constexpr int oA = oK + 2 * kKRegion;        // A^T fp32 [64][64]
-constexpr int oTf = oA + 64 * 64 * 4;        // T_00, T_11, T_10 fp32 32x32 blocks
-constexpr int oVec = oTf + 3 * kTB * 4;      // g, beta, G x 64 fp32
+constexpr int oTf = oK;                      // T_00, T_11, T_10 fp32 32x32 blocks (K is dead once K K^T is done)
+constexpr int oVec = oA + 64 * 64 * 4;       // g, beta, G x 64 fp32
 constexpr int oBar = oVec + 3 * 64 * 4;
 constexpr int oMisc = oBar + 8;
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
+static_assert(3 * kTB * 4 <= 2 * kKRegion, "T blocks fit in the K tile");
 
 // One 8-value piece (row `row`, columns 8 ch ..) of the T hi/lo tiles in global memory.
 __device__ __forceinline__ void put_split_global(uint8_t* tile, int row, int ch, const float* x8) {
@@ -59,7 +60,7 @@ __device__ __forceinline__ void put_split_global(uint8_t* tile, int row, int ch,
     *reinterpret_cast<uint4*>(tile + kTile64 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 4) gdn_chunk_t_kernel(const ChunkTArgs p) {
+__global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTArgs p) {
     const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int H = p.H, dk = p.d_k;
     const int q = threadIdx.x;
