@@ -94,19 +94,34 @@ __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTAr
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    // K tile (rows beyond the chunk and key columns beyond d_k are zero)
-    for (int e = q; e < 2 * 64 * 8; e += kThreads) {
-        const int region = e >> 9, r = (e >> 3) & 63, ch = e & 7;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < nv && region * 64 < dk)
-            val = *reinterpret_cast<const uint4*>(p.k + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
-                                                  region * 64 + ch * 8);
-        *reinterpret_cast<uint4*>(sm + oK + region * kKRegion + sw128_offset(r, ch * 16)) = val;
-    }
-    if (q < 64) {
-        const long long idx = (row_base + c0 + q) * H + h;
-        gv[q] = (q < nv) ? p.g[idx] : 0.f;
-        bv[q] = (q < nv) ? bf16_to_f32(p.beta[idx]) : 0.f;
+    // K tile (rows beyond the chunk and key columns beyond d_k are zero):
+    // every load of this thread is in flight before the first store
+    {
+        constexpr int kPer = 2 * 64 * 8 / kThreads;
+        uint4 val[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = q + u * kThreads, region = e >> 9, r = (e >> 3) & 63, ch = e & 7;
+            val[u] = make_uint4(0, 0, 0, 0);
+            if (r < nv && region * 64 < dk)
+                val[u] = *reinterpret_cast<const uint4*>(p.k + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                         region * 64 + ch * 8);
+        }
+        float gq = 0.f, bq = 0.f;
+        if (q < nv) {
+            const long long idx = (row_base + c0 + q) * H + h;
+            gq = p.g[idx];
+            bq = bf16_to_f32(p.beta[idx]);
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = q + u * kThreads, region = e >> 9, r = (e >> 3) & 63, ch = e & 7;
+            *reinterpret_cast<uint4*>(sm + oK + region * kKRegion + sw128_offset(r, ch * 16)) = val[u];
+        }
+        if (q < 64) {
+            gv[q] = gq;
+            bv[q] = bq;
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
