@@ -84,8 +84,10 @@ typedef enum {
 GDN_API const char* gdn_status_string(gdn_status status);
 
 /*
- * Bytes of device workspace gdn_chunk_fwd needs for these sizes (may be 0).
- * varlen != 0 when cu_seqlens will be given (B is then the sequence count).
+ * Bytes of device workspace gdn_chunk_fwd uses for these sizes: the bf16
+ * hi/lo tiles of T = (I + A)^-1 of every chunk, 16 KB per chunk and head
+ * (0 for unsupported sizes).  varlen != 0 when cu_seqlens will be given
+ * (B is then the sequence count).
  */
 GDN_API size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
 
@@ -99,8 +101,13 @@ GDN_API size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_
  *   initial_state (N,H,d_k,d_v) fp32 or NULL (zeros)
  *   cu_seqlens    NULL (dense) or device int32[N+1] (packed; N = B)
  *   final_state   (N,H,d_k,d_v) fp32 or NULL (not written)
- *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size()
- *                 bytes (may be NULL when that size is 0)
+ *   workspace     optional device scratch, 256-byte aligned.  With at least
+ *                 gdn_chunk_fwd_workspace_size() bytes, every chunk's T is
+ *                 formed first by a chunk-parallel kernel and the chunk chain
+ *                 reads it (the faster route); with NULL or fewer bytes the
+ *                 chunk chain forms T itself.  Both routes give the same
+ *                 arithmetic.  A non-NULL workspace that is not 256-byte
+ *                 aligned returns GDN_ERR_MISALIGNED.
  * Returns GDN_OK once the work is enqueued on `stream`.
  */
 GDN_API gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,

@@ -108,8 +108,8 @@ const char* gdn_status_string(gdn_status status) {
 }
 
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
-    (void)B; (void)T; (void)H; (void)d_k; (void)d_v; (void)varlen;
-    return 0;
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
+    return tiles_bytes(B, T, H, varlen);
 }
 
 size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
@@ -130,16 +130,19 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
     if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
-    (void)workspace;
-    (void)workspace_bytes;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return GDN_ERR_MISALIGNED;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
-    // the forward forms T inside the chunk chain (its prep warpgroup runs one
-    // chunk ahead); the backward computes all T tiles first, chunk-parallel
+    // With a workspace, every chunk's T tiles come first from the
+    // chunk-parallel kernel and the chunk chain only copies them in; without
+    // one, the chain's prep warpgroup forms T itself, one chunk ahead.
+    const size_t tb = tiles_bytes(B, T, H, cu_seqlens != nullptr);
+    uint8_t* tiles = (workspace && workspace_bytes >= tb && tb > 0) ? static_cast<uint8_t*>(workspace) : nullptr;
+    if (tiles && !launch_tiles(k, g, beta, cu_seqlens, tiles, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
     gdn::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens;
-    a.out = out; a.final_state = final_state; a.chunk_states = nullptr; a.chunk_T = nullptr;
+    a.out = out; a.final_state = final_state; a.chunk_states = nullptr; a.chunk_T = tiles;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
     if (!launched(gdn::launch_fwd_ws(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
     return GDN_OK;

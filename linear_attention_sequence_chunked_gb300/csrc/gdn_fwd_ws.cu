@@ -84,7 +84,7 @@ constexpr int kTB = 32 * kTS;                       // floats per block
 constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
-constexpr int kBars = 16;
+constexpr int kBars = 17;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 // backward: the dO tile [i][v] bf16 shares the R tiles' space (dead between
@@ -96,8 +96,11 @@ static_assert(kAlloc <= 232448, "shared memory");
 enum {
     B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
     B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_TCOPY = 11,
-    B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15
+    B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16
 };
+// named barrier 3 (warps 0 and 1): warp 0 has issued the MMAs on the chain's
+// critical path; warp 1 then queues the off-path ones (Q S, P Delta) behind them
+constexpr int kBarHandoff = 3;
 
 __device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, 128); }
 
@@ -266,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Q S goes to one of two column blocks by chunk parity: the output
             // of chunk c reads its block while chunk c+1's Q S is computed
             auto col_qs = [](int cj) { return (cj & 1) ? kColQS2 : kColQS; };
-            // C1 of chunk cj: K S and Q S (thread 0, stage cj full)
-            auto issue_c1 = [&](int cj) {
+            // C1 of chunk cj, K S (warp 0, stage cj full) and Q S (warp 1,
+            // queued behind K S; completion tracked by warp 1's P Delta commit)
+            auto issue_ks = [&](int cj) {
                 const uint32_t stage_c = smem_u32(sm + oStage + (cj & 1) * kStageBytes);
                 tc_fence_after();
                 constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
@@ -281,31 +285,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
                 }
                 mma_commit(bar(B_KS));
-                if (want_out) {
-                    const uint32_t cq = col_qs(cj);
+            };
+            auto issue_qs = [&](int cj) {
+                const uint32_t stage_c = smem_u32(sm + oStage + (cj & 1) * kStageBytes);
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+                const uint32_t cq = col_qs(cj);
 #pragma unroll
-                    for (int s = 0; s < kDk / 16; ++s) {
-                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                        const uint64_t a_q = desc_sw128(stage_c + koff + 64 * 128, 0, 1024);
-                        const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                        const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                        mma_bf16(tmem + cq, a_q, b_hi, id_s, s > 0);
-                        mma_bf16(tmem + cq, a_q, b_lo, id_s, 1);
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    const uint64_t a_q = desc_sw128(stage_c + koff + 64 * 128, 0, 1024);
+                    const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
+                    const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
+                    mma_bf16(tmem + cq, a_q, b_hi, id_s, s > 0);
+                    mma_bf16(tmem + cq, a_q, b_lo, id_s, 1);
+                }
+            };
+            // warp 0 issues K S of chunk cj once its stage is full, then hands
+            // off to warp 1 for Q S (the handoff happens even on a timeout, so
+            // warp 1 never waits on a barrier warp 0 skipped)
+            auto issue_c1 = [&](int cj) {
+                if (warp == 0) {
+                    const bool full = __all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + (cj & 1)), (cj >> 1) & 1, wl));
+                    if (full) {
+                        if (elect_one()) issue_ks(cj);
+                        __syncwarp();
+                        tma_done = cj + 1;
+                    } else if (lane == 0) {
+                        *abort_flag = 1;
+                    }
+                    named_bar_arrive(kBarHandoff, 64);
+                } else if (warp == 1) {
+                    tc::named_bar(kBarHandoff, 64);
+                    if (want_out && !*abort_flag) {
+                        if (elect_one()) issue_qs(cj);
+                        __syncwarp();
                     }
                 }
             };
             load_v(0);
             if (nchunks > 0) {
                 if (p.chunk_states && t == 0) store_state_tiles(0);
-                if (warp == 0) {
-                    if (__all_sync(0xffffffffu, mbar_wait(bar(B_FULL0), 0, wl))) {
-                        if (elect_one()) issue_c1(0);
-                        __syncwarp();
-                        tma_done = 1;
-                    } else if (lane == 0) {
-                        *abort_flag = 1;
-                    }
-                }
+                issue_c1(0);
             }
             for (int ci = 0; ci < nchunks; ++ci) {
                 const int c0 = t0 + ci * kChunk;
@@ -391,12 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar(1);
 
-                // ---- C5: S update and P Delta ----
+                // ---- C5: S update (warp 0) and P Delta (warp 1, behind it) ----
                 if (warp == 0) {
                     if (elect_one()) {
                         tc_fence_after();
                         constexpr uint32_t id_s = idesc(kFmtBf16, 1, 1, kDk, 64);
-                        constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
@@ -406,6 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColS, ak, rl, id_s, 1);
                         }
                         mma_commit(bar(B_S));
+                    }
+                    __syncwarp();
+                    named_bar_arrive(kBarHandoff, 64);
+                } else if (warp == 1) {
+                    tc::named_bar(kBarHandoff, 64);
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
                         if (want_out) {
 #pragma unroll
                             for (int s = 0; s < 4; ++s) {
@@ -428,15 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
-                // every MMA that reads this chunk's K/Q stage has completed
-                if (t == 0) {
-                    if (use_tma) {
-                        if (ci + kStages < nchunks) issue_tma(ci + kStages);
-                    } else {
-                        mbar_arrive(bar(B_SFREE0 + st));
-                    }
-                }
-                if (use_tma && ci + kStages < nchunks) tma_issued = ci + kStages + 1;
 
                 // ---- C6: state update ----
                 {
@@ -453,19 +472,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- next chunk's C1, issued ahead of this chunk's output ----
                 if (ci + 1 < nchunks) {
                     if (p.chunk_states && t == 0) store_state_tiles(ci + 1);
-                    if (warp == 0) {
-                        if (__all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + ((ci + 1) & 1)), ((ci + 1) >> 1) & 1, wl))) {
-                            if (elect_one()) issue_c1(ci + 1);
-                            __syncwarp();
-                            tma_done = ci + 2;
-                        } else if (lane == 0) {
-                            *abort_flag = 1;
-                        }
-                    }
+                    issue_c1(ci + 1);
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
+                // every MMA that reads this chunk's K/Q stage has completed: K S,
+                // the state update (warp 0) and Q S (warp 1, tracked by P Delta)
+                if (t == 0 && !*abort_flag) {
+                    if (use_tma) {
+                        if (ci + kStages < nchunks) {
+                            issue_tma(ci + kStages);
+                            tma_issued = ci + kStages + 1;  // thread 0's count drives the drain
+                        }
+                    } else {
+                        mbar_arrive(bar(B_SFREE0 + st));
+                    }
+                }
                 // ---- output ----
                 if (want_out) {
                     const bool mine = hrow < nv;
@@ -588,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 32; ++c) row[c] *= gi;
                     store_split_half(Dhi, Dlo, hrow, hf, row);
                 }
+                fence_proxy_async_smem();
                 load_do(it + 1);
                 __syncwarp();
                 bool ok = mbar_wait(bar(B_KS), ph, wl);
@@ -596,6 +620,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
+                // Q^T G starts the state-gradient product now (A = Q^T read
+                // MN-major from the stage); it runs under the dDelta epilogue
+                if (warp == 0) {
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
+                            const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
+                            const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColS, aq, gh, id, s > 0);
+                            mma_bf16(tmem + kColS, aq, gl, id, 1);
+                        }
+                    }
+                    __syncwarp();
+                }
 
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
@@ -652,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar(1);
 
-                // ---- C5: K^T X + Q^T G (A = K^T, Q^T read MN-major from the stage) ----
+                // ---- C5: K^T X added to Q^T G (A = K^T read MN-major from the stage) ----
                 if (warp == 0) {
                     if (elect_one()) {
                         tc_fence_after();
@@ -660,15 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
-                            const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
                             const uint64_t xh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
                             const uint64_t xl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                            const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                            const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColS, ak, xh, id, s > 0);
+                            mma_bf16(tmem + kColS, ak, xh, id, 1);
                             mma_bf16(tmem + kColS, ak, xl, id, 1);
-                            mma_bf16(tmem + kColS, aq, gh, id, 1);
-                            mma_bf16(tmem + kColS, aq, gl, id, 1);
                         }
                         mma_commit(bar(B_S));
                     }
@@ -711,10 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 0) {
                 if (elect_one()) mma_commit(bar(B_DRAIN0));
                 __syncwarp();
+            } else if (warp == 1) {
+                if (elect_one()) mma_commit(bar(B_DRAIN2));
+                __syncwarp();
             }
             if (t == 0) {
                 record_error(p.err, kErrTimeout);
                 mbar_wait(bar(B_DRAIN0), 0, wl);
+                mbar_wait(bar(B_DRAIN2), 0, wl);
                 for (int ci = tma_done; ci < tma_issued; ++ci)
                     mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
             }

@@ -81,6 +81,36 @@ def test_resume_from_final_state():
             G.compare(Sb, S, 1e-4, None, "resume state")
 
 
+@pytest.mark.parametrize("dk,dv,lens", [(128, 128, [1, 63, 65, 0, 700, 64]), (64, 256, [129, 300])])
+def test_forward_routes_agree_bitwise(dk, dv, lens):
+    """T from the chunk-parallel kernel (workspace given) and T formed inside
+    the chunk chain (no workspace) give the same bits; the no-workspace route
+    also matches the oracle."""
+    import torch
+    wl = W.random_workload(B=1, T=0, H=2, d_k=dk, d_v=dv, seed=11, seqlens=lens,
+                           initial_state=True)
+    d = G.to_device(wl)
+    N = len(lens)
+    outs = []
+    for with_ws in (True, False):
+        out = torch.empty(d["v"].shape, dtype=torch.bfloat16, device="cuda")
+        fs = torch.empty((N, 2, dk, dv), dtype=torch.float32, device="cuda")
+        nbytes = gdn.gdn_chunk_fwd_workspace_size(N, wl.T, 2, dk, dv, True)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if with_ws else None
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.scale,
+                          d["initial_state"], d["cu_seqlens"], out, fs, N, wl.T, 2, dk, dv,
+                          ws, nbytes if with_ws else 0)
+        assert gdn.gdn_get_last_device_error() == 0
+        torch.cuda.synchronize()
+        outs.append((G.bf16_to_np(out), fs.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+    o_ref, S_ref = recurrence.workload_fwd(wl)
+    G.compare(outs[1][0], o_ref, G.TOL_RMS_IID, G.TOL_MAX_IID, "no-workspace out")
+    G.compare(outs[1][1], S_ref, G.TOL_RMS_IID, G.TOL_MAX_IID, "no-workspace state")
+
+
 def test_repeat_launches_are_bitwise_equal():
     wl = W.make_workload(2, B=2, H=4, T=1024, with_grad=True)
     o1, S1 = G.run_fwd(wl)
