@@ -450,8 +450,8 @@ def bf16_np(t):
 
 
 def load_traffic():
-    """Per-launch DRAM traffic of the forward kernel from the committed ncu
-    summary, when it was taken on the current kernel source."""
+    """DRAM traffic of one forward call (its launches summed) from the
+    committed ncu summary, when it was taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -459,13 +459,15 @@ def load_traffic():
     except Exception:
         return None
     import hashlib
-    src = os.path.join(ROOT, "linear_attention_sequence_chunked_gb300", "csrc", d.get("source", ""))
-    try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-    except Exception:
-        return None
-    if digest != d.get("sha256"):
+    csrc = os.path.join(ROOT, "linear_attention_sequence_chunked_gb300", "csrc")
+    for name, digest in d.get("sources", {}).items():
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except Exception:
+            return None
+    if not d.get("sources"):
         return None
     return d.get("bytes_per_launch")
 
