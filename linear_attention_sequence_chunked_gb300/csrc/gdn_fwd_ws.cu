@@ -1,16 +1,20 @@
 // Chunked gated delta rule, warp-specialised tensor-core chunk chain: the
 // forward, and the reverse-chunk chain of state gradients of the backward.
 //
-// One CTA (256 threads) per (64-column value slice, head, sequence).  Two
-// warpgroups run concurrently, one chunk apart:
+// One CTA (384 threads) per (64-column value slice, head, sequence).  Two
+// groups of warps run concurrently, one chunk apart:
 //
-//   prep  (warps 4-7), chunk c+1:  g cumsum; [K;Q] K^T on the tensor cores;
-//         A = beta_i (k_i.k_j) exp(G_i - G_j) (j < i) and the causal score
-//         P = (q_i.k_j) exp(G_i - G_j) (j <= i); T = (I + A)^-1 in fp32 on the
-//         CUDA cores; T and P written as bf16 hi/lo operand tiles.
-//   chain (warps 0-3), chunk c:    K S, Q S -> R = beta o (V - gam o (K S));
+//   prep  (warps 8-11), chunk c+1: g cumsum; Q K^T on the tensor cores and
+//         the causal score P = (q_i.k_j) exp(G_i - G_j) (j <= i) as bf16 hi/lo
+//         operand tiles; T = (I + A)^-1, A = beta_i (k_i.k_j) exp(G_i - G_j)
+//         (j < i), copied in from the chunk-parallel kernel's tiles or, with
+//         none given, formed here (K K^T on the tensor cores, fp32 inverse on
+//         the CUDA cores).
+//   chain (warps 0-7), chunk c:    K S, Q S -> R = beta o (V - gam o (K S));
 //         Delta = T R; S <- gam_n S + K^T (dec o Delta); O = scale
-//         [gam o (Q S) + P Delta].  S (fp32) lives in the chain's registers.
+//         [gam o (Q S) + P Delta].  S (fp32) lives in the chain's registers,
+//         each row split between the two warps that share its TMEM
+//         subpartition.
 //
 // Backward mode walks the chunks from last to first with the same prep; the
 // chain carries dS, the gradient w.r.t. a chunk's end state, and steps it to
@@ -49,7 +53,9 @@ namespace {
 using namespace sm100;
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kChainThreads = 256;  // warps 0-7
+constexpr int kPrepThreads = 128;   // warps 8-11
+constexpr int kThreads = kChainThreads + kPrepThreads;
 constexpr int kVs = 64;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
@@ -102,7 +108,7 @@ enum {
 // critical path; warp 1 then queues the off-path ones (Q S, P Delta) behind them
 constexpr int kBarHandoff = 3;
 
-__device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, 128); }
+__device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, id == 1 ? kChainThreads : kPrepThreads); }
 
 // Arguments of both directions.
 struct ChainArgs {
@@ -203,10 +209,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
 
-    if (warp < 4) {
-        // ======================= chain warpgroup =======================
+    if (warp < 8) {
+        // ======================= chain warps =======================
+        // Warps w and w + 4 share TMEM subpartition w % 4.  State rows: lane
+        // l of warp w holds row 32 (w % 4) + l, columns 32 (w / 4) .. + 31 of
+        // the slice.  M = 64 rows: lanes l and l + 16 of warps w and w + 4
+        // hold row 16 (w % 4) + l % 16, one 16-column quarter each.
         const int t = tid;
-        const int srow = t < dk ? t : -1;
+        const int sw = warp & 3, hs = warp >> 2;
+        const int srow_all = 32 * sw + lane;
+        const int srow = srow_all < dk ? srow_all : -1;
+        const int hrow = 16 * sw + (lane & 15);
+        const int cq = 16 * (2 * hs + (lane >> 4));  // first column of this lane's quarter
+        const uint32_t lb = static_cast<uint32_t>(sw * 32) << 16;
+        // quarter row cq .. cq + 15 of M = 64 accumulator row hrow (no wait)
+        auto ld_q16 = [&](uint32_t col, float* v) { tmem_ld_pair16(tmem + lb + col + 32 * hs, v); };
+        // the two 16-byte chunks of columns cq .. cq + 15 of a split row
+        auto store_q16 = [&](uint8_t* thi, uint8_t* tlo, int row, const float* x) {
+            store_split_chunk(thi, tlo, row, cq >> 3, x);
+            store_split_chunk(thi, tlo, row, (cq >> 3) + 1, x + 8);
+        };
+        // columns 32 hs .. + 31 of M = 128 accumulator row srow_all
+        auto ld_s32 = [&](uint32_t col, float* v) {
+            tmem_ld16(tmem + lb + col + 32 * hs, v);
+            tmem_ld16(tmem + lb + col + 32 * hs + 16, v + 16);
+            tmem_ld_wait();
+        };
         const long long KV = static_cast<long long>(dk) * V;
         const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
         const float scale = p.scale;
@@ -222,18 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (use_tma) tma_issued = min(kStages, nchunks);
 
-        float S[kVs];
+        float S[32];
 #pragma unroll
-        for (int j = 0; j < kVs; ++j) S[j] = 0.f;
+        for (int j = 0; j < 32; ++j) S[j] = 0.f;
         if (srow >= 0 && p.state_in) {
-            const float* src = p.state_in + state_off + static_cast<long long>(srow) * V;
+            const float* src = p.state_in + state_off + static_cast<long long>(srow) * V + 32 * hs;
 #pragma unroll
-            for (int j = 0; j < kVs; j += 4) {
+            for (int j = 0; j < 32; j += 4) {
                 const float4 t4 = *reinterpret_cast<const float4*>(src + j);
                 S[j] = t4.x; S[j + 1] = t4.y; S[j + 2] = t4.z; S[j + 3] = t4.w;
             }
         }
-        store_split_row(Shi, Slo, t, S);
+        store_split_half(Shi, Slo, srow_all, hs, S);
         fence_proxy_async_smem();
         named_bar(1);
 
@@ -250,20 +278,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool aborted = false;
         if constexpr (!kBwd) {
-            // half a value row of this slice (row hrow of the chunk, columns
-            // 32*hf.. of the slice), packed bf16; the next chunk's half row is
+            // a quarter value row of this slice (row hrow of the chunk, columns
+            // cq .. cq + 15 of the slice), packed bf16; the next chunk's is
             // fetched as soon as the current one is consumed
-            const int hrow = m64_half_row(warp, lane), hf = lane >> 4;
-            uint4 vraw[4];
+            uint4 vraw[2];
             auto load_v = [&](int cj) {
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) vraw[ch] = make_uint4(0, 0, 0, 0);
+                vraw[0] = vraw[1] = make_uint4(0, 0, 0, 0);
                 const int cc0 = t0 + cj * kChunk;
                 if (cj < nchunks && hrow < min(kChunk, t1 - cc0)) {
                     const uint4* src = reinterpret_cast<const uint4*>(
-                        p.v + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) vraw[ch] = src[ch];
+                        p.v + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
+                    vraw[0] = src[0];
+                    vraw[1] = src[1];
                 }
             };
             // Q S goes to one of two column blocks by chunk parity: the output
@@ -350,11 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C2: R = beta o (V - gam o (K S)) ----
                 {
-                    float row[32];
-                    ld_half32(tmem, warp, kColKS, row);
+                    float row[16];
+                    ld_q16(kColKS, row);
+                    tmem_ld_wait();
                     const float bj = bv[hrow], gj = gam[hrow];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < 2; ++ch) {
                         const uint32_t w4[4] = {vraw[ch].x, vraw[ch].y, vraw[ch].z, vraw[ch].w};
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
@@ -363,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             row[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * row[c + 1]);
                         }
                     }
-                    store_split_half(Rhi, Rlo, hrow, hf, row);
+                    store_q16(Rhi, Rlo, hrow, row);
                 }
                 load_v(ci + 1);
                 fence_proxy_async_smem();
@@ -400,13 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C4: Delta tiles and dec o Delta tiles ----
                 {
-                    float row[32];
-                    ld_half32(tmem, warp, kColD, row);
-                    store_split_half(Dhi, Dlo, hrow, hf, row);
+                    float row[16];
+                    ld_q16(kColD, row);
+                    tmem_ld_wait();
+                    store_q16(Dhi, Dlo, hrow, row);
                     const float dj = dec[hrow];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) row[c] *= dj;
-                    store_split_half(Rhi, Rlo, hrow, hf, row);
+                    for (int c = 0; c < 16; ++c) row[c] *= dj;
+                    store_q16(Rhi, Rlo, hrow, row);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -459,12 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C6: state update ----
                 {
-                    float row[64];
+                    float row[32];
                     const float gC = gam[63];
-                    ld_row64(tmem, warp, kColS, row);
+                    ld_s32(kColS, row);
 #pragma unroll
-                    for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
-                    store_split_row(Shi, Slo, t, S);
+                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                    store_split_half(Shi, Slo, srow_all, hs, S);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -493,15 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (want_out) {
                     const bool mine = hrow < nv;
                     const float gi = gam[hrow];
-                    float qs[32], pd[32];
-                    ld_half32_nowait(tmem, warp, col_qs(ci), qs);
-                    ld_half32_nowait(tmem, warp, kColPD, pd);
+                    float qs[16], pd[16];
+                    ld_q16(col_qs(ci), qs);
+                    ld_q16(kColPD, pd);
                     tmem_ld_wait();
                     if (mine) {
                         uint4* dst = reinterpret_cast<uint4*>(
-                            p.out + ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
+                            p.out + ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
+                        for (int j = 0; j < 2; ++j) {
                             uint32_t w4[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -518,21 +546,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) { aborted = true; break; }
             }
         } else {
-            // half a dO row of this slice (row hrow of the chunk, columns
-            // 32*hf.. of the slice), packed bf16; the next chunk's half row is
+            // a quarter dO row of this slice (row hrow of the chunk, columns
+            // cq .. cq + 15 of the slice), packed bf16; the next chunk's is
             // fetched as soon as the current one is consumed
-            const int hrow = m64_half_row(warp, lane), hf = lane >> 4;
-            uint4 oraw[4];
+            uint4 oraw[2];
             auto load_do = [&](int it) {
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) oraw[ch] = make_uint4(0, 0, 0, 0);
+                oraw[0] = oraw[1] = make_uint4(0, 0, 0, 0);
                 if (it >= nchunks) return;
                 const int cc0 = t0 + chunk_of(it) * kChunk;
                 if (hrow < min(kChunk, t1 - cc0)) {
                     const uint4* src = reinterpret_cast<const uint4*>(
-                        p.d_out + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * hf);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) oraw[ch] = src[ch];
+                        p.d_out + ((row_base + cc0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
+                    oraw[0] = src[0];
+                    oraw[1] = src[1];
                 }
             };
             load_do(0);
@@ -551,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.chunk_states && t == 0) store_state_tiles(ci);
                 // dO tile (single buffer: the previous chunk's P^T dO has completed)
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4*>(dOt + sw128_offset(hrow, (4 * hf + ch) * 16)) = oraw[ch];
+                for (int ch = 0; ch < 2; ++ch)
+                    *reinterpret_cast<uint4*>(dOt + sw128_offset(hrow, ((cq >> 3) + ch) * 16)) = oraw[ch];
                 fence_proxy_async_smem();
                 // K/Q tiles of this chunk
                 if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
@@ -603,13 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
                 {
-                    float row[32];
+                    float row[16];
                     const float gi = scale * gam[hrow];  // dO rows beyond the chunk are zero
+                    unpack8(oraw[0], row);
+                    unpack8(oraw[1], row + 8);
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) unpack8(oraw[ch], row + ch * 8);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) row[c] *= gi;
-                    store_split_half(Dhi, Dlo, hrow, hf, row);
+                    for (int c = 0; c < 16; ++c) row[c] *= gi;
+                    store_q16(Dhi, Dlo, hrow, row);
                 }
                 fence_proxy_async_smem();
                 load_do(it + 1);
@@ -641,13 +667,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
                     const float dj = dec[hrow];
-                    float kds[32], pdo[32];
-                    ld_half32_nowait(tmem, warp, kColKS, kds);
-                    ld_half32_nowait(tmem, warp, kColQS, pdo);
+                    float kds[16], pdo[16];
+                    ld_q16(kColKS, kds);
+                    ld_q16(kColQS, pdo);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
-                    store_split_half(Rhi, Rlo, hrow, hf, kds);
+                    for (int c = 0; c < 16; ++c) kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
+                    store_q16(Rhi, Rlo, hrow, kds);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -682,12 +708,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C4: X = -beta gam o dBhat -> R tiles (dDelta consumed) ----
                 {
-                    float row[32];
-                    ld_half32(tmem, warp, kColD, row);
+                    float row[16];
+                    ld_q16(kColD, row);
+                    tmem_ld_wait();
                     const float f = -bv[hrow] * gam[hrow];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) row[c] *= f;
-                    store_split_half(Rhi, Rlo, hrow, hf, row);
+                    for (int c = 0; c < 16; ++c) row[c] *= f;
+                    store_q16(Rhi, Rlo, hrow, row);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -728,12 +755,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C6: dS <- gam_n dS + (K^T X + Q^T G) ----
                 {
-                    float row[64];
+                    float row[32];
                     const float gC = gam[63];
-                    ld_row64(tmem, warp, kColS, row);
+                    ld_s32(kColS, row);
 #pragma unroll
-                    for (int c = 0; c < kVs; ++c) S[c] = fmaf(gC, S[c], row[c]);
-                    store_split_row(Shi, Slo, t, S);
+                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                    store_split_half(Shi, Slo, srow_all, hs, S);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -759,15 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
             }
         } else if (p.state_out && srow >= 0) {
-            float* dst = p.state_out + state_off + static_cast<long long>(srow) * V;
+            float* dst = p.state_out + state_off + static_cast<long long>(srow) * V + 32 * hs;
 #pragma unroll
-            for (int j = 0; j < kVs; j += 4)
+            for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     } else {
         // ======================= prep warpgroup =======================
-        const int q = tid - 128;          // 0..127
-        const int sub = warp - 4;         // TMEM subpartition
+        const int q = tid - kChainThreads;  // 0..127
+        const int sub = warp - 8;           // TMEM subpartition
         float* At = reinterpret_cast<float*>(sm + oA);  // A^T, row stride 64
         float* T00 = reinterpret_cast<float*>(sm + oTf);  // row-major 32x32 blocks of T
         float* T11 = T00 + kTB;
@@ -831,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // gram K K^T and Q K^T (two M = 64 products), running while the
             // gates are formed
-            if (warp == 4) {
+            if (warp == 8) {
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
@@ -1060,7 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (q == 0 && tcopy_out) mbar_wait(bar(B_TCOPY), tcopy_it & 1, wl);  // no copy outlives the CTA
         if (aborted) {
-            if (warp == 4) {
+            if (warp == 8) {
                 if (elect_one()) mma_commit(bar(B_DRAIN1));
                 __syncwarp();
             }
