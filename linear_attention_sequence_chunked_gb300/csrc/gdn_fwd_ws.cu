@@ -55,7 +55,8 @@ using namespace tc;
 
 constexpr int kChainThreads = 256;  // warps 0-7
 constexpr int kPrepThreads = 128;   // warps 8-11
-constexpr int kThreads = kChainThreads + kPrepThreads;
+constexpr int kIssuerWarp = 12;     // forward output: MMAs off the chain's critical path
+constexpr int kThreads = kChainThreads + kPrepThreads + 32;
 constexpr int kVs = 64;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
@@ -90,7 +91,7 @@ constexpr int kTB = 32 * kTS;                       // floats per block
 constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
-constexpr int kBars = 17;
+constexpr int kBars = 21;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 // backward: the dO tile [i][v] bf16 shares the R tiles' space (dead between
@@ -102,11 +103,11 @@ static_assert(kAlloc <= 232448, "shared memory");
 enum {
     B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
     B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_TCOPY = 11,
-    B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16
+    B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16,
+    // forward output: warp 0 has issued K S / T R / the state update of a
+    // chunk (the issuer warp queues Q S and P Delta behind them); Q S done
+    B_KSI = 17, B_TRI = 18, B_SI = 19, B_QSD = 20
 };
-// named barrier 3 (warps 0 and 1): warp 0 has issued the MMAs on the chain's
-// critical path; warp 1 then queues the off-path ones (Q S, P Delta) behind them
-constexpr int kBarHandoff = 3;
 
 __device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, id == 1 ? kChainThreads : kPrepThreads); }
 
@@ -295,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Q S goes to one of two column blocks by chunk parity: the output
             // of chunk c reads its block while chunk c+1's Q S is computed
             auto col_qs = [](int cj) { return (cj & 1) ? kColQS2 : kColQS; };
-            // C1 of chunk cj, K S (warp 0, stage cj full) and Q S (warp 1,
-            // queued behind K S; completion tracked by warp 1's P Delta commit)
+            // C1 of chunk cj: K S (warp 0, stage cj full); Q S follows from the
+            // issuer warp, queued behind it
             auto issue_ks = [&](int cj) {
                 const uint32_t stage_c = smem_u32(sm + oStage + (cj & 1) * kStageBytes);
                 tc_fence_after();
@@ -312,40 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar(B_KS));
             };
-            auto issue_qs = [&](int cj) {
-                const uint32_t stage_c = smem_u32(sm + oStage + (cj & 1) * kStageBytes);
-                tc_fence_after();
-                constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
-                const uint32_t cq = col_qs(cj);
-#pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                    const uint64_t a_q = desc_sw128(stage_c + koff + 64 * 128, 0, 1024);
-                    const uint64_t b_hi = desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024);
-                    const uint64_t b_lo = desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024);
-                    mma_bf16(tmem + cq, a_q, b_hi, id_s, s > 0);
-                    mma_bf16(tmem + cq, a_q, b_lo, id_s, 1);
-                }
-            };
-            // warp 0 issues K S of chunk cj once its stage is full, then hands
-            // off to warp 1 for Q S (the handoff happens even on a timeout, so
-            // warp 1 never waits on a barrier warp 0 skipped)
+            // warp 0 issues K S of chunk cj once its stage is full
             auto issue_c1 = [&](int cj) {
                 if (warp == 0) {
                     const bool full = __all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + (cj & 1)), (cj >> 1) & 1, wl));
                     if (full) {
-                        if (elect_one()) issue_ks(cj);
+                        if (elect_one()) {
+                            issue_ks(cj);
+                            if (want_out) mbar_arrive(bar(B_KSI));
+                        }
                         __syncwarp();
                         tma_done = cj + 1;
                     } else if (lane == 0) {
                         *abort_flag = 1;
-                    }
-                    named_bar_arrive(kBarHandoff, 64);
-                } else if (warp == 1) {
-                    tc::named_bar(kBarHandoff, 64);
-                    if (want_out && !*abort_flag) {
-                        if (elect_one()) issue_qs(cj);
-                        __syncwarp();
                     }
                 }
             };
@@ -416,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColD, tl, rh, id, 1);
                         }
                         mma_commit(bar(B_D));
+                        if (want_out) mbar_arrive(bar(B_TRI));
                     }
                     __syncwarp();
                 }
@@ -440,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar(1);
 
-                // ---- C5: S update (warp 0) and P Delta (warp 1, behind it) ----
+                // ---- C5: S update (warp 0); P Delta follows from the issuer warp ----
                 if (warp == 0) {
                     if (elect_one()) {
                         tc_fence_after();
@@ -454,34 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColS, ak, rl, id_s, 1);
                         }
                         mma_commit(bar(B_S));
-                    }
-                    __syncwarp();
-                    named_bar_arrive(kBarHandoff, 64);
-                } else if (warp == 1) {
-                    tc::named_bar(kBarHandoff, 64);
-                    if (elect_one()) {
-                        tc_fence_after();
-                        constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
-                        if (want_out) {
-#pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const uint64_t ph_ = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 32, 0, 1024);
-                                const uint64_t pl_ = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 32, 0, 1024);
-                                const uint64_t dh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                                const uint64_t dl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                                mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
-                                mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
-                                mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
-                            }
-                        }
-                        mma_commit(bar(B_PD));
+                        if (want_out) mbar_arrive(bar(B_SI));
                     }
                     __syncwarp();
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
+                // C6 overwrites the S tiles: Q S (issuer warp) has read them
+                if (want_out && !mbar_wait(bar(B_QSD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
-                if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
+                if (p.chunk_states && t == 0) bulk_wait_read_all();  // ... and so have the bulk copies
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
 
@@ -503,10 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_c1(ci + 1);
                 }
                 __syncwarp();
-                if (!mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
+                if (want_out && !mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
                 // every MMA that reads this chunk's K/Q stage has completed: K S,
-                // the state update (warp 0) and Q S (warp 1, tracked by P Delta)
+                // the state update (warp 0) and Q S (issuer warp, tracked by P Delta)
                 if (t == 0 && !*abort_flag) {
                     if (use_tma) {
                         if (ci + kStages < nchunks) {
@@ -774,14 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 0) {
                 if (elect_one()) mma_commit(bar(B_DRAIN0));
                 __syncwarp();
-            } else if (warp == 1) {
-                if (elect_one()) mma_commit(bar(B_DRAIN2));
-                __syncwarp();
             }
             if (t == 0) {
                 record_error(p.err, kErrTimeout);
                 mbar_wait(bar(B_DRAIN0), 0, wl);
-                mbar_wait(bar(B_DRAIN2), 0, wl);
                 for (int ci = tma_done; ci < tma_issued; ++ci)
                     mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
             }
@@ -791,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
-    } else {
+    } else if (warp < 8 + kPrepThreads / 32) {
         // ======================= prep warpgroup =======================
         const int q = tid - kChainThreads;  // 0..127
         const int sub = warp - 8;           // TMEM subpartition
@@ -1094,6 +1053,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 0) {
                 record_error(p.err, kErrTimeout);
                 mbar_wait(bar(B_DRAIN1), 0, wl);
+            }
+        }
+    } else if (warp == kIssuerWarp) {
+        // ============ off-path MMAs of the forward output (issuer warp) ============
+        // Q S and P Delta are needed only by the output epilogue.  tcgen05
+        // issue blocks at the tensor pipe's rate, so this warp, which has no
+        // epilogue work, queues them behind warp 0's critical products: the
+        // first half of Q S (key columns 0-63) behind K S, the second half
+        // behind T R, P Delta behind the state update.
+        if constexpr (!kBwd) {
+            if (want_out && nchunks > 0) {
+                const uint32_t shi = smem_u32(sm + oShi), slo = smem_u32(sm + oSlo);
+                const uint32_t dhi = smem_u32(sm + oDhi), dlo = smem_u32(sm + oDlo);
+                bool ok = true;
+                for (int ci = 0; ci < nchunks && ok; ++ci) {
+                    const uint32_t ph = ci & 1;
+                    const int slot = ci & 1;
+                    const uint32_t stage_c = smem_u32(sm + oStage + (ci & 1) * kStageBytes);
+                    const uint32_t cq = (ci & 1) ? kColQS2 : kColQS;
+                    constexpr uint32_t id_s = idesc(kFmtBf16, 0, 1, 64, 64);
+                    auto qs_steps = [&](int s0, int s1) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int s = s0; s < s1; ++s) {
+                            const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                            const uint64_t a_q = desc_sw128(stage_c + koff + 64 * 128, 0, 1024);
+                            mma_bf16(tmem + cq, a_q, desc_sw128(shi + s * 2048, kTileS, 1024), id_s, s > 0);
+                            mma_bf16(tmem + cq, a_q, desc_sw128(slo + s * 2048, kTileS, 1024), id_s, 1);
+                        }
+                    };
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KSI), ph, wl));
+                    if (!ok) break;
+                    if (elect_one()) qs_steps(0, kDk / 32);
+                    __syncwarp();
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_TRI), ph, wl));
+                    if (!ok) break;
+                    if (elect_one()) {
+                        qs_steps(kDk / 32, kDk / 16);
+                        mma_commit(bar(B_QSD));
+                    }
+                    __syncwarp();
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SI), ph, wl));
+                    if (!ok) break;
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_p = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ph_ = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 32, 0, 1024);
+                            const uint64_t pl_ = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 32, 0, 1024);
+                            const uint64_t dh = desc_sw128(dhi + s * 2048, kTile64, 1024);
+                            const uint64_t dl = desc_sw128(dlo + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColPD, ph_, dh, id_p, s > 0);
+                            mma_bf16(tmem + kColPD, ph_, dl, id_p, 1);
+                            mma_bf16(tmem + kColPD, pl_, dh, id_p, 1);
+                        }
+                        mma_commit(bar(B_PD));
+                    }
+                    __syncwarp();
+                }
+                if (!ok && lane == 0) *abort_flag = 1;  // the chain records the timeout
+                // nothing this warp issued is in flight when the CTA frees its TMEM
+                if (elect_one()) mma_commit(bar(B_DRAIN2));
+                __syncwarp();
+                mbar_wait(bar(B_DRAIN2), 0, wl);
             }
         }
     }
