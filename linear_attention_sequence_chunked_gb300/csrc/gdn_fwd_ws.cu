@@ -105,8 +105,10 @@ enum {
     B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_TCOPY = 11,
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16,
     // forward output: warp 0 has issued K S / T R / the state update of a
-    // chunk (the issuer warp queues Q S and P Delta behind them); Q S done
-    B_KSI = 17, B_TRI = 18, B_SI = 19, B_QSD = 20
+    // chunk (the issuer warp queues Q S and P Delta behind them); Q S done.
+    // Backward: warp 0 has issued K dS (the issuer queues P^T dO behind it),
+    // the G tile is written (the issuer issues Q^T G), Q^T G done.
+    B_KSI = 17, B_TRI = 18, B_SI = 19, B_QSD = 20, B_GI = B_TRI
 };
 
 __device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, id == 1 ? kChainThreads : kPrepThreads); }
@@ -564,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColKS, a_k, b_lo, id_s, 1);
                         }
                         mma_commit(bar(B_KS));
+                        mbar_arrive(bar(B_KSI));
                     }
                     __syncwarp();
                 }
@@ -573,23 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
 
-                // ---- P^T dO (A = P tile read MN-major) ----
-                if (warp == 0) {
-                    if (elect_one()) {
-                        tc_fence_after();
-                        constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t p_hi = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 2048, kTile64, 1024);
-                            const uint64_t p_lo = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 2048, kTile64, 1024);
-                            const uint64_t b_o = desc_sw128(smem_u32(dOt) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
-                            mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
-                        }
-                        mma_commit(bar(B_PD));
-                    }
-                    __syncwarp();
-                }
+                // P^T dO comes from the issuer warp (behind K dS, once P is in)
                 // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
                 {
                     float row[16];
@@ -609,21 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
-                // Q^T G starts the state-gradient product now (A = Q^T read
-                // MN-major from the stage); it runs under the dDelta epilogue
+                // the G tile is in: the issuer warp starts the state-gradient
+                // product with Q^T G, which runs under the dDelta epilogue
                 if (warp == 0) {
-                    if (elect_one()) {
-                        tc_fence_after();
-                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t aq = desc_sw128(stage_a + 64 * 128 + s * 2048, kRegionBytes, 1024);
-                            const uint64_t gh = desc_sw128(smem_u32(Dhi) + s * 2048, kTile64, 1024);
-                            const uint64_t gl = desc_sw128(smem_u32(Dlo) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColS, aq, gh, id, s > 0);
-                            mma_bf16(tmem + kColS, aq, gl, id, 1);
-                        }
-                    }
+                    if (elect_one()) mbar_arrive(bar(B_GI));
                     __syncwarp();
                 }
 
@@ -685,7 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C5: K^T X added to Q^T G (A = K^T read MN-major from the stage) ----
                 if (warp == 0) {
-                    if (elect_one()) {
+                    // Q^T G (issuer warp) has completed: K^T X accumulates onto it
+                    const bool qg = __all_sync(0xffffffffu, mbar_wait(bar(B_QSD), ph, wl));
+                    if (!qg && lane == 0) *abort_flag = 1;
+                    if (qg && elect_one()) {
                         tc_fence_after();
                         constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
 #pragma unroll
@@ -1062,7 +1041,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue work, queues them behind warp 0's critical products: the
         // first half of Q S (key columns 0-63) behind K S, the second half
         // behind T R, P Delta behind the state update.
-        if constexpr (!kBwd) {
+        if constexpr (kBwd) {
+            // backward: P^T dO (A = P tile read MN-major) behind K dS once the
+            // prep's P tiles are in; Q^T G (A = Q^T read MN-major from the
+            // stage) once the chain has written the G tile
+            if (nchunks > 0) {
+                const uint32_t dot = smem_u32(sm + oRhi), dhi = smem_u32(sm + oDhi), dlo = smem_u32(sm + oDlo);
+                bool ok = true;
+                for (int it = 0; it < nchunks && ok; ++it) {
+                    const uint32_t ph = it & 1, ph2 = (it >> 1) & 1;
+                    const int slot = it & 1;
+                    const uint32_t stage_c = smem_u32(sm + oStage + (it & 1) * kStageBytes);
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KSI), ph, wl) && mbar_wait(bar(B_READY0 + slot), ph2, wl));
+                    if (!ok) break;
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t p_hi = desc_sw128(smem_u32(sm + oP + (2 * slot) * kTile64) + s * 2048, kTile64, 1024);
+                            const uint64_t p_lo = desc_sw128(smem_u32(sm + oP + (2 * slot + 1) * kTile64) + s * 2048, kTile64, 1024);
+                            const uint64_t b_o = desc_sw128(dot + s * 2048, kTile64, 1024);
+                            mma_bf16(tmem + kColQS, p_hi, b_o, id_p, s > 0);
+                            mma_bf16(tmem + kColQS, p_lo, b_o, id_p, 1);
+                        }
+                        mma_commit(bar(B_PD));
+                    }
+                    __syncwarp();
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_GI), ph, wl));
+                    if (!ok) break;
+                    if (elect_one()) {
+                        tc_fence_after();
+                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t aq = desc_sw128(stage_c + 64 * 128 + s * 2048, kRegionBytes, 1024);
+                            mma_bf16(tmem + kColS, aq, desc_sw128(dhi + s * 2048, kTile64, 1024), id, s > 0);
+                            mma_bf16(tmem + kColS, aq, desc_sw128(dlo + s * 2048, kTile64, 1024), id, 1);
+                        }
+                        mma_commit(bar(B_QSD));
+                    }
+                    __syncwarp();
+                }
+                if (!ok && lane == 0) *abort_flag = 1;  // the chain records the timeout
+                if (elect_one()) mma_commit(bar(B_DRAIN2));
+                __syncwarp();
+                mbar_wait(bar(B_DRAIN2), 0, wl);
+            }
+        } else {
             if (want_out && nchunks > 0) {
                 const uint32_t shi = smem_u32(sm + oShi), slo = smem_u32(sm + oSlo);
                 const uint32_t dhi = smem_u32(sm + oDhi), dlo = smem_u32(sm + oDlo);
