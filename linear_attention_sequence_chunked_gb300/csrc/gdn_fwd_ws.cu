@@ -91,7 +91,7 @@ constexpr int kTB = 32 * kTS;                       // floats per block
 constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
-constexpr int kBars = 21;
+constexpr int kBars = 19;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 // backward: the dO tile [i][v] bf16 shares the R tiles' space (dead between
@@ -104,11 +104,9 @@ enum {
     B_FULL0 = 0, B_FULL1 = 1, B_GRAM = 2, B_KS = 3, B_D = 4, B_S = 5, B_PD = 6,
     B_READY0 = 7, B_READY1 = 8, B_TFREE0 = 9, B_TFREE1 = 10, B_TCOPY = 11,
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16,
-    // forward output: warp 0 has issued K S / T R / the state update of a
-    // chunk (the issuer warp queues Q S and P Delta behind them); Q S done.
-    // Backward: warp 0 has issued K dS (the issuer queues P^T dO behind it),
-    // the G tile is written (the issuer issues Q^T G), Q^T G done.
-    B_KSI = 17, B_TRI = 18, B_SI = 19, B_QSD = 20, B_GI = B_TRI
+    // backward: warp 0 has issued K dS (the issuer warp issues P^T dO with
+    // it); forward: Q S done; backward: Q^T G done
+    B_KSI = 17, B_QSD = 18
 };
 
 __device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, id == 1 ? kChainThreads : kPrepThreads); }
@@ -320,10 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (warp == 0) {
                     const bool full = __all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + (cj & 1)), (cj >> 1) & 1, wl));
                     if (full) {
-                        if (elect_one()) {
-                            issue_ks(cj);
-                            if (want_out) mbar_arrive(bar(B_KSI));
-                        }
+                        if (elect_one()) issue_ks(cj);
                         __syncwarp();
                         tma_done = cj + 1;
                     } else if (lane == 0) {
@@ -398,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColD, tl, rh, id, 1);
                         }
                         mma_commit(bar(B_D));
-                        if (want_out) mbar_arrive(bar(B_TRI));
                     }
                     __syncwarp();
                 }
@@ -437,7 +431,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + kColS, ak, rl, id_s, 1);
                         }
                         mma_commit(bar(B_S));
-                        if (want_out) mbar_arrive(bar(B_SI));
                     }
                     __syncwarp();
                 }
@@ -596,12 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
-                // the G tile is in: the issuer warp starts the state-gradient
-                // product with Q^T G, which runs under the dDelta epilogue
-                if (warp == 0) {
-                    if (elect_one()) mbar_arrive(bar(B_GI));
-                    __syncwarp();
-                }
 
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
@@ -659,12 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar(1);
 
-                // ---- C5: K^T X added to Q^T G (A = K^T read MN-major from the stage) ----
+                // ---- C5: K^T X (A = K^T read MN-major from the stage); Q^T G comes from the issuer warp ----
                 if (warp == 0) {
-                    // Q^T G (issuer warp) has completed: K^T X accumulates onto it
-                    const bool qg = __all_sync(0xffffffffu, mbar_wait(bar(B_QSD), ph, wl));
-                    if (!qg && lane == 0) *abort_flag = 1;
-                    if (qg && elect_one()) {
+                    if (elect_one()) {
                         tc_fence_after();
                         constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
 #pragma unroll
@@ -672,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
                             const uint64_t xh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
                             const uint64_t xl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColS, ak, xh, id, 1);
+                            mma_bf16(tmem + kColS, ak, xh, id, s > 0);
                             mma_bf16(tmem + kColS, ak, xl, id, 1);
                         }
                         mma_commit(bar(B_S));
@@ -681,6 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
+                // Q^T G (issuer warp, its own TMEM block) has completed too
+                if (!mbar_wait(bar(B_QSD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
                 named_bar(1);
@@ -697,11 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ---- C6: dS <- gam_n dS + (K^T X + Q^T G) ----
                 {
-                    float row[32];
+                    float row[32], qg[32];
                     const float gC = gam[63];
                     ld_s32(kColS, row);
+                    ld_s32(kColG, qg);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c] + qg[c]);
                     store_split_half(Shi, Slo, srow_all, hs, S);
                 }
                 fence_proxy_async_smem();
@@ -1036,15 +1023,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kIssuerWarp) {
         // ============ off-path MMAs of the forward output (issuer warp) ============
-        // Q S and P Delta are needed only by the output epilogue.  tcgen05
-        // issue blocks at the tensor pipe's rate, so this warp, which has no
-        // epilogue work, queues them behind warp 0's critical products: the
-        // first half of Q S (key columns 0-63) behind K S, the second half
-        // behind T R, P Delta behind the state update.
+        // Q S and P Delta are needed only by the output epilogue, and the
+        // tensor pipe shares its time between MMAs of different issuing
+        // threads, so this warp (no epilogue work of its own) issues them
+        // only once warp 0's critical product has completed, into the
+        // epilogue that follows it: the first half of Q S (key columns 0-63)
+        // after K S, the second half after T R, P Delta after the state
+        // update.
         if constexpr (kBwd) {
-            // backward: P^T dO (A = P tile read MN-major) behind K dS once the
-            // prep's P tiles are in; Q^T G (A = Q^T read MN-major from the
-            // stage) once the chain has written the G tile
+            // backward: P^T dO (A = P tile read MN-major) with K dS once the
+            // prep's P tiles are in (dDelta needs both); Q^T G (A = Q^T read
+            // MN-major from the stage) once T^T dDelta has completed
             if (nchunks > 0) {
                 const uint32_t dot = smem_u32(sm + oRhi), dhi = smem_u32(sm + oDhi), dlo = smem_u32(sm + oDlo);
                 bool ok = true;
@@ -1068,7 +1057,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(bar(B_PD));
                     }
                     __syncwarp();
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_GI), ph, wl));
+                    // Q^T G into its own TMEM block (the K K^T block, free when T
+                    // comes from the chunk-parallel kernel), in the X epilogue's
+                    // window: after T^T dDelta has completed
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_D), ph, wl));
                     if (!ok) break;
                     if (elect_one()) {
                         tc_fence_after();
@@ -1076,8 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t aq = desc_sw128(stage_c + 64 * 128 + s * 2048, kRegionBytes, 1024);
-                            mma_bf16(tmem + kColS, aq, desc_sw128(dhi + s * 2048, kTile64, 1024), id, s > 0);
-                            mma_bf16(tmem + kColS, aq, desc_sw128(dlo + s * 2048, kTile64, 1024), id, 1);
+                            mma_bf16(tmem + kColG, aq, desc_sw128(dhi + s * 2048, kTile64, 1024), id, s > 0);
+                            mma_bf16(tmem + kColG, aq, desc_sw128(dlo + s * 2048, kTile64, 1024), id, 1);
                         }
                         mma_commit(bar(B_QSD));
                     }
@@ -1109,18 +1101,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + cq, a_q, desc_sw128(slo + s * 2048, kTileS, 1024), id_s, 1);
                         }
                     };
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KSI), ph, wl));
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KS), ph, wl));
                     if (!ok) break;
                     if (elect_one()) qs_steps(0, kDk / 32);
                     __syncwarp();
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_TRI), ph, wl));
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_D), ph, wl));
                     if (!ok) break;
                     if (elect_one()) {
                         qs_steps(kDk / 32, kDk / 16);
                         mma_commit(bar(B_QSD));
                     }
                     __syncwarp();
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SI), ph, wl));
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S), ph, wl));
                     if (!ok) break;
                     if (elect_one()) {
                         tc_fence_after();
@@ -1183,6 +1175,9 @@ cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t st
 }
 
 cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    // the backward chain takes T from the chunk-parallel kernel: its Q^T G
+    // product uses the TMEM block that the in-place K K^T would occupy
+    if (a.T > 0 && a.chunk_T == nullptr) return cudaErrorInvalidValue;
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = nullptr; c.d_out = a.d_out; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.d_final_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.state_out = a.d_initial_state;
