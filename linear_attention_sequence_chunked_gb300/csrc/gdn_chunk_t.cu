@@ -216,24 +216,43 @@ __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTAr
     }
     __syncthreads();
     {
-        // lower-left 16x16 block of T_bb (b = q / 64): X = A_10 T_00 (16x16
-        // blocks of the 32x32 diagonal block), thread q: row r, columns c4 .. c4 + 3
+        // lower-left 16x16 block of T_bb (b = 0, 1): X = A_10 T_00 (16x16
+        // blocks of the 32x32 diagonal block); threads q < 32 take a 4x4 block
+        // of X (block b = q / 16, rows r4 .. r4 + 3, columns c4 .. c4 + 3):
+        // per k one 16-byte load of A_10's column and one of T_00's row
+        if (q < 32) {
+            const int b4 = q >> 4, r4 = ((q >> 2) & 3) * 4, c4 = (q & 3) * 4;
+            const float* tb = b4 ? T11 : T00;
+            const int o = 32 * b4;
+            float acc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float4 a4 = *reinterpret_cast<const float4*>(At + (o + k) * 64 + o + 16 + r4);
+                const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[i][0] = fmaf(av[i], t4.x, acc[i][0]); acc[i][1] = fmaf(av[i], t4.y, acc[i][1]);
+                    acc[i][2] = fmaf(av[i], t4.z, acc[i][2]); acc[i][3] = fmaf(av[i], t4.w, acc[i][3]);
+                }
+            }
+            float* xs4 = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(xs4 + (r4 + i) * 64 + c4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
+        __syncthreads();
+        // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower
+        // triangular), block b = q / 64, thread q: row r, columns c4 .. c4 + 3
         const int bb = q >> 6, r = (q >> 2) & 15, c4 = (q & 3) * 4;
         float* tb = bb ? T11 : T00;
         const int o = 32 * bb;  // first row/column of the 32x32 block in A
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float a = At[(o + k) * 64 + o + 16 + r];
-            const float4 t4 = *reinterpret_cast<const float4*>(tb + k * kTS + c4);
-            acc.x = fmaf(a, t4.x, acc.x); acc.y = fmaf(a, t4.y, acc.y);
-            acc.z = fmaf(a, t4.z, acc.z); acc.w = fmaf(a, t4.w, acc.w);
-        }
-        float* xs = At + (o + 16) * 64 + o;  // upper triangle of A^T: free
-        *reinterpret_cast<float4*>(xs + r * 64 + c4) = acc;
-        __syncthreads();
-        // T_10 = -T_11 X (T_11 the lower-right 16x16 block, unit lower triangular)
-        acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
+        float* xs = At + (o + 16) * 64 + o;
+        float4 acc = *reinterpret_cast<const float4*>(xs + r * 64 + c4);
 #pragma unroll 4
         for (int k = 0; k < r; ++k) {
             const float a = tb[(16 + r) * kTS + 16 + k];
@@ -245,27 +264,38 @@ __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTAr
     }
     __syncthreads();
     {
-        // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), thread q:
-        // row r = q / 4, columns c8 .. c8 + 7
+        // T_10 of the 64x64 matrix: X = A_10 T_00 (32x32 blocks), threads
+        // q < 64 take a 4x4 block (rows r4 .. r4 + 3, columns c4 .. c4 + 3):
+        // per k one 16-byte load of A_10's column (contiguous in A^T) and one
+        // of T_00's row for 16 FMAs; each element sums over k in order
+        float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
+        if (q < 64) {
+            const int r4 = (q >> 3) * 4, c4 = (q & 7) * 4;
+            float acc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float4 a4 = *reinterpret_cast<const float4*>(At + k * 64 + 32 + r4);
+                const float4 t4 = *reinterpret_cast<const float4*>(T00 + k * kTS + c4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[i][0] = fmaf(av[i], t4.x, acc[i][0]); acc[i][1] = fmaf(av[i], t4.y, acc[i][1]);
+                    acc[i][2] = fmaf(av[i], t4.z, acc[i][2]); acc[i][3] = fmaf(av[i], t4.w, acc[i][3]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(xs + (r4 + i) * 64 + c4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
+        __syncthreads();
+        // T_10 = -T_11 X (T_11 unit lower triangular), thread q: row r = q / 4,
+        // columns c8 .. c8 + 7
         const int r = q >> 2, c8 = (q & 3) * 8;
         float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const float a = At[k * 64 + 32 + r];
-            const float4 t0v = *reinterpret_cast<const float4*>(T00 + k * kTS + c8);
-            const float4 t1v = *reinterpret_cast<const float4*>(T00 + k * kTS + c8 + 4);
-            acc[0] = fmaf(a, t0v.x, acc[0]); acc[1] = fmaf(a, t0v.y, acc[1]);
-            acc[2] = fmaf(a, t0v.z, acc[2]); acc[3] = fmaf(a, t0v.w, acc[3]);
-            acc[4] = fmaf(a, t1v.x, acc[4]); acc[5] = fmaf(a, t1v.y, acc[5]);
-            acc[6] = fmaf(a, t1v.z, acc[6]); acc[7] = fmaf(a, t1v.w, acc[7]);
-        }
-        float* xs = At + 32 * 64;  // rows 32-63, columns 0-31 of A^T: free
-        *reinterpret_cast<float4*>(xs + r * 64 + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4*>(xs + r * 64 + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        __syncthreads();
-        // T_10 = -T_11 X (T_11 unit lower triangular)
         const float4 u0 = *reinterpret_cast<const float4*>(xs + r * 64 + c8);
         const float4 u1 = *reinterpret_cast<const float4*>(xs + r * 64 + c8 + 4);
         acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
