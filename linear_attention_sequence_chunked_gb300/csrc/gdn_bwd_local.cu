@@ -116,10 +116,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a sequence's end (and sequences whose bounds are invalid)
     const int maxc = p.max_chunks;
     const long long total = static_cast<long long>(maxc) * H * p.N;
+    // (item counts stay far below 2^32: 32-bit division)
     auto decode = [&](long long f, Item& it) -> bool {
-        it.ci = static_cast<int>(f % maxc);
-        it.h = static_cast<int>((f / maxc) % H);
-        it.n = static_cast<int>(f / (static_cast<long long>(maxc) * H));
+        const uint32_t fu = static_cast<uint32_t>(f), mc = static_cast<uint32_t>(maxc);
+        const uint32_t ch = fu / mc;
+        it.ci = static_cast<int>(fu - ch * mc);
+        it.h = static_cast<int>(ch % static_cast<uint32_t>(H));
+        it.n = static_cast<int>(ch / static_cast<uint32_t>(H));
         if (!seq_range(p.cu_seqlens, it.n, p.N, p.T, p.err, it.b, it.t0, it.t1)) return false;
         return it.ci < (it.t1 - it.t0 + kChunk - 1) / kChunk;
     };
@@ -610,6 +613,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, yh, sal, id_n, 1);
                         mma_bf16(tmem + cdK, yl, sah, id_n, 1);
                     }
+                    if (vs + 1 == nsl) {
+                        // chunk-wide part: K K^T and Q K^T (M = 64 each) into the
+                        // scratch columns, queued behind the last slice's products
+                        constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
+#pragma unroll
+                        for (int s = 0; s < kDk / 16; ++s) {
+                            mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
+                            mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
+                        }
+                    }
                 }
                 __syncwarp();
             }
@@ -623,35 +636,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- the next item's inputs land while this item's chunk-wide part
         // runs: K/Q into the other buffer (RC, RD are dead), T, slice 0 states
+        // (issued below, after the first chunk-wide products)
         Item nxt{};
         const long long fn = next_valid(f + gridDim.x, nxt);
-        if (fn < total) {
-            if (tid == 0 && !failed) {
-                issue_inputs(nxt, smem_u32(sm + oRC));
-                issue_s0(nxt, 0);
-                issue_ds(nxt, 0);
-            }
-        }
 
-        // ---- chunk-wide part: re-form K K^T and Q K^T (M = 64 each) ----
-        if (warp == 0) {
-            if (elect_one()) {
-                tc_fence_after();
-                constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
-                for (int s = 0; s < kDk / 16; ++s) {
-                    mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
-                    mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
-                }
-            }
-            __syncwarp();
+        // ---- chunk-wide part (K K^T and Q K^T came with the last slice's batch) ----
+        if (fn < total && tid == 0 && !failed) {
+            issue_inputs(nxt, smem_u32(sm + oRC));
+            issue_s0(nxt, 0);
+            issue_ds(nxt, 0);
         }
-        // gates and the first slice's rows of the next item, while the products run
-        if (fn < total) {
-            fetch_gates(nxt);
-            fetch_rows(nxt, 0);
-        }
-        mma_sync_wait();
         // column-sum terms E [64][64] fp32 in the (dead) P tiles, column index
         // XOR-swizzled by the row so that row-parallel writes and
         // column-parallel reads both spread over the banks
@@ -732,6 +726,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
+        }
+        // gates and the first slice's rows of the next item, while the products run
+        if (fn < total) {
+            fetch_gates(nxt);
+            fetch_rows(nxt, 0);
         }
         mma_sync_wait();
         __syncthreads();

@@ -169,7 +169,15 @@ __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTAr
         const float Gi = Gv[i], bi = bv[i];
         float mdec[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mdec[k] = (j0 + k < i) ? exp_nonpos(Gi - Gv[j0 + k]) : 0.f;
+        for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 g4 = *reinterpret_cast<const float4*>(Gv + j0 + 4 * k4);
+            const float gj[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 4 * k4 + e;
+                mdec[k] = (j0 + k < i) ? exp_nonpos(Gi - gj[e]) : 0.f;
+            }
+        }
         float lo[32];
         ld_half32(tmem, warp, 0, lo);
 #pragma unroll
