@@ -117,6 +117,23 @@ GDN_API gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
                          int B, int T, int H, int d_k, int d_v,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Token-serial forward: the same recurrence and arguments as gdn_chunk_fwd
+ * (without a workspace), applied one token at a time ("Research Sprint Day 1",
+ * section "The GDN update": decay, read v_old = S^T k, write the error
+ * beta (v - v_old) along k, read out scale S^T q), with the fp32 state in
+ * registers.  Meant for decode (a few tokens per call, state carried through
+ * initial_state / final_state) and as a second GPU path for checks; for long
+ * sequences gdn_chunk_fwd is much faster.  Same validation, layouts and error
+ * behaviour as gdn_chunk_fwd; T = 0 copies initial_state (or zeros) to
+ * final_state.
+ */
+GDN_API gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                             const float* g, const gdn_bf16* beta, float scale,
+                             const float* initial_state, const int32_t* cu_seqlens,
+                             gdn_bf16* out, float* final_state,
+                             int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
+
 /* Bytes of device workspace gdn_chunk_bwd needs for these sizes. */
 GDN_API size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
 

@@ -104,6 +104,24 @@ cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStr
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream);
 
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
+
+// Token-serial forward (decode path; the same recurrence token by token).
+struct RecurrentArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const float* g;
+    const uint16_t* beta;
+    float scale;
+    const float* initial_state;   // may be null (zeros)
+    const int32_t* cu_seqlens;
+    uint16_t* out;
+    float* final_state;           // may be null
+    int N, T, H, d_k, d_v;
+    int* err;
+};
+
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream);
 // Warp-specialised tensor-core forward (prep and chain warpgroups);
 // wait_limit bounds every mbarrier wait (polls).
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);

@@ -68,6 +68,8 @@ def load():
         lib.gdn_chunk_fwd.restype = i
         lib.gdn_chunk_bwd.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp, sz, vp]
         lib.gdn_chunk_bwd.restype = i
+        lib.gdn_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
+        lib.gdn_recurrent_fwd.restype = i
         lib.gdn_get_last_device_error.argtypes = [vp]
         lib.gdn_get_last_device_error.restype = i
         lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
@@ -134,6 +136,14 @@ def gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_f
                               _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "gdn_chunk_bwd")
+
+
+def gdn_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                      B, T, H, d_k, d_v, stream=None):
+    st = load().gdn_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                  _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                  _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
+    _check(st, "gdn_recurrent_fwd")
 
 
 def gdn_chunk_bwd_noalloc(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,

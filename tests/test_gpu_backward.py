@@ -47,6 +47,18 @@ def test_varlen_gradients():
         G.compare(res["dS0"][4, h], ref["dS0"][4, h], 1e-6, None, "empty seq")
 
 
+def test_varlen_gradients_dk128_many_items():
+    """Packed sequences at d_k=128 with more (chunk, head) items than SMs: the
+    persistent local-gradient pass walks several items per CTA, including
+    ragged tails read by TMA and empty or one-token sequences."""
+    lens = [1, 63, 65, 0, 3000, 64, 129, 700]
+    wl = W.random_workload(B=1, T=0, H=3, d_k=128, d_v=128, seed=17, seqlens=lens,
+                           initial_state=True, with_grad=True, d_final_state=True)
+    res = G.run_bwd(wl)
+    _check_grads(wl, res, [(s, h) for s in range(len(lens)) for h in range(3) if lens[s] > 0],
+                 "varlen128")
+
+
 def test_config2_shape_gradients_sampled():
     wl = W.make_workload(2, with_grad=True)
     res = G.run_bwd(wl)
