@@ -388,6 +388,9 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, ws_b_n)
 
+    # ---- decode: the token-serial path, one token per call ----
+    decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None
     accuracy = None
@@ -433,6 +436,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "accuracy": accuracy,
+            "decode": decode,
         }
         print(json.dumps(line), flush=True)
     barrier(world)
@@ -470,6 +474,43 @@ def load_traffic():
     if not d.get("sources"):
         return None
     return d.get("bytes_per_launch")
+
+
+def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, steps=50, warmup=5):
+    """gdn_recurrent_fwd one token per call, the state carried between two
+    buffers (decode of B sequences).  Its bytes are dominated by the fp32
+    state read and written per call: 8KV per (sequence, head) + the token's
+    q, k, v, out (bf16), g (fp32), beta (bf16).  At B=256 each state buffer
+    (256 MiB) exceeds L2, so every call reads its state from HBM."""
+    import numpy as np
+    rng = np.random.default_rng(7)
+    q = torch.from_numpy(rng.standard_normal((B, 1, H, K), dtype=np.float32)).to(dev).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.from_numpy(
+        rng.standard_normal((B, 1, H, K), dtype=np.float32)).to(dev), dim=-1).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((B, 1, H, V), dtype=np.float32)).to(dev).to(torch.bfloat16)
+    g = torch.full((B, 1, H), -0.05, dtype=torch.float32, device=dev)
+    beta = torch.full((B, 1, H), 0.5, dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, 1, H, V), dtype=torch.bfloat16, device=dev)
+    st = [torch.zeros((B, H, K, V), dtype=torch.float32, device=dev) for _ in range(2)]
+    scale = K ** -0.5
+    for i in range(warmup):
+        gdn.gdn_recurrent_fwd(q, k, v, g, beta, scale, st[i & 1], None, out, st[1 - (i & 1)],
+                              B, 1, H, K, V, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        gdn.gdn_recurrent_fwd(q, k, v, g, beta, scale, st[i & 1], None, out, st[1 - (i & 1)],
+                              B, 1, H, K, V, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / steps
+    nbytes = B * H * (8 * K * V + 2 * (2 * K + 2 * V) + 4 + 2)
+    return {"config": f"B={B} sequences x H={H}, d_k={K}, d_v={V}, one token per call",
+            "value": B * H / t, "unit": UNIT, "us_per_call": t * 1e6,
+            "roofline": {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": nbytes / t / 1e9 / hbm}}
 
 
 def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, ws_b_n):
@@ -535,6 +576,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
