@@ -43,24 +43,6 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
     return r;
 }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 64 values of one row into
-// the swizzled rows `row` of two 128-byte-wide operand tiles.
-__device__ __forceinline__ void store_split_row(uint8_t* tile_hi, uint8_t* tile_lo, int row, const float* x) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = x[ch * 8 + 2 * e], b = x[ch * 8 + 2 * e + 1];
-            h[e] = cvt_bf16x2(a, b);
-            l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
-        }
-        const uint32_t off = sw128_offset(row, ch * 16);
-        *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-}
-
 // One 16-byte chunk (8 values, columns 8*ch .. 8*ch+7) of a split row.
 __device__ __forceinline__ void store_split_chunk(uint8_t* tile_hi, uint8_t* tile_lo, int row, int ch,
                                                   const float* x8) {
@@ -81,20 +63,6 @@ __device__ __forceinline__ void store_split_half(uint8_t* tile_hi, uint8_t* tile
                                                  const float* x) {
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) store_split_chunk(tile_hi, tile_lo, row, 4 * hf + ch, x + 8 * ch);
-}
-
-// Rows of M = 64 accumulators (cta_group::1): rows 16w..16w+15 sit in lanes
-// 32w..32w+15 of TMEM subpartition w; lanes 16..31 are unused.
-__device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
-
-// 64 fp32 columns of this thread's TMEM lane (subpartition `sub`).
-__device__ __forceinline__ void ld_row64(uint32_t tmem, int sub, uint32_t col, float* v) {
-    const uint32_t a = tmem + (static_cast<uint32_t>(sub * 32) << 16) + col;
-    tmem_ld16(a, v);
-    tmem_ld16(a + 16, v + 16);
-    tmem_ld16(a + 32, v + 32);
-    tmem_ld16(a + 48, v + 48);
-    tmem_ld_wait();
 }
 
 // Half rows of M = 64 accumulators, every lane busy: lane l of warp w holds
