@@ -134,6 +134,48 @@ GDN_API gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const
                              gdn_bf16* out, float* final_state,
                              int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
+/*
+ * Prologue: q/k L2 normalisation and the two gates from their raw inputs
+ * ("Research Sprint Day 2 - Rooflines", GDN layer pseudocode steps 4 and 5),
+ * producing the q, k, g, beta that gdn_chunk_fwd / gdn_chunk_bwd take.
+ *   q_raw, k_raw  (rows, H, d_k) bf16; either may be NULL (then q / k must be
+ *                 NULL too and that tensor is not touched)
+ *   q, k          (rows, H, d_k) bf16 out: x / sqrt(|x|^2 + 1e-6) per row, in fp32, RNE
+ *   a, b          (rows, H) fp32 raw gate inputs
+ *   A_log, dt_bias (H) fp32; dt_bias may be NULL (zeros); A_log is required
+ *                 for gate_mode 1
+ *   gate_mode     1: g = -exp(A_log[h]) softplus(a + dt_bias[h])   (decay gate)
+ *                 2: g = lower sigmoid(a + dt_bias[h])              (bounded gate,
+ *                    fla issue #1550's CP2 test uses lower = -5)
+ *   beta_scale    beta = beta_scale sigmoid(b) (2 allows negative eigenvalues)
+ *   g             (rows, H) fp32 out;  beta (rows, H) bf16 out
+ *   rows          tokens (B * T dense, total T packed);  d_k in {64, 128}
+ * Returns GDN_OK once enqueued; GDN_ERR_INVALID_ARG for a bad mode, missing
+ * pointer or inconsistent q/k pair, GDN_ERR_MISALIGNED for a pointer that is
+ * not 16-byte aligned.
+ */
+GDN_API gdn_status gdn_prologue_fwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a,
+                            const float* b, const float* A_log, const float* dt_bias,
+                            int gate_mode, float lower, float beta_scale, gdn_bf16* q,
+                            gdn_bf16* k, float* g, gdn_bf16* beta, int rows, int H, int d_k,
+                            cudaStream_t stream);
+
+/*
+ * Reverse mode of gdn_prologue_fwd, from the gradients w.r.t. its outputs
+ * (dq, dk, dg, dbeta, as gdn_chunk_bwd returns them): dq_raw, dk_raw (bf16),
+ * da, db (fp32, (rows, H)) and the per-head sums dA_log, ddt_bias (fp32 (H),
+ * each may be NULL; dA_log is not written for gate_mode 2).  With
+ * r = (|x|^2 + 1e-6)^-1/2 and y = r x: dx = r (dy - y (y . dy)).  The per-head
+ * sums run in a fixed order (deterministic).
+ */
+GDN_API gdn_status gdn_prologue_bwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a,
+                            const float* b, const float* A_log, const float* dt_bias,
+                            int gate_mode, float lower, float beta_scale, const gdn_bf16* dq,
+                            const gdn_bf16* dk, const float* dg, const gdn_bf16* dbeta,
+                            gdn_bf16* dq_raw, gdn_bf16* dk_raw, float* da, float* db,
+                            float* dA_log, float* ddt_bias, int rows, int H, int d_k,
+                            cudaStream_t stream);
+
 /* Bytes of device workspace gdn_chunk_bwd needs for these sizes. */
 GDN_API size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
 

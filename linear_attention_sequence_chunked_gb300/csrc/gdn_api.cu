@@ -51,6 +51,15 @@ gdn_status check_shapes(int B, int T, int H, int d_k, int d_v) {
     return GDN_OK;
 }
 
+gdn_status check_prologue(int rows, int H, int d_k, int gate_mode, const float* A_log) {
+    if (rows < 0 || H < 1) return GDN_ERR_INVALID_ARG;
+    if (d_k != 64 && d_k != 128) return GDN_ERR_UNSUPPORTED;
+    if (gate_mode != 1 && gate_mode != 2) return GDN_ERR_INVALID_ARG;
+    if (gate_mode == 1 && !A_log) return GDN_ERR_INVALID_ARG;
+    if (static_cast<long long>(rows) * H * d_k >= (1LL << 40)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
 // Chunk slots of a per-chunk workspace array (see chunk_slot_base).
 long long chunk_slots(int B, int T, int varlen) {
     if (varlen) return static_cast<long long>(T / gdn::kChunk) + B;
@@ -167,6 +176,50 @@ gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
     if (!launched(gdn::launch_recurrent(a, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status gdn_prologue_fwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a, const float* b,
+                            const float* A_log, const float* dt_bias, int gate_mode, float lower,
+                            float beta_scale, gdn_bf16* q, gdn_bf16* k, float* g, gdn_bf16* beta,
+                            int rows, int H, int d_k, cudaStream_t stream) {
+    gdn_status st = check_prologue(rows, H, d_k, gate_mode, A_log);
+    if (st != GDN_OK) return st;
+    if (rows > 0 && (!a || !b || !g || !beta)) return GDN_ERR_INVALID_ARG;
+    if ((q_raw == nullptr) != (q == nullptr) || (k_raw == nullptr) != (k == nullptr)) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q_raw, k_raw, a, b, A_log, dt_bias, q, k, g, beta};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::PrologueArgs pa{};
+    pa.q_raw = q_raw; pa.k_raw = k_raw; pa.a = a; pa.b = b; pa.A_log = A_log; pa.dt_bias = dt_bias;
+    pa.gate_mode = gate_mode; pa.lower = lower; pa.beta_scale = beta_scale;
+    pa.q = q; pa.k = k; pa.g = g; pa.beta = beta; pa.rows = rows; pa.H = H; pa.d_k = d_k;
+    if (!launched(gdn::launch_prologue_fwd(pa, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status gdn_prologue_bwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a, const float* b,
+                            const float* A_log, const float* dt_bias, int gate_mode, float lower,
+                            float beta_scale, const gdn_bf16* dq, const gdn_bf16* dk, const float* dg,
+                            const gdn_bf16* dbeta, gdn_bf16* dq_raw, gdn_bf16* dk_raw, float* da,
+                            float* db, float* dA_log, float* ddt_bias, int rows, int H, int d_k,
+                            cudaStream_t stream) {
+    gdn_status st = check_prologue(rows, H, d_k, gate_mode, A_log);
+    if (st != GDN_OK) return st;
+    if (rows > 0 && (!a || !b || !dg || !dbeta || !da || !db)) return GDN_ERR_INVALID_ARG;
+    if (q_raw && (!dq || !dq_raw)) return GDN_ERR_INVALID_ARG;
+    if (k_raw && (!dk || !dk_raw)) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q_raw, k_raw, a, b, A_log, dt_bias, dq, dk, dg, dbeta, dq_raw, dk_raw,
+                          da, db, dA_log, ddt_bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::PrologueArgs pa{};
+    pa.q_raw = q_raw; pa.k_raw = k_raw; pa.a = a; pa.b = b; pa.A_log = A_log; pa.dt_bias = dt_bias;
+    pa.gate_mode = gate_mode; pa.lower = lower; pa.beta_scale = beta_scale;
+    pa.dq = dq; pa.dk = dk; pa.dg = dg; pa.dbeta = dbeta;
+    pa.dq_raw = dq_raw; pa.dk_raw = dk_raw; pa.da = da; pa.db = db; pa.dA_log = dA_log; pa.ddt_bias = ddt_bias;
+    pa.rows = rows; pa.H = H; pa.d_k = d_k;
+    if (!launched(gdn::launch_prologue_bwd(pa, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

@@ -122,6 +122,39 @@ struct RecurrentArgs {
 };
 
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream);
+
+// Prologue (q/k L2 normalisation, gates) and its reverse mode.
+struct PrologueArgs {
+    const uint16_t* q_raw;        // (rows, H, d_k) bf16; null: q not normalised here
+    const uint16_t* k_raw;        // likewise
+    const float* a;               // (rows, H) raw decay-gate input
+    const float* b;               // (rows, H) raw beta input
+    const float* A_log;           // (H), decay gate only
+    const float* dt_bias;         // (H) or null (zeros)
+    int gate_mode;                // 1: -exp(A_log) softplus(a + dt_bias); 2: lower sigmoid(a + dt_bias)
+    float lower;                  // gate_mode 2
+    float beta_scale;             // beta = beta_scale sigmoid(b)
+    uint16_t* q;                  // forward outputs: q_hat, k_hat (bf16), g (fp32), beta (bf16)
+    uint16_t* k;
+    float* g;
+    uint16_t* beta;
+    const uint16_t* dq;           // backward inputs: gradients w.r.t. q_hat, k_hat, g, beta
+    const uint16_t* dk;
+    const float* dg;
+    const uint16_t* dbeta;
+    uint16_t* dq_raw;             // backward outputs
+    uint16_t* dk_raw;
+    float* da;
+    float* db;
+    float* dA_log;                // (H) or null
+    float* ddt_bias;              // (H) or null
+    int rows;                     // tokens (B * T)
+    int H;
+    int d_k;
+};
+
+cudaError_t launch_prologue_fwd(const PrologueArgs& a, cudaStream_t stream);
+cudaError_t launch_prologue_bwd(const PrologueArgs& a, cudaStream_t stream);
 // Warp-specialised tensor-core forward (prep and chain warpgroups);
 // wait_limit bounds every mbarrier wait (polls).
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);

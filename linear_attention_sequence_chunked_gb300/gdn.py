@@ -70,6 +70,10 @@ def load():
         lib.gdn_chunk_bwd.restype = i
         lib.gdn_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
         lib.gdn_recurrent_fwd.restype = i
+        lib.gdn_prologue_fwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 4 + [i] * 3 + [vp]
+        lib.gdn_prologue_fwd.restype = i
+        lib.gdn_prologue_bwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 10 + [i] * 3 + [vp]
+        lib.gdn_prologue_bwd.restype = i
         lib.gdn_get_last_device_error.argtypes = [vp]
         lib.gdn_get_last_device_error.restype = i
         lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
@@ -144,6 +148,25 @@ def gdn_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, f
                                   _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
                                   _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
     _check(st, "gdn_recurrent_fwd")
+
+
+def gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias, gate_mode, lower, beta_scale,
+                     q, k, g, beta, rows, H, d_k, stream=None):
+    st = load().gdn_prologue_fwd(_ptr(q_raw), _ptr(k_raw), _ptr(a), _ptr(b), _ptr(A_log),
+                                 _ptr(dt_bias), int(gate_mode), float(lower), float(beta_scale),
+                                 _ptr(q), _ptr(k), _ptr(g), _ptr(beta), rows, H, d_k, _stream(stream))
+    _check(st, "gdn_prologue_fwd")
+
+
+def gdn_prologue_bwd(q_raw, k_raw, a, b, A_log, dt_bias, gate_mode, lower, beta_scale,
+                     dq, dk, dg, dbeta, dq_raw, dk_raw, da, db, dA_log, ddt_bias, rows, H, d_k,
+                     stream=None):
+    st = load().gdn_prologue_bwd(_ptr(q_raw), _ptr(k_raw), _ptr(a), _ptr(b), _ptr(A_log),
+                                 _ptr(dt_bias), int(gate_mode), float(lower), float(beta_scale),
+                                 _ptr(dq), _ptr(dk), _ptr(dg), _ptr(dbeta), _ptr(dq_raw),
+                                 _ptr(dk_raw), _ptr(da), _ptr(db), _ptr(dA_log), _ptr(ddt_bias),
+                                 rows, H, d_k, _stream(stream))
+    _check(st, "gdn_prologue_bwd")
 
 
 def gdn_chunk_bwd_noalloc(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
