@@ -390,6 +390,8 @@ def run_ours(args):
 
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
+    # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
+    prologue = None if args.no_decode else measure_prologue(gdn, torch, dev, stream, hbm, B * T, H, K)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None
@@ -437,6 +439,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "accuracy": accuracy,
             "decode": decode,
+            "prologue": prologue,
         }
         print(json.dumps(line), flush=True)
     barrier(world)
@@ -511,6 +514,57 @@ def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, step
             "value": B * H / t, "unit": UNIT, "us_per_call": t * 1e6,
             "roofline": {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm, "unit": "GB/s",
                          "frac": nbytes / t / 1e9 / hbm}}
+
+
+def measure_prologue(gdn, torch, dev, stream, hbm, rows, H, K, steps=20, warmup=3):
+    """gdn_prologue_fwd and gdn_prologue_bwd (decay gate, beta factor 2) on
+    rows x H (token, head) rows; HBM-bound, algorithmic bytes: forward reads
+    q, k and writes their normalised copies (bf16) plus the gates; backward
+    reads q, k and the two gradients and writes dq, dk (bf16) plus the gate
+    gradients."""
+    gen = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn((rows, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    k = torch.randn((rows, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    a = torch.randn((rows, H), device=dev, generator=gen)
+    b = torch.randn((rows, H), device=dev, generator=gen)
+    A_log = torch.rand((H,), device=dev, generator=gen)
+    dtb = torch.rand((H,), device=dev, generator=gen) - 0.5
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    g = torch.empty((rows, H), device=dev)
+    beta = torch.empty((rows, H), device=dev, dtype=torch.bfloat16)
+    dq = torch.randn((rows, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    dk = torch.randn((rows, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    dg = torch.randn((rows, H), device=dev, generator=gen)
+    dbeta = torch.randn((rows, H), device=dev, generator=gen).to(torch.bfloat16)
+    dqr, dkr = torch.empty_like(q), torch.empty_like(k)
+    da, db = torch.empty_like(a), torch.empty_like(b)
+    dA, ddt = torch.empty_like(A_log), torch.empty_like(dtb)
+
+    def fwd():
+        gdn.gdn_prologue_fwd(q, k, a, b, A_log, dtb, 1, -5.0, 2.0, qo, ko, g, beta, rows, H, K, stream)
+
+    def bwd():
+        gdn.gdn_prologue_bwd(q, k, a, b, A_log, dtb, 1, -5.0, 2.0, dq, dk, dg, dbeta, dqr, dkr,
+                             da, db, dA, ddt, rows, H, K, stream)
+
+    res = {}
+    n = rows * H
+    for name, fn, nbytes in (("fwd", fwd, n * (8 * K + 4 + 4 + 4 + 2)),
+                             ("bwd", bwd, n * (12 * K + 4 + 4 + 4 + 2 + 4 + 4))):
+        for _ in range(warmup):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / steps
+        res[name] = {"us": t * 1e6, "achieved_gbs": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / hbm}
+    res["config"] = f"{rows} tokens x H={H}, d_k={K}, decay gate, beta factor 2"
+    return res
 
 
 def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, ws_b_n):
