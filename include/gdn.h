@@ -135,6 +135,20 @@ GDN_API gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const
                              int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
 /*
+ * Token-serial forward of the per-channel-gate (KDA) variant that cuLA issue
+ * #126 runs: g is (B, T, H, d_k) fp32, one log decay per key channel, and the
+ * state update decays each key row of S by its own factor,
+ * S <- diag(exp(g_t)) S; everything else (arguments, layouts, validation,
+ * errors) is as gdn_recurrent_fwd.  Only this token-serial path exists for
+ * the per-channel gate.
+ */
+GDN_API gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                 const float* g, const gdn_bf16* beta, float scale,
+                                 const float* initial_state, const int32_t* cu_seqlens,
+                                 gdn_bf16* out, float* final_state,
+                                 int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
+
+/*
  * Prologue: q/k L2 normalisation and the two gates from their raw inputs
  * ("Research Sprint Day 2 - Rooflines", GDN layer pseudocode steps 4 and 5),
  * producing the q, k, g, beta that gdn_chunk_fwd / gdn_chunk_bwd take.

@@ -99,6 +99,28 @@ BwdLayout bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     return L;
 }
 
+gdn_status recurrent(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                     const gdn_bf16* beta, float scale, const float* initial_state,
+                     const int32_t* cu_seqlens, gdn_bf16* out, float* final_state, int B, int T,
+                     int H, int d_k, int d_v, int per_channel, cudaStream_t stream) {
+    gdn_status st = check_shapes(B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, out, initial_state, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    gdn::RecurrentArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
+    a.per_channel_gate = per_channel;
+    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
+    if (!launched(gdn::launch_recurrent(a, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,21 +184,17 @@ gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
                              const float* initial_state, const int32_t* cu_seqlens,
                              gdn_bf16* out, float* final_state,
                              int B, int T, int H, int d_k, int d_v, cudaStream_t stream) {
-    gdn_status st = check_shapes(B, T, H, d_k, d_v);
-    if (st != GDN_OK) return st;
-    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, out, initial_state, final_state};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
-    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
-    int* err = error_word();
-    if (!err) return GDN_ERR_CUDA;
-    gdn::RecurrentArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
-    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
-    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
-    if (!launched(gdn::launch_recurrent(a, stream))) return GDN_ERR_CUDA;
-    return GDN_OK;
+    return recurrent(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, B, T, H,
+                     d_k, d_v, 0, stream);
+}
+
+gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                 const float* g, const gdn_bf16* beta, float scale,
+                                 const float* initial_state, const int32_t* cu_seqlens,
+                                 gdn_bf16* out, float* final_state,
+                                 int B, int T, int H, int d_k, int d_v, cudaStream_t stream) {
+    return recurrent(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, B, T, H,
+                     d_k, d_v, 1, stream);
 }
 
 gdn_status gdn_prologue_fwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a, const float* b,

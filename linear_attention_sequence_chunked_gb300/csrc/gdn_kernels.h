@@ -110,13 +110,14 @@ struct RecurrentArgs {
     const uint16_t* q;
     const uint16_t* k;
     const uint16_t* v;
-    const float* g;
+    const float* g;               // (B,T,H) fp32, or (B,T,H,d_k) with per_channel_gate
     const uint16_t* beta;
     float scale;
     const float* initial_state;   // may be null (zeros)
     const int32_t* cu_seqlens;
     uint16_t* out;
     float* final_state;           // may be null
+    int per_channel_gate;         // one log decay per key channel (KDA)
     int N, T, H, d_k, d_v;
     int* err;
 };

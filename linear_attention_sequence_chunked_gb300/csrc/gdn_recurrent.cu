@@ -8,6 +8,10 @@
 // The columns of S evolve independently (column j only sees v_t[j]), so the
 // value dimension is split across CTAs.
 //
+// The per-channel-gate (KDA) variant of cuLA issue #126 takes g of shape
+// (B, T, H, d_k): S <- diag(exp(g_t)) S decays each key row by its own factor;
+// the rest of the update is unchanged.
+//
 // One CTA (128 threads) per (32-column value slice, head, sequence).  Thread
 // (column jc = tid / 4, key block kb = tid % 4) holds rows kb*d_k/4 ..
 // (kb+1)*d_k/4 - 1 of column jc in registers; the two sums over the key
@@ -26,17 +30,19 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kCols = 32;  // value columns per CTA
 
-// One token's inputs as this thread needs them.
-template <int KB>
+// One token's inputs as this thread needs them (gk: the per-channel gates of
+// this thread's key rows, kPerChannel only).
+template <int KB, bool kPerChannel>
 struct TokenIn {
     uint4 k[KB / 8];
     uint4 q[KB / 8];
+    float4 gk[kPerChannel ? KB / 4 : 1];
     float v, g, beta;
 };
 
-template <int KB>
+template <int KB, bool kPerChannel>
 __device__ __forceinline__ void load_token(const RecurrentArgs& p, long long row, int h, int kb, int col,
-                                           TokenIn<KB>& in) {
+                                           TokenIn<KB, kPerChannel>& in) {
     const long long kq = (row * p.H + h) * static_cast<long long>(p.d_k) + kb * KB;
     const uint4* ks = reinterpret_cast<const uint4*>(p.k + kq);
     const uint4* qs = reinterpret_cast<const uint4*>(p.q + kq);
@@ -47,7 +53,13 @@ __device__ __forceinline__ void load_token(const RecurrentArgs& p, long long row
     }
     const long long gi = row * p.H + h;
     in.v = bf16_to_f32(p.v[gi * p.d_v + col]);
-    in.g = p.g[gi];
+    if constexpr (kPerChannel) {
+        const float4* gs = reinterpret_cast<const float4*>(p.g + kq);
+#pragma unroll
+        for (int c = 0; c < KB / 4; ++c) in.gk[c] = gs[c];
+    } else {
+        in.g = p.g[gi];
+    }
     in.beta = bf16_to_f32(p.beta[gi]);
 }
 
@@ -80,7 +92,7 @@ __device__ __forceinline__ float dot_rows(const float* x, const float* y) {
     return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
-template <int K>
+template <int K, bool kPerChannel>
 __global__ void __launch_bounds__(kThreads) gdn_recurrent_kernel(const RecurrentArgs p) {
     constexpr int KB = K / 4;  // key rows per thread
     const int vs = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -97,17 +109,27 @@ __global__ void __launch_bounds__(kThreads) gdn_recurrent_kernel(const Recurrent
     for (int i = 0; i < KB; ++i)
         S[i] = p.initial_state ? p.initial_state[state_off + static_cast<long long>(kb * KB + i) * p.d_v + col] : 0.f;
 
-    TokenIn<KB> cur, nxt;
-    if (t0 < t1) load_token<KB>(p, row_base + t0, h, kb, col, cur);
+    TokenIn<KB, kPerChannel> cur, nxt;
+    if (t0 < t1) load_token<KB, kPerChannel>(p, row_base + t0, h, kb, col, cur);
     for (int t = t0; t < t1; ++t) {
-        if (t + 1 < t1) load_token<KB>(p, row_base + t + 1, h, kb, col, nxt);
+        if (t + 1 < t1) load_token<KB, kPerChannel>(p, row_base + t + 1, h, kb, col, nxt);
         float kk[KB], qq[KB];
         unpack_rows<KB>(cur.k, kk);
         unpack_rows<KB>(cur.q, qq);
         // decay, read, write (the error, not the value), readout
-        const float alpha = expf(cur.g);
+        if constexpr (kPerChannel) {
 #pragma unroll
-        for (int i = 0; i < KB; ++i) S[i] *= alpha;
+            for (int c = 0; c < KB / 4; ++c) {
+                S[4 * c] *= expf(cur.gk[c].x);
+                S[4 * c + 1] *= expf(cur.gk[c].y);
+                S[4 * c + 2] *= expf(cur.gk[c].z);
+                S[4 * c + 3] *= expf(cur.gk[c].w);
+            }
+        } else {
+            const float alpha = expf(cur.g);
+#pragma unroll
+            for (int i = 0; i < KB; ++i) S[i] *= alpha;
+        }
         const float v_old = column_sum(dot_rows<KB>(S, kk));
         const float e = cur.beta * (cur.v - v_old);
 #pragma unroll
@@ -126,10 +148,17 @@ __global__ void __launch_bounds__(kThreads) gdn_recurrent_kernel(const Recurrent
 
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     dim3 grid(a.d_v / kCols, a.H, a.N);
-    if (a.d_k == 64)
-        gdn_recurrent_kernel<64><<<grid, kThreads, 0, stream>>>(a);
-    else
-        gdn_recurrent_kernel<128><<<grid, kThreads, 0, stream>>>(a);
+    if (a.per_channel_gate) {
+        if (a.d_k == 64)
+            gdn_recurrent_kernel<64, true><<<grid, kThreads, 0, stream>>>(a);
+        else
+            gdn_recurrent_kernel<128, true><<<grid, kThreads, 0, stream>>>(a);
+    } else {
+        if (a.d_k == 64)
+            gdn_recurrent_kernel<64, false><<<grid, kThreads, 0, stream>>>(a);
+        else
+            gdn_recurrent_kernel<128, false><<<grid, kThreads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -70,6 +70,8 @@ def load():
         lib.gdn_chunk_bwd.restype = i
         lib.gdn_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
         lib.gdn_recurrent_fwd.restype = i
+        lib.gdn_kda_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
+        lib.gdn_kda_recurrent_fwd.restype = i
         lib.gdn_prologue_fwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 4 + [i] * 3 + [vp]
         lib.gdn_prologue_fwd.restype = i
         lib.gdn_prologue_bwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 10 + [i] * 3 + [vp]
@@ -148,6 +150,14 @@ def gdn_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, f
                                   _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
                                   _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
     _check(st, "gdn_recurrent_fwd")
+
+
+def gdn_kda_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                          B, T, H, d_k, d_v, stream=None):
+    st = load().gdn_kda_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                      _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                      _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
+    _check(st, "gdn_kda_recurrent_fwd")
 
 
 def gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias, gate_mode, lower, beta_scale,
