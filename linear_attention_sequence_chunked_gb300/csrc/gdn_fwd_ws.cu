@@ -36,8 +36,9 @@
 //
 // Hand-offs are mbarriers (bounded waits): stage full (TMA), gram done,
 // prep ready (T, P, gates of a chunk), slot free (T, P, gates double-buffered
-// by chunk parity), and the chain's own MMA completions.  Warpgroup-internal
-// ordering uses named barriers 1 (chain) and 2 (prep).
+// by chunk parity), and the MMA completions that the chain and the issuer
+// warp (warp 12: the MMAs off the chain's critical path) wait on.  Ordering
+// within the chain warps and within the prep warps uses named barriers 1 and 2.
 #include <cuda.h>
 #include <string.h>
 
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
                 __syncwarp();
-                // gates, T and P of this chunk from the prep warpgroup
+                // gates, T and P of this chunk from the prep warps
                 if (!mbar_wait(bar(B_READY0 + slot), ph2, wl)) *abort_flag = 1;
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
@@ -717,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     } else if (warp < 8 + kPrepThreads / 32) {
-        // ======================= prep warpgroup =======================
+        // ======================= prep warps =======================
         const int q = tid - kChainThreads;  // 0..127
         const int sub = warp - 8;           // TMEM subpartition
         float* At = reinterpret_cast<float*>(sm + oA);  // A^T, row stride 64
