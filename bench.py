@@ -106,6 +106,17 @@ def barrier(world):
         dist.barrier()
 
 
+def rank_seed(rank):
+    """Seed of rank r's batch: every rank draws its own independent problems."""
+    return 2 + 1000 * rank
+
+
+def aggregate_rate(world, units_per_rank, t_max):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (weak scaling, each rank holds a batch of the same shape)."""
+    return world * units_per_rank / t_max
+
+
 def max_over_ranks(x, world, device):
     if world == 1:
         return x
@@ -293,7 +304,7 @@ def run_ours(args):
 
     B, T, H, K, V = (SHAPE[k] for k in ("B", "T", "H", "d_k", "d_v"))
     wl = W.make_workload(2, B=B, T=T, H=H, d_k=K, d_v=V, with_grad=True,
-                         seed=2 + 1000 * rank)
+                         seed=rank_seed(rank))
     q, k, v = _bf16(wl.q, torch, dev), _bf16(wl.k, torch, dev), _bf16(wl.v, torch, dev)
     g = torch.from_numpy(wl.g).to(dev)
     beta = _bf16(wl.beta, torch, dev)
@@ -386,7 +397,11 @@ def run_ours(args):
     # ---- end to end through the public API with pinned host buffers ----
     e2e = None
     if not args.no_e2e:
+        barrier(world)
         e2e = measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, ws_b_n)
+        t_e2e = max_over_ranks(e2e["ms_per_step"] * 1e-3, world, dev)
+        e2e["ms_per_step"] = t_e2e * 1e3
+        e2e["value"] = aggregate_rate(world, th, t_e2e)
 
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
@@ -419,7 +434,7 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * th / t_step, "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": aggregate_rate(world, th, t_step), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -430,8 +445,8 @@ def run_ours(args):
                        "l2": "flushed between steps (write of 2x L2) and inputs > L2"},
             "roofline": roof_fwd,
             "roofline_bwd": roof_bwd,
-            "fwd": {"tokens_heads_per_s": world * th / t_fwd_max, "ms": t_fwd_max * 1e3},
-            "bwd": {"tokens_heads_per_s": world * th / t_bwd_max, "ms": t_bwd_max * 1e3},
+            "fwd": {"tokens_heads_per_s": aggregate_rate(world, th, t_fwd_max), "ms": t_fwd_max * 1e3},
+            "bwd": {"tokens_heads_per_s": aggregate_rate(world, th, t_bwd_max), "ms": t_bwd_max * 1e3},
             "gpu_launches": int(launches),
             "wall_s_timed": t_wall,
             "clocks": clk,
