@@ -1,10 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the chunked gated delta rule operator on one GB300.
 
-One step = the whole hot path over one batch: gdn_chunk_fwd followed by
-gdn_chunk_bwd (upstream dO ~ N(0,1)) on the dense workload B=4, H=16,
-T=4096, d_k=d_v=128 (bf16 I/O, fp32 state), inputs resident in HBM.
-Prints ONE JSON line (rank 0).
+One step = the whole hot path over one batch, as a training step runs it:
+gdn_chunk_fwd_save (output, final state, and every chunk's start state and T
+tiles kept for the backward) followed by gdn_chunk_bwd_saved (upstream
+dO ~ N(0,1)) on the dense workload B=4, H=16, T=4096, d_k=d_v=128 (bf16 I/O,
+fp32 state), inputs resident in HBM.  The inference forward (gdn_chunk_fwd,
+nothing kept) is timed beside it.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -318,20 +320,22 @@ def run_ours(args):
     dg = torch.empty_like(g)
     db = torch.empty_like(beta)
     dS0 = torch.empty((B, H, K, V), dtype=torch.float32, device=dev)
-    ws_f_n = gdn.gdn_chunk_fwd_workspace_size(B, T, H, K, V, 0)
-    ws_b_n = gdn.gdn_chunk_bwd_workspace_size(B, T, H, K, V, 0)
+    # training route: the forward keeps every chunk's start state and T tiles
+    # (saved buffer), the backward reuses them
+    ws_f_n = gdn.gdn_chunk_saved_size(B, T, H, K, V, 0)
+    ws_b_n = gdn.gdn_chunk_bwd_saved_workspace_size(B, T, H, K, V, 0)
     ws_f = torch.empty(max(ws_f_n, 1), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(ws_b_n, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def fwd():
-        gdn.gdn_chunk_fwd(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V,
-                          ws_f if ws_f_n else None, ws_f_n, stream)
+        gdn.gdn_chunk_fwd_save(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V,
+                               ws_f, ws_f_n, stream)
 
     def bwd():
-        gdn.gdn_chunk_bwd(q, k, v, g, beta, scale, None, None, dO, None, dq, dk, dv, dg, db,
-                          dS0, B, T, H, K, V, ws_b if ws_b_n else None, ws_b_n, stream)
+        gdn.gdn_chunk_bwd_saved(q, k, v, g, beta, scale, None, dO, None, dq, dk, dv, dg, db,
+                                dS0, B, T, H, K, V, ws_f, ws_f_n, ws_b, ws_b_n, stream)
 
     for _ in range(args.warmup):
         fwd()
@@ -403,6 +407,11 @@ def run_ours(args):
         e2e["ms_per_step"] = t_e2e * 1e3
         e2e["value"] = aggregate_rate(world, th, t_e2e)
 
+    # ---- inference forward (gdn_chunk_fwd, nothing kept) on the same inputs ----
+    t_inf = measure_inference_fwd(gdn, (q, k, v, g, beta, scale, out, fs), (B, T, H, K, V), flush,
+                                  stream, torch, max(5, min(args.steps, 20)))
+    t_inf = max_over_ranks(t_inf, world, dev)
+    roof_inf = roof(t_inf, f_fwd, b_fwd)
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
     # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
@@ -445,6 +454,8 @@ def run_ours(args):
                        "l2": "flushed between steps (write of 2x L2) and inputs > L2"},
             "roofline": roof_fwd,
             "roofline_bwd": roof_bwd,
+            "inference_fwd": {"tokens_heads_per_s": aggregate_rate(world, th, t_inf), "ms": t_inf * 1e3,
+                              "roofline": roof_inf},
             "fwd": {"tokens_heads_per_s": aggregate_rate(world, th, t_fwd_max), "ms": t_fwd_max * 1e3},
             "bwd": {"tokens_heads_per_s": aggregate_rate(world, th, t_bwd_max), "ms": t_bwd_max * 1e3},
             "gpu_launches": int(launches),
@@ -492,6 +503,32 @@ def load_traffic():
     if not d.get("sources"):
         return None
     return d.get("bytes_per_launch")
+
+
+def measure_inference_fwd(gdn, tensors, dims, flush, stream, torch, steps, warmup=3):
+    """gdn_chunk_fwd alone (inference: output and final state, nothing kept
+    for a backward) on the step's inputs, L2 flushed before each call;
+    returns the mean duration in seconds."""
+    q, k, v, g, beta, scale, out, fs = tensors
+    B, T, H, K, V = dims
+    n = gdn.gdn_chunk_fwd_workspace_size(B, T, H, K, V, 0)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+
+    def call():
+        gdn.gdn_chunk_fwd(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V,
+                          ws if n else None, n, stream)
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
 
 
 def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, steps=50, warmup=5):
@@ -623,13 +660,13 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
             if i >= 2:
                 stream.wait_event(out_done[i - 2])      # set j's outputs were read out
             di, do = d_in[j], d_out[j]
-            gdn.gdn_chunk_fwd(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
-                              wl.scale, None, None, bf(do["out"]), do["fs"], B, T, H, K, V,
-                              ws_f if ws_f_n else None, ws_f_n, stream)
-            gdn.gdn_chunk_bwd(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
-                              wl.scale, None, None, bf(di["dO"]), None, bf(do["dq"]), bf(do["dk"]),
-                              bf(do["dv"]), do["dg"], bf(do["dbeta"]), do["dS0"], B, T, H, K, V,
-                              ws_b if ws_b_n else None, ws_b_n, stream)
+            gdn.gdn_chunk_fwd_save(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
+                                   wl.scale, None, None, bf(do["out"]), do["fs"], B, T, H, K, V,
+                                   ws_f, ws_f_n, stream)
+            gdn.gdn_chunk_bwd_saved(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
+                                    wl.scale, None, bf(di["dO"]), None, bf(do["dq"]), bf(do["dk"]),
+                                    bf(do["dv"]), do["dg"], bf(do["dbeta"]), do["dS0"], B, T, H, K, V,
+                                    ws_f, ws_f_n, ws_b, ws_b_n, stream)
             comp_done[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[i])

@@ -215,6 +215,61 @@ GDN_API gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Training route: a forward that keeps what the backward would otherwise
+ * recompute, and the backward that reuses it.  fla issue #1550's validation
+ * plan names both variants, retained and recomputed chunk states;
+ * gdn_chunk_bwd recomputes them (no memory kept between the calls), this
+ * route retains them (one T kernel and one chain pass fewer per step).
+ *
+ * Bytes of the saved-for-backward buffer for these sizes: every chunk's start
+ * state (4 d_k d_v bytes per chunk and head, as bf16 hi/lo operand tiles),
+ * then the T = (I + A)^-1 tiles (16 KB per chunk and head); 0 for unsupported
+ * sizes.  At B=4, H=16, T=4096, d_k=d_v=128: 320 MiB.
+ */
+GDN_API size_t gdn_chunk_saved_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
+ * gdn_chunk_fwd that also fills `saved` (device, 256-byte aligned, at least
+ * gdn_chunk_saved_size() bytes; contents on entry do not matter): one chunk
+ * chain writes out, final_state and every chunk's start state; the T tiles
+ * come from the chunk-parallel kernel first.  out and final_state are
+ * bitwise those of gdn_chunk_fwd.  Arguments, layouts and errors as
+ * gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG for a missing or short `saved` and
+ * GDN_ERR_MISALIGNED for a misaligned one.
+ */
+GDN_API gdn_status gdn_chunk_fwd_save(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                              const float* g, const gdn_bf16* beta, float scale,
+                              const float* initial_state, const int32_t* cu_seqlens,
+                              gdn_bf16* out, float* final_state,
+                              int B, int T, int H, int d_k, int d_v,
+                              void* saved, size_t saved_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace gdn_chunk_bwd_saved needs: the per-chunk
+ * end-state gradients (4 d_k d_v bytes per chunk and head). */
+GDN_API size_t gdn_chunk_bwd_saved_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
+ * gdn_chunk_bwd from the buffer that gdn_chunk_fwd_save filled for the same
+ * q, k, v, g, beta, initial_state and cu_seqlens (the caller keeps them
+ * unchanged in between; nothing checks this).  It skips the T kernel and the
+ * forward state pass: only the reverse chain of state gradients and the
+ * chunk-parallel gradient pass run.  The initial state is not an argument
+ * (the saved start states hold it).  Gradients are bitwise those of
+ * gdn_chunk_bwd.  `saved` is only read; `workspace` (256-byte aligned, at
+ * least gdn_chunk_bwd_saved_workspace_size() bytes) is scratch.  Errors as
+ * gdn_chunk_bwd.
+ */
+GDN_API gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                               const float* g, const gdn_bf16* beta, float scale,
+                               const int32_t* cu_seqlens,
+                               const gdn_bf16* d_out, const float* d_final_state,
+                               gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                               gdn_bf16* dbeta, float* d_initial_state,
+                               int B, int T, int H, int d_k, int d_v,
+                               const void* saved, size_t saved_bytes,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word of
  * the current device: GDN_OK, GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT
  * (GDN_ERR_CUDA if the synchronisation or the read itself failed).

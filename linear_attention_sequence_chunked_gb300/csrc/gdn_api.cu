@@ -99,6 +99,95 @@ BwdLayout bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     return L;
 }
 
+// Saved-for-backward buffer of the training route (gdn_chunk_fwd_save ->
+// gdn_chunk_bwd_saved): every chunk's start state in the same per-chunk
+// layout as the backward workspace, then the T tiles.
+struct SavedLayout {
+    size_t states, tiles, total;
+};
+
+SavedLayout saved_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
+    SavedLayout L{};
+    const size_t per_state = sizeof(float) * static_cast<size_t>(d_k) * d_v;
+    L.states = 0;
+    L.tiles = round_up(per_state * chunk_slots(B, T, varlen) * H);
+    L.total = L.tiles + tiles_bytes(B, T, H, varlen);
+    return L;
+}
+
+// Per-chunk end-state gradients: the only workspace of gdn_chunk_bwd_saved.
+size_t dstates_bytes(int B, int T, int H, int d_k, int d_v, int varlen) {
+    return round_up(sizeof(float) * static_cast<size_t>(d_k) * d_v * chunk_slots(B, T, varlen) * H);
+}
+
+// Host checks shared by the forward entry points.
+gdn_status check_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                     const gdn_bf16* beta, const float* initial_state, const int32_t* cu_seqlens,
+                     const gdn_bf16* out, const float* final_state, int B, int T, int H, int d_k,
+                     int d_v) {
+    gdn_status st = check_shapes(B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, out, initial_state, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
+
+// Host checks shared by the backward entry points.
+gdn_status check_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                     const gdn_bf16* beta, const float* initial_state, const int32_t* cu_seqlens,
+                     const gdn_bf16* d_out, const float* d_final_state, const gdn_bf16* dq,
+                     const gdn_bf16* dk, const gdn_bf16* dv, const float* dg, const gdn_bf16* dbeta,
+                     const float* d_initial_state, int B, int T, int H, int d_k, int d_v) {
+    gdn_status st = check_shapes(B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, d_out, dq, dk, dv, dg, dbeta,
+                          initial_state, d_final_state, d_initial_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
+
+// A caller buffer of `need` bytes: present, large enough, 256-byte aligned.
+gdn_status check_buffer(const void* p, size_t bytes, size_t need) {
+    if (need == 0) return GDN_OK;
+    if (!p || bytes < need) return GDN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p) & (kAlign - 1)) return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
+
+// Backward passes 2 (reverse chain of end-state gradients into `dstates`)
+// and 3 (chunk-parallel local gradients), from the chunk start states and T
+// tiles that pass 1 or the saving forward left.
+gdn_status launch_bwd_passes(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                             const float* g, const gdn_bf16* beta, float scale,
+                             const int32_t* cu_seqlens, const gdn_bf16* d_out,
+                             const float* d_final_state, gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv,
+                             float* dg, gdn_bf16* dbeta, float* d_initial_state, int B, int T,
+                             int H, int d_k, int d_v, const float* states, float* dstates,
+                             const uint8_t* tiles, int* err, cudaStream_t stream) {
+    gdn::BwdChainArgs c{};
+    c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
+    c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;
+    c.chunk_dstates = dstates; c.chunk_T = tiles; c.d_initial_state = d_initial_state;
+    c.N = B; c.T = T; c.H = H; c.d_k = d_k; c.d_v = d_v; c.err = err;
+    if (!launched(gdn::launch_bwd_chain(c, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+
+    gdn::BwdLocalArgs l{};
+    l.q = q; l.k = k; l.v = v; l.g = g; l.beta = beta; l.d_out = d_out; l.scale = scale;
+    l.cu_seqlens = cu_seqlens; l.chunk_states = states; l.chunk_dstates = dstates; l.chunk_T = tiles;
+    l.dq = dq; l.dk = dk; l.dv = dv; l.dg = dg; l.dbeta = dbeta;
+    l.N = B; l.T = T; l.H = H; l.d_k = d_k; l.d_v = d_v; l.err = err;
+    l.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
+    if (l.max_chunks > 0 && !launched(gdn::launch_bwd_local(l, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 gdn_status recurrent(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
                      const gdn_bf16* beta, float scale, const float* initial_state,
                      const int32_t* cu_seqlens, gdn_bf16* out, float* final_state, int B, int T,
@@ -154,13 +243,8 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
                          gdn_bf16* out, float* final_state,
                          int B, int T, int H, int d_k, int d_v,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    gdn_status st = check_shapes(B, T, H, d_k, d_v);
+    gdn_status st = check_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
-    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, out, initial_state, final_state};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
-    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return GDN_ERR_MISALIGNED;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
@@ -249,21 +333,13 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
                          gdn_bf16* dbeta, float* d_initial_state,
                          int B, int T, int H, int d_k, int d_v,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    gdn_status st = check_shapes(B, T, H, d_k, d_v);
+    gdn_status st = check_bwd(q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv,
+                              dg, dbeta, d_initial_state, B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
-    if (T > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
-        return GDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, d_out, dq, dk, dv, dg, dbeta,
-                          initial_state, d_final_state, d_initial_state};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
-    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_MISALIGNED;
     const int varlen = cu_seqlens != nullptr;
     const BwdLayout L = bwd_layout(B, T, H, d_k, d_v, varlen);
-    if (L.total > 0) {
-        if (!workspace || workspace_bytes < L.total) return GDN_ERR_INVALID_ARG;
-        if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return GDN_ERR_MISALIGNED;
-    }
+    st = check_buffer(workspace, workspace_bytes, L.total);
+    if (st != GDN_OK) return st;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
@@ -280,24 +356,73 @@ gdn_status gdn_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     f.out = nullptr; f.final_state = nullptr; f.chunk_states = states; f.chunk_T = tiles;
     f.N = B; f.T = T; f.H = H; f.d_k = d_k; f.d_v = d_v; f.err = err;
     if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    return launch_bwd_passes(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                             d_initial_state, B, T, H, d_k, d_v, states, dstates, tiles, err, stream);
+}
 
-    // pass 2: reverse chain of state gradients
-    gdn::BwdChainArgs c{};
-    c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
-    c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;
-    c.chunk_dstates = dstates; c.chunk_T = tiles; c.d_initial_state = d_initial_state;
-    c.N = B; c.T = T; c.H = H; c.d_k = d_k; c.d_v = d_v; c.err = err;
-    if (!launched(gdn::launch_bwd_chain(c, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+size_t gdn_chunk_saved_size(int B, int T, int H, int d_k, int d_v, int varlen) {
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
+    return saved_layout(B, T, H, d_k, d_v, varlen).total;
+}
 
-    // pass 3: chunk-parallel local gradients
-    gdn::BwdLocalArgs l{};
-    l.q = q; l.k = k; l.v = v; l.g = g; l.beta = beta; l.d_out = d_out; l.scale = scale;
-    l.cu_seqlens = cu_seqlens; l.chunk_states = states; l.chunk_dstates = dstates; l.chunk_T = tiles;
-    l.dq = dq; l.dk = dk; l.dv = dv; l.dg = dg; l.dbeta = dbeta;
-    l.N = B; l.T = T; l.H = H; l.d_k = d_k; l.d_v = d_v; l.err = err;
-    l.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
-    if (l.max_chunks > 0 && !launched(gdn::launch_bwd_local(l, stream))) return GDN_ERR_CUDA;
+size_t gdn_chunk_bwd_saved_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
+    return dstates_bytes(B, T, H, d_k, d_v, varlen);
+}
+
+gdn_status gdn_chunk_fwd_save(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                              const float* g, const gdn_bf16* beta, float scale,
+                              const float* initial_state, const int32_t* cu_seqlens,
+                              gdn_bf16* out, float* final_state,
+                              int B, int T, int H, int d_k, int d_v,
+                              void* saved, size_t saved_bytes, cudaStream_t stream) {
+    gdn_status st = check_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    const SavedLayout L = saved_layout(B, T, H, d_k, d_v, cu_seqlens != nullptr);
+    st = check_buffer(saved, saved_bytes, L.total);
+    if (st != GDN_OK) return st;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    char* s = static_cast<char*>(saved);
+    float* states = L.total ? reinterpret_cast<float*>(s + L.states) : nullptr;
+    uint8_t* tiles = L.total ? reinterpret_cast<uint8_t*>(s + L.tiles) : nullptr;
+    if (L.total > 0 && !launch_tiles(k, g, beta, cu_seqlens, tiles, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
+    // one chain pass writes the output, the final state and every chunk's start state
+    gdn::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens;
+    a.out = out; a.final_state = final_state; a.chunk_states = states; a.chunk_T = tiles;
+    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
+    if (!launched(gdn::launch_fwd_ws(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                               const float* g, const gdn_bf16* beta, float scale,
+                               const int32_t* cu_seqlens,
+                               const gdn_bf16* d_out, const float* d_final_state,
+                               gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                               gdn_bf16* dbeta, float* d_initial_state,
+                               int B, int T, int H, int d_k, int d_v,
+                               const void* saved, size_t saved_bytes,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    gdn_status st = check_bwd(q, k, v, g, beta, nullptr, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg,
+                              dbeta, d_initial_state, B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    const int varlen = cu_seqlens != nullptr;
+    const SavedLayout L = saved_layout(B, T, H, d_k, d_v, varlen);
+    st = check_buffer(saved, saved_bytes, L.total);
+    if (st != GDN_OK) return st;
+    st = check_buffer(workspace, workspace_bytes, dstates_bytes(B, T, H, d_k, d_v, varlen));
+    if (st != GDN_OK) return st;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    const char* s = static_cast<const char*>(saved);
+    const float* states = L.total ? reinterpret_cast<const float*>(s + L.states) : nullptr;
+    const uint8_t* tiles = L.total ? reinterpret_cast<const uint8_t*>(s + L.tiles) : nullptr;
+    return launch_bwd_passes(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                             d_initial_state, B, T, H, d_k, d_v, states, static_cast<float*>(workspace), tiles,
+                             err, stream);
 }
 
 gdn_status gdn_get_last_device_error(cudaStream_t stream) {

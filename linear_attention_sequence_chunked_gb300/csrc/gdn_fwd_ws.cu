@@ -328,9 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             load_v(0);
+            // the K S MMAs (critical path) go out before the start-state copies,
+            // which read the same tiles
             if (nchunks > 0) {
-                if (p.chunk_states && t == 0) store_state_tiles(0);
                 issue_c1(0);
+                if (p.chunk_states && t == 0) store_state_tiles(0);
             }
             for (int ci = 0; ci < nchunks; ++ci) {
                 const int c0 = t0 + ci * kChunk;
@@ -458,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(1);
                 // ---- next chunk's C1, issued ahead of this chunk's output ----
                 if (ci + 1 < nchunks) {
-                    if (p.chunk_states && t == 0) store_state_tiles(ci + 1);
                     issue_c1(ci + 1);
+                    if (p.chunk_states && t == 0) store_state_tiles(ci + 1);
                 }
                 __syncwarp();
                 if (want_out && !mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;

@@ -78,6 +78,14 @@ def load():
         lib.gdn_prologue_bwd.restype = i
         lib.gdn_get_last_device_error.argtypes = [vp]
         lib.gdn_get_last_device_error.restype = i
+        lib.gdn_chunk_saved_size.argtypes = [i] * 6
+        lib.gdn_chunk_saved_size.restype = sz
+        lib.gdn_chunk_bwd_saved_workspace_size.argtypes = [i] * 6
+        lib.gdn_chunk_bwd_saved_workspace_size.restype = sz
+        lib.gdn_chunk_fwd_save.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp, sz, vp]
+        lib.gdn_chunk_fwd_save.restype = i
+        lib.gdn_chunk_bwd_saved.argtypes = [vp] * 5 + [f] + [vp] * 9 + [i] * 5 + [vp, sz, vp, sz, vp]
+        lib.gdn_chunk_bwd_saved.restype = i
         lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
         lib.gdn_chunk_bwd_noalloc.restype = i
         lib.gdn_kernel_launches.argtypes = []
@@ -142,6 +150,35 @@ def gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_f
                               _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "gdn_chunk_bwd")
+
+
+def gdn_chunk_saved_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_chunk_saved_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
+def gdn_chunk_bwd_saved_workspace_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_chunk_bwd_saved_workspace_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
+def gdn_chunk_fwd_save(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                       B, T, H, d_k, d_v, saved, saved_bytes, stream=None):
+    st = load().gdn_chunk_fwd_save(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                   _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                   _ptr(final_state), B, T, H, d_k, d_v, _ptr(saved),
+                                   int(saved_bytes), _stream(stream))
+    _check(st, "gdn_chunk_fwd_save")
+
+
+def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state,
+                        dq, dk, dv, dg, dbeta, d_initial_state, B, T, H, d_k, d_v,
+                        saved, saved_bytes, workspace=None, workspace_bytes=0, stream=None):
+    st = load().gdn_chunk_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                    _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                    _ptr(d_initial_state), B, T, H, d_k, d_v, _ptr(saved),
+                                    int(saved_bytes), _ptr(workspace), int(workspace_bytes),
+                                    _stream(stream))
+    _check(st, "gdn_chunk_bwd_saved")
 
 
 def gdn_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
@@ -224,8 +261,11 @@ def _workspace(nbytes, device):
 
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
-                               cu_seqlens=None, output_final_state=True, stream=None):
-    """Allocate outputs and run gdn_chunk_fwd.  Returns (out, final_state)."""
+                               cu_seqlens=None, output_final_state=True, stream=None,
+                               save_for_backward=False):
+    """Allocate outputs and run gdn_chunk_fwd.  Returns (out, final_state), or
+    (out, final_state, saved) with save_for_backward: gdn_chunk_fwd_save, whose
+    `saved` buffer chunk_gated_delta_rule_bwd(..., saved=saved) reuses."""
     import torch
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
     if scale is None:
@@ -233,6 +273,12 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
     fs = (torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=v.device)
           if output_final_state else None)
+    if save_for_backward:
+        nbytes = gdn_chunk_saved_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+        saved = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
+        gdn_chunk_fwd_save(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs,
+                           B, T, H, d_k, d_v, saved, nbytes, stream)
+        return out, fs, saved
     nbytes = gdn_chunk_fwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
     ws = _workspace(nbytes, v.device)
     gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs,
@@ -241,8 +287,10 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=None, initial_state=None,
-                               cu_seqlens=None, d_final_state=None, stream=None):
-    """Allocate gradients and run gdn_chunk_bwd.  Returns a dict of tensors."""
+                               cu_seqlens=None, d_final_state=None, stream=None, saved=None):
+    """Allocate gradients and run gdn_chunk_bwd, or gdn_chunk_bwd_saved when
+    `saved` (from chunk_gated_delta_rule_fwd(..., save_for_backward=True) on
+    the same inputs) is given.  Returns a dict of tensors."""
     import torch
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
     if scale is None:
@@ -254,6 +302,14 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=None, initial_stat
                dg=torch.empty(g.shape, dtype=torch.float32, device=dev),
                dbeta=torch.empty(beta.shape, dtype=torch.bfloat16, device=dev),
                d_initial_state=torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=dev))
+    if saved is not None:
+        nbytes = gdn_chunk_bwd_saved_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+        ws = _workspace(nbytes, dev)
+        gdn_chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state,
+                            res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"],
+                            res["d_initial_state"], B, T, H, d_k, d_v, saved, saved.numel(),
+                            ws, nbytes, stream)
+        return res
     nbytes = gdn_chunk_bwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
     ws = _workspace(nbytes, dev)
     gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,

@@ -95,3 +95,50 @@ def test_workspace_sizes(lib):
     b = gdn.gdn_chunk_bwd_workspace_size(4, 8192, 16, 128, 128, 0)
     assert b > a > 4 * 64 * 16 * 128 * 128 * 4  # at least one fp32 state per chunk
     assert gdn.gdn_chunk_bwd_workspace_size(1, 4096, 16, 96, 128, 0) == 0  # unsupported
+
+
+def test_saved_route_sizes(lib):
+    """The saved buffer is every chunk's fp32-sized start state then the T
+    tiles; the saved-route workspace is the end-state gradients alone."""
+    B, T, H, K, V = 4, 4096, 16, 128, 128
+    chunks = B * T // 64
+    state = 4 * K * V * chunks * H
+    tiles = 16384 * chunks * H
+    assert gdn.gdn_chunk_saved_size(B, T, H, K, V, 0) == state + tiles == 320 * 2**20
+    assert gdn.gdn_chunk_bwd_saved_workspace_size(B, T, H, K, V, 0) == state
+    # together they hold what the recomputing backward's workspace holds
+    assert (gdn.gdn_chunk_saved_size(B, T, H, K, V, 0) + gdn.gdn_chunk_bwd_saved_workspace_size(B, T, H, K, V, 0)
+            == gdn.gdn_chunk_bwd_workspace_size(B, T, H, K, V, 0))
+    # packed: floor(T / 64) + N chunk slots
+    assert gdn.gdn_chunk_bwd_saved_workspace_size(3, 200, 2, 64, 64, 1) == 256 * ((200 // 64 + 3) * 2 * 64 * 64 * 4 // 256)
+    assert gdn.gdn_chunk_saved_size(1, 0, 1, 64, 64, 0) == 0
+    assert gdn.gdn_chunk_saved_size(1, 64, 1, 96, 64, 0) == 0  # unsupported
+
+
+def test_saved_route_host_validation(lib):
+    l = gdn.load()
+    need = gdn.gdn_chunk_saved_size(1, 128, 1, 64, 64, 0)
+    wneed = gdn.gdn_chunk_bwd_saved_workspace_size(1, 128, 1, 64, 64, 0)
+    assert need > 0 and wneed > 0
+
+    def fwd(saved, nbytes, out=FAKE, d_k=64):
+        return l.gdn_chunk_fwd_save(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, None, out, None,
+                                    1, 128, 1, d_k, 64, saved, nbytes, None)
+
+    def bwd(saved, nbytes, ws=FAKE, ws_bytes=wneed, dq=FAKE, d_v=64):
+        return l.gdn_chunk_bwd_saved(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, FAKE, None,
+                                     dq, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 1, 64, d_v,
+                                     saved, nbytes, ws, ws_bytes, None)
+    assert fwd(None, 0) == 1                  # saved buffer missing
+    assert fwd(FAKE, need - 1) == 1           # too small
+    assert fwd(FAKE + 16, need) == 3          # not 256-byte aligned
+    assert fwd(FAKE, need, out=None) == 1
+    assert fwd(FAKE, need, d_k=32) == 2
+    assert bwd(None, 0) == 1
+    assert bwd(FAKE, need - 1) == 1
+    assert bwd(FAKE + 64, need) == 3
+    assert bwd(FAKE, need, ws=None, ws_bytes=0) == 1   # gradient workspace missing
+    assert bwd(FAKE, need, ws_bytes=wneed - 1) == 1
+    assert bwd(FAKE, need, ws=FAKE + 32) == 3
+    assert bwd(FAKE, need, dq=None) == 1
+    assert bwd(FAKE, need, d_v=48) == 2
