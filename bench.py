@@ -412,6 +412,12 @@ def run_ours(args):
                                   stream, torch, max(5, min(args.steps, 20)))
     t_inf = max_over_ranks(t_inf, world, dev)
     roof_inf = roof(t_inf, f_fwd, b_fwd)
+    # ---- peak probes (our copy and tcgen05 GEMM kernels), in this run ----
+    probes = None if args.no_probes else measure_probes(gdn, torch, dev, stream)
+    if probes:
+        for r in (roof_fwd, roof_bwd, roof_inf):
+            if r["bound"] == "hbm":
+                r["frac_of_probe"] = r["achieved"] / probes["copy_gbs"]
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
     # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
@@ -464,6 +470,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "accuracy": accuracy,
+            "probes": probes,
             "decode": decode,
             "prologue": prologue,
         }
@@ -529,6 +536,41 @@ def measure_inference_fwd(gdn, tensors, dims, flush, stream, torch, steps, warmu
         e1.record(stream)
     torch.cuda.synchronize()
     return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
+
+
+def measure_probes(gdn, torch, dev, stream, copy_bytes=2 << 30, n=8192, steps=10, warmup=3):
+    """The peak probes in this run (our own kernels): a 2 GiB copy, counted
+    as bytes read + bytes written, and an n x n by n x n bf16 GEMM on the
+    tensor cores (2 n^3 FLOPs per call)."""
+    src = torch.empty(copy_bytes, dtype=torch.uint8, device=dev).random_(0, 255)
+    dst = torch.empty_like(src)
+
+    def timed(call):
+        for _ in range(warmup):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
+
+    t_copy = timed(lambda: gdn.gdn_probe_copy(src, dst, copy_bytes, stream))
+    del src, dst
+    g = torch.Generator(device=dev).manual_seed(11)
+    A = torch.randn((n, n), device=dev, generator=g).to(torch.bfloat16)
+    B = torch.randn((n, n), device=dev, generator=g).to(torch.bfloat16)
+    C = torch.empty((n, n), device=dev, dtype=torch.bfloat16)
+    t_gemm = timed(lambda: gdn.gdn_probe_gemm_bf16(A, B, C, n, n, n, stream))
+    st = gdn.gdn_get_last_device_error()
+    if st != 0:
+        raise SystemExit(f"device error in the probes: {gdn.gdn_status_string(st)}")
+    return {"copy_gbs": 2 * copy_bytes / t_copy / 1e9, "copy_bytes": copy_bytes,
+            "bf16_gemm_tflops": 2.0 * n ** 3 / t_gemm / 1e12, "gemm": f"{n}x{n} by {n}x{n}, bf16, fp32 accumulate",
+            "kernels": "gdn_probe_copy, gdn_probe_gemm_bf16 (tcgen05), median of "
+                       f"{steps} after {warmup} warm-up"}
 
 
 def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, steps=50, warmup=5):
@@ -702,6 +744,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-probes", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

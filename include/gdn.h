@@ -305,6 +305,31 @@ GDN_API gdn_status gdn_chunk_bwd_noalloc(const gdn_bf16* q, const gdn_bf16* k, c
                          int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
 /*
+ * Peak probes: the denominators of a roofline, measured on the caller's GPU
+ * in the same run as the operator ("Research Sprint Day 2 - Rooflines",
+ * section "Rooflines": FLOP/s from 8192 x 8192 by 8192 x 8192 dense matmuls,
+ * bandwidth from copying a 2 GB tensor).  Measurement tools, not part of
+ * the operator; both are asynchronous on `stream`.
+ *
+ * gdn_probe_copy: dst[0 .. bytes) = src[0 .. bytes) with 16-byte vector
+ * loads and stores (streaming cache hints).  bytes % 16 != 0 or a NULL
+ * pointer (bytes > 0) returns GDN_ERR_INVALID_ARG; a pointer that is not
+ * 16-byte aligned GDN_ERR_MISALIGNED.  The buffers must not overlap.
+ */
+GDN_API gdn_status gdn_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+
+/*
+ * gdn_probe_gemm_bf16: C = A B^T on the tensor cores (tcgen05, fp32
+ * accumulation in tensor memory, bf16 round-to-nearest-even output).
+ *   A (M, K), B (N, K), C (M, N): bf16, row-major, 16-byte aligned.
+ *   M % 128 == 0, N % 256 == 0, K % 64 == 0, each <= 65536, else
+ *   GDN_ERR_UNSUPPORTED; non-positive sizes or NULL GDN_ERR_INVALID_ARG.
+ * A bounded wait that gives up sets GDN_ERR_TIMEOUT in the device error word.
+ */
+GDN_API gdn_status gdn_probe_gemm_bf16(const gdn_bf16* A, const gdn_bf16* B, gdn_bf16* C, int M, int N, int K,
+                                       cudaStream_t stream);
+
+/*
  * Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points).  Library bookkeeping with no counterpart
  * on the pages; lets a caller count the kernels inside a timed region.

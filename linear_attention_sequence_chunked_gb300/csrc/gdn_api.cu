@@ -425,6 +425,28 @@ gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
                              err, stream);
 }
 
+gdn_status gdn_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream) {
+    if (bytes % 16) return GDN_ERR_INVALID_ARG;
+    if (bytes == 0) return GDN_OK;
+    if (!src || !dst) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return GDN_ERR_MISALIGNED;
+    if (!launched(gdn::launch_probe_copy(src, dst, bytes, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status gdn_probe_gemm_bf16(const gdn_bf16* A, const gdn_bf16* B, gdn_bf16* C, int M, int N, int K,
+                               cudaStream_t stream) {
+    if (M <= 0 || N <= 0 || K <= 0) return GDN_ERR_INVALID_ARG;
+    if (M % 128 || N % 256 || K % 64) return GDN_ERR_UNSUPPORTED;
+    if (M > 65536 || N > 65536 || K > 65536) return GDN_ERR_UNSUPPORTED;
+    if (!A || !B || !C) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GDN_ERR_MISALIGNED;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    if (!launched(gdn::launch_probe_gemm(A, B, C, M, N, K, err, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 gdn_status gdn_get_last_device_error(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
     int value = 0;

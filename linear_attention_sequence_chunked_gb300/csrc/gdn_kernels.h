@@ -156,6 +156,13 @@ struct PrologueArgs {
 
 cudaError_t launch_prologue_fwd(const PrologueArgs& a, cudaStream_t stream);
 cudaError_t launch_prologue_bwd(const PrologueArgs& a, cudaStream_t stream);
+
+// Peak probes (measurement only): a 16-byte-vector copy of `bytes` (a
+// multiple of 16), and the bf16 GEMM C[M][N] = A[M][K] B[N][K]^T with
+// M % 128 == 0, N % 256 == 0, K % 64 == 0.
+cudaError_t launch_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+cudaError_t launch_probe_gemm(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, int* err,
+                              cudaStream_t stream);
 // Warp-specialised tensor-core forward (prep and chain warpgroups);
 // wait_limit bounds every mbarrier wait (polls).
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);

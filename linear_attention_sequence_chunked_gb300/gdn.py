@@ -86,6 +86,10 @@ def load():
         lib.gdn_chunk_fwd_save.restype = i
         lib.gdn_chunk_bwd_saved.argtypes = [vp] * 5 + [f] + [vp] * 9 + [i] * 5 + [vp, sz, vp, sz, vp]
         lib.gdn_chunk_bwd_saved.restype = i
+        lib.gdn_probe_copy.argtypes = [vp, vp, sz, vp]
+        lib.gdn_probe_copy.restype = i
+        lib.gdn_probe_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, vp]
+        lib.gdn_probe_gemm_bf16.restype = i
         lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
         lib.gdn_chunk_bwd_noalloc.restype = i
         lib.gdn_kernel_launches.argtypes = []
@@ -179,6 +183,15 @@ def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_stat
                                     int(saved_bytes), _ptr(workspace), int(workspace_bytes),
                                     _stream(stream))
     _check(st, "gdn_chunk_bwd_saved")
+
+
+def gdn_probe_copy(src, dst, nbytes, stream=None):
+    _check(load().gdn_probe_copy(_ptr(src), _ptr(dst), int(nbytes), _stream(stream)), "gdn_probe_copy")
+
+
+def gdn_probe_gemm_bf16(A, B, C, M, N, K, stream=None):
+    _check(load().gdn_probe_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)),
+           "gdn_probe_gemm_bf16")
 
 
 def gdn_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,

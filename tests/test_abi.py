@@ -142,3 +142,19 @@ def test_saved_route_host_validation(lib):
     assert bwd(FAKE, need, ws=FAKE + 32) == 3
     assert bwd(FAKE, need, dq=None) == 1
     assert bwd(FAKE, need, d_v=48) == 2
+
+
+def test_probe_host_validation(lib):
+    l = gdn.load()
+    assert l.gdn_probe_copy(FAKE, FAKE + 4096, 0, None) == 0          # nothing to do
+    assert l.gdn_probe_copy(FAKE, FAKE + 4096, 24, None) == 1         # not a multiple of 16
+    assert l.gdn_probe_copy(None, FAKE, 32, None) == 1
+    assert l.gdn_probe_copy(FAKE + 8, FAKE + 4096, 32, None) == 3
+    g = l.gdn_probe_gemm_bf16
+    assert g(FAKE, FAKE, FAKE, 0, 256, 64, None) == 1
+    assert g(FAKE, FAKE, FAKE, 192, 256, 64, None) == 2                 # M % 128
+    assert g(FAKE, FAKE, FAKE, 128, 128, 64, None) == 2                 # N % 256
+    assert g(FAKE, FAKE, FAKE, 128, 256, 96, None) == 2                 # K % 64
+    assert g(FAKE, FAKE, FAKE, 128, 256, 65536 + 64, None) == 2
+    assert g(None, FAKE, FAKE, 128, 256, 64, None) == 1
+    assert g(FAKE, FAKE + 2, FAKE, 128, 256, 64, None) == 3
