@@ -21,8 +21,10 @@
 // next item's K/Q tiles (TMA), T tiles and first state tiles (bulk copies)
 // land in buffers the current item no longer reads: the K/Q tiles alternate
 // between two buffers, the other one holding the current item's -dBhat-side
-// tiles.  Within an item the dS tiles of the next value slice load as soon as
-// the products that read this slice's dS have completed.  Warps w and w + 4
+// tiles.  Within an item the next value slice's S0 tiles load into this
+// slice's dS buffer as soon as the products that read dS have completed, and
+// its dS tiles into this slice's S0 buffer after the last product that reads
+// S0 (the two state buffers swap roles every slice).  Warps w and w + 4
 // share a TMEM subpartition and
 // split the 64 columns of each accumulator row between them, and within a
 // warp lanes l and l + 16 take 16 columns each of row 16 w + l (tcgen05.ld
@@ -158,18 +160,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto state_src = [&](const float* base, const Item& it, int vs) {
         return reinterpret_cast<const uint8_t*>(base) + ((slot_of(it) * H + it.h) * nsl + vs) * (2LL * dk * 128);
     };
-    auto issue_s0 = [&](const Item& it, int vs) {
+    // The two state buffers SA and SB swap roles every value slice: slice vs
+    // reads S0 from SA and dS from SB when vs is even, the other way round
+    // when odd.  So the next slice's S0 can land in this slice's dS buffer
+    // as soon as the products that read dS complete, and its dS in this
+    // slice's S0 buffer after the last product that reads S0.
+    auto issue_s0 = [&](const Item& it, int vs, int dst) {
         const uint8_t* s = state_src(p.chunk_states, it, vs);
         mbar_arrive_expect_tx(s0bar, 2 * nb);
-        bulk_g2s(smem_u32(sm + oSA), s, nb, s0bar);
-        bulk_g2s(smem_u32(sm + oSA + kTileS), s + nb, nb, s0bar);
+        bulk_g2s(smem_u32(sm + dst), s, nb, s0bar);
+        bulk_g2s(smem_u32(sm + dst + kTileS), s + nb, nb, s0bar);
         s0_out = true;
     };
-    auto issue_ds = [&](const Item& it, int vs) {
+    auto issue_ds = [&](const Item& it, int vs, int dst) {
         const uint8_t* s = state_src(p.chunk_dstates, it, vs);
         mbar_arrive_expect_tx(dsbar, 2 * nb);
-        bulk_g2s(smem_u32(sm + oSB), s, nb, dsbar);
-        bulk_g2s(smem_u32(sm + oSB + kTileS), s + nb, nb, dsbar);
+        bulk_g2s(smem_u32(sm + dst), s, nb, dsbar);
+        bulk_g2s(smem_u32(sm + dst + kTileS), s + nb, nb, dsbar);
         ds_out = true;
     };
 
@@ -190,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (f < total) {
             issue_inputs(cur, smem_u32(sm + oKQ0));
-            issue_s0(cur, 0);
-            issue_ds(cur, 0);
+            issue_s0(cur, 0, oSA);
+            issue_ds(cur, 0, oSB);
         }
     }
     // d_k = 64: key rows 64-127 of the state tiles stay zero (the copies
@@ -382,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // per-row accumulators (thread mrow) across value slices
         float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
         for (int vs = 0; vs < nsl; ++vs) {
+            const int oS0 = (vs & 1) ? oSB : oSA;  // this slice's S0 tiles
+            const int oDS = (vs & 1) ? oSA : oSB;  // this slice's dS tiles
             // ---- slice loads: S0 tiles, dO tile, V row ----
             wait_copy(s0bar, s0phase, s0_out);
 #pragma unroll
@@ -406,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
 #pragma unroll
                     for (int s = 0; s < kDk / 16; ++s) {
-                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA) + s * 2048, kTileS, 1024), id_k, s > 0);
-                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSA + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oS0) + s * 2048, kTileS, 1024), id_k, s > 0);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oS0 + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
                     }
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
@@ -419,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oSA) + s * 32, 0, 1024), id_n, (vs > 0 || s > 0) ? 1u : 0u);
-                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024), id_n, 1);
+                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oS0) + s * 32, 0, 1024), id_n, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cU, ao, desc_sw128(t64(oS0 + kTileS) + s * 32, 0, 1024), id_n, 1);
                     }
                 }
                 __syncwarp();
@@ -451,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
                     for (int s = 0; s < kDk / 16; ++s) {
-                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB) + s * 2048, kTileS, 1024), id_k, s > 0);
-                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oSB + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS) + s * 2048, kTileS, 1024), id_k, s > 0);
+                        mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
                     }
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
@@ -476,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c4 = 0; c4 < 4; ++c4) {
                         const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
                         float ah[8], al[8], bh[8], bl[8];
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oSA + off), ah);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oSA + kTileS + off), al);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oSB + off), bh);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oSB + kTileS + off), bl);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + off), ah);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + kTileS + off), al);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + off), bh);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + kTileS + off), bl);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
                     }
@@ -541,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t eh = desc_sw128(t64(oRC) + s * 32, 0, 1024);
                         const uint64_t el = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
-                        const uint64_t sbh = desc_sw128(t64(oSB) + s * 32, 0, 1024);
-                        const uint64_t sbl = desc_sw128(t64(oSB + kTileS) + s * 32, 0, 1024);
+                        const uint64_t sbh = desc_sw128(t64(oDS) + s * 32, 0, 1024);
+                        const uint64_t sbl = desc_sw128(t64(oDS + kTileS) + s * 32, 0, 1024);
                         mma_bf16(tmem + cdK, eh, sbh, id_n, (vs > 0 || s > 0) ? 1u : 0u);
                         mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
                         mma_bf16(tmem + cdK, el, sbh, id_n, 1);
@@ -552,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_sync_wait();
             // every product that reads this slice's dS tiles has completed
-            if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1);
+            // the next slice's S0 goes into this slice's (now free) dS buffer
+            if (tid == 0 && vs + 1 < nsl && !failed) issue_s0(cur, vs + 1, oDS);
             {
                 // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RB, Y -> RD
                 const float bi = bv[mrow], gi = gam[mrow];
@@ -605,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdA, ch_, dh, id_c, (vs > 0 || s > 0) ? 1u : 0u);
                         mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
                         mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
-                        const uint64_t sah = desc_sw128(t64(oSA) + s * 32, 0, 1024);
-                        const uint64_t sal = desc_sw128(t64(oSA + kTileS) + s * 32, 0, 1024);
+                        const uint64_t sah = desc_sw128(t64(oS0) + s * 32, 0, 1024);
+                        const uint64_t sal = desc_sw128(t64(oS0 + kTileS) + s * 32, 0, 1024);
                         const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
                         const uint64_t yl = desc_sw128(t64(oRD + kTile64) + s * 32, 0, 1024);
                         mma_bf16(tmem + cdK, yh, sah, id_n, 1);
@@ -629,7 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (vs + 1 < nsl) fetch_rows(cur, vs + 1);  // while the batch runs
             mma_sync_wait();
             __syncthreads();
-            if (tid == 0 && vs + 1 < nsl && !failed) issue_s0(cur, vs + 1);  // the S0 tiles are free
+            // the S0 tiles are free: the next slice's dS goes there
+            if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1, oS0);
             if (*abort_flag) break;
         }
         if (*abort_flag) break;
@@ -643,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- chunk-wide part (K K^T and Q K^T came with the last slice's batch) ----
         if (fn < total && tid == 0 && !failed) {
             issue_inputs(nxt, smem_u32(sm + oRC));
-            issue_s0(nxt, 0);
-            issue_ds(nxt, 0);
+            issue_s0(nxt, 0, oSA);
+            issue_ds(nxt, 0, oSB);
         }
         // column-sum terms E [64][64] fp32 in the (dead) P tiles, column index
         // XOR-swizzled by the row so that row-parallel writes and
