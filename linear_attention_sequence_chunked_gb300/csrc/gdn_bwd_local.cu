@@ -71,8 +71,8 @@ constexpr int oKQ1 = oRB + 2 * kTile64;         // [K;Q] of odd items; the other
 constexpr int oVec = oKQ1 + 2 * kRegionBytes;   // g, beta, G, gam, dec, colsum
 constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
 constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half
-constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles
-constexpr int oMisc = oBar + 32;                // TMEM slot, abort flag
+constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles, off-path MMA
+constexpr int oMisc = oBar + 40;                // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 232448, "shared memory");
@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ibar = smem_u32(barp + 1);
     const uint32_t s0bar = smem_u32(barp + 2);
     const uint32_t dsbar = smem_u32(barp + 3);
+    // MMAs whose results only the item's outputs read (U += dO S0^T, dP +=
+    // dO Delta^T) are committed here, after the products an epilogue waits
+    // for, so they run in that epilogue's window
+    const uint32_t nbar = smem_u32(barp + 4);
 
     // item f of the flat (chunk, head, sequence) order; false for chunks past
     // a sequence's end (and sequences whose bounds are invalid)
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(barp + i), 1);
+        for (int i = 0; i < 5; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
         *abort_flag = 0;
         if (use_tma) {
@@ -228,6 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
         }
         phase ^= 1u;
+        tc_fence_after();
+    };
+    // wait for the last commit on `bar` (issued inside an MMA batch)
+    auto mma_wait = [&]() {
+        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) {
+            failed = true;
+            *abort_flag = 1;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+    };
+    uint32_t nphase = 0;
+    auto off_path_wait = [&]() {
+        if (!mbar_wait(nbar, nphase, kDefaultWaitLimit)) {
+            failed = true;
+            *abort_flag = 1;
+        }
+        nphase ^= 1u;
         tc_fence_after();
     };
     uint32_t iphase = 0, s0phase = 0, dsphase = 0;
@@ -424,17 +446,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
                         mma_bf16(tmem + cX2, desc_sw128(t64(oP + kTile64) + s * 2048, kTile64, 1024), bo, id_p, 1);
                     }
-                    // B = S0 tile read K-major: [N = key row d][K = value column]
+                    mma_commit(bar);  // K S0 and P^T dO: the R epilogue reads them
+                    // U += dO S0^T (B = S0 tile read K-major: [N = key row d][K =
+                    // value column]), off the path: it runs in the R epilogue
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
                         mma_bf16(tmem + cU, ao, desc_sw128(t64(oS0) + s * 32, 0, 1024), id_n, (vs > 0 || s > 0) ? 1u : 0u);
                         mma_bf16(tmem + cU, ao, desc_sw128(t64(oS0 + kTileS) + s * 32, 0, 1024), id_n, 1);
                     }
+                    mma_commit(nbar);
                 }
                 __syncwarp();
             }
-            mma_sync_wait();
+            mma_wait();
             float ks0[16], pdo[16];
             ld_cols(cX1, ks0);
             ld_cols(cX2, pdo);
@@ -495,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             mma_sync_wait();
+            off_path_wait();  // U of this slice (long done: it ran in the R epilogue)
             {
                 // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
                 // dec o Delta -> RC;  dd = dec * sum_v (K dS) Delta for the decay term of dG
@@ -520,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncthreads();
 
-            // ---- batch 3: dBhat = T^T dDelta -> X1;  dP += dO Delta^T;  dK += (dec o Delta) dS^T ----
+            // ---- batch 3: dBhat = T^T dDelta -> X1;  dK += (dec o Delta) dS^T;  dP += dO Delta^T (off the path) ----
             if (warp == 0) {
                 if (elect_one()) {
                     tc_fence_after();
@@ -537,14 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cX1, th, dl, id_b, 1);
                         mma_bf16(tmem + cX1, tl, dh, id_b, 1);
                     }
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
-                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                        mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
-                        mma_bf16(tmem + cdP, ao, dl, id_p, 1);
-                    }
                     // B = dS tile read K-major: [N = key row d][K = value column]
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
@@ -556,10 +574,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
                         mma_bf16(tmem + cdK, el, sbh, id_n, 1);
                     }
+                    mma_commit(bar);  // dBhat (the dV epilogue) and the last reader of the dS tiles
+                    // dP += dO Delta^T, read only at the item's end: it runs in the dV epilogue
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdP, ao, dh, id_p, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cdP, ao, dl, id_p, 1);
+                    }
+                    mma_commit(nbar);
                 }
                 __syncwarp();
             }
-            mma_sync_wait();
+            mma_wait();
             // every product that reads this slice's dS tiles has completed
             // the next slice's S0 goes into this slice's (now free) dS buffer
             if (tid == 0 && vs + 1 < nsl && !failed) issue_s0(cur, vs + 1, oDS);
@@ -638,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (vs + 1 < nsl) fetch_rows(cur, vs + 1);  // while the batch runs
             mma_sync_wait();
+            off_path_wait();  // dP: the next slice rewrites the dO and Delta tiles it reads
             __syncthreads();
             // the S0 tiles are free: the next slice's dS goes there
             if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1, oS0);
