@@ -785,9 +785,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) { aborted = true; break; }
 
             // gram K K^T and Q K^T (two M = 64 products), running while the
-            // gates are formed
+            // gates are formed.  Forward with T tiles given (only Q K^T): issued
+            // once the chain's T R of the previous chunk has completed, so it
+            // runs in that chunk's Delta epilogue window instead of beside the
+            // state update that follows it
             if (warp == 8) {
-                if (elect_one()) {
+                bool go = true;
+                if (!kBwd && load_t && it > 0) {
+                    go = __all_sync(0xffffffffu, mbar_wait(bar(B_D), (it - 1) & 1, wl));
+                    if (!go && lane == 0) *abort_flag = 1;
+                }
+                if (go && elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_g = idesc(kFmtBf16, 0, 0, 64, 64);
                     const uint32_t stage_a = smem_u32(stage);
