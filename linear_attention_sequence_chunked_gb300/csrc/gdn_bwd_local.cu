@@ -85,6 +85,7 @@ struct Item {
 
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_bwd_local_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                         const __grid_constant__ CUtensorMap tmap_dq, const __grid_constant__ CUtensorMap tmap_dk,
                          const BwdLocalArgs p) {
     const int H = p.H, V = p.d_v, dk = p.d_k;
     const int tid = threadIdx.x;
@@ -426,6 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             unpack8(v_raw[1], vrow + 8);
             fence_proxy_async_smem();
             tc_fence_before();
+            // the previous item's dq / dk tile stores have read the R tiles
+            if (tid == 0 && vs == 0) bulk_wait_read_all();
             __syncthreads();
 
             // ---- batch 1: K S0 -> X1, P^T dO -> X2, U += dO S0^T ----
@@ -783,15 +786,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gi = gam[i];
             // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
             float dgq = 0.f;
-#pragma unroll 1
+            // all six accumulator reads in flight before the one wait
+            float u[2][16], q2[2][16], kk2[2][16];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
+                tmem_ld_pair16(tmem + lb + cU + cpair, u[r]);
+                tmem_ld_pair16(tmem + lb + cX1 + cpair, q2[r]);
+                tmem_ld_pair16(tmem + lb + cdK + cpair, kk2[r]);
+            }
+            tmem_ld_wait();
+            // a full chunk at d_k = 128 stages its dq / dk rows in the (free) R
+            // tiles, 128-byte swizzled like the q / k tiles, for one TMA store
+            // per 64-column region: consecutive tokens are H d_k apart in
+            // global memory, so per-thread 16-byte stores would touch a sector
+            // each; a ragged chunk stores per thread (a box would cross into
+            // the next rows)
+            const bool tma_out = use_tma && nv == kChunk;
+#pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int c16 = 4 * hc + 2 * r + (lane >> 4);
-                const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
-                float u[16], q2[16], kk2[16];
-                tmem_ld_pair16(tmem + lb + cU + cpair, u);
-                tmem_ld_pair16(tmem + lb + cX1 + cpair, q2);
-                tmem_ld_pair16(tmem + lb + cdK + cpair, kk2);
-                tmem_ld_wait();
                 const int region = c16 >> 2, cc = (c16 & 3) * 16;
                 float qrow[16];
                 {
@@ -800,24 +814,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
                 }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[e], dgq);
-                if (i < nv && c16 * 16 < dk) {
+                for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[r][e], dgq);
+                uint4 wq4[2], wk4[2];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t wq[4], wk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = half * 8 + 2 * e;
+                        wq[e] = pack_bf16x2(fmaf(scale * gi, u[r][c], q2[r][c]), fmaf(scale * gi, u[r][c + 1], q2[r][c + 1]));
+                        wk[e] = pack_bf16x2(kk2[r][c], kk2[r][c + 1]);
+                    }
+                    wq4[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    wk4[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                }
+                if (tma_out) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t off = region * kTile64 + sw128_offset(i, cc * 2 + 16 * half);
+                        *reinterpret_cast<uint4*>(sm + oRA + off) = wq4[half];
+                        *reinterpret_cast<uint4*>(sm + oRB + off) = wk4[half];
+                    }
+                } else if (i < nv && c16 * 16 < dk) {
                     uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
                     uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        uint32_t wq[4], wk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = half * 8 + 2 * e;
-                            wq[e] = pack_bf16x2(fmaf(scale * gi, u[c], q2[c]), fmaf(scale * gi, u[c + 1], q2[c + 1]));
-                            wk[e] = pack_bf16x2(kk2[c], kk2[c + 1]);
-                        }
-                        dq[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                        dkp[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                        dq[half] = wq4[half];
+                        dkp[half] = wk4[half];
                     }
                 }
             }
+            if (tma_out) fence_proxy_async_smem();
             // dG_63 also collects the decay terms sum_j dd_j (all rows, both halves)
             {
                 float v = acc_dd;
@@ -842,6 +870,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 part[4] = dbeta_a;
             }
             __syncthreads();
+            if (tma_out && tid == 0) {
+                const int z = static_cast<int>(row_base + c0);
+#pragma unroll
+                for (int region = 0; region < 2; ++region) {
+                    tma_store_3d(&tmap_dq, region * 64, h, z, smem_u32(sm + oRA + region * kTile64));
+                    tma_store_3d(&tmap_dk, region * 64, h, z, smem_u32(sm + oRB + region * kTile64));
+                }
+                bulk_commit();
+            }
             if (lead && hc == 0) {
                 float dgam = acc_dgam + dgq + part[1];
                 float sdd = 0.f;
@@ -901,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i_out) mbar_wait(ibar, iphase, kDefaultWaitLimit);
         if (s0_out) mbar_wait(s0bar, s0phase, kDefaultWaitLimit);
         if (ds_out) mbar_wait(dsbar, dsphase, kDefaultWaitLimit);
+        bulk_wait_all();  // the dq / dk tile stores
     }
     tc_fence_before();
     __syncthreads();
@@ -912,10 +950,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (a.max_chunks == 0) return cudaSuccess;
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
-    CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
+    CUtensorMap mk, mq, mdq, mdk;  // used for d_k = 128 only (d_k = 64 tiles use plain loads and stores)
     memset(&mk, 0, sizeof(mk));
     memset(&mq, 0, sizeof(mq));
-    if (rows > 0 && a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
+    memset(&mdq, 0, sizeof(mdq));
+    memset(&mdk, 0, sizeof(mdk));
+    if (rows > 0 && a.d_k == kDk &&
+        (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H) ||
+         !make_qk_map(&mdq, a.dq, rows, a.H) || !make_qk_map(&mdk, a.dk, rows, a.H)))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
@@ -926,7 +968,7 @@ cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long items = static_cast<long long>(a.max_chunks) * a.H * a.N;
     const int grid = static_cast<int>(items < sms ? items : sms);
-    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, a);
+    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, mdq, mdk, a);
     return cudaGetLastError();
 }
 

@@ -87,6 +87,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         : "memory");
 }
 
+// shared -> global tile store, tracked by the issuing thread's bulk groups
+// (x is the innermost coordinate; never negative for a store)
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
 // Untiled bulk copies (16-byte aligned addresses, size a multiple of 16).
 // global -> shared, completion counted on the mbarrier as transaction bytes
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -74,6 +74,26 @@ def run_bwd(wl, dev="cuda"):
     return res
 
 
+def run_train(wl, dev="cuda"):
+    """The training route: forward keeping its chunk states, backward from
+    them.  Returns (out, final_state, gradients) like run_fwd and run_bwd."""
+    import torch
+    from linear_attention_sequence_chunked_gb300 import gdn
+    d = to_device(wl, dev)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"])
+    common = dict(scale=wl.scale, initial_state=d["initial_state"], cu_seqlens=d["cu_seqlens"])
+    out, fs, saved = gdn.chunk_gated_delta_rule_fwd(*args, save_for_backward=True, **common)
+    r = gdn.chunk_gated_delta_rule_bwd(*args, d["d_out"], d_final_state=d["d_final_state"], saved=saved,
+                                       **common)
+    st = gdn.gdn_get_last_device_error()
+    assert st == 0, gdn.gdn_status_string(st)
+    torch.cuda.synchronize()
+    res = {n: bf16_to_np(r[n]) for n in ("dq", "dk", "dv", "dbeta")}
+    res["dg"] = r["dg"].cpu().numpy()
+    res["dS0"] = r["d_initial_state"].cpu().numpy()
+    return bf16_to_np(out), fs.cpu().numpy(), res
+
+
 def unit_rows(wl, units):
     """Boolean masks selecting the (sequence, head) units in token tensors."""
     bounds = wl.seq_bounds()
