@@ -86,7 +86,7 @@ struct Item {
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_bwd_local_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_dq, const __grid_constant__ CUtensorMap tmap_dk,
-                         const BwdLocalArgs p) {
+                         const __grid_constant__ CUtensorMap tmap_dv, const BwdLocalArgs p) {
     const int H = p.H, V = p.d_v, dk = p.d_k;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -427,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             unpack8(v_raw[1], vrow + 8);
             fence_proxy_async_smem();
             tc_fence_before();
-            // the previous item's dq / dk tile stores have read the R tiles
-            if (tid == 0 && vs == 0) bulk_wait_read_all();
+            // the previous item's dq / dk and the previous slice's dV tile
+            // stores have read their source tiles (rewritten in this slice)
+            if (tid == 0) bulk_wait_read_all();
             __syncthreads();
 
             // ---- batch 1: K S0 -> X1, P^T dO -> X2, U += dO S0^T ----
@@ -607,17 +608,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sv = fmaf(vrow[c], db[c], sv);
                     sk = fmaf(ks0[c], db[c], sk);
                 }
-                if (mrow < nv) {
+                uint4 dv4[2];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
+                    dv4[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                if (nv == kChunk) {
+                    // a full chunk stages this slice's dV rows in the dead (dec o
+                    // Delta) tile, 128-byte swizzled, for one TMA store
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+                        *reinterpret_cast<uint4*>(sm + oRC + sw128_offset(mrow, cb * 2 + 16 * half)) = dv4[half];
+                } else if (mrow < nv) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
-                        dst[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
+                    for (int half = 0; half < 2; ++half) dst[half] = dv4[half];
                 }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) t16[c] = -db[c];
@@ -631,6 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
+            if (nv == kChunk && tid == 0) {
+                tma_store_3d(&tmap_dv, vs * kVs, h, static_cast<int>(row_base + c0), smem_u32(sm + oRC));
+                bulk_commit();
+            }
 
             // ---- batch 4: dA += (-dBhat) Delta^T;  dK += Y S0^T ----
             if (warp == 0) {
@@ -686,6 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- chunk-wide part (K K^T and Q K^T came with the last slice's batch) ----
         if (fn < total && tid == 0 && !failed) {
+            bulk_wait_read_all();  // the last slice's dV tile store has read its source
             issue_inputs(nxt, smem_u32(sm + oRC));
             issue_s0(nxt, 0, oSA);
             issue_ds(nxt, 0, oSB);
@@ -947,6 +962,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+// 3-D view {inner, head, token row} of a (rows, H, inner) bf16 tensor, box
+// {64, 1, 64}: one 64-column slice of a chunk's rows, 128-byte swizzled.
+bool make_rows_map(CUtensorMap* m, const uint16_t* base, long long rows, int H, int inner) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(H) * inner * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (a.max_chunks == 0) return cudaSuccess;
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
@@ -959,6 +990,9 @@ cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
         (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H) ||
          !make_qk_map(&mdq, a.dq, rows, a.H) || !make_qk_map(&mdk, a.dk, rows, a.H)))
         return cudaErrorInvalidValue;
+    CUtensorMap mdv;  // dV tile stores (full chunks, any d_k)
+    memset(&mdv, 0, sizeof(mdv));
+    if (rows > 0 && !make_rows_map(&mdv, a.dv, rows, a.H, a.d_v)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -968,7 +1002,7 @@ cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long items = static_cast<long long>(a.max_chunks) * a.H * a.N;
     const int grid = static_cast<int>(items < sms ? items : sms);
-    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, mdq, mdk, a);
+    gdn_bwd_local_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, mdq, mdk, mdv, a);
     return cudaGetLastError();
 }
 
