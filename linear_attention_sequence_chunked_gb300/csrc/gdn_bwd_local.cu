@@ -962,22 +962,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-namespace {
-// 3-D view {inner, head, token row} of a (rows, H, inner) bf16 tensor, box
-// {64, 1, 64}: one 64-column slice of a chunk's rows, 128-byte swizzled.
-bool make_rows_map(CUtensorMap* m, const uint16_t* base, long long rows, int H, int inner) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(H) * inner * 2};
-    cuuint32_t box[3] = {64, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-}  // namespace
-
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream) {
     if (a.max_chunks == 0) return cudaSuccess;
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
