@@ -46,20 +46,6 @@ constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(3 * kTB * 4 <= 2 * kKRegion, "T blocks fit in the K tile");
 
-// One 8-value piece (row `row`, columns 8 ch ..) of the T hi/lo tiles in global memory.
-__device__ __forceinline__ void put_split_global(uint8_t* tile, int row, int ch, const float* x8) {
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float a = x8[2 * e], b = x8[2 * e + 1];
-        hw[e] = cvt_bf16x2(a, b);
-        lw[e] = cvt_bf16x2(a - __uint_as_float(hw[e] << 16), b - __uint_as_float(hw[e] & 0xffff0000u));
-    }
-    const uint32_t off = sw128_offset(row, ch * 16);
-    *reinterpret_cast<uint4*>(tile + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(tile + kTile64 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-}
-
 __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTArgs p) {
     const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int H = p.H, dk = p.d_k;
@@ -324,16 +310,26 @@ __global__ void __launch_bounds__(kThreads, 6) gdn_chunk_t_kernel(const ChunkTAr
     __syncthreads();
     {
         // column col of T = row col of the tile (read MN-major for T, K-major
-        // for T^T); this thread writes entries 32 hf .. 32 hf + 31 of it
+        // for T^T); this thread writes entries 32 hf .. 32 hf + 31 of it.  The
+        // hi/lo tiles are staged in the A^T scratch (dead now) and leave in
+        // one 16 KB bulk copy: per-thread 16-byte stores into 128-byte tile
+        // rows would each touch their own sector
         const int col = q & 63, hf = q >> 6;
         const float* src = col < 32 ? (hf ? T10 : T00) : (hf ? T11 : nullptr);
         const int cc = col & 31;
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = src ? src[i * kTS + cc] : 0.f;
-        uint8_t* tile = p.chunk_T + (slot * H + h) * static_cast<long long>(kChunkTBytes);
+        uint8_t* stage = sm + oA;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) put_split_global(tile, col, 4 * hf + c4, v + 8 * c4);
+        for (int c4 = 0; c4 < 4; ++c4) store_split_chunk(stage, stage + kTile64, col, 4 * hf + c4, v + 8 * c4);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (q == 0) {
+        bulk_s2g(p.chunk_T + (slot * H + h) * static_cast<long long>(kChunkTBytes), smem_u32(sm + oA), kChunkTBytes);
+        bulk_commit();
+        bulk_wait_all();
     }
     if (!ok) {  // the product never signalled: record it and let it land before the TMEM is freed
         record_error(p.err, kErrTimeout);
