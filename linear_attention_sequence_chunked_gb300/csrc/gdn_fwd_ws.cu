@@ -445,6 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // ... and so have the bulk copies
                 named_bar(1);
                 if (*abort_flag) { aborted = true; break; }
+                // every MMA that reads this chunk's K/Q stage has completed (K S,
+                // the state update, Q S; the prep's gram long before): the stage
+                // takes chunk ci + 2's tiles now, a whole epilogue window earlier
+                // than after the output
+                if (t == 0) {
+                    if (use_tma) {
+                        if (ci + kStages < nchunks) {
+                            issue_tma(ci + kStages);
+                            tma_issued = ci + kStages + 1;  // thread 0's count drives the drain
+                        }
+                    } else {
+                        mbar_arrive(bar(B_SFREE0 + st));
+                    }
+                }
 
                 // ---- C6: state update ----
                 {
@@ -466,18 +480,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (want_out && !mbar_wait(bar(B_PD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
-                // every MMA that reads this chunk's K/Q stage has completed: K S,
-                // the state update (warp 0) and Q S (issuer warp, tracked by P Delta)
-                if (t == 0 && !*abort_flag) {
-                    if (use_tma) {
-                        if (ci + kStages < nchunks) {
-                            issue_tma(ci + kStages);
-                            tma_issued = ci + kStages + 1;  // thread 0's count drives the drain
-                        }
-                    } else {
-                        mbar_arrive(bar(B_SFREE0 + st));
-                    }
-                }
                 // ---- output ----
                 if (want_out) {
                     const bool mine = hrow < nv;
