@@ -439,7 +439,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (!mbar_wait(bar(B_S), ph, wl)) *abort_flag = 1;
-                // C6 overwrites the S tiles: Q S (issuer warp) has read them
+                tc_fence_after();
+                // ---- C6: state update (its TMEM read and FMAs run while Q S,
+                // the last reader of the S tiles it overwrites, completes) ----
+                {
+                    float row[32];
+                    const float gC = gam[63];
+                    ld_s32(kColS, row);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c]);
+                }
+                // the S tiles get overwritten: Q S (issuer warp) has read them
                 if (want_out && !mbar_wait(bar(B_QSD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // ... and so have the bulk copies
@@ -460,15 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
 
-                // ---- C6: state update ----
-                {
-                    float row[32];
-                    const float gC = gam[63];
-                    ld_s32(kColS, row);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], row[c]);
-                    store_split_half(Shi, Slo, srow_all, hs, S);
-                }
+                store_split_half(Shi, Slo, srow_all, hs, S);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar(1);
