@@ -18,6 +18,8 @@
 // before the row sums (warp shuffles); lane r computes row r's gates.  The
 // per-head sums run in a second kernel, one CTA per head, in a fixed order,
 // so they are deterministic.
+#include <cooperative_groups.h>
+
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -153,20 +155,31 @@ __global__ void __launch_bounds__(32 * kWarps) gdn_prologue_bwd_kernel(const Pro
 }
 
 // Per-head sums over every (token) row: ddt_bias[h] = sum da, dA_log[h] =
-// sum dg g (decay gate).  One CTA per head; each thread sums a fixed set of
-// rows (four accumulators, four loads in flight), then a fixed-order tree.
+// sum dg g (decay gate).  One cluster of kSumSplit CTAs per head: CTA r sums
+// the r-th contiguous part of the rows (each thread a fixed set of rows, four
+// accumulators, four loads in flight, then a fixed-order tree), and CTA 0 adds
+// the parts in rank order through distributed shared memory, so the result
+// is deterministic.  (A head's rows are H floats apart: one CTA per head left
+// most of the GPU idle on a strided read.)
 constexpr int kSumThreads = 1024;
-__global__ void __launch_bounds__(kSumThreads) gdn_prologue_head_sums_kernel(const PrologueArgs p) {
-    const int h = blockIdx.x;
+constexpr int kSumSplit = 8;
+__global__ void __cluster_dims__(kSumSplit, 1, 1) __launch_bounds__(kSumThreads)
+    gdn_prologue_head_sums_kernel(const PrologueArgs p) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int h = blockIdx.x / kSumSplit;
+    const int part = static_cast<int>(cluster.block_rank());
+    const long long rows = p.rows;
+    const long long r0 = rows * part / kSumSplit, r1 = rows * (part + 1) / kSumSplit;
     const bool decay = p.gate_mode == 1;
     const float eA = decay ? expf(p.A_log[h]) : 0.f;
     const float dtb = p.dt_bias ? p.dt_bias[h] : 0.f;
     float s_da[4] = {0.f, 0.f, 0.f, 0.f}, s_dA[4] = {0.f, 0.f, 0.f, 0.f};
-    for (long long t0 = threadIdx.x; t0 < p.rows; t0 += 4LL * kSumThreads) {
+    for (long long t0 = r0 + threadIdx.x; t0 < r1; t0 += 4LL * kSumThreads) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const long long t = t0 + static_cast<long long>(u) * kSumThreads;
-            if (t < p.rows) {
+            if (t < r1) {
                 const long long row = t * p.H + h;
                 s_da[u] += p.da[row];
                 if (decay) s_dA[u] = fmaf(p.dg[row], -eA * softplusf_(p.a[row] + dtb), s_dA[u]);
@@ -184,10 +197,18 @@ __global__ void __launch_bounds__(kSumThreads) gdn_prologue_head_sums_kernel(con
         }
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        if (p.ddt_bias) p.ddt_bias[h] = red[0][0];
-        if (p.dA_log && decay) p.dA_log[h] = red[1][0];
+    cluster.sync();  // every part's sums are in its shared memory
+    if (part == 0 && threadIdx.x == 0) {
+        float da = 0.f, dA = 0.f;
+        for (int r = 0; r < kSumSplit; ++r) {
+            const float* rr = cluster.map_shared_rank(&red[0][0], r);
+            da += rr[0];
+            dA += rr[kSumThreads];
+        }
+        if (p.ddt_bias) p.ddt_bias[h] = da;
+        if (p.dA_log && decay) p.dA_log[h] = dA;
     }
+    cluster.sync();  // the parts' shared memory stays until CTA 0 has read it
 }
 
 }  // namespace
@@ -213,7 +234,7 @@ cudaError_t launch_prologue_bwd(const PrologueArgs& a, cudaStream_t stream) {
         gdn_prologue_bwd_kernel<128><<<grid, 32 * kWarps, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (a.ddt_bias || a.dA_log) gdn_prologue_head_sums_kernel<<<a.H, kSumThreads, 0, stream>>>(a);
+    if (a.ddt_bias || a.dA_log) gdn_prologue_head_sums_kernel<<<a.H * kSumSplit, kSumThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
