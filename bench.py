@@ -666,7 +666,9 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
     its inputs in from pinned host memory and its outputs and gradients back,
     all inside the timed region.  A step's inputs sit in one pinned host
     block and its results in one device block (each tensor a 256-byte
-    aligned view), so each direction is one copy per step.  Steps are
+    aligned view), so each direction is one copy per step (the results two:
+    the forward's as soon as the forward ends, the gradients after the
+    backward).  Steps are
     pipelined the way a prefetching loader runs them: step i + 1's inputs go
     in (copy stream) and step i - 1's results come out (a second copy stream)
     while step i computes; device blocks alternate between two sets, ordered
@@ -677,10 +679,11 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
     in_specs = [("q", (B, T, H, K), torch.int16), ("k", (B, T, H, K), torch.int16),
                 ("v", (B, T, H, V), torch.int16), ("g", (B, T, H), torch.float32),
                 ("beta", (B, T, H), torch.int16), ("dO", (B, T, H, V), torch.int16)]
-    out_specs = [("out", (B, T, H, V), torch.int16), ("dq", (B, T, H, K), torch.int16),
-                 ("dk", (B, T, H, K), torch.int16), ("dv", (B, T, H, V), torch.int16),
-                 ("dg", (B, T, H), torch.float32), ("dbeta", (B, T, H), torch.int16),
-                 ("fs", tuple(fs.shape), torch.float32), ("dS0", tuple(dS0.shape), torch.float32)]
+    # the forward's results first: they start back while the backward runs
+    out_specs = [("out", (B, T, H, V), torch.int16), ("fs", tuple(fs.shape), torch.float32),
+                 ("dq", (B, T, H, K), torch.int16), ("dk", (B, T, H, K), torch.int16),
+                 ("dv", (B, T, H, V), torch.int16), ("dg", (B, T, H), torch.float32),
+                 ("dbeta", (B, T, H), torch.int16), ("dS0", tuple(dS0.shape), torch.float32)]
 
     def layout(specs):
         offs, off = {}, 0
@@ -711,8 +714,11 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
 
+    fwd_bytes = out_offs["dq"][0]  # out and the final state
+
     def run(n_steps):
         in_ready = [ev() for _ in range(n_steps)]
+        fwd_done = [ev() for _ in range(n_steps)]
         comp_done = [ev() for _ in range(n_steps)]
         out_done = [ev() for _ in range(n_steps)]
         for i in range(n_steps):
@@ -729,14 +735,17 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
             gdn.gdn_chunk_fwd_save(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
                                    wl.scale, None, None, bf(do["out"]), do["fs"], B, T, H, K, V,
                                    ws_f, ws_f_n, stream)
+            fwd_done[i].record(stream)
             gdn.gdn_chunk_bwd_saved(bf(di["q"]), bf(di["k"]), bf(di["v"]), di["g"], bf(di["beta"]),
                                     wl.scale, None, bf(di["dO"]), None, bf(do["dq"]), bf(do["dk"]),
                                     bf(do["dv"]), do["dg"], bf(do["dbeta"]), do["dS0"], B, T, H, K, V,
                                     ws_f, ws_f_n, ws_b, ws_b_n, stream)
             comp_done[i].record(stream)
             with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done[i])
+                h_out_blk[:fwd_bytes].copy_(d_out_blk[j][:fwd_bytes], non_blocking=True)
                 s_out.wait_event(comp_done[i])
-                h_out_blk.copy_(d_out_blk[j], non_blocking=True)
+                h_out_blk[fwd_bytes:].copy_(d_out_blk[j][fwd_bytes:], non_blocking=True)
                 out_done[i].record(s_out)
         return out_done[-1]
 
@@ -757,7 +766,8 @@ def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, 
         raise SystemExit("e2e: non-finite results read back")
     return {"value": B * T * H / t, "unit": UNIT, "h2d_bytes_per_step": int(in_bytes),
             "d2h_bytes_per_step": int(out_bytes), "ms_per_step": t * 1e3, "steps": reps,
-            "pipelined": "copies of the neighbouring steps overlap each step's compute; one copy per direction"}
+            "pipelined": "copies of the neighbouring steps overlap each step's compute; inputs one copy, "
+                         "results two (forward outputs while the backward runs, then the gradients)"}
 
 
 def main():
