@@ -155,3 +155,31 @@ def test_prologue_end_to_end_through_the_operator():
     G.compare(ddt.cpu().numpy(), ddt_r, G.TOL_RMS_GRAD, None, "ddt_bias")
     G.compare(dA.cpu().numpy(), dA_r, G.TOL_RMS_GRAD, None, "dA_log")
     assert metrics.rel_l2(G.bf16_to_np(out), o_ref) < G.TOL_RMS_IID
+
+
+@pytest.mark.parametrize("rows", [1, 5, 9])
+def test_prologue_backward_head_sums_with_few_rows(rows):
+    """The per-head sums split a head's rows over a cluster of CTAs; with fewer
+    rows than parts some CTAs sum nothing and the totals must still be right."""
+    import torch
+    H, dk = 3, 64
+    q, k, a, b, A_log, dtb = _inputs(max(rows, 4), H, dk, seed=60 + rows)
+    q, k, a, b = q[:rows], k[:rows], a[:rows], b[:rows]
+    rng = np.random.default_rng(61)
+    dq = _f32(rng.standard_normal((rows, H, dk)))
+    dk_ = _f32(rng.standard_normal((rows, H, dk)))
+    dg = rng.standard_normal((rows, H)).astype(np.float32)
+    dbeta = _f32(rng.standard_normal((rows, H)))
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    out = {n: torch.empty((rows, H, dk), dtype=torch.bfloat16, device="cuda") for n in ("dq", "dk")}
+    da = torch.empty((rows, H), dtype=torch.float32, device="cuda")
+    db = torch.empty_like(da)
+    dA = torch.empty((H,), dtype=torch.float32, device="cuda")
+    ddt = torch.empty_like(dA)
+    gdn.gdn_prologue_bwd(_dev_bf16(q, torch), _dev_bf16(k, torch), t(a), t(b), t(A_log), t(dtb), 1, -5.0, 1.0,
+                         _dev_bf16(dq, torch), _dev_bf16(dk_, torch), t(dg), _dev_bf16(dbeta, torch),
+                         out["dq"], out["dk"], da, db, dA, ddt, rows, H, dk)
+    torch.cuda.synchronize()
+    _, _, dA_r, ddt_r = P.gates_bwd(a, b, dg, dbeta, A_log, dtb, mode="decay", lower=-5.0, beta_scale=1.0)
+    G.compare(ddt.cpu().numpy(), ddt_r, 1e-5, None, "ddt_bias")
+    G.compare(dA.cpu().numpy(), dA_r, 1e-5, None, "dA_log")

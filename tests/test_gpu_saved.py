@@ -122,3 +122,15 @@ def test_saved_route_full_size_matches_recomputing_route():
             G.compare(G.bf16_to_np(rb[n])[bb, t0:t1, h], ref[n][bb, t0:t1, h], G.TOL_RMS_GRAD, None,
                       f"{n} s{s} h{h}")
     assert np.isfinite(G.bf16_to_np(b[0])).all()
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 256), (64, 64)])
+def test_saved_route_packed_other_widths(dk, dv):
+    """Packed sequences at the other key and value widths: the training route
+    stays bitwise the recomputing route."""
+    lens = [70, 0, 129, 64, 1]
+    wl = W.random_workload(B=1, T=0, H=2, d_k=dk, d_v=dv, seed=dk + dv, seqlens=lens, initial_state=True,
+                           with_grad=True, d_final_state=True, beta_max=2.0)
+    a, b, (n_fwd, n_bwd) = _routes(wl)
+    _assert_bitwise(a, b)
+    assert n_fwd == 2 and n_bwd == 2
