@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ----------------------------------------------------------------------------
-# algorithmic work (per token-head; C = 64); fixed formulas, see the design notes
+# algorithmic work per token-head (C = 64): fixed formulas, frozen before tuning
 # ----------------------------------------------------------------------------
 
 def fwd_flops(K, V, C=CHUNK):
