@@ -418,6 +418,8 @@ def run_ours(args):
         for r in (roof_fwd, roof_bwd, roof_inf):
             if r["bound"] == "hbm":
                 r["frac_of_probe"] = r["achieved"] / probes["copy_gbs"]
+    # ---- sequence split on the long slow-decay workload ----
+    split = None if args.no_decode else measure_split(gdn, torch, dev, stream)
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
     # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
@@ -471,6 +473,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "accuracy": accuracy,
             "probes": probes,
+            "split": split,
             "decode": decode,
             "prologue": prologue,
         }
@@ -571,6 +574,59 @@ def measure_probes(gdn, torch, dev, stream, copy_bytes=2 << 30, n=8192, steps=10
             "bf16_gemm_tflops": 2.0 * n ** 3 / t_gemm / 1e12, "gemm": f"{n}x{n} by {n}x{n}, bf16, fp32 accumulate",
             "kernels": "gdn_probe_copy, gdn_probe_gemm_bf16 (tcgen05), median of "
                        f"{steps} after {warmup} warm-up"}
+
+
+def measure_split(gdn, torch, dev, stream, T=65536, H=16, K=128, V=128, segs=(4, 8), steps=5, warmup=2):
+    """The sequence split on the long slow-decay workload (one sequence,
+    T = 65536, 16 heads: 32 chains unsplit): gdn_chunk_fwd against
+    gdn_chunk_fwd_split at a few segment counts, L2 flushed before each call.
+    Inputs follow that workload's recipe (q, v ~ N(0,1), k L2-normalised,
+    g = -1e-3, beta = sigmoid(N(0,1) - 2)), drawn on the device."""
+    gen = torch.Generator(device=dev).manual_seed(4)
+    q = torch.randn((1, T, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn((1, T, H, K), device=dev, generator=gen), dim=-1).to(torch.bfloat16)
+    v = torch.randn((1, T, H, V), device=dev, generator=gen).to(torch.bfloat16)
+    g = torch.full((1, T, H), -1e-3, device=dev)
+    beta = torch.sigmoid(torch.randn((1, T, H), device=dev, generator=gen) - 2.0).to(torch.bfloat16)
+    out = torch.empty_like(v)
+    fs = torch.empty((1, H, K, V), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    scale = K ** -0.5
+
+    def timed(call):
+        for _ in range(warmup):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
+
+    n = gdn.gdn_chunk_fwd_workspace_size(1, T, H, K, V, 0)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    t_u = timed(lambda: gdn.gdn_chunk_fwd(q, k, v, g, beta, scale, None, None, out, fs, 1, T, H, K, V,
+                                          ws, n, stream))
+    ref = out.float().clone()
+    del ws
+    res = {"config": f"1 sequence x T={T} x H={H}, d_k={K}, d_v={V}, g = -1e-3 (slow decay)",
+           "unsplit_ms": t_u * 1e3, "unsplit_tokens_heads_per_s": T * H / t_u}
+    for nseg in segs:
+        n = gdn.gdn_chunk_fwd_split_workspace_size(1, T, H, K, V, nseg)
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        t_s = timed(lambda: gdn.gdn_chunk_fwd_split(q, k, v, g, beta, scale, None, out, fs, 1, T, H, K, V,
+                                                    nseg, ws, n, stream))
+        diff = float((out.float() - ref).norm() / ref.norm())
+        res[f"nseg_{nseg}"] = {"ms": t_s * 1e3, "tokens_heads_per_s": T * H / t_s, "speedup": t_u / t_s,
+                               "rel_l2_vs_unsplit": diff}
+        del ws
+    st = gdn.gdn_get_last_device_error()
+    if st != 0:
+        raise SystemExit(f"device error in the split measurement: {gdn.gdn_status_string(st)}")
+    return res
 
 
 def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, steps=50, warmup=5):

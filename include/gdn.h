@@ -305,6 +305,32 @@ GDN_API gdn_status gdn_chunk_bwd_noalloc(const gdn_bf16* q, const gdn_bf16* k, c
                          int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
 /*
+ * Sequence split: gdn_chunk_fwd (dense inputs, no cu_seqlens) with every
+ * sequence run as nseg segments of whole chunks, for long sequences with few
+ * heads, where one chain per (sequence, head, value slice) leaves most of the
+ * GPU idle.  cuLA issue #126 ("Hypothesis") describes the scheme: each
+ * segment maps its start state affinely, S_end = M S_start + b, and the
+ * carries compose in order.  Here b is a segment's end state from a zero
+ * start and M its end state from the identity with zero values (both from
+ * the chunk chain), the composition is fp32, and each segment then runs
+ * from its true start.  Costs about three times the chain work of the
+ * unsplit forward, in nseg times as many chains.
+ *   nseg >= 1; more segments than chunks are clamped to one chunk each.
+ *   workspace: device, 256-byte aligned, gdn_chunk_fwd_split_workspace_size()
+ *   bytes (a few arrays of the inputs' and the states' sizes).
+ * Outputs as gdn_chunk_fwd, to within rounding (not bitwise: the carries
+ * change the order of the arithmetic).  Errors as gdn_chunk_fwd, plus
+ * GDN_ERR_INVALID_ARG for nseg < 1 or a missing or short workspace and
+ * GDN_ERR_UNSUPPORTED for B T >= 2^31.
+ */
+GDN_API size_t gdn_chunk_fwd_split_workspace_size(int B, int T, int H, int d_k, int d_v, int nseg);
+GDN_API gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                               const float* g, const gdn_bf16* beta, float scale,
+                               const float* initial_state, gdn_bf16* out, float* final_state,
+                               int B, int T, int H, int d_k, int d_v, int nseg,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Peak probes: the denominators of a roofline, measured on the caller's GPU
  * in the same run as the operator ("Research Sprint Day 2 - Rooflines",
  * section "Rooflines": FLOP/s from 8192 x 8192 by 8192 x 8192 dense matmuls,

@@ -188,6 +188,35 @@ gdn_status launch_bwd_passes(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     return GDN_OK;
 }
 
+// Workspace of the sequence split: segment bounds, T tiles of the packed
+// segments, zero values and a scratch output for the transition run, the
+// identity start states, the segments' M and b, and their true start states.
+struct SplitLayout {
+    size_t cu, tiles, zeros, mout, ident, mfin, bfin, starts, total;
+};
+
+SplitLayout split_layout(int B, int T, int H, int d_k, int d_v, int nseg) {
+    SplitLayout L{};
+    const long long nseq = static_cast<long long>(B) * nseg;
+    const long long rows = static_cast<long long>(B) * T;
+    L.cu = 0;
+    L.tiles = round_up(sizeof(int32_t) * (nseq + 1));
+    L.zeros = L.tiles + tiles_bytes(static_cast<int>(nseq), static_cast<int>(rows), H, 1);
+    L.mout = L.zeros + round_up(2ull * rows * H * d_k);
+    L.ident = L.mout + round_up(2ull * rows * H * d_k);
+    L.mfin = L.ident + round_up(4ull * nseq * H * d_k * d_k);
+    L.bfin = L.mfin + round_up(4ull * nseq * H * d_k * d_k);
+    L.starts = L.bfin + round_up(4ull * nseq * H * d_k * d_v);
+    L.total = L.starts + round_up(4ull * nseq * H * d_k * d_v);
+    return L;
+}
+
+// Segments actually used: at least one chunk each.
+int split_segments(int T, int nseg) {
+    const int nch = (T + gdn::kChunk - 1) / gdn::kChunk;
+    return nseg < nch ? nseg : (nch > 0 ? nch : 1);
+}
+
 gdn_status recurrent(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
                      const gdn_bf16* beta, float scale, const float* initial_state,
                      const int32_t* cu_seqlens, gdn_bf16* out, float* final_state, int B, int T,
@@ -423,6 +452,66 @@ gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
     return launch_bwd_passes(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
                              d_initial_state, B, T, H, d_k, d_v, states, static_cast<float*>(workspace), tiles,
                              err, stream);
+}
+
+size_t gdn_chunk_fwd_split_workspace_size(int B, int T, int H, int d_k, int d_v, int nseg) {
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK || nseg < 1) return 0;
+    if (static_cast<long long>(B) * T >= (1LL << 31)) return 0;
+    return split_layout(B, T, H, d_k, d_v, split_segments(T, nseg)).total;
+}
+
+gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                               const gdn_bf16* beta, float scale, const float* initial_state, gdn_bf16* out,
+                               float* final_state, int B, int T, int H, int d_k, int d_v, int nseg,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    gdn_status st = check_fwd(q, k, v, g, beta, initial_state, nullptr, out, final_state, B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    if (nseg < 1) return GDN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * T >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if (T == 0)  // nothing to split: the state passes through
+        return gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, nullptr, out, final_state, B, T, H, d_k, d_v,
+                             nullptr, 0, stream);
+    const int ns = split_segments(T, nseg);
+    const SplitLayout L = split_layout(B, T, H, d_k, d_v, ns);
+    st = check_buffer(workspace, workspace_bytes, L.total);
+    if (st != GDN_OK) return st;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    char* w = static_cast<char*>(workspace);
+    gdn::SplitArgs sa{};
+    sa.cu = reinterpret_cast<int32_t*>(w + L.cu);
+    sa.ident = reinterpret_cast<float*>(w + L.ident);
+    sa.initial_state = initial_state;
+    sa.m_fin = reinterpret_cast<const float*>(w + L.mfin);
+    sa.b_fin = reinterpret_cast<const float*>(w + L.bfin);
+    sa.starts = reinterpret_cast<float*>(w + L.starts);
+    sa.final_state = final_state;
+    sa.B = B; sa.T = T; sa.H = H; sa.d_k = d_k; sa.d_v = d_v; sa.nseg = ns;
+    const int nseq = B * ns, rows = B * T;
+    uint8_t* tiles = reinterpret_cast<uint8_t*>(w + L.tiles);
+    if (!launched(gdn::launch_split_setup(sa, stream))) return GDN_ERR_CUDA;
+    if (!launch_tiles(k, g, beta, sa.cu, tiles, nseq, rows, H, d_k, err, stream)) return GDN_ERR_CUDA;
+    gdn::FwdArgs f{};
+    f.q = q; f.k = k; f.g = g; f.beta = beta; f.scale = scale; f.cu_seqlens = sa.cu; f.chunk_T = tiles;
+    f.N = nseq; f.T = rows; f.H = H; f.d_k = d_k; f.err = err; f.chunk_states = nullptr;
+    if (ns == 1) {  // one segment per sequence: the plain chain over the packed sequences
+        f.v = v; f.d_v = d_v; f.initial_state = initial_state; f.out = out; f.final_state = final_state;
+        if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    // carries: b from a zero start (the output is overwritten below), M from
+    // the identity with zero values
+    f.v = v; f.d_v = d_v; f.initial_state = nullptr; f.out = out; f.final_state = reinterpret_cast<float*>(w + L.bfin);
+    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    if (cudaMemsetAsync(w + L.zeros, 0, 2ull * rows * H * d_k, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    f.v = reinterpret_cast<const gdn_bf16*>(w + L.zeros); f.d_v = d_k; f.initial_state = sa.ident;
+    f.out = reinterpret_cast<gdn_bf16*>(w + L.mout); f.final_state = reinterpret_cast<float*>(w + L.mfin);
+    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    // true start states (and the final state), then every segment from its start
+    if (!launched(gdn::launch_split_compose(sa, stream))) return GDN_ERR_CUDA;
+    f.v = v; f.d_v = d_v; f.initial_state = sa.starts; f.out = out; f.final_state = nullptr;
+    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
 gdn_status gdn_probe_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream) {

@@ -157,6 +157,21 @@ struct PrologueArgs {
 cudaError_t launch_prologue_fwd(const PrologueArgs& a, cudaStream_t stream);
 cudaError_t launch_prologue_bwd(const PrologueArgs& a, cudaStream_t stream);
 
+// Sequence split (segments with composed affine carries): setup of the
+// segment bounds and identity start states, and the fp32 composition.
+struct SplitArgs {
+    int32_t* cu;                  // [B nseg + 1] segment bounds as packed sequences
+    float* ident;                 // [B nseg][H][d_k][d_k] identity start states
+    const float* initial_state;   // [B][H][d_k][d_v] or null (zeros)
+    const float* m_fin;           // [B nseg][H][d_k][d_k] segment transitions M
+    const float* b_fin;           // [B nseg][H][d_k][d_v] segment offsets b
+    float* starts;                // [B nseg][H][d_k][d_v] true segment start states
+    float* final_state;           // [B][H][d_k][d_v] or null
+    int B, T, H, d_k, d_v, nseg;
+};
+cudaError_t launch_split_setup(const SplitArgs& a, cudaStream_t stream);
+cudaError_t launch_split_compose(const SplitArgs& a, cudaStream_t stream);
+
 // Peak probes (measurement only): a 16-byte-vector copy of `bytes` (a
 // multiple of 16), and the bf16 GEMM C[M][N] = A[M][K] B[N][K]^T with
 // M % 128 == 0, N % 256 == 0, K % 64 == 0.

@@ -86,6 +86,10 @@ def load():
         lib.gdn_chunk_fwd_save.restype = i
         lib.gdn_chunk_bwd_saved.argtypes = [vp] * 5 + [f] + [vp] * 9 + [i] * 5 + [vp, sz, vp, sz, vp]
         lib.gdn_chunk_bwd_saved.restype = i
+        lib.gdn_chunk_fwd_split_workspace_size.argtypes = [i] * 6
+        lib.gdn_chunk_fwd_split_workspace_size.restype = sz
+        lib.gdn_chunk_fwd_split.argtypes = [vp] * 5 + [f] + [vp] * 3 + [i] * 6 + [vp, sz, vp]
+        lib.gdn_chunk_fwd_split.restype = i
         lib.gdn_probe_copy.argtypes = [vp, vp, sz, vp]
         lib.gdn_probe_copy.restype = i
         lib.gdn_probe_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, vp]
@@ -183,6 +187,18 @@ def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_stat
                                     int(saved_bytes), _ptr(workspace), int(workspace_bytes),
                                     _stream(stream))
     _check(st, "gdn_chunk_bwd_saved")
+
+
+def gdn_chunk_fwd_split_workspace_size(B, T, H, d_k, d_v, nseg) -> int:
+    return int(load().gdn_chunk_fwd_split_workspace_size(B, T, H, d_k, d_v, nseg))
+
+
+def gdn_chunk_fwd_split(q, k, v, g, beta, scale, initial_state, out, final_state, B, T, H, d_k, d_v, nseg,
+                        workspace, workspace_bytes, stream=None):
+    st = load().gdn_chunk_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                    _ptr(initial_state), _ptr(out), _ptr(final_state), B, T, H, d_k, d_v,
+                                    int(nseg), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "gdn_chunk_fwd_split")
 
 
 def gdn_probe_copy(src, dst, nbytes, stream=None):
@@ -296,6 +312,24 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     ws = _workspace(nbytes, v.device)
     gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs,
                   B, T, H, d_k, d_v, ws, nbytes, stream)
+    return out, fs
+
+
+def chunk_gated_delta_rule_fwd_split(q, k, v, g, beta, nseg, scale=None, initial_state=None,
+                                     output_final_state=True, stream=None):
+    """Allocate outputs and run gdn_chunk_fwd_split (dense inputs, every
+    sequence as nseg segments).  Returns (out, final_state)."""
+    import torch
+    B, T, H, d_k, d_v = _dims(q, v, None)
+    if scale is None:
+        scale = d_k ** -0.5
+    out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    fs = (torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=v.device)
+          if output_final_state else None)
+    nbytes = gdn_chunk_fwd_split_workspace_size(B, T, H, d_k, d_v, nseg)
+    ws = _workspace(nbytes, v.device)
+    gdn_chunk_fwd_split(q, k, v, g, beta, scale, initial_state, out, fs, B, T, H, d_k, d_v, nseg,
+                        ws, nbytes, stream)
     return out, fs
 
 

@@ -158,3 +158,23 @@ def test_probe_host_validation(lib):
     assert g(FAKE, FAKE, FAKE, 128, 256, 65536 + 64, None) == 2
     assert g(None, FAKE, FAKE, 128, 256, 64, None) == 1
     assert g(FAKE, FAKE + 2, FAKE, 128, 256, 64, None) == 3
+
+
+def test_split_host_validation(lib):
+    l = gdn.load()
+    need = gdn.gdn_chunk_fwd_split_workspace_size(2, 256, 2, 64, 64, 3)
+    assert need > 0
+    assert gdn.gdn_chunk_fwd_split_workspace_size(2, 256, 2, 64, 64, 0) == 0
+    # more segments than chunks are clamped: the same layout as one segment per chunk
+    assert (gdn.gdn_chunk_fwd_split_workspace_size(2, 256, 2, 64, 64, 99)
+            == gdn.gdn_chunk_fwd_split_workspace_size(2, 256, 2, 64, 64, 4))
+
+    def call(nseg=3, ws=FAKE, nbytes=need, out=FAKE, d_k=64):
+        return l.gdn_chunk_fwd_split(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, out, None, 2, 256, 2, d_k, 64,
+                                     nseg, ws, nbytes, None)
+    assert call(nseg=0) == 1
+    assert call(ws=None, nbytes=0) == 1
+    assert call(nbytes=need - 1) == 1
+    assert call(ws=FAKE + 32) == 3
+    assert call(out=None) == 1
+    assert call(d_k=96) == 2
