@@ -7,6 +7,7 @@ script, the thin ctypes binding and the seeded synthetic workloads.
 
 from .gdn import (  # noqa: F401
     GdnError,
+    chunk_gated_delta_rule,
     chunk_gated_delta_rule_bwd,
     chunk_gated_delta_rule_fwd,
     gdn_chunk_bwd,

@@ -363,3 +363,59 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=None, initial_stat
                   res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"],
                   res["d_initial_state"], B, T, H, d_k, d_v, ws, nbytes, stream)
     return res
+
+
+# ----------------------------------------------------------------------------
+# autograd: the training route behind torch.autograd
+# ----------------------------------------------------------------------------
+
+def _autograd_function():
+    import torch
+
+    class _ChunkGatedDeltaRule(torch.autograd.Function):
+        """Forward: gdn_chunk_fwd_save (the output, the final state, and every
+        chunk's start state and T tiles kept for the backward).  Backward:
+        gdn_chunk_bwd_saved from them."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, g, beta, initial_state, scale, cu_seqlens):
+            out, fs, saved = chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=scale,
+                                                        initial_state=initial_state,
+                                                        cu_seqlens=cu_seqlens, save_for_backward=True)
+            ctx.save_for_backward(q, k, v, g, beta, saved)
+            ctx.scale = scale
+            ctx.cu_seqlens = cu_seqlens
+            ctx.has_initial_state = initial_state is not None
+            return out, fs
+
+        @staticmethod
+        def backward(ctx, d_out, d_fs):
+            q, k, v, g, beta, saved = ctx.saved_tensors
+            if d_out is None:
+                d_out = torch.zeros_like(v)
+            d_out = d_out.to(torch.bfloat16).contiguous()
+            d_fs = None if d_fs is None else d_fs.to(torch.float32).contiguous()
+            r = chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=ctx.scale,
+                                           cu_seqlens=ctx.cu_seqlens, d_final_state=d_fs, saved=saved)
+            d_s0 = r["d_initial_state"] if ctx.has_initial_state else None
+            return r["dq"], r["dk"], r["dv"], r["dg"], r["dbeta"], d_s0, None, None
+
+    return _ChunkGatedDeltaRule
+
+
+_AUTOGRAD = None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None):
+    """The chunked gated delta rule with autograd: (B, T, H, d_k) bf16 q, k;
+    (B, T, H, d_v) bf16 v; (B, T, H) fp32 g and bf16 beta; optional fp32
+    initial state (N, H, d_k, d_v) and int32 cu_seqlens (packed inputs, B = 1).
+    Returns (out (B, T, H, d_v) bf16, final_state (N, H, d_k, d_v) fp32); the
+    backward runs from the chunk states the forward kept (gradients w.r.t.
+    q, k, v, g, beta and initial_state, in their dtypes)."""
+    global _AUTOGRAD
+    if _AUTOGRAD is None:
+        _AUTOGRAD = _autograd_function()
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    return _AUTOGRAD.apply(q, k, v, g, beta, initial_state, float(scale), cu_seqlens)
