@@ -420,6 +420,8 @@ def run_ours(args):
                 r["frac_of_probe"] = r["achieved"] / probes["copy_gbs"]
     # ---- sequence split on the long slow-decay workload ----
     split = None if args.no_decode else measure_split(gdn, torch, dev, stream)
+    # ---- per-channel gate (KDA): chunked CUDA-core forward beside the token-serial one ----
+    kda = None if args.no_decode else measure_kda(gdn, torch, dev, stream, clk)
     # ---- decode: the token-serial path, one token per call ----
     decode = None if args.no_decode else measure_decode(gdn, torch, dev, stream, hbm)
     # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
@@ -474,6 +476,7 @@ def run_ours(args):
             "accuracy": accuracy,
             "probes": probes,
             "split": split,
+            "kda": kda,
             "decode": decode,
             "prologue": prologue,
         }
@@ -627,6 +630,64 @@ def measure_split(gdn, torch, dev, stream, T=65536, H=16, K=128, V=128, segs=(4,
     if st != 0:
         raise SystemExit(f"device error in the split measurement: {gdn.gdn_status_string(st)}")
     return res
+
+
+FP32_LANES_PER_SM = 128   # fp32 FMA lanes per SM (4 sub-partitions x 32)
+SMS = 152
+
+
+def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, steps=5, warmup=2):
+    """The per-channel-gate (KDA) forward at the headline shape: the chunked
+    fp32 CUDA-core kernel (gdn_kda_chunk_fwd) beside the token-serial one
+    (gdn_kda_recurrent_fwd), L2 flushed before each call.  Inputs: q, v ~
+    N(0,1), k L2-normalised, g = -5 sigmoid(N(0,1) + 2) per key channel (the
+    bounded gate with lower bound -5), beta = sigmoid(N(0,1)), zero initial
+    state; drawn on the device.  The chunked kernel runs on the CUDA cores, so
+    its roofline is fp32 FMA: the chunk algebra's FLOPs (the forward formula,
+    the decay exponentials not counted) against 152 SMs x 128 lanes x 2 FLOP
+    at the SM clock sampled in this run."""
+    gen = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn((B, T, H, K), device=dev, generator=gen).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn((B, T, H, K), device=dev, generator=gen), dim=-1).to(torch.bfloat16)
+    v = torch.randn((B, T, H, V), device=dev, generator=gen).to(torch.bfloat16)
+    g = -5.0 * torch.sigmoid(torch.randn((B, T, H, K), device=dev, generator=gen) + 2.0)
+    beta = torch.sigmoid(torch.randn((B, T, H), device=dev, generator=gen)).to(torch.bfloat16)
+    out = torch.empty_like(v)
+    fs = torch.empty((B, H, K, V), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    scale = K ** -0.5
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
+
+    t_c = timed(gdn.gdn_kda_chunk_fwd, steps)
+    o_c = out.float().clone()
+    t_r = timed(gdn.gdn_kda_recurrent_fwd, 2)
+    diff = float((out.float() - o_c).norm() / out.float().norm())
+    st = gdn.gdn_get_last_device_error()
+    if st != 0:
+        raise SystemExit(f"device error in the KDA measurement: {gdn.gdn_status_string(st)}")
+    units = B * T * H
+    mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
+    peak = SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    ach = fwd_flops(K, V) * units / t_c / 1e12
+    return {"config": f"B={B} T={T} H={H} d_k={K} d_v={V}, per-channel g in (-5, 0)",
+            "chunk_ms": t_c * 1e3, "chunk_tokens_heads_per_s": units / t_c,
+            "token_serial_ms": t_r * 1e3, "token_serial_tokens_heads_per_s": units / t_r,
+            "speedup_vs_token_serial": t_r / t_c, "out_rel_l2_chunk_vs_token_serial": diff,
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                         "peak_from": f"{SMS} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 FLOP x {mhz:.0f} MHz",
+                         "traffic": None}}
 
 
 def measure_decode(gdn, torch, dev, stream, hbm, B=256, H=16, K=128, V=128, steps=50, warmup=5):

@@ -139,14 +139,33 @@ GDN_API gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const
  * #126 runs: g is (B, T, H, d_k) fp32, one log decay per key channel, and the
  * state update decays each key row of S by its own factor,
  * S <- diag(exp(g_t)) S; everything else (arguments, layouts, validation,
- * errors) is as gdn_recurrent_fwd.  Only this token-serial path exists for
- * the per-channel gate.
+ * errors) is as gdn_recurrent_fwd.  gdn_kda_chunk_fwd below is the
+ * chunked form of the same recurrence.
  */
 GDN_API gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
                                  const float* g, const gdn_bf16* beta, float scale,
                                  const float* initial_state, const int32_t* cu_seqlens,
                                  gdn_bf16* out, float* final_state,
                                  int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
+
+/*
+ * Chunked forward of the same per-channel-gate (KDA) recurrence: the sequence
+ * is cut into chunks of 64 tokens, each chunk's gram A_ij = beta_i sum_c
+ * k_ic k_jc exp(G_ic - G_jc) (j < i; G the per-channel running sum of g
+ * inside the chunk) and causal score are formed with the decay inside the
+ * sum over key channels, T = (I + A)^-1 by blocked forward substitution, and
+ * the state passes from chunk to chunk, S <- diag(exp(G_n)) S +
+ * (exp(G_n - G) o K)^T Delta.  All arithmetic fp32 on the CUDA cores; one
+ * thread block per (64 value columns, head, sequence).  Arguments, layouts,
+ * validation and errors as gdn_kda_recurrent_fwd (g is (B, T, H, d_k) fp32,
+ * documented domain g <= 0; no workspace).  Same result as the token-serial
+ * kernel up to fp32 rounding order.
+ */
+GDN_API gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                     const float* g, const gdn_bf16* beta, float scale,
+                                     const float* initial_state, const int32_t* cu_seqlens,
+                                     gdn_bf16* out, float* final_state,
+                                     int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
 /*
  * Prologue: q/k L2 normalisation and the two gates from their raw inputs

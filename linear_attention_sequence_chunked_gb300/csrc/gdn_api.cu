@@ -310,6 +310,22 @@ gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
                      d_k, d_v, 1, stream);
 }
 
+gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                             const gdn_bf16* beta, float scale, const float* initial_state,
+                             const int32_t* cu_seqlens, gdn_bf16* out, float* final_state, int B, int T,
+                             int H, int d_k, int d_v, cudaStream_t stream) {
+    gdn_status st = check_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    gdn::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
+    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
+    if (!launched(gdn::launch_kda_chunk(a, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 gdn_status gdn_prologue_fwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const float* a, const float* b,
                             const float* A_log, const float* dt_bias, int gate_mode, float lower,
                             float beta_scale, gdn_bf16* q, gdn_bf16* k, float* g, gdn_bf16* beta,

@@ -72,6 +72,8 @@ def load():
         lib.gdn_recurrent_fwd.restype = i
         lib.gdn_kda_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
         lib.gdn_kda_recurrent_fwd.restype = i
+        lib.gdn_kda_chunk_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
+        lib.gdn_kda_chunk_fwd.restype = i
         lib.gdn_prologue_fwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 4 + [i] * 3 + [vp]
         lib.gdn_prologue_fwd.restype = i
         lib.gdn_prologue_bwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 10 + [i] * 3 + [vp]
@@ -224,6 +226,28 @@ def gdn_kda_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, ou
                                       _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
                                       _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
     _check(st, "gdn_kda_recurrent_fwd")
+
+
+def gdn_kda_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                      B, T, H, d_k, d_v, stream=None):
+    st = load().gdn_kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                  _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                  _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
+    _check(st, "gdn_kda_chunk_fwd")
+
+
+def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None, stream=None):
+    """Allocate out and the final state and run gdn_kda_chunk_fwd: q, k
+    (B, T, H, d_k) bf16; v (B, T, H, d_v) bf16; g (B, T, H, d_k) fp32 (one log
+    decay per key channel); beta (B, T, H) bf16.  Returns (out, final_state)."""
+    import torch
+    B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = d_k ** -0.5
+    out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
+    fs = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=v.device)
+    gdn_kda_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs, B, T, H, d_k, d_v, stream)
+    return out, fs
 
 
 def gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias, gate_mode, lower, beta_scale,

@@ -73,6 +73,22 @@ def test_recurrent_host_validation(lib, over, code):
     assert st == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(d_k=96), 2), (dict(d_v=32), 2), (dict(B=0), 1), (dict(T=-1), 1), (dict(q=None), 1),
+    (dict(g=None), 1), (dict(out=None), 1), (dict(k=FAKE + 2), 3), (dict(g=FAKE + 4), 3),
+    (dict(final_state=FAKE + 4), 3), (dict(cu_seqlens=FAKE + 2), 3), (dict(H=70000), 2),
+])
+def test_kda_chunk_host_validation(lib, over, code):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=1.0, initial_state=None,
+                cu_seqlens=None, out=FAKE, final_state=None, B=1, T=64, H=1, d_k=64, d_v=64)
+    args.update(over)
+    st = gdn.load().gdn_kda_chunk_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"],
+                                       args["scale"], args["initial_state"], args["cu_seqlens"],
+                                       args["out"], args["final_state"], args["B"], args["T"],
+                                       args["H"], args["d_k"], args["d_v"], None)
+    assert st == code
+
+
 def test_backward_host_validation(lib):
     l = gdn.load()
     need = gdn.gdn_chunk_bwd_workspace_size(1, 128, 1, 64, 64, 0)
