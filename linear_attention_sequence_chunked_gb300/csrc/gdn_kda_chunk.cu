@@ -23,7 +23,11 @@
 //
 // One thread block per (value slice of 64 columns, head, sequence) walks the
 // sequence chunk by chunk with its d_k x 64 slice of the state in shared
-// memory (the value columns of the recurrence are independent).
+// memory (the value columns of the recurrence are independent).  Shared rows
+// are padded to a multiple of four floats (and to 4 banks mod 32), so every
+// product reads its operands as 16-byte vectors: a thread owns four adjacent
+// output columns and a few rows, and each step of the reduction takes four
+// terms at once.
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -32,12 +36,12 @@ namespace gdn {
 namespace {
 
 constexpr int kVs = 64;        // value columns per block
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // 16 x 16: ti = thread / 16 (rows), tj = thread % 16 (4-column group)
 
 template <int K>
 struct KdaSmem {
-    static constexpr int LDK = K + 1;
-    static constexpr int LDC = kChunk + 1;
+    static constexpr int LDK = K + 4;       // rows of d_k floats
+    static constexpr int LDC = kChunk + 4;  // rows of 64 floats
     static constexpr int kFloats = 64 * LDK * 3    // Ks, Qs, Gk
                                    + 64 * LDC * 4  // Vt, Tm, Pm, Au
                                    + K * LDC       // Ss
@@ -46,9 +50,18 @@ struct KdaSmem {
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
-// Rows [row0, row0 + nv) of a (.., T, H, D) tensor for head h, columns
-// [col0, col0 + W), into a 64 x LD fp32 tile; rows >= nv are zero.  Eight
-// bf16 or four fp32 values per 16-byte load.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+__device__ __forceinline__ void fma4(float (&acc)[4], float a, float4 b) {
+    acc[0] = fmaf(a, b.x, acc[0]);
+    acc[1] = fmaf(a, b.y, acc[1]);
+    acc[2] = fmaf(a, b.z, acc[2]);
+    acc[3] = fmaf(a, b.w, acc[3]);
+}
+
+// Rows [row0, row0 + nv) of a (.., T, H, D) bf16 tensor for head h, columns
+// [col0, col0 + W), widened into a 64 x LD fp32 tile; rows >= nv are zero.
 template <int W, int LD>
 __device__ __forceinline__ void load_rows_bf16(const uint16_t* __restrict__ src, long long row0, int H,
                                                int h, int D, int col0, int nv, float* dst) {
@@ -60,15 +73,14 @@ __device__ __forceinline__ void load_rows_bf16(const uint16_t* __restrict__ src,
         if (r < nv)
             raw = *reinterpret_cast<const uint4*>(src + ((row0 + r) * H + h) * static_cast<long long>(D) +
                                                   col0 + c);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            dst[r * LD + c + 2 * m] = __uint_as_float(w4[m] << 16);
-            dst[r * LD + c + 2 * m + 1] = __uint_as_float(w4[m] & 0xffff0000u);
-        }
+        st4(dst + r * LD + c, make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)));
+        st4(dst + r * LD + c + 4, make_float4(__uint_as_float(raw.z << 16), __uint_as_float(raw.z & 0xffff0000u),
+                                              __uint_as_float(raw.w << 16), __uint_as_float(raw.w & 0xffff0000u)));
     }
 }
 
+// The same for a (.., T, H, W) fp32 tensor (all W columns).
 template <int W, int LD>
 __device__ __forceinline__ void load_rows_f32(const float* __restrict__ src, long long row0, int H, int h,
                                               int nv, float* dst) {
@@ -77,20 +89,59 @@ __device__ __forceinline__ void load_rows_f32(const float* __restrict__ src, lon
         const int r = e / kPerRow;
         const int c = (e % kPerRow) * 4;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < nv) x = *reinterpret_cast<const float4*>(src + ((row0 + r) * H + h) * static_cast<long long>(W) + c);
-        dst[r * LD + c] = x.x;
-        dst[r * LD + c + 1] = x.y;
-        dst[r * LD + c + 2] = x.z;
-        dst[r * LD + c + 3] = x.w;
+        if (r < nv) x = ld4(src + ((row0 + r) * H + h) * static_cast<long long>(W) + c);
+        st4(dst + r * LD + c, x);
+    }
+}
+
+// acc[r][.] += sum_{kk < KD} A[i_r][kk] B[kk][4 tj .. 4 tj + 3] for the rows
+// i_r = ti + 16 r: A and B row-major, four reduction terms per step (one
+// 16-byte read of each of the TM rows of A and of four rows of B).
+template <int TM, int KD>
+__device__ __forceinline__ void mm_rows(float (&acc)[TM][4], const float* A, int lda, const float* B, int ldb,
+                                        int ti, int tj) {
+#pragma unroll 2
+    for (int k0 = 0; k0 < KD; k0 += 4) {
+        float4 b[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b[q] = ld4(B + (k0 + q) * ldb + 4 * tj);
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            const float4 a = ld4(A + (ti + 16 * r) * lda + k0);
+            fma4(acc[r], a.x, b[0]);
+            fma4(acc[r], a.y, b[1]);
+            fma4(acc[r], a.z, b[2]);
+            fma4(acc[r], a.w, b[3]);
+        }
+    }
+}
+
+// acc[4 m + e][.] += sum_{j < 64} At[j][64 m + 4 ti + e] B[j][4 tj .. 4 tj + 3]
+// (m < K / 64, e < 4): the product with a transposed left operand, whose rows
+// are read as 16-byte vectors along the output rows.
+template <int K>
+__device__ __forceinline__ void mm_trans(float (&acc)[K / 16][4], const float* At, int lda, const float* B,
+                                         int ldb, int ti, int tj) {
+#pragma unroll 4
+    for (int j = 0; j < 64; ++j) {
+        const float4 b = ld4(B + j * ldb + 4 * tj);
+#pragma unroll
+        for (int m = 0; m < K / 64; ++m) {
+            const float4 a = ld4(At + j * lda + 64 * m + 4 * ti);
+            fma4(acc[4 * m + 0], a.x, b);
+            fma4(acc[4 * m + 1], a.y, b);
+            fma4(acc[4 * m + 2], a.z, b);
+            fma4(acc[4 * m + 3], a.w, b);
+        }
     }
 }
 
 // A (strict lower, times beta_i) and, when `score`, P (lower with the
-// diagonal) in one pass over the key channels, sharing each pair's decay
-// factor.  Thread t owns rows i = t/16 + 16 r and columns j = t%16 + 16 s
-// (r, s < 4); pairs with s > r lie above the diagonal for every thread and are
-// skipped at compile time; pairs with s == r that lie above the diagonal take
-// a zero exponent (their value is masked on store).
+// diagonal) in one pass over the key channels, four channels per step,
+// sharing each pair's decay factor.  Thread t owns rows i = ti + 16 r and
+// columns j = tj + 16 s (r, s < 4): pairs with s > r lie above the diagonal
+// for every thread and are skipped at compile time; pairs with s == r that lie
+// above the diagonal take a zero exponent (their value is masked on store).
 template <int K, int LDK, int LDC>
 __device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs, const float* Gk,
                                                const float* bs, float* Au, float* Pm, bool score) {
@@ -100,27 +151,33 @@ __device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs,
     for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int s = 0; s < 4; ++s) a[r][s] = p[r][s] = 0.f;
-#pragma unroll 2
-    for (int c = 0; c < K; ++c) {
-        float gi[4], ki[4], qi[4], gj[4], kj[4];
+    for (int c = 0; c < K; c += 4) {
+        float gi[4][4], ki[4][4], qi[4][4], gj[4][4], kj[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            gi[r] = Gk[(ti + 16 * r) * LDK + c];
-            ki[r] = Ks[(ti + 16 * r) * LDK + c];
-            qi[r] = Qs[(ti + 16 * r) * LDK + c];
-            gj[r] = Gk[(tj + 16 * r) * LDK + c];
-            kj[r] = Ks[(tj + 16 * r) * LDK + c];
+            const float4 g4 = ld4(Gk + (ti + 16 * r) * LDK + c);
+            const float4 k4 = ld4(Ks + (ti + 16 * r) * LDK + c);
+            const float4 q4 = ld4(Qs + (ti + 16 * r) * LDK + c);
+            const float4 h4 = ld4(Gk + (tj + 16 * r) * LDK + c);
+            const float4 l4 = ld4(Ks + (tj + 16 * r) * LDK + c);
+            gi[r][0] = g4.x; gi[r][1] = g4.y; gi[r][2] = g4.z; gi[r][3] = g4.w;
+            ki[r][0] = k4.x; ki[r][1] = k4.y; ki[r][2] = k4.z; ki[r][3] = k4.w;
+            qi[r][0] = q4.x; qi[r][1] = q4.y; qi[r][2] = q4.z; qi[r][3] = q4.w;
+            gj[r][0] = h4.x; gj[r][1] = h4.y; gj[r][2] = h4.z; gj[r][3] = h4.w;
+            kj[r][0] = l4.x; kj[r][1] = l4.y; kj[r][2] = l4.z; kj[r][3] = l4.w;
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-            for (int s = 0; s <= r; ++s) {
-                // s < r: j < i for every thread; s == r: j <= i only when tj <= ti
-                const bool below = s < r || tj <= ti;
-                const float ke = kj[s] * __expf(below ? gi[r] - gj[s] : 0.f);
-                a[r][s] = fmaf(ki[r], ke, a[r][s]);
-                p[r][s] = fmaf(qi[r], ke, p[r][s]);
-            }
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int s = 0; s <= r; ++s) {
+                    // s < r: j < i for every thread; s == r: j <= i only when tj <= ti
+                    const bool below = s < r || tj <= ti;
+                    const float ke = kj[s][e] * __expf(below ? gi[r][e] - gj[s][e] : 0.f);
+                    a[r][s] = fmaf(ki[r][e], ke, a[r][s]);
+                    p[r][s] = fmaf(qi[r][e], ke, p[r][s]);
+                }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -142,10 +199,11 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
     const int n = blockIdx.z;
     const int V = p.d_v;
     const int H = p.H;
+    const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
     int b, t0, t1;
     if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
 
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     float* Ks = sm;              // k; then exp(G) o k; then scratch of the inverse
     float* Qs = Ks + 64 * LDK;   // q; then exp(G) o q
     float* Gk = Qs + 64 * LDK;   // g; then G; then exp(G_n - G) o k
@@ -160,9 +218,10 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
 
     const bool with_out = p.out != nullptr;
     const long long state_off = (static_cast<long long>(n) * H + h) * K * V + vs * kVs;
-    for (int e = threadIdx.x; e < K * kVs; e += blockDim.x) {
-        const int i = e / kVs, j = e % kVs;
-        Ss[i * LDC + j] = p.initial_state ? p.initial_state[state_off + static_cast<long long>(i) * V + j] : 0.f;
+    for (int e = threadIdx.x; e < K * kVs / 4; e += blockDim.x) {
+        const int i = e / (kVs / 4), j = (e % (kVs / 4)) * 4;
+        st4(Ss + i * LDC + j, p.initial_state ? ld4(p.initial_state + state_off + static_cast<long long>(i) * V + j)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f));
     }
     const long long row_base = static_cast<long long>(b) * p.T;
     const float scale = p.scale;
@@ -204,42 +263,72 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
             Gk[i * LDK + c] = kv * expf(Gn[c] - G);
         }
         __syncthreads();
-        // R = beta o (V - (exp(G) o K) S0), in place over V
-        block_mm<64, kVs, K, 4, 4>(
-            [&](int i, int d) { return Ks[i * LDK + d]; },
-            [&](int d, int c) { return Ss[d * LDC + c]; },
-            [&](int i, int c, float acc) { Vt[i * LDC + c] = bs[i] * (Vt[i * LDC + c] - acc); });
+        {
+            // R = beta o (V - (exp(G) o K) S0), in place over V
+            float acc[4][4] = {};
+            mm_rows<4, K>(acc, Ks, LDK, Ss, LDC, ti, tj);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = ti + 16 * r;
+                float* vr = Vt + i * LDC + 4 * tj;
+                const float4 v4 = ld4(vr);
+                const float be = bs[i];
+                st4(vr, make_float4(be * (v4.x - acc[r][0]), be * (v4.y - acc[r][1]), be * (v4.z - acc[r][2]),
+                                    be * (v4.w - acc[r][3])));
+            }
+        }
         __syncthreads();
         chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
-        // Delta = T R
-        block_mm<64, kVs, 64, 4, 4>(
-            [&](int i, int j) { return Tm[i * LDC + j]; },
-            [&](int j, int c) { return Vt[j * LDC + c]; },
-            [&](int i, int c, float acc) { Au[i * LDC + c] = acc; });
+        {
+            // Delta = T R
+            float acc[4][4] = {};
+            mm_rows<4, 64>(acc, Tm, LDC, Vt, LDC, ti, tj);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                st4(Au + (ti + 16 * r) * LDC + 4 * tj, make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]));
+        }
         __syncthreads();
         if (with_out) {
             // O = scale [(exp(G) o Q) S0 + P Delta]
-            block_mm<64, kVs, K + 64, 4, 4>(
-                [&](int i, int kk) { return kk < K ? Qs[i * LDK + kk] : Pm[i * LDC + kk - K]; },
-                [&](int kk, int c) { return kk < K ? Ss[kk * LDC + c] : Au[(kk - K) * LDC + c]; },
-                [&](int i, int c, float acc) {
-                    if (i < nv)
-                        p.out[((row_base + c0 + i) * H + h) * static_cast<long long>(V) + vs * kVs + c] =
-                            f32_to_bf16(scale * acc);
-                });
+            float acc[4][4] = {};
+            mm_rows<4, K>(acc, Qs, LDK, Ss, LDC, ti, tj);
+            mm_rows<4, 64>(acc, Pm, LDC, Au, LDC, ti, tj);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = ti + 16 * r;
+                if (i < nv) {
+                    const uint32_t lo = static_cast<uint32_t>(f32_to_bf16(scale * acc[r][0])) |
+                                        (static_cast<uint32_t>(f32_to_bf16(scale * acc[r][1])) << 16);
+                    const uint32_t hi = static_cast<uint32_t>(f32_to_bf16(scale * acc[r][2])) |
+                                        (static_cast<uint32_t>(f32_to_bf16(scale * acc[r][3])) << 16);
+                    *reinterpret_cast<uint2*>(p.out + ((row_base + c0 + i) * H + h) * static_cast<long long>(V) +
+                                              vs * kVs + 4 * tj) = make_uint2(lo, hi);
+                }
+            }
             __syncthreads();
         }
-        // S1 = diag(exp(G_n)) S0 + (exp(G_n - G) o K)^T Delta
-        block_mm<K, kVs, 64, 4, 4>(
-            [&](int a, int j) { return Gk[j * LDK + a]; },
-            [&](int j, int c) { return Au[j * LDC + c]; },
-            [&](int a, int c, float acc) { Ss[a * LDC + c] = fmaf(gn[a], Ss[a * LDC + c], acc); });
+        {
+            // S1 = diag(exp(G_n)) S0 + (exp(G_n - G) o K)^T Delta
+            float acc[K / 16][4] = {};
+            mm_trans<K>(acc, Gk, LDK, Au, LDC, ti, tj);
+#pragma unroll
+            for (int m = 0; m < K / 64; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int a = 64 * m + 4 * ti + e;
+                    float* sr = Ss + a * LDC + 4 * tj;
+                    const float4 s4 = ld4(sr);
+                    const float ga = gn[a];
+                    st4(sr, make_float4(fmaf(ga, s4.x, acc[4 * m + e][0]), fmaf(ga, s4.y, acc[4 * m + e][1]),
+                                        fmaf(ga, s4.z, acc[4 * m + e][2]), fmaf(ga, s4.w, acc[4 * m + e][3])));
+                }
+        }
     }
     __syncthreads();
     if (p.final_state) {
-        for (int e = threadIdx.x; e < K * kVs; e += blockDim.x) {
-            const int i = e / kVs, j = e % kVs;
-            p.final_state[state_off + static_cast<long long>(i) * V + j] = Ss[i * LDC + j];
+        for (int e = threadIdx.x; e < K * kVs / 4; e += blockDim.x) {
+            const int i = e / (kVs / 4), j = (e % (kVs / 4)) * 4;
+            st4(p.final_state + state_off + static_cast<long long>(i) * V + j, ld4(Ss + i * LDC + j));
         }
     }
 }
