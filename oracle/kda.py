@@ -11,11 +11,17 @@ S by its own factor:
     o_t = scale S^T q_t
 (S is K x V, key rows i, value columns j).  With all channels equal it is the
 scalar-gate operator, which a test pins against the C oracle.
+
+kda_chunk_fwd_head is a second formulation of the same operator: the chunk
+algebra with the per-channel decay inside the key dot products (the form a
+chunked kernel evaluates).  In exact arithmetic it equals the token loop; the
+tests pin the two against each other to ~1e-12.
 """
 
 from __future__ import annotations
 
 import numpy as np
+from scipy.linalg import solve_triangular
 
 
 def kda_fwd_head(q, k, v, g, beta, scale, S0=None):
@@ -58,4 +64,42 @@ def kda_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None):
                                     beta[b, t0:t1, h], scale, s0)
             o[b, t0:t1, h] = o_h
             S[n, h] = S_h
+    return o, S
+
+
+def kda_chunk_fwd_head(q, k, v, g, beta, scale, S0=None, chunk=64):
+    """kda_fwd_head evaluated chunk by chunk.  Per chunk of n <= chunk tokens
+    with start state S0 and the per-channel running sums G_i = g_1 + ... + g_i
+    (vectors of K):
+        A_ij  = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)   for j < i, else 0
+        P_ij  =        sum_c q_ic k_jc exp(G_ic - G_jc)   for j <= i, else 0
+        Tm    = (I + A)^-1
+        Delta = Tm [beta o (V - (exp(G) o K) S0)]
+        O     = scale [(exp(G) o Q) S0 + P Delta]
+        S1    = diag(exp(G_n)) S0 + (exp(G_n - G) o K)^T Delta
+    (exp(G) o K scales k_ic by exp(G_ic)).  Every pair's exponent is masked to
+    j <= i before exp, so it is <= 0 for g <= 0.  Returns (o, S) in fp64."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64)
+    T, K = k.shape
+    V = v.shape[1]
+    S = np.zeros((K, V)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((T, V))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        Q, Kc, Vc, b = q[sl], k[sl], v[sl], beta[sl]
+        n = Kc.shape[0]
+        G = np.cumsum(g[sl], axis=0)                                   # (n, K)
+        i, j = np.indices((n, n))
+        expo = np.where((i >= j)[:, :, None], G[:, None, :] - G[None, :, :], -np.inf)
+        KE = Kc[None, :, :] * np.exp(expo)                             # k_jc exp(G_ic - G_jc)
+        A = np.where(i > j, b[:, None] * np.einsum("ic,ijc->ij", Kc, KE), 0.0)
+        P = np.einsum("ic,ijc->ij", Q, KE)
+        Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
+        Delta = Tm @ (b[:, None] * (Vc - (np.exp(G) * Kc) @ S))
+        o[sl] = scale * ((np.exp(G) * Q) @ S + P @ Delta)
+        S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * Kc).T @ Delta
     return o, S

@@ -1,6 +1,7 @@
 """Pins of the fp64 per-channel-gate (KDA) oracle: equal channels reduce to
 the scalar-gate C oracle, beta = 0 is pure per-channel decay, the T = 1
-closed form, and planted mistakes that the pins catch."""
+closed form, the chunked formulation equals the token loop, and planted
+mistakes that the pins catch."""
 
 import numpy as np
 import pytest
@@ -68,3 +69,104 @@ def test_planted_mistakes_are_caught():
     assert not np.allclose(S, S_wrong, rtol=1e-6)
     S_late = a[:, None] * (S0 + beta[0] * np.outer(k[0], v[0] - S0.T @ k[0]))
     assert not np.allclose(S, S_late, rtol=1e-6)
+
+
+
+def _rel(x, r):
+    return float(np.max(np.abs(x - r)) / max(np.max(np.abs(r)), 1e-300))
+
+
+@pytest.mark.parametrize("T,chunk", [(1, 64), (37, 64), (64, 64), (65, 64), (150, 64), (150, 16), (41, 5)])
+def test_chunked_equals_token_loop(T, chunk):
+    """The per-channel chunk algebra reaches the token loop's result: one
+    token, a ragged single chunk, exact multiples, a ragged tail, and chunk
+    sizes that cut the sequence into many pieces."""
+    q, k, v, g, beta, S0 = _head(T, 6, 5, 10 + T + chunk)
+    beta = beta * 2.0
+    o_ref, S_ref = kda.kda_fwd_head(q, k, v, g, beta, 0.45, S0)
+    o, S = kda.kda_chunk_fwd_head(q, k, v, g, beta, 0.45, S0, chunk=chunk)
+    assert _rel(o, o_ref) < 1e-12 and _rel(S, S_ref) < 1e-12, (_rel(o, o_ref), _rel(S, S_ref))
+
+
+def test_chunked_equals_token_loop_wider_heads():
+    q, k, v, g, beta, S0 = _head(130, 16, 12, 21)
+    o_ref, S_ref = kda.kda_fwd_head(q, k, v, g, beta, 0.25, S0)
+    o, S = kda.kda_chunk_fwd_head(q, k, v, g, beta, 0.25, S0)
+    assert _rel(o, o_ref) < 1e-12 and _rel(S, S_ref) < 1e-12
+
+
+def _factorised_chunk_head(q, k, v, g, beta, scale, S0, chunk=64):
+    """A planted mistake: the decay of a pair written as exp(G_i) exp(-G_j),
+    without masking before exp."""
+    T, K = k.shape
+    S = np.array(S0, dtype=np.float64)
+    o = np.zeros((T, v.shape[1]))
+    with np.errstate(over="ignore", invalid="ignore"):
+        for c0 in range(0, T, chunk):
+            sl = slice(c0, min(T, c0 + chunk))
+            Q, Kc, Vc, b = q[sl], k[sl], v[sl], beta[sl]
+            n = Kc.shape[0]
+            G = np.cumsum(g[sl], axis=0)
+            up, down = np.exp(G) * Kc, np.exp(-G) * Kc
+            i, j = np.indices((n, n))
+            A = np.where(i > j, b[:, None] * (up @ down.T), 0.0)
+            P = np.where(i >= j, (np.exp(G) * Q) @ down.T, 0.0)
+            Tm = np.linalg.inv(np.eye(n) + A)
+            Delta = Tm @ (b[:, None] * (Vc - up @ S))
+            o[sl] = scale * ((np.exp(G) * Q) @ S + P @ Delta)
+            S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * Kc).T @ Delta
+    return o, S
+
+
+def test_strong_decay_needs_the_masked_exponent():
+    """Per-channel log decays down to -40 per token: inside a 64-token chunk
+    G reaches about -2500.  The masked form stays finite and exact; writing a
+    pair's decay as exp(G_i) exp(-G_j) overflows."""
+    q, k, v, g, beta, S0 = _head(128, 6, 5, 22)
+    g = g * 80.0
+    o_ref, S_ref = kda.kda_fwd_head(q, k, v, g, beta, 0.5, S0)
+    o, S = kda.kda_chunk_fwd_head(q, k, v, g, beta, 0.5, S0)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    assert _rel(o, o_ref) < 1e-12 and _rel(S, S_ref) < 1e-12
+    o_bad, S_bad = _factorised_chunk_head(q, k, v, g, beta, 0.5, S0)
+    assert not (np.isfinite(o_bad).all() and _rel(o_bad, o_ref) < 1e-6)
+
+
+def test_chunked_planted_mistakes_are_caught():
+    """The chunked pin catches a scalar gate (the per-channel decays replaced
+    by their mean), a causal score without its diagonal, and the gram with its
+    diagonal kept."""
+    q, k, v, g, beta, S0 = _head(100, 6, 5, 23)
+    o_ref, S_ref = kda.kda_fwd_head(q, k, v, g, beta, 0.5, S0)
+    gm = np.repeat(g.mean(axis=1, keepdims=True), 6, axis=1)
+    o, S = kda.kda_chunk_fwd_head(q, k, v, gm, beta, 0.5, S0)
+    assert _rel(o, o_ref) > 1e-6
+
+    def variant(drop_p_diag, keep_a_diag):
+        T = 100
+        S = np.array(S0)
+        o = np.zeros((T, 5))
+        for c0 in range(0, T, 64):
+            sl = slice(c0, min(T, c0 + 64))
+            Q, Kc, Vc, b = q[sl], k[sl], v[sl], beta[sl]
+            n = Kc.shape[0]
+            G = np.cumsum(g[sl], axis=0)
+            i, j = np.indices((n, n))
+            expo = np.where((i >= j)[:, :, None], G[:, None, :] - G[None, :, :], -np.inf)
+            KE = Kc[None, :, :] * np.exp(expo)
+            A = np.where((i >= j) if keep_a_diag else (i > j), b[:, None] * np.einsum("ic,ijc->ij", Kc, KE), 0.0)
+            P = np.einsum("ic,ijc->ij", Q, KE)
+            if drop_p_diag:
+                P = np.where(i > j, P, 0.0)
+            Tm = np.linalg.inv(np.eye(n) + A)
+            Delta = Tm @ (b[:, None] * (Vc - (np.exp(G) * Kc) @ S))
+            o[sl] = 0.5 * ((np.exp(G) * Q) @ S + P @ Delta)
+            S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * Kc).T @ Delta
+        return o, S
+
+    for flags in ((False, False), (True, False), (False, True)):
+        o, S = variant(*flags)
+        if flags == (False, False):
+            assert _rel(o, o_ref) < 1e-12   # the variant itself is the right algebra
+        else:
+            assert _rel(o, o_ref) > 1e-6, flags
