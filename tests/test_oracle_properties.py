@@ -1,9 +1,9 @@
 """Property tests of the fp64 oracle over random shapes (hypothesis; CPU
 only): three independent formulations of the same operator agree on any
 input -- the per-token recurrence (C), the chunked WY algebra at any chunk
-length, and the segment composition at any cut points -- and the
+length, and the segment composition at any cut points -- the
 per-channel-gate recurrence reduces to the scalar one when its channels
-are equal."""
+are equal, and its chunk algebra equals its token loop."""
 
 import numpy as np
 import pytest
@@ -70,3 +70,20 @@ def test_per_channel_gate_with_equal_channels_is_the_scalar_gate(shape, seed):
     o1, S1 = _lib().fwd_head(q, k, v, g, beta, 0.3, S0)
     o2, S2 = kda.kda_fwd_head(q, k, v, np.repeat(g[:, None], K, axis=1), beta, 0.3, S0)
     assert _rel(o2, o1) < 1e-12 and _rel(S2, S1) < 1e-12
+
+
+@SETTINGS
+@given(shape=shapes, chunk=st.integers(1, 70), seed=st.integers(0, 2**31 - 1),
+       beta_max=st.sampled_from([1.0, 2.0]), g_low=st.sampled_from([-0.05, -0.5, -4.0, -40.0]))
+def test_per_channel_chunk_algebra_equals_its_token_loop(shape, chunk, seed, beta_max, g_low):
+    """Per-channel decays drawn independently per token and key channel, down
+    to -40 per token (exponents far below the fp64 range of exp inside a
+    chunk)."""
+    T, K, V = shape
+    r = np.random.default_rng(seed)
+    q, k, v, _, beta, S0 = _head(seed, T, K, V, beta_max, g_low)
+    g = r.uniform(g_low, 0.0, (T, K))
+    o1, S1 = kda.kda_fwd_head(q, k, v, g, beta, 0.6, S0)
+    o2, S2 = kda.kda_chunk_fwd_head(q, k, v, g, beta, 0.6, S0, chunk=chunk)
+    assert np.isfinite(o2).all() and np.isfinite(S2).all()
+    assert _rel(o2, o1) < 1e-10 and _rel(S2, S1) < 1e-10
