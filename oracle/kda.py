@@ -16,6 +16,11 @@ kda_chunk_fwd_head is a second formulation of the same operator: the chunk
 algebra with the per-channel decay inside the key dot products (the form a
 chunked kernel evaluates).  In exact arithmetic it equals the token loop; the
 tests pin the two against each other to ~1e-12.
+
+kda_bwd_head is the reverse mode of the token loop (gradients of
+L = <o, dO> + <S_T, dS_T> with respect to every input), pinned by central
+finite differences and, with all channels equal, by the scalar-gate C
+oracle's reverse mode.
 """
 
 from __future__ import annotations
@@ -103,3 +108,61 @@ def kda_chunk_fwd_head(q, k, v, g, beta, scale, S0=None, chunk=64):
         o[sl] = scale * ((np.exp(G) * Q) @ S + P @ Delta)
         S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * Kc).T @ Delta
     return o, S
+
+
+def kda_bwd_head(q, k, v, g, beta, scale, S0, dO, dS_final, checkpoint=64):
+    """Reverse mode of kda_fwd_head, token by token from t = T down to 1, with
+    the state recomputed forward from checkpoints every `checkpoint` tokens.
+    Per token (S' = diag(exp(g_t)) S_{t-1}, e = v_t - S'^T k_t,
+    S_t = S' + beta_t k_t e^T, o_t = scale S_t^T q_t), with dS the gradient
+    with respect to S_t:
+        dS    += scale q_t dO_t^T;        dq_t = scale S_t dO_t
+        dbeta_t = k_t^T dS e;             de = beta_t dS^T k_t
+        dv_t  = de;                        dk_t = beta_t dS e - S' de
+        dS'   = dS - k_t de^T;             dg_t = rowsum(dS' o S')   (per key channel)
+        dS_{t-1} = diag(exp(g_t)) dS'
+    Returns dict of dq, dk (T, K), dv (T, V), dg (T, K), dbeta (T,), dS0 (K, V)."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64)
+    dO = np.asarray(dO, np.float64)
+    T, K = k.shape
+    V = v.shape[1]
+    S = np.zeros((K, V)) if S0 is None else np.array(S0, dtype=np.float64)
+    # forward: the state at the start of every checkpoint segment
+    starts = []
+    for t in range(T):
+        if t % checkpoint == 0:
+            starts.append(S.copy())
+        S = np.exp(g[t])[:, None] * S
+        S = S + beta[t] * np.outer(k[t], v[t] - S.T @ k[t])
+    out = dict(dq=np.zeros((T, K)), dk=np.zeros((T, K)), dv=np.zeros((T, V)), dg=np.zeros((T, K)),
+               dbeta=np.zeros(T), dS0=None)
+    dS = np.zeros((K, V)) if dS_final is None else np.array(dS_final, dtype=np.float64)
+    for si in range(len(starts) - 1, -1, -1):
+        t0 = si * checkpoint
+        t1 = min(T, t0 + checkpoint)
+        # recompute S'_t and S_t inside the segment
+        Sp, St = [], []
+        S = starts[si].copy()
+        for t in range(t0, t1):
+            S = np.exp(g[t])[:, None] * S
+            Sp.append(S.copy())
+            S = S + beta[t] * np.outer(k[t], v[t] - S.T @ k[t])
+            St.append(S.copy())
+        for t in range(t1 - 1, t0 - 1, -1):
+            P, Sn = Sp[t - t0], St[t - t0]
+            dS = dS + scale * np.outer(q[t], dO[t])
+            out["dq"][t] = scale * (Sn @ dO[t])
+            e = v[t] - P.T @ k[t]
+            out["dbeta"][t] = k[t] @ dS @ e
+            de = beta[t] * (dS.T @ k[t])
+            out["dv"][t] = de
+            out["dk"][t] = beta[t] * (dS @ e) - P @ de
+            dSp = dS - np.outer(k[t], de)
+            out["dg"][t] = np.sum(dSp * P, axis=1)
+            dS = np.exp(g[t])[:, None] * dSp
+    out["dS0"] = dS
+    return out

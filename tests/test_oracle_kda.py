@@ -1,7 +1,8 @@
 """Pins of the fp64 per-channel-gate (KDA) oracle: equal channels reduce to
 the scalar-gate C oracle, beta = 0 is pure per-channel decay, the T = 1
-closed form, the chunked formulation equals the token loop, and planted
-mistakes that the pins catch."""
+closed form, the chunked formulation equals the token loop, the reverse mode
+matches central finite differences and (equal channels) the scalar C
+oracle's reverse mode, and planted mistakes that the pins catch."""
 
 import numpy as np
 import pytest
@@ -170,3 +171,66 @@ def test_chunked_planted_mistakes_are_caught():
             assert _rel(o, o_ref) < 1e-12   # the variant itself is the right algebra
         else:
             assert _rel(o, o_ref) > 1e-6, flags
+
+
+
+def _fd_check(bwd, T, K, V, seed, checkpoint=64):
+    q, k, v, g, beta, S0 = _head(T, K, V, seed)
+    beta = beta * 2.0
+    r = np.random.default_rng(seed + 1)
+    dO = r.standard_normal((T, V))
+    dSf = r.standard_normal((K, V))
+    scale = 0.7
+
+    def loss(args):
+        o, S = kda.kda_fwd_head(*args[:5], scale, args[5])
+        return float(np.sum(o * dO) + np.sum(S * dSf))
+
+    grads = bwd(q, k, v, g, beta, scale, S0, dO, dSf, checkpoint=checkpoint)
+    args = [q, k, v, g, beta, S0]
+    worst = {}
+    for ai, name in enumerate(["dq", "dk", "dv", "dg", "dbeta", "dS0"]):
+        fd = np.zeros_like(args[ai])
+        for idx in np.ndindex(args[ai].shape):
+            ap = [a.copy() for a in args]
+            am = [a.copy() for a in args]
+            ap[ai][idx] += 1e-6
+            am[ai][idx] -= 1e-6
+            fd[idx] = (loss(ap) - loss(am)) / 2e-6
+        worst[name] = _rel(grads[name], fd)
+    return worst
+
+
+@pytest.mark.parametrize("T,K,V,checkpoint", [(7, 3, 4, 64), (8, 4, 3, 3), (1, 2, 2, 64)])
+def test_reverse_mode_matches_finite_differences(T, K, V, checkpoint):
+    """Every gradient (dg per key channel) against central differences of
+    L = <o, dO> + <S_T, dS_T>, with and without checkpoint segments."""
+    worst = _fd_check(kda.kda_bwd_head, T, K, V, 30 + T, checkpoint)
+    assert all(e < 1e-7 for e in worst.values()), worst
+
+
+def test_reverse_mode_with_equal_channels_is_the_scalar_reverse_mode(lib):
+    """All channels equal: every gradient equals the scalar-gate C oracle's,
+    with dg summed over the key channels."""
+    q, k, v, g, beta, S0 = _head(150, 6, 5, 40)
+    gs = g[:, 0]
+    r = np.random.default_rng(41)
+    dO = r.standard_normal((150, 5))
+    dSf = r.standard_normal((6, 5))
+    a = kda.kda_bwd_head(q, k, v, np.repeat(gs[:, None], 6, axis=1), beta * 2.0, 0.4, S0, dO, dSf)
+    b = lib.bwd_head(q, k, v, gs, beta * 2.0, 0.4, S0, dO, dSf)
+    for name in ("dq", "dk", "dv", "dbeta", "dS0"):
+        assert _rel(a[name], b[name]) < 1e-12, name
+    assert _rel(a["dg"].sum(axis=1), b["dg"]) < 1e-12
+
+
+def test_reverse_mode_planted_mistake_is_caught():
+    """A per-channel gate gradient summed over the value columns of the state
+    before the decay (dS' o S_{t-1} instead of dS' o S') breaks the
+    finite-difference pin."""
+    def wrong(q, k, v, g, beta, scale, S0, dO, dSf, checkpoint=64):
+        out = kda.kda_bwd_head(q, k, v, g, beta, scale, S0, dO, dSf, checkpoint)
+        out["dg"] = out["dg"] * np.exp(-g)    # the pre-decay state's rows
+        return out
+    worst = _fd_check(wrong, 7, 3, 4, 37)
+    assert worst["dg"] > 1e-6 and worst["dq"] < 1e-7
