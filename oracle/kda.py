@@ -72,6 +72,31 @@ def kda_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None):
     return o, S
 
 
+def _kda_chunk(Q, Kc, Vc, gc, bc, S0):
+    """Intermediates of one chunk of the per-channel chunk algebra (fp64)."""
+    n = Kc.shape[0]
+    G = np.cumsum(gc, axis=0)                                          # (n, K)
+    i, j = np.indices((n, n))
+    expo = np.where((i >= j)[:, :, None], G[:, None, :] - G[None, :, :], -np.inf)
+    E = np.exp(expo)                                                   # exp(G_ic - G_jc), 0 above
+    KE = Kc[None, :, :] * E                                            # k_jc E_ijc
+    Ap = np.where(i > j, np.einsum("ic,ijc->ij", Kc, KE), 0.0)          # A without beta
+    A = bc[:, None] * Ap
+    P = np.einsum("ic,ijc->ij", Q, KE)
+    Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
+    Gam = np.exp(G)
+    KG, QG = Gam * Kc, Gam * Q
+    U = Vc - KG @ S0                                                   # V - (exp(G) o K) S0
+    R = bc[:, None] * U
+    Delta = Tm @ R
+    Dn = np.exp(G[-1][None, :] - G)                                    # exp(G_n - G)
+    Kt = Dn * Kc
+    gn = np.exp(G[-1])
+    S1 = gn[:, None] * S0 + Kt.T @ Delta
+    return dict(G=G, E=E, Ap=Ap, A=A, P=P, Tm=Tm, Gam=Gam, KG=KG, QG=QG, U=U, R=R, Delta=Delta,
+                Dn=Dn, Kt=Kt, gn=gn, S0=S0, S1=S1, lower=(i >= j), strict=(i > j))
+
+
 def kda_chunk_fwd_head(q, k, v, g, beta, scale, S0=None, chunk=64):
     """kda_fwd_head evaluated chunk by chunk.  Per chunk of n <= chunk tokens
     with start state S0 and the per-channel running sums G_i = g_1 + ... + g_i
@@ -84,30 +109,97 @@ def kda_chunk_fwd_head(q, k, v, g, beta, scale, S0=None, chunk=64):
         S1    = diag(exp(G_n)) S0 + (exp(G_n - G) o K)^T Delta
     (exp(G) o K scales k_ic by exp(G_ic)).  Every pair's exponent is masked to
     j <= i before exp, so it is <= 0 for g <= 0.  Returns (o, S) in fp64."""
-    q = np.asarray(q, np.float64)
-    k = np.asarray(k, np.float64)
-    v = np.asarray(v, np.float64)
-    g = np.asarray(g, np.float64)
-    beta = np.asarray(beta, np.float64)
+    q, k, v, g, beta = (np.asarray(x, np.float64) for x in (q, k, v, g, beta))
     T, K = k.shape
     V = v.shape[1]
     S = np.zeros((K, V)) if S0 is None else np.array(S0, dtype=np.float64)
     o = np.zeros((T, V))
     for c0 in range(0, T, chunk):
         sl = slice(c0, min(T, c0 + chunk))
-        Q, Kc, Vc, b = q[sl], k[sl], v[sl], beta[sl]
-        n = Kc.shape[0]
-        G = np.cumsum(g[sl], axis=0)                                   # (n, K)
-        i, j = np.indices((n, n))
-        expo = np.where((i >= j)[:, :, None], G[:, None, :] - G[None, :, :], -np.inf)
-        KE = Kc[None, :, :] * np.exp(expo)                             # k_jc exp(G_ic - G_jc)
-        A = np.where(i > j, b[:, None] * np.einsum("ic,ijc->ij", Kc, KE), 0.0)
-        P = np.einsum("ic,ijc->ij", Q, KE)
-        Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
-        Delta = Tm @ (b[:, None] * (Vc - (np.exp(G) * Kc) @ S))
-        o[sl] = scale * ((np.exp(G) * Q) @ S + P @ Delta)
-        S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * Kc).T @ Delta
+        f = _kda_chunk(q[sl], k[sl], v[sl], g[sl], beta[sl], S)
+        o[sl] = scale * (f["QG"] @ S + f["P"] @ f["Delta"])
+        S = f["S1"]
     return o, S
+
+
+def kda_chunk_bwd_head(q, k, v, g, beta, scale, S0, dO, dS_final, chunk=64):
+    """Reverse mode of kda_chunk_fwd_head: chunks from last to first, carrying
+    dS (the gradient with respect to the chunk-end state).  Per chunk, in
+    reverse order of the forward steps:
+      O = scale [QG S0 + P Delta]      dQG = scale dO S0^T, dS0 = scale QG^T dO,
+                                       dP = scale dO Delta^T (j <= i), dDelta = scale P^T dO
+      S1 = diag(gn) S0 + Kt^T Delta    dS0 += diag(gn) dS, dG_n += gn o rowsum(dS o S0),
+                                       dKt = Delta dS^T, dDelta += Kt dS
+      Kt = exp(G_n - G) o K            dK += dKt o exp(G_n - G); X = dKt o Kt: dG_n += colsum X, dG -= X
+      Delta = Tm R                     dR = Tm^T dDelta, dA = -dR Delta^T (j < i)
+      R = beta o (V - KG S0)           dV = beta o dR, dbeta += rowsum(dR o U),
+                                       dKG = -(beta o dR) S0^T, dS0 -= KG^T (beta o dR)
+      KG = exp(G) o K, QG = exp(G) o Q dK += dKG o exp(G), dQ += dQG o exp(G), dG += dKG o KG + dQG o QG
+      A = beta o A', A'_ij = sum_c k_ic k_jc E_ijc (j < i)
+                                       dbeta += rowsum(dA o A'); W = beta o dA:
+                                       dk_i += sum_j W_ij k_j o E_ij, dk_j += sum_i W_ij k_i o E_ij
+      P_ij = sum_c q_ic k_jc E_ijc     dq_i += sum_j dP_ij k_j o E_ij, dk_j += sum_i dP_ij q_i o E_ij
+      E_ijc = exp(G_ic - G_jc)         Y_ijc = (W_ij k_ic + dP_ij q_ic) k_jc E_ijc:
+                                       dG_i += sum_j Y_ij, dG_j -= sum_i Y_ij
+      G = cumsum(g)                    dg = reverse running sum of dG, per channel
+    Returns dict of dq, dk (T, K), dv (T, V), dg (T, K), dbeta (T,), dS0 (K, V)."""
+    q, k, v, g, beta, dO = (np.asarray(x, np.float64) for x in (q, k, v, g, beta, dO))
+    T, K = k.shape
+    V = v.shape[1]
+    S = np.zeros((K, V)) if S0 is None else np.array(S0, dtype=np.float64)
+    chunks = []
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        f = _kda_chunk(q[sl], k[sl], v[sl], g[sl], beta[sl], S)
+        chunks.append((sl, f))
+        S = f["S1"]
+    out = dict(dq=np.zeros((T, K)), dk=np.zeros((T, K)), dv=np.zeros((T, V)), dg=np.zeros((T, K)),
+               dbeta=np.zeros(T), dS0=None)
+    dS = np.zeros((K, V)) if dS_final is None else np.array(dS_final, dtype=np.float64)
+    for sl, f in reversed(chunks):
+        Q, Kc, bc, dOc, S0c = q[sl], k[sl], beta[sl], dO[sl], f["S0"]
+        E = f["E"]
+        # output
+        dQG = scale * dOc @ S0c.T
+        dS0 = scale * f["QG"].T @ dOc
+        dP = np.where(f["lower"], scale * dOc @ f["Delta"].T, 0.0)
+        dDelta = scale * f["P"].T @ dOc
+        # state update
+        dS0 += f["gn"][:, None] * dS
+        dG = np.zeros_like(f["G"])
+        dG[-1] += f["gn"] * np.sum(dS * S0c, axis=1)
+        dKt = f["Delta"] @ dS.T
+        dDelta += f["Kt"] @ dS
+        dK = dKt * f["Dn"]
+        X = dKt * f["Kt"]
+        dG[-1] += X.sum(axis=0)
+        dG -= X
+        # triangular solve and residual
+        dR = f["Tm"].T @ dDelta
+        dA = np.where(f["strict"], -dR @ f["Delta"].T, 0.0)
+        dv = bc[:, None] * dR
+        dbeta = np.sum(dR * f["U"], axis=1)
+        dKG = -(bc[:, None] * dR) @ S0c.T
+        dS0 -= f["KG"].T @ (bc[:, None] * dR)
+        dK += dKG * f["Gam"]
+        dQ = dQG * f["Gam"]
+        dG += dKG * f["KG"] + dQG * f["QG"]
+        # the two decayed sums
+        dbeta += np.sum(dA * f["Ap"], axis=1)
+        W = bc[:, None] * dA
+        dK += np.einsum("ij,jc,ijc->ic", W, Kc, E) + np.einsum("ij,ic,ijc->jc", W, Kc, E)
+        dQ += np.einsum("ij,jc,ijc->ic", dP, Kc, E)
+        dK += np.einsum("ij,ic,ijc->jc", dP, Q, E)
+        Y = (W[:, :, None] * Kc[:, None, :] + dP[:, :, None] * Q[:, None, :]) * Kc[None, :, :] * E
+        dG += Y.sum(axis=1) - Y.sum(axis=0)
+        out["dq"][sl] = dQ
+        out["dk"][sl] = dK
+        out["dv"][sl] = dv
+        out["dbeta"][sl] = dbeta
+        out["dg"][sl] = np.cumsum(dG[::-1], axis=0)[::-1]
+        dS = dS0
+    out["dS0"] = dS
+    return out
 
 
 def kda_bwd_head(q, k, v, g, beta, scale, S0, dO, dS_final, checkpoint=64):

@@ -234,3 +234,61 @@ def test_reverse_mode_planted_mistake_is_caught():
         return out
     worst = _fd_check(wrong, 7, 3, 4, 37)
     assert worst["dg"] > 1e-6 and worst["dq"] < 1e-7
+
+
+CHUNK_BWD_CASES = [(7, 3, 4, 64, -0.5), (150, 6, 5, 64, -0.5), (97, 4, 8, 16, -0.5), (41, 5, 3, 5, -4.0),
+                   (128, 6, 5, 64, -40.0), (1, 2, 2, 64, -0.5)]
+
+
+def _bwd_inputs(T, K, V, g_low, seed):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((T, K))
+    k = r.standard_normal((T, K))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = r.standard_normal((T, V))
+    g = r.uniform(g_low, 0.0, (T, K))
+    beta = r.uniform(0.0, 2.0, T)
+    S0 = r.standard_normal((K, V))
+    return q, k, v, g, beta, S0, r.standard_normal((T, V)), r.standard_normal((K, V))
+
+
+@pytest.mark.parametrize("T,K,V,chunk,g_low", CHUNK_BWD_CASES)
+def test_chunked_reverse_mode_equals_token_reverse_mode(T, K, V, chunk, g_low):
+    """The reverse mode of the per-channel chunk algebra (derived step by step
+    through the chunk's intermediates) gives the token loop's gradients:
+    ragged chunks, chunk sizes 64 / 16 / 5, decays down to -40 per token."""
+    q, k, v, g, beta, S0, dO, dSf = _bwd_inputs(T, K, V, g_low, 50 + T)
+    a = kda.kda_bwd_head(q, k, v, g, beta, 0.6, S0, dO, dSf)
+    b = kda.kda_chunk_bwd_head(q, k, v, g, beta, 0.6, S0, dO, dSf, chunk=chunk)
+    for name in a:
+        assert _rel(b[name], a[name]) < 1e-11, (name, _rel(b[name], a[name]))
+
+
+MUTATIONS = [
+    ("gram column-role key gradient dropped",
+     ' + np.einsum("ij,ic,ijc->jc", W, Kc, E)', ""),
+    ("decay-exponent gradient of the earlier token dropped",
+     "dG += Y.sum(axis=1) - Y.sum(axis=0)", "dG += Y.sum(axis=1)"),
+    ("gram gradient kept on the diagonal",
+     'dA = np.where(f["strict"], -dR @ f["Delta"].T, 0.0)', 'dA = np.where(f["lower"], -dR @ f["Delta"].T, 0.0)'),
+    ("gate gradient summed forward instead of backward",
+     'out["dg"][sl] = np.cumsum(dG[::-1], axis=0)[::-1]', 'out["dg"][sl] = np.cumsum(dG, axis=0)'),
+    ("state-decay gate gradient dropped",
+     'dG[-1] += f["gn"] * np.sum(dS * S0c, axis=1)', "pass"),
+]
+
+
+@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_chunked_reverse_mode_planted_mistakes_are_caught(what, old, new):
+    """Each mistake, planted in a copy of the chunked reverse mode's source,
+    breaks its agreement with the token loop's reverse mode."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(kda.kda_chunk_bwd_head))
+    assert src.count(old) == 1, what
+    ns = dict(vars(kda))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    q, k, v, g, beta, S0, dO, dSf = _bwd_inputs(150, 6, 5, -0.5, 60)
+    ref = kda.kda_bwd_head(q, k, v, g, beta, 0.6, S0, dO, dSf)
+    bad = ns["kda_chunk_bwd_head"](q, k, v, g, beta, 0.6, S0, dO, dSf, chunk=64)
+    assert max(_rel(bad[n], ref[n]) for n in ref) > 1e-6, what
