@@ -18,6 +18,13 @@ computed here left to right (M <- A_t M, b <- A_t b + B_t), independently of
 S_start.  The start state of segment j + 1 is the composition
     S_start(j + 1) = M_j S_start(j) + b_j,
 and each segment then runs the ordinary recurrence from its true start.
+
+#126's own kernel is the per-channel-gate (KDA) variant, where the decay is
+diag(exp(g_t)) with g_t in R^K; there the per-token map is
+    A_t = (I - beta_t k_t k_t^T) diag(exp(g_t)),   B_t = beta_t k_t v_t^T
+(the decay scales the key rows before the read, so it sits on the right), and
+the same carries and composition apply.  segment_carry takes g of shape (n,)
+or (n, K) and builds the matching A_t.
 """
 
 from __future__ import annotations
@@ -26,7 +33,8 @@ import numpy as np
 
 
 def segment_carry(k, v, g, beta):
-    """(M (K x K), b (K x V)) of one segment: k (n, K), v (n, V), g, beta (n,)."""
+    """(M (K x K), b (K x V)) of one segment: k (n, K), v (n, V), beta (n,);
+    g (n,) for one decay per token, or (n, K) for one per key channel."""
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     g = np.asarray(g, np.float64)
@@ -35,7 +43,7 @@ def segment_carry(k, v, g, beta):
     M = np.eye(K)
     b = np.zeros((K, v.shape[1]))
     for t in range(n):
-        A = np.exp(g[t]) * (np.eye(K) - beta[t] * np.outer(k[t], k[t]))
+        A = (np.eye(K) - beta[t] * np.outer(k[t], k[t])) * np.exp(g[t])   # columns scaled: (.) diag(exp g)
         M = A @ M
         b = A @ b + beta[t] * np.outer(k[t], v[t])
     return M, b
