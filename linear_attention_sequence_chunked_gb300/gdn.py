@@ -105,10 +105,18 @@ def load():
 
 
 def _ptr(x):
+    """Device address of a tensor argument (None and raw integer addresses
+    pass through).  The kernels read every tensor as dense row-major device
+    memory, so a strided view or a host tensor is refused here, before any
+    call into the library."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(x.shape)} strides {x.stride()}")
+    if x.device.type != "cuda":
+        raise ValueError(f"expected a CUDA tensor, got one on {x.device}")
     return x.data_ptr()
 
 

@@ -194,3 +194,18 @@ def test_split_host_validation(lib):
     assert call(ws=FAKE + 32) == 3
     assert call(out=None) == 1
     assert call(d_k=96) == 2
+
+
+def test_tensor_arguments_must_be_dense_device_memory(lib):
+    """The binding refuses a strided view or a host tensor before calling the
+    library (the kernels would read either as dense device memory)."""
+    import torch
+    x = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16)
+    g = torch.zeros((1, 64, 1, 64))
+    beta = torch.zeros((1, 64, 1), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="contiguous"):
+        gdn.gdn_kda_chunk_fwd(x.transpose(1, 3), x, x, g, beta, 1.0, None, None, x, None, 1, 64, 1, 64, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gdn_kda_chunk_fwd(x, x, x, g, beta, 1.0, None, None, x, None, 1, 64, 1, 64, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.chunk_gated_delta_rule_fwd(x, x, x, g[..., 0], beta)
