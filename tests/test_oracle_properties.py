@@ -87,3 +87,33 @@ def test_per_channel_chunk_algebra_equals_its_token_loop(shape, chunk, seed, bet
     o2, S2 = kda.kda_chunk_fwd_head(q, k, v, g, beta, 0.6, S0, chunk=chunk)
     assert np.isfinite(o2).all() and np.isfinite(S2).all()
     assert _rel(o2, o1) < 1e-10 and _rel(S2, S1) < 1e-10
+
+
+@SETTINGS
+@given(shape=st.tuples(st.integers(1, 80), st.integers(1, 6), st.integers(1, 5)), chunk=st.integers(1, 70),
+       seed=st.integers(0, 2**31 - 1), g_low=st.sampled_from([-0.05, -0.5, -4.0, -40.0]))
+def test_per_channel_chunked_reverse_mode_equals_token_reverse_mode(shape, chunk, seed, g_low):
+    T, K, V = shape
+    r = np.random.default_rng(seed)
+    q, k, v, _, beta, S0 = _head(seed, T, K, V, 2.0, g_low)
+    g = r.uniform(g_low, 0.0, (T, K))
+    dO = r.standard_normal((T, V))
+    dSf = r.standard_normal((K, V))
+    a = kda.kda_bwd_head(q, k, v, g, beta, 0.6, S0, dO, dSf)
+    b = kda.kda_chunk_bwd_head(q, k, v, g, beta, 0.6, S0, dO, dSf, chunk=chunk)
+    for name in a:
+        assert np.isfinite(b[name]).all(), name
+        assert _rel(b[name], a[name]) < 1e-9, name
+
+
+@SETTINGS
+@given(shape=shapes, seed=st.integers(0, 2**31 - 1), data=st.data())
+def test_per_channel_segment_composition_equals_token_loop(shape, seed, data):
+    T, K, V = shape
+    r = np.random.default_rng(seed)
+    q, k, v, _, beta, S0 = _head(seed, T, K, V, 2.0, -0.5)
+    g = r.uniform(-0.5, 0.0, (T, K))
+    cuts = sorted(set(data.draw(st.lists(st.integers(1, max(1, T - 1)), max_size=8)))) if T > 1 else []
+    o1, S1 = kda.kda_fwd_head(q, k, v, g, beta, 0.4, S0)
+    o2, S2, _ = segments.segmented_fwd(kda.kda_fwd_head, q, k, v, g, beta, 0.4, S0, cuts)
+    assert _rel(o2, o1) < 1e-10 and _rel(S2, S1) < 1e-10
