@@ -292,6 +292,12 @@ GDN_API gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, con
  * Synchronises `stream`, then returns and clears the device error word of
  * the current device: GDN_OK, GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT
  * (GDN_ERR_CUDA if the synchronisation or the read itself failed).
+ * The word is one per device, not one per stream: with library calls in
+ * flight on several streams of the same device, the code returned (and
+ * cleared) may come from another stream's call.  Callers that need to tell
+ * their calls apart serialise them, or synchronise the device before
+ * reading.  The first error recorded wins; later ones are dropped until the
+ * word is cleared.
  */
 GDN_API gdn_status gdn_get_last_device_error(cudaStream_t stream);
 

@@ -20,10 +20,11 @@ constexpr size_t kAlign = 256;
 // Kernels launched by this process through the library.
 std::atomic<uint64_t> g_launches{0};
 
-// Each launch_* helper enqueues exactly one kernel; count it on success.
-bool launched(cudaError_t e) {
+// Count the `kernels` kernels that a launch_* helper enqueued, on success.
+// Most helpers enqueue exactly one; the callers of the others pass their count.
+bool launched(cudaError_t e, int kernels = 1) {
     if (e != cudaSuccess) return false;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_launches.fetch_add(static_cast<uint64_t>(kernels), std::memory_order_relaxed);
     return true;
 }
 
@@ -341,7 +342,8 @@ gdn_status gdn_prologue_fwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const 
     pa.q_raw = q_raw; pa.k_raw = k_raw; pa.a = a; pa.b = b; pa.A_log = A_log; pa.dt_bias = dt_bias;
     pa.gate_mode = gate_mode; pa.lower = lower; pa.beta_scale = beta_scale;
     pa.q = q; pa.k = k; pa.g = g; pa.beta = beta; pa.rows = rows; pa.H = H; pa.d_k = d_k;
-    if (!launched(gdn::launch_prologue_fwd(pa, stream))) return GDN_ERR_CUDA;
+    if (!launched(gdn::launch_prologue_fwd(pa, stream), static_cast<long long>(rows) * H == 0 ? 0 : 1))
+        return GDN_ERR_CUDA;
     return GDN_OK;
 }
 
@@ -366,7 +368,9 @@ gdn_status gdn_prologue_bwd(const gdn_bf16* q_raw, const gdn_bf16* k_raw, const 
     pa.dq = dq; pa.dk = dk; pa.dg = dg; pa.dbeta = dbeta;
     pa.dq_raw = dq_raw; pa.dk_raw = dk_raw; pa.da = da; pa.db = db; pa.dA_log = dA_log; pa.ddt_bias = ddt_bias;
     pa.rows = rows; pa.H = H; pa.d_k = d_k;
-    if (!launched(gdn::launch_prologue_bwd(pa, stream))) return GDN_ERR_CUDA;
+    // the row kernel, then the per-head sums when dA_log or ddt_bias is asked for
+    const int kernels = static_cast<long long>(rows) * H == 0 ? 0 : 1 + ((dA_log || ddt_bias) ? 1 : 0);
+    if (!launched(gdn::launch_prologue_bwd(pa, stream), kernels)) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

@@ -16,7 +16,10 @@
 // The fla issue #1550 "Intermediate rounding diagnosis" names the
 // intermediates (triangular inverse, causal QK score, write product w, WY
 // value tensor u) whose bf16 rounding causes most of the error of earlier
-// chunk kernels; here every intermediate stays fp32.
+// chunk kernels.  Here no computed intermediate is rounded to bf16 alone:
+// the inverse, the decays and the state are fp32, and where the tensor-core
+// kernels feed a computed quantity to an MMA it goes in as two bf16 parts
+// (hi + lo, about 16 mantissa bits) with fp32 accumulation.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -74,63 +77,6 @@ __device__ __forceinline__ bool seq_range(const int32_t* cu, int n, int N, int T
 __device__ __forceinline__ long long chunk_slot_base(const int32_t* cu, int n, int T) {
     if (cu == nullptr) return static_cast<long long>(n) * ((T + kChunk - 1) / kChunk);
     return static_cast<long long>(cu[n] / kChunk) + n;
-}
-
-// Block-cooperative small matrix product on shared-memory operands:
-//   store(i, j, sum_{kk < KD} a(i, kk) * b(kk, j))  for i < M, j < N.
-// Each thread owns a TM x TN micro-tile whose rows/columns are strided by
-// M/TM and N/TN, so neighbouring threads touch neighbouring columns.
-template <int M, int N, int KD, int TM, int TN, class FA, class FB, class FS>
-__device__ __forceinline__ void block_mm(FA a, FB b, FS store) {
-    constexpr int RI = M / TM;
-    constexpr int RJ = N / TN;
-    static_assert(M % TM == 0 && N % TN == 0, "tile");
-    for (int t = threadIdx.x; t < RI * RJ; t += blockDim.x) {
-        const int ti = t / RJ;
-        const int tj = t % RJ;
-        float acc[TM][TN];
-#pragma unroll
-        for (int r = 0; r < TM; ++r)
-#pragma unroll
-            for (int c = 0; c < TN; ++c) acc[r][c] = 0.f;
-#pragma unroll 4
-        for (int kk = 0; kk < KD; ++kk) {
-            float av[TM], bv[TN];
-#pragma unroll
-            for (int r = 0; r < TM; ++r) av[r] = a(ti + r * RI, kk);
-#pragma unroll
-            for (int c = 0; c < TN; ++c) bv[c] = b(kk, tj + c * RJ);
-#pragma unroll
-            for (int r = 0; r < TM; ++r)
-#pragma unroll
-                for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
-        }
-#pragma unroll
-        for (int r = 0; r < TM; ++r)
-#pragma unroll
-            for (int c = 0; c < TN; ++c) store(ti + r * RI, tj + c * RJ, acc[r][c]);
-    }
-}
-
-// Inclusive running sum of g over the 64 chunk positions (warp 0 only):
-// G[i] = g[0] + ... + g[i].  Also writes gam[i] = exp(G[i]).
-__device__ __forceinline__ void chunk_cumsum(const float* g, float* G, float* gam) {
-    if (threadIdx.x < 32) {
-        const int l = threadIdx.x;
-        float a = g[2 * l];
-        float b = a + g[2 * l + 1];
-        float s = b;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            float o = __shfl_up_sync(0xffffffffu, s, off);
-            if (l >= off) s += o;
-        }
-        const float base = s - b;
-        G[2 * l] = base + a;
-        G[2 * l + 1] = s;
-        gam[2 * l] = expf(base + a);
-        gam[2 * l + 1] = expf(s);
-    }
 }
 
 // T = (I + A)^-1 for a 64 x 64 strictly lower A (row stride LD), written to

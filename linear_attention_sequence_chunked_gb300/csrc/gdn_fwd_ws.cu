@@ -1176,11 +1176,32 @@ cudaError_t launch_chain(const ChainArgs& a, uint32_t wait_limit, cudaStream_t s
     return cudaGetLastError();
 }
 
+// No tokens at all (T = 0): every sequence is empty, so its final state is
+// its initial state (or zero).  One block per (head, sequence); the packed
+// offsets are still checked.
+__global__ void __launch_bounds__(256) gdn_state_passthrough_kernel(FwdArgs p) {
+    const int h = blockIdx.x, n = blockIdx.y;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+    if (p.final_state == nullptr) return;
+    const long long KV = static_cast<long long>(p.d_k) * p.d_v;
+    const long long off = (static_cast<long long>(n) * p.H + h) * KV;
+    float4* dst = reinterpret_cast<float4*>(p.final_state + off);
+    const float4* src = p.initial_state ? reinterpret_cast<const float4*>(p.initial_state + off) : nullptr;
+    for (long long i = threadIdx.x; i < KV / 4; i += blockDim.x)
+        dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
-    if (rows == 0) return launch_fwd_simt(a, stream);  // nothing to load: state pass-through only
+    if (rows == 0) {
+        // nothing to load: state pass-through only
+        if (a.N == 0 || a.H == 0) return cudaSuccess;
+        gdn_state_passthrough_kernel<<<dim3(a.H, a.N), 256, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = a.out; c.state_out = a.final_state;

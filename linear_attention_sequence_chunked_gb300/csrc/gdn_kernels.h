@@ -103,8 +103,6 @@ cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStr
 // Backward pass 3: one CTA per (chunk, head, sequence).
 cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream);
 
-cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
-
 // Chunked forward of the per-channel-gate variant (g is (.., H, d_k)), fp32 on
 // the CUDA cores; uses q, k, v, g, beta, scale, initial_state, cu_seqlens,
 // out, final_state and the sizes of FwdArgs (not chunk_states or chunk_T).

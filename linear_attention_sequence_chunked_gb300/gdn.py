@@ -249,6 +249,7 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     (B, T, H, d_k) bf16; v (B, T, H, d_v) bf16; g (B, T, H, d_k) fp32 (one log
     decay per key channel); beta (B, T, H) bf16.  Returns (out, final_state)."""
     import torch
+    _validate(q, k, v, g, beta, initial_state, cu_seqlens, per_channel_gate=True)
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
     if scale is None:
         scale = d_k ** -0.5
@@ -314,6 +315,48 @@ def _dims(q, v, cu_seqlens):
     return B, T, H, d_k, d_v
 
 
+def _validate(q, k, v, g, beta, initial_state=None, cu_seqlens=None, d_out=None,
+              d_final_state=None, per_channel_gate=False):
+    """Dtype, shape and device checks of the convenience wrappers, before any
+    library call: the kernels read each tensor with a fixed element type and
+    extent, so a mismatch would otherwise read past a buffer or give silent
+    garbage."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError(f"q must be (B, T, H, d_k), got shape {tuple(q.shape)}")
+    Bq, T, H, d_k = q.shape
+    want = [("q", q, torch.bfloat16, (Bq, T, H, d_k)),
+            ("k", k, torch.bfloat16, (Bq, T, H, d_k)),
+            ("v", v, torch.bfloat16, None),
+            ("g", g, torch.float32, (Bq, T, H, d_k) if per_channel_gate else (Bq, T, H)),
+            ("beta", beta, torch.bfloat16, (Bq, T, H))]
+    if v.dim() != 4 or tuple(v.shape[:3]) != (Bq, T, H):
+        raise ValueError(f"v must be (B, T, H, d_v) with q's (B, T, H), got {tuple(v.shape)}")
+    d_v = v.shape[3]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise ValueError(f"cu_seqlens must be int32, got {cu_seqlens.dtype}")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be a 1-D tensor of N + 1 offsets")
+        N = cu_seqlens.numel() - 1
+        want.append(("cu_seqlens", cu_seqlens, torch.int32, (N + 1,)))
+    else:
+        N = Bq
+    if initial_state is not None:
+        want.append(("initial_state", initial_state, torch.float32, (N, H, d_k, d_v)))
+    if d_out is not None:
+        want.append(("d_out", d_out, torch.bfloat16, (Bq, T, H, d_v)))
+    if d_final_state is not None:
+        want.append(("d_final_state", d_final_state, torch.float32, (N, H, d_k, d_v)))
+    for name, t, dtype, shape in want:
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}: all tensors must share one device")
+
+
 def _workspace(nbytes, device):
     import torch
     if nbytes == 0:
@@ -328,6 +371,7 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     (out, final_state, saved) with save_for_backward: gdn_chunk_fwd_save, whose
     `saved` buffer chunk_gated_delta_rule_bwd(..., saved=saved) reuses."""
     import torch
+    _validate(q, k, v, g, beta, initial_state, cu_seqlens)
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
     if scale is None:
         scale = d_k ** -0.5
@@ -352,6 +396,7 @@ def chunk_gated_delta_rule_fwd_split(q, k, v, g, beta, nseg, scale=None, initial
     """Allocate outputs and run gdn_chunk_fwd_split (dense inputs, every
     sequence as nseg segments).  Returns (out, final_state)."""
     import torch
+    _validate(q, k, v, g, beta, initial_state)
     B, T, H, d_k, d_v = _dims(q, v, None)
     if scale is None:
         scale = d_k ** -0.5
@@ -371,6 +416,9 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_out, scale=None, initial_stat
     `saved` (from chunk_gated_delta_rule_fwd(..., save_for_backward=True) on
     the same inputs) is given.  Returns a dict of tensors."""
     import torch
+    _validate(q, k, v, g, beta, initial_state, cu_seqlens, d_out=d_out, d_final_state=d_final_state)
+    if saved is not None and (saved.dtype != torch.uint8 or saved.device != q.device):
+        raise ValueError("saved must be the uint8 buffer that the saving forward returned, on q's device")
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
     if scale is None:
         scale = d_k ** -0.5
@@ -448,6 +496,7 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, cu_
     global _AUTOGRAD
     if _AUTOGRAD is None:
         _AUTOGRAD = _autograd_function()
+    _validate(q, k, v, g, beta, initial_state, cu_seqlens)
     if scale is None:
         scale = q.shape[-1] ** -0.5
     return _AUTOGRAD.apply(q, k, v, g, beta, initial_state, float(scale), cu_seqlens)

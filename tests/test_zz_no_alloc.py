@@ -14,7 +14,7 @@ import pytest
 
 from linear_attention_sequence_chunked_gb300 import gdn
 from linear_attention_sequence_chunked_gb300 import workloads as W
-from oracle import metrics
+from oracle import metrics, recurrence
 from tests import gpu_helpers as G
 
 pytestmark = pytest.mark.gpu
@@ -43,15 +43,26 @@ def _noalloc_bwd(wl):
 
 
 def test_noalloc_backward_matches_workspace_backward_twice():
+    """Same kernels on the same values as gdn_chunk_bwd with a caller
+    workspace, so every gradient must be bitwise equal, on the first call and
+    on a second one that finds the previous call's scratch contents; both
+    also within the gradient tolerance of the fp64 reverse-mode oracle."""
     wl = W.random_workload(B=2, T=200, H=2, d_k=128, d_v=128, seed=21, beta_max=2.0,
                            initial_state=True, with_grad=True, d_final_state=True)
     ref = G.run_bwd(wl)
+    units = [(s, h) for s in range(2) for h in range(2)]
+    oracle = recurrence.workload_bwd(wl, units=units)
     for call in range(2):
         res = _noalloc_bwd(wl)
         for name in ref:
-            e = metrics.rel_l2(res[name], ref[name])
             assert np.all(np.isfinite(res[name])), (call, name)
-            assert e <= G.TOL_RMS_GRAD, (call, name, e)
+            assert np.array_equal(res[name].view(np.uint32), ref[name].view(np.uint32)), (call, name)
+        for (b, t0, t1, h, s) in G.unit_rows(wl, units):
+            for name in ("dq", "dk", "dv", "dg", "dbeta"):
+                e = metrics.rel_l2(res[name][b, t0:t1, h], oracle[name][b, t0:t1, h])
+                assert e <= G.TOL_RMS_GRAD, (call, name, s, h, e)
+            e = metrics.rel_l2(res["dS0"][s, h], oracle["dS0"][s, h])
+            assert e <= G.TOL_RMS_GRAD, (call, "dS0", s, h, e)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
