@@ -427,6 +427,11 @@ def run_ours(args):
     # ---- prologue (q/k normalisation, gates) and its reverse mode at this shape ----
     prologue = None if args.no_decode else measure_prologue(gdn, torch, dev, stream, hbm, B * T, H, K)
 
+    # ---- the other synthetic workloads: throughput, and accuracy on rank 0 at N = 1 ----
+    configs = None
+    if not args.no_configs:
+        configs = measure_configs(gdn, torch, dev, stream, peaks,
+                                  accuracy=(rank == 0 and world == 1 and not args.no_cpu_baseline))
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None
     accuracy = None
@@ -479,6 +484,7 @@ def run_ours(args):
             "kda": kda,
             "decode": decode,
             "prologue": prologue,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     barrier(world)
@@ -778,6 +784,181 @@ def measure_prologue(gdn, torch, dev, stream, hbm, rows, H, K, steps=20, warmup=
     return res
 
 
+def _dev_inputs(wl, torch, dev):
+    d = dict(q=_bf16(wl.q, torch, dev), k=_bf16(wl.k, torch, dev), v=_bf16(wl.v, torch, dev),
+             g=torch.from_numpy(wl.g).to(dev), beta=_bf16(wl.beta, torch, dev))
+    d["cu"] = None if wl.cu_seqlens is None else torch.from_numpy(wl.cu_seqlens).to(dev)
+    d["dO"] = None if wl.d_out is None else _bf16(wl.d_out, torch, dev)
+    return d
+
+
+def _timed(call, torch, stream, flush, steps, warmup=3):
+    for _ in range(warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
+
+
+def measure_configs(gdn, torch, dev, stream, peaks, accuracy, steps=10):
+    """Throughput and accuracy on the other synthetic workloads, beside the
+    headline step:
+      * correlated varlen (2 x 5120 packed, H=12, d=128, bounded gates;
+        fla issue #1550's CP2 inputs): inference forward, out/state rel-RMS
+        over all 24 (sequence, head) units;
+      * slow decay (B=1, T=65536, H=16, d=128, g = -1e-3; cuLA issue #126's
+        64K heads): inference forward, per-head rel-L2 in 8 windows of 8192
+        tokens, all 16 heads;
+      * training shape (B=8, T=4096, H=16, d_k=128, d_v=256, beta in (0,2)):
+        the training step (forward keeping states + backward from them),
+        out/state/gradient rel-RMS on heads 0 and 15 of batch 0;
+      * the dense sweep's d_k = 64 rows at T=4096 ((64,64), (64,128)):
+        inference forward, out/state rel-RMS on three units.
+    Each call is timed with CUDA events after 3 warm-up calls, L2 flushed
+    before each call.  With `accuracy` (rank 0, one GPU) the fp64 oracle is
+    run on the units named above and compared with the timed call's
+    results."""
+    import numpy as np
+    from linear_attention_sequence_chunked_gb300 import workloads as W
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    res = {}
+
+    def roof(t, flops, nbytes):
+        bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
+        if bound == "hbm":
+            ach = nbytes / t / 1e9
+            return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+        ach = flops / t / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tflops, "unit": "TFLOP/s", "frac": ach / tflops}
+
+    def fwd_case(name, wl, units, windows=False):
+        d = _dev_inputs(wl, torch, dev)
+        N, T, H, K, V = wl.n_seq, wl.T, wl.H, wl.d_k, wl.d_v
+        varlen = wl.cu_seqlens is not None
+        out = torch.empty(d["v"].shape, dtype=torch.bfloat16, device=dev)
+        fs = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+        n = gdn.gdn_chunk_fwd_workspace_size(N, T, H, K, V, varlen)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        t = _timed(lambda: gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.scale, None,
+                                             d["cu"], out, fs, N, T, H, K, V, ws, n, stream),
+                   torch, stream, flush, steps)
+        st = gdn.gdn_get_last_device_error()
+        if st != 0:
+            raise SystemExit(f"device error in {name}: {gdn.gdn_status_string(st)}")
+        th = wl.token_heads
+        r = {"ms": t * 1e3, "tokens_heads_per_s": th / t,
+             "roofline": roof(t, fwd_flops(K, V) * th, fwd_bytes(K, V) * th + 4 * K * V * N * H)}
+        if accuracy:
+            from oracle import metrics, recurrence
+            o_ref, S_ref = recurrence.workload_fwd(wl, units=units)
+            o = bf16_np(out)
+            S = fs.cpu().numpy()
+            per = []
+            for (s_, h_) in units:
+                b_, t0, t1 = wl.seq_bounds()[s_]
+                e = {"unit": [s_, h_], "out_rel_rms": metrics.rel_l2(o[b_, t0:t1, h_], o_ref[b_, t0:t1, h_]),
+                     "state_rel_rms": metrics.rel_l2(S[s_, h_], S_ref[s_, h_])}
+                if windows:
+                    e["window_rel_l2"] = metrics.window_rel_l2(o[b_, t0:t1, h_], o_ref[b_, t0:t1, h_], axis=0)
+                per.append(e)
+            acc = {"units": len(units),
+                   "out_rel_rms_max": max(e["out_rel_rms"] for e in per),
+                   "state_rel_rms_max": max(e["state_rel_rms"] for e in per)}
+            if not windows:
+                sel = [(wl.seq_bounds()[s_], h_) for (s_, h_) in units]
+                acc["out_rel_rms_all"] = metrics.rel_l2(
+                    np.concatenate([o[b_, t0:t1, h_].ravel() for (b_, t0, t1), h_ in sel]),
+                    np.concatenate([o_ref[b_, t0:t1, h_].ravel() for (b_, t0, t1), h_ in sel]))
+            else:
+                acc["window_rel_l2_max"] = max(max(e["window_rel_l2"]) for e in per)
+                acc["window_rel_l2_per_head"] = [[round(x, 7) for x in e["window_rel_l2"]] for e in per]
+            r["accuracy"] = acc
+        return r
+
+    wl3 = W.make_workload(3)
+    res["correlated_varlen"] = fwd_case("correlated varlen", wl3,
+                                        [(s_, h_) for s_ in range(wl3.n_seq) for h_ in range(wl3.H)])
+    res["correlated_varlen"]["config"] = "2 x 5120 packed, H=12, d_k=d_v=128, correlated q/k, g = -5 sigmoid(N)"
+    if accuracy:
+        res["correlated_varlen"]["accuracy"]["pages_context"] = (
+            "fla ordinary chunk kernel 1.3509 % rel-RMS on its CP2 inputs (fla issue #1550); threshold 0.008")
+    del wl3
+    wl4 = W.make_workload(4)
+    res["slow_decay"] = fwd_case("slow decay", wl4, [(0, h_) for h_ in range(wl4.H)], windows=True)
+    res["slow_decay"]["config"] = "B=1 T=65536 H=16 d_k=d_v=128, g = -1e-3, 8 windows of 8192 tokens"
+    if accuracy:
+        res["slow_decay"]["accuracy"]["pages_context"] = (
+            "cuLA intracard split on H200: windows 1-7 at about 7.3e-3 rel-L2 (cuLA issue #126)")
+    del wl4
+    for (dk, dv) in ((64, 64), (64, 128)):
+        wl2 = W.make_workload(2, d_k=dk, d_v=dv)
+        key = f"dense_dk{dk}_dv{dv}"
+        res[key] = fwd_case(key, wl2, [(0, 0), (1, 7), (3, 15)])
+        res[key]["config"] = f"B=4 T=4096 H=16 d_k={dk} d_v={dv}"
+        del wl2
+
+    # training shape: the training step
+    wl5 = W.make_workload(5, with_grad=True)
+    d = _dev_inputs(wl5, torch, dev)
+    B, T, H, K, V = wl5.B, wl5.T, wl5.H, wl5.d_k, wl5.d_v
+    out = torch.empty(d["v"].shape, dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((B, H, K, V), dtype=torch.float32, device=dev)
+    grads = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]), dv=torch.empty_like(d["v"]),
+                 dg=torch.empty_like(d["g"]), dbeta=torch.empty_like(d["beta"]),
+                 dS0=torch.empty((B, H, K, V), dtype=torch.float32, device=dev))
+    nf = gdn.gdn_chunk_saved_size(B, T, H, K, V, 0)
+    nb = gdn.gdn_chunk_bwd_saved_workspace_size(B, T, H, K, V, 0)
+    ws_f = torch.empty(nf, dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        gdn.gdn_chunk_fwd_save(d["q"], d["k"], d["v"], d["g"], d["beta"], wl5.scale, None, None, out, fs,
+                               B, T, H, K, V, ws_f, nf, stream)
+
+    def bwd():
+        gdn.gdn_chunk_bwd_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], wl5.scale, None, d["dO"], None,
+                                grads["dq"], grads["dk"], grads["dv"], grads["dg"], grads["dbeta"],
+                                grads["dS0"], B, T, H, K, V, ws_f, nf, ws_b, nb, stream)
+    t_f = _timed(fwd, torch, stream, flush, steps)
+    t_b = _timed(lambda: (fwd(), bwd()), torch, stream, flush, steps) - t_f
+    st = gdn.gdn_get_last_device_error()
+    if st != 0:
+        raise SystemExit(f"device error in the training shape: {gdn.gdn_status_string(st)}")
+    th = wl5.token_heads
+    r = {"config": "B=8 T=4096 H=16 d_k=128 d_v=256, beta in (0,2): forward keeping states + backward",
+         "step_ms": (t_f + t_b) * 1e3, "tokens_heads_per_s": th / (t_f + t_b),
+         "fwd_ms": t_f * 1e3, "bwd_ms": t_b * 1e3,
+         "roofline_fwd": roof(t_f, fwd_flops(K, V) * th, fwd_bytes(K, V) * th + 4 * K * V * B * H),
+         "roofline_bwd": roof(t_b, bwd_flops(K, V) * th, bwd_bytes(K, V) * th)}
+    if accuracy:
+        from oracle import metrics, recurrence
+        units = [(0, 0), (0, 15)]
+        o_ref, S_ref = recurrence.workload_fwd(wl5, units=units)
+        g_ref = recurrence.workload_bwd(wl5, units=units)
+        o = bf16_np(out)
+        S = fs.cpu().numpy()
+        gg = {n_: (bf16_np(x) if x.dtype == torch.bfloat16 else x.cpu().numpy()) for n_, x in grads.items()}
+        acc = {"units": units}
+        for (s_, h_) in units:
+            e = {"out": metrics.rel_l2(o[s_, :, h_], o_ref[s_, :, h_]),
+                 "state": metrics.rel_l2(S[s_, h_], S_ref[s_, h_])}
+            for n_ in ("dq", "dk", "dv", "dg", "dbeta"):
+                e[n_] = metrics.rel_l2(gg[n_][s_, :, h_], g_ref[n_][s_, :, h_])
+            e["dS0"] = metrics.rel_l2(gg["dS0"][s_, h_], g_ref["dS0"][s_, h_])
+            acc[f"rel_rms_b{s_}_h{h_}"] = e
+        r["accuracy"] = acc
+    res["training_shape"] = r
+    return res
+
+
 def measure_e2e(args, wl, dev, stream, gdn, torch, fs, dS0, ws_f, ws_f_n, ws_b, ws_b_n):
     """The step through the public API with host buffers: every step copies
     its inputs in from pinned host memory and its outputs and gradients back,
@@ -897,6 +1078,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-probes", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1202,6 +1202,7 @@ cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t st
         gdn_state_passthrough_kernel<<<dim3(a.H, a.N), 256, 0, stream>>>(a);
         return cudaGetLastError();
     }
+    if (a.d_k == kDk && a.chunk_T != nullptr) return launch_fwd_chain(a, wait_limit, stream);
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = a.out; c.state_out = a.final_state;
