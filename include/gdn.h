@@ -105,9 +105,11 @@ GDN_API size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_
  *                 gdn_chunk_fwd_workspace_size() bytes, every chunk's T is
  *                 formed first by a chunk-parallel kernel and the chunk chain
  *                 reads it (the faster route); with NULL or fewer bytes the
- *                 chunk chain forms T itself.  Both routes give the same
- *                 arithmetic.  A non-NULL workspace that is not 256-byte
- *                 aligned returns GDN_ERR_MISALIGNED.
+ *                 chunk chain forms T itself.  At d_k = 64 both routes give
+ *                 the same bits; at d_k = 128 the workspace route forms the
+ *                 output's causal term as (P T) R instead of P (T R), so the
+ *                 two agree to rounding.  A non-NULL workspace that is not
+ *                 256-byte aligned returns GDN_ERR_MISALIGNED.
  * Returns GDN_OK once the work is enqueued on `stream`.
  */
 GDN_API gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
@@ -379,6 +381,30 @@ GDN_API gdn_status gdn_probe_copy(const void* src, void* dst, size_t bytes, cuda
  */
 GDN_API gdn_status gdn_probe_gemm_bf16(const gdn_bf16* A, const gdn_bf16* B, gdn_bf16* C, int M, int N, int K,
                                        cudaStream_t stream);
+
+/*
+ * gdn_chunk_fwd with a caller-chosen bound on the kernels' hand-off waits
+ * (mbarrier waits between the warps of a CTA), for exercising failure
+ * detection.  wait_limit counts polls (0 = the default; each poll may
+ * suspend the thread until the awaited phase completes, so a small bound
+ * alone rarely runs out).  With stall_first_wait != 0 the issuing warp of
+ * every CTA first waits on a hand-off that nothing signals, so that wait
+ * runs out: the CTA records GDN_ERR_TIMEOUT in the device error word (read
+ * it with gdn_get_last_device_error), waits with the default bound for every
+ * copy and tensor-core product it started, and leaves without writing its
+ * final state, so the context stays usable.  Library bookkeeping with no
+ * counterpart on the pages.  Takes a workspace of at least
+ * gdn_chunk_fwd_workspace_size() bytes and d_k = 128 (the kernels whose drain
+ * waits keep their own bound); otherwise GDN_ERR_UNSUPPORTED.  Other
+ * arguments and errors as gdn_chunk_fwd.
+ */
+GDN_API gdn_status gdn_chunk_fwd_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                    const float* g, const gdn_bf16* beta, float scale,
+                                    const float* initial_state, const int32_t* cu_seqlens,
+                                    gdn_bf16* out, float* final_state,
+                                    int B, int T, int H, int d_k, int d_v,
+                                    void* workspace, size_t workspace_bytes, uint32_t wait_limit,
+                                    int stall_first_wait, cudaStream_t stream);
 
 /*
  * Number of CUDA kernels this library has launched in this process so far

@@ -267,12 +267,14 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int v
     return bwd_layout(B, T, H, d_k, d_v, varlen).total;
 }
 
-gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
-                         const float* g, const gdn_bf16* beta, float scale,
-                         const float* initial_state, const int32_t* cu_seqlens,
-                         gdn_bf16* out, float* final_state,
-                         int B, int T, int H, int d_k, int d_v,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+gdn_status chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                     const gdn_bf16* beta, float scale, const float* initial_state, const int32_t* cu_seqlens,
+                     gdn_bf16* out, float* final_state, int B, int T, int H, int d_k, int d_v, void* workspace,
+                     size_t workspace_bytes, uint32_t wait_limit, int stall, cudaStream_t stream) {
     gdn_status st = check_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return GDN_ERR_MISALIGNED;
@@ -288,9 +290,41 @@ gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens;
     a.out = out; a.final_state = final_state; a.chunk_states = nullptr; a.chunk_T = tiles;
-    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
-    if (!launched(gdn::launch_fwd_ws(a, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err; a.stall = stall;
+    if (!launched(gdn::launch_fwd_ws(a, wait_limit, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                         const float* g, const gdn_bf16* beta, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         gdn_bf16* out, float* final_state,
+                         int B, int T, int H, int d_k, int d_v,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v,
+                     workspace, workspace_bytes, gdn::kDefaultWaitLimit, 0, stream);
+}
+
+gdn_status gdn_chunk_fwd_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                    const float* g, const gdn_bf16* beta, float scale,
+                                    const float* initial_state, const int32_t* cu_seqlens,
+                                    gdn_bf16* out, float* final_state,
+                                    int B, int T, int H, int d_k, int d_v,
+                                    void* workspace, size_t workspace_bytes, uint32_t wait_limit,
+                                    int stall_first_wait, cudaStream_t stream) {
+    // only the stacked-product chain (d_k = 128, T tiles given) drains with
+    // its own bound; the other kernels keep the default hand-off bound
+    if (d_k != 128) return GDN_ERR_UNSUPPORTED;
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return check_shapes(B, T, H, d_k, d_v);
+    const size_t tb = tiles_bytes(B, T, H, cu_seqlens != nullptr);
+    if (tb > 0 && (!workspace || workspace_bytes < tb)) return GDN_ERR_UNSUPPORTED;
+    return chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v,
+                     workspace, workspace_bytes, wait_limit ? wait_limit : gdn::kDefaultWaitLimit,
+                     stall_first_wait != 0, stream);
 }
 
 gdn_status gdn_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,

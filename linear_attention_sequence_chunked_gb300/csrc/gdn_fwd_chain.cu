@@ -1,16 +1,14 @@
 // Chunked gated delta rule forward, d_k = 128, with the T tiles of every
-// chunk given (chunk-parallel inverse): the tensor-core chunk chain with
-// stacked M = 128 products.
+// chunk given (chunk-parallel inverse): the tensor-core chunk chain.
 //
-// Per chunk (C = 64 tokens, S0 the chunk's start state, one 64-column value
-// slice of it per CTA) the chain needs
+// Per chunk (C = 64 tokens, S0 the chunk's start state) the chain needs
 //     R     = beta o (V - gam o (K S0))
 //     Delta = T R                          (= u - w S0 of the WY form)
 //     S1    = gam_n S0 + K^T (dec o Delta)
 //     O     = scale [gam o (Q S0) + P Delta],   P = (Q K^T) o M (causal decay)
 // and only the first three are on the serial path.  Two stacked products
-// carry the output along with them at no extra tensor-pipe time (an M = 128
-// product costs what an M = 64 one does):
+// carry the output along at no extra tensor-pipe time (an M = 128 product
+// costs what an M = 64 one does):
 //     [K; Q] S0      -> rows 0-63: K S0,   rows 64-127: Q S0
 //     [T; P T] R     -> rows 0-63: Delta,  rows 64-127: P T R = P Delta
 // P T is formed one chunk ahead by the prep warps (as T^T P^T, so that its
@@ -20,28 +18,44 @@
 // epilogues while those of subpartitions 2-3 ("Q warps") form the output
 // beside them; all eight update the state.
 //
+// The value columns of the state evolve independently ("Research Sprint
+// Day 1", the GDN update: column j of S only ever meets v_j), so each CTA's
+// 64-column slice runs as two independent sub-chains of 32 columns, A and B,
+// half a chunk apart.  Every product of one sub-chain is issued while the
+// other sub-chain's warps run an epilogue, so the tensor pipe's latency is
+// hidden behind CUDA-core work instead of stalling the chain.  Per chunk c the
+// epilogue warps run, in order,
+//     (a) R of A            (b) S update of B (chunk c - 1)
+//     (c) dec o Delta of A, output of A
+//     (d) R of B            (e) S update of A
+//     (f) dec o Delta of B, output of B
+// and a dedicated issuer warp issues each phase's product as soon as that
+// phase's operand tiles are stored.  Split operands x = hi + lo sit side by
+// side in one 64-column tile ([x_hi | x_lo], 32 columns each), so one N = 64
+// product A [x_hi | x_lo] gives both halves and the epilogue adds them.
+//
 // Warps:
-//   0-7   chain: K warps 0, 1, 4, 5 (R, then dec o Delta), Q warps 2, 3, 6, 7
-//         (output); all: S <- gam_n S + acc.  S (fp32) lives in registers,
-//         thread (subpartition sp, half hs, lane l) holding row 32 sp + l,
-//         columns 32 hs .. 32 hs + 31 of the slice.  Warp 0 issues the three
-//         chain products.
-//   8-11  prep, one chunk ahead: gates (g cumsum, gam, dec), Q K^T on the
-//         tensor cores, P = (Q K^T) o M as bf16 hi/lo tiles, the chunk's T
-//         tiles copied in from the workspace, T^T P^T on the tensor cores into
-//         the P T operand tiles.
+//   0-7   epilogues.  K warps 0, 1, 4, 5; Q warps 2, 3, 6, 7.  Thread
+//         (subpartition sp, half hs, lane l) takes token row 32 (sp & 1) + l of
+//         the chunk, state row 32 sp + l, and columns 16 hs .. 16 hs + 15 of
+//         each sub-chain.  The fp32 state lives in their registers.
+//   8-11  prep, one chunk ahead: gates (g cumsum, gam, dec), Q K^T, P as bf16
+//         hi/lo tiles, the chunk's T tiles copied in, T^T P^T into the P T
+//         operand tiles.
+//   12    issues the chain's products and the K/Q tile loads.
 //
-// Precision: computed operands (S, R, dec o Delta, T, P, P T) enter the
-// MMAs as bf16 hi + lo pairs (hi*hi + hi*lo + lo*hi, or hi + lo against an
-// exact bf16 input), accumulation is fp32 in TMEM, the state is fp32 in
-// registers: fla issue #1550 ("Intermediate rounding diagnosis") traces the
-// error of bf16 chunk kernels to rounding the inverse, the score and u.
+// Precision: computed operands (S, R, dec o Delta, T, P, P T) enter the MMAs
+// as bf16 hi + lo pairs, accumulation is fp32 in TMEM, the state is fp32 in
+// registers (fla issue #1550, "Intermediate rounding diagnosis", traces the
+// error of bf16 chunk kernels to rounding the inverse, the score and u).
 //
-// Hand-offs are mbarriers with bounded waits; a wait that runs out sets the
-// CTA's abort flag, and every group decides to leave at a barrier that
-// reduces the flag over the whole group, so no thread is left waiting at a
-// named barrier.  Before the CTA frees its TMEM every issued MMA, TMA load
-// and bulk copy is waited for with the default (long) bound.
+// Hand-offs are mbarriers with bounded waits and named barriers between the
+// epilogue warps and the issuer.  A wait that runs out marks the CTA bad; the
+// decision to leave is taken at the two per-chunk barriers every epilogue
+// thread and the issuer pass (an OR-reduction over all of them), so no
+// thread is left waiting at a named barrier.  Before the CTA frees its TMEM,
+// every issued MMA, TMA load and bulk copy is waited for with the default
+// (long) bound.
 #include <cuda.h>
 #include <string.h>
 
@@ -59,51 +73,35 @@ using namespace tc;
 
 constexpr int kChainThreads = 256;  // warps 0-7
 constexpr int kPrepThreads = 128;   // warps 8-11
-constexpr int kThreads = kChainThreads + kPrepThreads;
+constexpr int kIssuerWarp = 12;
+constexpr int kThreads = kChainThreads + kPrepThreads + 32;
 constexpr int kVs = 64;
-constexpr int kStages = 3;     // K/Q stages: chunk c + 3 loads while chunk c finishes
+constexpr int kStages = 3;          // K/Q stages: chunk c + 3 loads while chunk c finishes
 constexpr uint32_t kTmemCols = 512;
 
-#ifndef GDN_FWD_NSTACK
-#define GDN_FWD_NSTACK 1
-#endif
-#ifndef GDN_FWD_GATE
-#define GDN_FWD_GATE 0
-#endif
-// The chain's products against a split operand x = hi + lo run as one
-// N = 128 product A [x_hi | x_lo] (the two parts side by side, 128 TMEM
-// columns) instead of two N = 64 ones: half the MMA instructions, and A is
-// read from shared memory once.  The epilogue adds the two halves.
-constexpr bool kNStack = GDN_FWD_NSTACK != 0;
-// The prep issues its products in the chain's epilogue windows: Q K^T of
-// chunk c once [K; Q] S0 of chunk c - 1 has completed, T^T P^T of chunk c
-// once [T; P T] R of chunk c - 1 has.
-constexpr bool kGate = GDN_FWD_GATE != 0;
-constexpr uint32_t kAccCols = kNStack ? 128 : 64;
-constexpr uint32_t kColKQ = 0;                   // [K; Q] S0            (M = 128)
-constexpr uint32_t kColD = kAccCols;             // [T; P T] R           (M = 128)
-constexpr uint32_t kColS = 2 * kAccCols;         // K^T (dec o Delta)    (M = 128, rows = key index)
-constexpr uint32_t kColQK = 3 * kAccCols;        // prep: Q K^T          (M = 64)
-constexpr uint32_t kColPT = 3 * kAccCols + 64;   // prep: T^T P^T        (M = 64)
-static_assert(kColPT + 64 <= kTmemCols, "tensor memory");
+// TMEM column blocks (M = 128 unless noted; X = sub-chain A or B)
+constexpr uint32_t kColKQ = 0;      // [K; Q] [S_hi | S_lo] of X at 64 X
+constexpr uint32_t kColD = 128;     // [T; P T] [R_hi | R_lo] of X at 128 + 64 X
+constexpr uint32_t kColS = 256;     // K^T [dX_hi | dX_lo] of X at 256 + 64 X
+constexpr uint32_t kColQK = 384;    // prep: Q K^T (M = 64)
+constexpr uint32_t kColPT = 448;    // prep: T^T P^T (M = 64)
 
 constexpr int kStageBytes = 2 * kRegionBytes;  // two 64-column key regions of [K rows; Q rows]
-constexpr int kTileS = kDk * 128;
+constexpr int kTileSX = kDk * 128;             // a sub-chain's state tile: 128 key rows x [hi 32 | lo 32]
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int oStage = 0;
-constexpr int oShi = oStage + kStages * kStageBytes;
-constexpr int oSlo = oShi + kTileS;
-constexpr int oRhi = oSlo + kTileS;       // R, then dec o Delta (hi)
-constexpr int oRlo = oRhi + kTile64;
-constexpr int oT = oRlo + kTile64;        // T^T [slot][hi, lo]
-constexpr int oPT = oT + 4 * kTile64;     // (P T)^T [slot][hi, lo]; P itself before T^T P^T has read it
+constexpr int oS = oStage + kStages * kStageBytes;  // state tiles of A, B
+constexpr int oR = oS + 2 * kTileSX;                // R, then dec o Delta, of A, B: 64 token rows x [hi | lo]
+constexpr int oT = oR + 2 * kTile64;                // T^T [slot][hi, lo]
+constexpr int oPT = oT + 4 * kTile64;               // (P T)^T [slot][hi, lo]; P itself before T^T P^T has read it
+constexpr int oO = oPT + 4 * kTile64;               // output staging: 64 token rows x 64 columns bf16
 constexpr int kVecSlots = 3;
-constexpr int oVec = oPT + 4 * kTile64;   // [chunk % 3][g, beta, G, gam, dec] x 64 fp32
+constexpr int oVec = oO + kTile64;                  // [chunk % 3][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + kVecSlots * kVecFloats * 4;
-constexpr int kBars = 16;
-constexpr int oMisc = oBar + kBars * 8;   // TMEM slot, abort flag, chain progress
+constexpr int kBars = 20;
+constexpr int oMisc = oBar + kBars * 8;             // TMEM slot
 constexpr int kBytes = oMisc + 16;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 232448, "shared memory");
@@ -112,11 +110,21 @@ static_assert(kAlloc <= 232448, "shared memory");
 constexpr uint32_t kLboTPT = oPT - oT;
 
 enum {
-    B_FULL0 = 0, B_FULL1 = 1, B_FULL2 = 2, B_KQ = 3, B_D = 4, B_S = 5, B_GRAM = 6, B_PT = 7,
-    B_READY0 = 8, B_READY1 = 9, B_TFREE0 = 10, B_TFREE1 = 11, B_TCOPY = 12,
-    B_DRAIN0 = 13, B_DRAIN1 = 14
+    B_FULL0 = 0, B_KQ0 = 3, B_D0 = 5, B_S0 = 7,   // FULL: 3 stages; KQ, D, S: one per sub-chain
+    B_GRAM = 9, B_PT = 10, B_READY0 = 11, B_TFREE0 = 13, B_TCOPY = 15,
+    B_DRAIN0 = 16, B_DRAIN1 = 17, B_STALL = 18     // B_STALL: never signalled (failure-detection test)
 };
 static_assert(B_DRAIN1 < kBars, "barriers");
+
+// named barriers
+constexpr int NB_CHAIN = 1;                         // epilogue warps (256)
+constexpr int NB_PREP = 2;                          // prep warps (128)
+constexpr int NB_C2 = 3;                            // + X: R of X stored (K warps + issuer, 160)
+constexpr int NB_C4 = 5;                            // + X: dec o Delta of X stored (K warps + issuer, 160)
+constexpr int NB_C6 = 7;                            // + X: state tile of X stored (epilogue warps + issuer, 288)
+constexpr int NB_OUT = 9;                           // Q warps (128)
+constexpr int kKIss = 128 + 32;
+constexpr int kAllIss = kChainThreads + 32;
 
 // bar.sync with an OR-reduction of `pred` over the `count` participating
 // threads: every participant gets the same answer
@@ -130,10 +138,17 @@ __device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
     return r != 0;
 }
 
-// 32 consecutive TMEM columns of this thread's lane (row), no wait
-__device__ __forceinline__ void ld32_nowait(uint32_t taddr, float* v) {
-    tmem_ld16(taddr, v);
-    tmem_ld16(taddr + 16, v + 16);
+// 8 values as bf16 hi and lo parts (x = hi + lo to ~16 bits)
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = x[2 * e], b = x[2 * e + 1];
+        h[e] = cvt_bf16x2(a, b);
+        l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 struct ChainFwdParams {
@@ -148,7 +163,7 @@ constexpr uint32_t kDrainLimit = 4000000u;
 
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_fwd_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
-                         const ChainFwdParams prm) {
+                         const __grid_constant__ CUtensorMap tmap_o, const ChainFwdParams prm) {
     const FwdArgs& p = prm.a;
     const int vs = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int H = p.H, V = p.d_v;
@@ -162,9 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + oMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oMisc + 4);
-    // chain progress for the prep's product scheduling: 2 ci + 1 once [K; Q]
-    // S0 of chunk ci has completed, 2 ci + 2 once [T; P T] R has
-    volatile int* progress = reinterpret_cast<volatile int*>(sm + oMisc + 8);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const long long row_base = static_cast<long long>(b) * p.T;
@@ -181,317 +193,381 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBars; ++i) mbar_init(bar(i), 1);
         fence_mbar_init();
         *abort_flag = 0;
-        *progress = 0;
-        if (nchunks > 0) {
-            tma_prefetch_desc(&tmap_k);
-            tma_prefetch_desc(&tmap_q);
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    auto issue_tma = [&](int ci) {
-        const int st = ci % kStages;
-        uint8_t* base = sm + oStage + st * kStageBytes;
-        const int z = static_cast<int>(row_base + t0 + ci * kChunk);
-        mbar_arrive_expect_tx(bar(B_FULL0 + st), kStageBytes);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            tma_load_3d(smem_u32(base + r * kRegionBytes), &tmap_k, r * 64, h, z, bar(B_FULL0 + st));
-            tma_load_3d(smem_u32(base + r * kRegionBytes + 64 * 128), &tmap_q, r * 64, h, z, bar(B_FULL0 + st));
-        }
-    };
-
     if (warp < 8) {
-        // ============================ chain warps ============================
+        // ============================ epilogue warps ============================
         const int t = tid;
         const int sp = warp & 3, hs = warp >> 2;
         const bool kw = sp < 2;                 // K warp (rows 0-63 of the stacked products)
         const int srow = 32 * sp + lane;        // state row (key index)
-        const int i = 32 * (sp & 1) + lane;     // token row of the chunk (K and Q warps alike)
+        const int i = 32 * (sp & 1) + lane;     // token row of the chunk
         const uint32_t lb = static_cast<uint32_t>(sp * 32) << 16;
-        const uint32_t cq = 32 * hs;            // first column of this thread's half
-        // this thread's 32 values of an M = 128 accumulator at column block col
-        // (with the N-stacked split, the hi and lo products' halves added)
-        auto ld_acc = [&](uint32_t col, float* x) {
-            ld32_nowait(tmem + lb + col + cq, x);
-            if (kNStack) {
-                float y[32];
-                ld32_nowait(tmem + lb + col + 64 + cq, y);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] += y[c];
-            } else {
-                tmem_ld_wait();
-            }
-        };
+        const int c0 = 16 * hs;                 // this thread's first column within a sub-chain
         const long long KV = static_cast<long long>(kDk) * V;
         const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kVs;
         const float scale = p.scale;
-        uint8_t* Shi = sm + oShi;
-        uint8_t* Slo = sm + oSlo;
-        uint8_t* Rhi = sm + oRhi;
-        uint8_t* Rlo = sm + oRlo;
-        int tma_issued = 0, tma_done = 0;  // thread 0's count of stage loads issued / consumed
-        if (t == 0) {
-            for (int c = 0; c < kStages && c < nchunks; ++c) issue_tma(c);
-            tma_issued = min(kStages, nchunks);
-        }
+        const long long nsl = V / kVs;
 
-        float S[32];
+        // this thread's 16 values of sub-chain X's accumulator at `col` (the
+        // hi and lo products' halves added)
+        auto ld_acc = [&](uint32_t col, float* x) {
+            float y[16];
+            tmem_ld16(tmem + lb + col + c0, x);
+            tmem_ld16(tmem + lb + col + 32 + c0, y);
+            tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = 0.f;
-        if (p.initial_state) {
-            const float* src = p.initial_state + state_off + static_cast<long long>(srow) * V + cq;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 t4 = *reinterpret_cast<const float4*>(src + j);
-                S[j] = t4.x; S[j + 1] = t4.y; S[j + 2] = t4.z; S[j + 3] = t4.w;
-            }
-        }
-        store_split_half(Shi, Slo, srow, hs, S);
-        fence_proxy_async_smem();
-        named_bar(1, kChainThreads);
-
-        auto store_state_tiles = [&](int ci) {
-            const long long nsl = V / kVs;
-            uint8_t* dst = reinterpret_cast<uint8_t*>(p.chunk_states) +
-                           (((slot0 + ci) * H + h) * nsl + vs) * (2LL * kDk * 128);
-            bulk_s2g(dst, smem_u32(Shi), kDk * 128);
-            bulk_s2g(dst + kDk * 128, smem_u32(Slo), kDk * 128);
-            bulk_commit();
+            for (int c = 0; c < 16; ++c) x[c] += y[c];
         };
-        // K warps: this row's 32 values of the slice, packed bf16, one chunk ahead
-        uint4 vraw[4];
+        // 16 values into row `row` of a [hi 32 | lo 32] sub-chain tile
+        auto store_sub = [&](uint8_t* tile, int row, const float* x) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                uint4 hi, lo;
+                split8(x + 8 * e, hi, lo);
+                *reinterpret_cast<uint4*>(tile + sw128_offset(row, (2 * hs + e) * 16)) = hi;
+                *reinterpret_cast<uint4*>(tile + sw128_offset(row, (4 + 2 * hs + e) * 16)) = lo;
+            }
+        };
+        // the training route keeps every chunk's start state as bf16 hi/lo
+        // operand tiles in the layout the backward reads: [slot][head][value
+        // slice][hi, lo] of 128 key rows x 128 bytes (64 columns, 128-byte
+        // swizzle); this thread writes its 16 columns of sub-chain X
+        auto save_state = [&](int cj, int X, const float* x) {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(p.chunk_states) +
+                           (((slot0 + cj) * H + h) * nsl + vs) * (2LL * kDk * 128);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                uint4 hi, lo;
+                split8(x + 8 * e, hi, lo);
+                const uint32_t off = sw128_offset(srow, (4 * X + 2 * hs + e) * 16);
+                *reinterpret_cast<uint4*>(dst + off) = hi;
+                *reinterpret_cast<uint4*>(dst + kDk * 128 + off) = lo;
+            }
+        };
+
+        // the state: sub-chain A's 16 columns, then B's
+        float S[2][16];
+#pragma unroll
+        for (int X = 0; X < 2; ++X) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) S[X][j] = 0.f;
+            if (p.initial_state) {
+                const float* src = p.initial_state + state_off + static_cast<long long>(srow) * V + 32 * X + c0;
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(src + j);
+                    S[X][j] = t4.x; S[X][j + 1] = t4.y; S[X][j + 2] = t4.z; S[X][j + 3] = t4.w;
+                }
+            }
+            store_sub(sm + oS + X * kTileSX, srow, S[X]);
+            if (p.chunk_states && nchunks > 0) save_state(0, X, S[X]);
+        }
+        fence_proxy_async_smem();
+        // the issuer takes the initial state tiles from here
+        bool aborted = bar_or(NB_C6, kAllIss, false);
+
+        // K warps: the row's 16 values of each sub-chain, packed bf16, one chunk ahead
+        uint4 vraw[2][2];
         auto load_v = [&](int cj) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) vraw[e] = make_uint4(0, 0, 0, 0);
+            for (int X = 0; X < 2; ++X) vraw[X][0] = vraw[X][1] = make_uint4(0, 0, 0, 0);
             if (!kw || cj >= nchunks) return;
             const int cc0 = t0 + cj * kChunk;
             if (i < min(kChunk, t1 - cc0)) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.v + ((row_base + cc0 + i) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
+                const uint16_t* row = p.v + ((row_base + cc0 + i) * H + h) * static_cast<long long>(V) + vs * kVs;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) vraw[e] = src[e];
+                for (int X = 0; X < 2; ++X) {
+                    const uint4* src = reinterpret_cast<const uint4*>(row + 32 * X + c0);
+                    vraw[X][0] = src[0];
+                    vraw[X][1] = src[1];
+                }
             }
         };
-        // warp 0: [K; Q] S0 of chunk cj once its stage is full
-        auto issue_kq = [&](int cj) -> bool {
-            const bool full =
-                __all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + cj % kStages), (cj / kStages) & 1, wl));
-            if (full) {
-                if (elect_one()) {
-                    tc_fence_after();
-                    const uint32_t stage_c = smem_u32(sm + oStage + (cj % kStages) * kStageBytes);
-                    constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 128, kAccCols);
+        load_v(0);
+
+        float qs[16];
+        // (a), (d): R of sub-chain X (K warps) / gam o (Q S0) of X (Q warps)
+        auto phase_r = [&](int X, const float* bv, const float* gam) {
+            if (kw) {
+                float x[16];
+                ld_acc(kColKQ + 64 * X, x);
+                const float bj = bv[i], gj = gam[i];
 #pragma unroll
-                    for (int s = 0; s < kDk / 16; ++s) {
-                        const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
-                        const uint64_t a = desc_sw128(stage_c + koff, 0, 1024);
-                        // N = 128: [S_hi | S_lo], the lo tile kTileS after the hi tile
-                        mma_bf16(tmem + kColKQ, a, desc_sw128(smem_u32(Shi) + s * 2048, kTileS, 1024), id, s > 0);
-                        if (!kNStack)
-                            mma_bf16(tmem + kColKQ, a, desc_sw128(smem_u32(Slo) + s * 2048, kTileS, 1024), id, 1);
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t w4[4] = {vraw[X][e].x, vraw[X][e].y, vraw[X][e].z, vraw[X][e].w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int c = 8 * e + 2 * m;
+                        x[c] = bj * (__uint_as_float(w4[m] << 16) - gj * x[c]);
+                        x[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * x[c + 1]);
                     }
-                    mma_commit(bar(B_KQ));
                 }
-                __syncwarp();
+                store_sub(sm + oR + X * kTile64, i, x);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_arrive(NB_C2 + X, kKIss);
+            } else {
+                ld_acc(kColKQ + 64 * X, qs);
+                const float gi = gam[i];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) qs[c] *= gi;
             }
-            return full;
+        };
+        // (c), (f): dec o Delta of X (K warps) / output of X (Q warps)
+        auto phase_d = [&](int X, const float* dec, int c0tok, int nv) {
+            if (kw) {
+                float x[16];
+                ld_acc(kColD + 64 * X, x);
+                const float dj = dec[i];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) x[c] *= dj;
+                store_sub(sm + oR + X * kTile64, i, x);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_arrive(NB_C4 + X, kKIss);
+            } else {
+                float pd[16];
+                ld_acc(kColD + 64 * X, pd);
+                if (want_out) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        w[m] = cvt_bf16x2(scale * (qs[2 * m] + pd[2 * m]), scale * (qs[2 * m + 1] + pd[2 * m + 1]));
+                    if (nv == kChunk) {
+                        // full chunk: into the staging tile, stored by TMA after B
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            *reinterpret_cast<uint4*>(sm + oO + sw128_offset(i, (4 * X + 2 * hs + e) * 16)) =
+                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    } else if (i < nv) {
+                        // ragged chunk: the rows past its end belong to the next sequence
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            p.out + ((row_base + c0tok + i) * H + h) * static_cast<long long>(V) + vs * kVs + 32 * X + c0);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+            }
+        };
+        // (b), (e): S <- gam_n S + K^T (dec o Delta) for sub-chain X, chunk cj
+        auto phase_s = [&](int X, int cj, float gC, bool bad) -> bool {
+            bad = !mbar_wait(bar(B_S0 + X), cj & 1, wl) || bad;
+            tc_fence_after();
+            float x[16];
+            ld_acc(kColS + 64 * X, x);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) S[X][c] = fmaf(gC, S[X][c], x[c]);
+            store_sub(sm + oS + X * kTileSX, srow, S[X]);
+            if (p.chunk_states && cj + 1 < nchunks) save_state(cj + 1, X, S[X]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            return bar_or(NB_C6 + X, kAllIss, bad || *abort_flag);
         };
 
-        load_v(0);
-        bool aborted = false;
-        if (nchunks > 0) {
-            bool ok = true;
-            if (warp == 0) {
-                ok = issue_kq(0);
-                if (ok) tma_done = 1;
-            }
-            if (!ok && lane == 0) *abort_flag = 1;
-            if (p.chunk_states && t == 0) store_state_tiles(0);
-        }
-        for (int ci = 0; ci < nchunks; ++ci) {
-            const int c0 = t0 + ci * kChunk;
-            const int nv = min(kChunk, t1 - c0);
-            const int slot = ci & 1, st = ci % kStages;
-            const uint32_t ph = ci & 1, ph2 = (ci >> 1) & 1;
-            const uint32_t stage_a = smem_u32(sm + oStage + st * kStageBytes);
+        for (int ci = 0; ci < nchunks && !aborted; ++ci) {
+            const int c0tok = t0 + ci * kChunk;
+            const int nv = min(kChunk, t1 - c0tok);
+            const int slot = ci & 1;
+            const uint32_t ph = ci & 1;
             const float* vec = reinterpret_cast<const float*>(sm + oVec) + (ci % kVecSlots) * kVecFloats;
             const float* bv = vec + 64;
             const float* gam = vec + 192;
             const float* dec = vec + 256;
 
-            // gates, T and P T of this chunk (prep), [K; Q] S0 (issued at the end of the previous chunk)
-            __syncwarp();
-            bool ok = mbar_wait(bar(B_READY0 + slot), ph2, wl);
-            ok = mbar_wait(bar(B_KQ), ph, wl) && ok;
+            // (a) R of A: gates and P T of this chunk from the prep, [K; Q] S0 of A
+            bool bad = !mbar_wait(bar(B_READY0 + slot), (ci >> 1) & 1, wl);
+            bad = !mbar_wait(bar(B_KQ0 + 0), ph, wl) || bad;
             tc_fence_after();
-            if (bar_or(1, kChainThreads, !ok || *abort_flag)) { aborted = true; break; }
-            if (t == 0) *progress = 2 * ci + 1;
-            const float gC = gam[63];
-            float qs[32];
-            if (kw) {
-                // ---- C2: R = beta o (V - gam o (K S0)) -> R tiles ----
-                float x[32];
-                ld_acc(kColKQ, x);
-                const float bj = bv[i], gj = gam[i];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t w4[4] = {vraw[e].x, vraw[e].y, vraw[e].z, vraw[e].w};
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int c = e * 8 + 2 * m;
-                        x[c] = bj * (__uint_as_float(w4[m] << 16) - gj * x[c]);
-                        x[c + 1] = bj * (__uint_as_float(w4[m] & 0xffff0000u) - gj * x[c + 1]);
-                    }
-                }
-                store_split_half(Rhi, Rlo, i, hs, x);
-                load_v(ci + 1);
+            phase_r(0, bv, gam);
+            // (b) S update of B for the previous chunk
+            if (ci > 0) {
+                const float* pvec = reinterpret_cast<const float*>(sm + oVec) + ((ci - 1) % kVecSlots) * kVecFloats;
+                if (phase_s(1, ci - 1, pvec[192 + 63], bad)) { aborted = true; break; }
+                bad = false;
+            }
+            // (c) dec o Delta of A, output of A
+            if (!kw && want_out && nv == kChunk) {
+                // the staging tile's previous TMA store has read it
+                if (t == 64) bulk_wait_read_all();
+                named_bar(NB_OUT, 128);
+            }
+            bad = !mbar_wait(bar(B_D0 + 0), ph, wl) || bad;
+            tc_fence_after();
+            phase_d(0, dec, c0tok, nv);
+            // (d) R of B
+            bad = !mbar_wait(bar(B_KQ0 + 1), ph, wl) || bad;
+            tc_fence_after();
+            phase_r(1, bv, gam);
+            load_v(ci + 1);
+            // (e) S update of A
+            if (phase_s(0, ci, gam[63], bad)) { aborted = true; break; }
+            // (f) dec o Delta of B, output of B
+            bad = !mbar_wait(bar(B_D0 + 1), ph, wl);
+            tc_fence_after();
+            // both [T; P T] R of this chunk have read the slot's T and P T tiles
+            // (and the prep's T^T P^T long before): the prep may refill it
+            if (t == 0 && !bad) mbar_arrive(bar(B_TFREE0 + slot));
+            phase_d(1, dec, c0tok, nv);
+            if (!kw && want_out && nv == kChunk) {
                 fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar(3, 128);
-                // ---- C3: [T; P T] R (warp 0) ----
-                if (warp == 0) {
-                    if (elect_one()) {
-                        tc_fence_after();
-                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 128, 64);
-                        constexpr uint32_t idw = idesc(kFmtBf16, 1, 1, 128, kAccCols);
-                        const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
-                        const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t ah = desc_sw128(thi + s * 2048, kLboTPT, 1024);
-                            const uint64_t al = desc_sw128(tlo + s * 2048, kLboTPT, 1024);
-                            // N = 128: [R_hi | R_lo], the lo tile kTile64 after the hi tile
-                            const uint64_t rh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
-                            const uint64_t rl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
-                            mma_bf16(tmem + kColD, ah, rh, idw, s > 0);
-                            if (!kNStack) mma_bf16(tmem + kColD, ah, rl, id, 1);
-                            mma_bf16(tmem + kColD, al, rh, id, 1);
-                        }
-                        mma_commit(bar(B_D));
-                    }
-                    __syncwarp();
-                }
-            } else {
-                // ---- Q warps: gam o (Q S0) of this row, kept until P Delta arrives ----
-                ld_acc(kColKQ, qs);
-                const float gi = gam[i];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) qs[c] *= gi;
-            }
-            __syncwarp();
-            bool bad = !mbar_wait(bar(B_D), ph, wl);
-            tc_fence_after();
-            // [T; P T] R has read the slot's T and P T tiles (and the prep's
-            // T^T P^T long before): the prep may fill the slot for chunk ci + 2
-            if (t == 0 && !bad) {
-                mbar_arrive(bar(B_TFREE0 + slot));
-                *progress = 2 * ci + 2;
-            }
-            if (kw) {
-                // ---- C4: dec o Delta -> R tiles (T R has read them) ----
-                float x[32];
-                ld_acc(kColD, x);
-                const float dj = dec[i];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] *= dj;
-                store_split_half(Rhi, Rlo, i, hs, x);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar(3, 128);
-                // ---- C5: S update K^T (dec o Delta) (warp 0) ----
-                if (warp == 0) {
-                    if (elect_one()) {
-                        tc_fence_after();
-                        constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, kAccCols);
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t ak = desc_sw128(stage_a + s * 2048, kRegionBytes, 1024);
-                            mma_bf16(tmem + kColS, ak, desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024), id, s > 0);
-                            if (!kNStack)
-                                mma_bf16(tmem + kColS, ak, desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024), id, 1);
-                        }
-                        mma_commit(bar(B_S));
-                    }
-                    __syncwarp();
-                }
-            } else {
-                // ---- output: O = scale [gam o (Q S0) + P Delta] ----
-                float pd[32];
-                ld_acc(kColD, pd);
-                if (want_out && i < nv) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        p.out + ((row_base + c0 + i) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int c = e * 8 + 2 * m;
-                            w4[m] = cvt_bf16x2(scale * (qs[c] + pd[c]), scale * (qs[c + 1] + pd[c + 1]));
-                        }
-                        dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
+                named_bar(NB_OUT, 128);
+                if (t == 64) {
+                    tma_store_3d(&tmap_o, vs * kVs, h, static_cast<int>(row_base + c0tok), smem_u32(sm + oO));
+                    bulk_commit();
                 }
             }
-            __syncwarp();
-            // ---- C6: S <- gam_n S + K^T (dec o Delta) ----
-            bad = !mbar_wait(bar(B_S), ph, wl) || bad;
-            tc_fence_after();
-            {
-                float x[32];
-                ld_acc(kColS, x);
+            if (bad) *abort_flag = 1;
+        }
+        if (!aborted && nchunks > 0) {
+            // S update of B for the last chunk
+            const float* pvec =
+                reinterpret_cast<const float*>(sm + oVec) + ((nchunks - 1) % kVecSlots) * kVecFloats;
+            aborted = phase_s(1, nchunks - 1, pvec[192 + 63], false);
+        }
+        if (t == 64) bulk_wait_all();  // the output tile stores
+        if (aborted) {
+            if (t == 0) record_error(p.err, kErrTimeout);
+        } else if (p.final_state) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], x[c]);
-            }
-            // the stage's readers ([K; Q] S0, the update, the prep's Q K^T) have
-            // all completed: it takes chunk ci + 3's tiles
-            if (t == 0 && ci + kStages < nchunks) {
-                issue_tma(ci + kStages);
-                tma_issued = ci + kStages + 1;
-            }
-            if (p.chunk_states) {
-                // the bulk copy of this chunk's start-state tiles has read them
-                if (t == 0) bulk_wait_read_all();
-                named_bar(1, kChainThreads);
-            }
-            store_split_half(Shi, Slo, srow, hs, S);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (bar_or(1, kChainThreads, bad || *abort_flag)) { aborted = true; break; }
-            // ---- next chunk's [K; Q] S0 ----
-            if (ci + 1 < nchunks) {
-                bool ok2 = true;
-                if (warp == 0) {
-                    ok2 = issue_kq(ci + 1);
-                    if (ok2) tma_done = ci + 2;
-                }
-                if (!ok2 && lane == 0) *abort_flag = 1;
-                if (p.chunk_states && t == 0) store_state_tiles(ci + 1);
+            for (int X = 0; X < 2; ++X) {
+                float* dst = p.final_state + state_off + static_cast<long long>(srow) * V + 32 * X + c0;
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) = make_float4(S[X][j], S[X][j + 1], S[X][j + 2], S[X][j + 3]);
             }
         }
-        if (p.chunk_states && t == 0) bulk_wait_all();
-        if (aborted) {
-            // nothing warp 0 issued, no stage load and no bulk copy outlives the CTA
-            if (warp == 0) {
-                if (elect_one()) mma_commit(bar(B_DRAIN0));
-                __syncwarp();
+    } else if (warp == kIssuerWarp) {
+        // ============================ issuer warp ============================
+        int tma_issued = 0, tma_done = 0;   // stage loads issued / waited for (chunk counts)
+        auto issue_tma = [&](int ci) {
+            const int st = ci % kStages;
+            uint8_t* base = sm + oStage + st * kStageBytes;
+            const int z = static_cast<int>(row_base + t0 + ci * kChunk);
+            mbar_arrive_expect_tx(bar(B_FULL0 + st), kStageBytes);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                tma_load_3d(smem_u32(base + r * kRegionBytes), &tmap_k, r * 64, h, z, bar(B_FULL0 + st));
+                tma_load_3d(smem_u32(base + r * kRegionBytes + 64 * 128), &tmap_q, r * 64, h, z, bar(B_FULL0 + st));
             }
-            if (t == 0) {
+        };
+        if (lane == 0) {
+            if (nchunks > 0) {
+                tma_prefetch_desc(&tmap_k);
+                tma_prefetch_desc(&tmap_q);
+                if (want_out) tma_prefetch_desc(&tmap_o);
+            }
+            for (int c = 0; c < kStages && c < nchunks; ++c) issue_tma(c);
+        }
+        tma_issued = min(kStages, nchunks);
+        // stage of chunk cj loaded (once per chunk, before its first product)
+        auto wait_full = [&](int cj) -> bool {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FULL0 + cj % kStages), (cj / kStages) & 1, wl));
+            if (ok) tma_done = cj + 1;
+            return ok;
+        };
+        // [K; Q] [S_hi | S_lo] of sub-chain X, chunk cj
+        auto issue_kq = [&](int X, int cj) {
+            if (elect_one()) {
+                tc_fence_after();
+                const uint32_t stage_c = smem_u32(sm + oStage + (cj % kStages) * kStageBytes);
+                const uint32_t sx = smem_u32(sm + oS + X * kTileSX);
+                constexpr uint32_t id = idesc(kFmtBf16, 0, 1, 128, 64);
+#pragma unroll
+                for (int s = 0; s < kDk / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * kRegionBytes + (s & 3) * 32;
+                    mma_bf16(tmem + kColKQ + 64 * X, desc_sw128(stage_c + koff, 0, 1024),
+                             desc_sw128(sx + s * 2048, kTileSX, 1024), id, s > 0);
+                }
+                mma_commit(bar(B_KQ0 + X));
+            }
+            __syncwarp();
+        };
+        // [T; P T] [R_hi | R_lo] of X (both parts of [T; P T])
+        auto issue_tr = [&](int X, int cj) {
+            if (elect_one()) {
+                tc_fence_after();
+                const int slot = cj & 1;
+                const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
+                const uint32_t tlo = smem_u32(sm + oT + (slot * 2 + 1) * kTile64);
+                const uint32_t rx = smem_u32(sm + oR + X * kTile64);
+                constexpr uint32_t id = idesc(kFmtBf16, 1, 1, 128, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t r = desc_sw128(rx + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColD + 64 * X, desc_sw128(thi + s * 2048, kLboTPT, 1024), r, id, s > 0);
+                    mma_bf16(tmem + kColD + 64 * X, desc_sw128(tlo + s * 2048, kLboTPT, 1024), r, id, 1);
+                }
+                mma_commit(bar(B_D0 + X));
+            }
+            __syncwarp();
+        };
+        // K^T [dX_hi | dX_lo] of X (A = K^T read MN-major from the stage)
+        auto issue_upd = [&](int X, int cj) {
+            if (elect_one()) {
+                tc_fence_after();
+                const uint32_t stage_c = smem_u32(sm + oStage + (cj % kStages) * kStageBytes);
+                const uint32_t rx = smem_u32(sm + oR + X * kTile64);
+                constexpr uint32_t id = idesc(kFmtBf16, 1, 1, kDk, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + kColS + 64 * X, desc_sw128(stage_c + s * 2048, kRegionBytes, 1024),
+                             desc_sw128(rx + s * 2048, kTile64, 1024), id, s > 0);
+                mma_commit(bar(B_S0 + X));
+            }
+            __syncwarp();
+        };
+
+        // failure-detection test: a wait that nothing ends runs out
+        bool bad = p.stall && !__all_sync(0xffffffffu, mbar_wait(bar(B_STALL), 0, wl));
+        // initial state tiles stored
+        bool aborted = bar_or(NB_C6, kAllIss, bad);
+        if (!aborted && nchunks > 0) {
+            bad = !wait_full(0);
+            if (!bad) {
+                issue_kq(0, 0);
+                issue_kq(1, 0);
+            }
+        }
+        for (int ci = 0; ci < nchunks && !aborted; ++ci) {
+            named_bar(NB_C2 + 0, kKIss);             // (a) R of A stored
+            issue_tr(0, ci);
+            if (ci > 0) {
+                if (bar_or(NB_C6 + 1, kAllIss, bad)) { aborted = true; break; }   // (b)
+                // every product that reads chunk ci - 1's stage has completed
+                if (lane == 0 && ci + 2 < nchunks) issue_tma(ci + 2);
+                if (ci + 2 < nchunks) tma_issued = ci + 3;
+                issue_kq(1, ci);
+            }
+            named_bar(NB_C4 + 0, kKIss);             // (c) dec o Delta of A stored
+            issue_upd(0, ci);
+            named_bar(NB_C2 + 1, kKIss);             // (d) R of B stored
+            issue_tr(1, ci);
+            if (bar_or(NB_C6 + 0, kAllIss, bad)) { aborted = true; break; }       // (e)
+            if (ci + 1 < nchunks) {
+                if (wait_full(ci + 1)) issue_kq(0, ci + 1);
+                else bad = true;
+            }
+            named_bar(NB_C4 + 1, kKIss);             // (f) dec o Delta of B stored
+            issue_upd(1, ci);
+        }
+        if (!aborted && nchunks > 0) aborted = bar_or(NB_C6 + 1, kAllIss, bad);   // last (b)
+        if (aborted) {
+            // nothing this warp issued (products, stage loads) outlives the CTA
+            if (elect_one()) mma_commit(bar(B_DRAIN0));
+            __syncwarp();
+            if (lane == 0) {
+                *abort_flag = 1;
                 record_error(p.err, kErrTimeout);
                 mbar_wait(bar(B_DRAIN0), 0, kDrainLimit);
                 for (int c = tma_done; c < tma_issued; ++c)
                     mbar_wait(bar(B_FULL0 + c % kStages), (c / kStages) & 1, kDrainLimit);
             }
-        } else if (p.final_state) {
-            float* dst = p.final_state + state_off + static_cast<long long>(srow) * V + cq;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            __syncwarp();
         }
     } else {
         // ============================ prep warps ============================
@@ -509,15 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     b_pre = bf16_to_f32(p.beta[idx]);
                 }
             }
-        };
-        // warp 8: wait (bounded) until the chain's progress reaches `target`
-        auto wait_progress = [&](int target) -> bool {
-            for (uint32_t n = 0; n < wl; ++n) {
-                if (*progress >= target) return true;
-                if (*abort_flag) return false;
-                __nanosleep(64);
-            }
-            return false;
         };
         load_gates(0);
         bool tcopy_out = false;  // thread q == 0: a T tile copy is in flight (phase tcopy_it & 1)
@@ -538,16 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* gam = vec + 192;
             float* dec = vec + 256;
 
-            // stage of this chunk loaded; its slot free ([T; P T] R of chunk it - 2 done)
+            // stage of this chunk loaded; its slot free (both [T; P T] R of chunk it - 2 done)
             bool ok = mbar_wait(bar(B_FULL0 + st), (it / kStages) & 1, wl);
             if (it >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((it - 2) >> 1) & 1, wl) && ok;
             if (bar_or(2, kPrepThreads, !ok || *abort_flag)) { aborted = true; break; }
 
             // Q K^T (M = 64) while the gates are formed
             if (warp == 8) {
-                const bool go = !kGate || it == 0 || wait_progress(2 * (it - 1) + 1);
-                if (!go && lane == 0) *abort_flag = 1;
-                if (go && elect_one()) {
+                if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
                     const uint32_t sa = smem_u32(stage);
@@ -623,9 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // (P T)^T = T^T P^T (M = 64): A = T^T tile (K-major), B = P tile (K-major)
             if (warp == 8) {
-                const bool go = !kGate || it == 0 || wait_progress(2 * (it - 1) + 2);
-                if (!go && lane == 0) *abort_flag = 1;
-                if (go && elect_one()) {
+                if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
                     const uint32_t thi = smem_u32(sm + oT + (slot * 2 + 0) * kTile64);
@@ -684,16 +747,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_chain(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
     if (a.d_k != kDk || a.chunk_T == nullptr || a.d_v % kVs != 0) return cudaErrorInvalidValue;
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
-    CUtensorMap mk, mq;
+    CUtensorMap mk, mq, mo;
     memset(&mk, 0, sizeof(mk));
     memset(&mq, 0, sizeof(mq));
+    memset(&mo, 0, sizeof(mo));
     if (rows <= 0 || !make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H))
         return cudaErrorInvalidValue;
+    if (a.out && !make_rows_map(&mo, a.out, rows, a.H, a.d_v)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_fwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
     ChainFwdParams prm{a, wait_limit};
     dim3 grid(a.d_v / kVs, a.H, a.N);
-    gdn_fwd_chain_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, prm);
+    gdn_fwd_chain_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mq, mo, prm);
     return cudaGetLastError();
 }
 

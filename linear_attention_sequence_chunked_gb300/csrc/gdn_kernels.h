@@ -27,6 +27,8 @@ struct FwdArgs {
     int d_k;
     int d_v;
     int* err;               // device error word
+    int stall;              // failure-detection test only: the stacked-product chain's issuer first
+                            // waits on a hand-off that nothing signals (bounded), so the CTA times out
 };
 
 // Backward pass 2 (reverse state-gradient chain; the chunk chain kernel in

@@ -98,6 +98,8 @@ def load():
         lib.gdn_probe_gemm_bf16.restype = i
         lib.gdn_chunk_bwd_noalloc.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp]
         lib.gdn_chunk_bwd_noalloc.restype = i
+        lib.gdn_chunk_fwd_wait_limit.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp, sz, ctypes.c_uint32, i, vp]
+        lib.gdn_chunk_fwd_wait_limit.restype = i
         lib.gdn_kernel_launches.argtypes = []
         lib.gdn_kernel_launches.restype = ctypes.c_uint64
         _lib = lib
@@ -157,6 +159,20 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final
                               _ptr(final_state), B, T, H, d_k, d_v, _ptr(workspace),
                               int(workspace_bytes), _stream(stream))
     _check(st, "gdn_chunk_fwd")
+
+
+def gdn_chunk_fwd_wait_limit(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+                             B, T, H, d_k, d_v, workspace, workspace_bytes, wait_limit, stall_first_wait=0,
+                             stream=None):
+    """gdn_chunk_fwd with a chosen bound (polls) on the kernels' hand-off
+    waits, and optionally a first wait that nothing ends: for exercising
+    failure detection."""
+    st = load().gdn_chunk_fwd_wait_limit(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                         _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                         _ptr(final_state), B, T, H, d_k, d_v, _ptr(workspace),
+                                         int(workspace_bytes), int(wait_limit), int(stall_first_wait),
+                                         _stream(stream))
+    _check(st, "gdn_chunk_fwd_wait_limit")
 
 
 def gdn_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,

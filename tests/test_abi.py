@@ -209,3 +209,16 @@ def test_tensor_arguments_must_be_dense_device_memory(lib):
         gdn.gdn_kda_chunk_fwd(x, x, x, g, beta, 1.0, None, None, x, None, 1, 64, 1, 64, 64)
     with pytest.raises(ValueError, match="CUDA"):
         gdn.chunk_gated_delta_rule_fwd(x, x, x, g[..., 0], beta)
+
+
+def test_wait_limit_entry_host_validation(lib):
+    import ctypes
+    f = lib.gdn_chunk_fwd_wait_limit
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + \
+        [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    p = 1 << 20  # never dereferenced: every case is refused on the host
+    # d_k = 64 is refused (its kernels keep the default bound), as is a missing workspace
+    assert f(p, p, p, p, p, 1.0, None, None, p, None, 1, 128, 1, 64, 64, p, 1 << 20, 1, 0, None) == 2
+    assert f(p, p, p, p, p, 1.0, None, None, p, None, 1, 128, 1, 128, 64, None, 0, 1, 0, None) == 2
+    assert f(p, p, p, p, p, 1.0, None, None, p, None, 0, 128, 1, 128, 64, p, 1 << 20, 1, 0, None) == 1
