@@ -105,11 +105,9 @@ GDN_API size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_
  *                 gdn_chunk_fwd_workspace_size() bytes, every chunk's T is
  *                 formed first by a chunk-parallel kernel and the chunk chain
  *                 reads it (the faster route); with NULL or fewer bytes the
- *                 chunk chain forms T itself.  At d_k = 64 both routes give
- *                 the same bits; at d_k = 128 the workspace route forms the
- *                 output's causal term as (P T) R instead of P (T R), so the
- *                 two agree to rounding.  A non-NULL workspace that is not
- *                 256-byte aligned returns GDN_ERR_MISALIGNED.
+ *                 chunk chain forms T itself.  Both routes give the same
+ *                 arithmetic.  A non-NULL workspace that is not 256-byte
+ *                 aligned returns GDN_ERR_MISALIGNED.
  * Returns GDN_OK once the work is enqueued on `stream`.
  */
 GDN_API gdn_status gdn_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
@@ -394,9 +392,9 @@ GDN_API gdn_status gdn_probe_gemm_bf16(const gdn_bf16* A, const gdn_bf16* B, gdn
  * copy and tensor-core product it started, and leaves without writing its
  * final state, so the context stays usable.  Library bookkeeping with no
  * counterpart on the pages.  Takes a workspace of at least
- * gdn_chunk_fwd_workspace_size() bytes and d_k = 128 (the kernels whose drain
- * waits keep their own bound); otherwise GDN_ERR_UNSUPPORTED.  Other
- * arguments and errors as gdn_chunk_fwd.
+ * gdn_chunk_fwd_workspace_size() bytes and d_k = 128 (the tile route this
+ * test covers); otherwise GDN_ERR_UNSUPPORTED.  Other arguments and errors
+ * as gdn_chunk_fwd.
  */
 GDN_API gdn_status gdn_chunk_fwd_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
                                     const float* g, const gdn_bf16* beta, float scale,

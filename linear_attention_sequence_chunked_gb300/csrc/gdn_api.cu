@@ -316,8 +316,7 @@ gdn_status gdn_chunk_fwd_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const 
                                     int B, int T, int H, int d_k, int d_v,
                                     void* workspace, size_t workspace_bytes, uint32_t wait_limit,
                                     int stall_first_wait, cudaStream_t stream) {
-    // only the stacked-product chain (d_k = 128, T tiles given) drains with
-    // its own bound; the other kernels keep the default hand-off bound
+    // the route this failure-detection entry covers: d_k = 128 with the T tiles given
     if (d_k != 128) return GDN_ERR_UNSUPPORTED;
     if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return check_shapes(B, T, H, d_k, d_v);
     const size_t tb = tiles_bytes(B, T, H, cu_seqlens != nullptr);

@@ -92,7 +92,7 @@ constexpr int kTB = 32 * kTS;                       // floats per block
 constexpr int oVec = oTf + 3 * kTB * 4;             // [slot][g, beta, G, gam, dec] x 64 fp32
 constexpr int kVecFloats = 5 * 64;
 constexpr int oBar = oVec + 2 * kVecFloats * 4;
-constexpr int kBars = 19;
+constexpr int kBars = 20;
 constexpr int oMisc = oBar + kBars * 8;             // TMEM slot, abort flag
 constexpr int kBytes = oMisc + 16;
 // backward: the dO tile [i][v] bf16 shares the R tiles' space (dead between
@@ -107,10 +107,31 @@ enum {
     B_SFREE0 = 12, B_SFREE1 = 13, B_DRAIN0 = 14, B_DRAIN1 = 15, B_DRAIN2 = 16,
     // backward: warp 0 has issued K dS (the issuer warp issues P^T dO with
     // it); forward: Q S done; backward: Q^T G done
-    B_KSI = 17, B_QSD = 18
+    B_KSI = 17, B_QSD = 18,
+    // failure-detection test: a hand-off that nothing signals
+    B_STALL = 19
 };
 
 __device__ __forceinline__ void named_bar(int id) { tc::named_bar(id, id == 1 ? kChainThreads : kPrepThreads); }
+
+// Named barrier 1 (chain warps) or 2 (prep warps) that also ORs `pred` over
+// its participants, so that every thread of the group takes the same
+// decision (to leave after a wait ran out) whatever moment the shared abort
+// flag was raised by another group.
+__device__ __forceinline__ bool named_bar_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(id == 1 ? kChainThreads : kPrepThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Bound of the waits that drain in-flight copies and products before a CTA
+// leaves, independent of the hand-off bound: a short hand-off bound never
+// lets a copy or a product outlive the CTA.
+constexpr uint32_t kDrainLimit = kDefaultWaitLimit;
 
 // Arguments of both directions.
 struct ChainArgs {
@@ -129,6 +150,7 @@ struct ChainArgs {
     const uint8_t* chunk_T;       // T operand tiles of every chunk (may be null: formed in place)
     int N, T, H, d_k, d_v;
     int* err;
+    int stall;                    // failure-detection test (forward): first wait on a hand-off nothing signals
 };
 
 struct WsParams {
@@ -331,6 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the K S MMAs (critical path) go out before the start-state copies,
             // which read the same tiles
             if (nchunks > 0) {
+                // failure-detection test: a wait that nothing ends runs out
+                if (p.stall && warp == 0 && !__all_sync(0xffffffffu, mbar_wait(bar(B_STALL), 0, wl)) && lane == 0)
+                    *abort_flag = 1;
                 issue_c1(0);
                 if (p.chunk_states && t == 0) store_state_tiles(0);
             }
@@ -351,8 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(B_KS), ph, wl) && ok;
                 if (!ok) *abort_flag = 1;
                 tc_fence_after();
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
 
                 // ---- C2: R = beta o (V - gam o (K S)) ----
                 {
@@ -402,8 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
 
                 // ---- C4: Delta tiles and dec o Delta tiles ----
                 {
@@ -453,8 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (want_out && !mbar_wait(bar(B_QSD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // ... and so have the bulk copies
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
                 // every MMA that reads this chunk's K/Q stage has completed (K S,
                 // the state update, Q S; the prep's gram long before): the stage
                 // takes chunk ci + 2's tiles now, a whole epilogue window earlier
@@ -506,9 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                named_bar(1);
+                const bool quit = named_bar_or(1, *abort_flag);
                 if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
-                if (*abort_flag) { aborted = true; break; }
+                if (quit) { aborted = true; break; }
             }
         } else {
             // a quarter dO row of this slice (row hrow of the chunk, columns
@@ -547,8 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 // K/Q tiles of this chunk
                 if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
                 tma_done = it + 1;
 
                 // ---- C1: K dS (stage and dS tiles only) ----
@@ -573,8 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 // gates, T and P of this chunk from the prep warps
                 if (!mbar_wait(bar(B_READY0 + slot), ph2, wl)) *abort_flag = 1;
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
 
                 // P^T dO comes from the issuer warp (behind K dS, once P is in)
                 // G = scale gam o dO -> D tiles (B operand of Q^T G), while the MMAs run
@@ -594,8 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(B_PD), ph, wl) && ok;
                 if (!ok) *abort_flag = 1;
                 tc_fence_after();
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
 
                 // ---- C2: dDelta = scale P^T dO + dec o (K dS) -> R tiles ----
                 {
@@ -636,8 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!mbar_wait(bar(B_D), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
 
                 // ---- C4: X = -beta gam o dBhat -> R tiles (dDelta consumed) ----
                 {
@@ -676,8 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar(B_QSD), ph, wl)) *abort_flag = 1;
                 tc_fence_after();
                 if (p.chunk_states && t == 0) bulk_wait_read_all();  // C6 overwrites the S tiles
-                named_bar(1);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(1, *abort_flag)) { aborted = true; break; }
                 // every MMA that reads this chunk's K/Q stage has completed
                 if (t == 0) {
                     if (use_tma) {
@@ -700,9 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar(1);
+                const bool quit = named_bar_or(1, *abort_flag);
                 if (t == 0) mbar_arrive(bar(B_TFREE0 + slot));  // T tiles and gates of this slot consumed
-                if (*abort_flag) { aborted = true; break; }
+                if (quit) { aborted = true; break; }
             }
         }
         if (p.chunk_states && t == 0) bulk_wait_all();
@@ -713,9 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (t == 0) {
                 record_error(p.err, kErrTimeout);
-                mbar_wait(bar(B_DRAIN0), 0, wl);
+                mbar_wait(bar(B_DRAIN0), 0, kDrainLimit);
                 for (int ci = tma_done; ci < tma_issued; ++ci)
-                    mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, wl);
+                    mbar_wait(bar(B_FULL0 + (ci & 1)), (ci >> 1) & 1, kDrainLimit);
             }
         } else if (p.state_out && srow >= 0) {
             float* dst = p.state_out + state_off + static_cast<long long>(srow) * V + 32 * hs;
@@ -768,8 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!use_tma) {
                 if (it >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((it - 2) >> 1) & 1, wl);
                 if (!ok) *abort_flag = 1;
-                named_bar(2);
-                if (*abort_flag) { aborted = true; break; }
+                if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
                 for (int e = q; e < 2 * 64 * 8; e += 128) {
                     const int which = e >> 9;
                     const int r = (e >> 3) & 63, ch = e & 7;
@@ -785,8 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (q == 0) mbar_arrive(bar(B_FULL0 + st));
             }
             if (!mbar_wait(bar(B_FULL0 + st), ph2, wl)) *abort_flag = 1;
-            named_bar(2);
-            if (*abort_flag) { aborted = true; break; }
+            if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
 
             // gram K K^T and Q K^T (two M = 64 products), running while the
             // gates are formed.  Forward with T tiles given (only Q K^T): issued
@@ -820,8 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = true;
             if (it >= 2) ok = mbar_wait(bar(B_TFREE0 + slot), ((it - 2) >> 1) & 1, wl);
             if (!ok) *abort_flag = 1;
-            named_bar(2);
-            if (*abort_flag) { aborted = true; break; }
+            if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
             if (load_t && q == 0) {
                 // T tiles of this chunk (from the chunk-parallel inverse) into the free slot
                 mbar_arrive_expect_tx(bar(B_TCOPY), 2 * kTile64);
@@ -857,8 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (!mbar_wait(bar(B_GRAM), ph, wl)) *abort_flag = 1;
             tc_fence_after();
-            named_bar(2);
-            if (*abort_flag) { aborted = true; break; }
+            if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
 
             // All four warps form the chunk's decayed products: thread (warp w,
             // lane l) takes row i = 16 (w - 4) + l % 16 and columns 32 (l / 16) ..
@@ -1015,8 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar(2);
-            if (*abort_flag) { aborted = true; break; }
+            if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
             if (q == 0) {
                 if (load_t) {
                     if (mbar_wait(bar(B_TCOPY), it & 1, wl)) tcopy_out = false;
@@ -1025,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!tcopy_out) mbar_arrive(bar(B_READY0 + slot));
             }
         }
-        if (q == 0 && tcopy_out) mbar_wait(bar(B_TCOPY), tcopy_it & 1, wl);  // no copy outlives the CTA
+        if (q == 0 && tcopy_out) mbar_wait(bar(B_TCOPY), tcopy_it & 1, kDrainLimit);  // no copy outlives the CTA
         if (aborted) {
             if (warp == 8) {
                 if (elect_one()) mma_commit(bar(B_DRAIN1));
@@ -1033,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (q == 0) {
                 record_error(p.err, kErrTimeout);
-                mbar_wait(bar(B_DRAIN1), 0, wl);
+                mbar_wait(bar(B_DRAIN1), 0, kDrainLimit);
             }
         }
     } else if (warp == kIssuerWarp) {
@@ -1093,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok && lane == 0) *abort_flag = 1;  // the chain records the timeout
                 if (elect_one()) mma_commit(bar(B_DRAIN2));
                 __syncwarp();
-                mbar_wait(bar(B_DRAIN2), 0, wl);
+                mbar_wait(bar(B_DRAIN2), 0, kDrainLimit);
             }
         } else {
             if (want_out && nchunks > 0) {
@@ -1150,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // nothing this warp issued is in flight when the CTA frees its TMEM
                 if (elect_one()) mma_commit(bar(B_DRAIN2));
                 __syncwarp();
-                mbar_wait(bar(B_DRAIN2), 0, wl);
+                mbar_wait(bar(B_DRAIN2), 0, kDrainLimit);
             }
         }
     }
@@ -1202,12 +1214,11 @@ cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t st
         gdn_state_passthrough_kernel<<<dim3(a.H, a.N), 256, 0, stream>>>(a);
         return cudaGetLastError();
     }
-    if (a.d_k == kDk && a.chunk_T != nullptr) return launch_fwd_chain(a, wait_limit, stream);
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = a.out; c.state_out = a.final_state;
     c.chunk_states = a.chunk_states; c.chunk_T = a.chunk_T;
-    c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err;
+    c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err; c.stall = a.stall;
     return launch_chain<false>(c, wait_limit, stream);
 }
 

@@ -27,8 +27,8 @@ struct FwdArgs {
     int d_k;
     int d_v;
     int* err;               // device error word
-    int stall;              // failure-detection test only: the stacked-product chain's issuer first
-                            // waits on a hand-off that nothing signals (bounded), so the CTA times out
+    int stall;              // failure-detection test only: the chain first waits on a hand-off that
+                            // nothing signals (bounded), so the CTA times out
 };
 
 // Backward pass 2 (reverse state-gradient chain; the chunk chain kernel in
@@ -184,11 +184,9 @@ cudaError_t launch_probe_copy(const void* src, void* dst, size_t bytes, cudaStre
 cudaError_t launch_probe_gemm(const uint16_t* A, const uint16_t* B, uint16_t* C, int M, int N, int K, int* err,
                               cudaStream_t stream);
 // Warp-specialised tensor-core forward (prep and chain warpgroups);
-// wait_limit bounds every mbarrier wait (polls).  Takes the stacked-product
-// chain (launch_fwd_chain) for d_k = 128 with T tiles given.
+// wait_limit bounds every hand-off mbarrier wait (polls); the waits that
+// drain in-flight copies and products before a CTA leaves keep the default.
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
-// The stacked-product forward chain: d_k = 128 and chunk_T required.
-cudaError_t launch_fwd_chain(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 constexpr uint32_t kDefaultWaitLimit = 4000000u;
 
 }  // namespace gdn

@@ -30,12 +30,6 @@ __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// bar.arrive: count this thread towards a named barrier of `count` threads
-// without waiting (the other participants wait with named_bar)
-__device__ __forceinline__ void named_bar_arrive(int id, int count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
     const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
     const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
