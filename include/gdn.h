@@ -149,23 +149,66 @@ GDN_API gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, c
                                  int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
 
 /*
+ * Bytes of the optional workspace of gdn_kda_chunk_fwd: T and P of every
+ * chunk in fp32, 32 KB per chunk and head (0 for unsupported sizes).  varlen
+ * as in gdn_chunk_fwd_workspace_size.
+ */
+GDN_API size_t gdn_kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
  * Chunked forward of the same per-channel-gate (KDA) recurrence: the sequence
  * is cut into chunks of 64 tokens, each chunk's gram A_ij = beta_i sum_c
  * k_ic k_jc exp(G_ic - G_jc) (j < i; G the per-channel running sum of g
  * inside the chunk) and causal score are formed with the decay inside the
  * sum over key channels, T = (I + A)^-1 by blocked forward substitution, and
  * the state passes from chunk to chunk, S <- diag(exp(G_n)) S +
- * (exp(G_n - G) o K)^T Delta.  All arithmetic fp32 on the CUDA cores; one
- * thread block per (64 value columns, head, sequence).  Arguments, layouts,
- * validation and errors as gdn_kda_recurrent_fwd (g is (B, T, H, d_k) fp32,
- * documented domain g <= 0; no workspace).  Same result as the token-serial
- * kernel up to fp32 rounding order.
+ * (exp(G_n - G) o K)^T Delta.  All arithmetic fp32 on the CUDA cores; the
+ * walk runs one thread block per (64 value columns, head, sequence).
+ * Arguments, layouts, validation and errors as gdn_kda_recurrent_fwd (g is
+ * (B, T, H, d_k) fp32, documented domain g <= 0), plus:
+ *   workspace     optional device scratch, 256-byte aligned.  With at least
+ *                 gdn_kda_chunk_fwd_workspace_size() bytes, every chunk's T
+ *                 and P are formed first by a chunk-parallel kernel and the
+ *                 walk reads them (the faster route); with NULL or fewer
+ *                 bytes the walk forms them itself.  Both routes give the
+ *                 same bits.  A non-NULL workspace that is not 256-byte
+ *                 aligned returns GDN_ERR_MISALIGNED.
+ * Same result as the token-serial kernel up to fp32 rounding order.
  */
 GDN_API gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
                                      const float* g, const gdn_bf16* beta, float scale,
                                      const float* initial_state, const int32_t* cu_seqlens,
                                      gdn_bf16* out, float* final_state,
-                                     int B, int T, int H, int d_k, int d_v, cudaStream_t stream);
+                                     int B, int T, int H, int d_k, int d_v,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace gdn_kda_chunk_bwd needs for these sizes. */
+GDN_API size_t gdn_kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen);
+
+/*
+ * Backward of gdn_kda_chunk_fwd: the reverse mode of its chunk algebra,
+ * chunk by chunk from the last, with the gradient w.r.t. each chunk's end
+ * state carried backwards.  Arguments, layouts, validation and errors as
+ * gdn_chunk_bwd, except that g and dg are (B, T, H, d_k) fp32: dg is the
+ * gradient w.r.t. each token's per-channel log decay.  Four kernels, all fp32
+ * on the CUDA cores: T and P of every chunk (chunk-parallel); the forward
+ * walk recording each chunk's start state; the reverse walk of the state
+ * gradient (one block per 64 value columns, head and sequence); the local
+ * gradients of every chunk (chunk-parallel), which sum over the value columns
+ * once and evaluate the decayed pair sums of the gram and the causal score
+ * once per chunk.  `workspace` (256-byte aligned, at least
+ * gdn_kda_chunk_bwd_workspace_size() bytes, contents on entry ignored) holds
+ * T and P and the per-chunk states and state gradients.  Every sum runs in a
+ * fixed order: repeated calls give the same bits.
+ */
+GDN_API gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                     const float* g, const gdn_bf16* beta, float scale,
+                                     const float* initial_state, const int32_t* cu_seqlens,
+                                     const gdn_bf16* d_out, const float* d_final_state,
+                                     gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                                     gdn_bf16* dbeta, float* d_initial_state,
+                                     int B, int T, int H, int d_k, int d_v,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Prologue: q/k L2 normalisation and the two gates from their raw inputs

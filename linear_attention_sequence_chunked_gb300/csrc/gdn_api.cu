@@ -189,6 +189,40 @@ gdn_status launch_bwd_passes(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     return GDN_OK;
 }
 
+// Per-chunk T and P of the per-channel-gate variant (fp32, 32 KB per chunk
+// and head): the forward's optional workspace and the backward's first part.
+size_t kda_tp_bytes(int B, int T, int H, int varlen) {
+    return round_up(sizeof(float) * gdn::kKdaTpFloats * chunk_slots(B, T, varlen) * H);
+}
+
+// T and P of every chunk into `tp` (chunk-parallel kernel).
+bool launch_kda_tp_pass(const gdn_bf16* q, const gdn_bf16* k, const float* g, const gdn_bf16* beta,
+                        const int32_t* cu_seqlens, float* tp, int B, int T, int H, int d_k, int* err,
+                        cudaStream_t stream) {
+    gdn::KdaTpArgs t{};
+    t.q = q; t.k = k; t.g = g; t.beta = beta; t.cu_seqlens = cu_seqlens; t.chunk_tp = tp;
+    t.N = B; t.T = T; t.H = H; t.d_k = d_k; t.err = err;
+    t.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
+    if (t.max_chunks == 0) return true;
+    return launched(gdn::launch_kda_tp(t, stream));
+}
+
+// Backward workspace of the per-channel-gate variant: T and P, the chunk
+// start states (forward walk), the end-state gradients (reverse walk).
+struct KdaBwdLayout {
+    size_t tp, states, dstates, total;
+};
+
+KdaBwdLayout kda_bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
+    KdaBwdLayout L{};
+    const size_t per = round_up(sizeof(float) * static_cast<size_t>(d_k) * d_v * chunk_slots(B, T, varlen) * H);
+    L.tp = 0;
+    L.states = kda_tp_bytes(B, T, H, varlen);
+    L.dstates = L.states + per;
+    L.total = L.dstates + per;
+    return L;
+}
+
 // Workspace of the sequence split: segment bounds, T tiles of the packed
 // segments, zero values and a scratch output for the transition run, the
 // identity start states, the segments' M and b, and their true start states.
@@ -344,19 +378,79 @@ gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
                      d_k, d_v, 1, stream);
 }
 
+size_t gdn_kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
+    return kda_tp_bytes(B, T, H, varlen);
+}
+
 gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
                              const gdn_bf16* beta, float scale, const float* initial_state,
                              const int32_t* cu_seqlens, gdn_bf16* out, float* final_state, int B, int T,
-                             int H, int d_k, int d_v, cudaStream_t stream) {
+                             int H, int d_k, int d_v, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
     gdn_status st = check_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return GDN_ERR_MISALIGNED;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
+    // With a workspace, every chunk's T and P come first from the
+    // chunk-parallel kernel and the walk loads them; without one, the walk
+    // forms them itself.
+    const size_t tb = kda_tp_bytes(B, T, H, cu_seqlens != nullptr);
+    float* tp = (workspace && workspace_bytes >= tb && tb > 0) ? static_cast<float*>(workspace) : nullptr;
+    if (tp && !launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
     gdn::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
+    a.chunk_tp = tp;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.err = err;
     if (!launched(gdn::launch_kda_chunk(a, stream))) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+size_t gdn_kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
+    if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
+    return kda_bwd_layout(B, T, H, d_k, d_v, varlen).total;
+}
+
+gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                             const gdn_bf16* beta, float scale, const float* initial_state,
+                             const int32_t* cu_seqlens, const gdn_bf16* d_out, const float* d_final_state,
+                             gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg, gdn_bf16* dbeta,
+                             float* d_initial_state, int B, int T, int H, int d_k, int d_v, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    gdn_status st = check_bwd(q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state, dq, dk, dv,
+                              dg, dbeta, d_initial_state, B, T, H, d_k, d_v);
+    if (st != GDN_OK) return st;
+    const KdaBwdLayout L = kda_bwd_layout(B, T, H, d_k, d_v, cu_seqlens != nullptr);
+    st = check_buffer(workspace, workspace_bytes, L.total);
+    if (st != GDN_OK) return st;
+    int* err = error_word();
+    if (!err) return GDN_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    float* tp = L.total ? reinterpret_cast<float*>(ws + L.tp) : nullptr;
+    float* states = L.total ? reinterpret_cast<float*>(ws + L.states) : nullptr;
+    float* dstates = L.total ? reinterpret_cast<float*>(ws + L.dstates) : nullptr;
+    const int max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
+    if (max_chunks > 0) {
+        // T and P of every chunk, then the forward walk recording each chunk's start state
+        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
+        gdn::FwdArgs f{};
+        f.q = q; f.k = k; f.v = v; f.g = g; f.beta = beta; f.scale = scale;
+        f.initial_state = initial_state; f.cu_seqlens = cu_seqlens;
+        f.out = nullptr; f.final_state = nullptr; f.chunk_states = states; f.chunk_tp = tp;
+        f.N = B; f.T = T; f.H = H; f.d_k = d_k; f.d_v = d_v; f.err = err;
+        if (!launched(gdn::launch_kda_chunk(f, stream))) return GDN_ERR_CUDA;
+    }
+    gdn::KdaBwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.d_out = d_out; a.scale = scale;
+    a.cu_seqlens = cu_seqlens; a.d_final_state = d_final_state;
+    a.chunk_tp = tp; a.chunk_states = states; a.chunk_dstates = dstates; a.d_initial_state = d_initial_state;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
+    a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.max_chunks = max_chunks; a.err = err;
+    // the reverse walk (also when T = 0: it passes d_final_state to d_initial_state)
+    if (!launched(gdn::launch_kda_bwd_chain(a, stream))) return GDN_ERR_CUDA;
+    if (max_chunks > 0 && !launched(gdn::launch_kda_bwd_local(a, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

@@ -28,15 +28,25 @@
 // product reads its operands as 16-byte vectors: a thread owns four adjacent
 // output columns and a few rows, and each step of the reduction takes four
 // terms at once.
+//
+// T and P depend on the keys, queries, gates and betas of one chunk only.
+// Given a workspace, gdn_kda_tp_kernel forms them for every chunk in parallel
+// (one block per chunk and head) and the walk above loads them, so the
+// serial chain keeps only the products with the state: the gram's decay
+// exponentials, about a third of a million per chunk, leave the critical
+// path.  The walk can also record every chunk's start state (the forward state
+// pass of the backward).
 #include "gdn_common.cuh"
+#include "gdn_kda_common.cuh"
 #include "gdn_kernels.h"
 
 namespace gdn {
 
 namespace {
 
-constexpr int kVs = 64;        // value columns per block
-constexpr int kThreads = 256;  // 16 x 16: ti = thread / 16 (rows), tj = thread % 16 (4-column group)
+using namespace kda;
+
+constexpr int kVs = 64;  // value columns per block; 16 x 16 threads: ti = thread / 16 (rows), tj = thread % 16
 
 template <int K>
 struct KdaSmem {
@@ -50,147 +60,8 @@ struct KdaSmem {
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-
-__device__ __forceinline__ void fma4(float (&acc)[4], float a, float4 b) {
-    acc[0] = fmaf(a, b.x, acc[0]);
-    acc[1] = fmaf(a, b.y, acc[1]);
-    acc[2] = fmaf(a, b.z, acc[2]);
-    acc[3] = fmaf(a, b.w, acc[3]);
-}
-
-// Rows [row0, row0 + nv) of a (.., T, H, D) bf16 tensor for head h, columns
-// [col0, col0 + W), widened into a 64 x LD fp32 tile; rows >= nv are zero.
-template <int W, int LD>
-__device__ __forceinline__ void load_rows_bf16(const uint16_t* __restrict__ src, long long row0, int H,
-                                               int h, int D, int col0, int nv, float* dst) {
-    constexpr int kPerRow = W / 8;
-    for (int e = threadIdx.x; e < 64 * kPerRow; e += blockDim.x) {
-        const int r = e / kPerRow;
-        const int c = (e % kPerRow) * 8;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nv)
-            raw = *reinterpret_cast<const uint4*>(src + ((row0 + r) * H + h) * static_cast<long long>(D) +
-                                                  col0 + c);
-        st4(dst + r * LD + c, make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)));
-        st4(dst + r * LD + c + 4, make_float4(__uint_as_float(raw.z << 16), __uint_as_float(raw.z & 0xffff0000u),
-                                              __uint_as_float(raw.w << 16), __uint_as_float(raw.w & 0xffff0000u)));
-    }
-}
-
-// The same for a (.., T, H, W) fp32 tensor (all W columns).
-template <int W, int LD>
-__device__ __forceinline__ void load_rows_f32(const float* __restrict__ src, long long row0, int H, int h,
-                                              int nv, float* dst) {
-    constexpr int kPerRow = W / 4;
-    for (int e = threadIdx.x; e < 64 * kPerRow; e += blockDim.x) {
-        const int r = e / kPerRow;
-        const int c = (e % kPerRow) * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < nv) x = ld4(src + ((row0 + r) * H + h) * static_cast<long long>(W) + c);
-        st4(dst + r * LD + c, x);
-    }
-}
-
-// acc[r][.] += sum_{kk < KD} A[i_r][kk] B[kk][4 tj .. 4 tj + 3] for the rows
-// i_r = ti + 16 r: A and B row-major, four reduction terms per step (one
-// 16-byte read of each of the TM rows of A and of four rows of B).
-template <int TM, int KD>
-__device__ __forceinline__ void mm_rows(float (&acc)[TM][4], const float* A, int lda, const float* B, int ldb,
-                                        int ti, int tj) {
-#pragma unroll 2
-    for (int k0 = 0; k0 < KD; k0 += 4) {
-        float4 b[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) b[q] = ld4(B + (k0 + q) * ldb + 4 * tj);
-#pragma unroll
-        for (int r = 0; r < TM; ++r) {
-            const float4 a = ld4(A + (ti + 16 * r) * lda + k0);
-            fma4(acc[r], a.x, b[0]);
-            fma4(acc[r], a.y, b[1]);
-            fma4(acc[r], a.z, b[2]);
-            fma4(acc[r], a.w, b[3]);
-        }
-    }
-}
-
-// acc[4 m + e][.] += sum_{j < 64} At[j][64 m + 4 ti + e] B[j][4 tj .. 4 tj + 3]
-// (m < K / 64, e < 4): the product with a transposed left operand, whose rows
-// are read as 16-byte vectors along the output rows.
 template <int K>
-__device__ __forceinline__ void mm_trans(float (&acc)[K / 16][4], const float* At, int lda, const float* B,
-                                         int ldb, int ti, int tj) {
-#pragma unroll 4
-    for (int j = 0; j < 64; ++j) {
-        const float4 b = ld4(B + j * ldb + 4 * tj);
-#pragma unroll
-        for (int m = 0; m < K / 64; ++m) {
-            const float4 a = ld4(At + j * lda + 64 * m + 4 * ti);
-            fma4(acc[4 * m + 0], a.x, b);
-            fma4(acc[4 * m + 1], a.y, b);
-            fma4(acc[4 * m + 2], a.z, b);
-            fma4(acc[4 * m + 3], a.w, b);
-        }
-    }
-}
-
-// A (strict lower, times beta_i) and, when `score`, P (lower with the
-// diagonal) in one pass over the key channels, four channels per step,
-// sharing each pair's decay factor.  Thread t owns rows i = ti + 16 r and
-// columns j = tj + 16 s (r, s < 4): pairs with s > r lie above the diagonal
-// for every thread and are skipped at compile time; pairs with s == r that lie
-// above the diagonal take a zero exponent (their value is masked on store).
-template <int K, int LDK, int LDC>
-__device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs, const float* Gk,
-                                               const float* bs, float* Au, float* Pm, bool score) {
-    const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
-    float a[4][4], p[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < 4; ++s) a[r][s] = p[r][s] = 0.f;
-    for (int c = 0; c < K; c += 4) {
-        float gi[4][4], ki[4][4], qi[4][4], gj[4][4], kj[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 g4 = ld4(Gk + (ti + 16 * r) * LDK + c);
-            const float4 k4 = ld4(Ks + (ti + 16 * r) * LDK + c);
-            const float4 q4 = ld4(Qs + (ti + 16 * r) * LDK + c);
-            const float4 h4 = ld4(Gk + (tj + 16 * r) * LDK + c);
-            const float4 l4 = ld4(Ks + (tj + 16 * r) * LDK + c);
-            gi[r][0] = g4.x; gi[r][1] = g4.y; gi[r][2] = g4.z; gi[r][3] = g4.w;
-            ki[r][0] = k4.x; ki[r][1] = k4.y; ki[r][2] = k4.z; ki[r][3] = k4.w;
-            qi[r][0] = q4.x; qi[r][1] = q4.y; qi[r][2] = q4.z; qi[r][3] = q4.w;
-            gj[r][0] = h4.x; gj[r][1] = h4.y; gj[r][2] = h4.z; gj[r][3] = h4.w;
-            kj[r][0] = l4.x; kj[r][1] = l4.y; kj[r][2] = l4.z; kj[r][3] = l4.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int s = 0; s <= r; ++s) {
-                    // s < r: j < i for every thread; s == r: j <= i only when tj <= ti
-                    const bool below = s < r || tj <= ti;
-                    const float ke = kj[s][e] * __expf(below ? gi[r][e] - gj[s][e] : 0.f);
-                    a[r][s] = fmaf(ki[r][e], ke, a[r][s]);
-                    p[r][s] = fmaf(qi[r][e], ke, p[r][s]);
-                }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const int i = ti + 16 * r, j = tj + 16 * s;
-            Au[i * LDC + j] = (j < i) ? bs[i] * a[r][s] : 0.f;
-            if (score) Pm[i * LDC + j] = (j <= i) ? p[r][s] : 0.f;
-        }
-}
-
-template <int K>
-__global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p) {
+__global__ void __launch_bounds__(kThreads, 1) gdn_kda_chunk_kernel(const FwdArgs p) {
     using L = KdaSmem<K>;
     constexpr int LDK = L::LDK;
     constexpr int LDC = L::LDC;
@@ -217,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
     float* gn = Gn + K;          // exp(G_n)
 
     const bool with_out = p.out != nullptr;
+    const long long slot_base = chunk_slot_base(p.cu_seqlens, n, p.T);
     const long long state_off = (static_cast<long long>(n) * H + h) * K * V + vs * kVs;
     for (int e = threadIdx.x; e < K * kVs / 4; e += blockDim.x) {
         const int i = e / (kVs / 4), j = (e % (kVs / 4)) * 4;
@@ -228,11 +100,25 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
 
     for (int c0 = t0; c0 < t1; c0 += kChunk) {
         const int nv = min(kChunk, t1 - c0);
+        const long long slot = (slot_base + (c0 - t0) / kChunk) * H + h;
+        const float* tp = p.chunk_tp ? p.chunk_tp + slot * kKdaTpFloats : nullptr;
         __syncthreads();
+        if (p.chunk_states) {
+            // the state this chunk starts from, fp32 [slot][H][d_k][d_v]
+            float* dst = p.chunk_states + slot * K * V + vs * kVs;
+            for (int e = threadIdx.x; e < K * kVs / 4; e += blockDim.x) {
+                const int i = e / (kVs / 4), j = (e % (kVs / 4)) * 4;
+                st4(dst + static_cast<long long>(i) * V + j, ld4(Ss + i * LDC + j));
+            }
+        }
         load_rows_bf16<K, LDK>(p.k, row_base + c0, H, h, K, 0, nv, Ks);
         if (with_out) load_rows_bf16<K, LDK>(p.q, row_base + c0, H, h, K, 0, nv, Qs);
         load_rows_bf16<kVs, LDC>(p.v, row_base + c0, H, h, V, vs * kVs, nv, Vt);
         load_rows_f32<K, LDK>(p.g, row_base + c0, H, h, nv, Gk);
+        if (tp) {
+            load_tile64<LDC>(tp, Tm);
+            if (with_out) load_tile64<LDC>(tp + 64 * 64, Pm);
+        }
         if (threadIdx.x < 64) {
             const int r = threadIdx.x;
             bs[r] = (r < nv) ? bf16_to_f32(p.beta[(row_base + c0 + r) * H + h]) : 0.f;
@@ -240,18 +126,11 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
         __syncthreads();
         // running sum of the gate per channel (rows >= nv add 0, so G_n is
         // the running sum at the chunk's last token)
-        for (int c = threadIdx.x; c < K; c += blockDim.x) {
-            float s = 0.f;
-            for (int i = 0; i < 64; ++i) {
-                s += Gk[i * LDK + c];
-                Gk[i * LDK + c] = s;
-            }
-            Gn[c] = s;
-            gn[c] = expf(s);
+        chunk_gate_cumsum<K, LDK>(Gk, Gn, gn);
+        if (!tp) {
+            gram_and_score<K, LDK, LDC>(Ks, Qs, Gk, bs, Au, Pm, with_out);
+            __syncthreads();
         }
-        __syncthreads();
-        gram_and_score<K, LDK, LDC>(Ks, Qs, Gk, bs, Au, Pm, with_out);
-        __syncthreads();
         // the decayed operands, in place: exp(G) o k, exp(G) o q, exp(G_n - G) o k
         for (int e = threadIdx.x; e < 64 * K; e += blockDim.x) {
             const int i = e / K, c = e % K;
@@ -278,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
             }
         }
         __syncthreads();
-        chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
+        if (!tp) chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
         {
             // Delta = T R
             float acc[4][4] = {};
@@ -333,6 +212,70 @@ __global__ void __launch_bounds__(kThreads) gdn_kda_chunk_kernel(const FwdArgs p
     }
 }
 
+// T = (I + A)^-1 and the causal score P of one chunk (one block per chunk,
+// head and sequence), written to the per-chunk workspace as two row-major
+// 64 x 64 fp32 tiles.  The same steps as the walk's own gram and inverse, so
+// both routes give the same T and P bit for bit.
+template <int K>
+struct KdaTpSmem {
+    static constexpr int LDK = K + 4;
+    static constexpr int LDC = kChunk + 4;
+    static constexpr size_t kBytes = sizeof(float) * (64 * LDK * 3 + 64 * LDC * 3 + 64);
+};
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs p) {
+    using L = KdaTpSmem<K>;
+    constexpr int LDK = L::LDK;
+    constexpr int LDC = L::LDC;
+    const int ci = blockIdx.x;
+    const int h = blockIdx.y;
+    const int n = blockIdx.z;
+    const int H = p.H;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+    const int c0 = t0 + ci * kChunk;
+    if (c0 >= t1) return;
+    const int nv = min(kChunk, t1 - c0);
+
+    extern __shared__ __align__(16) float sm[];
+    float* Ks = sm;             // k; then scratch of the inverse
+    float* Qs = Ks + 64 * LDK;  // q
+    float* Gk = Qs + 64 * LDK;  // g; then G
+    float* Au = Gk + 64 * LDK;  // A
+    float* Pm = Au + 64 * LDC;  // P
+    float* Tm = Pm + 64 * LDC;  // T
+    float* bs = Tm + 64 * LDC;
+
+    const long long row0 = static_cast<long long>(b) * p.T + c0;
+    load_rows_bf16<K, LDK>(p.k, row0, H, h, K, 0, nv, Ks);
+    load_rows_bf16<K, LDK>(p.q, row0, H, h, K, 0, nv, Qs);
+    load_rows_f32<K, LDK>(p.g, row0, H, h, nv, Gk);
+    if (threadIdx.x < 64) {
+        const int r = threadIdx.x;
+        bs[r] = (r < nv) ? bf16_to_f32(p.beta[(row0 + r) * H + h]) : 0.f;
+    }
+    __syncthreads();
+    chunk_gate_cumsum<K, LDK>(Gk, nullptr, nullptr);
+    gram_and_score<K, LDK, LDC>(Ks, Qs, Gk, bs, Au, Pm, true);
+    __syncthreads();
+    chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
+    float* dst = p.chunk_tp + ((chunk_slot_base(p.cu_seqlens, n, p.T) + ci) * H + h) * kKdaTpFloats;
+    store_tile64<LDC>(Tm, dst);
+    store_tile64<LDC>(Pm, dst + 64 * 64);
+}
+
+template <int K>
+cudaError_t launch_kda_tp_k(const KdaTpArgs& a, cudaStream_t stream) {
+    const size_t smem = KdaTpSmem<K>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(gdn_kda_tp_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.max_chunks, a.H, a.N);
+    gdn_kda_tp_kernel<K><<<grid, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int K>
 cudaError_t launch_kda_chunk_k(const FwdArgs& a, cudaStream_t stream) {
     const size_t smem = KdaSmem<K>::kBytes;
@@ -349,6 +292,11 @@ cudaError_t launch_kda_chunk_k(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_kda_chunk(const FwdArgs& a, cudaStream_t stream) {
     if (a.d_k == 64) return launch_kda_chunk_k<64>(a, stream);
     return launch_kda_chunk_k<128>(a, stream);
+}
+
+cudaError_t launch_kda_tp(const KdaTpArgs& a, cudaStream_t stream) {
+    if (a.d_k == 64) return launch_kda_tp_k<64>(a, stream);
+    return launch_kda_tp_k<128>(a, stream);
 }
 
 }  // namespace gdn

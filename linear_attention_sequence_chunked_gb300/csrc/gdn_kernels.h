@@ -19,8 +19,11 @@ struct FwdArgs {
     uint16_t* out;          // may be null: skip the output
     float* final_state;     // may be null
     float* chunk_states;    // may be null: per-chunk start states, bf16 hi/lo operand tiles
-                            // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v])
+                            // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v]);
+                            // plain fp32 [slot][H][d_k][d_v] for the per-channel-gate walk
     const uint8_t* chunk_T; // may be null: per-chunk T operand tiles [slot][H][2 x 8 KB], read
+    const float* chunk_tp;  // may be null (per-channel-gate walk): per-chunk T and P, fp32
+                            // [slot][H][2][64][64], read
     int N;                  // sequences (B dense, or cu_seqlens length - 1)
     int T;                  // tokens per batch row (dense) / total tokens (packed)
     int H;
@@ -107,8 +110,65 @@ cudaError_t launch_bwd_local(const BwdLocalArgs& a, cudaStream_t stream);
 
 // Chunked forward of the per-channel-gate variant (g is (.., H, d_k)), fp32 on
 // the CUDA cores; uses q, k, v, g, beta, scale, initial_state, cu_seqlens,
-// out, final_state and the sizes of FwdArgs (not chunk_states or chunk_T).
+// out (may be null), final_state, chunk_states, chunk_tp and the sizes of
+// FwdArgs (not chunk_T).  Without chunk_tp each chunk's T and P are formed in
+// the walk.
 cudaError_t launch_kda_chunk(const FwdArgs& a, cudaStream_t stream);
+
+// T and P of every chunk of the per-channel-gate variant (chunk-parallel).
+struct KdaTpArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const float* g;               // (.., H, d_k)
+    const uint16_t* beta;
+    const int32_t* cu_seqlens;
+    float* chunk_tp;              // [slot][H][2][64][64]
+    int N;
+    int T;
+    int H;
+    int d_k;
+    int max_chunks;               // chunks of the longest sequence (grid.x)
+    int* err;
+};
+
+cudaError_t launch_kda_tp(const KdaTpArgs& a, cudaStream_t stream);
+
+// Floats of one chunk's T and P in the per-chunk workspace (T, then P).
+constexpr int kKdaTpFloats = 2 * 64 * 64;
+
+// Backward of the per-channel-gate variant: the reverse state-gradient walk
+// (one block per 64 value columns, head and sequence) and the chunk-parallel
+// local gradients (one block per chunk, head and sequence).
+struct KdaBwdArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const float* g;               // (.., H, d_k)
+    const uint16_t* beta;
+    const uint16_t* d_out;
+    float scale;
+    const int32_t* cu_seqlens;
+    const float* d_final_state;   // may be null (zeros)
+    const float* chunk_tp;        // [slot][H][2][64][64]: T, P
+    const float* chunk_states;    // [slot][H][d_k][d_v]: start state of each chunk
+    float* chunk_dstates;         // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
+    float* d_initial_state;       // may be null
+    uint16_t* dq;
+    uint16_t* dk;
+    uint16_t* dv;
+    float* dg;                    // (.., H, d_k)
+    uint16_t* dbeta;
+    int N;
+    int T;
+    int H;
+    int d_k;
+    int d_v;
+    int max_chunks;
+    int* err;
+};
+
+cudaError_t launch_kda_bwd_chain(const KdaBwdArgs& a, cudaStream_t stream);
+cudaError_t launch_kda_bwd_local(const KdaBwdArgs& a, cudaStream_t stream);
 
 // Token-serial forward (decode path; the same recurrence token by token).
 struct RecurrentArgs {

@@ -72,8 +72,14 @@ def load():
         lib.gdn_recurrent_fwd.restype = i
         lib.gdn_kda_recurrent_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
         lib.gdn_kda_recurrent_fwd.restype = i
-        lib.gdn_kda_chunk_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp]
+        lib.gdn_kda_chunk_fwd_workspace_size.argtypes = [i] * 6
+        lib.gdn_kda_chunk_fwd_workspace_size.restype = sz
+        lib.gdn_kda_chunk_fwd.argtypes = [vp] * 5 + [f] + [vp] * 4 + [i] * 5 + [vp, sz, vp]
         lib.gdn_kda_chunk_fwd.restype = i
+        lib.gdn_kda_chunk_bwd_workspace_size.argtypes = [i] * 6
+        lib.gdn_kda_chunk_bwd_workspace_size.restype = sz
+        lib.gdn_kda_chunk_bwd.argtypes = [vp] * 5 + [f] + [vp] * 10 + [i] * 5 + [vp, sz, vp]
+        lib.gdn_kda_chunk_bwd.restype = i
         lib.gdn_prologue_fwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 4 + [i] * 3 + [vp]
         lib.gdn_prologue_fwd.restype = i
         lib.gdn_prologue_bwd.argtypes = [vp] * 6 + [i, f, f] + [vp] * 10 + [i] * 3 + [vp]
@@ -252,18 +258,39 @@ def gdn_kda_recurrent_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, ou
     _check(st, "gdn_kda_recurrent_fwd")
 
 
+def gdn_kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
+def gdn_kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v, varlen) -> int:
+    return int(load().gdn_kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v, int(bool(varlen))))
+
+
 def gdn_kda_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
-                      B, T, H, d_k, d_v, stream=None):
+                      B, T, H, d_k, d_v, workspace=None, workspace_bytes=0, stream=None):
     st = load().gdn_kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                                   _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
-                                  _ptr(final_state), B, T, H, d_k, d_v, _stream(stream))
+                                  _ptr(final_state), B, T, H, d_k, d_v, _ptr(workspace),
+                                  int(workspace_bytes), _stream(stream))
     _check(st, "gdn_kda_chunk_fwd")
 
 
+def gdn_kda_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
+                      dq, dk, dv, dg, dbeta, d_initial_state, B, T, H, d_k, d_v,
+                      workspace=None, workspace_bytes=0, stream=None):
+    st = load().gdn_kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                  _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out),
+                                  _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                  _ptr(dbeta), _ptr(d_initial_state), B, T, H, d_k, d_v,
+                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "gdn_kda_chunk_bwd")
+
+
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None, stream=None):
-    """Allocate out and the final state and run gdn_kda_chunk_fwd: q, k
-    (B, T, H, d_k) bf16; v (B, T, H, d_v) bf16; g (B, T, H, d_k) fp32 (one log
-    decay per key channel); beta (B, T, H) bf16.  Returns (out, final_state)."""
+    """Allocate out, the final state and the per-chunk workspace and run
+    gdn_kda_chunk_fwd: q, k (B, T, H, d_k) bf16; v (B, T, H, d_v) bf16;
+    g (B, T, H, d_k) fp32 (one log decay per key channel); beta (B, T, H)
+    bf16.  Returns (out, final_state)."""
     import torch
     _validate(q, k, v, g, beta, initial_state, cu_seqlens, per_channel_gate=True)
     B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
@@ -271,8 +298,37 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
         scale = d_k ** -0.5
     out = torch.empty(v.shape, dtype=torch.bfloat16, device=v.device)
     fs = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=v.device)
-    gdn_kda_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs, B, T, H, d_k, d_v, stream)
+    nbytes = gdn_kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+    ws = _workspace(nbytes, v.device)
+    gdn_kda_chunk_fwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, out, fs, B, T, H, d_k, d_v,
+                      ws, nbytes, stream)
     return out, fs
+
+
+def chunk_kda_bwd(q, k, v, g, beta, d_out, scale=None, initial_state=None, cu_seqlens=None,
+                  d_final_state=None, stream=None):
+    """Allocate gradients and the workspace and run gdn_kda_chunk_bwd (the
+    per-channel-gate backward).  Returns a dict of dq, dk, dv, dg (per key
+    channel, fp32), dbeta and d_initial_state."""
+    import torch
+    _validate(q, k, v, g, beta, initial_state, cu_seqlens, d_out=d_out, d_final_state=d_final_state,
+              per_channel_gate=True)
+    B, T, H, d_k, d_v = _dims(q, v, cu_seqlens)
+    if scale is None:
+        scale = d_k ** -0.5
+    dev = v.device
+    res = dict(dq=torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+               dk=torch.empty(k.shape, dtype=torch.bfloat16, device=dev),
+               dv=torch.empty(v.shape, dtype=torch.bfloat16, device=dev),
+               dg=torch.empty(g.shape, dtype=torch.float32, device=dev),
+               dbeta=torch.empty(beta.shape, dtype=torch.bfloat16, device=dev),
+               d_initial_state=torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=dev))
+    nbytes = gdn_kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v, cu_seqlens is not None)
+    ws = _workspace(nbytes, dev)
+    gdn_kda_chunk_bwd(q, k, v, g, beta, scale, initial_state, cu_seqlens, d_out, d_final_state,
+                      res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"], res["d_initial_state"],
+                      B, T, H, d_k, d_v, ws, nbytes, stream)
+    return res
 
 
 def gdn_prologue_fwd(q_raw, k_raw, a, b, A_log, dt_bias, gate_mode, lower, beta_scale,

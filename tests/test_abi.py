@@ -85,8 +85,38 @@ def test_kda_chunk_host_validation(lib, over, code):
     st = gdn.load().gdn_kda_chunk_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"],
                                        args["scale"], args["initial_state"], args["cu_seqlens"],
                                        args["out"], args["final_state"], args["B"], args["T"],
-                                       args["H"], args["d_k"], args["d_v"], None)
+                                       args["H"], args["d_k"], args["d_v"], None, 0, None)
     assert st == code
+
+
+def test_kda_chunk_workspace(lib):
+    """The per-channel-gate forward's optional workspace is every chunk's T
+    and P in fp32 (32 KB per chunk and head); a misaligned one is refused."""
+    assert gdn.gdn_kda_chunk_fwd_workspace_size(4, 4096, 16, 128, 128, 0) == 4 * 64 * 16 * 32768
+    assert gdn.gdn_kda_chunk_fwd_workspace_size(3, 200, 2, 64, 64, 1) == (200 // 64 + 3) * 2 * 32768
+    assert gdn.gdn_kda_chunk_fwd_workspace_size(1, 64, 1, 96, 64, 0) == 0
+    st = gdn.load().gdn_kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, None, FAKE, None,
+                                       1, 64, 1, 64, 64, FAKE + 16, 1 << 20, None)
+    assert st == 3
+
+
+def test_kda_backward_host_validation(lib):
+    l = gdn.load()
+    B, T, H, K, V = 1, 128, 1, 64, 64
+    need = gdn.gdn_kda_chunk_bwd_workspace_size(B, T, H, K, V, 0)
+    # T and P, the start states and the end-state gradients of every chunk
+    assert need == 2 * (32768 + 2 * 4 * K * V)
+    assert gdn.gdn_kda_chunk_bwd_workspace_size(B, T, H, 96, V, 0) == 0
+
+    def call(ws, ws_bytes, d_k=64, dq=FAKE, g=FAKE):
+        return l.gdn_kda_chunk_bwd(FAKE, FAKE, FAKE, g, FAKE, 1.0, None, None, FAKE, None,
+                                   dq, FAKE, FAKE, FAKE, FAKE, None, B, T, H, d_k, V, ws, ws_bytes, None)
+    assert call(None, 0) == 1                   # workspace missing
+    assert call(FAKE, need - 1) == 1            # workspace too small
+    assert call(FAKE + 16, need) == 3           # workspace not 256-byte aligned
+    assert call(FAKE, need, d_k=32) == 2
+    assert call(FAKE, need, dq=None) == 1
+    assert call(FAKE, need, g=FAKE + 4) == 3
 
 
 def test_backward_host_validation(lib):

@@ -33,7 +33,9 @@ def _case(B, T, H, dk, dv, seed, seqlens=None):
     return q, k, v, g, beta, s0, cu
 
 
-def _run(torch, fn, q, k, v, g, beta, s0, cu, scale):
+def _run(torch, fn, q, k, v, g, beta, s0, cu, scale, tp=False):
+    """One forward call; with tp, gdn_kda_chunk_fwd gets its workspace (every
+    chunk's T and P formed first by the chunk-parallel kernel)."""
     Bd, n_tok, H, dk = q.shape
     dv = v.shape[3]
     d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
@@ -42,8 +44,13 @@ def _run(torch, fn, q, k, v, g, beta, s0, cu, scale):
     out = torch.empty((Bd, n_tok, H, dv), dtype=torch.bfloat16, device="cuda")
     fs = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device="cuda")
     B = n_seq if cu is not None else Bd
+    extra = {}
+    if tp:
+        nbytes = gdn.gdn_kda_chunk_fwd_workspace_size(B, n_tok, H, dk, dv, cu is not None)
+        extra = dict(workspace=torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda"),
+                     workspace_bytes=nbytes)
     fn(bf(q), bf(k), bf(v), d(g), bf(beta), scale, d(s0), None if cu is None else d(cu), out, fs,
-       B, n_tok, H, dk, dv)
+       B, n_tok, H, dk, dv, **extra)
     st = gdn.gdn_get_last_device_error()
     assert st == 0, gdn.gdn_status_string(st)
     torch.cuda.synchronize()
@@ -100,26 +107,44 @@ def _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, scale, what):
         G.compare(S[s], S_ref[s], TOL_STATE_FP32, None, f"{what} state {s}")
 
 
+@pytest.mark.parametrize("tp", [False, True], ids=["walk", "tp"])
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128), (128, 256)])
-def test_kda_chunk_matches_oracle(dk, dv):
-    """Three chunks per sequence, the last one ragged (150 = 2 x 64 + 22)."""
+def test_kda_chunk_matches_oracle(dk, dv, tp):
+    """Three chunks per sequence, the last one ragged (150 = 2 x 64 + 22); the
+    walk that forms T and P itself, and the route that reads them from the
+    chunk-parallel kernel's workspace."""
     import torch
     q, k, v, g, beta, s0, cu = _case(2, 150, 2, dk, dv, seed=100 + dk + dv)
     scale = dk ** -0.5
-    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, scale)
+    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, scale, tp=tp)
     _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, scale, "kda chunk")
 
 
-def test_kda_chunk_varlen_matches_oracle():
+@pytest.mark.parametrize("tp", [False, True], ids=["walk", "tp"])
+def test_kda_chunk_varlen_matches_oracle(tp):
     """Packed sequences of 1, 63, 64, 65, 0 and 200 tokens: resets at every
     boundary, chunks never straddle sequences, an empty sequence passes its
     initial state through unchanged."""
     import torch
     lens = [1, 63, 64, 65, 0, 200]
     q, k, v, g, beta, s0, cu = _case(1, 0, 2, 128, 64, seed=12, seqlens=lens)
-    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1)
+    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1, tp=tp)
     _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, 0.1, "kda chunk varlen")
     assert np.array_equal(S[4], s0[4])
+
+
+@pytest.mark.parametrize("dk,dv,lens", [(128, 128, None), (64, 256, None), (128, 64, [1, 63, 64, 65, 0, 200])])
+def test_kda_chunk_tp_route_is_bitwise_the_walk(dk, dv, lens):
+    """T and P from the chunk-parallel kernel are the walk's own (same steps,
+    same order), so the two routes agree bit for bit."""
+    import torch
+    if lens is None:
+        q, k, v, g, beta, s0, cu = _case(2, 200, 2, dk, dv, seed=31 + dk)
+    else:
+        q, k, v, g, beta, s0, cu = _case(1, 0, 2, dk, dv, seed=32, seqlens=lens)
+    o1, S1 = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1)
+    o2, S2 = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1, tp=True)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
 
 
 def test_kda_chunk_strong_per_channel_decay():
@@ -168,3 +193,152 @@ def test_kda_chunk_long_sequence_sampled_heads():
     torch.cuda.synchronize()
     _check_against_oracle(G.bf16_to_np(out), fs.cpu().numpy(), q, k, v, g, beta, s0, cu, 128 ** -0.5,
                           "kda chunk T=4096")
+
+
+# ---------------------------------------------------------------------------
+# the chunked backward (gdn_kda_chunk_bwd)
+# ---------------------------------------------------------------------------
+
+TOL_DG_FP32 = 1e-3    # dg: fp32 output, a reverse running sum of cancelling terms
+TOL_DS0_FP32 = 1e-4   # d_initial_state: fp32 output of the reverse state walk
+
+
+def _bwd_case(B, T, H, dk, dv, seed, seqlens=None, with_states=True):
+    q, k, v, g, beta, s0, cu = _case(B, T, H, dk, dv, seed, seqlens)
+    rng = np.random.default_rng(seed + 1000)
+    dO = W.f32_to_bf16_bits(rng.standard_normal(v.shape).astype(np.float32))
+    dfs = (rng.standard_normal(s0.shape) * 0.1).astype(np.float32) if with_states else None
+    return q, k, v, g, beta, (s0 if with_states else None), cu, dO, dfs
+
+
+def _run_bwd(torch, q, k, v, g, beta, s0, cu, scale, dO, dfs):
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+    bf = lambda x: d(x.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    r = gdn.chunk_kda_bwd(bf(q), bf(k), bf(v), d(g), bf(beta), bf(dO), scale=scale,
+                          initial_state=None if s0 is None else d(s0),
+                          cu_seqlens=None if cu is None else d(cu),
+                          d_final_state=None if dfs is None else d(dfs))
+    st = gdn.gdn_get_last_device_error()
+    assert st == 0, gdn.gdn_status_string(st)
+    torch.cuda.synchronize()
+    res = {n: G.bf16_to_np(r[n]) for n in ("dq", "dk", "dv", "dbeta")}
+    res["dg"] = r["dg"].cpu().numpy()
+    res["dS0"] = r["d_initial_state"].cpu().numpy()
+    return res
+
+
+def _bounds(q, cu):
+    if cu is None:
+        return [(b, 0, q.shape[1]) for b in range(q.shape[0])]
+    return [(0, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)]
+
+
+def _bwd_ref(q, k, v, g, beta, s0, cu, scale, dO, dfs, fn=kda.kda_chunk_bwd_head):
+    f = W.bf16_bits_to_f32
+    qf, kf, vf, bt, dOf = f(q), f(k), f(v), f(beta), f(dO)
+    H = q.shape[2]
+    out = dict(dq=np.zeros(q.shape), dk=np.zeros(k.shape), dv=np.zeros(v.shape), dg=np.zeros(g.shape),
+               dbeta=np.zeros(beta.shape), dS0=np.zeros((len(_bounds(q, cu)), H, q.shape[3], v.shape[3])))
+    for s, (b, t0, t1) in enumerate(_bounds(q, cu)):
+        for h in range(H):
+            r = fn(qf[b, t0:t1, h], kf[b, t0:t1, h], vf[b, t0:t1, h], g[b, t0:t1, h], bt[b, t0:t1, h], scale,
+                   None if s0 is None else s0[s, h], dOf[b, t0:t1, h], None if dfs is None else dfs[s, h])
+            for n in ("dq", "dk", "dv", "dg", "dbeta"):
+                out[n][b, t0:t1, h] = r[n]
+            out["dS0"][s, h] = r["dS0"]
+    return out
+
+
+def _check_bwd(res, ref, q, cu, what, k=None):
+    """Per (sequence, head): the bf16 gradients within the gradient tolerance,
+    dg and d_initial_state within their fp32 ones.  With k given, dg is
+    measured against the size of the terms whose sum it is, q o dq + k o dk,
+    instead of its own size: under very strong decay those terms cancel to
+    ~1e-9 and only fp32 rounding of the O(1) terms is left (the oracle is
+    fp64)."""
+    f = W.bf16_bits_to_f32
+    for s, (b, t0, t1) in enumerate(_bounds(q, cu)):
+        for h in range(q.shape[2]):
+            if t1 > t0:
+                for n in ("dq", "dk", "dv", "dbeta"):
+                    G.compare(res[n][b, t0:t1, h], ref[n][b, t0:t1, h], G.TOL_RMS_GRAD, None,
+                              f"{what} {n} s{s} h{h}")
+                if k is None:
+                    G.compare(res["dg"][b, t0:t1, h], ref["dg"][b, t0:t1, h], TOL_DG_FP32, None,
+                              f"{what} dg s{s} h{h}")
+                else:
+                    terms = (np.abs(f(q[b, t0:t1, h]) * ref["dq"][b, t0:t1, h])
+                             + np.abs(f(k[b, t0:t1, h]) * ref["dk"][b, t0:t1, h]))
+                    err = np.linalg.norm(res["dg"][b, t0:t1, h] - ref["dg"][b, t0:t1, h]) / np.linalg.norm(terms)
+                    assert err <= TOL_DG_FP32, f"{what} dg s{s} h{h}: {err:.3e} of the terms' norm"
+            G.compare(res["dS0"][s, h], ref["dS0"][s, h], TOL_DS0_FP32, None, f"{what} dS0 s{s} h{h}")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128), (128, 256)])
+def test_kda_chunk_bwd_matches_oracle(dk, dv):
+    """Every gradient against the fp64 reverse mode of the chunk algebra:
+    three chunks per sequence with a ragged tail, initial state and an
+    upstream gradient on the final state."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(2, 150, 2, dk, dv, seed=200 + dk + dv)
+    scale = dk ** -0.5
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, scale, dO, dfs)
+    _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, scale, dO, dfs), q, cu, "kda bwd")
+
+
+def test_kda_chunk_bwd_matches_token_loop_reverse_mode():
+    """The same gradients against the reverse mode of the token-by-token
+    recurrence (a formulation with no chunk algebra at all)."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(1, 100, 2, 64, 64, seed=210)
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 0.125, dO, dfs)
+    ref = _bwd_ref(q, k, v, g, beta, s0, cu, 0.125, dO, dfs, fn=kda.kda_bwd_head)
+    _check_bwd(res, ref, q, cu, "kda bwd vs token loop")
+
+
+def test_kda_chunk_bwd_varlen():
+    """Packed sequences of 1, 63, 64, 65, 0 and 130 tokens: the empty one
+    hands its final-state gradient to its initial state unchanged."""
+    import torch
+    lens = [1, 63, 64, 65, 0, 130]
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(1, 0, 2, 128, 64, seed=211, seqlens=lens)
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 0.1, dO, dfs)
+    _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, 0.1, dO, dfs), q, cu, "kda bwd varlen")
+    assert np.array_equal(res["dS0"][4], dfs[4])
+
+
+def test_kda_chunk_bwd_without_states_and_exact_chunks():
+    """No initial state, no final-state gradient, T a multiple of 64."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(2, 128, 2, 128, 128, seed=212, with_states=False)
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs)
+    _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs), q, cu, "kda bwd no states")
+
+
+def test_kda_chunk_bwd_strong_decay_and_repeats_bitwise():
+    """Per-channel log decays down to -40 per token stay finite; a second
+    call gives the same bits (every sum in a fixed order)."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(1, 200, 2, 128, 128, seed=213)
+    g = (g * 8.0).astype(np.float32)
+    r1 = _run_bwd(torch, q, k, v, g, beta, s0, cu, 0.09, dO, dfs)
+    r2 = _run_bwd(torch, q, k, v, g, beta, s0, cu, 0.09, dO, dfs)
+    for n in r1:
+        assert np.isfinite(r1[n]).all(), n
+        assert np.array_equal(r1[n], r2[n]), n
+    _check_bwd(r1, _bwd_ref(q, k, v, g, beta, s0, cu, 0.09, dO, dfs), q, cu, "kda bwd strong decay", k=k)
+
+
+def test_kda_chunk_bwd_zero_length():
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(2, 0, 2, 64, 64, seed=214)
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 0.125, dO, dfs)
+    assert np.array_equal(res["dS0"], dfs)
+
+
+def test_kda_chunk_bwd_long_sequence():
+    """T = 4096 (64 chunks through both walks), d_k = d_v = 128."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(1, 4096, 1, 128, 128, seed=215)
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs)
+    _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs), q, cu, "kda bwd T=4096")
