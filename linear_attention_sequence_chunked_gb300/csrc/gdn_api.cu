@@ -195,12 +195,24 @@ size_t kda_tp_bytes(int B, int T, int H, int varlen) {
     return round_up(sizeof(float) * gdn::kKdaTpFloats * chunk_slots(B, T, varlen) * H);
 }
 
-// T and P of every chunk into `tp` (chunk-parallel kernel).
+// Operand blocks of the tensor-core walk (d_k = 128), 129 KB per chunk and head.
+size_t kda_blocks_bytes(int B, int T, int H, int varlen) {
+    return round_up(static_cast<size_t>(gdn::kKdaBlkBytes) * chunk_slots(B, T, varlen) * H);
+}
+
+// The per-channel-gate forward's workspace: the walk's operand blocks
+// (d_k = 128) or fp32 T and P (d_k = 64).
+size_t kda_fwd_ws_bytes(int B, int T, int H, int d_k, int varlen) {
+    return d_k == 128 ? kda_blocks_bytes(B, T, H, varlen) : kda_tp_bytes(B, T, H, varlen);
+}
+
+// T and P of every chunk into `tp` (fp32) and / or the walk's operand blocks
+// into `tiles` (chunk-parallel kernel).
 bool launch_kda_tp_pass(const gdn_bf16* q, const gdn_bf16* k, const float* g, const gdn_bf16* beta,
-                        const int32_t* cu_seqlens, float* tp, int B, int T, int H, int d_k, int* err,
-                        cudaStream_t stream) {
+                        const int32_t* cu_seqlens, float* tp, uint8_t* tiles, int B, int T, int H, int d_k,
+                        int* err, cudaStream_t stream) {
     gdn::KdaTpArgs t{};
-    t.q = q; t.k = k; t.g = g; t.beta = beta; t.cu_seqlens = cu_seqlens; t.chunk_tp = tp;
+    t.q = q; t.k = k; t.g = g; t.beta = beta; t.cu_seqlens = cu_seqlens; t.chunk_tp = tp; t.tiles = tiles;
     t.N = B; t.T = T; t.H = H; t.d_k = d_k; t.err = err;
     t.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
     if (t.max_chunks == 0) return true;
@@ -380,7 +392,7 @@ gdn_status gdn_kda_recurrent_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn
 
 size_t gdn_kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v, int varlen) {
     if (check_shapes(B, T, H, d_k, d_v) != GDN_OK) return 0;
-    return kda_tp_bytes(B, T, H, varlen);
+    return kda_fwd_ws_bytes(B, T, H, d_k, varlen);
 }
 
 gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
@@ -393,12 +405,26 @@ gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return GDN_ERR_MISALIGNED;
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
-    // With a workspace, every chunk's T and P come first from the
-    // chunk-parallel kernel and the walk loads them; without one, the walk
-    // forms them itself.
-    const size_t tb = kda_tp_bytes(B, T, H, cu_seqlens != nullptr);
-    float* tp = (workspace && workspace_bytes >= tb && tb > 0) ? static_cast<float*>(workspace) : nullptr;
-    if (tp && !launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
+    // With a workspace, every chunk's T and P (and at d_k = 128 the decayed
+    // operands) come first from the chunk-parallel kernel: d_k = 128 then runs
+    // the tensor-core walk over the operand blocks, d_k = 64 the CUDA-core walk
+    // reading T and P.  Without one, the CUDA-core walk forms them itself.
+    const size_t need = kda_fwd_ws_bytes(B, T, H, d_k, cu_seqlens != nullptr);
+    const bool fast = workspace && workspace_bytes >= need && need > 0;
+    if (fast && d_k == 128) {
+        uint8_t* tiles = static_cast<uint8_t*>(workspace);
+        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, nullptr, tiles, B, T, H, d_k, err, stream))
+            return GDN_ERR_CUDA;
+        gdn::KdaWalkArgs w{};
+        w.v = v; w.tiles = tiles; w.scale = scale; w.initial_state = initial_state; w.cu_seqlens = cu_seqlens;
+        w.out = out; w.final_state = final_state; w.chunk_states = nullptr;
+        w.N = B; w.T = T; w.H = H; w.d_v = d_v; w.err = err;
+        if (!launched(gdn::launch_kda_walk(w, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    float* tp = fast ? static_cast<float*>(workspace) : nullptr;
+    if (tp && !launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, nullptr, B, T, H, d_k, err, stream))
+        return GDN_ERR_CUDA;
     gdn::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.initial_state = initial_state; a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
@@ -434,7 +460,8 @@ gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     const int max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
     if (max_chunks > 0) {
         // T and P of every chunk, then the forward walk recording each chunk's start state
-        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, B, T, H, d_k, err, stream)) return GDN_ERR_CUDA;
+        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, nullptr, B, T, H, d_k, err, stream))
+            return GDN_ERR_CUDA;
         gdn::FwdArgs f{};
         f.q = q; f.k = k; f.v = v; f.g = g; f.beta = beta; f.scale = scale;
         f.initial_state = initial_state; f.cu_seqlens = cu_seqlens;

@@ -39,6 +39,7 @@
 #include "gdn_common.cuh"
 #include "gdn_kda_common.cuh"
 #include "gdn_kernels.h"
+#include "gdn_tc_common.cuh"
 
 namespace gdn {
 
@@ -223,6 +224,45 @@ struct KdaTpSmem {
     static constexpr size_t kBytes = sizeof(float) * (64 * LDK * 3 + 64 * LDC * 3 + 64);
 };
 
+// The decayed operands exp(G) o k, exp(G) o q, exp(G_n - G) o k of a chunk as
+// bf16 hi/lo tiles of the tensor-core walk's operand block, and its vectors
+// exp(G_n), beta (d_k = 128).
+template <int K, int LDK>
+__device__ __forceinline__ void write_decayed_operands(uint8_t* blk, const float* Ks, const float* Qs,
+                                                       const float* Gk, const float* bs) {
+    for (int e = threadIdx.x; e < 64 * (K / 8); e += blockDim.x) {
+        const int i = e / (K / 8), ch = e % (K / 8);
+        const int region = ch >> 3;
+        float kg[8], qg[8], kt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = 8 * ch + j;
+            const float G = Gk[i * LDK + c];
+            const float kv = Ks[i * LDK + c];
+            const float eg = expf(G);
+            kg[j] = kv * eg;
+            qg[j] = Qs[i * LDK + c] * eg;
+            kt[j] = kv * expf(Gk[63 * LDK + c] - G);
+        }
+        uint8_t* r = blk + region * 8192;
+        tc::store_split_chunk(r + kKdaBlkKG, r + kKdaBlkKG + 16384, i, ch & 7, kg);
+        tc::store_split_chunk(r + kKdaBlkQG, r + kKdaBlkQG + 16384, i, ch & 7, qg);
+        tc::store_split_chunk(r + kKdaBlkKt, r + kKdaBlkKt + 16384, i, ch & 7, kt);
+    }
+    float* vec = reinterpret_cast<float*>(blk + kKdaBlkVec);
+    for (int c = threadIdx.x; c < K; c += blockDim.x) vec[c] = expf(Gk[63 * LDK + c]);
+    if (threadIdx.x < 64) vec[K + threadIdx.x] = bs[threadIdx.x];
+}
+
+// A 64 x 64 shared tile (row stride LD) as a bf16 hi/lo operand tile pair.
+template <int LD>
+__device__ __forceinline__ void write_split_tile64(uint8_t* hi, uint8_t* lo, const float* src) {
+    for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
+        const int i = e >> 3, ch = e & 7;
+        tc::store_split_chunk(hi, lo, i, ch, src + i * LD + 8 * ch);
+    }
+}
+
 template <int K>
 __global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs p) {
     using L = KdaTpSmem<K>;
@@ -258,11 +298,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs
     __syncthreads();
     chunk_gate_cumsum<K, LDK>(Gk, nullptr, nullptr);
     gram_and_score<K, LDK, LDC>(Ks, Qs, Gk, bs, Au, Pm, true);
+    const long long slot = (chunk_slot_base(p.cu_seqlens, n, p.T) + ci) * H + h;
+    uint8_t* blk = nullptr;
+    if constexpr (K == 128) {
+        if (p.tiles) {
+            blk = p.tiles + slot * kKdaBlkBytes;
+            write_decayed_operands<K, LDK>(blk, Ks, Qs, Gk, bs);
+        }
+    }
     __syncthreads();
     chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
-    float* dst = p.chunk_tp + ((chunk_slot_base(p.cu_seqlens, n, p.T) + ci) * H + h) * kKdaTpFloats;
-    store_tile64<LDC>(Tm, dst);
-    store_tile64<LDC>(Pm, dst + 64 * 64);
+    if (p.chunk_tp) {
+        float* dst = p.chunk_tp + slot * kKdaTpFloats;
+        store_tile64<LDC>(Tm, dst);
+        store_tile64<LDC>(Pm, dst + 64 * 64);
+    }
+    if (blk) {
+        write_split_tile64<LDC>(blk + kKdaBlkT, blk + kKdaBlkT + 8192, Tm);
+        write_split_tile64<LDC>(blk + kKdaBlkP, blk + kKdaBlkP + 8192, Pm);
+    }
 }
 
 template <int K>

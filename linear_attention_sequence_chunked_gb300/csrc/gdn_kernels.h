@@ -122,7 +122,9 @@ struct KdaTpArgs {
     const float* g;               // (.., H, d_k)
     const uint16_t* beta;
     const int32_t* cu_seqlens;
-    float* chunk_tp;              // [slot][H][2][64][64]
+    float* chunk_tp;              // may be null: [slot][H][2][64][64] fp32 T, P
+    uint8_t* tiles;               // may be null (d_k = 128 only): [slot][H] operand blocks of the
+                                  // tensor-core walk (layout below)
     int N;
     int T;
     int H;
@@ -132,6 +134,38 @@ struct KdaTpArgs {
 };
 
 cudaError_t launch_kda_tp(const KdaTpArgs& a, cudaStream_t stream);
+
+// Per-chunk operand block of the tensor-core per-channel-gate walk (d_k = 128),
+// in the byte layout of its shared memory: bf16 hi/lo tiles, rows of 128 bytes
+// swizzled in 1024-byte atoms; a d_k-wide tile is two 64-channel regions of 8 KB.
+constexpr int kKdaBlkKG = 0;          // exp(G) o k          hi (16 KB), lo (16 KB); rows = tokens
+constexpr int kKdaBlkQG = 32768;      // exp(G) o q
+constexpr int kKdaBlkKt = 65536;      // exp(G_n - G) o k
+constexpr int kKdaBlkT = 98304;       // T                   hi (8 KB), lo (8 KB)
+constexpr int kKdaBlkP = 114688;      // P
+constexpr int kKdaBlkVec = 131072;    // exp(G_n) (128 fp32), beta (64 fp32)
+constexpr int kKdaBlkBytes = 132096;
+constexpr int kKdaBlkSplit = kKdaBlkKt;  // the walk refills [0, split) and [split, end) separately
+
+// The tensor-core walk of the per-channel-gate forward (d_k = 128): one CTA
+// per (64 value columns, head, sequence) over the operand blocks above.
+struct KdaWalkArgs {
+    const uint16_t* v;
+    const uint8_t* tiles;
+    float scale;
+    const float* initial_state;   // may be null
+    const int32_t* cu_seqlens;
+    uint16_t* out;                // may be null
+    float* final_state;           // may be null
+    float* chunk_states;          // may be null: fp32 [slot][H][d_k][d_v] start state of each chunk
+    int N;
+    int T;
+    int H;
+    int d_v;
+    int* err;
+};
+
+cudaError_t launch_kda_walk(const KdaWalkArgs& a, uint32_t wait_limit, cudaStream_t stream);
 
 // Floats of one chunk's T and P in the per-chunk workspace (T, then P).
 constexpr int kKdaTpFloats = 2 * 64 * 64;

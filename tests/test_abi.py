@@ -90,9 +90,10 @@ def test_kda_chunk_host_validation(lib, over, code):
 
 
 def test_kda_chunk_workspace(lib):
-    """The per-channel-gate forward's optional workspace is every chunk's T
-    and P in fp32 (32 KB per chunk and head); a misaligned one is refused."""
-    assert gdn.gdn_kda_chunk_fwd_workspace_size(4, 4096, 16, 128, 128, 0) == 4 * 64 * 16 * 32768
+    """The per-channel-gate forward's optional workspace: at d_k = 128 the
+    tensor-core walk's operand block of every chunk (129 KB per chunk and
+    head), at d_k = 64 T and P in fp32 (32 KB); a misaligned one is refused."""
+    assert gdn.gdn_kda_chunk_fwd_workspace_size(4, 4096, 16, 128, 128, 0) == 4 * 64 * 16 * 132096
     assert gdn.gdn_kda_chunk_fwd_workspace_size(3, 200, 2, 64, 64, 1) == (200 // 64 + 3) * 2 * 32768
     assert gdn.gdn_kda_chunk_fwd_workspace_size(1, 64, 1, 96, 64, 0) == 0
     st = gdn.load().gdn_kda_chunk_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, None, FAKE, None,

@@ -133,10 +133,12 @@ def test_kda_chunk_varlen_matches_oracle(tp):
     assert np.array_equal(S[4], s0[4])
 
 
-@pytest.mark.parametrize("dk,dv,lens", [(128, 128, None), (64, 256, None), (128, 64, [1, 63, 64, 65, 0, 200])])
+@pytest.mark.parametrize("dk,dv,lens", [(64, 64, None), (64, 256, None), (64, 128, [1, 63, 64, 65, 0, 200])])
 def test_kda_chunk_tp_route_is_bitwise_the_walk(dk, dv, lens):
-    """T and P from the chunk-parallel kernel are the walk's own (same steps,
-    same order), so the two routes agree bit for bit."""
+    """At d_k = 64, T and P from the chunk-parallel kernel are the CUDA-core
+    walk's own (same steps, same order), so the two routes agree bit for bit.
+    (At d_k = 128 the workspace route is the tensor-core walk, checked against
+    the oracle above.)"""
     import torch
     if lens is None:
         q, k, v, g, beta, s0, cu = _case(2, 200, 2, dk, dv, seed=31 + dk)
