@@ -169,10 +169,12 @@ GDN_API size_t gdn_kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, in
  *   workspace     optional device scratch, 256-byte aligned.  With at least
  *                 gdn_kda_chunk_fwd_workspace_size() bytes, every chunk's T
  *                 and P are formed first by a chunk-parallel kernel and the
- *                 walk reads them (the faster route); with NULL or fewer
- *                 bytes the walk forms them itself.  Both routes give the
- *                 same bits.  A non-NULL workspace that is not 256-byte
- *                 aligned returns GDN_ERR_MISALIGNED.
+ *                 walk reads them (the faster route: at d_k = 128 the walk
+ *                 runs on the tensor cores over bf16 hi/lo operands); with
+ *                 NULL or fewer bytes the walk forms them itself, fp32
+ *                 throughout.  Both routes compute the same
+ *                 algebra and agree within rounding.  A non-NULL workspace
+ *                 that is not 256-byte aligned returns GDN_ERR_MISALIGNED.
  * Same result as the token-serial kernel up to fp32 rounding order.
  */
 GDN_API gdn_status gdn_kda_chunk_fwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,

@@ -219,10 +219,11 @@ bool launch_kda_tp_pass(const gdn_bf16* q, const gdn_bf16* k, const float* g, co
     return launched(gdn::launch_kda_tp(t, stream));
 }
 
-// Backward workspace of the per-channel-gate variant: T and P, the chunk
-// start states (forward walk), the end-state gradients (reverse walk).
+// Backward workspace of the per-channel-gate variant: T and P (fp32), the
+// chunk start states (forward walk), the end-state gradients (reverse walk),
+// and at d_k = 128 the tensor-core walk's operand blocks.
 struct KdaBwdLayout {
-    size_t tp, states, dstates, total;
+    size_t tp, states, dstates, blocks, total;
 };
 
 KdaBwdLayout kda_bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
@@ -231,7 +232,8 @@ KdaBwdLayout kda_bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     L.tp = 0;
     L.states = kda_tp_bytes(B, T, H, varlen);
     L.dstates = L.states + per;
-    L.total = L.dstates + per;
+    L.blocks = L.dstates + per;
+    L.total = L.blocks + (d_k == 128 ? kda_blocks_bytes(B, T, H, varlen) : 0);
     return L;
 }
 
@@ -457,11 +459,22 @@ gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     float* tp = L.total ? reinterpret_cast<float*>(ws + L.tp) : nullptr;
     float* states = L.total ? reinterpret_cast<float*>(ws + L.states) : nullptr;
     float* dstates = L.total ? reinterpret_cast<float*>(ws + L.dstates) : nullptr;
+    uint8_t* blocks = (L.total && d_k == 128) ? reinterpret_cast<uint8_t*>(ws + L.blocks) : nullptr;
     const int max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
     if (max_chunks > 0) {
-        // T and P of every chunk, then the forward walk recording each chunk's start state
-        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, nullptr, B, T, H, d_k, err, stream))
+        // T and P of every chunk, then the forward walk recording each chunk's
+        // start state (at d_k = 128 the tensor-core walk over the operand blocks)
+        if (!launch_kda_tp_pass(q, k, g, beta, cu_seqlens, tp, blocks, B, T, H, d_k, err, stream))
             return GDN_ERR_CUDA;
+        if (blocks) {
+            gdn::KdaWalkArgs w{};
+            w.v = v; w.tiles = blocks; w.scale = scale; w.initial_state = initial_state;
+            w.cu_seqlens = cu_seqlens; w.out = nullptr; w.final_state = nullptr; w.chunk_states = states;
+            w.N = B; w.T = T; w.H = H; w.d_v = d_v; w.err = err;
+            if (!launched(gdn::launch_kda_walk(w, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+        }
+    }
+    if (max_chunks > 0 && !blocks) {
         gdn::FwdArgs f{};
         f.q = q; f.k = k; f.v = v; f.g = g; f.beta = beta; f.scale = scale;
         f.initial_state = initial_state; f.cu_seqlens = cu_seqlens;
@@ -472,11 +485,15 @@ gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     gdn::KdaBwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.d_out = d_out; a.scale = scale;
     a.cu_seqlens = cu_seqlens; a.d_final_state = d_final_state;
-    a.chunk_tp = tp; a.chunk_states = states; a.chunk_dstates = dstates; a.d_initial_state = d_initial_state;
+    a.chunk_tp = tp; a.tiles = blocks; a.chunk_states = states; a.chunk_dstates = dstates;
+    a.d_initial_state = d_initial_state;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta;
     a.N = B; a.T = T; a.H = H; a.d_k = d_k; a.d_v = d_v; a.max_chunks = max_chunks; a.err = err;
-    // the reverse walk (also when T = 0: it passes d_final_state to d_initial_state)
-    if (!launched(gdn::launch_kda_bwd_chain(a, stream))) return GDN_ERR_CUDA;
+    // the reverse walk (also when T = 0: it passes d_final_state to d_initial_state);
+    // at d_k = 128 on the tensor cores over the operand blocks
+    if (!launched(blocks ? gdn::launch_kda_bwd_chain_tc(a, gdn::kDefaultWaitLimit, stream)
+                         : gdn::launch_kda_bwd_chain(a, stream)))
+        return GDN_ERR_CUDA;
     if (max_chunks > 0 && !launched(gdn::launch_kda_bwd_local(a, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }

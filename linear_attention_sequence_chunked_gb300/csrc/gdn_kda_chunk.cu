@@ -213,45 +213,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_kda_chunk_kernel(const FwdArg
     }
 }
 
-// T = (I + A)^-1 and the causal score P of one chunk (one block per chunk,
-// head and sequence), written to the per-chunk workspace as two row-major
-// 64 x 64 fp32 tiles.  The same steps as the walk's own gram and inverse, so
-// both routes give the same T and P bit for bit.
-template <int K>
-struct KdaTpSmem {
-    static constexpr int LDK = K + 4;
-    static constexpr int LDC = kChunk + 4;
-    static constexpr size_t kBytes = sizeof(float) * (64 * LDK * 3 + 64 * LDC * 3 + 64);
-};
-
-// The decayed operands exp(G) o k, exp(G) o q, exp(G_n - G) o k of a chunk as
-// bf16 hi/lo tiles of the tensor-core walk's operand block, and its vectors
-// exp(G_n), beta (d_k = 128).
-template <int K, int LDK>
-__device__ __forceinline__ void write_decayed_operands(uint8_t* blk, const float* Ks, const float* Qs,
-                                                       const float* Gk, const float* bs) {
-    for (int e = threadIdx.x; e < 64 * (K / 8); e += blockDim.x) {
-        const int i = e / (K / 8), ch = e % (K / 8);
-        const int region = ch >> 3;
+// One 64-channel region of the decayed operands exp(G) o k, exp(G) o q,
+// exp(G_n - G) o k of a chunk (rows of stride LDH, row 63 holding G_n) as
+// bf16 hi/lo tiles of the tensor-core walk's operand block, and the region's
+// exp(G_n).
+template <int LDH>
+__device__ __forceinline__ void write_decayed_region(uint8_t* blk, int region, const float* Ks, const float* Qs,
+                                                     const float* Gk) {
+    uint8_t* r = blk + region * 8192;
+    for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
+        const int i = e >> 3, ch = e & 7;
         float kg[8], qg[8], kt[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int c = 8 * ch + j;
-            const float G = Gk[i * LDK + c];
-            const float kv = Ks[i * LDK + c];
+            const float G = Gk[i * LDH + c];
+            const float kv = Ks[i * LDH + c];
             const float eg = expf(G);
             kg[j] = kv * eg;
-            qg[j] = Qs[i * LDK + c] * eg;
-            kt[j] = kv * expf(Gk[63 * LDK + c] - G);
+            qg[j] = Qs[i * LDH + c] * eg;
+            kt[j] = kv * expf(Gk[63 * LDH + c] - G);
         }
-        uint8_t* r = blk + region * 8192;
-        tc::store_split_chunk(r + kKdaBlkKG, r + kKdaBlkKG + 16384, i, ch & 7, kg);
-        tc::store_split_chunk(r + kKdaBlkQG, r + kKdaBlkQG + 16384, i, ch & 7, qg);
-        tc::store_split_chunk(r + kKdaBlkKt, r + kKdaBlkKt + 16384, i, ch & 7, kt);
+        tc::store_split_chunk(r + kKdaBlkKG, r + kKdaBlkKG + 16384, i, ch, kg);
+        tc::store_split_chunk(r + kKdaBlkQG, r + kKdaBlkQG + 16384, i, ch, qg);
+        tc::store_split_chunk(r + kKdaBlkKt, r + kKdaBlkKt + 16384, i, ch, kt);
     }
     float* vec = reinterpret_cast<float*>(blk + kKdaBlkVec);
-    for (int c = threadIdx.x; c < K; c += blockDim.x) vec[c] = expf(Gk[63 * LDK + c]);
-    if (threadIdx.x < 64) vec[K + threadIdx.x] = bs[threadIdx.x];
+    if (threadIdx.x < 64) vec[64 * region + threadIdx.x] = expf(Gk[63 * LDH + threadIdx.x]);
 }
 
 // A 64 x 64 shared tile (row stride LD) as a bf16 hi/lo operand tile pair.
@@ -263,10 +251,23 @@ __device__ __forceinline__ void write_split_tile64(uint8_t* hi, uint8_t* lo, con
     }
 }
 
+// T = (I + A)^-1 and the causal score P of one chunk (one block per chunk,
+// head and sequence), written to the per-chunk workspace as two row-major
+// 64 x 64 fp32 tiles and / or (d_k = 128) with the decayed operands as the
+// tensor-core walk's operand block.  The key channels are taken 64 at a time
+// (the gram's register sums carry over, in the walk's own order, so both
+// routes form the same T and P), which keeps the block at 105 KB of shared
+// memory: two blocks share an SM.
+struct KdaTpSmem {
+    static constexpr int LDH = 64 + 4;      // rows of 64 channels
+    static constexpr int LDC = kChunk + 4;
+    static constexpr size_t kBytes = sizeof(float) * (64 * LDH * 3 + 64 * LDC * 3 + 64);
+};
+
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs p) {
-    using L = KdaTpSmem<K>;
-    constexpr int LDK = L::LDK;
+__global__ void __launch_bounds__(kThreads, 2) gdn_kda_tp_kernel(const KdaTpArgs p) {
+    using L = KdaTpSmem;
+    constexpr int LDH = L::LDH;
     constexpr int LDC = L::LDC;
     const int ci = blockIdx.x;
     const int h = blockIdx.y;
@@ -279,33 +280,35 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs
     const int nv = min(kChunk, t1 - c0);
 
     extern __shared__ __align__(16) float sm[];
-    float* Ks = sm;             // k; then scratch of the inverse
-    float* Qs = Ks + 64 * LDK;  // q
-    float* Gk = Qs + 64 * LDK;  // g; then G
-    float* Au = Gk + 64 * LDK;  // A
+    float* Ks = sm;             // k (64 channels); then scratch of the inverse
+    float* Qs = Ks + 64 * LDH;  // q
+    float* Gk = Qs + 64 * LDH;  // g; then G
+    float* Au = Gk + 64 * LDH;  // A
     float* Pm = Au + 64 * LDC;  // P
     float* Tm = Pm + 64 * LDC;  // T
     float* bs = Tm + 64 * LDC;
 
     const long long row0 = static_cast<long long>(b) * p.T + c0;
-    load_rows_bf16<K, LDK>(p.k, row0, H, h, K, 0, nv, Ks);
-    load_rows_bf16<K, LDK>(p.q, row0, H, h, K, 0, nv, Qs);
-    load_rows_f32<K, LDK>(p.g, row0, H, h, nv, Gk);
+    const long long slot = (chunk_slot_base(p.cu_seqlens, n, p.T) + ci) * H + h;
+    uint8_t* blk = nullptr;
+    if constexpr (K == 128) blk = p.tiles ? p.tiles + slot * kKdaBlkBytes : nullptr;
     if (threadIdx.x < 64) {
         const int r = threadIdx.x;
         bs[r] = (r < nv) ? bf16_to_f32(p.beta[(row0 + r) * H + h]) : 0.f;
     }
-    __syncthreads();
-    chunk_gate_cumsum<K, LDK>(Gk, nullptr, nullptr);
-    gram_and_score<K, LDK, LDC>(Ks, Qs, Gk, bs, Au, Pm, true);
-    const long long slot = (chunk_slot_base(p.cu_seqlens, n, p.T) + ci) * H + h;
-    uint8_t* blk = nullptr;
-    if constexpr (K == 128) {
-        if (p.tiles) {
-            blk = p.tiles + slot * kKdaBlkBytes;
-            write_decayed_operands<K, LDK>(blk, Ks, Qs, Gk, bs);
-        }
+    float a[4][4] = {}, pp[4][4] = {};
+    for (int hf = 0; hf < K / 64; ++hf) {
+        if (hf) __syncthreads();
+        load_rows_bf16<64, LDH>(p.k, row0, H, h, K, 64 * hf, nv, Ks);
+        load_rows_bf16<64, LDH>(p.q, row0, H, h, K, 64 * hf, nv, Qs);
+        load_rows_f32_cols<64, LDH>(p.g, row0, H, h, K, 64 * hf, nv, Gk);
+        __syncthreads();
+        chunk_gate_cumsum<64, LDH>(Gk, nullptr, nullptr);
+        gram_accumulate<64, LDH>(Ks, Qs, Gk, a, pp);
+        if (blk) write_decayed_region<LDH>(blk, hf, Ks, Qs, Gk);
     }
+    gram_store<LDC>(a, pp, bs, Au, Pm, true);
+    if (blk && threadIdx.x < 64) reinterpret_cast<float*>(blk + kKdaBlkVec)[K + threadIdx.x] = bs[threadIdx.x];
     __syncthreads();
     chunk_unit_lower_inverse<LDC>(Au, Tm, Ks);
     if (p.chunk_tp) {
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_kda_tp_kernel(const KdaTpArgs
 
 template <int K>
 cudaError_t launch_kda_tp_k(const KdaTpArgs& a, cudaStream_t stream) {
-    const size_t smem = KdaTpSmem<K>::kBytes;
+    const size_t smem = KdaTpSmem::kBytes;
     cudaError_t e = cudaFuncSetAttribute(gdn_kda_tp_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -103,16 +103,14 @@ __device__ __forceinline__ void mm_trans(float (&acc)[K / 16][4], const float* A
 // columns j = tj + 16 s (r, s < 4): pairs with s > r lie above the diagonal
 // for every thread and are skipped at compile time; pairs with s == r that lie
 // above the diagonal take a zero exponent (their value is masked on store).
-template <int K, int LDK, int LDC>
-__device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs, const float* Gk,
-                                               const float* bs, float* Au, float* Pm, bool score) {
+// gram_accumulate adds KC channels (rows of stride LDK) to the register sums;
+// channel blocks taken one after another give the same sums, in the same
+// order, as one pass over all of them.
+template <int KC, int LDK>
+__device__ __forceinline__ void gram_accumulate(const float* Ks, const float* Qs, const float* Gk, float (&a)[4][4],
+                                                float (&p)[4][4]) {
     const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
-    float a[4][4], p[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < 4; ++s) a[r][s] = p[r][s] = 0.f;
-    for (int c = 0; c < K; c += 4) {
+    for (int c = 0; c < KC; c += 4) {
         float gi[4][4], ki[4][4], qi[4][4], gj[4][4], kj[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -140,6 +138,12 @@ __device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs,
                     p[r][s] = fmaf(qi[r][e], ke, p[r][s]);
                 }
     }
+}
+
+template <int LDC>
+__device__ __forceinline__ void gram_store(const float (&a)[4][4], const float (&p)[4][4], const float* bs, float* Au,
+                                           float* Pm, bool score) {
+    const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -148,6 +152,29 @@ __device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs,
             Au[i * LDC + j] = (j < i) ? bs[i] * a[r][s] : 0.f;
             if (score) Pm[i * LDC + j] = (j <= i) ? p[r][s] : 0.f;
         }
+}
+
+template <int K, int LDK, int LDC>
+__device__ __forceinline__ void gram_and_score(const float* Ks, const float* Qs, const float* Gk,
+                                               const float* bs, float* Au, float* Pm, bool score) {
+    float a[4][4] = {}, p[4][4] = {};
+    gram_accumulate<K, LDK>(Ks, Qs, Gk, a, p);
+    gram_store<LDC>(a, p, bs, Au, Pm, score);
+}
+
+// Rows [row0, row0 + nv) of a (.., T, H, D) fp32 tensor for head h, columns
+// [col0, col0 + W), into a 64 x LD tile; rows >= nv are zero.
+template <int W, int LD>
+__device__ __forceinline__ void load_rows_f32_cols(const float* __restrict__ src, long long row0, int H, int h,
+                                                   int D, int col0, int nv, float* dst) {
+    constexpr int kPerRow = W / 4;
+    for (int e = threadIdx.x; e < 64 * kPerRow; e += blockDim.x) {
+        const int r = e / kPerRow;
+        const int c = (e % kPerRow) * 4;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < nv) x = ld4(src + ((row0 + r) * H + h) * static_cast<long long>(D) + col0 + c);
+        st4(dst + r * LD + c, x);
+    }
 }
 
 // Generic register-blocked products.  The output has NCG groups of four

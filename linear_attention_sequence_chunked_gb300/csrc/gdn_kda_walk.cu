@@ -379,7 +379,342 @@ __global__ void __launch_bounds__(kWalkThreads, 1) gdn_kda_walk_kernel(const Kda
     if (warp == 0) tmem_dealloc(tmem, kWalkTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// The reverse walk of the backward (state gradients), d_k = 128.  Per chunk,
+// from the last, with dS the gradient w.r.t. the chunk's end state:
+//   dDelta = scale P^T dO + Kt dS          dR = T^T dDelta
+//   dS0    = scale QG^T dO + diag(exp(G_n)) dS - KG^T (beta o dR)
+// over the same operand blocks as the forward walk (P^T, T^T, QG^T and KG^T
+// are the block's tiles read in the other major order).  dO is exact in bf16;
+// dS, dDelta and beta o dR are split into hi + lo parts.  dS lives in fp32
+// registers like the forward walk's S.  Per chunk it records dS for the
+// chunk-parallel gradient pass; the refills of the operand block follow the
+// order the products read it: Kt, T, P and the vectors once T^T dDelta is
+// done, KG and QG once the dS0 products are.
+// ---------------------------------------------------------------------------
+
+constexpr uint32_t kChainTmemCols = 512;
+constexpr uint32_t kColPO = 0;     // P^T dO (M = 64)
+constexpr uint32_t kColKD = 64;    // Kt dS (M = 64)
+constexpr uint32_t kColR = 128;    // T^T dDelta (M = 64)
+constexpr uint32_t kColQO = 192;   // QG^T dO (M = 128)
+constexpr uint32_t kColKR = 256;   // KG^T (beta o dR) (M = 128)
+
+constexpr int cBlk = 0;
+constexpr int cShi = cBlk + kKdaBlkBytes;     // dS hi, lo
+constexpr int cSlo = cShi + kWalkK * 128;
+constexpr int cO = cSlo + kWalkK * 128;       // dO (bf16, exact)
+constexpr int cEhi = cO + kTile64;            // dDelta hi, lo
+constexpr int cElo = cEhi + kTile64;
+constexpr int cRhi = cElo + kTile64;          // beta o dR hi, lo
+constexpr int cRlo = cRhi + kTile64;
+constexpr int cBar = cRlo + kTile64;
+enum { C_FULLA = 0, C_FULLB, C_KD, C_PO, C_QO, C_R, C_KR, C_DRAIN, kChainBars };
+constexpr int cMisc = cBar + kChainBars * 8;
+constexpr int kChainAlloc = cMisc + 16 + 1024;
+static_assert(kChainAlloc <= 232448, "shared memory");
+
+__global__ void __launch_bounds__(kWalkThreads, 1) gdn_kda_bwd_chain_tc_kernel(const KdaBwdArgs p, uint32_t wl) {
+    const int vs = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int H = p.H, V = p.d_v;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int b, t0, t1;
+    if (!seq_range(p.cu_seqlens, n, p.N, p.T, p.err, b, t0, t1)) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + smem_align_pad(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + cBar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + cMisc);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+    const long long row_base = static_cast<long long>(b) * p.T;
+    const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+    const long long slot0 = chunk_slot_base(p.cu_seqlens, n, p.T);
+    auto blk = [&](int ci) { return p.tiles + ((slot0 + ci) * H + h) * static_cast<long long>(kKdaBlkBytes); };
+    const uint32_t sblk = smem_u32(sm + cBlk);
+    auto copy_a = [&](int ci) {
+        mbar_arrive_expect_tx(bar(C_FULLA), kKdaBlkSplit);
+        bulk_g2s(sblk, blk(ci), kKdaBlkSplit, bar(C_FULLA));
+    };
+    auto copy_b = [&](int ci) {
+        mbar_arrive_expect_tx(bar(C_FULLB), kKdaBlkBytes - kKdaBlkSplit);
+        bulk_g2s(sblk + kKdaBlkSplit, blk(ci) + kKdaBlkSplit, kKdaBlkBytes - kKdaBlkSplit, bar(C_FULLB));
+    };
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), kChainTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kChainBars; ++i) mbar_init(bar(i), 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    int issued_a = 0, issued_b = 0;
+    if (tid == 0 && nchunks > 0) {
+        copy_a(nchunks - 1);
+        copy_b(nchunks - 1);
+        issued_a = issued_b = 1;
+    }
+
+    const int sw = warp & 3, hs = warp >> 2;
+    const int srow = 32 * sw + lane;
+    const int hrow = 16 * sw + (lane & 15);
+    const int cq = 16 * (2 * hs + (lane >> 4));
+    const uint32_t lb = static_cast<uint32_t>(sw * 32) << 16;
+    auto ld_q16 = [&](uint32_t col, float* v) { tmem_ld_pair16(tmem + lb + col + 32 * hs, v); };
+    auto store_q16 = [&](uint8_t* thi, uint8_t* tlo, const float* x) {
+        store_split_chunk(thi, tlo, hrow, cq >> 3, x);
+        store_split_chunk(thi, tlo, hrow, (cq >> 3) + 1, x + 8);
+    };
+    auto ld_s32 = [&](uint32_t col, float* v) {
+        tmem_ld16(tmem + lb + col + 32 * hs, v);
+        tmem_ld16(tmem + lb + col + 32 * hs + 16, v + 16);
+        tmem_ld_wait();
+    };
+    uint8_t* Shi = sm + cShi;
+    uint8_t* Slo = sm + cSlo;
+    uint8_t* Ot = sm + cO;
+    uint8_t* Ehi = sm + cEhi;
+    uint8_t* Elo = sm + cElo;
+    uint8_t* Rhi = sm + cRhi;
+    uint8_t* Rlo = sm + cRlo;
+    const float* vec = reinterpret_cast<const float*>(sm + cBlk + kKdaBlkVec);
+
+    const long long KV = static_cast<long long>(kWalkK) * V;
+    const long long state_off = (static_cast<long long>(n) * H + h) * KV + vs * kWalkVs;
+    float dS[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dS[j] = 0.f;
+    if (p.d_final_state) {
+        const float* src = p.d_final_state + state_off + static_cast<long long>(srow) * V + 32 * hs;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(src + j);
+            dS[j] = t4.x; dS[j + 1] = t4.y; dS[j + 2] = t4.z; dS[j + 3] = t4.w;
+        }
+    }
+    store_split_half(Shi, Slo, srow, hs, dS);
+
+    // dO of a chunk: two 16-byte pieces a thread (rows t / 8 and t / 8 + 32,
+    // the (t % 8)-th 8 columns of the slice), held in registers until stored
+    uint4 oraw[2];
+    auto load_o = [&](int cj) {
+        oraw[0] = oraw[1] = make_uint4(0, 0, 0, 0);
+        if (cj < 0) return;
+        const int cc0 = t0 + cj * kChunk;
+        const int nvj = min(kChunk, t1 - cc0);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int r = (tid >> 3) + 32 * u;
+            if (r < nvj)
+                oraw[u] = *reinterpret_cast<const uint4*>(p.d_out + ((row_base + cc0 + r) * H + h) *
+                                                                        static_cast<long long>(V) +
+                                                          vs * kWalkVs + 8 * (tid & 7));
+        }
+    };
+    load_o(nchunks - 1);
+
+    const float scale = p.scale;
+    bool ok = true;
+    for (int it = 0; it < nchunks; ++it) {
+        const int ci = nchunks - 1 - it;
+        const uint32_t ph = it & 1;
+        {
+            // the gradient w.r.t. this chunk's end state
+            float* dst = p.chunk_dstates + ((slot0 + ci) * H + h) * KV + static_cast<long long>(srow) * V +
+                         vs * kWalkVs + 32 * hs;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            *reinterpret_cast<uint4*>(Ot + sw128_offset((tid >> 3) + 32 * u, 16 * (tid & 7))) = oraw[u];
+        load_o(ci - 1);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- Kt dS (critical), P^T dO, then QG^T dO once KG / QG are in ----
+        if (warp == 0) {
+            const bool fb = __all_sync(0xffffffffu, mbar_wait(bar(C_FULLB), ph, wl));
+            if (fb && lane == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < kWalkK / 16; ++s) {
+                    const uint32_t koff = (s >> 2) * 8192 + (s & 3) * 32;
+                    const uint64_t ah = desc_sw128(sblk + kKdaBlkKt + koff, 0, 1024);
+                    const uint64_t al = desc_sw128(sblk + kKdaBlkKt + 16384 + koff, 0, 1024);
+                    const uint64_t bh = desc_sw128(smem_u32(Shi) + s * 2048, kWalkK * 128, 1024);
+                    const uint64_t bl = desc_sw128(smem_u32(Slo) + s * 2048, kWalkK * 128, 1024);
+                    mma_bf16(tmem + kColKD, ah, bh, id_k, s > 0);
+                    mma_bf16(tmem + kColKD, ah, bl, id_k, 1);
+                    mma_bf16(tmem + kColKD, al, bh, id_k, 1);
+                }
+                mma_commit(bar(C_KD));
+                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_sw128(sblk + kKdaBlkP + s * 2048, 8192, 1024);
+                    const uint64_t al = desc_sw128(sblk + kKdaBlkP + 8192 + s * 2048, 8192, 1024);
+                    const uint64_t bo = desc_sw128(smem_u32(Ot) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColPO, ah, bo, id_t, s > 0);
+                    mma_bf16(tmem + kColPO, al, bo, id_t, 1);
+                }
+                mma_commit(bar(C_PO));
+            }
+            __syncwarp();
+            const bool fa = fb && __all_sync(0xffffffffu, mbar_wait(bar(C_FULLA), ph, wl));
+            if (fa && lane == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_q = idesc(kFmtBf16, 1, 1, kWalkK, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_sw128(sblk + kKdaBlkQG + s * 2048, 8192, 1024);
+                    const uint64_t al = desc_sw128(sblk + kKdaBlkQG + 16384 + s * 2048, 8192, 1024);
+                    const uint64_t bo = desc_sw128(smem_u32(Ot) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColQO, ah, bo, id_q, s > 0);
+                    mma_bf16(tmem + kColQO, al, bo, id_q, 1);
+                }
+                mma_commit(bar(C_QO));
+            }
+            __syncwarp();
+            if (!fa) ok = false;
+        }
+        // ---- dDelta = scale P^T dO + Kt dS ----
+        bool w_ok = mbar_wait(bar(C_KD), ph, wl) && mbar_wait(bar(C_PO), ph, wl) && mbar_wait(bar(C_FULLB), ph, wl);
+        tc_fence_after();
+        float be = 0.f, gnr = 0.f;
+        if (w_ok) {
+            float a[16], k[16];
+            ld_q16(kColPO, a);
+            ld_q16(kColKD, k);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) a[c] = fmaf(scale, a[c], k[c]);
+            store_q16(Ehi, Elo, a);
+            be = vec[kWalkK + hrow];
+            gnr = vec[srow];
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!(ok && w_ok))) { ok = false; break; }
+        tc_fence_after();
+        // ---- dR = T^T dDelta ----
+        if (warp == 0) {
+            if (lane == 0) {
+                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_sw128(sblk + kKdaBlkT + s * 2048, 8192, 1024);
+                    const uint64_t al = desc_sw128(sblk + kKdaBlkT + 8192 + s * 2048, 8192, 1024);
+                    const uint64_t bh = desc_sw128(smem_u32(Ehi) + s * 2048, kTile64, 1024);
+                    const uint64_t bl = desc_sw128(smem_u32(Elo) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColR, ah, bh, id_t, s > 0);
+                    mma_bf16(tmem + kColR, ah, bl, id_t, 1);
+                    mma_bf16(tmem + kColR, al, bh, id_t, 1);
+                }
+                mma_commit(bar(C_R));
+            }
+            __syncwarp();
+        }
+        w_ok = mbar_wait(bar(C_R), ph, wl);
+        tc_fence_after();
+        if (w_ok) {
+            float r[16];
+            ld_q16(kColR, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) r[c] *= be;
+            store_q16(Rhi, Rlo, r);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!(ok && w_ok))) { ok = false; break; }
+        tc_fence_after();
+        // Kt, T, P read by finished products, the vectors by every thread:
+        // the previous chunk's come in now
+        if (tid == 0 && ci > 0) {
+            copy_b(ci - 1);
+            issued_b = it + 2;
+        }
+        // ---- KG^T (beta o dR) ----
+        if (warp == 0) {
+            if (lane == 0) {
+                constexpr uint32_t id_q = idesc(kFmtBf16, 1, 1, kWalkK, 64);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ah = desc_sw128(sblk + kKdaBlkKG + s * 2048, 8192, 1024);
+                    const uint64_t al = desc_sw128(sblk + kKdaBlkKG + 16384 + s * 2048, 8192, 1024);
+                    const uint64_t bh = desc_sw128(smem_u32(Rhi) + s * 2048, kTile64, 1024);
+                    const uint64_t bl = desc_sw128(smem_u32(Rlo) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + kColKR, ah, bh, id_q, s > 0);
+                    mma_bf16(tmem + kColKR, ah, bl, id_q, 1);
+                    mma_bf16(tmem + kColKR, al, bh, id_q, 1);
+                }
+                mma_commit(bar(C_KR));
+            }
+            __syncwarp();
+        }
+        // ---- dS0 = scale QG^T dO + diag(exp(G_n)) dS - KG^T (beta o dR) ----
+        w_ok = mbar_wait(bar(C_KR), ph, wl) && mbar_wait(bar(C_QO), ph, wl);
+        tc_fence_after();
+        if (w_ok) {
+            float qo[32], kr[32];
+            ld_s32(kColQO, qo);
+            ld_s32(kColKR, kr);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) dS[c] = fmaf(scale, qo[c], fmaf(gnr, dS[c], -kr[c]));
+            store_split_half(Shi, Slo, srow, hs, dS);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!(ok && w_ok))) { ok = false; break; }
+        tc_fence_after();
+        // KG / QG and dO read by finished products: the previous chunk's KG / QG come in
+        if (tid == 0 && ci > 0) {
+            copy_a(ci - 1);
+            issued_a = it + 2;
+        }
+    }
+
+    if (ok && p.d_initial_state) {
+        float* dst = p.d_initial_state + state_off + static_cast<long long>(srow) * V + 32 * hs;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
+    }
+    if (tid == 0) {
+        if (!ok) record_error(p.err, kErrTimeout);
+        if (issued_a > 0) mbar_wait(bar(C_FULLA), (issued_a - 1) & 1, kDefaultWaitLimit);
+        if (issued_b > 0) mbar_wait(bar(C_FULLB), (issued_b - 1) & 1, kDefaultWaitLimit);
+    }
+    if (warp == 0) {
+        if (lane == 0) mma_commit(bar(C_DRAIN));
+        __syncwarp();
+        mbar_wait(bar(C_DRAIN), 0, kDefaultWaitLimit);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
+}
+
 }  // namespace
+
+cudaError_t launch_kda_bwd_chain_tc(const KdaBwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(gdn_kda_bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kChainAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.d_v / kWalkVs, a.H, a.N);
+    gdn_kda_bwd_chain_tc_kernel<<<grid, kWalkThreads, kChainAlloc, stream>>>(a, wait_limit);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kda_walk(const KdaWalkArgs& a, uint32_t wait_limit, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(gdn_kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

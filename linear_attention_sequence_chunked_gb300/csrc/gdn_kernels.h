@@ -184,6 +184,7 @@ struct KdaBwdArgs {
     const int32_t* cu_seqlens;
     const float* d_final_state;   // may be null (zeros)
     const float* chunk_tp;        // [slot][H][2][64][64]: T, P
+    const uint8_t* tiles;         // d_k = 128: [slot][H] operand blocks of the tensor-core walk
     const float* chunk_states;    // [slot][H][d_k][d_v]: start state of each chunk
     float* chunk_dstates;         // [slot][H][d_k][d_v]: gradient w.r.t. each chunk's end state
     float* d_initial_state;       // may be null
@@ -203,6 +204,10 @@ struct KdaBwdArgs {
 
 cudaError_t launch_kda_bwd_chain(const KdaBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_kda_bwd_local(const KdaBwdArgs& a, cudaStream_t stream);
+
+// The reverse walk of the per-channel-gate backward on the tensor cores
+// (d_k = 128): as launch_kda_bwd_chain, over the operand blocks in a.tiles.
+cudaError_t launch_kda_bwd_chain_tc(const KdaBwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 
 // Token-serial forward (decode path; the same recurrence token by token).
 struct RecurrentArgs {

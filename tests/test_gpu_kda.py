@@ -133,12 +133,13 @@ def test_kda_chunk_varlen_matches_oracle(tp):
     assert np.array_equal(S[4], s0[4])
 
 
-@pytest.mark.parametrize("dk,dv,lens", [(64, 64, None), (64, 256, None), (64, 128, [1, 63, 64, 65, 0, 200])])
-def test_kda_chunk_tp_route_is_bitwise_the_walk(dk, dv, lens):
-    """At d_k = 64, T and P from the chunk-parallel kernel are the CUDA-core
-    walk's own (same steps, same order), so the two routes agree bit for bit.
-    (At d_k = 128 the workspace route is the tensor-core walk, checked against
-    the oracle above.)"""
+@pytest.mark.parametrize("dk,dv,lens", [(64, 64, None), (128, 256, None), (128, 128, [1, 63, 64, 65, 0, 200]),
+                                         (64, 128, [1, 63, 64, 65, 0, 200])])
+def test_kda_chunk_routes_agree(dk, dv, lens):
+    """The workspace route (T and P from the chunk-parallel kernel; at
+    d_k = 128 the tensor-core walk over bf16 hi/lo operands) against the
+    walk that forms everything itself in fp32, and a repeat of the workspace
+    route bitwise."""
     import torch
     if lens is None:
         q, k, v, g, beta, s0, cu = _case(2, 200, 2, dk, dv, seed=31 + dk)
@@ -146,7 +147,11 @@ def test_kda_chunk_tp_route_is_bitwise_the_walk(dk, dv, lens):
         q, k, v, g, beta, s0, cu = _case(1, 0, 2, dk, dv, seed=32, seqlens=lens)
     o1, S1 = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1)
     o2, S2 = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1, tp=True)
-    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+    o3, S3 = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, 0.1, tp=True)
+    assert np.array_equal(o2, o3) and np.array_equal(S2, S3)
+    G.compare(o2, o1, G.TOL_RMS_IID, G.TOL_MAX_IID, "routes out")
+    for s in range(S1.shape[0]):
+        G.compare(S2[s], S1[s], TOL_STATE_FP32, None, f"routes state {s}")
 
 
 def test_kda_chunk_strong_per_channel_decay():
