@@ -643,43 +643,65 @@ SMS = 152
 
 
 def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, steps=5, warmup=2):
-    """The per-channel-gate (KDA) forward at the headline shape: the chunked
-    fp32 CUDA-core kernel (gdn_kda_chunk_fwd) beside the token-serial one
-    (gdn_kda_recurrent_fwd), L2 flushed before each call.  Inputs: q, v ~
-    N(0,1), k L2-normalised, g = -5 sigmoid(N(0,1) + 2) per key channel (the
-    bounded gate with lower bound -5), beta = sigmoid(N(0,1)), zero initial
-    state; drawn on the device.  The chunked kernel runs on the CUDA cores, so
-    its roofline is fp32 FMA: the chunk algebra's FLOPs (the forward formula,
-    the decay exponentials not counted) against 152 SMs x 128 lanes x 2 FLOP
-    at the SM clock sampled in this run."""
+    """The per-channel-gate (KDA) operator at the headline shape, L2 flushed
+    before each call: the chunked forward through its workspace route (the
+    chunk-parallel T/P kernel on the CUDA cores, then the tensor-core walk),
+    the same forward without a workspace (fp32 CUDA-core walk), the
+    token-serial forward, and the chunked backward (gdn_kda_chunk_bwd).
+    Inputs: q, v, dO ~ N(0,1), k L2-normalised, g = -5 sigmoid(N(0,1) + 2) per
+    key channel (the bounded gate with lower bound -5), beta = sigmoid(N(0,1)),
+    zero initial state; drawn on the device.  The roofline line is the
+    forward's chunk-algebra FLOPs (decay exponentials not counted) against
+    the fp32 FMA rate of 152 SMs x 128 lanes x 2 FLOP at the sampled SM
+    clock: its dominant kernel, the T/P kernel, runs on the CUDA cores."""
     gen = torch.Generator(device=dev).manual_seed(5)
     q = torch.randn((B, T, H, K), device=dev, generator=gen).to(torch.bfloat16)
     k = torch.nn.functional.normalize(torch.randn((B, T, H, K), device=dev, generator=gen), dim=-1).to(torch.bfloat16)
     v = torch.randn((B, T, H, V), device=dev, generator=gen).to(torch.bfloat16)
     g = -5.0 * torch.sigmoid(torch.randn((B, T, H, K), device=dev, generator=gen) + 2.0)
     beta = torch.sigmoid(torch.randn((B, T, H), device=dev, generator=gen)).to(torch.bfloat16)
+    d_out = torch.randn((B, T, H, V), device=dev, generator=gen).to(torch.bfloat16)
     out = torch.empty_like(v)
     fs = torch.empty((B, H, K, V), dtype=torch.float32, device=dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     scale = K ** -0.5
+    nf = gdn.gdn_kda_chunk_fwd_workspace_size(B, T, H, K, V, 0)
+    wf = torch.empty(nf, dtype=torch.uint8, device=dev)
+    nb = gdn.gdn_kda_chunk_bwd_workspace_size(B, T, H, K, V, 0)
+    wb = torch.empty(nb, dtype=torch.uint8, device=dev)
+    grads = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(g),
+             torch.empty_like(beta), torch.empty((B, H, K, V), dtype=torch.float32, device=dev)]
 
     def timed(fn, n):
         for _ in range(warmup):
-            fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, stream)
+            fn()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         torch.cuda.synchronize()
         for e0, e1 in ev:
             flush.zero_()
             e0.record(stream)
-            fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, stream)
+            fn()
             e1.record(stream)
         torch.cuda.synchronize()
         return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e-3
 
-    t_c = timed(gdn.gdn_kda_chunk_fwd, steps)
+    def fwd(ws, nbytes, fn=gdn.gdn_kda_chunk_fwd):
+        def run():
+            if fn is gdn.gdn_kda_chunk_fwd:
+                fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, ws, nbytes, stream)
+            else:
+                fn(q, k, v, g, beta, scale, None, None, out, fs, B, T, H, K, V, stream)
+        return run
+
+    def bwd():
+        gdn.gdn_kda_chunk_bwd(q, k, v, g, beta, scale, None, None, d_out, None, *grads, B, T, H, K, V, wb, nb, stream)
+
+    t_c = timed(fwd(wf, nf), steps)
     o_c = out.float().clone()
-    t_r = timed(gdn.gdn_kda_recurrent_fwd, 2)
+    t_w = timed(fwd(None, 0), 2)
+    t_r = timed(fwd(None, 0, gdn.gdn_kda_recurrent_fwd), 2)
     diff = float((out.float() - o_c).norm() / out.float().norm())
+    t_b = timed(bwd, steps)
     st = gdn.gdn_get_last_device_error()
     if st != 0:
         raise SystemExit(f"device error in the KDA measurement: {gdn.gdn_status_string(st)}")
@@ -689,8 +711,10 @@ def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, s
     ach = fwd_flops(K, V) * units / t_c / 1e12
     return {"config": f"B={B} T={T} H={H} d_k={K} d_v={V}, per-channel g in (-5, 0)",
             "chunk_ms": t_c * 1e3, "chunk_tokens_heads_per_s": units / t_c,
+            "chunk_fp32_walk_ms": t_w * 1e3,
             "token_serial_ms": t_r * 1e3, "token_serial_tokens_heads_per_s": units / t_r,
             "speedup_vs_token_serial": t_r / t_c, "out_rel_l2_chunk_vs_token_serial": diff,
+            "bwd_ms": t_b * 1e3, "fwd_bwd_tokens_heads_per_s": units / (t_c + t_b),
             "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                          "peak_from": f"{SMS} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 FLOP x {mhz:.0f} MHz",
                          "traffic": None}}
