@@ -494,7 +494,9 @@ gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     if (!launched(blocks ? gdn::launch_kda_bwd_chain_tc(a, gdn::kDefaultWaitLimit, stream)
                          : gdn::launch_kda_bwd_chain(a, stream)))
         return GDN_ERR_CUDA;
-    if (max_chunks > 0 && !launched(gdn::launch_kda_bwd_local(a, stream))) return GDN_ERR_CUDA;
+    if (max_chunks > 0 && !launched(blocks ? gdn::launch_kda_bwd_local_tc(a, gdn::kDefaultWaitLimit, stream)
+                                           : gdn::launch_kda_bwd_local(a, stream)))
+        return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

@@ -208,6 +208,9 @@ cudaError_t launch_kda_bwd_local(const KdaBwdArgs& a, cudaStream_t stream);
 // The reverse walk of the per-channel-gate backward on the tensor cores
 // (d_k = 128): as launch_kda_bwd_chain, over the operand blocks in a.tiles.
 cudaError_t launch_kda_bwd_chain_tc(const KdaBwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
+// The local gradients on the tensor cores (d_k = 128): as launch_kda_bwd_local,
+// over the operand blocks in a.tiles.
+cudaError_t launch_kda_bwd_local_tc(const KdaBwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 
 // Token-serial forward (decode path; the same recurrence token by token).
 struct RecurrentArgs {
