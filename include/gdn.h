@@ -192,13 +192,15 @@ GDN_API size_t gdn_kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, in
  * chunk by chunk from the last, with the gradient w.r.t. each chunk's end
  * state carried backwards.  Arguments, layouts, validation and errors as
  * gdn_chunk_bwd, except that g and dg are (B, T, H, d_k) fp32: dg is the
- * gradient w.r.t. each token's per-channel log decay.  Four kernels, all fp32
- * on the CUDA cores: T and P of every chunk (chunk-parallel); the forward
- * walk recording each chunk's start state; the reverse walk of the state
- * gradient (one block per 64 value columns, head and sequence); the local
- * gradients of every chunk (chunk-parallel), which sum over the value columns
- * once and evaluate the decayed pair sums of the gram and the causal score
- * once per chunk.  `workspace` (256-byte aligned, at least
+ * gradient w.r.t. each token's per-channel log decay.  Four kernels: T and P
+ * of every chunk (chunk-parallel, CUDA cores); the forward walk recording
+ * each chunk's start state; the reverse walk of the state gradient (one
+ * block per 64 value columns, head and sequence); the local gradients of
+ * every chunk (chunk-parallel), which sum over the value columns once and
+ * evaluate the decayed pair sums of the gram and the causal score once per
+ * chunk.  At d_k = 128 the walks and the local gradients' products run on
+ * the tensor cores (bf16 hi/lo operands, fp32 accumulation); at d_k = 64
+ * everything is fp32 on the CUDA cores.  `workspace` (256-byte aligned, at least
  * gdn_kda_chunk_bwd_workspace_size() bytes, contents on entry ignored) holds
  * T and P and the per-chunk states and state gradients.  Every sum runs in a
  * fixed order: repeated calls give the same bits.
