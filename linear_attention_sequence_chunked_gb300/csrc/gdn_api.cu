@@ -219,9 +219,9 @@ bool launch_kda_tp_pass(const gdn_bf16* q, const gdn_bf16* k, const float* g, co
     return launched(gdn::launch_kda_tp(t, stream));
 }
 
-// Backward workspace of the per-channel-gate variant: T and P (fp32), the
-// chunk start states (forward walk), the end-state gradients (reverse walk),
-// and at d_k = 128 the tensor-core walk's operand blocks.
+// Backward workspace of the per-channel-gate variant: T and P (fp32, d_k = 64
+// only), the chunk start states (forward walk), the end-state gradients
+// (reverse walk), and at d_k = 128 the tensor-core passes' operand blocks.
 struct KdaBwdLayout {
     size_t tp, states, dstates, blocks, total;
 };
@@ -230,7 +230,7 @@ KdaBwdLayout kda_bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
     KdaBwdLayout L{};
     const size_t per = round_up(sizeof(float) * static_cast<size_t>(d_k) * d_v * chunk_slots(B, T, varlen) * H);
     L.tp = 0;
-    L.states = kda_tp_bytes(B, T, H, varlen);
+    L.states = d_k == 128 ? 0 : kda_tp_bytes(B, T, H, varlen);  // fp32 T, P: the CUDA-core passes only
     L.dstates = L.states + per;
     L.blocks = L.dstates + per;
     L.total = L.blocks + (d_k == 128 ? kda_blocks_bytes(B, T, H, varlen) : 0);
@@ -456,7 +456,7 @@ gdn_status gdn_kda_chunk_bwd(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     int* err = error_word();
     if (!err) return GDN_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
-    float* tp = L.total ? reinterpret_cast<float*>(ws + L.tp) : nullptr;
+    float* tp = (L.total && d_k != 128) ? reinterpret_cast<float*>(ws + L.tp) : nullptr;
     float* states = L.total ? reinterpret_cast<float*>(ws + L.states) : nullptr;
     float* dstates = L.total ? reinterpret_cast<float*>(ws + L.dstates) : nullptr;
     uint8_t* blocks = (L.total && d_k == 128) ? reinterpret_cast<uint8_t*>(ws + L.blocks) : nullptr;
