@@ -81,11 +81,80 @@ constexpr int edP = edA + 64 * LDP * 4;
 constexpr int edQ = edP + 64 * LDP * 4;
 constexpr int edK = edQ + 64 * LDF * 4;
 constexpr int edG = edK + 64 * LDF * 4;
-constexpr int eVec = edG + 64 * LDF * 4;  // beta, G_n, exp(G_n), gsum, dbeta parts [4][64], X column parts [4][128]
-constexpr int kEVecFloats = 64 + 3 * kLK + 4 * 64 + 4 * kLK;
+constexpr int eVec = edG + 64 * LDF * 4;  // beta, G_n, exp(G_n), gsum, dbeta parts [4][64], X column parts [4][128], [4][64]
+constexpr int kEVecFloats = 64 + 3 * kLK + 4 * 64 + 4 * kLK + 4 * 64 + 16 * kLK;
 static_assert(eVec + kEVecFloats * 4 <= sBar, "end-phase tiles fit below the barriers");
 
 __device__ __forceinline__ float bf(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+
+// Eight rows of one 16 x 16 tile of pairs (rows i = 16 I + 8 half + r of
+// sub-block I, the 16 columns j of sub-block J <= I) of the decayed pair sums
+// for key channel c, each pair's factor E = exp(G_ic - G_jc) formed once (a
+// masked difference, <= 0):
+//   u1_i = sum_j dA_ij k_jc E   (j < i),      u2_i = sum_j dP_ij k_jc E   (j <= i),
+//   w_j += (beta_i dA_ij k_ic + dP_ij q_ic) E   (i > j for dA, i >= j for dP).
+// Each row's u1, u2 go straight into dq, dk, dG of row i (this thread owns
+// channel c of these rows), with sum_c k_ic u1_ic (dbeta) summed over the warp's
+// channels into dbc; the row loop is kept rolled so the code stays small.
+// dA and dP hold every entry of the tile; on the diagonal tile the pairs above
+// the diagonal are skipped and dA's diagonal counts as 0.
+__device__ __forceinline__ void pair_rows(int I, int J, int half, int c, int lane, int wq, const float* Gs,
+                                          const uint16_t* Ks, const uint16_t* Qs, const float* dA, const float* dP,
+                                          const float* bs, float* dQ, float* dK, float* dG, float* dbc,
+                                          float (&w)[16]) {
+    const bool diag = I == J;
+    float gj[16], kj[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+        const int j = 16 * J + jj;
+        gj[jj] = Gs[j * LDF + c];
+        kj[jj] = bf(Ks + j * LDB + c);
+    }
+#pragma unroll 1
+    for (int r = 0; r < 8; ++r) {
+        const int ii = 8 * half + r;
+        const int i = 16 * I + ii;
+        const float gi = Gs[i * LDF + c];
+        const float ki = bf(Ks + i * LDB + c);
+        const float qi = bf(Qs + i * LDB + c);
+        const float be = bs[i];
+        const float bki = be * ki;
+        float u1 = 0.f, u2 = 0.f, u1b = 0.f, u2b = 0.f;
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 av = *reinterpret_cast<const float4*>(dA + i * LDP + 16 * J + 4 * j4);
+            const float4 qv = *reinterpret_cast<const float4*>(dP + i * LDP + 16 * J + 4 * j4);
+            const float a4[4] = {av.x, av.y, av.z, av.w};
+            const float q4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int jj = 4 * j4 + m;
+                const bool on = !diag || jj <= ii;
+                const float e = on ? __expf(gi - gj[jj]) : 0.f;
+                const float ad = (diag && jj == ii) ? 0.f : a4[m];
+                const float ke = kj[jj] * e;
+                // two accumulators a row keep the dependent FMA chains short
+                if (m & 1) {
+                    u1b = fmaf(ad, ke, u1b);
+                    u2b = fmaf(q4[m], ke, u2b);
+                } else {
+                    u1 = fmaf(ad, ke, u1);
+                    u2 = fmaf(q4[m], ke, u2);
+                }
+                w[jj] = fmaf(fmaf(ad, bki, q4[m] * qi), e, w[jj]);
+            }
+        }
+        u1 += u1b;
+        u2 += u2b;
+        dQ[i * LDF + c] += u2;
+        dK[i * LDF + c] = fmaf(be, u1, dK[i * LDF + c]);
+        dG[i * LDF + c] = fmaf(bki, u1, fmaf(qi, u2, dG[i * LDF + c]));
+        float part = ki * u1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) dbc[wq * 64 + i] += part;
+    }
+}
 
 __global__ void __launch_bounds__(kLThreads, 1) gdn_kda_local_tc_kernel(const KdaBwdArgs p, uint32_t wl) {
     const int ci = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -395,6 +464,8 @@ __global__ void __launch_bounds__(kLThreads, 1) gdn_kda_local_tc_kernel(const Kd
         float* gsum = gn + kLK;
         float* dbq = gsum + kLK;      // [4][64]
         float* xs = dbq + 4 * 64;     // [4][128]
+        float* dbc = xs + 4 * kLK;    // [4][64]: per warp of the pair sums, sum_c k o u1' of each row
+        float* wsc = dbc + 4 * 64;    // [16][128]: column sums of the upper row halves
         for (int e = tid; e < 64 * (kLK / 8); e += kLThreads) {
             const int r = e / (kLK / 8), c = (e % (kLK / 8)) * 8;
             uint4 kk = make_uint4(0u, 0u, 0u, 0u), qq = kk;
@@ -498,111 +569,43 @@ __global__ void __launch_bounds__(kLThreads, 1) gdn_kda_local_tc_kernel(const Kd
         }
         __syncthreads();
 
-        // ---- the decayed pair sums (thread: rows ki + 8 r, channels kj + 32 e) ----
-        constexpr int NCG = kLK / 4, RS = kLThreads / NCG, TM = 64 / RS;
-        const int ki = tid / NCG, kj = tid % NCG;
-        float dbr[TM];
+        // ---- the decayed pair sums, 16 x 16 tiles of pairs: thread t takes
+        // key channel t % 128 and half the rows of each tile (t / 128), so each
+        // pair's decay factor serves both sides (row i: u1, u2; column j: w);
+        // the column sums of the two halves meet in shared memory ----
+        {
+            const int c = tid & (kLK - 1), half = tid >> 7;
+            for (int e = tid; e < 4 * 64; e += kLThreads) dbc[e] = 0.f;
+            __syncthreads();
+            for (int J = 0; J < 4; ++J) {
+                float w[16];
 #pragma unroll
-        for (int r0 = 0; r0 < TM; r0 += 4) {
-            float u1[4][4] = {}, u2[4][4] = {}, gi[4][4];
+                for (int jj = 0; jj < 16; ++jj) w[jj] = 0.f;
+                for (int I = J; I < 4; ++I)
+                    pair_rows(I, J, half, c, lane, warp & 3, Gs, Ks, Qs, dA, dP, bs, dQ, dK, dG, dbc, w);
+                // column side of sub-block J: the upper half's sums, then the rows
+                if (half == 1) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) gi[r][e] = Gs[(ki + RS * (r0 + r)) * LDF + kj + NCG * e];
-            const int imax = ki + RS * (r0 + 3);
-            for (int j = 0; j <= imax; ++j) {
-                float kj4[4], gj4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kj4[e] = bf(Ks + j * LDB + kj + NCG * e);
-                    gj4[e] = Gs[j * LDF + kj + NCG * e];
+                    for (int jj = 0; jj < 16; ++jj) wsc[jj * kLK + c] = w[jj];
                 }
+                __syncthreads();
+                if (half == 0) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = ki + RS * (r0 + r);
-                    if (j <= i) {
-                        const float a = (j < i) ? dA[i * LDP + j] : 0.f;
-                        const float q = dP[i * LDP + j];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float ke = kj4[e] * __expf(gi[r][e] - gj4[e]);
-                            u1[r][e] = fmaf(a, ke, u1[r][e]);
-                            u2[r][e] = fmaf(q, ke, u2[r][e]);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = 16 * J + jj;
+                        const float wj = w[jj] + wsc[jj * kLK + c];
+                        dK[j * LDF + c] += wj;
+                        dG[j * LDF + c] = fmaf(-bf(Ks + j * LDB + c), wj, dG[j * LDF + c]);
                     }
                 }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = ki + RS * (r0 + r);
-                const float be = bs[i];
-                float part = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = kj + NCG * e;
-                    const float kv = bf(Ks + i * LDB + c);
-                    const float qv = bf(Qs + i * LDB + c);
-                    dQ[i * LDF + c] += u2[r][e];
-                    dK[i * LDF + c] = fmaf(be, u1[r][e], dK[i * LDF + c]);
-                    dG[i * LDF + c] = fmaf(be * kv, u1[r][e], fmaf(qv, u2[r][e], dG[i * LDF + c]));
-                    part = fmaf(kv, u1[r][e], part);
-                }
-                dbr[r0 + r] = part;
+                __syncthreads();
             }
         }
-#pragma unroll
-        for (int r0 = 0; r0 < TM; r0 += 4) {
-            float w[4][4] = {}, gj[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) gj[r][e] = Gs[(ki + RS * (r0 + r)) * LDF + kj + NCG * e];
-            const int jmin = ki + RS * r0;
-            for (int i = jmin; i < 64; ++i) {
-                float ki4[4], qi4[4], gi4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    ki4[e] = bf(Ks + i * LDB + kj + NCG * e);
-                    qi4[e] = bf(Qs + i * LDB + kj + NCG * e);
-                    gi4[e] = Gs[i * LDF + kj + NCG * e];
-                }
-                const float be = bs[i];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int j = ki + RS * (r0 + r);
-                    if (i >= j) {
-                        const float a = (i > j) ? be * dA[i * LDP + j] : 0.f;
-                        const float q = dP[i * LDP + j];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float t = fmaf(a, ki4[e], q * qi4[e]);
-                            w[r][e] = fmaf(t, __expf(gi4[e] - gj[r][e]), w[r][e]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int j = ki + RS * (r0 + r);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = kj + NCG * e;
-                    const float kv = bf(Ks + j * LDB + c);
-                    dK[j * LDF + c] += w[r][e];
-                    dG[j * LDF + c] = fmaf(-kv, w[r][e], dG[j * LDF + c]);
-                }
-            }
-        }
+        __syncthreads();
         // dbeta = sum_c dR o U (the slices) + sum_c k o u1'
-#pragma unroll
-        for (int r = 0; r < TM; ++r) {
-            const int i = ki + RS * r;
-            float part = dbr[r];
-#pragma unroll
-            for (int o = NCG / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (kj == 0 && i < nv)
-                p.dbeta[(row0 + i) * H + h] = f32_to_bf16((dbq[i] + dbq[64 + i]) + part);
-        }
+        if (tid < nv)
+            p.dbeta[(row0 + tid) * H + h] = f32_to_bf16((dbq[tid] + dbq[64 + tid]) +
+                                                        ((dbc[tid] + dbc[64 + tid]) + (dbc[128 + tid] + dbc[192 + tid])));
         __syncthreads();
         // dq, dk (bf16), eight channels a thread
         for (int e = tid; e < 64 * (kLK / 8); e += kLThreads) {
