@@ -108,7 +108,7 @@ def _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, scale, what):
 
 
 @pytest.mark.parametrize("tp", [False, True], ids=["walk", "tp"])
-@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128), (128, 256)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128), (128, 256)])
 def test_kda_chunk_matches_oracle(dk, dv, tp):
     """Three chunks per sequence, the last one ragged (150 = 2 x 64 + 22); the
     walk that forms T and P itself, and the route that reads them from the
@@ -154,15 +154,17 @@ def test_kda_chunk_routes_agree(dk, dv, lens):
         G.compare(S2[s], S1[s], TOL_STATE_FP32, None, f"routes state {s}")
 
 
-def test_kda_chunk_strong_per_channel_decay():
+@pytest.mark.parametrize("tp", [False, True], ids=["walk", "tp"])
+def test_kda_chunk_strong_per_channel_decay(tp):
     """Per-channel log decays down to -40 per token: inside a chunk the
     exponents G_ic - G_jc reach about -2500, far below the fp32 range of exp;
-    formed as masked differences they underflow to 0 and never overflow."""
+    formed as masked differences they underflow to 0 and never overflow (the
+    decayed operands of the tensor-core walk likewise)."""
     import torch
     q, k, v, g, beta, s0, cu = _case(1, 200, 2, 128, 128, seed=13)
     g = (g * 8.0).astype(np.float32)
     scale = 128 ** -0.5
-    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, scale)
+    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, scale, tp=tp)
     assert np.isfinite(o).all() and np.isfinite(S).all()
     _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, scale, "kda chunk strong decay")
 
@@ -281,7 +283,7 @@ def _check_bwd(res, ref, q, cu, what, k=None):
             G.compare(res["dS0"][s, h], ref["dS0"][s, h], TOL_DS0_FP32, None, f"{what} dS0 s{s} h{h}")
 
 
-@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128), (128, 256)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128), (128, 256)])
 def test_kda_chunk_bwd_matches_oracle(dk, dv):
     """Every gradient against the fp64 reverse mode of the chunk algebra:
     three chunks per sequence with a ragged tail, initial state and an
