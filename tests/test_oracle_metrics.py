@@ -1,4 +1,4 @@
-"""The error metrics every parity verdict goes through, pinned to values
+"""The error metrics every parity check goes through, pinned to values
 worked out by hand (CPU only).
 
 * rel_l2 is the relative L2 of the cuLA issue #126 reproduction (a 1e-30
