@@ -351,3 +351,17 @@ def test_kda_chunk_bwd_long_sequence():
     q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(1, 4096, 1, 128, 128, seed=215)
     res = _run_bwd(torch, q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs)
     _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, 128 ** -0.5, dO, dfs), q, cu, "kda bwd T=4096")
+
+
+def test_kda_chunk_beta_up_to_two():
+    """beta in (0, 2) (the range that allows negative eigenvalues of the
+    transition): forward through the workspace route and backward, at
+    d_k = 128, against the oracle."""
+    import torch
+    q, k, v, g, beta, s0, cu, dO, dfs = _bwd_case(2, 150, 2, 128, 128, seed=216)
+    beta = W.f32_to_bf16_bits(2.0 * W.bf16_bits_to_f32(beta))
+    scale = 128 ** -0.5
+    o, S = _run(torch, gdn.gdn_kda_chunk_fwd, q, k, v, g, beta, s0, cu, scale, tp=True)
+    _check_against_oracle(o, S, q, k, v, g, beta, s0, cu, scale, "kda beta<2")
+    res = _run_bwd(torch, q, k, v, g, beta, s0, cu, scale, dO, dfs)
+    _check_bwd(res, _bwd_ref(q, k, v, g, beta, s0, cu, scale, dO, dfs), q, cu, "kda bwd beta<2")
