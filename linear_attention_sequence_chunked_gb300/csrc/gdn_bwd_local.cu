@@ -16,20 +16,25 @@
 // tensor memory across 64-column value slices, so each CTA writes complete
 // gradients: no partial sums leave the chip.
 //
-// Persistent CTAs (one per SM, 256 threads) walk the (chunk, head, sequence)
-// items with a grid stride.  While one item's chunk-wide products run, the
-// next item's K/Q tiles (TMA), T tiles and first state tiles (bulk copies)
-// land in buffers the current item no longer reads: the K/Q tiles alternate
-// between two buffers, the other one holding the current item's -dBhat-side
-// tiles.  Within an item the next value slice's S0 tiles load into this
-// slice's dS buffer as soon as the products that read dS have completed, and
-// its dS tiles into this slice's S0 buffer after the last product that reads
-// S0 (the two state buffers swap roles every slice).  Warps w and w + 4
-// share a TMEM subpartition and
-// split the 64 columns of each accumulator row between them, and within a
-// warp lanes l and l + 16 take 16 columns each of row 16 w + l (tcgen05.ld
-// 16x32bx2), so every lane works in each epilogue.  Computed MMA
-// operands are split into bf16 hi + lo, accumulation is fp32.
+// Persistent CTAs (one per SM) walk the (chunk, head, sequence) items with a
+// grid stride.  Warps 0-7 load, run every epilogue and write the gradients;
+// warp 8 issues every MMA batch, each after a hand-off barrier that delivers
+// its operands (a long batch blocks the thread that issues it until the
+// tensor pipe has taken most of it, so an epilogue warp that issued would hold
+// up every barrier after it).  Warps 9-11 only complete the issuer's
+// warpgroup, whose registers go to the epilogue warpgroups.  While one item's
+// chunk-wide products run, the next item's K/Q tiles (TMA), T tiles and first
+// state tiles (bulk copies) land in buffers the current item no longer reads:
+// the K/Q tiles alternate between two buffers, the other one holding the
+// current item's -dBhat-side tiles.  Within an item the next value slice's S0
+// tiles load into this slice's dS buffer as soon as the products that read dS
+// have completed, and its dS tiles into this slice's S0 buffer after the last
+// product that reads S0 (the two state buffers swap roles every slice).
+// Warps w and w + 4 share a TMEM subpartition and split the 64 columns of each
+// accumulator row between them, and within a warp lanes l and l + 16 take 16
+// columns each of row 16 w + l (tcgen05.ld 16x32bx2), so every lane works in
+// each epilogue.  Computed MMA operands are split into bf16 hi + lo,
+// accumulation is fp32.
 #include <cuda.h>
 #include <string.h>
 
@@ -45,7 +50,14 @@ namespace {
 using namespace sm100;
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kEpi = 256;                 // warps 0-7: loads, epilogues, outputs
+constexpr int kIssuerWarp = 8;            // warp 8: issues every MMA (warps 9-11 idle)
+constexpr int kThreads = kEpi + 128;
+// registers: 168 a thread at launch (384 threads); the issuer's warpgroup
+// gives up 32 of them (its unrolled descriptor arithmetic needs ~130), the two
+// epilogue warpgroups take 16 more: 128 x 136 + 256 x 184 = 384 x 168
+constexpr int kRegLaunch = 168, kRegIssuer = 136, kRegEpi = 184;
+static_assert(128 * kRegIssuer + 256 * kRegEpi == kThreads * kRegLaunch, "register split");
 constexpr int kVs = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileS = kDk * 128;  // 128 rows x 128 B
@@ -70,13 +82,31 @@ constexpr int oRB = oRA + 2 * kTile64;          // dDelta -> -dBhat; later dQK [
 constexpr int oKQ1 = oRB + 2 * kTile64;         // [K;Q] of odd items; the other item's RC, RD tiles
 constexpr int oVec = oKQ1 + 2 * kRegionBytes;   // g, beta, G, gam, dec, colsum
 constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
-constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half
-constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles, off-path MMA
-constexpr int oMisc = oBar + 40;                // TMEM slot, abort flag
-constexpr int kBytes = oMisc + 16;
+constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half;
+                                                // earlier in the item's end the [4][64] partial column sums
+constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles, off-path MMA, drain
+constexpr int oMisc = oBar + 48;                // TMEM slot, abort flag
+constexpr int oDV = (oMisc + 16 + 1023) / 1024 * 1024;  // a full chunk's dV rows of one slice, staged for the TMA store
+constexpr int kBytes = oDV + kTile64;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 232448, "shared memory");
 static_assert(2 * kTile64 * 2 == 2 * kRegionBytes, "RC, RD fill a K/Q buffer");
+
+// Named barrier 1: the epilogue warps among themselves.
+__device__ __forceinline__ void epi_sync() { named_bar(1, kEpi); }
+
+// Named barrier 2: the hand-off of a batch's operands from the epilogue warps
+// to the issuer warp, which also ORs `pred` (a bounded wait ran out) over the
+// nine warps, so that both sides leave the item loop at the same hand-off.
+__device__ __forceinline__ bool handoff(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(kEpi + 32)
+        : "memory");
+    return r != 0;
+}
 
 // One (chunk, head, sequence) item.
 struct Item {
@@ -118,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dO Delta^T) are committed here, after the products an epilogue waits
     // for, so they run in that epilogue's window
     const uint32_t nbar = smem_u32(barp + 4);
+    // the issuer's last commit before the CTA leaves
+    const uint32_t dbar = smem_u32(barp + 5);
 
     // item f of the flat (chunk, head, sequence) order; false for chunks past
     // a sequence's end (and sequences whose bounds are invalid)
@@ -193,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(smem_u32(barp + i), 1);
+        for (int i = 0; i < 6; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
         *abort_flag = 0;
         if (use_tma) {
@@ -223,18 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t phase = 0;
     bool failed = false;  // a bounded wait ran out (reported through the error word)
-    auto mma_sync_wait = [&]() {
-        if (warp == 0) {
-            if (elect_one()) mma_commit(bar);
-            __syncwarp();
-        }
-        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) {
-            failed = true;
-            *abort_flag = 1;
-        }
-        phase ^= 1u;
-        tc_fence_after();
-    };
     // wait for the last commit on `bar` (issued inside an MMA batch)
     auto mma_wait = [&]() {
         if (!mbar_wait(bar, phase, kDefaultWaitLimit)) {
@@ -297,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long r0 = first_row(it);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const int e = tid + k * kThreads, r = e >> 3, ch = e & 7;
+            const int e = tid + k * kEpi, r = e >> 3, ch = e & 7;
             do_raw[k] = make_uint4(0, 0, 0, 0);
             if (r < nvv)
                 do_raw[k] = *reinterpret_cast<const uint4*>(
@@ -311,129 +331,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             v_raw[1] = src[1];
         }
     };
-    if (f < total) {
+    if (f < total && warp < kIssuerWarp) {
         fetch_gates(cur);
         fetch_rows(cur, 0);
     }
 
-    for (int k = 0; f < total; ++k) {
-        const int h = cur.h;
-        const int c0 = cur.t0 + cur.ci * kChunk;
-        const int nv = min(kChunk, cur.t1 - c0);
-        const long long row_base = static_cast<long long>(cur.b) * p.T;
-        const uint32_t oKQ = (k & 1) ? oKQ1 : oKQ0;   // this item's K/Q buffer
-        const uint32_t oRC = (k & 1) ? oKQ0 : oKQ1;   // -> dec o Delta, then free
-        const uint32_t oRD = oRC + 2 * kTile64;       // Y = -beta gam dBhat
-        const uint32_t aKQ = smem_u32(sm + oKQ);
-        auto kdesc_K = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + (s & 3) * 32, 0, 1024); };
-        auto kdesc_Q = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + 64 * 128 + (s & 3) * 32, 0, 1024); };
-        // K or Q read MN-major as a B operand [K = token][N = key column], N = 128
-        auto mn_K = [&](int s) { return desc_sw128(aKQ + s * 2048, kRegionBytes, 1024); };
-        auto mn_Q = [&](int s) { return desc_sw128(aKQ + 64 * 128 + s * 2048, kRegionBytes, 1024); };
-        auto t64 = [&](int off) { return smem_u32(sm + off); };
-
-        // ---- item inputs: gates; K/Q (d_k = 64: plain loads), T tiles ----
-        if (tid < 64) {
-            gv[tid] = g_pre;
-            bv[tid] = b_pre;
-        }
-        if (!use_tma) {
-            // rows beyond the chunk and key columns beyond d_k are zero
-            for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
-                const int which = e >> 10;                // 0: K, 1: Q
-                const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
-                const int r = (e >> 3) & 63, ch = e & 7;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (r < nv && region * 64 < dk) {
-                    const uint16_t* src = which ? p.q : p.k;
-                    val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
-                                                          region * 64 + ch * 8);
-                }
-                *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
-            }
-        }
-        wait_copy(ibar, iphase, i_out);
-        if (use_tma && nv < kChunk) {
-            // the box also read the rows after the chunk: zero them
-            for (int e = tid; e < 2 * 2 * 64 * 8; e += kThreads) {
-                const int which = e >> 10, region = (e >> 9) & 1, r = (e >> 3) & 63, ch = e & 7;
-                if (r >= nv)
-                    *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) =
-                        make_uint4(0, 0, 0, 0);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (*abort_flag) break;
-        if (tid < 32) {
-            const float a = gv[2 * tid];
-            const float bb = a + gv[2 * tid + 1];
-            float s = bb;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, s, off);
-                if (tid >= off) s += o;
-            }
-            const float base = s - bb;
-            Gv[2 * tid] = base + a;
-            Gv[2 * tid + 1] = s;
-            gam[2 * tid] = exp_nonpos(base + a);
-            gam[2 * tid + 1] = exp_nonpos(s);
-        }
-        __syncthreads();
-        if (tid < 64) dec[tid] = exp_nonpos(Gv[63] - Gv[tid]);
-
-        // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
-        if (warp == 0) {
+    if (warp >= kIssuerWarp) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegIssuer));
+      // warps 9-11 only complete the issuer's warpgroup
+      if (warp == kIssuerWarp) {
+        // ---- the issuer warp: every MMA batch, in the epilogue warps' order,
+        // each once the hand-off has delivered its operands; the epilogue
+        // warps never wait for an issue (a long batch blocks its issuing
+        // thread until the tensor pipe has taken most of it) ----
+        for (int k = 0; f < total; ++k) {
+            const uint32_t oKQ = (k & 1) ? oKQ1 : oKQ0;
+            const uint32_t oRC = (k & 1) ? oKQ0 : oKQ1;
+            const uint32_t oRD = oRC + 2 * kTile64;
+            const uint32_t aKQ = smem_u32(sm + oKQ);
+            auto kdesc_K = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + (s & 3) * 32, 0, 1024); };
+            auto kdesc_Q = [&](int s) { return desc_sw128(aKQ + (s >> 2) * kRegionBytes + 64 * 128 + (s & 3) * 32, 0, 1024); };
+            // K or Q read MN-major as a B operand [K = token][N = key column], N = 128
+            auto mn_K = [&](int s) { return desc_sw128(aKQ + s * 2048, kRegionBytes, 1024); };
+            auto mn_Q = [&](int s) { return desc_sw128(aKQ + 64 * 128 + s * 2048, kRegionBytes, 1024); };
+            auto t64 = [&](int off) { return smem_u32(sm + off); };
+            // P: Q K^T -> X1
+            if (handoff(false)) break;
             if (elect_one()) {
                 tc_fence_after();
                 constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
 #pragma unroll
                 for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
+                mma_commit(bar);
             }
             __syncwarp();
-        }
-        mma_sync_wait();
-        {
-            float row[16];
-            ld_cols(cX1, row);
-            tmem_ld_wait();
-            const float Gi = Gv[mrow];
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) row[kk] = (cb + kk <= mrow) ? row[kk] * exp_nonpos(Gi - Gv[cb + kk]) : 0.f;
-            store_cols(oP, mrow, row);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // per-row accumulators (thread mrow) across value slices
-        float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
-        for (int vs = 0; vs < nsl; ++vs) {
-            const int oS0 = (vs & 1) ? oSB : oSA;  // this slice's S0 tiles
-            const int oDS = (vs & 1) ? oSA : oSB;  // this slice's dS tiles
-            // ---- slice loads: S0 tiles, dO tile, V row ----
-            wait_copy(s0bar, s0phase, s0_out);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int e = tid + kk * kThreads, r = e >> 3, ch = e & 7;
-                *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[kk];
-            }
-            // columns cb .. cb + 15 of value row mrow
-            float vrow[16];
-            unpack8(v_raw[0], vrow);
-            unpack8(v_raw[1], vrow + 8);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            // the previous item's dq / dk and the previous slice's dV tile
-            // stores have read their source tiles (rewritten in this slice)
-            if (tid == 0) bulk_wait_read_all();
-            __syncthreads();
-
-            // ---- batch 1: K S0 -> X1, P^T dO -> X2, U += dO S0^T ----
-            if (warp == 0) {
+            bool quit = false;
+            for (int vs = 0; vs < nsl; ++vs) {
+                const int oS0 = (vs & 1) ? oSB : oSA;
+                const int oDS = (vs & 1) ? oSA : oSB;
+                // batch 1
+                if (handoff(false)) {
+                    quit = true;
+                    break;
+                }
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
@@ -462,27 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(nbar);
                 }
                 __syncwarp();
-            }
-            mma_wait();
-            float ks0[16], pdo[16];
-            ld_cols(cX1, ks0);
-            ld_cols(cX2, pdo);
-            tmem_ld_wait();
-            {
-                float row[16];
-                const float bj = bv[mrow], gj = gam[mrow];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
-                store_cols(oRA, mrow, row);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            // the dS tiles of this slice
-            wait_copy(dsbar, dsphase, ds_out);
-            __syncthreads();
-
-            // ---- batch 2: K dS -> X1, Delta = T R -> X2 ----
-            if (warp == 0) {
+                // batch 2
+                if (handoff(false)) {
+                    quit = true;
+                    break;
+                }
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
@@ -502,56 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cX2, th, rl, id_t, 1);
                         mma_bf16(tmem + cX2, tl, rh, id_t, 1);
                     }
+                    mma_commit(bar);
                 }
                 __syncwarp();
-            }
-            {
-                // <dS, S0> over 32 values of state row d (hi + lo is the fp32
-                // value to ~16 bits), while the batch runs
-                const int d = tid & 127, hs = tid >> 7;
-                if (d < dk) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
-                        float ah[8], al[8], bh[8], bl[8];
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + off), ah);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + kTileS + off), al);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + off), bh);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + kTileS + off), bl);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
-                    }
+                // batch 3
+                if (handoff(false)) {
+                    quit = true;
+                    break;
                 }
-            }
-            mma_sync_wait();
-            off_path_wait();  // U of this slice (long done: it ran in the R epilogue)
-            {
-                // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
-                // dec o Delta -> RC;  dd = dec * sum_v (K dS) Delta for the decay term of dG
-                const float dj = dec[mrow];
-                float dd = 0.f;
-                float kds[16], dl[16];
-                ld_cols(cX1, kds);
-                ld_cols(cX2, dl);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    dd = fmaf(kds[c], dl[c], dd);
-                    kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
-                }
-                store_cols(oRB, mrow, kds);
-                store_cols(oRA, mrow, dl);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) dl[c] *= dj;
-                store_cols(oRC, mrow, dl);
-                acc_dd = fmaf(dj, dd, acc_dd);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-
-            // ---- batch 3: dBhat = T^T dDelta -> X1;  dK += (dec o Delta) dS^T;  dP += dO Delta^T (off the path) ----
-            if (warp == 0) {
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
@@ -567,7 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cX1, th, dl, id_b, 1);
                         mma_bf16(tmem + cX1, tl, dh, id_b, 1);
                     }
-                    // B = dS tile read K-major: [N = key row d][K = value column]
+                    mma_commit(bar);  // dBhat: the dV epilogue reads it
+                    // the rest is read only at the item's end and runs in the dV
+                    // epilogue: dK += (dec o Delta) dS^T, the last reader of the dS
+                    // tiles (B = dS tile read K-major: [N = key row d][K = value column])
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t eh = desc_sw128(t64(oRC) + s * 32, 0, 1024);
@@ -578,8 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, eh, sbl, id_n, 1);
                         mma_bf16(tmem + cdK, el, sbh, id_n, 1);
                     }
-                    mma_commit(bar);  // dBhat (the dV epilogue) and the last reader of the dS tiles
-                    // dP += dO Delta^T, read only at the item's end: it runs in the dV epilogue
+                    // dP += dO Delta^T
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
@@ -591,63 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(nbar);
                 }
                 __syncwarp();
-            }
-            mma_wait();
-            // every product that reads this slice's dS tiles has completed
-            // the next slice's S0 goes into this slice's (now free) dS buffer
-            if (tid == 0 && vs + 1 < nsl && !failed) issue_s0(cur, vs + 1, oDS);
-            {
-                // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RB, Y -> RD
-                const float bi = bv[mrow], gi = gam[mrow];
-                float sv = 0.f, sk = 0.f;
-                float db[16], t16[16];
-                ld_cols(cX1, db);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    sv = fmaf(vrow[c], db[c], sv);
-                    sk = fmaf(ks0[c], db[c], sk);
+                // batch 4
+                if (handoff(false)) {
+                    quit = true;
+                    break;
                 }
-                uint4 dv4[2];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
-                    dv4[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-                if (nv == kChunk) {
-                    // a full chunk stages this slice's dV rows in the dead (dec o
-                    // Delta) tile, 128-byte swizzled, for one TMA store
-#pragma unroll
-                    for (int half = 0; half < 2; ++half)
-                        *reinterpret_cast<uint4*>(sm + oRC + sw128_offset(mrow, cb * 2 + 16 * half)) = dv4[half];
-                } else if (mrow < nv) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) dst[half] = dv4[half];
-                }
-#pragma unroll
-                for (int c = 0; c < 16; ++c) t16[c] = -db[c];
-                store_cols(oRB, mrow, t16);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
-                store_cols(oRD, mrow, t16);
-                acc_dbeta += sv - gi * sk;
-                acc_dgam -= bi * sk;
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (nv == kChunk && tid == 0) {
-                tma_store_3d(&tmap_dv, vs * kVs, h, static_cast<int>(row_base + c0), smem_u32(sm + oRC));
-                bulk_commit();
-            }
-
-            // ---- batch 4: dA += (-dBhat) Delta^T;  dK += Y S0^T ----
-            if (warp == 0) {
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
@@ -679,18 +511,312 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
                         }
                     }
+                    mma_commit(bar);
                 }
                 __syncwarp();
             }
-            if (vs + 1 < nsl) fetch_rows(cur, vs + 1);  // while the batch runs
-            mma_sync_wait();
+            if (quit) break;
+            Item nxt{};
+            const long long fn = next_valid(f + gridDim.x, nxt);
+            // final products
+            if (handoff(false)) break;
+            if (elect_one()) {
+                tc_fence_after();
+                constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
+                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                    const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
+                    mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
+                }
+                mma_commit(bar);  // dQ2: the dq outputs read it
+                // the dK products complete while the dq outputs are formed
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                    const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                    mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
+                    mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
+                    const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
+                    const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
+                    const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
+                    const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
+                    mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
+                    mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
+                    mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
+                    mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
+                }
+                mma_commit(nbar);
+            }
+            __syncwarp();
+            cur = nxt;
+            f = fn;
+        }
+        // the CTA leaves once every product it issued has completed
+        if (elect_one()) mma_commit(dbar);
+        __syncwarp();
+        if (!mbar_wait(dbar, 0, kDefaultWaitLimit)) record_error(p.err, kErrTimeout);
+      }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegEpi));
+    for (int k = 0; f < total; ++k) {
+        const int h = cur.h;
+        const int c0 = cur.t0 + cur.ci * kChunk;
+        const int nv = min(kChunk, cur.t1 - c0);
+        const long long row_base = static_cast<long long>(cur.b) * p.T;
+        const uint32_t oKQ = (k & 1) ? oKQ1 : oKQ0;   // this item's K/Q buffer
+        const uint32_t oRC = (k & 1) ? oKQ0 : oKQ1;   // -> dec o Delta, then free
+        const uint32_t oRD = oRC + 2 * kTile64;       // Y = -beta gam dBhat
+
+        // ---- item inputs: gates; K/Q (d_k = 64: plain loads), T tiles ----
+        if (tid < 64) {
+            gv[tid] = g_pre;
+            bv[tid] = b_pre;
+        }
+        if (!use_tma) {
+            // rows beyond the chunk and key columns beyond d_k are zero
+            for (int e = tid; e < 2 * 2 * 64 * 8; e += kEpi) {
+                const int which = e >> 10;                // 0: K, 1: Q
+                const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
+                const int r = (e >> 3) & 63, ch = e & 7;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (r < nv && region * 64 < dk) {
+                    const uint16_t* src = which ? p.q : p.k;
+                    val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                          region * 64 + ch * 8);
+                }
+                *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+            }
+        }
+        wait_copy(ibar, iphase, i_out);
+        if (use_tma && nv < kChunk) {
+            // the box also read the rows after the chunk: zero them
+            for (int e = tid; e < 2 * 2 * 64 * 8; e += kEpi) {
+                const int which = e >> 10, region = (e >> 9) & 1, r = (e >> 3) & 63, ch = e & 7;
+                if (r >= nv)
+                    *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) =
+                        make_uint4(0, 0, 0, 0);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        // hand-off: the issuer warp starts Q K^T (both sides leave here, and
+        // at every later hand-off, if a bounded wait ran out)
+        if (handoff(*abort_flag != 0)) break;
+        if (tid < 32) {
+            const float a = gv[2 * tid];
+            const float bb = a + gv[2 * tid + 1];
+            float s = bb;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, s, off);
+                if (tid >= off) s += o;
+            }
+            const float base = s - bb;
+            Gv[2 * tid] = base + a;
+            Gv[2 * tid + 1] = s;
+            gam[2 * tid] = exp_nonpos(base + a);
+            gam[2 * tid + 1] = exp_nonpos(s);
+        }
+        // the previous item's dq tile store has read the P tiles' space
+        if (tid == 0) bulk_wait_read_all();
+        epi_sync();
+        if (tid < 64) dec[tid] = exp_nonpos(Gv[63] - Gv[tid]);
+
+        // ---- P = (Q K^T) o M (j <= i) as operand tiles ----
+        mma_wait();
+        // decay factors exp(G_i - G_j) (j <= i) of row mrow, columns cb .. cb + 15:
+        // the P epilogue and the item's end both read them
+        float mdec[16];
+        {
+            float row[16];
+            ld_cols(cX1, row);
+            tmem_ld_wait();
+            const float Gi = Gv[mrow];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                mdec[kk] = (cb + kk <= mrow) ? exp_nonpos(Gi - Gv[cb + kk]) : 0.f;
+                row[kk] = (cb + kk <= mrow) ? row[kk] * mdec[kk] : 0.f;
+            }
+            store_cols(oP, mrow, row);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+
+        // per-row accumulators (thread mrow) across value slices
+        float acc_dbeta = 0.f, acc_dgam = 0.f, acc_dd = 0.f, acc_SdS = 0.f;
+        bool quit = false;
+        for (int vs = 0; vs < nsl; ++vs) {
+            const int oS0 = (vs & 1) ? oSB : oSA;  // this slice's S0 tiles
+            const int oDS = (vs & 1) ? oSA : oSB;  // this slice's dS tiles
+            // ---- slice loads: S0 tiles, dO tile, V row ----
+            wait_copy(s0bar, s0phase, s0_out);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const int e = tid + kk * kEpi, r = e >> 3, ch = e & 7;
+                *reinterpret_cast<uint4*>(sm + oDO + sw128_offset(r, ch * 16)) = do_raw[kk];
+            }
+            // columns cb .. cb + 15 of value row mrow
+            float vrow[16];
+            unpack8(v_raw[0], vrow);
+            unpack8(v_raw[1], vrow + 8);
+            // the next slice's rows load while this slice runs
+            if (vs + 1 < nsl) fetch_rows(cur, vs + 1);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // the previous item's dq / dk and the previous slice's dV tile
+            // stores have read their source tiles (rewritten in this slice)
+            if (tid == 0) bulk_wait_read_all();
+            // ---- batch 1 (issuer): K S0 -> X1, P^T dO -> X2, U += dO S0^T ----
+            if (handoff(*abort_flag != 0)) {
+                quit = true;
+                break;
+            }
+            mma_wait();
+            float ks0[16], pdo[16];
+            ld_cols(cX1, ks0);
+            ld_cols(cX2, pdo);
+            tmem_ld_wait();
+            {
+                float row[16];
+                const float bj = bv[mrow], gj = gam[mrow];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) row[c] = bj * (vrow[c] - gj * ks0[c]);
+                store_cols(oRA, mrow, row);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // the dS tiles of this slice
+            wait_copy(dsbar, dsphase, ds_out);
+            // ---- batch 2 (issuer): K dS -> X1, Delta = T R -> X2 ----
+            if (handoff(*abort_flag != 0)) {
+                quit = true;
+                break;
+            }
+            {
+                // <dS, S0> over 32 values of state row d (hi + lo is the fp32
+                // value to ~16 bits), while the batch runs
+                const int d = tid & 127, hs = tid >> 7;
+                if (d < dk) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t off = sw128_offset(d, (4 * hs + c4) * 16);
+                        float ah[8], al[8], bh[8], bl[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + off), ah);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oS0 + kTileS + off), al);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + off), bh);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + oDS + kTileS + off), bl);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc_SdS = fmaf(ah[e] + al[e], bh[e] + bl[e], acc_SdS);
+                    }
+                }
+            }
+            mma_wait();
+            off_path_wait();  // U of this slice (long done: it ran in the R epilogue)
+            {
+                // dDelta = scale P^T dO + dec o (K dS) -> RB;  Delta -> RA (replaces R);
+                // dec o Delta -> RC;  dd = dec * sum_v (K dS) Delta for the decay term of dG
+                const float dj = dec[mrow];
+                float dd = 0.f;
+                float kds[16], dl[16];
+                ld_cols(cX1, kds);
+                ld_cols(cX2, dl);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    dd = fmaf(kds[c], dl[c], dd);
+                    kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
+                }
+                store_cols(oRB, mrow, kds);
+                store_cols(oRA, mrow, dl);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) dl[c] *= dj;
+                store_cols(oRC, mrow, dl);
+                acc_dd = fmaf(dj, dd, acc_dd);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // ---- batch 3 (issuer): dBhat = T^T dDelta -> X1;  dK += (dec o Delta) dS^T;
+            // dP += dO Delta^T (off the path) ----
+            if (handoff(*abort_flag != 0)) {
+                quit = true;
+                break;
+            }
+            mma_wait();
+            {
+                // dV = beta o dBhat; dbeta / dgam row terms; -dBhat -> RB, Y -> RD
+                const float bi = bv[mrow], gi = gam[mrow];
+                float sv = 0.f, sk = 0.f;
+                float db[16], t16[16];
+                ld_cols(cX1, db);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    sv = fmaf(vrow[c], db[c], sv);
+                    sk = fmaf(ks0[c], db[c], sk);
+                }
+                uint4 dv4[2];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16x2(bi * db[half * 8 + 2 * e], bi * db[half * 8 + 2 * e + 1]);
+                    dv4[half] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                if (nv == kChunk) {
+                    // a full chunk stages this slice's dV rows, 128-byte
+                    // swizzled, for one TMA store
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+                        *reinterpret_cast<uint4*>(sm + oDV + sw128_offset(mrow, cb * 2 + 16 * half)) = dv4[half];
+                } else if (mrow < nv) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.dv + ((row_base + c0 + mrow) * H + h) * static_cast<long long>(V) + vs * kVs + cb);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) dst[half] = dv4[half];
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) t16[c] = -db[c];
+                store_cols(oRB, mrow, t16);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) t16[c] = -bi * gi * db[c];
+                store_cols(oRD, mrow, t16);
+                acc_dbeta += sv - gi * sk;
+                acc_dgam -= bi * sk;
+            }
+            // once dK += (dec o Delta) dS^T has completed, the next slice's S0
+            // goes into this slice's dS buffer (the wait leaves the phase to
+            // the off-path wait at the slice's end)
+            if (tid == 0 && vs + 1 < nsl && !failed) {
+                if (mbar_wait(nbar, nphase, kDefaultWaitLimit)) {
+                    issue_s0(cur, vs + 1, oDS);
+                } else {
+                    failed = true;
+                    *abort_flag = 1;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // ---- batch 4 (issuer): dA += (-dBhat) Delta^T;  dK += Y S0^T ----
+            if (handoff(*abort_flag != 0)) {
+                quit = true;
+                break;
+            }
+            // the hand-off also completed this slice's dV tile
+            if (nv == kChunk && tid == 0) {
+                tma_store_3d(&tmap_dv, vs * kVs, h, static_cast<int>(row_base + c0), smem_u32(sm + oDV));
+                bulk_commit();
+            }
+            mma_wait();
             off_path_wait();  // dP: the next slice rewrites the dO and Delta tiles it reads
-            __syncthreads();
+            epi_sync();
             // the S0 tiles are free: the next slice's dS goes there
             if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1, oS0);
-            if (*abort_flag) break;
         }
-        if (*abort_flag) break;
+        if (quit) break;
 
         // ---- the next item's inputs land while this item's chunk-wide part
         // runs: K/Q into the other buffer (RC, RD are dead), T, slice 0 states
@@ -700,7 +826,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- chunk-wide part (K K^T and Q K^T came with the last slice's batch) ----
         if (fn < total && tid == 0 && !failed) {
-            bulk_wait_read_all();  // the last slice's dV tile store has read its source
             issue_inputs(nxt, smem_u32(sm + oRC));
             issue_s0(nxt, 0, oSA);
             issue_ds(nxt, 0, oSB);
@@ -712,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rowsum = 0.f, dbeta_a = 0.f;
         {
             const int i = mrow;
-            const float Gi = Gv[i], bi = bv[i];
+            const float bi = bv[i];
             float kk[16], da[16], qk[16], dp[16];
             const int col = cb;
             ld_cols(cX1, kk);
@@ -724,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int j = col + c;
-                const float m = (j <= i) ? exp_nonpos(Gi - Gv[j]) : 0.f;
+                const float m = mdec[c];
                 // A side (strictly lower): dA o (K K^T o Ms)
                 const float kkm = (j < i) ? kk[c] * m : 0.f;
                 const float a = (j < i) ? da[c] : 0.f;
@@ -737,7 +862,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 e16[c] = dms + dpm * qk[c];
                 rowsum += e16[c];
             }
-            // stores after the loop: they may alias the decay loads
 #pragma unroll
             for (int c = 0; c < 16; ++c) E[i * 64 + ((col + c) ^ (i & 31))] = e16[c];
             store_cols(oRA, i, dkk);
@@ -752,47 +876,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (tid < 64) {
+        // ---- final products (issuer): dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
+        if (handoff(*abort_flag != 0)) break;
+        // column sums of E while the products run: four partial sums of 16
+        // rows per column, then their sum
+        {
+            float* cpart = reinterpret_cast<float*>(sm + oPart);
+            const int col = tid & 63, r0 = 16 * (tid >> 6);
             float c = 0.f;
-            for (int i = 0; i < 64; ++i) c += E[i * 64 + (tid ^ (i & 31))];
-            colsum[tid] = c;
-        }
-        // ---- final products: dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
-        if (warp == 0) {
-            if (elect_one()) {
-                tc_fence_after();
-                constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
-                constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-                    const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-                    const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                    const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                    mma_bf16(tmem + cX1, qh, mn_K(s), id_n, s > 0);
-                    mma_bf16(tmem + cX1, ql, mn_K(s), id_n, 1);
-                    mma_bf16(tmem + cdK, kh, mn_K(s), id_n, 1);
-                    mma_bf16(tmem + cdK, kl, mn_K(s), id_n, 1);
-                    const uint64_t qth = desc_sw128(t64(oRB) + s * 2048, kTile64, 1024);
-                    const uint64_t qtl = desc_sw128(t64(oRB + kTile64) + s * 2048, kTile64, 1024);
-                    const uint64_t kth = desc_sw128(t64(oRA) + s * 2048, kTile64, 1024);
-                    const uint64_t ktl = desc_sw128(t64(oRA + kTile64) + s * 2048, kTile64, 1024);
-                    mma_bf16(tmem + cdK, qth, mn_Q(s), id_t, 1);
-                    mma_bf16(tmem + cdK, qtl, mn_Q(s), id_t, 1);
-                    mma_bf16(tmem + cdK, kth, mn_K(s), id_t, 1);
-                    mma_bf16(tmem + cdK, ktl, mn_K(s), id_t, 1);
-                }
-            }
-            __syncwarp();
+            for (int i = r0; i < r0 + 16; ++i) c += E[i * 64 + (col ^ (i & 31))];
+            cpart[tid] = c;
         }
         // gates and the first slice's rows of the next item, while the products run
         if (fn < total) {
             fetch_gates(nxt);
             fetch_rows(nxt, 0);
         }
-        mma_sync_wait();
-        __syncthreads();
+        epi_sync();
+        if (tid < 64) {
+            const float* cpart = reinterpret_cast<const float*>(sm + oPart);
+            colsum[tid] = (cpart[tid] + cpart[64 + tid]) + (cpart[128 + tid] + cpart[192 + tid]);
+        }
+        mma_wait();  // dQ2
+        epi_sync();
         // ---- outputs of row mrow (key columns 64 hc .. 64 hc + 63: 16-column
         // groups 4 hc + 2 r + lane / 16 of this lane) ----
         float dG = 0.f, dbeta = 0.f;
@@ -801,62 +908,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gi = gam[i];
             // U = dO S0^T: dQ term scale gam U and dgam term scale q . U
             float dgq = 0.f;
-            // all six accumulator reads in flight before the one wait
-            float u[2][16], q2[2][16], kk2[2][16];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
-                tmem_ld_pair16(tmem + lb + cU + cpair, u[r]);
-                tmem_ld_pair16(tmem + lb + cX1 + cpair, q2[r]);
-                tmem_ld_pair16(tmem + lb + cdK + cpair, kk2[r]);
-            }
-            tmem_ld_wait();
-            // a full chunk at d_k = 128 stages its dq / dk rows in the (free) R
-            // tiles, 128-byte swizzled like the q / k tiles, for one TMA store
-            // per 64-column region: consecutive tokens are H d_k apart in
+            // a full chunk at d_k = 128 stages its dq / dk rows, 128-byte
+            // swizzled like the q / k tiles, for one TMA store per 64-column
+            // region (dq in the dead E scratch, dk in the dQK tiles once the dK
+            // products have read them): consecutive tokens are H d_k apart in
             // global memory, so per-thread 16-byte stores would touch a sector
             // each; a ragged chunk stores per thread (a box would cross into
             // the next rows)
             const bool tma_out = use_tma && nv == kChunk;
+            {
+                float u[2][16], q2[2][16];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int c16 = 4 * hc + 2 * r + (lane >> 4);
-                const int region = c16 >> 2, cc = (c16 & 3) * 16;
-                float qrow[16];
-                {
-                    const uint8_t* base = sm + oKQ + region * kRegionBytes + 64 * 128;
-                    unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2)), qrow);
-                    unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t cpair = 64 * hc + 32 * r;  // lanes 16-31 read 16 columns further
+                    tmem_ld_pair16(tmem + lb + cU + cpair, u[r]);
+                    tmem_ld_pair16(tmem + lb + cX1 + cpair, q2[r]);
                 }
+                tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[r][e], dgq);
-                uint4 wq4[2], wk4[2];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t wq[4], wk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = half * 8 + 2 * e;
-                        wq[e] = pack_bf16x2(fmaf(scale * gi, u[r][c], q2[r][c]), fmaf(scale * gi, u[r][c + 1], q2[r][c + 1]));
-                        wk[e] = pack_bf16x2(kk2[r][c], kk2[r][c + 1]);
+                for (int r = 0; r < 2; ++r) {
+                    const int c16 = 4 * hc + 2 * r + (lane >> 4);
+                    const int region = c16 >> 2, cc = (c16 & 3) * 16;
+                    float qrow[16];
+                    {
+                        const uint8_t* base = sm + oKQ + region * kRegionBytes + 64 * 128;
+                        unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2)), qrow);
+                        unpack8(*reinterpret_cast<const uint4*>(base + sw128_offset(i, cc * 2 + 16)), qrow + 8);
                     }
-                    wq4[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                    wk4[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-                }
-                if (tma_out) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dgq = fmaf(scale * qrow[e], u[r][e], dgq);
+                    uint4 wq4[2];
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        const uint32_t off = region * kTile64 + sw128_offset(i, cc * 2 + 16 * half);
-                        *reinterpret_cast<uint4*>(sm + oRA + off) = wq4[half];
-                        *reinterpret_cast<uint4*>(sm + oRB + off) = wk4[half];
+                        uint32_t wq[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = half * 8 + 2 * e;
+                            wq[e] = pack_bf16x2(fmaf(scale * gi, u[r][c], q2[r][c]), fmaf(scale * gi, u[r][c + 1], q2[r][c + 1]));
+                        }
+                        wq4[half] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                     }
-                } else if (i < nv && c16 * 16 < dk) {
-                    uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
-                    uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+                    if (tma_out) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+                            *reinterpret_cast<uint4*>(sm + oP + region * kTile64 + sw128_offset(i, cc * 2 + 16 * half)) = wq4[half];
+                    } else if (i < nv && c16 * 16 < dk) {
+                        uint4* dq = reinterpret_cast<uint4*>(p.dq + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) dq[half] = wq4[half];
+                    }
+                }
+            }
+            off_path_wait();  // the dK products
+            {
+                float kk2[2][16];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) tmem_ld_pair16(tmem + lb + cdK + 64 * hc + 32 * r, kk2[r]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int c16 = 4 * hc + 2 * r + (lane >> 4);
+                    const int region = c16 >> 2, cc = (c16 & 3) * 16;
+                    uint4 wk4[2];
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        dq[half] = wq4[half];
-                        dkp[half] = wk4[half];
+                        uint32_t wk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = half * 8 + 2 * e;
+                            wk[e] = pack_bf16x2(kk2[r][c], kk2[r][c + 1]);
+                        }
+                        wk4[half] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    }
+                    if (tma_out) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+                            *reinterpret_cast<uint4*>(sm + oRB + region * kTile64 + sw128_offset(i, cc * 2 + 16 * half)) = wk4[half];
+                    } else if (i < nv && c16 * 16 < dk) {
+                        uint4* dkp = reinterpret_cast<uint4*>(p.dk + ((row_base + c0 + i) * H + h) * static_cast<long long>(dk) + c16 * 16);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) dkp[half] = wk4[half];
                     }
                 }
             }
@@ -884,12 +1015,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 part[3] = rowsum;
                 part[4] = dbeta_a;
             }
-            __syncthreads();
+            epi_sync();
             if (tma_out && tid == 0) {
                 const int z = static_cast<int>(row_base + c0);
 #pragma unroll
                 for (int region = 0; region < 2; ++region) {
-                    tma_store_3d(&tmap_dq, region * 64, h, z, smem_u32(sm + oRA + region * kTile64));
+                    tma_store_3d(&tmap_dq, region * 64, h, z, smem_u32(sm + oP + region * kTile64));
                     tma_store_3d(&tmap_dk, region * 64, h, z, smem_u32(sm + oRB + region * kTile64));
                 }
                 bulk_commit();
@@ -908,12 +1039,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dbeta = acc_dbeta + part[0] + dbeta_a + part[4];
             }
         }
-        __syncthreads();
+        epi_sync();
         if (lead && hc == 0) {
             colsum[mrow] = dG;  // reuse as dG vector
             bv[mrow] = dbeta;   // reuse as dbeta vector
         }
-        __syncthreads();
+        epi_sync();
         // dg = reverse running sum of dG over the chunk (warp 0)
         if (tid < 32) {
             const int i0 = 63 - 2 * tid, i1 = 62 - 2 * tid;
@@ -936,24 +1067,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.dbeta[row] = f32_to_bf16(bv[i1]);
             }
         }
-        __syncthreads();
+        epi_sync();
         cur = nxt;
         f = fn;
     }
     if (failed) {
         record_error(p.err, kErrTimeout);
     }
-    // let every MMA and copy this CTA issued land before it leaves
-    if (warp == 0) {
-        if (elect_one()) mma_commit(bar);
-        __syncwarp();
-    }
+    // let every copy this thread issued land before the CTA leaves
     if (tid == 0) {
-        mbar_wait(bar, phase, kDefaultWaitLimit);
         if (i_out) mbar_wait(ibar, iphase, kDefaultWaitLimit);
         if (s0_out) mbar_wait(s0bar, s0phase, kDefaultWaitLimit);
         if (ds_out) mbar_wait(dsbar, dsphase, kDefaultWaitLimit);
         bulk_wait_all();  // the dq / dk tile stores
+    }
     }
     tc_fence_before();
     __syncthreads();
