@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(nbar);
                 }
                 __syncwarp();
-                // batch 2
+                // batch 2: K dS (runs in the R epilogue), then T R
                 if (handoff(false)) {
                     quit = true;
                     break;
@@ -410,12 +410,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-                    constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
                     for (int s = 0; s < kDk / 16; ++s) {
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS) + s * 2048, kTileS, 1024), id_k, s > 0);
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
                     }
+                }
+                __syncwarp();
+                if (handoff(false)) {
+                    quit = true;
+                    break;
+                }
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
@@ -437,8 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
-                    constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
-                    constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
@@ -450,9 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cX1, tl, dh, id_b, 1);
                     }
                     mma_commit(bar);  // dBhat: the dV epilogue reads it
-                    // the rest is read only at the item's end and runs in the dV
-                    // epilogue: dK += (dec o Delta) dS^T, the last reader of the dS
-                    // tiles (B = dS tile read K-major: [N = key row d][K = value column])
+                }
+                __syncwarp();
+                // batch 3, second part (once Delta and dec o Delta are stored):
+                // read only at the item's end, it runs in the dV epilogue
+                if (handoff(false)) {
+                    quit = true;
+                    break;
+                }
+                if (elect_one()) {
+                    tc_fence_after();
+                    constexpr uint32_t id_p = idesc(kFmtBf16, 0, 0, 64, 64);
+                    constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
+                    // dK += (dec o Delta) dS^T, the last reader of the dS tiles
+                    // (B = dS tile read K-major: [N = key row d][K = value column])
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t eh = desc_sw128(t64(oRC) + s * 32, 0, 1024);
@@ -486,13 +503,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        const uint64_t ch_ = desc_sw128(t64(oRB) + s * 32, 0, 1024);
-                        const uint64_t cl_ = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
-                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
-                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
-                        mma_bf16(tmem + cdA, ch_, dh, id_c, (vs > 0 || s > 0) ? 1u : 0u);
-                        mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
-                        mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
                         const uint64_t sah = desc_sw128(t64(oS0) + s * 32, 0, 1024);
                         const uint64_t sal = desc_sw128(t64(oS0 + kTileS) + s * 32, 0, 1024);
                         const uint64_t yh = desc_sw128(t64(oRD) + s * 32, 0, 1024);
@@ -500,6 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, yh, sah, id_n, 1);
                         mma_bf16(tmem + cdK, yh, sal, id_n, 1);
                         mma_bf16(tmem + cdK, yl, sah, id_n, 1);
+                    }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ch_ = desc_sw128(t64(oRB) + s * 32, 0, 1024);
+                        const uint64_t cl_ = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
+                        const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
+                        const uint64_t dl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
+                        mma_bf16(tmem + cdA, ch_, dh, id_c, (vs > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem + cdA, ch_, dl, id_c, 1);
+                        mma_bf16(tmem + cdA, cl_, dh, id_c, 1);
                     }
                     if (vs + 1 == nsl) {
                         // chunk-wide part: K K^T and Q K^T (M = 64 each) into the
@@ -679,6 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ld_cols(cX1, ks0);
             ld_cols(cX2, pdo);
             tmem_ld_wait();
+            tc_fence_before();
+            // the dS tiles of this slice
+            wait_copy(dsbar, dsphase, ds_out);
+            // ---- batch 2 (issuer), first part: K dS -> X1 (X1 and X2 are
+            // read), while R is formed ----
+            if (handoff(*abort_flag != 0)) {
+                quit = true;
+                break;
+            }
             {
                 float row[16];
                 const float bj = bv[mrow], gj = gam[mrow];
@@ -688,9 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            // the dS tiles of this slice
-            wait_copy(dsbar, dsphase, ds_out);
-            // ---- batch 2 (issuer): K dS -> X1, Delta = T R -> X2 ----
+            // ---- batch 2 (issuer), second part: Delta = T R -> X2 ----
             if (handoff(*abort_flag != 0)) {
                 quit = true;
                 break;
@@ -724,12 +751,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ld_cols(cX1, kds);
                 ld_cols(cX2, dl);
                 tmem_ld_wait();
+                tc_fence_before();
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     dd = fmaf(kds[c], dl[c], dd);
                     kds[c] = fmaf(scale, pdo[c], dj * kds[c]);
                 }
                 store_cols(oRB, mrow, kds);
+                fence_proxy_async_smem();
+                // ---- batch 3 (issuer): dBhat = T^T dDelta -> X1 ----
+                if (handoff(*abort_flag != 0)) {
+                    quit = true;
+                    break;
+                }
                 store_cols(oRA, mrow, dl);
 #pragma unroll
                 for (int c = 0; c < 16; ++c) dl[c] *= dj;
@@ -737,9 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_dd = fmaf(dj, dd, acc_dd);
             }
             fence_proxy_async_smem();
-            tc_fence_before();
-            // ---- batch 3 (issuer): dBhat = T^T dDelta -> X1;  dK += (dec o Delta) dS^T;
-            // dP += dO Delta^T (off the path) ----
+            // ---- batch 3, second part (issuer): dK += (dec o Delta) dS^T;  dP +=
+            // dO Delta^T (off the path) ----
             if (handoff(*abort_flag != 0)) {
                 quit = true;
                 break;
