@@ -851,18 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (quit) break;
 
-        // ---- the next item's inputs land while this item's chunk-wide part
-        // runs: K/Q into the other buffer (RC, RD are dead), T, slice 0 states
-        // (issued below, after the first chunk-wide products)
         Item nxt{};
         const long long fn = next_valid(f + gridDim.x, nxt);
 
         // ---- chunk-wide part (K K^T and Q K^T came with the last slice's batch) ----
-        if (fn < total && tid == 0 && !failed) {
-            issue_inputs(nxt, smem_u32(sm + oRC));
-            issue_s0(nxt, 0, oSA);
-            issue_ds(nxt, 0, oSB);
-        }
         // column-sum terms E [64][64] fp32 in the (dead) P tiles, column index
         // XOR-swizzled by the row so that row-parallel writes and
         // column-parallel reads both spread over the banks
@@ -911,6 +903,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         // ---- final products (issuer): dQ2 = dQK K -> X1..X2;  dK += dQK^T Q + dKK K + dKK^T K ----
         if (handoff(*abort_flag != 0)) break;
+        // the next item's inputs land while this item's end runs: K/Q into the
+        // other buffer (RC, RD are dead), T, slice 0 states (issued after the
+        // hand-off, so that no epilogue warp waits for the issuing thread)
+        if (fn < total && tid == 0 && !failed) {
+            issue_inputs(nxt, smem_u32(sm + oRC));
+            issue_s0(nxt, 0, oSA);
+            issue_ds(nxt, 0, oSB);
+        }
         // column sums of E while the products run: four partial sums of 16
         // rows per column, then their sum
         {
