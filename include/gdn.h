@@ -452,6 +452,32 @@ GDN_API gdn_status gdn_chunk_fwd_wait_limit(const gdn_bf16* q, const gdn_bf16* k
                                     int stall_first_wait, cudaStream_t stream);
 
 /*
+ * gdn_chunk_bwd_saved with a caller-chosen bound on the hand-off waits of the
+ * chunk-parallel gradient pass (mbarrier waits between its epilogue warps and
+ * its MMA-issuing warp), for exercising failure detection; the reverse chain
+ * of state gradients keeps the default bound.  wait_limit counts polls (0 =
+ * the default).  With stall_first_wait != 0 the epilogue warps of every CTA
+ * first wait on a barrier that nothing signals, so that wait runs out: at the
+ * next hand-off every warp of the CTA (the issuing warp included) leaves its
+ * loop, the CTA waits with the default bound for every copy and product it
+ * started, records GDN_ERR_TIMEOUT in the device error word (read it with
+ * gdn_get_last_device_error) and writes no gradient of dq, dk, dv, dg or
+ * dbeta, so the context stays usable.  Library bookkeeping with no
+ * counterpart on the pages.  Other arguments and errors as
+ * gdn_chunk_bwd_saved.
+ */
+GDN_API gdn_status gdn_chunk_bwd_saved_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                          const float* g, const gdn_bf16* beta, float scale,
+                                          const int32_t* cu_seqlens,
+                                          const gdn_bf16* d_out, const float* d_final_state,
+                                          gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                                          gdn_bf16* dbeta, float* d_initial_state,
+                                          int B, int T, int H, int d_k, int d_v,
+                                          const void* saved, size_t saved_bytes,
+                                          void* workspace, size_t workspace_bytes, uint32_t wait_limit,
+                                          int stall_first_wait, cudaStream_t stream);
+
+/*
  * Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points).  Library bookkeeping with no counterpart
  * on the pages; lets a caller count the kernels inside a timed region.

@@ -171,7 +171,8 @@ gdn_status launch_bwd_passes(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
                              const float* d_final_state, gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv,
                              float* dg, gdn_bf16* dbeta, float* d_initial_state, int B, int T,
                              int H, int d_k, int d_v, const float* states, float* dstates,
-                             const uint8_t* tiles, int* err, cudaStream_t stream) {
+                             const uint8_t* tiles, int* err, cudaStream_t stream,
+                             uint32_t local_wait_limit = gdn::kDefaultWaitLimit, int local_stall = 0) {
     gdn::BwdChainArgs c{};
     c.q = q; c.k = k; c.g = g; c.beta = beta; c.d_out = d_out; c.scale = scale;
     c.cu_seqlens = cu_seqlens; c.d_final_state = d_final_state;
@@ -184,6 +185,7 @@ gdn_status launch_bwd_passes(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf1
     l.cu_seqlens = cu_seqlens; l.chunk_states = states; l.chunk_dstates = dstates; l.chunk_T = tiles;
     l.dq = dq; l.dk = dk; l.dv = dv; l.dg = dg; l.dbeta = dbeta;
     l.N = B; l.T = T; l.H = H; l.d_k = d_k; l.d_v = d_v; l.err = err;
+    l.wait_limit = local_wait_limit; l.stall = local_stall;
     l.max_chunks = (T + gdn::kChunk - 1) / gdn::kChunk;
     if (l.max_chunks > 0 && !launched(gdn::launch_bwd_local(l, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
@@ -619,15 +621,16 @@ gdn_status gdn_chunk_fwd_save(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf
     return GDN_OK;
 }
 
-gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
-                               const float* g, const gdn_bf16* beta, float scale,
-                               const int32_t* cu_seqlens,
-                               const gdn_bf16* d_out, const float* d_final_state,
-                               gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
-                               gdn_bf16* dbeta, float* d_initial_state,
-                               int B, int T, int H, int d_k, int d_v,
-                               const void* saved, size_t saved_bytes,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+gdn_status chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
+                           const gdn_bf16* beta, float scale, const int32_t* cu_seqlens, const gdn_bf16* d_out,
+                           const float* d_final_state, gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                           gdn_bf16* dbeta, float* d_initial_state, int B, int T, int H, int d_k, int d_v,
+                           const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                           uint32_t local_wait_limit, int local_stall, cudaStream_t stream) {
     gdn_status st = check_bwd(q, k, v, g, beta, nullptr, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg,
                               dbeta, d_initial_state, B, T, H, d_k, d_v);
     if (st != GDN_OK) return st;
@@ -644,7 +647,40 @@ gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
     const uint8_t* tiles = L.total ? reinterpret_cast<const uint8_t*>(s + L.tiles) : nullptr;
     return launch_bwd_passes(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
                              d_initial_state, B, T, H, d_k, d_v, states, static_cast<float*>(workspace), tiles,
-                             err, stream);
+                             err, stream, local_wait_limit, local_stall);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_bwd_saved(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                               const float* g, const gdn_bf16* beta, float scale,
+                               const int32_t* cu_seqlens,
+                               const gdn_bf16* d_out, const float* d_final_state,
+                               gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                               gdn_bf16* dbeta, float* d_initial_state,
+                               int B, int T, int H, int d_k, int d_v,
+                               const void* saved, size_t saved_bytes,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                           d_initial_state, B, T, H, d_k, d_v, saved, saved_bytes, workspace, workspace_bytes,
+                           gdn::kDefaultWaitLimit, 0, stream);
+}
+
+gdn_status gdn_chunk_bwd_saved_wait_limit(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                          const float* g, const gdn_bf16* beta, float scale,
+                                          const int32_t* cu_seqlens,
+                                          const gdn_bf16* d_out, const float* d_final_state,
+                                          gdn_bf16* dq, gdn_bf16* dk, gdn_bf16* dv, float* dg,
+                                          gdn_bf16* dbeta, float* d_initial_state,
+                                          int B, int T, int H, int d_k, int d_v,
+                                          const void* saved, size_t saved_bytes,
+                                          void* workspace, size_t workspace_bytes, uint32_t wait_limit,
+                                          int stall_first_wait, cudaStream_t stream) {
+    return chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                           d_initial_state, B, T, H, d_k, d_v, saved, saved_bytes, workspace, workspace_bytes,
+                           wait_limit ? wait_limit : gdn::kDefaultWaitLimit, stall_first_wait != 0, stream);
 }
 
 size_t gdn_chunk_fwd_split_workspace_size(int B, int T, int H, int d_k, int d_v, int nseg) {

@@ -84,8 +84,8 @@ constexpr int oVec = oKQ1 + 2 * kRegionBytes;   // g, beta, G, gam, dec, colsum
 constexpr int oRed = oVec + 6 * 64 * 4;         // 16 floats reduction scratch
 constexpr int oPart = oRed + 64;                // [64 rows][8] per-row partial sums of the upper column half;
                                                 // earlier in the item's end the [4][64] partial column sums
-constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles, off-path MMA, drain
-constexpr int oMisc = oBar + 48;                // TMEM slot, abort flag
+constexpr int oBar = oPart + 64 * 8 * 4;        // mbarriers: MMA, item inputs, S0 tiles, dS tiles, off-path MMA, drain, stall
+constexpr int oMisc = oBar + 56;                // TMEM slot, abort flag
 constexpr int oDV = (oMisc + 16 + 1023) / 1024 * 1024;  // a full chunk's dV rows of one slice, staged for the TMA store
 constexpr int kBytes = oDV + kTile64;
 constexpr int kAlloc = kBytes + 1024;
@@ -150,6 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t nbar = smem_u32(barp + 4);
     // the issuer's last commit before the CTA leaves
     const uint32_t dbar = smem_u32(barp + 5);
+    // failure-detection test: a barrier that nothing signals
+    const uint32_t stallbar = smem_u32(barp + 6);
+    // bound of the hand-off waits (the drains before the CTA leaves keep the default)
+    const uint32_t wl = p.wait_limit ? p.wait_limit : kDefaultWaitLimit;
 
     // item f of the flat (chunk, head, sequence) order; false for chunks past
     // a sequence's end (and sequences whose bounds are invalid)
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(smem_u32(barp + i), 1);
+        for (int i = 0; i < 7; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
         *abort_flag = 0;
         if (use_tma) {
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;  // a bounded wait ran out (reported through the error word)
     // wait for the last commit on `bar` (issued inside an MMA batch)
     auto mma_wait = [&]() {
-        if (!mbar_wait(bar, phase, kDefaultWaitLimit)) {
+        if (!mbar_wait(bar, phase, wl)) {
             failed = true;
             *abort_flag = 1;
         }
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t nphase = 0;
     auto off_path_wait = [&]() {
-        if (!mbar_wait(nbar, nphase, kDefaultWaitLimit)) {
+        if (!mbar_wait(nbar, nphase, wl)) {
             failed = true;
             *abort_flag = 1;
         }
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t iphase = 0, s0phase = 0, dsphase = 0;
     auto wait_copy = [&](uint32_t b, uint32_t& ph, bool& out) {
-        if (mbar_wait(b, ph, kDefaultWaitLimit)) {
+        if (mbar_wait(b, ph, wl)) {
             ph ^= 1u;
             out = false;
         } else {
@@ -620,6 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(0, 0, 0, 0);
             }
         }
+        // failure-detection test: a first wait that nothing ends runs out
+        if (p.stall && k == 0 && !mbar_wait(stallbar, 0, wl)) {
+            failed = true;
+            *abort_flag = 1;
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         // hand-off: the issuer warp starts Q K^T (both sides leave here, and
@@ -824,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // goes into this slice's dS buffer (the wait leaves the phase to
             // the off-path wait at the slice's end)
             if (tid == 0 && vs + 1 < nsl && !failed) {
-                if (mbar_wait(nbar, nphase, kDefaultWaitLimit)) {
+                if (mbar_wait(nbar, nphase, wl)) {
                     issue_s0(cur, vs + 1, oDS);
                 } else {
                     failed = true;

@@ -81,6 +81,8 @@ struct BwdLocalArgs {
     int d_v;
     int max_chunks;               // chunks of the longest sequence (grid.x)
     int* err;
+    uint32_t wait_limit;          // polls of each hand-off wait (0: kDefaultWaitLimit); drains keep the default
+    int stall;                    // failure-detection test: the first item first waits on a barrier nothing signals
 };
 
 // T = (I + A)^-1 of every chunk as bf16 hi/lo operand tiles (chunk-parallel).

@@ -94,6 +94,9 @@ def load():
         lib.gdn_chunk_fwd_save.restype = i
         lib.gdn_chunk_bwd_saved.argtypes = [vp] * 5 + [f] + [vp] * 9 + [i] * 5 + [vp, sz, vp, sz, vp]
         lib.gdn_chunk_bwd_saved.restype = i
+        lib.gdn_chunk_bwd_saved_wait_limit.argtypes = ([vp] * 5 + [f] + [vp] * 9 + [i] * 5
+                                                       + [vp, sz, vp, sz, ctypes.c_uint32, i, vp])
+        lib.gdn_chunk_bwd_saved_wait_limit.restype = i
         lib.gdn_chunk_fwd_split_workspace_size.argtypes = [i] * 6
         lib.gdn_chunk_fwd_split_workspace_size.restype = sz
         lib.gdn_chunk_fwd_split.argtypes = [vp] * 5 + [f] + [vp] * 3 + [i] * 6 + [vp, sz, vp]
@@ -219,6 +222,22 @@ def gdn_chunk_bwd_saved(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_stat
                                     int(saved_bytes), _ptr(workspace), int(workspace_bytes),
                                     _stream(stream))
     _check(st, "gdn_chunk_bwd_saved")
+
+
+def gdn_chunk_bwd_saved_wait_limit(q, k, v, g, beta, scale, cu_seqlens, d_out, d_final_state,
+                                   dq, dk, dv, dg, dbeta, d_initial_state, B, T, H, d_k, d_v,
+                                   saved, saved_bytes, workspace, workspace_bytes, wait_limit,
+                                   stall_first_wait=0, stream=None):
+    """gdn_chunk_bwd_saved with a chosen bound (polls) on the gradient pass's
+    hand-off waits, and optionally a first wait that nothing ends: for
+    exercising failure detection."""
+    st = load().gdn_chunk_bwd_saved_wait_limit(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                               _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
+                                               _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                               _ptr(d_initial_state), B, T, H, d_k, d_v, _ptr(saved),
+                                               int(saved_bytes), _ptr(workspace), int(workspace_bytes),
+                                               int(wait_limit), int(stall_first_wait), _stream(stream))
+    _check(st, "gdn_chunk_bwd_saved_wait_limit")
 
 
 def gdn_chunk_fwd_split_workspace_size(B, T, H, d_k, d_v, nseg) -> int:
