@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 tc_fence_after();
                 constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
+#pragma unroll 1
                 for (int s = 0; s < kDk / 16; ++s) mma_bf16(tmem + cX1, kdesc_Q(s), kdesc_K(s), id, s > 0);
                 mma_commit(bar);
             }
@@ -383,12 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
                     constexpr uint32_t id_p = idesc(kFmtBf16, 1, 1, 64, 64);
                     constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < kDk / 16; ++s) {
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oS0) + s * 2048, kTileS, 1024), id_k, s > 0);
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oS0 + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
                     }
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t bo = desc_sw128(t64(oDO) + s * 2048, kTile64, 1024);
                         mma_bf16(tmem + cX2, desc_sw128(t64(oP) + s * 2048, kTile64, 1024), bo, id_p, s > 0);
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar);  // K S0 and P^T dO: the R epilogue reads them
                     // U += dO S0^T (B = S0 tile read K-major: [N = key row d][K =
                     // value column]), off the path: it runs in the R epilogue
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
                         mma_bf16(tmem + cU, ao, desc_sw128(t64(oS0) + s * 32, 0, 1024), id_n, (vs > 0 || s > 0) ? 1u : 0u);
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_k = idesc(kFmtBf16, 0, 1, 64, 64);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < kDk / 16; ++s) {
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS) + s * 2048, kTileS, 1024), id_k, s > 0);
                         mma_bf16(tmem + cX1, kdesc_K(s), desc_sw128(t64(oDS + kTileS) + s * 2048, kTileS, 1024), id_k, 1);
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 64);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t th = desc_sw128(t64(oT) + s * 2048, kTile64, 1024);
                         const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 2048, kTile64, 1024);
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
                     tc_fence_after();
                     constexpr uint32_t id_b = idesc(kFmtBf16, 0, 1, 64, 64);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t th = desc_sw128(t64(oT) + s * 32, 0, 1024);
                         const uint64_t tl = desc_sw128(t64(oT + kTile64) + s * 32, 0, 1024);
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
                     // dK += (dec o Delta) dS^T, the last reader of the dS tiles
                     // (B = dS tile read K-major: [N = key row d][K = value column])
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t eh = desc_sw128(t64(oRC) + s * 32, 0, 1024);
                         const uint64_t el = desc_sw128(t64(oRC + kTile64) + s * 32, 0, 1024);
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, el, sbh, id_n, 1);
                     }
                     // dP += dO Delta^T
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ao = desc_sw128(t64(oDO) + s * 32, 0, 1024);
                         const uint64_t dh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     constexpr uint32_t id_c = idesc(kFmtBf16, 0, 0, 64, 64);
                     constexpr uint32_t id_n = idesc(kFmtBf16, 0, 0, 64, 128);
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t sah = desc_sw128(t64(oS0) + s * 32, 0, 1024);
                         const uint64_t sal = desc_sw128(t64(oS0 + kTileS) + s * 32, 0, 1024);
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, yh, sal, id_n, 1);
                         mma_bf16(tmem + cdK, yl, sah, id_n, 1);
                     }
-#pragma unroll
+#pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ch_ = desc_sw128(t64(oRB) + s * 32, 0, 1024);
                         const uint64_t cl_ = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // chunk-wide part: K K^T and Q K^T (M = 64 each) into the
                         // scratch columns, queued behind the last slice's products
                         constexpr uint32_t id = idesc(kFmtBf16, 0, 0, 64, 64);
-#pragma unroll
+#pragma unroll 1
                         for (int s = 0; s < kDk / 16; ++s) {
                             mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
                             mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 constexpr uint32_t id_n = idesc(kFmtBf16, 0, 1, 64, 128);   // A K-major, B MN-major
                 constexpr uint32_t id_t = idesc(kFmtBf16, 1, 1, 64, 128);   // A MN-major (transposed)
-#pragma unroll
+#pragma unroll 1
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t qh = desc_sw128(t64(oRB) + s * 32, 0, 1024);
                     const uint64_t ql = desc_sw128(t64(oRB + kTile64) + s * 32, 0, 1024);
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar);  // dQ2: the dq outputs read it
                 // the dK products complete while the dq outputs are formed
-#pragma unroll
+#pragma unroll 1
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t kh = desc_sw128(t64(oRA) + s * 32, 0, 1024);
                     const uint64_t kl = desc_sw128(t64(oRA + kTile64) + s * 32, 0, 1024);
