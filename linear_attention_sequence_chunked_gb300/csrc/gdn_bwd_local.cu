@@ -53,9 +53,10 @@ using namespace tc;
 constexpr int kEpi = 256;                 // warps 0-7: loads, epilogues, outputs
 constexpr int kIssuerWarp = 8;            // warp 8: issues every MMA (warps 9-11 idle)
 constexpr int kThreads = kEpi + 128;
-// registers: 168 a thread at launch (384 threads); the issuer's warpgroup
-// gives up 32 of them (its unrolled descriptor arithmetic needs ~130), the two
-// epilogue warpgroups take 16 more: 128 x 136 + 256 x 184 = 384 x 168
+// registers: 168 a thread at launch (384 threads); the epilogue warps need
+// ~184 (more measured no faster), the issuer's rolled MMA loops far fewer, so
+// the issuer's warpgroup gives 32 a thread to the two epilogue warpgroups:
+// 128 x 136 + 256 x 184 = 384 x 168
 constexpr int kRegLaunch = 168, kRegIssuer = 136, kRegEpi = 184;
 static_assert(128 * kRegIssuer + 256 * kRegEpi == kThreads * kRegLaunch, "register split");
 constexpr int kVs = 64;
