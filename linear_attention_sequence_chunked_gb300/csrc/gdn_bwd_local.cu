@@ -832,8 +832,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // once dK += (dec o Delta) dS^T has completed, the next slice's S0
             // goes into this slice's dS buffer (the wait leaves the phase to
-            // the off-path wait at the slice's end)
-            if (tid == 0 && vs + 1 < nsl && !failed) {
+            // the off-path wait at the slice's end).  The copies are spread
+            // over warps 0-2 (thread 0: K/Q and T, 32: S0 tiles, 64: dS tiles),
+            // so that no one warp is held by all the issues
+            if (tid == 32 && vs + 1 < nsl && !failed) {
                 if (mbar_wait(nbar, nphase, wl)) {
                     issue_s0(cur, vs + 1, oDS);
                 } else {
@@ -857,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             off_path_wait();  // dP: the next slice rewrites the dO and Delta tiles it reads
             epi_sync();
             // the S0 tiles are free: the next slice's dS goes there
-            if (tid == 0 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1, oS0);
+            if (tid == 64 && vs + 1 < nsl && !failed) issue_ds(cur, vs + 1, oS0);
         }
         if (quit) break;
 
@@ -916,10 +918,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next item's inputs land while this item's end runs: K/Q into the
         // other buffer (RC, RD are dead), T, slice 0 states (issued after the
         // hand-off, so that no epilogue warp waits for the issuing thread)
-        if (fn < total && tid == 0 && !failed) {
-            issue_inputs(nxt, smem_u32(sm + oRC));
-            issue_s0(nxt, 0, oSA);
-            issue_ds(nxt, 0, oSB);
+        if (fn < total && !failed) {
+            if (tid == 0) issue_inputs(nxt, smem_u32(sm + oRC));
+            if (tid == 32) issue_s0(nxt, 0, oSA);
+            if (tid == 64) issue_ds(nxt, 0, oSB);
         }
         // column sums of E while the products run: four partial sums of 16
         // rows per column, then their sum
@@ -1118,12 +1120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_error(p.err, kErrTimeout);
     }
     // let every copy this thread issued land before the CTA leaves
-    if (tid == 0) {
-        if (i_out) mbar_wait(ibar, iphase, kDefaultWaitLimit);
-        if (s0_out) mbar_wait(s0bar, s0phase, kDefaultWaitLimit);
-        if (ds_out) mbar_wait(dsbar, dsphase, kDefaultWaitLimit);
-        bulk_wait_all();  // the dq / dk tile stores
-    }
+    if (i_out) mbar_wait(ibar, iphase, kDefaultWaitLimit);
+    if (s0_out) mbar_wait(s0bar, s0phase, kDefaultWaitLimit);
+    if (ds_out) mbar_wait(dsbar, dsphase, kDefaultWaitLimit);
+    if (tid == 0) bulk_wait_all();  // the dV / dq / dk tile stores
     }
     tc_fence_before();
     __syncthreads();
