@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto slot_of = [&](const Item& it) { return chunk_slot_base(p.cu_seqlens, it.n, p.T) + it.ci; };
 
-    // async copies, thread 0; each records what is in flight for the drain
+    // async copies (thread 0: K/Q and T; threads 32 and 64: S0 and dS tiles;
+    // thread 0 also at set-up); each thread records what it has in flight for
+    // its drain
     bool i_out = false, s0_out = false, ds_out = false;
     // K/Q (TMA, d_k = 128) and T tiles of item `it` into K/Q buffer kqb
     auto issue_inputs = [&](const Item& it, uint32_t kqb) {
