@@ -518,6 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem + cdK, yh, sal, id_n, 1);
                         mma_bf16(tmem + cdK, yl, sah, id_n, 1);
                     }
+                    // before the last slice, the epilogue warps wait only for
+                    // this last reader of the S0 tiles (the next slice's dS goes
+                    // there); dA runs into the next slice's start, and the next
+                    // slice's first commit covers it before Delta and -dBhat
+                    // are rewritten
+                    if (vs + 1 < nsl) mma_commit(bar);
 #pragma unroll 1
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t ch_ = desc_sw128(t64(oRB) + s * 32, 0, 1024);
@@ -537,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16(tmem + cX1, kdesc_K(s), kdesc_K(s), id, s > 0);
                             mma_bf16(tmem + cX2, kdesc_Q(s), kdesc_K(s), id, s > 0);
                         }
+                        mma_commit(bar);  // the item's end reads dA, K K^T and Q K^T
                     }
-                    mma_commit(bar);
                 }
                 __syncwarp();
             }
