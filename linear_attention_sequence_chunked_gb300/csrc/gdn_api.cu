@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "gdn.h"
 #include "gdn_common.cuh"
@@ -243,7 +244,7 @@ KdaBwdLayout kda_bwd_layout(int B, int T, int H, int d_k, int d_v, int varlen) {
 // segments, zero values and a scratch output for the transition run, the
 // identity start states, the segments' M and b, and their true start states.
 struct SplitLayout {
-    size_t cu, tiles, zeros, mout, ident, mfin, bfin, starts, total;
+    size_t cu, tiles, zeros, om, ob, ident, mfin, bfin, starts, total;
 };
 
 SplitLayout split_layout(int B, int T, int H, int d_k, int d_v, int nseg) {
@@ -253,13 +254,30 @@ SplitLayout split_layout(int B, int T, int H, int d_k, int d_v, int nseg) {
     L.cu = 0;
     L.tiles = round_up(sizeof(int32_t) * (nseq + 1));
     L.zeros = L.tiles + tiles_bytes(static_cast<int>(nseq), static_cast<int>(rows), H, 1);
-    L.mout = L.zeros + round_up(2ull * rows * H * d_k);
-    L.ident = L.mout + round_up(2ull * rows * H * d_k);
+    L.om = L.zeros + round_up(2ull * rows * H * d_k);
+    L.ob = L.om + round_up(4ull * rows * H * d_k);
+    L.ident = L.ob + round_up(4ull * rows * H * d_v);
     L.mfin = L.ident + round_up(4ull * nseq * H * d_k * d_k);
     L.bfin = L.mfin + round_up(4ull * nseq * H * d_k * d_k);
     L.starts = L.bfin + round_up(4ull * nseq * H * d_k * d_v);
     L.total = L.starts + round_up(4ull * nseq * H * d_k * d_v);
     return L;
+}
+
+// A second stream per device for the split's two carry runs, which run side
+// by side (one wave each when the segments' chains leave SMs idle); created
+// on first use and kept for the life of the process.
+constexpr int kMaxAuxDevices = 64;
+cudaStream_t g_aux_stream[kMaxAuxDevices] = {};
+std::mutex g_aux_mu;
+
+cudaStream_t aux_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAuxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_aux_mu);
+    if (!g_aux_stream[dev] && cudaStreamCreateWithFlags(&g_aux_stream[dev], cudaStreamNonBlocking) != cudaSuccess)
+        g_aux_stream[dev] = nullptr;
+    return g_aux_stream[dev];
 }
 
 // Segments actually used: at least one chunk each.
@@ -728,18 +746,52 @@ gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
         if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
         return GDN_OK;
     }
-    // carries: b from a zero start (the output is overwritten below), M from
-    // the identity with zero values
-    f.v = v; f.d_v = d_v; f.initial_state = nullptr; f.out = out; f.final_state = reinterpret_cast<float*>(w + L.bfin);
-    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
-    if (cudaMemsetAsync(w + L.zeros, 0, 2ull * rows * H * d_k, stream) != cudaSuccess) return GDN_ERR_CUDA;
-    f.v = reinterpret_cast<const gdn_bf16*>(w + L.zeros); f.d_v = d_k; f.initial_state = sa.ident;
-    f.out = reinterpret_cast<gdn_bf16*>(w + L.mout); f.final_state = reinterpret_cast<float*>(w + L.mfin);
-    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
-    // true start states (and the final state), then every segment from its start
+    // carries, side by side on two streams, outputs in fp32: b from a zero
+    // start (output O_b), M from the identity with zero values (output O_M,
+    // d_k columns); the chain is linear in its start state, so a segment's
+    // output is O_b + O_M S_start
+    cudaStream_t aux = aux_stream();
+    if (!aux) return GDN_ERR_CUDA;
+    cudaEvent_t forked = nullptr, joined = nullptr;
+    if (cudaEventCreateWithFlags(&forked, cudaEventDisableTiming) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&joined, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(forked);
+        return GDN_ERR_CUDA;
+    }
+    gdn_status rs = GDN_OK;
+    do {
+        if (cudaEventRecord(forked, stream) != cudaSuccess || cudaStreamWaitEvent(aux, forked, 0) != cudaSuccess) {
+            rs = GDN_ERR_CUDA;
+            break;
+        }
+        gdn::FwdArgs fb = f;
+        fb.v = v; fb.d_v = d_v; fb.initial_state = nullptr; fb.out = nullptr;
+        fb.out_f32 = reinterpret_cast<float*>(w + L.ob); fb.final_state = reinterpret_cast<float*>(w + L.bfin);
+        if (!launched(gdn::launch_fwd_ws_f32(fb, gdn::kDefaultWaitLimit, stream))) rs = GDN_ERR_CUDA;
+        gdn::FwdArgs fm = f;
+        fm.v = reinterpret_cast<const gdn_bf16*>(w + L.zeros); fm.d_v = d_k; fm.initial_state = sa.ident;
+        fm.out = nullptr; fm.out_f32 = reinterpret_cast<float*>(w + L.om);
+        fm.final_state = reinterpret_cast<float*>(w + L.mfin);
+        if (cudaMemsetAsync(w + L.zeros, 0, 2ull * rows * H * d_k, aux) != cudaSuccess) rs = GDN_ERR_CUDA;
+        else if (!launched(gdn::launch_fwd_ws_f32(fm, gdn::kDefaultWaitLimit, aux))) rs = GDN_ERR_CUDA;
+        // the join is recorded whatever happened above, so that the caller's
+        // stream never runs ahead of work left on the second stream
+        if (cudaEventRecord(joined, aux) != cudaSuccess || cudaStreamWaitEvent(stream, joined, 0) != cudaSuccess)
+            rs = GDN_ERR_CUDA;
+    } while (false);
+    cudaEventDestroy(forked);  // released once the recorded work has passed them
+    cudaEventDestroy(joined);
+    if (rs != GDN_OK) return rs;
+    // true start states (and the final state), then every segment's output
     if (!launched(gdn::launch_split_compose(sa, stream))) return GDN_ERR_CUDA;
-    f.v = v; f.d_v = d_v; f.initial_state = sa.starts; f.out = out; f.final_state = nullptr;
-    if (!launched(gdn::launch_fwd_ws(f, gdn::kDefaultWaitLimit, stream))) return GDN_ERR_CUDA;
+    gdn::SplitCorrectArgs ca{};
+    ca.ob = reinterpret_cast<const float*>(w + L.ob);
+    ca.om = reinterpret_cast<const float*>(w + L.om);
+    ca.starts = sa.starts; ca.cu = sa.cu; ca.out = out;
+    ca.nseq = nseq; ca.H = H; ca.d_k = d_k; ca.d_v = d_v; ca.err = err; ca.wait_limit = gdn::kDefaultWaitLimit;
+    const int nch = (T + gdn::kChunk - 1) / gdn::kChunk;
+    ca.max_chunks = (nch + ns - 1) / ns;
+    if (!launched(gdn::launch_split_correct(ca, stream))) return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

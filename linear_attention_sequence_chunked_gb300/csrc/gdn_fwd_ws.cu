@@ -145,6 +145,7 @@ struct ChainArgs {
     const float* state_in;        // forward: initial state; backward: final-state gradient (may be null)
     const int32_t* cu_seqlens;
     uint16_t* out;                // forward output (may be null)
+    float* out_f32;               // forward output in fp32 instead (the fp32-output instantiation only)
     float* state_out;             // forward: final state; backward: initial-state gradient (may be null)
     float* chunk_states;          // forward: chunk start states; backward: chunk end-state gradients (may be null)
     const uint8_t* chunk_T;       // T operand tiles of every chunk (may be null: formed in place)
@@ -158,7 +159,9 @@ struct WsParams {
     uint32_t wait_limit;
 };
 
-template <bool kBwd>
+// kF32Out: the forward writes its output in fp32 to out_f32 (the sequence
+// split's carry runs, whose outputs are combined later) instead of bf16.
+template <bool kBwd, bool kF32Out = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chain_ws_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                         const WsParams prm) {
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool use_tma = dk == kDk;
     const long long row_base = static_cast<long long>(b) * p.T;
     const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
-    const bool want_out = !kBwd && p.out != nullptr;
+    const bool want_out = !kBwd && (kF32Out ? p.out_f32 != nullptr : p.out != nullptr);
     // the prep forms P only where the chain uses it (output, or P^T dO), and
     // takes the T tiles from the chunk-parallel inverse when they are given
     const bool want_p = kBwd || want_out;
@@ -513,17 +516,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ld_q16(kColPD, pd);
                     tmem_ld_wait();
                     if (mine) {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            p.out + ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq);
+                        const long long oo = ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq;
+                        if constexpr (kF32Out) {
+                            float4* dst = reinterpret_cast<float4*>(p.out_f32 + oo);
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            uint32_t w4[4];
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_float4(scale * fmaf(gi, qs[4 * j], pd[4 * j]),
+                                                     scale * fmaf(gi, qs[4 * j + 1], pd[4 * j + 1]),
+                                                     scale * fmaf(gi, qs[4 * j + 2], pd[4 * j + 2]),
+                                                     scale * fmaf(gi, qs[4 * j + 3], pd[4 * j + 3]));
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(p.out + oo);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int c = j * 8 + 2 * e;
-                                w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]), scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                            for (int j = 0; j < 2; ++j) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = j * 8 + 2 * e;
+                                    w4[e] = pack_bf16x2(scale * fmaf(gi, qs[c], pd[c]), scale * fmaf(gi, qs[c + 1], pd[c + 1]));
+                                }
+                                dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
-                            dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
                     }
                 }
@@ -1171,7 +1184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool kBwd>
+template <bool kBwd, bool kF32Out = false>
 cudaError_t launch_chain(const ChainArgs& a, uint32_t wait_limit, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
     CUtensorMap mk, mq;  // used for d_k = 128 only (d_k = 64 tiles use plain loads)
@@ -1180,11 +1193,11 @@ cudaError_t launch_chain(const ChainArgs& a, uint32_t wait_limit, cudaStream_t s
     if (rows > 0 && a.d_k == kDk && (!make_qk_map(&mk, a.k, rows, a.H) || !make_qk_map(&mq, a.q, rows, a.H)))
         return cudaErrorInvalidValue;
     constexpr int smem = kAlloc;
-    cudaError_t e = cudaFuncSetAttribute(gdn_chain_ws_kernel<kBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(gdn_chain_ws_kernel<kBwd, kF32Out>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     WsParams prm{a, wait_limit};
     dim3 grid(a.d_v / kVs, a.H, a.N);
-    gdn_chain_ws_kernel<kBwd><<<grid, kThreads, smem, stream>>>(mk, mq, prm);
+    gdn_chain_ws_kernel<kBwd, kF32Out><<<grid, kThreads, smem, stream>>>(mk, mq, prm);
     return cudaGetLastError();
 }
 
@@ -1219,7 +1232,19 @@ cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t st
     c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = a.out; c.state_out = a.final_state;
     c.chunk_states = a.chunk_states; c.chunk_T = a.chunk_T;
     c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err; c.stall = a.stall;
+    c.out_f32 = nullptr;
     return launch_chain<false>(c, wait_limit, stream);
+}
+
+cudaError_t launch_fwd_ws_f32(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.cu_seqlens ? 1 : a.N) * a.T;
+    if (rows == 0 || a.out_f32 == nullptr) return cudaErrorInvalidValue;  // only the split's carry runs use it
+    ChainArgs c{};
+    c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
+    c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.out_f32 = a.out_f32;
+    c.state_out = a.final_state; c.chunk_states = a.chunk_states; c.chunk_T = a.chunk_T;
+    c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err; c.stall = 0;
+    return launch_chain<false, true>(c, wait_limit, stream);
 }
 
 cudaError_t launch_bwd_chain(const BwdChainArgs& a, uint32_t wait_limit, cudaStream_t stream) {

@@ -17,6 +17,7 @@ struct FwdArgs {
     const float* initial_state;
     const int32_t* cu_seqlens;
     uint16_t* out;          // may be null: skip the output
+    float* out_f32;         // launch_fwd_ws_f32 only: the output in fp32 [rows][H][d_v]
     float* final_state;     // may be null
     float* chunk_states;    // may be null: per-chunk start states, bf16 hi/lo operand tiles
                             // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v]);
@@ -280,6 +281,22 @@ struct SplitArgs {
 };
 cudaError_t launch_split_setup(const SplitArgs& a, cudaStream_t stream);
 cudaError_t launch_split_compose(const SplitArgs& a, cudaStream_t stream);
+// The split's outputs from its two carry runs: every segment's chain is linear
+// in its start state, so out = O_b + O_M S_start (O_b: the run from a zero
+// start, fp32 [rows][H][d_v]; O_M: the run from the identity with zero values,
+// fp32 [rows][H][d_k]; S_start: the composed start states), rounded to bf16.
+struct SplitCorrectArgs {
+    const float* ob;
+    const float* om;
+    const float* starts;          // [nseq][H][d_k][d_v]
+    const int32_t* cu;            // [nseq + 1] segment bounds (packed rows)
+    uint16_t* out;                // [rows][H][d_v]
+    int nseq, H, d_k, d_v;
+    int max_chunks;               // chunks of the longest segment
+    int* err;
+    uint32_t wait_limit;
+};
+cudaError_t launch_split_correct(const SplitCorrectArgs& a, cudaStream_t stream);
 
 // Peak probes (measurement only): a 16-byte-vector copy of `bytes` (a
 // multiple of 16), and the bf16 GEMM C[M][N] = A[M][K] B[N][K]^T with
@@ -291,6 +308,9 @@ cudaError_t launch_probe_gemm(const uint16_t* A, const uint16_t* B, uint16_t* C,
 // wait_limit bounds every hand-off mbarrier wait (polls); the waits that
 // drain in-flight copies and products before a CTA leaves keep the default.
 cudaError_t launch_fwd_ws(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
+// The same chain with the output written in fp32 to a.out_f32 (the sequence
+// split's carry runs); a.out is ignored.
+cudaError_t launch_fwd_ws_f32(const FwdArgs& a, uint32_t wait_limit, cudaStream_t stream);
 constexpr uint32_t kDefaultWaitLimit = 4000000u;
 
 }  // namespace gdn
