@@ -585,7 +585,7 @@ def measure_probes(gdn, torch, dev, stream, copy_bytes=2 << 30, n=8192, steps=10
                        f"{steps} after {warmup} warm-up"}
 
 
-def measure_split(gdn, torch, dev, stream, T=65536, H=16, K=128, V=128, segs=(4, 8), steps=5, warmup=2):
+def measure_split(gdn, torch, dev, stream, T=65536, H=16, K=128, V=128, segs=(2, 4), steps=5, warmup=2):
     """The sequence split on the long slow-decay workload (one sequence,
     T = 65536, 16 heads: 32 chains unsplit): gdn_chunk_fwd against
     gdn_chunk_fwd_split at a few segment counts, L2 flushed before each call.
