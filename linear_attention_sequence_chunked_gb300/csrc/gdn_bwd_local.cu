@@ -609,18 +609,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             bv[tid] = b_pre;
         }
         if (!use_tma) {
-            // rows beyond the chunk and key columns beyond d_k are zero
-            for (int e = tid; e < 2 * 2 * 64 * 8; e += kEpi) {
+            // rows beyond the chunk and key columns beyond d_k are zero; every
+            // load of this thread is in flight before the first store
+            constexpr int kPer = 2 * 2 * 64 * 8 / kEpi;
+            uint4 val[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int e = tid + u * kEpi;
                 const int which = e >> 10;                // 0: K, 1: Q
                 const int region = (e >> 9) & 1;          // key columns 0-63 / 64-127
                 const int r = (e >> 3) & 63, ch = e & 7;
-                uint4 val = make_uint4(0, 0, 0, 0);
+                val[u] = make_uint4(0, 0, 0, 0);
                 if (r < nv && region * 64 < dk) {
                     const uint16_t* src = which ? p.q : p.k;
-                    val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
-                                                          region * 64 + ch * 8);
+                    val[u] = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * static_cast<long long>(dk) +
+                                                             region * 64 + ch * 8);
                 }
-                *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int e = tid + u * kEpi, which = e >> 10, region = (e >> 9) & 1, r = (e >> 3) & 63, ch = e & 7;
+                *reinterpret_cast<uint4*>(sm + oKQ + region * kRegionBytes + which * 64 * 128 + sw128_offset(r, ch * 16)) = val[u];
             }
         }
         wait_copy(ibar, iphase, i_out);

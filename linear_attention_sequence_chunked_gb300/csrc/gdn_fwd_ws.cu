@@ -799,15 +799,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it >= 2) ok = mbar_wait(bar(B_SFREE0 + st), ((it - 2) >> 1) & 1, wl);
                 if (!ok) *abort_flag = 1;
                 if (named_bar_or(2, *abort_flag)) { aborted = true; break; }
-                for (int e = q; e < 2 * 64 * 8; e += 128) {
-                    const int which = e >> 9;
-                    const int r = (e >> 3) & 63, ch = e & 7;
-                    uint4 val = make_uint4(0, 0, 0, 0);
+                // every load of this thread is in flight before the first
+                // store (the stores could alias the loads for the compiler)
+                constexpr int kPer = 2 * 64 * 8 / 128;
+                uint4 val[kPer];
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int e = q + u * 128, which = e >> 9, r = (e >> 3) & 63, ch = e & 7;
+                    val[u] = make_uint4(0, 0, 0, 0);
                     if (r < nv) {
                         const uint16_t* src = which ? p.q : p.k;
-                        val = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
+                        val[u] = *reinterpret_cast<const uint4*>(src + ((row_base + c0 + r) * H + h) * 64LL + ch * 8);
                     }
-                    *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val;
+                }
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int e = q + u * 128, which = e >> 9, r = (e >> 3) & 63, ch = e & 7;
+                    *reinterpret_cast<uint4*>(stage + which * 64 * 128 + sw128_offset(r, ch * 16)) = val[u];
                 }
                 fence_proxy_async_smem();
                 named_bar(2);
