@@ -788,7 +788,8 @@ gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
     ca.ob = reinterpret_cast<const float*>(w + L.ob);
     ca.om = reinterpret_cast<const float*>(w + L.om);
     ca.starts = sa.starts; ca.cu = sa.cu; ca.out = out;
-    ca.nseq = nseq; ca.H = H; ca.d_k = d_k; ca.d_v = d_v; ca.err = err; ca.wait_limit = gdn::kDefaultWaitLimit;
+    ca.nseq = nseq; ca.H = H; ca.d_k = d_k; ca.d_v = d_v; ca.rows = rows; ca.T = T; ca.nseg = ns; ca.err = err;
+    ca.wait_limit = gdn::kDefaultWaitLimit;
     const int nch = (T + gdn::kChunk - 1) / gdn::kChunk;
     ca.max_chunks = (nch + ns - 1) / ns;
     if (!launched(gdn::launch_split_correct(ca, stream))) return GDN_ERR_CUDA;

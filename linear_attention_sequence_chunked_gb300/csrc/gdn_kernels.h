@@ -292,6 +292,8 @@ struct SplitCorrectArgs {
     const int32_t* cu;            // [nseq + 1] segment bounds (packed rows)
     uint16_t* out;                // [rows][H][d_v]
     int nseq, H, d_k, d_v;
+    long long rows;               // packed rows of all segments
+    int T, nseg;                  // tokens per sequence and segments per sequence (nseq = B nseg)
     int max_chunks;               // chunks of the longest segment
     int* err;
     uint32_t wait_limit;

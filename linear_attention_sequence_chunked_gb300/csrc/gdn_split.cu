@@ -11,6 +11,9 @@
 // file holds the two small kernels around those runs: the setup (segment
 // bounds as packed sequences, identity start states) and the composition
 // (fp32, sequential over a sequence's segments).
+#include <cuda.h>
+#include <string.h>
+
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tc_common.cuh"
@@ -20,20 +23,24 @@ namespace gdn {
 
 namespace {
 
-// cu[s] for s = 0 .. B nseg: sequence b's segment j starts at token
-// b T + 64 floor(j nch / nseg) (whole chunks), the last one ends at b T + T;
-// then the identity start state of every (segment, head).
+// First packed row of segment j of sequence b: b T + 64 floor(j nch / nseg)
+// (whole chunks); segment nseg - 1 ends at b T + T.
+__device__ __forceinline__ long long seg_start(long long b, int j, int T, int nseg) {
+    const long long nch = (T + kChunk - 1) / kChunk;
+    return b * T + (j == 0 ? 0 : kChunk * ((j * nch) / nseg));
+}
+
+// cu[s] for s = 0 .. B nseg (the segment bounds above); then the identity
+// start state of every (segment, head).
 __global__ void gdn_split_setup_kernel(const SplitArgs a) {
-    const long long nch = (a.T + kChunk - 1) / kChunk;
     const long long nseq = static_cast<long long>(a.B) * a.nseg;
     const long long kk = static_cast<long long>(a.d_k) * a.d_k;
     const long long total = nseq * a.H * kk;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total + nseq + 1;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (i <= nseq) {
-            const long long b = i / a.nseg, j = i % a.nseg;
-            long long pos = b * a.T + (j == 0 ? 0 : kChunk * ((j * nch) / a.nseg));
-            if (i == nseq) pos = static_cast<long long>(a.B) * a.T;
+            const long long pos = i == nseq ? static_cast<long long>(a.B) * a.T
+                                            : seg_start(i / a.nseg, static_cast<int>(i % a.nseg), a.T, a.nseg);
             a.cu[i] = static_cast<int32_t>(pos);
         } else {
             const long long e = i - nseq - 1;
@@ -95,57 +102,147 @@ __global__ void __launch_bounds__(kComposeThreads) gdn_split_compose_kernel(cons
     }
 }
 
-// out = bf16(O_b + O_M S_start) for the rows of one segment, on the tensor
+// out = bf16(O_b + O_M S_start) for every row of every segment, on the tensor
 // cores: per chunk of 64 rows, D[64 x N] = O_M[64 x d_k] S_start[d_k x N]
 // with both operands split into bf16 hi + lo (hi hi + hi lo + lo hi, fp32
-// accumulation in TMEM), N = 64 or 128 value columns.  Block (group of
-// kCorrG chunks, value block of N columns and head, segment); the segment's
-// start-state block is converted once and serves every chunk of the group.
-constexpr int kCorrThreads = 128;
-constexpr int kCorrG = 8;
+// accumulation in TMEM), N = 64 or 128 value columns.  The kernel mostly
+// moves bytes (O_M and O_b in fp32 in, out in bf16), so it is laid out for
+// bandwidth: one persistent CTA per SM walks a contiguous range of (segment,
+// head, value block, chunk) units, and each unit's 64 rows of O_M and O_b
+// come in as TMA boxes ahead of it: O_M into one fp32 staging tile,
+// converted into one of two pairs of hi/lo operand tiles at the top of its
+// unit and refilled for the next unit at once; O_b (32-column boxes,
+// 128-byte swizzled, so that the epilogue's reads of 16 rows at once fall on
+// distinct banks) into one of two staging tiles.  A unit's product runs into
+// one of two TMEM accumulators while the epilogue of the unit before it
+// (O_b + the product, to bf16) runs.  A unit past the end of its
+// segment copies and stores nothing.  The start-state block is converted
+// when a CTA's range enters a new (segment, head, value block).
+constexpr int kCorrThreads = 256;  // warps w and w + 4 share TMEM subpartition w % 4
 constexpr int kCorrTile = 64 * 128;  // 64 rows x 128 B
 
-__global__ void __launch_bounds__(kCorrThreads) gdn_split_correct_kernel(const SplitCorrectArgs a) {
+// A unit and where its rows are.  Units run value block fastest, then
+// head, then segment (chunk index c innermost of all); a CTA steps through
+// its range with corr_next, which does the divisions only when the segment
+// changes.
+struct CorrUnit {
+    int c, vb, h, n;     // chunk, value block, head, segment
+    long long t0, t1;    // the segment's packed rows [t0, t1)
+    long long r0;        // first row of the chunk
+    int nv;              // its rows inside the segment (0: past the segment's end)
+};
+
+__device__ __forceinline__ void corr_rows(const SplitCorrectArgs& a, CorrUnit& x) {
+    x.r0 = x.t0 + static_cast<long long>(x.c) * kChunk;
+    const long long left = x.t1 - x.r0;
+    x.nv = static_cast<int>(left < 0 ? 0 : (left < kChunk ? left : kChunk));
+}
+
+__device__ __forceinline__ void corr_segment(const SplitCorrectArgs& a, CorrUnit& x) {
+    // the segment's bounds by the setup's rule (no dependent loads of cu)
+    const long long b = x.n / a.nseg;
+    const int j = x.n % a.nseg;
+    x.t0 = seg_start(b, j, a.T, a.nseg);
+    x.t1 = j + 1 < a.nseg ? seg_start(b, j + 1, a.T, a.nseg) : (b + 1) * a.T;
+}
+
+__device__ __forceinline__ CorrUnit corr_unit(const SplitCorrectArgs& a, int nvb, long long u) {
+    CorrUnit x;
+    const long long combo = u / a.max_chunks;
+    x.c = static_cast<int>(u % a.max_chunks);
+    x.vb = static_cast<int>(combo % nvb);
+    x.h = static_cast<int>((combo / nvb) % a.H);
+    x.n = static_cast<int>(combo / (static_cast<long long>(nvb) * a.H));
+    corr_segment(a, x);
+    corr_rows(a, x);
+    return x;
+}
+
+__device__ __forceinline__ CorrUnit corr_next(const SplitCorrectArgs& a, int nvb, CorrUnit x) {
+    if (++x.c == a.max_chunks) {
+        x.c = 0;
+        if (++x.vb == nvb) {
+            x.vb = 0;
+            if (++x.h == a.H) {
+                x.h = 0;
+                ++x.n;
+                if (x.n < a.nseq) corr_segment(a, x);
+            }
+        }
+    }
+    corr_rows(a, x);
+    return x;
+}
+
+__global__ void __launch_bounds__(kCorrThreads, 1)
+    gdn_split_correct_kernel(const __grid_constant__ CUtensorMap tmap_om, const __grid_constant__ CUtensorMap tmap_ob,
+                             const SplitCorrectArgs a) {
     using namespace sm100;
     using namespace tc;
     const int K = a.d_k, V = a.d_v, H = a.H;
-    const int nb = V >= 128 ? 2 : 1;             // 64-column blocks of this CTA
+    const int nb = V >= 128 ? 2 : 1;             // 64-column blocks of a unit
     const int nvb = V / (64 * nb);               // value blocks per head
-    const int vb = blockIdx.y % nvb, h = blockIdx.y / nvb, n = blockIdx.z;
-    const int t0 = a.cu[n], t1 = a.cu[n + 1];
-    const int nch = (t1 - t0 + kChunk - 1) / kChunk;
-    const int c_begin = blockIdx.x * kCorrG, c_end = min(nch, c_begin + kCorrG);
-    if (c_begin >= c_end) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int v0 = vb * 64 * nb;                 // first value column of this CTA
     const int kreg = K / 64;                     // 64-column regions of d_k
+    const long long units = static_cast<long long>(a.nseq) * H * nvb * a.max_chunks;
+    const long long u_begin = units * blockIdx.x / gridDim.x;
+    const long long u_end = units * (blockIdx.x + 1) / gridDim.x;
+    if (u_begin >= u_end) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t wl = a.wait_limit;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + smem_align_pad(smem_raw);
     // B: S_start block, [d_k rows][64 value columns] per MN block, hi then lo;
-    // A: O_M rows, [64 rows][64 key columns] per region, hi then lo
+    // A: [2] O_M rows, [64 rows][64 key columns] per region, hi then lo; then
+    // the fp32 staging: O_M [64][d_k], O_b [2][2 nb boxes][64 rows][32 values]
     const int bBytes = K * 128;                  // one MN block (hi or lo)
+    const int obUnit = 64 * 64 * nb * 4;         // one unit's O_b staging
     uint8_t* Bhi = sm;
     uint8_t* Blo = sm + nb * bBytes;
-    uint8_t* Ahi = sm + 2 * nb * bBytes;
-    uint8_t* Alo = Ahi + kreg * kCorrTile;
-    uint64_t* barp = reinterpret_cast<uint64_t*>(Alo + kreg * kCorrTile);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(barp + 1);
-    const uint32_t bar = smem_u32(barp);
-    constexpr uint32_t kCorrCols = 128;
+    uint8_t* Aop = sm + 2 * nb * bBytes;         // [2][hi, lo][kreg regions]
+    const int aBytes = 2 * kreg * kCorrTile;
+    float* A32 = reinterpret_cast<float*>(Aop + 2 * aBytes);
+    uint8_t* B32 = reinterpret_cast<uint8_t*>(A32 + 64 * K);
+    uint64_t* barp = reinterpret_cast<uint64_t*>(B32 + 2 * obUnit);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(barp + 5);
+    const uint32_t bar_a = smem_u32(barp);
+    auto bar_mma = [&](int i) { return smem_u32(barp + 1 + i); };
+    auto bar_b = [&](int i) { return smem_u32(barp + 3 + i); };
+    constexpr uint32_t kCorrCols = 256;           // two 128-column accumulators
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), kCorrCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
+        tma_prefetch_desc(&tmap_om);
+        tma_prefetch_desc(&tmap_ob);
     }
-    // S_start[n][h][k][v0 .. v0 + 64 nb) as split MN-major tiles: row k, 8 values per 16-byte chunk
-    {
-        const float* src = a.starts + (static_cast<long long>(n) * H + h) * K * V + v0;
-        // K 8 nb chunks of 8 values, 4 .. 16 a thread: loads first, then the splits
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // one thread: a unit's O_M box, and its O_b boxes into staging buffer
+    // buf; a unit past its segment's end loads nothing and only arrives
+    auto issue_om = [&](const CorrUnit& x) {
+        mbar_arrive_expect_tx(bar_a, x.nv ? static_cast<uint32_t>(64 * K * 4) : 0u);
+        if (x.nv) tma_load_3d(smem_u32(A32), &tmap_om, 0, x.h, static_cast<int>(x.r0), bar_a);
+    };
+    auto issue_ob = [&](const CorrUnit& x, int buf) {
+        mbar_arrive_expect_tx(bar_b(buf), x.nv ? static_cast<uint32_t>(obUnit) : 0u);
+        if (x.nv)
+            for (int j = 0; j < 2 * nb; ++j)
+                tma_load_3d(smem_u32(B32 + buf * obUnit + j * 8192), &tmap_ob, x.vb * 64 * nb + 32 * j, x.h,
+                            static_cast<int>(x.r0), bar_b(buf));
+    };
+    // S_start[n][h][k][v0 .. v0 + 64 nb) as split MN-major tiles: row k, 8
+    // values per 16-byte chunk; loads first, then the splits
+    auto load_start = [&](const CorrUnit& x) {
+        const float* src = a.starts + (static_cast<long long>(x.n) * H + x.h) * K * V + x.vb * 64 * nb;
         for (int base = 0; base < K * 8 * nb; base += 4 * kCorrThreads) {
             float4 sv[8];
 #pragma unroll
@@ -162,121 +259,164 @@ __global__ void __launch_bounds__(kCorrThreads) gdn_split_correct_kernel(const S
             for (int i = 0; i < 4; ++i) {
                 const int e = base + tid + kCorrThreads * i, k = e / (8 * nb), c = e % (8 * nb);
                 if (e < K * 8 * nb) {
-                    const float x[8] = {sv[2 * i].x, sv[2 * i].y, sv[2 * i].z, sv[2 * i].w,
-                                        sv[2 * i + 1].x, sv[2 * i + 1].y, sv[2 * i + 1].z, sv[2 * i + 1].w};
-                    store_split_chunk(Bhi + (c >> 3) * bBytes, Blo + (c >> 3) * bBytes, k, c & 7, x);
+                    const float x8[8] = {sv[2 * i].x, sv[2 * i].y, sv[2 * i].z, sv[2 * i].w,
+                                         sv[2 * i + 1].x, sv[2 * i + 1].y, sv[2 * i + 1].z, sv[2 * i + 1].w};
+                    store_split_chunk(Bhi + (c >> 3) * bBytes, Blo + (c >> 3) * bBytes, k, c & 7, x8);
                 }
             }
         }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
+    };
 
-    uint32_t phase = 0;
+    // Every thread counts the copies and products in flight on each barrier
+    // (the issue decisions depend on the unit index only), so that a CTA
+    // whose wait ran out still lets each of them land before it leaves.
+    // Bit i of ph_*: the phase awaited next on barrier i of its pair.
+    uint32_t ph_a = 0, ph_mma = 0, ph_b = 0;
+    int pend_a = 0, pend_m0 = 0, pend_m1 = 0, pend_b0 = 0, pend_b1 = 0;
     bool failed = false;
-    const int row = 16 * warp + (lane & 15);      // accumulator row of this lane
-    const int cpart = 32 * (lane >> 4);           // its 32 columns of each 64-column block
-    // this thread's slots of the A tile: e = tid + 128 i -> row e / (d_k / 8),
-    // 8-value chunk e % (d_k / 8); the next chunk's values are loaded while
-    // the current chunk's product and epilogue run
-    const int na = K / 16;                        // slots per thread (8 or 4)
-    float4 pre[16];
-    auto load_a = [&](int c) {
-        const long long r0 = t0 + static_cast<long long>(c) * kChunk;
-        const int nv = min(kChunk, t1 - static_cast<int>(r0));
+    const int row = 16 * (warp & 3) + (lane & 15);  // accumulator row of this lane
+    const int cpart = 32 * (lane >> 4);             // its 32 columns of the 64-column block
+    // the block: warps 0-3 the first, 4-7 the second (one block: warps 4-7 idle)
+    const int my_blk = warp >> 2;
+    const bool epi = my_blk < nb;
+
+    // epilogue of the k-th unit x of this CTA: out = bf16(O_b + its product)
+    auto epilogue = [&](const CorrUnit& x, int k) {
+        const int buf = k & 1;
+        if (mbar_wait(bar_b(buf), (ph_b >> buf) & 1u, wl)) {
+            ph_b ^= 1u << buf;
+            if (buf) --pend_b1; else --pend_b0;
+        } else {
+            failed = true;
+        }
+        if (mbar_wait(bar_mma(buf), (ph_mma >> buf) & 1u, wl)) {
+            ph_mma ^= 1u << buf;
+            if (buf) --pend_m1; else --pend_m0;
+        } else {
+            failed = true;
+        }
+        tc_fence_after();
+        if (epi) {
+            float acc[32];
+            ld_half32(tmem, warp & 3, 128 * buf + 64 * my_blk, acc);
+            if (row < x.nv) {
+                // columns 64 my_blk + cpart .. + 31: row `row` of box 2 my_blk + cpart / 32,
+                // its 16-byte chunk q at q ^ (row % 8)
+                const uint8_t* box = B32 + buf * obUnit + (2 * my_blk + (cpart >> 5)) * 8192 + row * 128;
+                float4 ob4[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            pre[2 * i] = pre[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int e = tid + kCorrThreads * i, r = e / (K / 8), c8 = e % (K / 8);
-            if (i < na && r < nv) {
-                const float4* s4 = reinterpret_cast<const float4*>(a.om + ((r0 + r) * H + h) * K + 8 * c8);
-                pre[2 * i] = s4[0];
-                pre[2 * i + 1] = s4[1];
+                for (int q = 0; q < 8; ++q) ob4[q] = *reinterpret_cast<const float4*>(box + ((q ^ (row & 7)) << 4));
+                uint4* dst = reinterpret_cast<uint4*>(a.out + (x.r0 + row) * H * static_cast<long long>(V) +
+                                                      static_cast<long long>(x.h) * V + x.vb * 64 * nb +
+                                                      64 * my_blk + cpart);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x0 = ob4[2 * q], x1 = ob4[2 * q + 1];
+                    const float* y = acc + 8 * q;
+                    dst[q] = make_uint4(pack_bf16x2(x0.x + y[0], x0.y + y[1]), pack_bf16x2(x0.z + y[2], x0.w + y[3]),
+                                        pack_bf16x2(x1.x + y[4], x1.y + y[5]), pack_bf16x2(x1.z + y[6], x1.w + y[7]));
+                }
             }
         }
     };
-    load_a(c_begin);
-    for (int c = c_begin; c < c_end; ++c) {
-        const long long r0 = t0 + static_cast<long long>(c) * kChunk;
-        const int nv = min(kChunk, t1 - static_cast<int>(r0));
-        // A = O_M rows r0 .. r0 + 63 (rows past the segment are zero)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < na) {
-                const int e = tid + kCorrThreads * i, r = e / (K / 8), c8 = e % (K / 8);
-                const float x[8] = {pre[2 * i].x, pre[2 * i].y, pre[2 * i].z, pre[2 * i].w,
-                                    pre[2 * i + 1].x, pre[2 * i + 1].y, pre[2 * i + 1].z, pre[2 * i + 1].w};
-                store_split_chunk(Ahi + (c8 >> 3) * kCorrTile, Alo + (c8 >> 3) * kCorrTile, r, c8 & 7, x);
+
+    CorrUnit cur = corr_unit(a, nvb, u_begin);
+    CorrUnit prev = cur;
+    const bool two = u_begin + 1 < u_end;
+    if (tid == 0) {
+        issue_om(cur);
+        issue_ob(cur, 0);
+        if (two) issue_ob(corr_next(a, nvb, cur), 1);
+    }
+    pend_a = 1;
+    pend_b0 = 1;
+    pend_b1 = two ? 1 : 0;
+    for (long long u = u_begin; u < u_end; ++u) {
+        const int k = static_cast<int>(u - u_begin), buf = k & 1;
+        const CorrUnit nxt = corr_next(a, nvb, cur);  // used only while u + 1 < u_end
+        if (k == 0 || cur.c == 0) {
+            // a new (segment, head, value block): its start-state block, once
+            // the previous unit's product (the B tiles' last reader) is done;
+            // this wait consumes nothing, the epilogue waits on the same phase
+            if (k > 0 && !mbar_wait(bar_mma(buf ^ 1), (ph_mma >> (buf ^ 1)) & 1u, wl)) failed = true;
+            if (!failed) load_start(cur);
+        }
+        // A = O_M rows r0 .. r0 + 63 as split tiles in operand buffer buf
+        // (rows past the segment are zero); its last reader was the product
+        // of unit k - 2, whose epilogue has run
+        if (mbar_wait(bar_a, ph_a, wl)) {
+            ph_a ^= 1u;
+            --pend_a;
+        } else {
+            failed = true;
+        }
+        uint8_t* ahi = Aop + buf * aBytes;
+        uint8_t* alo = ahi + kreg * kCorrTile;
+#pragma unroll 8
+        for (int e = tid; e < 64 * (K / 8); e += kCorrThreads) {
+            const int r = e / (K / 8), c8 = e % (K / 8);
+            float x8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (r < cur.nv) {
+                const float4 v0 = *reinterpret_cast<const float4*>(A32 + r * K + 8 * c8);
+                const float4 v1 = *reinterpret_cast<const float4*>(A32 + r * K + 8 * c8 + 4);
+                x8[0] = v0.x; x8[1] = v0.y; x8[2] = v0.z; x8[3] = v0.w;
+                x8[4] = v1.x; x8[5] = v1.y; x8[6] = v1.z; x8[7] = v1.w;
             }
+            store_split_chunk(ahi + (c8 >> 3) * kCorrTile, alo + (c8 >> 3) * kCorrTile, r, c8 & 7, x8);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        // A32 is read out and the operand tiles are in; every thread takes
+        // the same decision to leave
+        if (__syncthreads_or(failed)) break;
+        tc_fence_after();
         if (warp == 0) {
+            if (u + 1 < u_end && lane == 0) issue_om(nxt);
+            __syncwarp();
             if (elect_one()) {
                 tc_fence_after();
                 const uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64 * nb);
-                const uint32_t ah = smem_u32(Ahi), al = smem_u32(Alo), bh = smem_u32(Bhi), bl = smem_u32(Blo);
+                const uint32_t ah = smem_u32(ahi), al = smem_u32(alo), bh = smem_u32(Bhi), bl = smem_u32(Blo);
                 for (int s = 0; s < K / 16; ++s) {
                     const uint32_t ao = (s >> 2) * kCorrTile + (s & 3) * 32;
                     const uint64_t da_h = desc_sw128(ah + ao, 0, 1024), da_l = desc_sw128(al + ao, 0, 1024);
                     const uint64_t db_h = desc_sw128(bh + s * 2048, bBytes, 1024);
                     const uint64_t db_l = desc_sw128(bl + s * 2048, bBytes, 1024);
-                    mma_bf16(tmem, da_h, db_h, id, s > 0);
-                    mma_bf16(tmem, da_h, db_l, id, 1);
-                    mma_bf16(tmem, da_l, db_h, id, 1);
+                    const uint32_t d = tmem + 128 * buf;
+                    mma_bf16(d, da_h, db_h, id, s > 0);
+                    mma_bf16(d, da_h, db_l, id, 1);
+                    mma_bf16(d, da_l, db_h, id, 1);
                 }
-                mma_commit(bar);
+                mma_commit(bar_mma(buf));
             }
             __syncwarp();
         }
-        // while the product runs: this chunk's O_b values and the next chunk's O_M
-        float4 ob[2][8];
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) ob[blk][q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (blk < nb && row < nv) {
-                const float4* b4 = reinterpret_cast<const float4*>(
-                    a.ob + (r0 + row) * H * static_cast<long long>(V) + static_cast<long long>(h) * V + v0 + 64 * blk + cpart);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) ob[blk][q] = b4[q];
+        if (u + 1 < u_end) ++pend_a;
+        if (buf) ++pend_m1; else ++pend_m0;
+        // the previous unit's epilogue while this unit's product runs; then
+        // its O_b staging buffer takes unit u + 1's
+        if (k > 0) {
+            epilogue(prev, k - 1);
+            tc_fence_before();
+            if (__syncthreads_or(failed)) break;
+            if (u + 1 < u_end) {
+                if (tid == 0) issue_ob(nxt, buf ^ 1);
+                if (buf) ++pend_b0; else ++pend_b1;
             }
         }
-        if (c + 1 < c_end) load_a(c + 1);
-        if (!mbar_wait(bar, phase, a.wait_limit)) failed = true;
-        phase ^= 1u;
-        tc_fence_after();
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            if (blk < nb) {
-                float acc[32];
-                ld_half32(tmem, warp, 64 * blk, acc);
-                if (row < nv) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        a.out + (r0 + row) * H * static_cast<long long>(V) + static_cast<long long>(h) * V + v0 + 64 * blk + cpart);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 x0 = ob[blk][2 * q], x1 = ob[blk][2 * q + 1];
-                        const float* y = acc + 8 * q;
-                        dst[q] = make_uint4(pack_bf16x2(x0.x + y[0], x0.y + y[1]), pack_bf16x2(x0.z + y[2], x0.w + y[3]),
-                                            pack_bf16x2(x1.x + y[4], x1.y + y[5]), pack_bf16x2(x1.z + y[6], x1.w + y[7]));
-                    }
-                }
-            }
-        }
-        tc_fence_before();
-        // the next chunk rewrites A and the accumulator; every thread takes
-        // the same decision to leave
-        if (__syncthreads_or(failed)) break;
+        prev = cur;
+        cur = nxt;
     }
+    if (!failed) epilogue(prev, static_cast<int>(u_end - 1 - u_begin));
     if (failed) {
         record_error(a.err, kErrTimeout);
-        // the product never signalled: let it land before the TMEM is freed
-        mbar_wait(bar, phase ^ 1u, kDefaultWaitLimit);
+        // let every copy and product still in flight land before the shared
+        // memory and the TMEM are given back
+        for (; pend_a > 0; --pend_a, ph_a ^= 1u) mbar_wait(bar_a, ph_a, kDefaultWaitLimit);
+        for (; pend_b0 > 0; --pend_b0, ph_b ^= 1u) mbar_wait(bar_b(0), ph_b & 1u, kDefaultWaitLimit);
+        for (; pend_b1 > 0; --pend_b1, ph_b ^= 2u) mbar_wait(bar_b(1), (ph_b >> 1) & 1u, kDefaultWaitLimit);
+        for (; pend_m0 > 0; --pend_m0, ph_mma ^= 1u) mbar_wait(bar_mma(0), ph_mma & 1u, kDefaultWaitLimit);
+        for (; pend_m1 > 0; --pend_m1, ph_mma ^= 2u) mbar_wait(bar_mma(1), (ph_mma >> 1) & 1u, kDefaultWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -298,14 +438,41 @@ cudaError_t launch_split_compose(const SplitArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+namespace {
+
+// 3-D view {inner, head, row} of a (rows, H, inner) fp32 tensor, box
+// {box_inner, 1, 64}; 128-byte swizzle when the box is 32 values wide.
+bool make_f32_rows_map(CUtensorMap* m, const float* base, long long rows, int H, int inner, int box_inner) {
+    tc::EncodeTiledFn fn = tc::encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 4, static_cast<cuuint64_t>(H) * inner * 4};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, box_inner == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_split_correct(const SplitCorrectArgs& a, cudaStream_t stream) {
-    if (a.max_chunks == 0 || a.nseq == 0) return cudaSuccess;
+    if (a.max_chunks == 0 || a.nseq == 0 || a.rows == 0) return cudaSuccess;
     const int nb = a.d_v >= 128 ? 2 : 1;
-    const int smem = 2 * nb * a.d_k * 128 + 2 * (a.d_k / 64) * kCorrTile + 16 + 1024;
+    CUtensorMap mom, mob;
+    memset(&mom, 0, sizeof(mom));
+    memset(&mob, 0, sizeof(mob));
+    if (!make_f32_rows_map(&mom, a.om, a.rows, a.H, a.d_k, a.d_k) || !make_f32_rows_map(&mob, a.ob, a.rows, a.H, a.d_v, 32))
+        return cudaErrorInvalidValue;
+    const int smem = 2 * nb * a.d_k * 128 + 4 * (a.d_k / 64) * kCorrTile + 64 * a.d_k * 4 + 2 * 64 * 64 * nb * 4 + 64 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gdn_split_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.max_chunks + kCorrG - 1) / kCorrG, a.H * (a.d_v / (64 * nb)), a.nseq);
-    gdn_split_correct_kernel<<<grid, kCorrThreads, smem, stream>>>(a);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long units = static_cast<long long>(a.nseq) * a.H * (a.d_v / (64 * nb)) * a.max_chunks;
+    const int grid = static_cast<int>(units < sms ? units : sms);
+    gdn_split_correct_kernel<<<grid, kCorrThreads, smem, stream>>>(mom, mob, a);
     return cudaGetLastError();
 }
 
