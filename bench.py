@@ -304,6 +304,15 @@ def run_ours(args):
     libbuild.build()
     gdn.load()
 
+    if args.split_only:
+        # profiling aid: only the sequence-split measurement at one segment
+        # count (one warm-up and one timed call per route), printed as JSON
+        if rank == 0:
+            r = measure_split(gdn, torch, dev, torch.cuda.current_stream(), segs=(args.split_only,), steps=1,
+                              warmup=1)
+            print(json.dumps(r))
+        return 0
+
     B, T, H, K, V = (SHAPE[k] for k in ("B", "T", "H", "d_k", "d_v"))
     wl = W.make_workload(2, B=B, T=T, H=H, d_k=K, d_v=V, with_grad=True,
                          seed=rank_seed(rank))
@@ -1104,6 +1113,8 @@ def main():
     ap.add_argument("--no-probes", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--split-only", type=int, default=0, metavar="NSEG",
+                    help="run only the sequence-split measurement at NSEG segments (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
