@@ -747,9 +747,10 @@ gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
         return GDN_OK;
     }
     // carries, side by side on two streams, outputs in fp32: b from a zero
-    // start (output O_b), M from the identity with zero values (output O_M,
-    // d_k columns); the chain is linear in its start state, so a segment's
-    // output is O_b + O_M S_start
+    // start (output O_b; a sequence's first segment from its initial state),
+    // M from the identity with zero values (output O_M, d_k columns); the
+    // chain is linear in its start state, so a later segment's output is
+    // O_b + O_M S_start
     cudaStream_t aux = aux_stream();
     if (!aux) return GDN_ERR_CUDA;
     cudaEvent_t forked = nullptr, joined = nullptr;
@@ -765,7 +766,10 @@ gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
             break;
         }
         gdn::FwdArgs fb = f;
-        fb.v = v; fb.d_v = d_v; fb.initial_state = nullptr; fb.out = nullptr;
+        // the zero-start run starts each sequence's first segment from its
+        // initial state (the setup put it there), so that segment needs no
+        // correction
+        fb.v = v; fb.d_v = d_v; fb.initial_state = sa.starts; fb.out = nullptr;
         fb.out_f32 = reinterpret_cast<float*>(w + L.ob); fb.final_state = reinterpret_cast<float*>(w + L.bfin);
         if (!launched(gdn::launch_fwd_ws_f32(fb, gdn::kDefaultWaitLimit, stream))) rs = GDN_ERR_CUDA;
         gdn::FwdArgs fm = f;

@@ -30,68 +30,100 @@ __device__ __forceinline__ long long seg_start(long long b, int j, int T, int ns
     return b * T + (j == 0 ? 0 : kChunk * ((j * nch) / nseg));
 }
 
-// cu[s] for s = 0 .. B nseg (the segment bounds above); then the identity
-// start state of every (segment, head).
+// cu[s] for s = 0 .. B nseg (the segment bounds above); the identity start
+// state of every (segment, head); and the zero-start run's start states:
+// a sequence's initial state for its first segment (so that segment's run
+// is already its true one), zero for the others.
 __global__ void gdn_split_setup_kernel(const SplitArgs a) {
     const long long nseq = static_cast<long long>(a.B) * a.nseg;
     const long long kk = static_cast<long long>(a.d_k) * a.d_k;
-    const long long total = nseq * a.H * kk;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total + nseq + 1;
+    const long long kv = static_cast<long long>(a.d_k) * a.d_v;
+    const long long total = nseq * a.H * kk, total_s = nseq * a.H * kv;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total + total_s + nseq + 1;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (i <= nseq) {
             const long long pos = i == nseq ? static_cast<long long>(a.B) * a.T
                                             : seg_start(i / a.nseg, static_cast<int>(i % a.nseg), a.T, a.nseg);
             a.cu[i] = static_cast<int32_t>(pos);
-        } else {
+        } else if (i <= nseq + total) {
             const long long e = i - nseq - 1;
             const long long r = (e % kk) / a.d_k, c = e % a.d_k;
             a.ident[e] = r == c ? 1.f : 0.f;
+        } else {
+            const long long e = i - nseq - 1 - total;   // [n][h][k][v]
+            const long long n = e / (a.H * kv), rest = e % (a.H * kv);
+            a.starts[e] = (n % a.nseg == 0 && a.initial_state) ? a.initial_state[(n / a.nseg) * a.H * kv + rest] : 0.f;
         }
     }
 }
 
 // Per (column block of 32, head, sequence): S = the sequence's initial state;
-// for each segment j in order, starts[j] = S and S <- M_j S + b_j; the last S
-// is the sequence's final state.  256 threads: thread t owns row t / 2 and
-// columns 16 (t % 2) .. + 15 of the block.
+// for each segment j in order, starts[j] = S and S <- M_j S + b_j (j = 0: S <-
+// b_0, the first segment's run having started from the initial state); the
+// last S is the sequence's final state.  256 threads: thread t owns row t / 2 and
+// columns 16 (t % 2) .. + 15 of the block; S sits in shared memory in rows of
+// 16-byte chunks, and each thread's row of M_j comes in 32 values at a time
+// (eight 16-byte loads in flight); every sum runs over m in order.
 constexpr int kComposeThreads = 256;
 constexpr int kCols = 32;
+constexpr int kSRow = kCols + 4;  // row stride of S (16-byte rows)
 __global__ void __launch_bounds__(kComposeThreads) gdn_split_compose_kernel(const SplitArgs a) {
     const int cb = blockIdx.x * kCols, h = blockIdx.y, b = blockIdx.z;
     const int K = a.d_k, V = a.d_v;
     const int t = threadIdx.x, r = t >> 1, c0 = 16 * (t & 1);
-    __shared__ float S[128][kCols + 1];
+    __shared__ __align__(16) float S[128][kSRow];
     const bool live = r < K;
     if (live) {
+        float4* srow = reinterpret_cast<float4*>(&S[r][c0]);
+        const float4* src = a.initial_state ? reinterpret_cast<const float4*>(
+                                                  a.initial_state + ((static_cast<long long>(b) * a.H + h) * K + r) * V + cb + c0)
+                                            : nullptr;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            S[r][c0 + c] = a.initial_state
-                               ? a.initial_state[((static_cast<long long>(b) * a.H + h) * K + r) * V + cb + c0 + c]
-                               : 0.f;
+        for (int c4 = 0; c4 < 4; ++c4) srow[c4] = src ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
     for (int j = 0; j < a.nseg; ++j) {
         const long long n = static_cast<long long>(b) * a.nseg + j;
         float acc[16];
         if (live) {
-            float* st = a.starts + ((n * a.H + h) * K + r) * V + cb + c0;
-            const float* bj = a.b_fin + ((n * a.H + h) * K + r) * V + cb + c0;
+            float4* st = reinterpret_cast<float4*>(a.starts + ((n * a.H + h) * K + r) * V + cb + c0);
+            const float4* bj = reinterpret_cast<const float4*>(a.b_fin + ((n * a.H + h) * K + r) * V + cb + c0);
+            const float4* srow = reinterpret_cast<const float4*>(&S[r][c0]);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                st[c] = S[r][c0 + c];
-                acc[c] = bj[c];
+            for (int c4 = 0; c4 < 4; ++c4) {
+                st[c4] = srow[c4];
+                const float4 b4 = bj[c4];
+                acc[4 * c4] = b4.x; acc[4 * c4 + 1] = b4.y; acc[4 * c4 + 2] = b4.z; acc[4 * c4 + 3] = b4.w;
             }
-            const float* mrow = a.m_fin + ((n * a.H + h) * K + r) * static_cast<long long>(K);
-            for (int m = 0; m < K; ++m) {
-                const float mv = mrow[m];
+            const float4* mrow = reinterpret_cast<const float4*>(a.m_fin + ((n * a.H + h) * K + r) * static_cast<long long>(K));
+            for (int m32 = 0; j > 0 && m32 < K; m32 += 32) {
+                float4 mv[8];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) acc[c] = fmaf(mv, S[m][c0 + c], acc[c]);
+                for (int u = 0; u < 8; ++u) mv[u] = mrow[m32 / 4 + u];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float mvals[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4* sm4 = reinterpret_cast<const float4*>(&S[m32 + 4 * u + e][c0]);
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const float4 s4 = sm4[c4];
+                            acc[4 * c4] = fmaf(mvals[e], s4.x, acc[4 * c4]);
+                            acc[4 * c4 + 1] = fmaf(mvals[e], s4.y, acc[4 * c4 + 1]);
+                            acc[4 * c4 + 2] = fmaf(mvals[e], s4.z, acc[4 * c4 + 2]);
+                            acc[4 * c4 + 3] = fmaf(mvals[e], s4.w, acc[4 * c4 + 3]);
+                        }
+                    }
+                }
             }
         }
         __syncthreads();
         if (live) {
+            float4* srow = reinterpret_cast<float4*>(&S[r][c0]);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) S[r][c0 + c] = acc[c];
+            for (int c4 = 0; c4 < 4; ++c4)
+                srow[c4] = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
         }
         __syncthreads();
     }
@@ -116,8 +148,10 @@ __global__ void __launch_bounds__(kComposeThreads) gdn_split_compose_kernel(cons
 // distinct banks) into one of two staging tiles.  A unit's product runs into
 // one of two TMEM accumulators while the epilogue of the unit before it
 // (O_b + the product, to bf16) runs.  A unit past the end of its
-// segment copies and stores nothing.  The start-state block is converted
-// when a CTA's range enters a new (segment, head, value block).
+// segment copies and stores nothing.  A sequence's first segment started its
+// zero-start run from the true initial state, so its units only convert
+// O_b (no O_M rows, no product).  The start-state block is converted when a
+// CTA's range enters a new (segment, head, value block).
 constexpr int kCorrThreads = 256;  // warps w and w + 4 share TMEM subpartition w % 4
 constexpr int kCorrTile = 64 * 128;  // 64 rows x 128 B
 
@@ -127,6 +161,7 @@ constexpr int kCorrTile = 64 * 128;  // 64 rows x 128 B
 // changes.
 struct CorrUnit {
     int c, vb, h, n;     // chunk, value block, head, segment
+    bool first;          // a sequence's first segment: out = O_b
     long long t0, t1;    // the segment's packed rows [t0, t1)
     long long r0;        // first row of the chunk
     int nv;              // its rows inside the segment (0: past the segment's end)
@@ -142,6 +177,7 @@ __device__ __forceinline__ void corr_segment(const SplitCorrectArgs& a, CorrUnit
     // the segment's bounds by the setup's rule (no dependent loads of cu)
     const long long b = x.n / a.nseg;
     const int j = x.n % a.nseg;
+    x.first = j == 0;
     x.t0 = seg_start(b, j, a.T, a.nseg);
     x.t1 = j + 1 < a.nseg ? seg_start(b, j + 1, a.T, a.nseg) : (b + 1) * a.T;
 }
@@ -229,8 +265,9 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
     // one thread: a unit's O_M box, and its O_b boxes into staging buffer
     // buf; a unit past its segment's end loads nothing and only arrives
     auto issue_om = [&](const CorrUnit& x) {
-        mbar_arrive_expect_tx(bar_a, x.nv ? static_cast<uint32_t>(64 * K * 4) : 0u);
-        if (x.nv) tma_load_3d(smem_u32(A32), &tmap_om, 0, x.h, static_cast<int>(x.r0), bar_a);
+        const bool load = x.nv && !x.first;
+        mbar_arrive_expect_tx(bar_a, load ? static_cast<uint32_t>(64 * K * 4) : 0u);
+        if (load) tma_load_3d(smem_u32(A32), &tmap_om, 0, x.h, static_cast<int>(x.r0), bar_a);
     };
     auto issue_ob = [&](const CorrUnit& x, int buf) {
         mbar_arrive_expect_tx(bar_b(buf), x.nv ? static_cast<uint32_t>(obUnit) : 0u);
@@ -298,7 +335,12 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
         tc_fence_after();
         if (epi) {
             float acc[32];
-            ld_half32(tmem, warp & 3, 128 * buf + 64 * my_blk, acc);
+            if (x.first) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            } else {
+                ld_half32(tmem, warp & 3, 128 * buf + 64 * my_blk, acc);
+            }
             if (row < x.nv) {
                 // columns 64 my_blk + cpart .. + 31: row `row` of box 2 my_blk + cpart / 32,
                 // its 16-byte chunk q at q ^ (row % 8)
@@ -339,7 +381,7 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
             // the previous unit's product (the B tiles' last reader) is done;
             // this wait consumes nothing, the epilogue waits on the same phase
             if (k > 0 && !mbar_wait(bar_mma(buf ^ 1), (ph_mma >> (buf ^ 1)) & 1u, wl)) failed = true;
-            if (!failed) load_start(cur);
+            if (!failed && !cur.first) load_start(cur);
         }
         // A = O_M rows r0 .. r0 + 63 as split tiles in operand buffer buf
         // (rows past the segment are zero); its last reader was the product
@@ -353,7 +395,7 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
         uint8_t* ahi = Aop + buf * aBytes;
         uint8_t* alo = ahi + kreg * kCorrTile;
 #pragma unroll 8
-        for (int e = tid; e < 64 * (K / 8); e += kCorrThreads) {
+        for (int e = tid; !cur.first && e < 64 * (K / 8); e += kCorrThreads) {
             const int r = e / (K / 8), c8 = e % (K / 8);
             float x8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (r < cur.nv) {
@@ -377,7 +419,9 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
                 tc_fence_after();
                 const uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64 * nb);
                 const uint32_t ah = smem_u32(ahi), al = smem_u32(alo), bh = smem_u32(Bhi), bl = smem_u32(Blo);
-                for (int s = 0; s < K / 16; ++s) {
+                // (a first-segment unit commits with no product: the barrier
+                // then only waits for the products before it)
+                for (int s = 0; !cur.first && s < K / 16; ++s) {
                     const uint32_t ao = (s >> 2) * kCorrTile + (s & 3) * 32;
                     const uint64_t da_h = desc_sw128(ah + ao, 0, 1024), da_l = desc_sw128(al + ao, 0, 1024);
                     const uint64_t db_h = desc_sw128(bh + s * 2048, bBytes, 1024);
@@ -426,7 +470,8 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
 }  // namespace
 
 cudaError_t launch_split_setup(const SplitArgs& a, cudaStream_t stream) {
-    const long long n = static_cast<long long>(a.B) * a.nseg * a.H * a.d_k * a.d_k + static_cast<long long>(a.B) * a.nseg + 1;
+    const long long n = static_cast<long long>(a.B) * a.nseg * a.H * a.d_k * (a.d_k + a.d_v) +
+                        static_cast<long long>(a.B) * a.nseg + 1;
     const long long blocks = (n + 255) / 256;
     gdn_split_setup_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(a);
     return cudaGetLastError();
