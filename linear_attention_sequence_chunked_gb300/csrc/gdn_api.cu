@@ -775,6 +775,7 @@ gdn_status gdn_chunk_fwd_split(const gdn_bf16* q, const gdn_bf16* k, const gdn_b
         gdn::FwdArgs fm = f;
         fm.v = reinterpret_cast<const gdn_bf16*>(w + L.zeros); fm.d_v = d_k; fm.initial_state = sa.ident;
         fm.out = nullptr; fm.out_f32 = reinterpret_cast<float*>(w + L.om);
+        fm.out_split = 1;  // O_M as bf16 hi and lo planes: the correction's operand tiles
         fm.final_state = reinterpret_cast<float*>(w + L.mfin);
         if (cudaMemsetAsync(w + L.zeros, 0, 2ull * rows * H * d_k, aux) != cudaSuccess) rs = GDN_ERR_CUDA;
         else if (!launched(gdn::launch_fwd_ws_f32(fm, gdn::kDefaultWaitLimit, aux))) rs = GDN_ERR_CUDA;

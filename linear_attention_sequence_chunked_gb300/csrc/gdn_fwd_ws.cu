@@ -146,6 +146,7 @@ struct ChainArgs {
     const int32_t* cu_seqlens;
     uint16_t* out;                // forward output (may be null)
     float* out_f32;               // forward output in fp32 instead (the fp32-output instantiation only)
+    int out_split;                // ... as bf16 hi and lo planes in out_f32's bytes (the split's identity run)
     float* state_out;             // forward: final state; backward: initial-state gradient (may be null)
     float* chunk_states;          // forward: chunk start states; backward: chunk end-state gradients (may be null)
     const uint8_t* chunk_T;       // T operand tiles of every chunk (may be null: formed in place)
@@ -518,13 +519,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (mine) {
                         const long long oo = ((row_base + c0 + hrow) * H + h) * static_cast<long long>(V) + vs * kVs + cq;
                         if constexpr (kF32Out) {
-                            float4* dst = reinterpret_cast<float4*>(p.out_f32 + oo);
+                            if (p.out_split) {
+                                // hi plane, then lo plane (x = hi + lo), each [rows][H][d_v] bf16
+                                float x[16];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_float4(scale * fmaf(gi, qs[4 * j], pd[4 * j]),
-                                                     scale * fmaf(gi, qs[4 * j + 1], pd[4 * j + 1]),
-                                                     scale * fmaf(gi, qs[4 * j + 2], pd[4 * j + 2]),
-                                                     scale * fmaf(gi, qs[4 * j + 3], pd[4 * j + 3]));
+                                for (int c = 0; c < 16; ++c) x[c] = scale * fmaf(gi, qs[c], pd[c]);
+                                const long long plane =
+                                    static_cast<long long>(p.cu_seqlens ? 1 : p.N) * p.T * H * static_cast<long long>(V);
+                                uint4* dhi = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out_f32) + oo);
+                                uint4* dlo = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out_f32) + plane + oo);
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    uint32_t wh[4], wl4[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int c = j * 8 + 2 * e;
+                                        split_bf16x2(x[c], x[c + 1], wh[e], wl4[e]);
+                                    }
+                                    dhi[j] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                                    dlo[j] = make_uint4(wl4[0], wl4[1], wl4[2], wl4[3]);
+                                }
+                            } else {
+                                float4* dst = reinterpret_cast<float4*>(p.out_f32 + oo);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    dst[j] = make_float4(scale * fmaf(gi, qs[4 * j], pd[4 * j]),
+                                                         scale * fmaf(gi, qs[4 * j + 1], pd[4 * j + 1]),
+                                                         scale * fmaf(gi, qs[4 * j + 2], pd[4 * j + 2]),
+                                                         scale * fmaf(gi, qs[4 * j + 3], pd[4 * j + 3]));
+                            }
                         } else {
                             uint4* dst = reinterpret_cast<uint4*>(p.out + oo);
 #pragma unroll
@@ -1250,6 +1273,7 @@ cudaError_t launch_fwd_ws_f32(const FwdArgs& a, uint32_t wait_limit, cudaStream_
     ChainArgs c{};
     c.q = a.q; c.k = a.k; c.v = a.v; c.d_out = nullptr; c.g = a.g; c.beta = a.beta; c.scale = a.scale;
     c.state_in = a.initial_state; c.cu_seqlens = a.cu_seqlens; c.out = nullptr; c.out_f32 = a.out_f32;
+    c.out_split = a.out_split;
     c.state_out = a.final_state; c.chunk_states = a.chunk_states; c.chunk_T = a.chunk_T;
     c.N = a.N; c.T = a.T; c.H = a.H; c.d_k = a.d_k; c.d_v = a.d_v; c.err = a.err; c.stall = 0;
     return launch_chain<false, true>(c, wait_limit, stream);

@@ -17,7 +17,9 @@ struct FwdArgs {
     const float* initial_state;
     const int32_t* cu_seqlens;
     uint16_t* out;          // may be null: skip the output
-    float* out_f32;         // launch_fwd_ws_f32 only: the output in fp32 [rows][H][d_v]
+    float* out_f32;         // launch_fwd_ws_f32 only: the output in fp32 [rows][H][d_v], or with
+                            // out_split its bf16 hi and lo parts as two planes [2][rows][H][d_v]
+    int out_split;          // launch_fwd_ws_f32 only (see out_f32)
     float* final_state;     // may be null
     float* chunk_states;    // may be null: per-chunk start states, bf16 hi/lo operand tiles
                             // [slot][H][d_v/64][hi, lo][d_k rows x 128 B] (the bytes of fp32 [d_k][d_v]);

@@ -211,7 +211,8 @@ __device__ __forceinline__ CorrUnit corr_next(const SplitCorrectArgs& a, int nvb
 }
 
 __global__ void __launch_bounds__(kCorrThreads, 1)
-    gdn_split_correct_kernel(const __grid_constant__ CUtensorMap tmap_om, const __grid_constant__ CUtensorMap tmap_ob,
+    gdn_split_correct_kernel(const __grid_constant__ CUtensorMap tmap_omh, const __grid_constant__ CUtensorMap tmap_oml,
+                             const __grid_constant__ CUtensorMap tmap_ob,
                              const SplitCorrectArgs a) {
     using namespace sm100;
     using namespace tc;
@@ -229,21 +230,23 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + smem_align_pad(smem_raw);
     // B: S_start block, [d_k rows][64 value columns] per MN block, hi then lo;
-    // A: [2] O_M rows, [64 rows][64 key columns] per region, hi then lo; then
-    // the fp32 staging: O_M [64][d_k], O_b [2][2 nb boxes][64 rows][32 values]
+    // A: [3] O_M rows, [64 rows][64 key columns] per region, hi then lo (the
+    // identity run wrote O_M as bf16 hi and lo planes, so its TMA boxes land
+    // as operand tiles); O_b staging [2][2 nb boxes][64 rows][32 values]
     const int bBytes = K * 128;                  // one MN block (hi or lo)
     const int obUnit = 64 * 64 * nb * 4;         // one unit's O_b staging
     uint8_t* Bhi = sm;
     uint8_t* Blo = sm + nb * bBytes;
-    uint8_t* Aop = sm + 2 * nb * bBytes;         // [2][hi, lo][kreg regions]
+    uint8_t* Aop = sm + 2 * nb * bBytes;         // [3][hi, lo][kreg regions]
     const int aBytes = 2 * kreg * kCorrTile;
-    float* A32 = reinterpret_cast<float*>(Aop + 2 * aBytes);
-    uint8_t* B32 = reinterpret_cast<uint8_t*>(A32 + 64 * K);
+    uint8_t* B32 = Aop + 3 * aBytes;
     uint64_t* barp = reinterpret_cast<uint64_t*>(B32 + 2 * obUnit);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(barp + 5);
-    const uint32_t bar_a = smem_u32(barp);
-    auto bar_mma = [&](int i) { return smem_u32(barp + 1 + i); };
-    auto bar_b = [&](int i) { return smem_u32(barp + 3 + i); };
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(barp + 10);
+    auto bar_a = [&](int i) { return smem_u32(barp + i); };          // O_M tiles of buffer i (of 3)
+    auto bar_mma = [&](int i) { return smem_u32(barp + 3 + i); };    // product into accumulator i
+    auto bar_b = [&](int i) { return smem_u32(barp + 5 + i); };      // O_b copy of buffer i
+    auto bar_tf = [&](int i) { return smem_u32(barp + 7 + i); };     // accumulator i read out
+    const uint32_t bar_drain = smem_u32(barp + 9);
     constexpr uint32_t kCorrCols = 256;           // two 128-column accumulators
 
     if (warp == 0) {
@@ -251,9 +254,10 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(smem_u32(barp + i), 1);
+        for (int i = 0; i < 10; ++i) mbar_init(smem_u32(barp + i), 1);
         fence_mbar_init();
-        tma_prefetch_desc(&tmap_om);
+        tma_prefetch_desc(&tmap_omh);
+        tma_prefetch_desc(&tmap_oml);
         tma_prefetch_desc(&tmap_ob);
     }
     fence_proxy_async_smem();
@@ -262,12 +266,21 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    // one thread: a unit's O_M box, and its O_b boxes into staging buffer
-    // buf; a unit past its segment's end loads nothing and only arrives
-    auto issue_om = [&](const CorrUnit& x) {
+    // one thread: a unit's O_M tiles into operand buffer j (rows past the
+    // segment come along; each output row reads only its own row of A, and
+    // those rows are not stored), and its O_b boxes into staging buffer buf;
+    // a unit past its segment's end, or of a first segment, loads nothing
+    // and only arrives
+    auto issue_om = [&](const CorrUnit& x, int j) {
         const bool load = x.nv && !x.first;
-        mbar_arrive_expect_tx(bar_a, load ? static_cast<uint32_t>(64 * K * 4) : 0u);
-        if (load) tma_load_3d(smem_u32(A32), &tmap_om, 0, x.h, static_cast<int>(x.r0), bar_a);
+        mbar_arrive_expect_tx(bar_a(j), load ? static_cast<uint32_t>(aBytes) : 0u);
+        if (load) {
+            const uint32_t dst = smem_u32(Aop + j * aBytes);
+            for (int r = 0; r < kreg; ++r) {
+                tma_load_3d(dst + r * kCorrTile, &tmap_omh, 64 * r, x.h, static_cast<int>(x.r0), bar_a(j));
+                tma_load_3d(dst + (kreg + r) * kCorrTile, &tmap_oml, 64 * r, x.h, static_cast<int>(x.r0), bar_a(j));
+            }
+        }
     };
     auto issue_ob = [&](const CorrUnit& x, int buf) {
         mbar_arrive_expect_tx(bar_b(buf), x.nv ? static_cast<uint32_t>(obUnit) : 0u);
@@ -278,13 +291,13 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
     };
     // S_start[n][h][k][v0 .. v0 + 64 nb) as split MN-major tiles: row k, 8
     // values per 16-byte chunk; loads first, then the splits
-    auto load_start = [&](const CorrUnit& x) {
+    auto load_start = [&](const CorrUnit& x, int th, int nth) {
         const float* src = a.starts + (static_cast<long long>(x.n) * H + x.h) * K * V + x.vb * 64 * nb;
-        for (int base = 0; base < K * 8 * nb; base += 4 * kCorrThreads) {
+        for (int base = 0; base < K * 8 * nb; base += 4 * nth) {
             float4 sv[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int e = base + tid + kCorrThreads * i, k = e / (8 * nb), c = e % (8 * nb);
+                const int e = base + th + nth * i, k = e / (8 * nb), c = e % (8 * nb);
                 sv[2 * i] = sv[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (e < K * 8 * nb) {
                     const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<long long>(k) * V + 8 * c);
@@ -294,7 +307,7 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int e = base + tid + kCorrThreads * i, k = e / (8 * nb), c = e % (8 * nb);
+                const int e = base + th + nth * i, k = e / (8 * nb), c = e % (8 * nb);
                 if (e < K * 8 * nb) {
                     const float x8[8] = {sv[2 * i].x, sv[2 * i].y, sv[2 * i].z, sv[2 * i].w,
                                          sv[2 * i + 1].x, sv[2 * i + 1].y, sv[2 * i + 1].z, sv[2 * i + 1].w};
@@ -304,164 +317,159 @@ __global__ void __launch_bounds__(kCorrThreads, 1)
         }
     };
 
-    // Every thread counts the copies and products in flight on each barrier
-    // (the issue decisions depend on the unit index only), so that a CTA
-    // whose wait ran out still lets each of them land before it leaves.
-    // Bit i of ph_*: the phase awaited next on barrier i of its pair.
-    uint32_t ph_a = 0, ph_mma = 0, ph_b = 0;
-    int pend_a = 0, pend_m0 = 0, pend_m1 = 0, pend_b0 = 0, pend_b1 = 0;
-    bool failed = false;
-    const int row = 16 * (warp & 3) + (lane & 15);  // accumulator row of this lane
-    const int cpart = 32 * (lane >> 4);             // its 32 columns of the 64-column block
-    // the block: warps 0-3 the first, 4-7 the second (one block: warps 4-7 idle)
-    const int my_blk = warp >> 2;
-    const bool epi = my_blk < nb;
-
-    // epilogue of the k-th unit x of this CTA: out = bf16(O_b + its product)
-    auto epilogue = [&](const CorrUnit& x, int k) {
-        const int buf = k & 1;
-        if (mbar_wait(bar_b(buf), (ph_b >> buf) & 1u, wl)) {
-            ph_b ^= 1u << buf;
-            if (buf) --pend_b1; else --pend_b0;
-        } else {
-            failed = true;
-        }
-        if (mbar_wait(bar_mma(buf), (ph_mma >> buf) & 1u, wl)) {
-            ph_mma ^= 1u << buf;
-            if (buf) --pend_m1; else --pend_m0;
-        } else {
-            failed = true;
-        }
-        tc_fence_after();
-        if (epi) {
-            float acc[32];
-            if (x.first) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            } else {
-                ld_half32(tmem, warp & 3, 128 * buf + 64 * my_blk, acc);
-            }
-            if (row < x.nv) {
-                // columns 64 my_blk + cpart .. + 31: row `row` of box 2 my_blk + cpart / 32,
-                // its 16-byte chunk q at q ^ (row % 8)
-                const uint8_t* box = B32 + buf * obUnit + (2 * my_blk + (cpart >> 5)) * 8192 + row * 128;
-                float4 ob4[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) ob4[q] = *reinterpret_cast<const float4*>(box + ((q ^ (row & 7)) << 4));
-                uint4* dst = reinterpret_cast<uint4*>(a.out + (x.r0 + row) * H * static_cast<long long>(V) +
-                                                      static_cast<long long>(x.h) * V + x.vb * 64 * nb +
-                                                      64 * my_blk + cpart);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 x0 = ob4[2 * q], x1 = ob4[2 * q + 1];
-                    const float* y = acc + 8 * q;
-                    dst[q] = make_uint4(pack_bf16x2(x0.x + y[0], x0.y + y[1]), pack_bf16x2(x0.z + y[2], x0.w + y[3]),
-                                        pack_bf16x2(x1.x + y[4], x1.y + y[5]), pack_bf16x2(x1.z + y[6], x1.w + y[7]));
-                }
-            }
-        }
+    // Warps 0-3 produce (the O_M conversion into the operand tiles, the
+    // products, the O_M copies), warps 4-7 consume (the epilogues, the O_b
+    // copies); the two groups meet only at mbarriers, whose phases follow
+    // from the unit index k of the CTA's range: unit k is completion k of the
+    // O_M barrier and completion k / 2 of the barriers of its buffer k % 2.
+    const bool producer = warp < 4;
+    const int gtid = tid & 127;                  // thread in its group
+    const int gbar = producer ? 1 : 2;           // the group's named barrier
+    auto group_or = [&](bool pred) -> bool {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"(static_cast<uint32_t>(pred)), "r"(gbar)
+            : "memory");
+        return r != 0;
     };
-
+    auto par = [](long long k) { return static_cast<uint32_t>((k >> 1) & 1); };  // phase of unit k on its buffer
+    bool failed = false;
+    const long long nk = u_end - u_begin;
     CorrUnit cur = corr_unit(a, nvb, u_begin);
-    CorrUnit prev = cur;
-    const bool two = u_begin + 1 < u_end;
-    if (tid == 0) {
-        issue_om(cur);
-        issue_ob(cur, 0);
-        if (two) issue_ob(corr_next(a, nvb, cur), 1);
-    }
-    pend_a = 1;
-    pend_b0 = 1;
-    pend_b1 = two ? 1 : 0;
-    for (long long u = u_begin; u < u_end; ++u) {
-        const int k = static_cast<int>(u - u_begin), buf = k & 1;
-        const CorrUnit nxt = corr_next(a, nvb, cur);  // used only while u + 1 < u_end
-        if (k == 0 || cur.c == 0) {
-            // a new (segment, head, value block): its start-state block, once
-            // the previous unit's product (the B tiles' last reader) is done;
-            // this wait consumes nothing, the epilogue waits on the same phase
-            if (k > 0 && !mbar_wait(bar_mma(buf ^ 1), (ph_mma >> (buf ^ 1)) & 1u, wl)) failed = true;
-            if (!failed && !cur.first) load_start(cur);
+
+    if (producer) {
+        // O_M tiles two units ahead in a ring of three operand buffers
+        long long om_issued = nk < 2 ? nk : 2, om_seen = 0;
+        CorrUnit ahead = corr_next(a, nvb, cur);      // the unit two ahead, once the loop runs
+        if (gtid == 0) {
+            issue_om(cur, 0);
+            if (nk > 1) issue_om(ahead, 1);
         }
-        // A = O_M rows r0 .. r0 + 63 as split tiles in operand buffer buf
-        // (rows past the segment are zero); its last reader was the product
-        // of unit k - 2, whose epilogue has run
-        if (mbar_wait(bar_a, ph_a, wl)) {
-            ph_a ^= 1u;
-            --pend_a;
-        } else {
-            failed = true;
-        }
-        uint8_t* ahi = Aop + buf * aBytes;
-        uint8_t* alo = ahi + kreg * kCorrTile;
-#pragma unroll 8
-        for (int e = tid; !cur.first && e < 64 * (K / 8); e += kCorrThreads) {
-            const int r = e / (K / 8), c8 = e % (K / 8);
-            float x8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (r < cur.nv) {
-                const float4 v0 = *reinterpret_cast<const float4*>(A32 + r * K + 8 * c8);
-                const float4 v1 = *reinterpret_cast<const float4*>(A32 + r * K + 8 * c8 + 4);
-                x8[0] = v0.x; x8[1] = v0.y; x8[2] = v0.z; x8[3] = v0.w;
-                x8[4] = v1.x; x8[5] = v1.y; x8[6] = v1.z; x8[7] = v1.w;
+        ahead = corr_next(a, nvb, ahead);
+        for (long long k = 0; k < nk; ++k) {
+            const int tb = static_cast<int>(k & 1), j = static_cast<int>(k % 3);
+            if ((k == 0 || cur.c == 0) && !cur.first) {
+                // a new (segment, head, value block): its start-state block,
+                // once the previous unit's product (the B tiles' last reader)
+                // is done; the group takes one decision to leave
+                if (k > 0 && !mbar_wait(bar_mma(tb ^ 1), par(k - 1), wl)) failed = true;
+                if (!failed) load_start(cur, gtid, 128);
+                fence_proxy_async_smem();
+                if (group_or(failed)) break;
             }
-            store_split_chunk(ahi + (c8 >> 3) * kCorrTile, alo + (c8 >> 3) * kCorrTile, r, c8 & 7, x8);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        // A32 is read out and the operand tiles are in; every thread takes
-        // the same decision to leave
-        if (__syncthreads_or(failed)) break;
-        tc_fence_after();
-        if (warp == 0) {
-            if (u + 1 < u_end && lane == 0) issue_om(nxt);
-            __syncwarp();
-            if (elect_one()) {
-                tc_fence_after();
-                const uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64 * nb);
-                const uint32_t ah = smem_u32(ahi), al = smem_u32(alo), bh = smem_u32(Bhi), bl = smem_u32(Blo);
-                // (a first-segment unit commits with no product: the barrier
-                // then only waits for the products before it)
-                for (int s = 0; !cur.first && s < K / 16; ++s) {
-                    const uint32_t ao = (s >> 2) * kCorrTile + (s & 3) * 32;
-                    const uint64_t da_h = desc_sw128(ah + ao, 0, 1024), da_l = desc_sw128(al + ao, 0, 1024);
-                    const uint64_t db_h = desc_sw128(bh + s * 2048, bBytes, 1024);
-                    const uint64_t db_l = desc_sw128(bl + s * 2048, bBytes, 1024);
-                    const uint32_t d = tmem + 128 * buf;
-                    mma_bf16(d, da_h, db_h, id, s > 0);
-                    mma_bf16(d, da_h, db_l, id, 1);
-                    mma_bf16(d, da_l, db_h, id, 1);
+            // warp 0 issues; after a wait ran out it only keeps step with the
+            // group (whose barriers above every warp must reach) and does no work
+            if (warp == 0 && !failed) {
+                bool ok = __all_sync(0xffffffffu, mbar_wait(bar_a(j), static_cast<uint32_t>((k / 3) & 1), wl));
+                if (ok) ++om_seen;
+                // accumulator tb: the epilogue of unit k - 2 has read it
+                ok = ok && (k < 2 || __all_sync(0xffffffffu, mbar_wait(bar_tf(tb), par(k - 2), wl)));
+                if (ok && elect_one()) {
+                    tc_fence_after();
+                    const uint32_t id = idesc(kFmtBf16, 0, 1, 64, 64 * nb);
+                    const uint32_t ah = smem_u32(Aop + j * aBytes), al = ah + kreg * kCorrTile;
+                    const uint32_t bh = smem_u32(Bhi), bl = smem_u32(Blo);
+                    const uint32_t d = tmem + 128 * tb;
+                    // (a first-segment unit commits with no product: the
+                    // barrier then only waits for the products before it)
+                    for (int s = 0; !cur.first && s < K / 16; ++s) {
+                        const uint32_t ao = (s >> 2) * kCorrTile + (s & 3) * 32;
+                        const uint64_t da_h = desc_sw128(ah + ao, 0, 1024), da_l = desc_sw128(al + ao, 0, 1024);
+                        const uint64_t db_h = desc_sw128(bh + s * 2048, bBytes, 1024);
+                        const uint64_t db_l = desc_sw128(bl + s * 2048, bBytes, 1024);
+                        mma_bf16(d, da_h, db_h, id, s > 0);
+                        mma_bf16(d, da_h, db_l, id, 1);
+                        mma_bf16(d, da_l, db_h, id, 1);
+                    }
+                    mma_commit(bar_mma(tb));
                 }
-                mma_commit(bar_mma(buf));
+                __syncwarp();
+                // unit k + 2's tiles into buffer (k + 2) % 3, whose last reader
+                // was the product of unit k - 1
+                if (ok && k + 2 < nk) {
+                    ok = k < 1 || __all_sync(0xffffffffu, mbar_wait(bar_mma(tb ^ 1), par(k - 1), wl));
+                    if (ok) {
+                        if (lane == 0) issue_om(ahead, static_cast<int>((k + 2) % 3));
+                        ++om_issued;
+                    }
+                }
+                if (!ok) failed = true;  // the consumer group times out on this unit's product too
             }
+            cur = corr_next(a, nvb, cur);
+            if (k + 3 < nk) ahead = corr_next(a, nvb, ahead);
+        }
+        // nothing the group issued outlives the CTA: its products, then its copies
+        if (warp == 0) {
+            if (elect_one()) mma_commit(bar_drain);
             __syncwarp();
+            if (!mbar_wait(bar_drain, 0, kDefaultWaitLimit)) failed = true;
+            for (; om_seen < om_issued; ++om_seen)
+                if (!mbar_wait(bar_a(static_cast<int>(om_seen % 3)), static_cast<uint32_t>((om_seen / 3) & 1),
+                               kDefaultWaitLimit))
+                    failed = true;
         }
-        if (u + 1 < u_end) ++pend_a;
-        if (buf) ++pend_m1; else ++pend_m0;
-        // the previous unit's epilogue while this unit's product runs; then
-        // its O_b staging buffer takes unit u + 1's
-        if (k > 0) {
-            epilogue(prev, k - 1);
-            tc_fence_before();
-            if (__syncthreads_or(failed)) break;
-            if (u + 1 < u_end) {
-                if (tid == 0) issue_ob(nxt, buf ^ 1);
-                if (buf) ++pend_b0; else ++pend_b1;
+    } else {
+        // consumer: O_b copies (two units ahead) and every epilogue
+        long long b_issued = nk < 2 ? nk : 2, b_seen = 0;  // O_b copies issued / seen complete
+        CorrUnit ahead = corr_next(a, nvb, cur);          // the unit two ahead, once the loop runs
+        if (gtid == 0) {
+            issue_ob(cur, 0);
+            if (nk > 1) issue_ob(ahead, 1);
+        }
+        ahead = corr_next(a, nvb, ahead);
+        const int sub = warp & 3;
+        const int row = 16 * sub + (lane & 15);       // accumulator row of this lane
+        const int cpart = 32 * (lane >> 4);           // its 32 columns of each 64-column block
+        for (long long k = 0; k < nk; ++k) {
+            const int buf = static_cast<int>(k & 1);
+            if (mbar_wait(bar_b(buf), par(k), wl)) ++b_seen;
+            else failed = true;
+            if (!mbar_wait(bar_mma(buf), par(k), wl)) failed = true;
+            tc_fence_after();
+            // out = bf16(O_b + the product) for row `row`, columns 64 blk + cpart .. + 31
+            for (int blk = 0; blk < nb; ++blk) {
+                float acc[32];
+                if (cur.first) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                } else {
+                    ld_half32(tmem, sub, 128 * buf + 64 * blk, acc);
+                }
+                if (row < cur.nv) {
+                    // row `row` of box 2 blk + cpart / 32, its 16-byte chunk q at q ^ (row % 8)
+                    const uint8_t* box = B32 + buf * obUnit + (2 * blk + (cpart >> 5)) * 8192 + row * 128;
+                    float4 ob4[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) ob4[q] = *reinterpret_cast<const float4*>(box + ((q ^ (row & 7)) << 4));
+                    uint4* dst = reinterpret_cast<uint4*>(a.out + (cur.r0 + row) * H * static_cast<long long>(V) +
+                                                          static_cast<long long>(cur.h) * V + cur.vb * 64 * nb +
+                                                          64 * blk + cpart);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 x0 = ob4[2 * q], x1 = ob4[2 * q + 1];
+                        const float* y = acc + 8 * q;
+                        dst[q] = make_uint4(pack_bf16x2(x0.x + y[0], x0.y + y[1]), pack_bf16x2(x0.z + y[2], x0.w + y[3]),
+                                            pack_bf16x2(x1.x + y[4], x1.y + y[5]), pack_bf16x2(x1.z + y[6], x1.w + y[7]));
+                    }
+                }
             }
+            tc_fence_before();
+            // staging buffer buf and accumulator buf are read out
+            if (group_or(failed)) break;
+            if (gtid == 0) {
+                mbar_arrive(bar_tf(buf));
+                if (k + 2 < nk) issue_ob(ahead, buf);
+            }
+            if (k + 2 < nk) ++b_issued;
+            cur = corr_next(a, nvb, cur);
+            if (k + 3 < nk) ahead = corr_next(a, nvb, ahead);
         }
-        prev = cur;
-        cur = nxt;
+        for (; b_seen < b_issued; ++b_seen)
+            if (!mbar_wait(bar_b(static_cast<int>(b_seen & 1)), par(b_seen), kDefaultWaitLimit)) failed = true;
     }
-    if (!failed) epilogue(prev, static_cast<int>(u_end - 1 - u_begin));
-    if (failed) {
-        record_error(a.err, kErrTimeout);
-        // let every copy and product still in flight land before the shared
-        // memory and the TMEM are given back
-        for (; pend_a > 0; --pend_a, ph_a ^= 1u) mbar_wait(bar_a, ph_a, kDefaultWaitLimit);
-        for (; pend_b0 > 0; --pend_b0, ph_b ^= 1u) mbar_wait(bar_b(0), ph_b & 1u, kDefaultWaitLimit);
-        for (; pend_b1 > 0; --pend_b1, ph_b ^= 2u) mbar_wait(bar_b(1), (ph_b >> 1) & 1u, kDefaultWaitLimit);
-        for (; pend_m0 > 0; --pend_m0, ph_mma ^= 1u) mbar_wait(bar_mma(0), ph_mma & 1u, kDefaultWaitLimit);
-        for (; pend_m1 > 0; --pend_m1, ph_mma ^= 2u) mbar_wait(bar_mma(1), (ph_mma >> 1) & 1u, kDefaultWaitLimit);
-    }
+    if (failed) record_error(a.err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kCorrCols);
@@ -504,12 +512,16 @@ bool make_f32_rows_map(CUtensorMap* m, const float* base, long long rows, int H,
 cudaError_t launch_split_correct(const SplitCorrectArgs& a, cudaStream_t stream) {
     if (a.max_chunks == 0 || a.nseq == 0 || a.rows == 0) return cudaSuccess;
     const int nb = a.d_v >= 128 ? 2 : 1;
-    CUtensorMap mom, mob;
-    memset(&mom, 0, sizeof(mom));
+    CUtensorMap momh, moml, mob;
+    memset(&momh, 0, sizeof(momh));
+    memset(&moml, 0, sizeof(moml));
     memset(&mob, 0, sizeof(mob));
-    if (!make_f32_rows_map(&mom, a.om, a.rows, a.H, a.d_k, a.d_k) || !make_f32_rows_map(&mob, a.ob, a.rows, a.H, a.d_v, 32))
+    const uint16_t* omh = reinterpret_cast<const uint16_t*>(a.om);
+    const uint16_t* oml = omh + a.rows * a.H * a.d_k;
+    if (!tc::make_rows_map(&momh, omh, a.rows, a.H, a.d_k) || !tc::make_rows_map(&moml, oml, a.rows, a.H, a.d_k) ||
+        !make_f32_rows_map(&mob, a.ob, a.rows, a.H, a.d_v, 32))
         return cudaErrorInvalidValue;
-    const int smem = 2 * nb * a.d_k * 128 + 4 * (a.d_k / 64) * kCorrTile + 64 * a.d_k * 4 + 2 * 64 * 64 * nb * 4 + 64 + 1024;
+    const int smem = 2 * nb * a.d_k * 128 + 6 * (a.d_k / 64) * kCorrTile + 2 * 64 * 64 * nb * 4 + 96 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gdn_split_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -517,7 +529,7 @@ cudaError_t launch_split_correct(const SplitCorrectArgs& a, cudaStream_t stream)
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long long units = static_cast<long long>(a.nseq) * a.H * (a.d_v / (64 * nb)) * a.max_chunks;
     const int grid = static_cast<int>(units < sms ? units : sms);
-    gdn_split_correct_kernel<<<grid, kCorrThreads, smem, stream>>>(mom, mob, a);
+    gdn_split_correct_kernel<<<grid, kCorrThreads, smem, stream>>>(momh, moml, mob, a);
     return cudaGetLastError();
 }
 

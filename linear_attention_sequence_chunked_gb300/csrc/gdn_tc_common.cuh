@@ -43,16 +43,18 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float a, float b) {
     return r;
 }
 
+// Two values split as x = hi + lo (both bf16, packed in pairs).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = cvt_bf16x2(a, b);
+    lo = cvt_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
+
 // One 16-byte chunk (8 values, columns 8*ch .. 8*ch+7) of a split row.
 __device__ __forceinline__ void store_split_chunk(uint8_t* tile_hi, uint8_t* tile_lo, int row, int ch,
                                                   const float* x8) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float a = x8[2 * e], b = x8[2 * e + 1];
-        h[e] = cvt_bf16x2(a, b);
-        l[e] = cvt_bf16x2(a - __uint_as_float(h[e] << 16), b - __uint_as_float(h[e] & 0xffff0000u));
-    }
+    for (int e = 0; e < 4; ++e) split_bf16x2(x8[2 * e], x8[2 * e + 1], h[e], l[e]);
     const uint32_t off = sw128_offset(row, ch * 16);
     *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
