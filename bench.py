@@ -313,6 +313,15 @@ def run_ours(args):
             print(json.dumps(r))
         return 0
 
+    if args.kda_once:
+        # profiling aid: one per-channel-gate forward (workspace route) and
+        # one backward at B,H,T (d_k = d_v = 128), printed as JSON
+        if rank == 0:
+            kb, kh, kt = (int(x) for x in args.kda_once.split(","))
+            print(json.dumps(measure_kda(gdn, torch, dev, torch.cuda.current_stream(), None, B=kb, H=kh, T=kt,
+                                         once=True)))
+        return 0
+
     B, T, H, K, V = (SHAPE[k] for k in ("B", "T", "H", "d_k", "d_v"))
     wl = W.make_workload(2, B=B, T=T, H=H, d_k=K, d_v=V, with_grad=True,
                          seed=rank_seed(rank))
@@ -651,7 +660,7 @@ FP32_LANES_PER_SM = 128   # fp32 FMA lanes per SM (4 sub-partitions x 32)
 SMS = 152
 
 
-def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, steps=5, warmup=2):
+def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, steps=5, warmup=2, once=False):
     """The per-channel-gate (KDA) operator at the headline shape, L2 flushed
     before each call: the chunked forward through its workspace route (the
     chunk-parallel T/P kernel on the CUDA cores, then the tensor-core walk),
@@ -659,7 +668,9 @@ def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, s
     token-serial forward, and the chunked backward (gdn_kda_chunk_bwd).
     Inputs: q, v, dO ~ N(0,1), k L2-normalised, g = -5 sigmoid(N(0,1) + 2) per
     key channel (the bounded gate with lower bound -5), beta = sigmoid(N(0,1)),
-    zero initial state; drawn on the device.  The roofline line is the
+    zero initial state; drawn on the device.  With once, a profiling aid:
+    one forward through the workspace route and one backward, untimed.  The
+    roofline line is the
     forward's chunk-algebra FLOPs (decay exponentials not counted) against
     the fp32 FMA rate of 152 SMs x 128 lanes x 2 FLOP at the sampled SM
     clock: its dominant kernel, the T/P kernel, runs on the CUDA cores."""
@@ -705,6 +716,14 @@ def measure_kda(gdn, torch, dev, stream, clk, B=4, H=16, T=4096, K=128, V=128, s
     def bwd():
         gdn.gdn_kda_chunk_bwd(q, k, v, g, beta, scale, None, None, d_out, None, *grads, B, T, H, K, V, wb, nb, stream)
 
+    if once:
+        fwd(wf, nf)()
+        bwd()
+        torch.cuda.synchronize()
+        st = gdn.gdn_get_last_device_error()
+        if st != 0:
+            raise SystemExit(f"device error in the KDA call: {gdn.gdn_status_string(st)}")
+        return {"config": f"B={B} T={T} H={H} d_k={K} d_v={V}", "once": True}
     t_c = timed(fwd(wf, nf), steps)
     o_c = out.float().clone()
     t_w = timed(fwd(None, 0), 2)
@@ -1115,6 +1134,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--split-only", type=int, default=0, metavar="NSEG",
                     help="run only the sequence-split measurement at NSEG segments (profiling)")
+    ap.add_argument("--kda-once", default="", metavar="B,H,T",
+                    help="run one per-channel-gate forward and backward at B,H,T (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
